@@ -1,0 +1,212 @@
+"""Checks that pin the CPU oracle to facts other than itself.
+
+Each pin takes an implementation ``fn(Q, K, V) -> O`` (fp16 CPU tensors in,
+float64 numpy array (B, M, d) out) and raises ``AssertionError`` when the
+implementation disagrees with a closed form, a brute-force evaluation written
+independently, a library special case, or an invariant of the graph
+``O = (exp(Q.K) / rowsum(exp(Q.K))) . V`` (Mirage documentation,
+tutorials/group-query-attention, "Define GQA Computation Graph").
+
+They are chosen so that a plausible slip anywhere in the oracle (a wrong sign
+on the exponent, a dropped normalisation or term, a transposed operand, a
+wrong row/batch index, a stray 1/sqrt(d) scale) fails at least one of them;
+``test_oracle_mutants.py`` plants such slips in a copy of the oracle and
+checks exactly that.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rand_inputs(B, M, N, d, a=0.5, seed=0):
+    # Local draw (not the shared recipe) so pins do not depend on its details.
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = (torch.rand((B, M, d), generator=g) * 2 * a - a).half()
+    k = (torch.rand((B, d, N), generator=g) * 2 * a - a).half()
+    v = torch.randn((B, N, d), generator=g).half()
+    return q, k, v
+
+
+def _close(got, want, rtol, atol, what):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, f"{what}: shape {got.shape} != {want.shape}"
+    err = np.abs(got - want)
+    bound = atol + rtol * np.abs(want)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
+                           f" (bound {bound.flat[err.argmax()]:.3e})")
+
+
+# ---------------------------------------------------------------- closed forms
+
+def pin_k_zero(fn):
+    """K = 0 makes every score 0, every weight 1/N: O[b,m,:] is the mean of V[b] over N."""
+    for (B, M, N, d) in [(2, 5, 37, 8), (1, 3, 130, 4)]:
+        q, _, v = _rand_inputs(B, M, N, d, seed=1)
+        k = torch.zeros((B, d, N), dtype=torch.float16)
+        want = v.double().numpy().mean(axis=1, keepdims=True).repeat(M, axis=1)
+        _close(fn(q, k, v), want, 1e-12, 1e-14, f"K=0 {B,M,N,d}")
+
+
+def pin_q_zero(fn):
+    """Q = 0 likewise gives the mean of V over N for every row."""
+    B, M, N, d = 2, 4, 19, 6
+    _, k, v = _rand_inputs(B, M, N, d, seed=2)
+    q = torch.zeros((B, M, d), dtype=torch.float16)
+    want = v.double().numpy().mean(axis=1, keepdims=True).repeat(M, axis=1)
+    _close(fn(q, k, v), want, 1e-12, 1e-14, "Q=0")
+
+
+def pin_v_constant(fn):
+    """V = c everywhere: the weights sum to one, so O = c."""
+    B, M, N, d = 2, 6, 23, 5
+    q, k, _ = _rand_inputs(B, M, N, d, a=1.0, seed=3)
+    v = torch.full((B, N, d), 0.75, dtype=torch.float16)
+    _close(fn(q, k, v), np.full((B, M, d), 0.75), 1e-13, 0.0, "V=const")
+
+
+def pin_single_key(fn):
+    """M = N = 1: one weight, equal to one, so O = V[b, 0, :] exactly."""
+    q, k, v = _rand_inputs(3, 1, 1, 7, a=2.0, seed=4)
+    got = np.asarray(fn(q, k, v))
+    want = v.double().numpy()
+    assert np.array_equal(got, want), f"M=N=1: {got} != {want}"
+
+
+def pin_one_hot(fn):
+    """d = 1, Q[m] = t_m, K[n] = 1 at n* else 0: the score row is t_m at n* and 0 elsewhere, so
+    O[m] = (e^t_m V[n*] + sum_{n != n*} V[n]) / (e^t_m + N - 1). Fails for exp(-s), shifted exps
+    or any missing exponential."""
+    ts = [0.5, -1.25, 2.0, 3.0, 0.0]
+    N, nstar = 11, 4
+    q = torch.tensor(ts, dtype=torch.float16).reshape(1, len(ts), 1)
+    k = torch.zeros((1, 1, N), dtype=torch.float16)
+    k[0, 0, nstar] = 1.0
+    g = torch.Generator("cpu").manual_seed(5)
+    v = torch.randn((1, N, 1), generator=g).half()
+    vv = [float(x) for x in v.double().flatten()]
+    rest = math.fsum(vv[n] for n in range(N) if n != nstar)
+    want = np.array([(math.exp(t) * vv[nstar] + rest) / (math.exp(t) + N - 1) for t in ts])
+    _close(fn(q, k, v), want.reshape(1, len(ts), 1), 1e-13, 1e-15, "one-hot")
+
+
+def pin_golden_worked_examples(fn):
+    """Hand-derived examples (tests/golden/worked_examples.json): exact fp16 inputs whose
+    outputs have short closed forms, evaluated here with the math module."""
+    with open(os.path.join(GOLDEN, "worked_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    env = {"e": math.e, "exp": math.exp}
+    for case in cases:
+        q = torch.tensor(case["Q"], dtype=torch.float16)
+        k = torch.tensor(case["K"], dtype=torch.float16)
+        v = torch.tensor(case["V"], dtype=torch.float16)
+        want = np.array([[[eval(expr, {"__builtins__": {}}, env) for expr in row]
+                          for row in batch] for batch in case["O"]], dtype=np.float64)
+        _close(fn(q, k, v), want, 1e-13, 1e-15, case["name"])
+
+
+# ----------------------------------------------------------------- brute force
+
+def brute_force(q, k, v):
+    """Pure-Python evaluation of the definition, one output element at a time:
+    O[b,m,c] = sum_n w_n V[b,n,c] / sum_n w_n, w_n = exp(sum_k Q[b,m,k] K[b,k,n]).
+    Uses exactly rounded sums (math.fsum) so it is independent of summation order."""
+    Q = q.double().tolist()
+    K = k.double().tolist()
+    V = v.double().tolist()
+    B, M, d = len(Q), len(Q[0]), len(Q[0][0])
+    N = len(K[0][0])
+    out = np.zeros((B, M, d))
+    for b in range(B):
+        for m in range(M):
+            w = [math.exp(math.fsum(Q[b][m][kk] * K[b][kk][n] for kk in range(d))) for n in range(N)]
+            tot = math.fsum(w)
+            for c in range(d):
+                out[b, m, c] = math.fsum(w[n] * V[b][n][c] for n in range(N)) / tot
+    return out
+
+
+def pin_brute_force(fn):
+    """Odd tiny shapes (B <= 2, M, N <= 17, d in {1, 2, 4}) against the pure-Python loop."""
+    for i, (B, M, N, d) in enumerate([(1, 1, 3, 1), (2, 3, 5, 2), (2, 7, 17, 4), (1, 17, 9, 4),
+                                      (2, 2, 16, 1)]):
+        q, k, v = _rand_inputs(B, M, N, d, a=1.5, seed=10 + i)
+        _close(fn(q, k, v), brute_force(q, k, v), 1e-12, 1e-14, f"brute {B,M,N,d}")
+
+
+# -------------------------------------------------------- library special case
+
+def pin_torch_softmax(fn):
+    """Softmax is shift-invariant, so the graph equals torch.softmax(Q@K, -1) @ V (float64)."""
+    for i, (B, M, N, d) in enumerate([(2, 64, 96, 64), (1, 9, 200, 128), (3, 5, 40, 16)]):
+        q, k, v = _rand_inputs(B, M, N, d, seed=20 + i)
+        want = (torch.softmax(q.double() @ k.double(), dim=-1) @ v.double()).numpy()
+        _close(fn(q, k, v), want, 1e-11, 1e-13, f"softmax {B,M,N,d}")
+
+
+# ------------------------------------------------------------------ invariants
+
+def pin_joint_permutation(fn):
+    """Reordering the N axis of K (columns) and V (rows) together leaves O unchanged."""
+    B, M, N, d = 2, 6, 29, 8
+    q, k, v = _rand_inputs(B, M, N, d, seed=30)
+    perm = torch.randperm(N, generator=torch.Generator("cpu").manual_seed(31))
+    _close(fn(q, k[:, :, perm].contiguous(), v[:, perm, :].contiguous()), fn(q, k, v),
+           1e-12, 1e-14, "permutation")
+
+
+def pin_convex_hull(fn):
+    """Each O[b,m,:] is a convex combination of V[b] rows: within V's per-column min/max."""
+    B, M, N, d = 3, 7, 33, 5
+    q, k, v = _rand_inputs(B, M, N, d, a=2.0, seed=40)
+    o = np.asarray(fn(q, k, v))
+    vv = v.double().numpy()
+    lo = vv.min(axis=1, keepdims=True) - 1e-14
+    hi = vv.max(axis=1, keepdims=True) + 1e-14
+    assert (o >= lo).all() and (o <= hi).all(), "O leaves the convex hull of V"
+
+
+def pin_batch_independence(fn):
+    """Batch b of a B=3 run equals a B=1 run on that slice, bit for bit."""
+    B, M, N, d = 3, 5, 21, 6
+    q, k, v = _rand_inputs(B, M, N, d, seed=50)
+    full = np.asarray(fn(q, k, v))
+    for b in range(B):
+        one = np.asarray(fn(q[b:b + 1].contiguous(), k[b:b + 1].contiguous(), v[b:b + 1].contiguous()))
+        assert np.array_equal(full[b:b + 1], one), f"batch {b} depends on other batches"
+
+
+def pin_score_shift(fn):
+    """With Q's last column set to one, adding c to K's last row adds c to every score of a row;
+    the normalisation cancels it, so O is unchanged. K's last row is drawn on a 1/64 grid so that
+    the shifted values stay exact in fp16."""
+    B, M, N, d = 2, 4, 27, 6
+    q, k, v = _rand_inputs(B, M, N, d, seed=60)
+    q[:, :, -1] = 1.0
+    g = torch.Generator("cpu").manual_seed(61)
+    k[:, -1, :] = (torch.randint(-64, 65, (B, N), generator=g).float() / 64).half()
+    k2 = k.clone()
+    k2[:, -1, :] = (k[:, -1, :].float() + 1.5).half()
+    assert torch.equal(k2[:, -1, :].float() - 1.5, k[:, -1, :].float())
+    _close(fn(q, k2, v), fn(q, k, v), 1e-12, 1e-14, "score shift")
+
+
+def pin_v_linearity(fn):
+    """O is linear in V: doubling V (exact in fp16) doubles O exactly."""
+    B, M, N, d = 1, 4, 15, 3
+    q, k, v = _rand_inputs(B, M, N, d, seed=70)
+    assert np.array_equal(np.asarray(fn(q, k, (v.float() * 2).half())), 2 * np.asarray(fn(q, k, v)))
+
+
+PINS = [pin_k_zero, pin_q_zero, pin_v_constant, pin_single_key, pin_one_hot,
+        pin_golden_worked_examples, pin_brute_force, pin_torch_softmax, pin_joint_permutation,
+        pin_convex_hull, pin_batch_independence, pin_score_shift, pin_v_linearity]
