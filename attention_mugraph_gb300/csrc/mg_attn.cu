@@ -1,0 +1,459 @@
+// mg_attn.cu -- host side of the C ABI declared in include/mg_attn.h: shape validation and
+// planning, the plan's device workspace, TMA tensor-map encoding, kernel launches (with
+// programmatic dependent launch), the host-buffer variant and the sticky status word.
+#include "mg_attn.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "mg_attn_kernels.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+void set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+
+mg_status fail(mg_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+mg_status cuda_fail(cudaError_t e, const char *what)
+{
+    set_error("%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    return MG_ERR_CUDA;
+}
+
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
+
+// The driver's tensor-map encoder, fetched through the runtime so that no libcuda link is needed.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int auto_stages(int64_t d) { return d == 64 ? 4 : 2; }
+
+using FwdKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const mg::FwdParams);
+
+FwdKernel fwd_kernel(int64_t d, int stages)
+{
+    if (d == 64) {
+        switch (stages) {
+        case 2: return mg::mg_attn_fwd_partial<64, 2>;
+        case 3: return mg::mg_attn_fwd_partial<64, 3>;
+        case 4: return mg::mg_attn_fwd_partial<64, 4>;
+        default: return nullptr;
+        }
+    }
+    if (d == 128 && stages == 2)
+        return mg::mg_attn_fwd_partial<128, 2>;
+    return nullptr;
+}
+
+using CombineKernel = void (*)(const float *, const float *, __half *, int, int);
+
+CombineKernel combine_kernel(int64_t d)
+{
+    return d == 64 ? mg::mg_attn_combine<64> : mg::mg_attn_combine<128>;
+}
+
+// Validation and tiling decisions; touches no GPU.
+mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int32_t num_sms,
+                 int32_t max_smem, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags)
+{
+    if (!info)
+        return fail(MG_ERR_INVALID_ARG, "info is NULL");
+    if (B <= 0 || M <= 0 || N <= 0 || d <= 0)
+        return fail(MG_ERR_INVALID_ARG, "dimensions must be positive (B=%lld M=%lld N=%lld d=%lld)", (long long)B,
+                    (long long)M, (long long)N, (long long)d);
+    if (B > kMaxDim || M > kMaxDim || N > kMaxDim || B * M > kMaxRows)
+        return fail(MG_ERR_INVALID_ARG, "dimensions too large (B, M, N <= 2^30 and B*M < 2^31)");
+    if (d != 64 && d != 128)
+        return fail(MG_ERR_UNSUPPORTED, "head dim d=%lld not supported (64 or 128)", (long long)d);
+    if (N % 8 != 0)
+        return fail(MG_ERR_LAYOUT, "N=%lld must be a multiple of 8 (16-byte row stride of K for TMA)",
+                    (long long)N);
+    if (num_sms <= 0)
+        return fail(MG_ERR_INVALID_ARG, "num_sms must be positive");
+    mg_attn_options o{};
+    if (opts)
+        o = *opts;
+    if (o.reserved != 0 || (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT)) != 0)
+        return fail(MG_ERR_CONFIG, "unknown option bits");
+    if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
+        return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
+
+    const int64_t m_tiles_per_b = (M + mg::kBlockM - 1) / mg::kBlockM;
+    const int64_t m_tiles = B * m_tiles_per_b;
+    const int64_t n_tiles = (N + mg::kBlockN - 1) / mg::kBlockN;
+
+    int64_t n_split = o.n_split;
+    if (n_split < 0 || n_split > n_tiles)
+        return fail(MG_ERR_CONFIG, "n_split=%lld out of range [0, %lld]", (long long)n_split, (long long)n_tiles);
+    if (n_split == 0) {
+        // One wave: as many splits per row tile as keep every SM busy, never fewer than one
+        // column tile per split.
+        n_split = m_tiles >= num_sms ? 1 : num_sms / m_tiles;
+        if (n_split > n_tiles)
+            n_split = n_tiles;
+        if (n_split < 1)
+            n_split = 1;
+    }
+    if (m_tiles * n_split > 0x7fffffffLL)
+        return fail(MG_ERR_INVALID_ARG, "grid too large");
+
+    int stages = o.stages == 0 ? auto_stages(d) : o.stages;
+    if (stages < 2 || stages > 4)
+        return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 4]", stages);
+    const uint32_t smem = mg::fwd_smem_bytes(static_cast<int>(d), stages);
+    if (!fwd_kernel(d, stages) || static_cast<int64_t>(smem) > max_smem)
+        return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
+                    (long long)d, stages, smem, max_smem);
+
+    std::memset(info, 0, sizeof(*info));
+    info->B = B;
+    info->M = M;
+    info->N = N;
+    info->d = d;
+    info->block_m = mg::kBlockM;
+    info->block_n = mg::kBlockN;
+    info->m_tiles = static_cast<int32_t>(m_tiles);
+    info->n_tiles = static_cast<int32_t>(n_tiles);
+    info->n_split = static_cast<int32_t>(n_split);
+    info->stages = stages;
+    info->threads = mg::kThreads;
+    info->grid_ctas = static_cast<int32_t>(m_tiles * n_split);
+    info->smem_bytes = static_cast<int32_t>(smem);
+    info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
+    info->kernels_per_run = n_split > 1 ? 2 : 1;
+    info->num_sms = num_sms;
+    const int64_t partial_bytes = n_split > 1 ? (n_split * B * M * d + n_split * B * M) * 4 : 0;
+    info->workspace_bytes = 256 + partial_bytes;
+    if (timeout_ns)
+        *timeout_ns = o.timeout_ns ? static_cast<unsigned long long>(o.timeout_ns) : kDefaultTimeoutNs;
+    if (flags)
+        *flags = o.flags;
+    g_last_error[0] = '\0';
+    return MG_OK;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// 3-D fp16 tensor map over a contiguous (d2, d1, d0) array (d0 innermost) with a box of
+// box0 x box1 x 1 elements and 128-byte swizzle; out-of-range elements read as zero.
+mg_status encode_3d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                    uint32_t box1)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return fail(MG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MG_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult %d", static_cast<int>(r));
+    return MG_OK;
+}
+
+}  // namespace
+
+struct mg_attn_plan {
+    int device = -1;
+    mg_attn_plan_info info{};
+    int flags = 0;
+    unsigned long long timeout_ns = kDefaultTimeoutNs;
+    void *workspace = nullptr;  // [status words | ws_o | ws_l]
+    int *status = nullptr;
+    float *ws_o = nullptr;
+    float *ws_l = nullptr;
+    FwdKernel fwd = nullptr;
+    CombineKernel combine = nullptr;
+    // Last encoded tensor maps and the pointers they were encoded for.
+    const void *map_ptr[3] = {nullptr, nullptr, nullptr};
+    CUtensorMap maps[3];
+    // Device staging for mg_attn_run_host, allocated by its first call.
+    void *staging = nullptr;
+};
+
+extern "C" {
+
+int32_t mg_attn_version(void) { return 10000; }
+
+const char *mg_attn_status_string(mg_status s)
+{
+    switch (s) {
+    case MG_OK: return "success";
+    case MG_ERR_INSUFFICIENT_SMEM: return "insufficient shared memory for the tile configuration";
+    case MG_ERR_LAYOUT: return "layout error (alignment or N % 8)";
+    case MG_ERR_CONFIG: return "configuration error (option out of range)";
+    case MG_ERR_INVALID_ARG: return "invalid argument";
+    case MG_ERR_UNSUPPORTED: return "unsupported head dim or device";
+    case MG_ERR_CUDA: return "CUDA error";
+    case MG_ERR_TIMEOUT: return "in-kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *mg_attn_last_error(void) { return g_last_error; }
+
+mg_status mg_attn_query(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int32_t num_sms,
+                        int32_t max_smem_optin, mg_attn_plan_info *info)
+{
+    return decide(B, M, N, d, opts, num_sms, max_smem_optin, info, nullptr, nullptr);
+}
+
+mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts,
+                          mg_attn_plan_t *out)
+{
+    if (!out)
+        return fail(MG_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0, sms = 0, smem_optin = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+        return fail(MG_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; this library is built for 10.3", dev,
+                    major, minor);
+
+    mg_attn_plan_info info;
+    unsigned long long timeout_ns = 0;
+    int flags = 0;
+    mg_status st = decide(B, M, N, d, opts, sms, smem_optin, &info, &timeout_ns, &flags);
+    if (st != MG_OK)
+        return st;
+
+    FwdKernel fwd = fwd_kernel(d, info.stages);
+    e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             info.smem_bytes);
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+        return fail(MG_ERR_UNSUPPORTED, "no sm_103a kernel image for device %d", dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute");
+
+    struct mg_attn_plan *p = new (std::nothrow) struct mg_attn_plan();
+    if (!p)
+        return fail(MG_ERR_CUDA, "out of host memory");
+    p->device = dev;
+    p->info = info;
+    p->flags = flags;
+    p->timeout_ns = timeout_ns;
+    p->fwd = fwd;
+    p->combine = combine_kernel(d);
+    e = cudaMalloc(&p->workspace, static_cast<size_t>(info.workspace_bytes));
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    }
+    uint8_t *ws = static_cast<uint8_t *>(p->workspace);
+    p->status = reinterpret_cast<int *>(ws);
+    if (info.n_split > 1) {
+        p->ws_o = reinterpret_cast<float *>(ws + 256);
+        p->ws_l = p->ws_o + static_cast<size_t>(info.n_split) * B * M * d;
+    }
+    e = cudaMemset(p->workspace, 0, 256);
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(p->workspace);
+        delete p;
+        return cuda_fail(e, "cudaMemset(status)");
+    }
+    *out = p;
+    return MG_OK;
+}
+
+mg_status mg_attn_plan(int64_t B, int64_t M, int64_t N, int64_t d, mg_attn_plan_t *out)
+{
+    return mg_attn_plan_ex(B, M, N, d, nullptr, out);
+}
+
+mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info)
+{
+    if (!plan || !info)
+        return fail(MG_ERR_INVALID_ARG, "NULL plan or info");
+    *info = plan->info;
+    return MG_OK;
+}
+
+mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const void *V, void *O,
+                      mg_stream_t stream)
+{
+    if (!plan || !Q || !K || !V || !O)
+        return fail(MG_ERR_INVALID_ARG, "NULL plan or tensor pointer");
+    if (misaligned(Q) || misaligned(K) || misaligned(V) || misaligned(O))
+        return fail(MG_ERR_LAYOUT, "Q, K, V and O must be 16-byte aligned");
+    const mg_attn_plan_info &in = plan->info;
+    const uint64_t B = in.B, M = in.M, N = in.N, d = in.d;
+
+    // Q (B, M, d): box 64 x 128 rows; K (B, d, N): box 64 columns x d rows; V (B, N, d): box 64 x 128 rows.
+    const void *ptrs[3] = {Q, K, V};
+    const uint64_t dims[3][3] = {{d, M, B}, {N, d, B}, {d, N, B}};
+    const uint32_t box1[3] = {128u, static_cast<uint32_t>(d), 128u};
+    for (int i = 0; i < 3; ++i) {
+        if (plan->map_ptr[i] != ptrs[i]) {
+            plan->map_ptr[i] = nullptr;
+            mg_status st = encode_3d(&plan->maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i]);
+            if (st != MG_OK)
+                return st;
+            plan->map_ptr[i] = ptrs[i];
+        }
+    }
+
+    mg::FwdParams prm;
+    prm.B = static_cast<int>(B);
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.m_tiles_per_b = static_cast<int>((M + mg::kBlockM - 1) / mg::kBlockM);
+    prm.n_tiles = in.n_tiles;
+    prm.n_split = in.n_split;
+    prm.O = static_cast<__half *>(O);
+    prm.ws_o = plan->ws_o;
+    prm.ws_l = plan->ws_l;
+    prm.status = plan->status;
+    prm.timeout_ns = plan->timeout_ns;
+    prm.inject_timeout = (plan->flags & MG_FLAG_INJECT_TIMEOUT) ? 1 : 0;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(in.grid_ctas), 1, 1);
+    cfg.blockDim = dim3(mg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(in.smem_bytes);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    void *fwd_args[4] = {&plan->maps[0], &plan->maps[1], &plan->maps[2], &prm};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(plan->fwd), fwd_args);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch mg_attn_fwd_partial");
+
+    if (in.n_split > 1) {
+        int rows = static_cast<int>(B * M);
+        int n_split = in.n_split;
+        const float *wo = plan->ws_o;
+        const float *wl = plan->ws_l;
+        __half *out = static_cast<__half *>(O);
+        const long long threads = static_cast<long long>(rows) * (static_cast<long long>(d) / 8);
+        cudaLaunchConfig_t cc = cfg;
+        cc.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256), 1, 1);
+        cc.blockDim = dim3(256, 1, 1);
+        cc.dynamicSmemBytes = 0;
+        void *cargs[5] = {&wo, &wl, &out, &rows, &n_split};
+        e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(plan->combine), cargs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "launch mg_attn_combine");
+    }
+    return MG_OK;
+}
+
+mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, const void *hV, void *hO,
+                           mg_stream_t stream)
+{
+    if (!plan || !hQ || !hK || !hV || !hO)
+        return fail(MG_ERR_INVALID_ARG, "NULL plan or host pointer");
+    const mg_attn_plan_info &in = plan->info;
+    const size_t bq = static_cast<size_t>(in.B * in.M * in.d) * 2;
+    const size_t bk = static_cast<size_t>(in.B * in.d * in.N) * 2;
+    const size_t bv = bk;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t oq = 0, ok = up(bq), ov = ok + up(bk), oo = ov + up(bv), total = oo + up(bq);
+    cudaError_t e;
+    if (!plan->staging) {
+        e = cudaMalloc(&plan->staging, total);
+        if (e != cudaSuccess) {
+            plan->staging = nullptr;
+            return cuda_fail(e, "cudaMalloc(staging)");
+        }
+    }
+    uint8_t *s = static_cast<uint8_t *>(plan->staging);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((e = cudaMemcpyAsync(s + oq, hQ, bq, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(s + ok, hK, bk, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(s + ov, hV, bv, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(host to device)");
+    mg_status r = mg_attn_run(plan, s + oq, s + ok, s + ov, s + oo, stream);
+    if (r != MG_OK)
+        return r;
+    if ((e = cudaMemcpyAsync(hO, s + oo, bq, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    return MG_OK;
+}
+
+mg_status mg_attn_get_status(mg_attn_plan_t plan)
+{
+    if (!plan)
+        return fail(MG_ERR_INVALID_ARG, "NULL plan");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceSynchronize");
+    int words[2] = {0, 0};
+    e = cudaMemcpy(words, plan->status, sizeof(words), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(status)");
+    if (words[0] == MG_ERR_TIMEOUT)
+        return fail(MG_ERR_TIMEOUT, "in-kernel wait on barrier %d ran out", words[1]);
+    if (words[0] != 0)
+        return fail(MG_ERR_CUDA, "unexpected device status %d", words[0]);
+    return MG_OK;
+}
+
+mg_status mg_attn_destroy(mg_attn_plan_t plan)
+{
+    if (!plan)
+        return fail(MG_ERR_INVALID_ARG, "NULL plan");
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaFree(plan->workspace);
+    if (plan->staging)
+        cudaFree(plan->staging);
+    delete plan;
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceSynchronize");
+    return MG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,495 @@
+// mg_attn_kernels.cuh -- the two device kernels of the exp-normalised GQA graph.
+//
+// Graph (Mirage documentation, tutorials/group-query-attention, "Define GQA Computation
+// Graph"): A = matmul(Q,K); E = exp(A); S = reduction(E,2); D = div(E,S); O = matmul(D,V).
+//
+// Kernel 1, mg_attn_fwd_partial: one CTA per (batch b, 128-row tile of Q, split j of the N
+// axis). The split owns a contiguous run of 128-column tiles of K/V and loops over them,
+// as the threadblock for-loop over N with a row-sum accumulator does in Mirage's attention
+// search space (blog "Reading Mirage's muGraph search and backend generation through the
+// GQA example", section 4.2-4.3: forloop dims and the REDTOX_LD_SUM accumulator). Per tile:
+//     S  = Q . K_tile                    tcgen05 MMA, fp32 in tensor memory
+//     P  = exp(S) (0 beyond N)           fp32, one thread per row; l += rowsum(P) in fp32
+//     O += fp16(P) . V_tile              tcgen05 MMA, fp32 in tensor memory
+// The divide by the row sum commutes with the second product, so it is deferred.
+// With one split the CTA divides and writes fp16 O; otherwise it writes the fp32 partial
+// numerator O_j and row sum l_j to the workspace.
+//
+// Kernel 2, mg_attn_combine: O = (sum_j O_j) / (sum_j l_j) -> fp16, the second threadblock
+// graph of the "attention" search configuration (blog, section 4.3). No max-subtraction
+// means the partials combine by plain sums.
+//
+// Warp roles of kernel 1 (192 threads):
+//   warp 0      TMA producer: Q once, then K/V tiles through a STAGES-deep mbarrier ring
+//   warp 1      tensor-memory allocator and MMA issuer (one thread)
+//   warps 2..5  softmax + epilogue, thread = row (tensor-memory lane), 128 rows
+// Tensor memory (512 columns): S double buffer at columns [0,128) and [128,256), O at
+// [256, 256 + d).
+//
+// Every wait is bounded by a global-timer deadline. A wait that runs out records
+// MG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag, and every role then
+// stops, drains the copies/MMAs it issued (again bounded), frees tensor memory and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace mg {
+
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kPBuffers = 2;
+constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
+
+template <int D>
+struct TileCfg {
+    static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+    static constexpr int kChunks = D / 64;                  // 128-byte column chunks of a d-wide row
+    static constexpr uint32_t kQBytes = kBlockM * D * 2;    // Q tile, K-major
+    static constexpr uint32_t kKBytes = D * kBlockN * 2;    // K tile, N contiguous
+    static constexpr uint32_t kVBytes = kBlockN * D * 2;    // V tile, d contiguous
+    static constexpr uint32_t kStageBytes = kKBytes + kVBytes;
+    static constexpr uint32_t kPBytes = kBlockM * kBlockN * 2;  // P tile, K-major
+    static constexpr uint32_t kChunkRows128 = 128 * 128;        // one 128-row x 128-byte chunk
+};
+
+// Shared-memory bytes of kernel 1 for a head dim and pipeline depth (+1024 for alignment).
+__host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages)
+{
+    return 1024u + static_cast<uint32_t>(128 * d * 2) + static_cast<uint32_t>(stages) * (2u * d * 128 * 2) +
+           static_cast<uint32_t>(kPBuffers) * (128u * 128 * 2) + 256u;
+}
+
+struct FwdParams {
+    int B, M, N;
+    int m_tiles_per_b;       // ceil(M / 128)
+    int n_tiles;             // ceil(N / 128)
+    int n_split;
+    __half *O;               // (B, M, d); written here when n_split == 1
+    float *ws_o;             // (n_split, B, M, d) partial numerators
+    float *ws_l;             // (n_split, B, M) partial row sums
+    int *status;             // [0] sticky status, [1] which wait ran out
+    unsigned long long timeout_ns;
+    int inject_timeout;
+};
+
+// Barrier indices inside the CTA's barrier array.
+template <int STAGES>
+struct Bars {
+    static constexpr int kQFull = 0;
+    static constexpr int kKvFull = 1;
+    static constexpr int kKvEmpty = kKvFull + STAGES;
+    static constexpr int kSFull = kKvEmpty + STAGES;
+    static constexpr int kSEmpty = kSFull + 2;
+    static constexpr int kPFull = kSEmpty + 2;
+    static constexpr int kPEmpty = kPFull + kPBuffers;
+    static constexpr int kOFull = kPEmpty + kPBuffers;
+    static constexpr int kDrain = kOFull + 1;
+    static constexpr int kNever = kDrain + 1;
+    static constexpr int kCount = kNever + 1;
+};
+
+struct WaitCtx {
+    volatile int *abort_flag;
+    int *status;
+    unsigned long long timeout_ns;
+};
+
+// Bounded parity wait. Returns false (and the caller unwinds) if the CTA is aborting or
+// the deadline passes; the first waiter to time out records where.
+__device__ __forceinline__ bool wait_bounded(const WaitCtx &w, uint32_t bar, uint32_t parity, int where)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if (*w.abort_flag)
+            return false;
+        if (ptx::globaltimer_ns() - t0 > w.timeout_ns) {
+            *w.abort_flag = 1;
+            if (atomicCAS(w.status, 0, kStatusTimeout) == 0)
+                atomicExch(w.status + 1, where);
+            return false;
+        }
+    }
+}
+
+// Bounded wait used only while unwinding: ignores the abort flag.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns)
+{
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > timeout_ns)
+            return;
+    }
+}
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    mg_attn_fwd_partial(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const FwdParams p)
+{
+    using C = TileCfg<D>;
+    using BI = Bars<STAGES>;
+    static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = ptx::smem_u32(smem);
+    const uint32_t sStage0 = sQ + C::kQBytes;
+    const uint32_t sP0 = sStage0 + STAGES * C::kStageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kQBytes + STAGES * C::kStageBytes + kPBuffers * C::kPBytes);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // CTA -> (b, split j, row tile mt); consecutive CTAs share (b, j) and so read the same
+    // K/V tiles close together in time.
+    const int cta = blockIdx.x;
+    const int mt = cta % p.m_tiles_per_b;
+    const int j = (cta / p.m_tiles_per_b) % p.n_split;
+    const int b = cta / (p.m_tiles_per_b * p.n_split);
+    const int m0 = mt * kBlockM;
+    const int t_begin = static_cast<int>((static_cast<long long>(j) * p.n_tiles) / p.n_split);
+    const int t_end = static_cast<int>((static_cast<long long>(j + 1) * p.n_tiles) / p.n_split);
+    const int T = t_end - t_begin;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(BI::kQFull), 1);
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(bar(BI::kKvFull + s), 1);
+            ptx::mbar_init(bar(BI::kKvEmpty + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(bar(BI::kSFull + s), 1);
+            ptx::mbar_init(bar(BI::kSEmpty + s), 128);
+        }
+        for (int s = 0; s < kPBuffers; ++s) {
+            ptx::mbar_init(bar(BI::kPFull + s), 128);
+            ptx::mbar_init(bar(BI::kPEmpty + s), 1);
+        }
+        ptx::mbar_init(bar(BI::kOFull), 1);
+        ptx::mbar_init(bar(BI::kDrain), 1);
+        ptx::mbar_init(bar(BI::kNever), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmQ);
+        ptx::prefetch_tensormap(&tmK);
+        ptx::prefetch_tensormap(&tmV);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    // Everything above touched only on-chip state; global memory waits for the previous grid.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+
+    const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            bool q_armed = false;
+            int armed[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s)
+                armed[s] = 0;
+            bool ok = true;
+            if (p.inject_timeout)
+                ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
+            if (ok) {
+                ptx::mbar_arrive_expect_tx(bar(BI::kQFull), C::kQBytes);
+                q_armed = true;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)  // Q[b, m0:m0+128, 64c:64c+64]
+                    ptx::tma_load_3d(sQ + c * C::kChunkRows128, &tmQ, bar(BI::kQFull), c * 64, m0, b);
+            }
+            for (int t = 0; ok && t < T; ++t) {
+                const int s = t % STAGES;
+                const uint32_t round = static_cast<uint32_t>(t / STAGES);
+                if (t >= STAGES && !wait_bounded(wc, bar(BI::kKvEmpty + s), (round & 1u) ^ 1u, BI::kKvEmpty + s)) {
+                    ok = false;
+                    break;
+                }
+                const int n0 = (t_begin + t) * kBlockN;
+                const uint32_t sK = sStage0 + s * C::kStageBytes;
+                const uint32_t sV = sK + C::kKBytes;
+                ptx::mbar_arrive_expect_tx(bar(BI::kKvFull + s), C::kStageBytes);
+                ++armed[s];
+                // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
+                ptx::tma_load_3d(sK, &tmK, bar(BI::kKvFull + s), n0, 0, b);
+                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKvFull + s), n0 + 64, 0, b);
+                // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kKvFull + s), c * 64, n0, b);
+            }
+            if (ok) {
+                // Tail: the commits that release the last stages must land before the CTA exits.
+                for (int u = T - STAGES > 0 ? T - STAGES : 0; ok && u < T; ++u)
+                    ok = wait_bounded(wc, bar(BI::kKvEmpty + u % STAGES), static_cast<uint32_t>(u / STAGES) & 1u,
+                                      BI::kKvEmpty + u % STAGES);
+            }
+            if (*abort_flag) {
+                // Unwind: every copy issued must land before the CTA's shared memory goes away.
+                if (q_armed)
+                    wait_drain(bar(BI::kQFull), 0, p.timeout_ns);
+#pragma unroll
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed[s] > 0)
+                        wait_drain(bar(BI::kKvFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockM, kBlockN, false, true);
+            constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
+            const uint32_t tmem_o = tmem + 256;
+            bool ok = wait_bounded(wc, bar(BI::kQFull), 0, BI::kQFull);
+            if (ok)
+                ptx::tc_fence_after();
+
+            // O += P_u . V_u for local tile u.
+            auto issue_pv = [&](int u) -> bool {
+                const int pb = u % kPBuffers;
+                if (!wait_bounded(wc, bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb))
+                    return false;
+                ptx::tc_fence_after();
+                const int s = u % STAGES;
+                const uint32_t sV = sStage0 + s * C::kStageBytes + C::kKBytes;
+                const uint32_t sP = sP0 + pb * C::kPBytes;
+#pragma unroll
+                for (int k = 0; k < kBlockN / 16; ++k) {
+                    // A = P: K-major, 128 rows x 128 bytes per 64-column chunk, 8-row groups 1024 B apart.
+                    const uint64_t a = ptx::sdesc_sw128(sP + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
+                    // B = V: N(=d)-major, 16 rows of 128 B per step; d-chunks 128 rows x 128 B apart.
+                    const uint64_t bd = ptx::sdesc_sw128(sV + k * 2048, C::kChunkRows128, 1024);
+                    ptx::mma_f16_ss(tmem_o, a, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(bar(BI::kKvEmpty + s));
+                ptx::mma_commit(bar(BI::kPEmpty + pb));
+                return true;
+            };
+
+            int t = 0;
+            for (; ok && t < T; ++t) {
+                const int s = t % STAGES;
+                if (!wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(t / STAGES) & 1u, BI::kKvFull + s)) {
+                    ok = false;
+                    break;
+                }
+                const int sb = t & 1;
+                if (t >= 2 &&
+                    !wait_bounded(wc, bar(BI::kSEmpty + sb), (static_cast<uint32_t>(t >> 1) & 1u) ^ 1u, BI::kSEmpty + sb)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t sK = sStage0 + s * C::kStageBytes;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    // A = Q: K-major; 16-column steps advance 32 B inside a 128-byte swizzle row.
+                    const uint64_t a = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
+                    // B = K: N-major; 16 d-rows per step (2048 B); the two 64-column halves D*128 B apart.
+                    const uint64_t bd = ptx::sdesc_sw128(sK + k * 2048, D * 128, 1024);
+                    ptx::mma_f16_ss(tmem + sb * kBlockN, a, bd, idesc_s, k > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(bar(BI::kSFull + sb));
+                if (t >= 1 && !issue_pv(t - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok && T > 0)
+                ok = issue_pv(T - 1);
+            if (ok) {
+                ptx::mma_commit(bar(BI::kOFull));
+                // Tail: the commits that release the last P buffers must land before the CTA exits.
+                for (int u = T - kPBuffers > 0 ? T - kPBuffers : 0; ok && u < T; ++u)
+                    ok = wait_bounded(wc, bar(BI::kPEmpty + u % kPBuffers), static_cast<uint32_t>(u / kPBuffers) & 1u,
+                                      BI::kPEmpty + u % kPBuffers);
+            } else {
+                // Unwind: wait for the MMAs already issued before tensor memory is freed.
+                ptx::mma_commit(bar(BI::kDrain));
+                wait_drain(bar(BI::kDrain), 0, p.timeout_ns);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax + epilogue
+        const int q4 = warp & 3;                 // tensor-memory lane quarter this warp may access
+        const int row = q4 * 32 + lane;          // row inside the 128-row tile
+        const bool warp_rows = (m0 + q4 * 32) < p.M;  // warp-uniform: any valid row in this warp
+        const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+        constexpr float kLog2e = 1.4426950408889634f;
+        // The decision to go on is taken by the whole warp, so that no lane reaches a
+        // warp-collective tcgen05.ld without the others.
+        auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+            const bool r = wait_bounded(wc, b_, parity, where);
+            return __all_sync(0xffffffffu, r);
+        };
+        float l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int sb = t & 1;
+            const int pb = t % kPBuffers;
+            if (!warp_wait(bar(BI::kSFull + sb), static_cast<uint32_t>(t >> 1) & 1u, BI::kSFull + sb)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (t >= kPBuffers &&
+                !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
+                           BI::kPEmpty + pb)) {
+                ok = false;
+                break;
+            }
+            const int n_valid = p.N - (t_begin + t) * kBlockN;  // columns of this tile inside N
+            if (warp_rows) {
+                const uint32_t p_row = sP0 + pb * C::kPBytes + row * 128;
+#pragma unroll 1
+                for (int c = 0; c < kBlockN / 32; ++c) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_addr + sb * kBlockN + c * 32, r);
+                    ptx::tmem_ld_wait(r);
+                    float e[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float x = __uint_as_float(r[i]);
+                        const float v = ptx::ex2_approx(x * kLog2e);
+                        e[i] = (c * 32 + i < n_valid) ? v : 0.f;
+                        l += e[i];
+                    }
+                    // 32 columns = four 16-byte units of the 128-byte swizzled row of chunk c/2.
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t unit = static_cast<uint32_t>((c & 1) * 4 + q);
+                        const uint32_t addr =
+                            p_row + (c >> 1) * C::kChunkRows128 + ((unit ^ static_cast<uint32_t>(row & 7)) << 4);
+                        ptx::st_shared_v4(addr, ptx::pack_half2(e[8 * q + 0], e[8 * q + 1]),
+                                          ptx::pack_half2(e[8 * q + 2], e[8 * q + 3]),
+                                          ptx::pack_half2(e[8 * q + 4], e[8 * q + 5]),
+                                          ptx::pack_half2(e[8 * q + 6], e[8 * q + 7]));
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(BI::kSEmpty + sb));
+            ptx::mbar_arrive(bar(BI::kPFull + pb));
+        }
+
+        if (ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull)) {
+            ptx::tc_fence_after();
+            const int grow = m0 + row;
+            if (warp_rows) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_addr + 256 + c * 32, r);
+                    ptx::tmem_ld_wait(r);
+                    if (grow < p.M) {
+                        if (p.n_split == 1) {
+                            __half *dst = p.O + (static_cast<size_t>(b) * p.M + grow) * D + c * 32;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint4 w;
+                                w.x = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 0]), l),
+                                                      __fdiv_rn(__uint_as_float(r[8 * q + 1]), l));
+                                w.y = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 2]), l),
+                                                      __fdiv_rn(__uint_as_float(r[8 * q + 3]), l));
+                                w.z = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 4]), l),
+                                                      __fdiv_rn(__uint_as_float(r[8 * q + 5]), l));
+                                w.w = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 6]), l),
+                                                      __fdiv_rn(__uint_as_float(r[8 * q + 7]), l));
+                                reinterpret_cast<uint4 *>(dst)[q] = w;
+                            }
+                        } else {
+                            float *dst =
+                                p.ws_o + ((static_cast<size_t>(j) * p.B + b) * p.M + grow) * D + c * 32;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                reinterpret_cast<float4 *>(dst)[q] =
+                                    make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        }
+                    }
+                }
+                if (grow < p.M && p.n_split > 1)
+                    p.ws_l[(static_cast<size_t>(j) * p.B + b) * p.M + grow] = l;
+            }
+        }
+    }
+
+    // Teardown: every tensor-memory access of the CTA is ordered before the free.
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// O[r, c] = (sum_j ws_o[j, r, c]) / (sum_j ws_l[j, r]) -> fp16, r = b*M + m. One thread per
+// 8 consecutive columns of a row; the j sum runs in a fixed order, so results are
+// reproducible run to run.
+template <int D>
+__global__ void __launch_bounds__(256)
+    mg_attn_combine(const float *__restrict__ ws_o, const float *__restrict__ ws_l, __half *__restrict__ O,
+                    int rows, int n_split)
+{
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    constexpr int kGroups = D / 8;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<long long>(rows) * kGroups)
+        return;
+    const int r = static_cast<int>(idx / kGroups);
+    const int g = static_cast<int>(idx % kGroups);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        acc[i] = 0.f;
+    float l = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < n_split; ++j) {
+        const float4 *src = reinterpret_cast<const float4 *>(ws_o + (static_cast<size_t>(j) * rows + r) * D + g * 8);
+        const float4 a = src[0];
+        const float4 c = src[1];
+        acc[0] += a.x;
+        acc[1] += a.y;
+        acc[2] += a.z;
+        acc[3] += a.w;
+        acc[4] += c.x;
+        acc[5] += c.y;
+        acc[6] += c.z;
+        acc[7] += c.w;
+        l += ws_l[static_cast<size_t>(j) * rows + r];
+    }
+    uint4 w;
+    w.x = ptx::pack_half2(__fdiv_rn(acc[0], l), __fdiv_rn(acc[1], l));
+    w.y = ptx::pack_half2(__fdiv_rn(acc[2], l), __fdiv_rn(acc[3], l));
+    w.z = ptx::pack_half2(__fdiv_rn(acc[4], l), __fdiv_rn(acc[5], l));
+    w.w = ptx::pack_half2(__fdiv_rn(acc[6], l), __fdiv_rn(acc[7], l));
+    *reinterpret_cast<uint4 *>(O + static_cast<size_t>(r) * D + g * 8) = w;
+}
+
+}  // namespace mg

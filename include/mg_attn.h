@@ -1,0 +1,170 @@
+/*
+ * mg_attn.h -- C ABI of the fused exp-normalised GQA attention kernels for GB300 (sm_103a).
+ *
+ * Operation (Mirage documentation, tutorials/group-query-attention, "Define GQA
+ * Computation Graph"; the same graph opens section 1 of the blog "Reading Mirage's
+ * muGraph search and backend generation through the GQA example"):
+ *
+ *     A = matmul(Q, K); E = exp(A); S = reduction(E, 2); D = div(E, S); O = matmul(D, V)
+ *
+ * that is, for every batch b, query row m and column c,
+ *
+ *     O[b,m,c] = sum_n exp(A[b,m,n]) V[b,n,c] / sum_n exp(A[b,m,n]),
+ *     A[b,m,n] = sum_k Q[b,m,k] K[b,k,n],
+ *
+ * with no max-subtraction and no 1/sqrt(d) scale, exactly as the graph is written.
+ *
+ * Tensors (all contiguous, row-major, IEEE fp16, device memory of the plan's device):
+ *     Q (B, M, d)   query rows
+ *     K (B, d, N)   keys, already transposed: d rows of N contiguous columns
+ *     V (B, N, d)   values
+ *     O (B, M, d)   output
+ * The shape and stride metadata is fixed when the plan is made, like the graph's
+ * input tensors, whose row-major strides are fixed when the graph is built (blog,
+ * section 2).
+ *
+ * Arithmetic: A and P.V accumulate in fp32 on the tensor cores; exp and the row sums are
+ * fp32; exp(A) is rounded to fp16 only as the operand of the second product; the final
+ * divide is one IEEE fp32 division per element, then round-to-nearest-even to fp16.
+ * Precondition: exp(A) must fit fp16, i.e. A <= ln(65504) ~ 11.09. Larger scores make the
+ * fp16 graph itself overflow; the result is then inf/NaN and no error is reported.
+ *
+ * Status codes: the first four mirror the error enum of Mirage's CUDA transpiler
+ * (blog, section 5.1: success, insufficient shared memory, layout error, config error).
+ *
+ * Threading: plans are independent objects. One plan must not run on two streams at
+ * the same time (its split workspace is shared by its launches). No call prints,
+ * aborts or exits the process.
+ */
+#ifndef MG_ATTN_H_
+#define MG_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *mg_stream_t;
+
+typedef struct mg_attn_plan *mg_attn_plan_t; /* opaque; owned by the library */
+
+typedef enum {
+    MG_OK = 0,
+    MG_ERR_INSUFFICIENT_SMEM = 1, /* the tile configuration does not fit the device's shared memory */
+    MG_ERR_LAYOUT = 2,            /* a pointer is not 16-byte aligned, or N % 8 != 0 */
+    MG_ERR_CONFIG = 3,            /* an option is out of range (n_split, stages, timeout) */
+    MG_ERR_INVALID_ARG = 4,       /* a dimension <= 0 or too large, a NULL pointer or NULL plan */
+    MG_ERR_UNSUPPORTED = 5,       /* d not in {64, 128}, or the device is not compute capability 10.3 */
+    MG_ERR_CUDA = 6,              /* a CUDA call failed; mg_attn_last_error() has the detail */
+    MG_ERR_TIMEOUT = 7            /* a bounded in-kernel wait ran out (reported by mg_attn_get_status) */
+} mg_status;
+
+/* Flags for mg_attn_options.flags. */
+#define MG_FLAG_NO_PDL 0x1         /* launch without programmatic dependent launch */
+#define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
+                                      barrier nothing arrives on, so the bounded-wait path runs and
+                                      the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */
+
+typedef struct {
+    int32_t n_split;    /* CTAs sharing one 128-row tile along N; 0 = automatic. 1 <= n_split <= ceil(N/128) */
+    int32_t stages;     /* K/V shared-memory pipeline depth; 0 = automatic; 2..4 (d = 128: 2 only) */
+    int32_t flags;      /* MG_FLAG_* bits */
+    int32_t reserved;   /* must be 0 */
+    int64_t timeout_ns; /* bound on every in-kernel wait; 0 = 1 second; otherwise 1e3 .. 6e10 */
+} mg_attn_options;
+
+typedef struct {
+    int64_t B, M, N, d;
+    int32_t block_m;         /* rows of Q per CTA tile (128) */
+    int32_t block_n;         /* columns of K per pipeline step (128) */
+    int32_t m_tiles;         /* B * ceil(M / block_m) */
+    int32_t n_tiles;         /* ceil(N / block_n) */
+    int32_t n_split;         /* CTAs per row tile; each takes a contiguous run of column tiles */
+    int32_t stages;          /* K/V pipeline depth */
+    int32_t threads;         /* threads per CTA of the fused kernel */
+    int32_t grid_ctas;       /* m_tiles * n_split */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA of the fused kernel */
+    int32_t tmem_cols;       /* tensor-memory columns allocated per CTA */
+    int32_t kernels_per_run; /* 1 when n_split == 1 (the fused kernel writes O), else 2 */
+    int32_t num_sms;         /* streaming multiprocessors the plan was sized for */
+    int64_t workspace_bytes; /* device bytes owned by the plan (split partials + status words) */
+} mg_attn_plan_info;
+
+/*
+ * Make a plan for one problem shape on the current CUDA device. Validates the shape,
+ * chooses the tiling and the N split from the device's SM count, and allocates the
+ * plan's device workspace (fp32 partial numerators n_split*B*M*d and row sums
+ * n_split*B*M, plus two status words). Synchronous. On success *out owns the plan.
+ * Errors: MG_ERR_INVALID_ARG (dims <= 0, B*M*d or d*N beyond 2^31, out == NULL),
+ * MG_ERR_UNSUPPORTED (d not 64/128, device not cc 10.3), MG_ERR_LAYOUT (N % 8 != 0),
+ * MG_ERR_INSUFFICIENT_SMEM, MG_ERR_CUDA (no device, allocation failed).
+ */
+mg_status mg_attn_plan(int64_t B, int64_t M, int64_t N, int64_t d, mg_attn_plan_t *out);
+
+/* As mg_attn_plan, with explicit options (NULL = defaults). Adds MG_ERR_CONFIG. */
+mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d,
+                          const mg_attn_options *opts, mg_attn_plan_t *out);
+
+/*
+ * Enqueue O = attention(Q, K, V) on `stream`. Asynchronous and stream-ordered: no
+ * synchronisation, no allocation. Q, K, V, O are device pointers with the plan's shape
+ * (see the top of this file), 16-byte aligned; O must not overlap the inputs. The caller
+ * keeps ownership of all four. With programmatic dependent launch (the default) the
+ * kernels still wait for all prior work on `stream` before touching global memory.
+ * Errors: MG_ERR_INVALID_ARG (NULL plan or pointer), MG_ERR_LAYOUT (misaligned pointer),
+ * MG_ERR_CUDA (descriptor encoding or launch failed; the plan's device must be current).
+ * In-kernel timeouts are not visible here; see mg_attn_get_status.
+ */
+mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const void *V,
+                      void *O, mg_stream_t stream);
+
+/*
+ * End-to-end variant for host buffers: copies Q, K, V from host memory into device
+ * buffers owned by the plan, runs as mg_attn_run, and copies O back into host memory,
+ * all enqueued on `stream` (pinned host memory makes the copies asynchronous; the caller
+ * synchronises the stream before reading hO). The plan's device staging buffers (the
+ * size of Q, K, V and O) are allocated by the first call on that plan and reused after.
+ * Errors: as mg_attn_run, plus MG_ERR_CUDA if the staging allocation fails.
+ */
+mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, const void *hV,
+                           void *hO, mg_stream_t stream);
+
+/* Synchronise the device, free the plan's workspace and the plan. NULL is MG_ERR_INVALID_ARG. */
+mg_status mg_attn_destroy(mg_attn_plan_t plan);
+
+/*
+ * Sticky device-side status of the plan: MG_OK, or MG_ERR_TIMEOUT once any in-kernel wait
+ * of any run of this plan ran out (the kernels then stop early and O is undefined).
+ * Synchronises the device to read it. MG_ERR_CUDA if the read itself fails.
+ */
+mg_status mg_attn_get_status(mg_attn_plan_t plan);
+
+/* Copy the plan's decisions into *info. */
+mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info);
+
+/*
+ * Host-only: the decisions mg_attn_plan_ex would take for this shape on a device with
+ * `num_sms` SMs and `max_smem_optin` bytes of opt-in shared memory per block, without
+ * touching any GPU. Same validation and error codes as mg_attn_plan_ex (minus device errors).
+ */
+mg_status mg_attn_query(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts,
+                        int32_t num_sms, int32_t max_smem_optin, mg_attn_plan_info *info);
+
+/* Static English text for a status code (never NULL). */
+const char *mg_attn_status_string(mg_status s);
+
+/* Detail of the last failure on the calling thread (e.g. the CUDA error name); "" if none. */
+const char *mg_attn_last_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int32_t mg_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MG_ATTN_H_ */

@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, exports every
+symbol include/mg_attn.h declares, its structs match the header's layout, the planner's
+decisions and validation, and the product package's independence from the oracle."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import attention_mugraph_gb300 as mg
+from attention_mugraph_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mg_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:mg_status|const char \*|int32_t)\s*\*?\s*(mg_attn_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    assert sorted(_lib.EXPORTS) == names
+    for name in names:
+        assert hasattr(lib, name), f"{name} not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    for name in names:
+        assert re.search(rf"\bT {name}$", out, re.M), f"{name} is not a defined text symbol"
+
+
+def test_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text("""
+#include <stdio.h>
+#include <stddef.h>
+#include "mg_attn.h"
+int main(void) {
+  printf("%zu %zu %zu\\n", sizeof(mg_attn_options), offsetof(mg_attn_options, timeout_ns), offsetof(mg_attn_options, flags));
+  printf("%zu %zu %zu %zu\\n", sizeof(mg_attn_plan_info), offsetof(mg_attn_plan_info, block_m),
+         offsetof(mg_attn_plan_info, num_sms), offsetof(mg_attn_plan_info, workspace_bytes));
+  return 0;
+}
+""")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    l1, l2 = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")[:2]
+    O, I = _lib.MgAttnOptions, _lib.MgAttnPlanInfo
+    assert [int(x) for x in l1.split()] == [ctypes.sizeof(O), O.timeout_ns.offset, O.flags.offset]
+    assert [int(x) for x in l2.split()] == [ctypes.sizeof(I), I.block_m.offset, I.num_sms.offset,
+                                            I.workspace_bytes.offset]
+
+
+def test_status_strings_and_version(lib):
+    for s in range(0, 8):
+        assert lib.mg_attn_status_string(s)
+    assert b"unknown" in lib.mg_attn_status_string(99)
+    assert lib.mg_attn_version() == 10000
+
+
+def tile_ranges(n_tiles, n_split):
+    # The fused kernel's split j owns tiles [j*T/S, (j+1)*T/S).
+    return [(j * n_tiles // n_split, (j + 1) * n_tiles // n_split) for j in range(n_split)]
+
+
+@pytest.mark.parametrize("B,M,N,d", [(2, 64, 1024, 64), (2, 256, 4096, 64), (16, 256, 4096, 64),
+                                     (16, 8, 32768, 128), (2, 256, 65536, 64), (1, 1, 8, 64), (300, 256, 256, 64)])
+def test_query_decisions(B, M, N, d):
+    info = mg.mg_attn_query(B, M, N, d, num_sms=152)
+    m_tiles = B * -(-M // 128)
+    n_tiles = -(-N // 128)
+    assert info["m_tiles"] == m_tiles and info["n_tiles"] == n_tiles
+    assert 1 <= info["n_split"] <= n_tiles
+    assert info["grid_ctas"] == m_tiles * info["n_split"]
+    if m_tiles >= 152:
+        assert info["n_split"] == 1
+    else:
+        assert info["grid_ctas"] <= 152  # one wave
+    assert info["kernels_per_run"] == (2 if info["n_split"] > 1 else 1)
+    assert info["smem_bytes"] <= 232448
+    rng = tile_ranges(n_tiles, info["n_split"])
+    assert rng[0][0] == 0 and rng[-1][1] == n_tiles
+    assert all(a < b for a, b in rng) and all(rng[i][1] == rng[i + 1][0] for i in range(len(rng) - 1))
+    ws = 256 + (info["n_split"] * B * M * (d + 1) * 4 if info["n_split"] > 1 else 0)
+    assert info["workspace_bytes"] == ws
+
+
+def test_query_options():
+    info = mg.mg_attn_query(2, 256, 4096, 64, 152, n_split=5, stages=2)
+    assert info["n_split"] == 5 and info["stages"] == 2
+    assert mg.mg_attn_query(2, 256, 4096, 128, 152)["stages"] == 2
+
+
+@pytest.mark.parametrize("args,kw,code", [
+    ((0, 256, 4096, 64), {}, mg.MG_ERR_INVALID_ARG),
+    ((2, -1, 4096, 64), {}, mg.MG_ERR_INVALID_ARG),
+    ((2, 256, 4096, 32), {}, mg.MG_ERR_UNSUPPORTED),
+    ((2, 256, 4100, 64), {}, mg.MG_ERR_LAYOUT),
+    ((2, 256, 4096, 64), {"n_split": 33}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"stages": 5}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x80}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 128), {"stages": 3}, mg.MG_ERR_INSUFFICIENT_SMEM),
+    ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),
+    ((2, 1 << 31, 4096, 64), {}, mg.MG_ERR_INVALID_ARG),
+])
+def test_query_rejects(args, kw, code):
+    with pytest.raises(mg.MgAttnError) as e:
+        mg.mg_attn_query(*args, num_sms=152, **kw)
+    assert e.value.status == code
+
+
+def test_null_arguments_rejected_without_gpu(lib):
+    assert lib.mg_attn_run(None, None, None, None, None, None) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_attn_run_host(None, None, None, None, None, None) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_attn_destroy(None) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_attn_get_status(None) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_attn_plan(2, 256, 4096, 64, None) == mg.MG_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_plan_without_device_fails_cleanly(lib):
+    h = ctypes.c_void_p()
+    st = lib.mg_attn_plan(2, 256, 4096, 64, ctypes.byref(h))
+    assert st == mg.MG_ERR_CUDA and not h.value
+    assert lib.mg_attn_last_error()
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "attention_mugraph_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "mg_oracle" not in text and "libmgoracle" not in text, f

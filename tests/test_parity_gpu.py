@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the same seeded
+fp16 inputs, elementwise within max|O_gpu - O_ref| <= 2e-3 * (1 + |O_ref|).
+
+Covers the five workloads at full size, a shape sweep with ragged M and N tails over both head
+dims, every N split and pipeline depth, degenerate inputs with closed forms, the largest N,
+determinism, the host-buffer entry point, CUDA-graph capture and the bounded-wait status path.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import attention_mugraph_gb300 as mg
+from attention_mugraph_gb300 import _lib, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 2e-3  # the acceptance bound: |err| <= RTOL * (1 + |ref|)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    _lib.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def assert_parity(o_gpu, ref, what=""):
+    o = o_gpu.float().cpu().numpy().astype(np.float64) if isinstance(o_gpu, torch.Tensor) else o_gpu
+    assert o.shape == ref.shape, what
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    err = np.abs(o - ref)
+    bound = RTOL * (1.0 + np.abs(ref))
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), (f"{what}: max err {err.max():.3e}; worst at {worst}: gpu {o[worst]} "
+                                  f"ref {ref[worst]}")
+    return float(err.max())
+
+
+def run_gpu(q, k, v, **opts):
+    B, M, d = q.shape
+    N = k.shape[2]
+    plan = mg.Plan(B, M, N, d, **opts)
+    Q, K, V = q.cuda(), k.cuda(), v.cuda()
+    O = torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda")
+    plan.run(Q, K, V, O)
+    torch.cuda.synchronize()
+    assert plan.status() == mg.MG_OK
+    return O, plan
+
+
+@pytest.mark.parametrize("name", inputs.CONFIG_ORDER)
+def test_workload_parity_full_size(name):
+    q, k, v, _ = inputs.make_config(name)
+    ref = oracle.attention(q, k, v)
+    O, plan = run_gpu(q, k, v)
+    assert_parity(O, ref, f"{name} n_split={plan.info['n_split']}")
+
+
+SWEEP = [  # (B, M, N, d, n_split) with ragged M (not a multiple of 128) and N (not of 128)
+    (1, 1, 8, 64, 0), (1, 1, 8, 128, 0), (3, 129, 136, 64, 0), (2, 300, 1000, 64, 3),
+    (1, 127, 4104, 128, 0), (2, 200, 2056, 64, 1), (1, 128, 128, 64, 1), (4, 64, 6216, 64, 7),
+    (1, 513, 256, 128, 2), (2, 17, 65544, 64, 0), (5, 33, 520, 128, 5), (1, 256, 384, 64, 3),
+    (7, 3, 1024, 128, 8), (1, 1000, 8192, 64, 0),
+]
+
+
+@pytest.mark.parametrize("B,M,N,d,n_split", SWEEP)
+def test_shape_sweep(B, M, N, d, n_split):
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=B * 1000 + M + N)
+    ref = oracle.attention(q, k, v)
+    O, _ = run_gpu(q, k, v, n_split=n_split)
+    assert_parity(O, ref, f"{B, M, N, d, n_split}")
+
+
+@pytest.mark.parametrize("n_split,stages", [(1, 4), (2, 2), (3, 3), (5, 4), (32, 2), (31, 3)])
+def test_split_and_pipeline_depth(n_split, stages):
+    q, k, v, _ = inputs.make_config("gqa")
+    ref = oracle.attention(q, k, v)
+    O, _ = run_gpu(q, k, v, n_split=n_split, stages=stages)
+    assert_parity(O, ref, f"n_split={n_split} stages={stages}")
+
+
+def test_k_zero_gives_mean_of_v_with_ragged_tail():
+    # Scores 0 everywhere -> every weight is exp(0)=1: any column past N that leaked into the row
+    # sum (zero-filled K gives exp(0)=1 too) would pull the mean toward 0.
+    B, M, N, d = 2, 130, 1032, 64
+    _, _, v = inputs.make_inputs(B, M, N, d, seed=3)
+    q = torch.randn((B, M, d)).half()
+    k = torch.zeros((B, d, N), dtype=torch.float16)
+    O, _ = run_gpu(q, k, v, n_split=3)
+    want = v.double().numpy().mean(axis=1, keepdims=True).repeat(M, axis=1)
+    assert_parity(O, want, "K=0")
+
+
+def test_constant_v():
+    B, M, N, d = 1, 64, 2048, 128
+    q, k, _ = inputs.make_inputs(B, M, N, d, 0.25, seed=4)
+    v = torch.full((B, N, d), -1.5, dtype=torch.float16)
+    O, _ = run_gpu(q, k, v)
+    assert torch.all(O.float() == -1.5) or assert_parity(O, np.full((B, M, d), -1.5), "V=const") is not None
+
+
+def test_single_key_single_query():
+    q, k, v = inputs.make_inputs(3, 1, 8, 64, 0.5, seed=5)
+    k[:, :, 1:] = -8.0  # exp(-8 * q) spread; keep it a normal problem with 8 keys
+    ref = oracle.attention(q, k, v)
+    O, _ = run_gpu(q, k, v)
+    assert_parity(O, ref, "M=1,N=8")
+
+
+def test_largest_n_sampled_rows():
+    # N = 2^20 keys: row sums of a million fp32 terms; checked on sampled rows.
+    B, M, N, d = 1, 256, 1 << 20, 64
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.5, seed=6)
+    O, plan = run_gpu(q, k, v)
+    rows = list(range(0, B * M, 17)) + [B * M - 1]
+    ref = oracle.attention_rows(q, k, v, rows)
+    got = O.float().cpu().numpy().astype(np.float64).reshape(-1, d)[rows]
+    assert_parity(got, ref, f"N=2^20 n_split={plan.info['n_split']}")
+
+
+def test_deterministic_and_pdl_invariant():
+    q, k, v, _ = inputs.make_config("gqa")
+    O1, _ = run_gpu(q, k, v)
+    O2, _ = run_gpu(q, k, v)
+    O3, _ = run_gpu(q, k, v, flags=mg.MG_FLAG_NO_PDL)
+    assert torch.equal(O1, O2) and torch.equal(O1, O3)
+
+
+def test_back_to_back_runs_on_side_stream():
+    # Many calls queued on one non-default stream, alternating two input sets, each checked.
+    sets = [inputs.make_inputs(2, 256, 4096, 64, 0.5, seed=s) for s in (10, 11)]
+    refs = [oracle.attention(*s) for s in sets]
+    plan = mg.Plan(2, 256, 4096, 64)
+    dev = [[t.cuda() for t in s] for s in sets]
+    outs = [torch.empty((2, 256, 64), dtype=torch.float16, device="cuda") for _ in range(6)]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i, o in enumerate(outs):
+            plan.run(*dev[i % 2], o, stream=stream)
+    stream.synchronize()
+    for i, o in enumerate(outs):
+        assert_parity(o, refs[i % 2], f"call {i}")
+
+
+def test_cuda_graph_capture_replay():
+    q, k, v, _ = inputs.make_config("gqa")
+    ref = oracle.attention(q, k, v)
+    plan = mg.Plan(2, 256, 4096, 64)
+    Q, K, V = q.cuda(), k.cuda(), v.cuda()
+    O = torch.zeros((2, 256, 64), dtype=torch.float16, device="cuda")
+    plan.run(Q, K, V, O)  # warm-up outside capture
+    torch.cuda.synchronize()
+    O.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        plan.run(Q, K, V, O, stream=s)
+        g.capture_end()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert_parity(O, ref, "graph replay")
+
+
+def test_host_buffer_entry_point():
+    q, k, v, _ = inputs.make_config("tiny")
+    ref = oracle.attention(q, k, v)
+    plan = mg.Plan(2, 64, 1024, 64)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty((2, 64, 64), dtype=torch.float16).pin_memory()
+    for _ in range(2):
+        plan.run_host(hq, hk, hv, ho)
+        torch.cuda.synchronize()
+        assert_parity(ho, ref, "run_host")
+
+
+def test_misaligned_pointer_rejected():
+    plan = mg.Plan(1, 128, 1024, 64)
+    buf = torch.zeros(1 * 128 * 64 + 8, dtype=torch.float16, device="cuda")
+    k = torch.zeros((1, 64, 1024), dtype=torch.float16, device="cuda")
+    v = torch.zeros((1, 1024, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(mg.MgAttnError) as e:
+        plan.run_ptr(buf.data_ptr() + 2, k.data_ptr(), v.data_ptr(), buf.data_ptr())
+    assert e.value.status == mg.MG_ERR_LAYOUT
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    # The load warp waits on a barrier nothing arrives on (before issuing any copy); the wait
+    # runs out after 2 ms, every role unwinds, and the plan's sticky status says so.
+    q, k, v, _ = inputs.make_config("tiny")
+    plan = mg.Plan(2, 64, 1024, 64, flags=mg.MG_FLAG_INJECT_TIMEOUT, timeout_ns=2_000_000)
+    Q, K, V = q.cuda(), k.cuda(), v.cuda()
+    O = torch.zeros((2, 64, 64), dtype=torch.float16, device="cuda")
+    plan.run(Q, K, V, O)
+    assert plan.status() == mg.MG_ERR_TIMEOUT
+    assert b"barrier" in _lib.load_library().mg_attn_last_error()
+    # The context is still usable: a normal plan runs and matches the oracle.
+    O2, _ = run_gpu(q, k, v)
+    assert_parity(O2, oracle.attention(q, k, v), "after timeout")
