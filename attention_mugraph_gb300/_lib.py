@@ -30,7 +30,7 @@ MG_FLAG_INJECT_TIMEOUT = 0x2
 # Every function include/mg_attn.h declares.
 EXPORTS = ("mg_attn_plan", "mg_attn_plan_ex", "mg_attn_run", "mg_attn_run_host", "mg_attn_destroy",
            "mg_attn_get_status", "mg_attn_get_info", "mg_attn_query", "mg_attn_status_string",
-           "mg_attn_last_error", "mg_attn_version")
+           "mg_attn_last_error", "mg_attn_version", "mg_attn_set_timing_events")
 
 
 class MgAttnOptions(ctypes.Structure):
@@ -91,6 +91,8 @@ def _bind(lib):
     lib.mg_attn_status_string.restype = ctypes.c_char_p
     lib.mg_attn_last_error.argtypes = []
     lib.mg_attn_last_error.restype = ctypes.c_char_p
+    lib.mg_attn_set_timing_events.argtypes = [vp, vp, vp]
+    lib.mg_attn_set_timing_events.restype = st
     lib.mg_attn_version.argtypes = []
     lib.mg_attn_version.restype = i32
     return lib
@@ -186,6 +188,15 @@ class Plan:
         _check(self._lib.mg_attn_run_host(self._h, hQ.data_ptr(), hK.data_ptr(), hV.data_ptr(), hO.data_ptr(),
                                           _stream_handle(stream)), "mg_attn_run_host")
         return hO
+
+    def set_timing_events(self, ev_begin=None, ev_end=None):
+        """Record two torch.cuda.Event objects around the fused kernel of later runs (None: off).
+        The events must already exist on the CUDA side (torch creates them on their first record)."""
+        b = ctypes.c_void_p(ev_begin.cuda_event) if ev_begin is not None else None
+        e = ctypes.c_void_p(ev_end.cuda_event) if ev_end is not None else None
+        if (ev_begin is not None and not b.value) or (ev_end is not None and not e.value):
+            raise ValueError("record the events once before handing them to the library")
+        _check(self._lib.mg_attn_set_timing_events(self._h, b, e), "mg_attn_set_timing_events")
 
     def status(self) -> int:
         """Sticky device status (synchronises the device): MG_OK or MG_ERR_TIMEOUT."""

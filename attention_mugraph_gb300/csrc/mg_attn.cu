@@ -208,6 +208,9 @@ struct mg_attn_plan {
     CUtensorMap maps[3];
     // Device staging for mg_attn_run_host, allocated by its first call.
     void *staging = nullptr;
+    // Optional events recorded around the fused kernel (mg_attn_set_timing_events).
+    cudaEvent_t ev_begin = nullptr;
+    cudaEvent_t ev_end = nullptr;
 };
 
 extern "C" {
@@ -309,6 +312,15 @@ mg_status mg_attn_plan(int64_t B, int64_t M, int64_t N, int64_t d, mg_attn_plan_
     return mg_attn_plan_ex(B, M, N, d, nullptr, out);
 }
 
+mg_status mg_attn_set_timing_events(mg_attn_plan_t plan, void *ev_begin, void *ev_end)
+{
+    if (!plan || (ev_begin == nullptr) != (ev_end == nullptr))
+        return fail(MG_ERR_INVALID_ARG, "NULL plan, or only one of the two events");
+    plan->ev_begin = static_cast<cudaEvent_t>(ev_begin);
+    plan->ev_end = static_cast<cudaEvent_t>(ev_end);
+    return MG_OK;
+}
+
 mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info)
 {
     if (!plan || !info)
@@ -368,9 +380,14 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     void *fwd_args[4] = {&plan->maps[0], &plan->maps[1], &plan->maps[2], &prm};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(plan->fwd), fwd_args);
+    cudaError_t e;
+    if (plan->ev_begin && (e = cudaEventRecord(plan->ev_begin, cfg.stream)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord(begin)");
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(plan->fwd), fwd_args);
     if (e != cudaSuccess)
         return cuda_fail(e, "launch mg_attn_fwd_partial");
+    if (plan->ev_end && (e = cudaEventRecord(plan->ev_end, cfg.stream)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord(end)");
 
     if (in.n_split > 1) {
         int rows = static_cast<int>(B * M);

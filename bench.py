@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused exp-normalised GQA attention path on GB300.
+
+One step = one ``mg_attn_run`` (the fused partial kernel plus, when the N axis is split, the
+combine kernel) over one batch of the GQA tutorial workload: Q (2,256,64), K (2,64,4096),
+V (2,4096,64) fp16, Q,K ~ U(-0.5,0.5), V ~ N(0,1), seed 0 (Mirage documentation,
+tutorials/group-query-attention, "Define GQA Computation Graph").
+
+Timing follows the method the Mirage docs describe for candidate kernels (warm-up runs,
+then CUDA events around a long run of back-to-back calls, time / calls), on one stream,
+with these additions:
+  * every step reads a different input/output buffer set; the sets together are more than
+    twice the L2 size, so each call reads its inputs from HBM, not L2;
+  * the timed steps are replayed from a CUDA graph (host launch cost excluded); a plain
+    stream loop is timed too and reported beside it;
+  * the fused kernel alone is timed with events the library records around it, for the
+    roofline fraction;
+  * the end-to-end number runs the host-buffer entry point: host->device copies of Q, K, V,
+    the kernels, and the device->host copy of O, every step.
+The CPU baseline is the fp64 oracle (test infrastructure) on the host cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU: one process per GPU under torch.distributed.run; every rank runs its own
+independent replica (the path needs no exchange), value = all ranks' FLOPs / max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GQA muGraph TFLOP/s and µs/call at 1 GB300; % of roofline"
+WORKLOAD = "gqa"  # Q (2,256,64), K (2,64,4096), V (2,4096,64)
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "mg_attn_fwd_partial_gqa.md")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
+    return ap.parse_args()
+
+
+def workload_shape():
+    from attention_mugraph_gb300 import inputs
+
+    B, M, N, d, a = inputs.CONFIGS[WORKLOAD]
+    return B, M, N, d, a
+
+
+def flops_per_step(B, M, N, d):
+    return 4.0 * B * M * N * d
+
+
+def bytes_per_step(B, M, N, d):
+    return 2.0 * (B * M * d + B * d * N + B * N * d + B * M * d)
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_PATH):
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest():
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in ("attention_mugraph_gb300/csrc/mg_attn_kernels.cuh", "attention_mugraph_gb300/csrc/ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it was taken
+    on the current kernel source (its digest line matches); else None."""
+    if not os.path.exists(TRAFFIC_PATH):
+        return None
+    fields = {}
+    with open(TRAFFIC_PATH) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU (oracle) timing
+
+def time_oracle(q, k, v, seconds: float, rows_per_call=None):
+    """Run the fp64 oracle repeatedly for about `seconds`; returns (calls, elapsed, rows, threads).
+    rows_per_call=None runs the whole workload per call, else that many leading rows."""
+    import oracle
+
+    lib = oracle.load_library()
+    threads = oracle.max_threads(lib)
+    B, M, d = q.shape
+    rows = list(range(B * M if rows_per_call is None else min(rows_per_call, B * M)))
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention_rows(q, k, v, rows, threads=threads, lib=lib)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return calls, el, len(rows), threads
+
+
+def cpu_baseline(q, k, v, seconds):
+    B, M, N, d = q.shape[0], q.shape[1], k.shape[2], q.shape[2]
+    calls, el, rows, threads = time_oracle(q, k, v, seconds)
+    fl = 4.0 * rows * N * d * calls
+    return {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{calls} full oracle evaluations of the {WORKLOAD} workload ({rows} rows x N={N} x d={d}, "
+                      f"fp64) in {el:.1f} s on {threads} host threads"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import torch
+
+    from attention_mugraph_gb300 import inputs
+
+    B, M, N, d, a = workload_shape()
+    q, k, v = inputs.make_inputs(B, M, N, d, a, seed=0)
+    import oracle
+
+    lib = oracle.load_library()
+    threads = oracle.max_threads(lib)
+    # Size each step's sample (leading rows of the workload) so the whole run takes ~2 minutes.
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, list(range(B * M)), threads=threads, lib=lib)
+    per_row = (time.perf_counter() - t0) / (B * M)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows_per_step = int(max(1, min(B * M, budget / max(per_row, 1e-9))))
+    rows = list(range(rows_per_step))
+    for _ in range(args.warmup):
+        oracle.attention_rows(q, k, v, rows, threads=threads, lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_rows(q, k, v, rows, threads=threads, lib=lib)
+    el = time.perf_counter() - t0
+    fl = 4.0 * rows_per_step * N * d * args.steps
+    value = fl / el / 1e12
+    sample = (f"each step: the first {rows_per_step} of {B * M} rows of the {WORKLOAD} workload "
+              f"(N={N}, d={d}) in fp64 on {threads} host threads")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(B, M, N, d, a, extra={"arm": "fp64 CPU oracle"}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    del torch
+
+
+def workload_config(B, M, N, d, a, extra=None):
+    cfg = {"workload": f"GQA tutorial graph: Q ({B},{M},{d}), K ({B},{d},{N}), V ({B},{N},{d}) fp16",
+           "B": B, "M": M, "N": N, "d": d, "inputs": f"Q,K ~ U(-{a},{a}), V ~ N(0,1), seed 0"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import attention_mugraph_gb300 as mg
+    from attention_mugraph_gb300 import build, inputs
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    build.build()
+    B, M, N, d, a = workload_shape()
+    fl = flops_per_step(B, M, N, d)
+    alg_bytes = bytes_per_step(B, M, N, d)
+
+    q, k, v = inputs.make_inputs(B, M, N, d, a, seed=0)
+    props = torch.cuda.get_device_properties(local_rank)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024)
+    set_bytes = int(alg_bytes)
+    n_sets = max(2, math.ceil(2 * l2 / set_bytes))
+    Qs = [q.cuda() for _ in range(n_sets)]
+    Ks = [k.cuda() for _ in range(n_sets)]
+    Vs = [v.cuda() for _ in range(n_sets)]
+    Os = [torch.empty((B, M, d), dtype=torch.float16, device="cuda") for _ in range(n_sets)]
+    ptrs = [(Qs[i].data_ptr(), Ks[i].data_ptr(), Vs[i].data_ptr(), Os[i].data_ptr()) for i in range(n_sets)]
+
+    plan = mg.Plan(B, M, N, d)
+    info = plan.info
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+
+    def step(i):
+        plan.run_ptr(*ptrs[i % n_sets], stream=sh)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+
+    # Graphs: one covers a whole rotation of buffer sets; a second covers the remainder.
+    def capture(count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(count):
+                step(i)
+            g.capture_end()
+        return g
+
+    full, rem = divmod(args.steps, n_sets)
+    g_full = capture(n_sets) if full else None
+    g_rem = capture(rem) if rem else None
+    for _ in range(3):  # graph warm-up
+        if g_full:
+            g_full.replay()
+        if g_rem:
+            g_rem.replay()
+    stream.synchronize()
+
+    def timed(fn):
+        barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        fn()
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    def graph_steps():
+        with torch.cuda.stream(stream):
+            for _ in range(full):
+                g_full.replay()
+            if g_rem:
+                g_rem.replay()
+
+    # Timed region 1 (the value): K steps replayed from CUDA graphs, clocks sampled meanwhile.
+    with ClockSampler(local_rank) as clocks:
+        ms_graph = timed(graph_steps)
+    clk = clocks.summary()
+
+    # Timed region 2: the same K steps as a plain host loop of mg_attn_run calls.
+    def loop_steps():
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step(i)
+
+    ms_loop = timed(loop_steps)
+
+    # Fused kernel alone: events recorded by the library around it, one rotation of sets.
+    n_k = min(args.steps, max(n_sets, 1000))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
+    for pair in evs:  # torch creates the CUDA event on its first record; the library re-records it
+        for ev in pair:
+            ev.record(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(n_k):
+            plan.set_timing_events(*evs[i])
+            step(i)
+    plan.set_timing_events(None, None)
+    stream.synchronize()
+    k_ms = [b.elapsed_time(e) for b, e in evs]
+    fwd_us = statistics.mean(k_ms) * 1e3
+    fwd_us_median = statistics.median(k_ms) * 1e3
+
+    # End to end through the host-buffer entry point (pinned host memory), every step copying
+    # Q, K, V in and O out.
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty((B, M, d), dtype=torch.float16).pin_memory()
+    n_e2e = min(args.steps, 2000)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            plan.run_host(hq, hk, hv, ho, stream=stream)
+    stream.synchronize()
+
+    def e2e_steps():
+        with torch.cuda.stream(stream):
+            for _ in range(n_e2e):
+                plan.run_host(hq, hk, hv, ho, stream=stream)
+
+    ms_e2e = timed(e2e_steps)
+    h2d = int(q.numel() + k.numel() + v.numel()) * 2
+    d2h = int(ho.numel()) * 2
+
+    st = plan.status()
+    if st != mg.MG_OK:
+        raise SystemExit(f"device status {st} after the bench")
+
+    peaks, peak_kind = load_peaks()
+    t_tensor = fl / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "hbm" if t_hbm >= t_tensor else "tensor"
+    if bound == "hbm":
+        achieved = alg_bytes / (fwd_us * 1e-6) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    else:
+        achieved = fl / (fwd_us * 1e-6) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+
+    if rank != 0:
+        return
+    us_graph = ms_graph * 1e3 / args.steps
+    us_loop = ms_loop * 1e3 / args.steps
+    value = fl * world * args.steps / (ms_graph * 1e-3) / 1e12
+    roof_t = max(t_tensor, t_hbm)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_graph / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": workload_config(B, M, N, d, a, extra={
+            "l2": (f"inputs larger than L2: {n_sets} rotating Q/K/V/O buffer sets of {set_bytes} B "
+                   f"({n_sets * set_bytes / 2**20:.0f} MiB, > 2x the {l2 / 2**20:.0f} MiB L2); each step "
+                   f"reads a set untouched for {n_sets - 1} steps"),
+            "launch": "CUDA graph replay of back-to-back mg_attn_run calls on one stream",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "n_split": info["n_split"], "grid_ctas": info["grid_ctas"], "stages": info["stages"],
+            "kernels_per_step": info["kernels_per_run"]}),
+        "us_per_call": us_graph,
+        "roofline_time_us": roof_t * 1e6,
+        "roofline_fraction_of_step": roof_t * 1e6 / us_graph,
+        "stream_loop": {"us_per_call": us_loop, "value": fl * args.steps / (ms_loop * 1e-3) / 1e12,
+                        "unit": "TFLOP/s"},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": recorded_traffic(), "kernel": "mg_attn_fwd_partial",
+                     "kernel_us_mean": fwd_us, "kernel_us_median": fwd_us_median,
+                     "algorithmic_bytes_per_launch": alg_bytes, "flops_per_launch": fl,
+                     "peak_source": f"{peak_kind}: MEASURED_PEAKS.json "
+                                    f"{'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'} (burst)",
+                     "tensor_frac": fl / (fwd_us * 1e-6) / 1e12 / peaks["bf16_tflops"]},
+        "e2e": {"value": fl * n_e2e / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": n_e2e, "us_per_call": ms_e2e * 1e3 / n_e2e},
+        "gpu_launches": args.steps * info["kernels_per_run"],
+        "clocks": clk,
+    }
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline(q, k, v, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    plan.destroy()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

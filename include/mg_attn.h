@@ -143,6 +143,17 @@ mg_status mg_attn_destroy(mg_attn_plan_t plan);
  */
 mg_status mg_attn_get_status(mg_attn_plan_t plan);
 
+/*
+ * Measurement hook. When both events are non-NULL, every later mg_attn_run / mg_attn_run_host
+ * on this plan records ev_begin on its stream just before the fused kernel's launch and ev_end
+ * just after it (before the combine kernel), so that cudaEventElapsedTime(ev_begin, ev_end)
+ * times the fused kernel alone. The events are cudaEvent_t handles owned by the caller, who
+ * keeps them alive while the hook is set; NULL, NULL removes it. A recorded event between two
+ * launches suspends the programmatic-launch overlap of those two kernels, so leave the hook
+ * off for throughput runs. Errors: MG_ERR_INVALID_ARG for a NULL plan or exactly one NULL event.
+ */
+mg_status mg_attn_set_timing_events(mg_attn_plan_t plan, void *ev_begin, void *ev_end);
+
 /* Copy the plan's decisions into *info. */
 mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info);
 
