@@ -395,9 +395,9 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
         const float *wo = plan->ws_o;
         const float *wl = plan->ws_l;
         __half *out = static_cast<__half *>(O);
-        const long long threads = static_cast<long long>(rows) * (static_cast<long long>(d) / 8);
+        const int rows_per_cta = d == 64 ? mg::CombineCfg<64>::kRows : mg::CombineCfg<128>::kRows;
         cudaLaunchConfig_t cc = cfg;
-        cc.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256), 1, 1);
+        cc.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), 1, 1);
         cc.blockDim = dim3(256, 1, 1);
         cc.dynamicSmemBytes = 0;
         void *cargs[5] = {&wo, &wl, &out, &rows, &n_split};

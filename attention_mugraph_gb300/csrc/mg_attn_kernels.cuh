@@ -448,48 +448,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// O[r, c] = (sum_j ws_o[j, r, c]) / (sum_j ws_l[j, r]) -> fp16, r = b*M + m. One thread per
-// 8 consecutive columns of a row; the j sum runs in a fixed order, so results are
+// O[r, c] = (sum_j ws_o[j, r, c]) / (sum_j ws_l[j, r]) -> fp16, r = b*M + m.
+// A CTA of 256 threads covers kRows rows. Thread (row, part, g) sums float4 column group g of its
+// row over the splits j = part, part + kParts, ... (independent loads, all in flight together);
+// the kParts partial sums then meet in shared memory in a fixed order, so the result is
 // reproducible run to run.
+template <int D>
+struct CombineCfg {
+    static constexpr int kGroups = D / 4;                  // float4 groups per row
+    static constexpr int kParts = 4;                       // split-index residues per row
+    static constexpr int kRows = 256 / (kGroups * kParts); // rows per CTA: 4 (d=64) or 2 (d=128)
+};
+
 template <int D>
 __global__ void __launch_bounds__(256)
     mg_attn_combine(const float *__restrict__ ws_o, const float *__restrict__ ws_l, __half *__restrict__ O,
                     int rows, int n_split)
 {
+    using CC = CombineCfg<D>;
+    __shared__ float4 part_o[CC::kParts][CC::kRows][CC::kGroups];
+    __shared__ float part_l[CC::kParts][CC::kRows];
+
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    constexpr int kGroups = D / 8;
-    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= static_cast<long long>(rows) * kGroups)
-        return;
-    const int r = static_cast<int>(idx / kGroups);
-    const int g = static_cast<int>(idx % kGroups);
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        acc[i] = 0.f;
+
+    const int g = threadIdx.x % CC::kGroups;
+    const int part = (threadIdx.x / CC::kGroups) % CC::kParts;
+    const int rl = threadIdx.x / (CC::kGroups * CC::kParts);
+    const int r = blockIdx.x * CC::kRows + rl;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
+    if (r < rows) {
+        const float4 *src = reinterpret_cast<const float4 *>(ws_o) + static_cast<size_t>(r) * CC::kGroups + g;
+        const size_t split_stride = static_cast<size_t>(rows) * CC::kGroups;
 #pragma unroll 4
-    for (int j = 0; j < n_split; ++j) {
-        const float4 *src = reinterpret_cast<const float4 *>(ws_o + (static_cast<size_t>(j) * rows + r) * D + g * 8);
-        const float4 a = src[0];
-        const float4 c = src[1];
-        acc[0] += a.x;
-        acc[1] += a.y;
-        acc[2] += a.z;
-        acc[3] += a.w;
-        acc[4] += c.x;
-        acc[5] += c.y;
-        acc[6] += c.z;
-        acc[7] += c.w;
-        l += ws_l[static_cast<size_t>(j) * rows + r];
+        for (int j = part; j < n_split; j += CC::kParts) {
+            const float4 a = src[static_cast<size_t>(j) * split_stride];
+            acc.x += a.x;
+            acc.y += a.y;
+            acc.z += a.z;
+            acc.w += a.w;
+            if (g == 0)
+                l += ws_l[static_cast<size_t>(j) * rows + r];
+        }
     }
-    uint4 w;
-    w.x = ptx::pack_half2(__fdiv_rn(acc[0], l), __fdiv_rn(acc[1], l));
-    w.y = ptx::pack_half2(__fdiv_rn(acc[2], l), __fdiv_rn(acc[3], l));
-    w.z = ptx::pack_half2(__fdiv_rn(acc[4], l), __fdiv_rn(acc[5], l));
-    w.w = ptx::pack_half2(__fdiv_rn(acc[6], l), __fdiv_rn(acc[7], l));
-    *reinterpret_cast<uint4 *>(O + static_cast<size_t>(r) * D + g * 8) = w;
+    part_o[part][rl][g] = acc;
+    if (g == 0)
+        part_l[part][rl] = l;
+    __syncthreads();
+    if (part == 0 && r < rows) {
+        float4 s = part_o[0][rl][g];
+        float ls = part_l[0][rl];
+#pragma unroll
+        for (int q = 1; q < CC::kParts; ++q) {
+            const float4 t = part_o[q][rl][g];
+            s.x += t.x;
+            s.y += t.y;
+            s.z += t.z;
+            s.w += t.w;
+            ls += part_l[q][rl];
+        }
+        uint2 w;
+        w.x = ptx::pack_half2(__fdiv_rn(s.x, ls), __fdiv_rn(s.y, ls));
+        w.y = ptx::pack_half2(__fdiv_rn(s.z, ls), __fdiv_rn(s.w, ls));
+        *reinterpret_cast<uint2 *>(O + static_cast<size_t>(r) * D + g * 4) = w;
+    }
 }
 
 }  // namespace mg

@@ -201,6 +201,27 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// 2^x on the FMA pipe, for offloading part of the exponentials from the MUFU unit.
+// Range reduction x = r + f with r = round-to-nearest(x), taken with the 1.5 * 2^23 shifter
+// (exact for |x| < 2^22), and f in [-1/2, 1/2]; 2^f by a degree-5 polynomial whose coefficients
+// minimise the maximum relative error on [-1/2, 1/2] (csrc/exp2_poly_fit.py, Remez exchange);
+// r is added to the exponent field. Relative error <= 2.2e-7 for x >= -125; smaller inputs are
+// clamped to -125 (a result near 2^-125, negligible next to any row sum).
+__device__ __forceinline__ float exp2_fma(float x)
+{
+    x = fmaxf(x, -125.0f);
+    const float t = x + 12582912.0f;
+    const float r = t - 12582912.0f;
+    const float f = x - r;
+    float p = 0x1.5c08e6p-10f;
+    p = fmaf(p, f, 0x1.3d0c52p-7f);
+    p = fmaf(p, f, 0x1.c6b6e4p-5f);
+    p = fmaf(p, f, 0x1.ebf918p-3f);
+    p = fmaf(p, f, 0x1.62e428p-1f);
+    p = fmaf(p, f, 0x1.000002p+0f);
+    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
 // Two fp32 values to one fp16x2 word, round-to-nearest-even; `lo` lands at the lower address.
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 {

@@ -361,17 +361,22 @@ def main():
 
     ms_loop = timed(loop_steps)
 
-    # Fused kernel alone: events recorded by the library around it, one rotation of sets.
-    n_k = min(args.steps, max(n_sets, 1000))
+    # Fused kernel alone: events recorded by the library around it. Each batch of launches is
+    # queued behind a device-side sleep so the host runs ahead and the events time the GPU, not
+    # the Python launch loop.
+    batch = 100
+    n_k = max(batch, (min(args.steps, max(n_sets, 1000)) // batch) * batch)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
     for pair in evs:  # torch creates the CUDA event on its first record; the library re-records it
         for ev in pair:
             ev.record(stream)
     stream.synchronize()
     with torch.cuda.stream(stream):
-        for i in range(n_k):
-            plan.set_timing_events(*evs[i])
-            step(i)
+        for b0 in range(0, n_k, batch):
+            torch.cuda._sleep(20_000_000)  # ~10 ms of GPU time while the host queues the batch
+            for i in range(b0, b0 + batch):
+                plan.set_timing_events(*evs[i])
+                step(i)
     plan.set_timing_events(None, None)
     stream.synchronize()
     k_ms = [b.elapsed_time(e) for b, e in evs]

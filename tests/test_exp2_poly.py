@@ -1,0 +1,44 @@
+"""The FMA-pipe exponential's polynomial: the constants compiled into the kernel are the ones the
+committed fit produces, and the fp32 evaluation (range reduction, Horner with fused multiply-adds,
+exponent-field add, emulated exactly on the CPU) stays within its relative-error bound."""
+
+import os
+import re
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "attention_mugraph_gb300", "csrc")
+sys.path.insert(0, CSRC)
+import exp2_poly_fit as fit  # noqa: E402
+
+
+def kernel_coefficients():
+    text = open(os.path.join(CSRC, "ptx.cuh")).read()
+    body = text[text.index("float exp2_fma(float x)"):]
+    body = body[:body.index("}")]
+    return np.array([float.fromhex(h) for h in re.findall(r"(0x[0-9a-fA-F.]+p[-+]\d+)f", body)], dtype=np.float32)
+
+
+def test_kernel_constants_are_the_fit():
+    c = fit.fit()
+    k = kernel_coefficients()
+    assert k.size == fit.DEGREE + 1
+    # Horner order in the kernel: highest degree first.
+    assert np.array_equal(k[::-1], c)
+
+
+def test_relative_error_bound():
+    c = fit.fit()
+    assert fit.max_rel_error(c, -30.0, 12.0) < 3e-7
+    # Integers are exact up to the polynomial's value at f = 0.
+    x = np.arange(-20, 12, dtype=np.float32)
+    y = fit.exp2_emulated(x, c).astype(np.float64)
+    assert np.max(np.abs(y / np.exp2(x.astype(np.float64)) - 1)) < 2e-7
+
+
+def test_underflow_clamp_is_tiny_and_positive():
+    c = fit.fit()
+    y = fit.exp2_emulated(np.array([-125.0, -200.0, -1e30], dtype=np.float32), c)
+    assert (y > 0).all() and (y < 1e-37).all()
