@@ -30,7 +30,7 @@ MG_FLAG_INJECT_TIMEOUT = 0x2
 # Every function include/mg_attn.h declares.
 EXPORTS = ("mg_attn_plan", "mg_attn_plan_ex", "mg_attn_run", "mg_attn_run_host", "mg_attn_destroy",
            "mg_attn_get_status", "mg_attn_get_info", "mg_attn_query", "mg_attn_status_string",
-           "mg_attn_last_error", "mg_attn_version", "mg_attn_set_timing_events")
+           "mg_attn_last_error", "mg_attn_version", "mg_attn_set_timing_events", "mg_attn_run_noalloc")
 
 
 class MgAttnOptions(ctypes.Structure):
@@ -93,6 +93,8 @@ def _bind(lib):
     lib.mg_attn_last_error.restype = ctypes.c_char_p
     lib.mg_attn_set_timing_events.argtypes = [vp, vp, vp]
     lib.mg_attn_set_timing_events.restype = st
+    lib.mg_attn_run_noalloc.argtypes = [i64, i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.mg_attn_run_noalloc.restype = st
     lib.mg_attn_version.argtypes = []
     lib.mg_attn_version.restype = i32
     return lib

@@ -441,6 +441,152 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
     return MG_OK;
 }
 
+// ------------------------------------------------------------------ allocation-free entry point
+}  // extern "C"
+
+namespace {
+
+// Scratch of mg_attn_run_noalloc: 256 bytes of status words, then the fp32 split partials
+// (numerators, then row sums). A file-scope device array: no allocation call ever creates it.
+__device__ __align__(256) unsigned char g_static_scratch[MG_ATTN_STATIC_SCRATCH_BYTES];
+
+struct StaticDevice {
+    bool ready = false;
+    unsigned char *scratch = nullptr;  // device address of g_static_scratch on this device
+    int sms = 0, smem_optin = 0;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+StaticDevice g_static_dev[kMaxDevices];
+
+// One-time, per-device set-up with that device current: check the device, look up the array's
+// device address (its host-side name is only a stand-in) and clear the status words.
+mg_status static_setup(StaticDevice **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(MG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    StaticDevice &sd = g_static_dev[dev];
+    if (!sd.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sd.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sd.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+                cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3)
+            return fail(MG_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; this library is built for 10.3",
+                        dev, major, minor);
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        e = cudaMemset(ptr, 0, 256);
+        if (e == cudaSuccess)
+            e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(static scratch status)");
+        sd.scratch = static_cast<unsigned char *>(ptr);
+        sd.ready = true;
+    }
+    *out = &sd;
+    return MG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const void *Q, const void *K,
+                              const void *V, void *O, mg_stream_t stream)
+{
+    if (!Q || !K || !V || !O)
+        return fail(MG_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (misaligned(Q) || misaligned(K) || misaligned(V) || misaligned(O))
+        return fail(MG_ERR_LAYOUT, "Q, K, V and O must be 16-byte aligned");
+    StaticDevice *sd = nullptr;
+    mg_status st = static_setup(&sd);
+    if (st != MG_OK)
+        return st;
+    mg_attn_plan_info in;
+    unsigned long long timeout_ns = 0;
+    int flags = 0;
+    st = decide(B, M, N, d, nullptr, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags);
+    if (st != MG_OK)
+        return st;
+    if (in.workspace_bytes > static_cast<int64_t>(MG_ATTN_STATIC_SCRATCH_BYTES))
+        return fail(MG_ERR_INVALID_ARG,
+                    "shape needs %lld bytes of split scratch; the static scratch holds %u bytes "
+                    "(use mg_attn_plan / mg_attn_run)",
+                    (long long)in.workspace_bytes, MG_ATTN_STATIC_SCRATCH_BYTES);
+    FwdKernel fwd = fwd_kernel(d, in.stages);
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, in.smem_bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute");
+
+    CUtensorMap maps[3];
+    const void *ptrs[3] = {Q, K, V};
+    const uint64_t uB = B, uM = M, uN = N, ud = d;
+    const uint64_t dims[3][3] = {{ud, uM, uB}, {uN, ud, uB}, {ud, uN, uB}};
+    const uint32_t box1[3] = {128u, static_cast<uint32_t>(d), 128u};
+    for (int i = 0; i < 3; ++i)
+        if ((st = encode_3d(&maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i])) != MG_OK)
+            return st;
+
+    mg::FwdParams prm;
+    prm.B = static_cast<int>(B);
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.m_tiles_per_b = static_cast<int>((M + mg::kBlockM - 1) / mg::kBlockM);
+    prm.n_tiles = in.n_tiles;
+    prm.n_split = in.n_split;
+    prm.O = static_cast<__half *>(O);
+    prm.status = reinterpret_cast<int *>(sd->scratch);
+    prm.ws_o = in.n_split > 1 ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
+    prm.ws_l = in.n_split > 1 ? prm.ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
+    prm.timeout_ns = timeout_ns;
+    prm.inject_timeout = 0;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(in.grid_ctas), 1, 1);
+    cfg.blockDim = dim3(mg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(in.smem_bytes);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *fwd_args[4] = {&maps[0], &maps[1], &maps[2], &prm};
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fwd), fwd_args);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch mg_attn_fwd_partial");
+    if (in.n_split > 1) {
+        int rows = static_cast<int>(B * M);
+        int n_split = in.n_split;
+        const float *wo = prm.ws_o;
+        const float *wl = prm.ws_l;
+        __half *out = static_cast<__half *>(O);
+        const int rows_per_cta = d == 64 ? mg::CombineCfg<64>::kRows : mg::CombineCfg<128>::kRows;
+        cudaLaunchConfig_t cc = cfg;
+        cc.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), 1, 1);
+        cc.blockDim = dim3(256, 1, 1);
+        cc.dynamicSmemBytes = 0;
+        void *cargs[5] = {&wo, &wl, &out, &rows, &n_split};
+        e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(combine_kernel(d)), cargs);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "launch mg_attn_combine");
+    }
+    return MG_OK;
+}
+
 mg_status mg_attn_get_status(mg_attn_plan_t plan)
 {
     if (!plan)

@@ -133,6 +133,31 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
 mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, const void *hV,
                            void *hO, mg_stream_t stream);
 
+/*
+ * Allocation-free variant of mg_attn_run, for callers that cannot call cudaMalloc: code that has
+ * handed all device memory to another allocator (a framework's caching pool), code on a latency
+ * path where cudaMalloc's implicit device synchronisation is not acceptable, and code under rules
+ * that forbid dynamic allocation after start-up. (The pages have no counterpart: Mirage's
+ * generated entry takes a caller-allocated buffer instead.)
+ *
+ * Same operation, tensors, tiling and kernels as a default plan for (B, M, N, d) run with
+ * mg_attn_run, so the results are the same. No plan is needed and nothing is allocated: the
+ * split partials and status words live in a file-scope device array of 8 MiB
+ * (MG_ATTN_STATIC_SCRATCH_BYTES) that every GPU loading this library holds until the process
+ * exits. Shapes whose split partials need more than that (e.g. d = 128 with a long N and few
+ * row tiles) are rejected with MG_ERR_INVALID_ARG and a message from mg_attn_last_error().
+ *
+ * The first call on each device (with that device current) does a one-time set-up: it looks up
+ * the array's device address and clears its status words. Make that first call before any
+ * stream capture. Every call shares the one array and it keeps the last call's contents, so
+ * calls that overlap on the GPU (other streams, other host threads) race: serialise them.
+ * In-kernel timeouts are recorded in the array's status words and not reported.
+ * Errors: as mg_attn_run and mg_attn_plan (shape validation, device checks).
+ */
+#define MG_ATTN_STATIC_SCRATCH_BYTES (8u << 20)
+mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const void *Q, const void *K,
+                              const void *V, void *O, mg_stream_t stream);
+
 /* Synchronise the device, free the plan's workspace and the plan. NULL is MG_ERR_INVALID_ARG. */
 mg_status mg_attn_destroy(mg_attn_plan_t plan);
 

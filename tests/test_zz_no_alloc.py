@@ -1,0 +1,74 @@
+"""The allocation-free entry point, mg_attn_run_noalloc, through the C ABI.
+
+It serves callers that cannot call cudaMalloc (device memory handed to another allocator, a
+latency path that cannot take cudaMalloc's implicit synchronisation, rules against allocating
+after start-up): its split partials live in a fixed 8 MiB device array inside the library. These
+checks compare it with the planned entry point (mg_attn_run) on the same inputs, on two calls in a
+row (the array keeps the previous call's contents), and check that a shape needing more scratch
+than the array holds is refused. This file is collected last so that a failure here never hides
+the other tests; it also passes alone in a fresh process.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import attention_mugraph_gb300 as mg
+from attention_mugraph_gb300 import _lib, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 2e-3  # the parity bound the other GPU tests use: |err| <= RTOL * (1 + |ref|)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return _lib.load_library()
+
+
+def _call(lib, shape, Q, K, V, O, stream):
+    B, M, N, d = shape
+    return lib.mg_attn_run_noalloc(B, M, N, d, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                   ctypes.c_void_p(stream.cuda_stream))
+
+
+@pytest.mark.parametrize("name", ["gqa", "decode", "tiny"])
+def test_noalloc_matches_planned_entry_point_on_two_calls(lib, name):
+    q, k, v, shape = inputs.make_config(name)
+    B, M, N, d = shape
+    Q, K, V = q.cuda(), k.cuda(), v.cuda()
+    stream = torch.cuda.current_stream()
+
+    plan = mg.Plan(B, M, N, d)
+    ref = torch.empty((B, M, d), dtype=torch.float16, device="cuda")
+    plan.run(Q, K, V, ref)
+    torch.cuda.synchronize()
+    want = ref.double().cpu().numpy()
+
+    for call in range(2):
+        O = torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda")
+        st = _call(lib, shape, Q, K, V, O, stream)
+        assert st == mg.MG_OK, lib.mg_attn_last_error()
+        torch.cuda.synchronize()
+        got = O.double().cpu().numpy()
+        assert np.isfinite(got).all(), f"{name} call {call}: non-finite output"
+        err = np.abs(got - want)
+        assert (err <= RTOL * (1 + np.abs(want))).all(), f"{name} call {call}: max err {err.max():.3e}"
+    plan.destroy()
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
+    # d = 128 with 4 row tiles and a long N splits 38 ways: 38 * 512 * 129 * 4 bytes > 8 MiB.
+    B, M, N, d = 4, 128, 8192, 128
+    info = mg.mg_attn_query(B, M, N, d, num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert info["workspace_bytes"] > 8 << 20
+    buf = torch.zeros(16, dtype=torch.float16, device="cuda")
+    st = lib.mg_attn_run_noalloc(B, M, N, d, buf.data_ptr(), buf.data_ptr(), buf.data_ptr(), buf.data_ptr(),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == mg.MG_ERR_INVALID_ARG
+    assert b"static scratch" in lib.mg_attn_last_error()
