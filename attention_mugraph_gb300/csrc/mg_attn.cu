@@ -62,9 +62,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-int auto_stages(int64_t d) { return d == 64 ? 4 : 2; }
+int auto_stages(int64_t d) { return d == 64 ? 6 : 3; }
 
-using FwdKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const mg::FwdParams);
+using FwdKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                           const CUtensorMap, const mg::FwdParams);
 
 FwdKernel fwd_kernel(int64_t d, int stages)
 {
@@ -73,11 +74,18 @@ FwdKernel fwd_kernel(int64_t d, int stages)
         case 2: return mg::mg_attn_fwd_partial<64, 2>;
         case 3: return mg::mg_attn_fwd_partial<64, 3>;
         case 4: return mg::mg_attn_fwd_partial<64, 4>;
+        case 5: return mg::mg_attn_fwd_partial<64, 5>;
+        case 6: return mg::mg_attn_fwd_partial<64, 6>;
         default: return nullptr;
         }
     }
-    if (d == 128 && stages == 2)
-        return mg::mg_attn_fwd_partial<128, 2>;
+    if (d == 128) {
+        switch (stages) {
+        case 2: return mg::mg_attn_fwd_partial<128, 2>;
+        case 3: return mg::mg_attn_fwd_partial<128, 3>;
+        default: return nullptr;
+        }
+    }
     return nullptr;
 }
 
@@ -134,8 +142,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         return fail(MG_ERR_INVALID_ARG, "grid too large");
 
     int stages = o.stages == 0 ? auto_stages(d) : o.stages;
-    if (stages < 2 || stages > 4)
-        return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 4]", stages);
+    if (stages < 2 || stages > 6)
+        return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 6]", stages);
     const uint32_t smem = mg::fwd_smem_bytes(static_cast<int>(d), stages);
     if (!fwd_kernel(d, stages) || static_cast<int64_t>(smem) > max_smem)
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
@@ -170,19 +178,21 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-// 3-D fp16 tensor map over a contiguous (d2, d1, d0) array (d0 innermost) with a box of
-// box0 x box1 x 1 elements and 128-byte swizzle; out-of-range elements read as zero.
+// 3-D tensor map over a contiguous (d2, d1, d0) array (d0 innermost) of fp16 (elem = 2) or fp32
+// (elem = 4) with a box of box0 x box1 x 1 elements and 128-byte swizzle; out-of-range elements
+// read as zero and are not written.
 mg_status encode_3d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
-                    uint32_t box1)
+                    uint32_t box1, uint32_t elem = 2)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc)
         return fail(MG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint64_t strides[2] = {d0 * elem, d0 * d1 * elem};
     cuuint32_t box[3] = {box0, box1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+    const CUtensorMapDataType dt = elem == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -203,9 +213,10 @@ struct mg_attn_plan {
     float *ws_l = nullptr;
     FwdKernel fwd = nullptr;
     CombineKernel combine = nullptr;
-    // Last encoded tensor maps and the pointers they were encoded for.
-    const void *map_ptr[3] = {nullptr, nullptr, nullptr};
-    CUtensorMap maps[3];
+    // Tensor maps Q, K, V, O (re-encoded when a pointer changes) and the fp32 partial workspace
+    // (encoded once; zero when the plan has one split and no workspace).
+    const void *map_ptr[4] = {nullptr, nullptr, nullptr, nullptr};
+    CUtensorMap maps[5];
     // Device staging for mg_attn_run_host, allocated by its first call.
     void *staging = nullptr;
     // Optional events recorded around the fused kernel (mg_attn_set_timing_events).
@@ -291,9 +302,17 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     }
     uint8_t *ws = static_cast<uint8_t *>(p->workspace);
     p->status = reinterpret_cast<int *>(ws);
+    std::memset(p->maps, 0, sizeof(p->maps));
     if (info.n_split > 1) {
         p->ws_o = reinterpret_cast<float *>(ws + 256);
         p->ws_l = p->ws_o + static_cast<size_t>(info.n_split) * B * M * d;
+        // ws_o as (n_split*B, M, d) fp32, stored in {32, 128} boxes.
+        st = encode_3d(&p->maps[4], p->ws_o, d, M, static_cast<uint64_t>(info.n_split) * B, 32u, 128u, 4);
+        if (st != MG_OK) {
+            cudaFree(p->workspace);
+            delete p;
+            return st;
+        }
     }
     e = cudaMemset(p->workspace, 0, 256);
     if (e == cudaSuccess)
@@ -339,11 +358,12 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     const mg_attn_plan_info &in = plan->info;
     const uint64_t B = in.B, M = in.M, N = in.N, d = in.d;
 
-    // Q (B, M, d): box 64 x 128 rows; K (B, d, N): box 64 columns x d rows; V (B, N, d): box 64 x 128 rows.
-    const void *ptrs[3] = {Q, K, V};
-    const uint64_t dims[3][3] = {{d, M, B}, {N, d, B}, {d, N, B}};
-    const uint32_t box1[3] = {128u, static_cast<uint32_t>(d), 128u};
-    for (int i = 0; i < 3; ++i) {
+    // Q (B, M, d): box 64 x 128 rows; K (B, d, N): box 64 columns x d rows; V (B, N, d): box 64 x 128
+    // rows; O (B, M, d): box 64 x 128 rows.
+    const void *ptrs[4] = {Q, K, V, O};
+    const uint64_t dims[4][3] = {{d, M, B}, {N, d, B}, {d, N, B}, {d, M, B}};
+    const uint32_t box1[4] = {128u, static_cast<uint32_t>(d), 128u, 128u};
+    for (int i = 0; i < 4; ++i) {
         if (plan->map_ptr[i] != ptrs[i]) {
             plan->map_ptr[i] = nullptr;
             mg_status st = encode_3d(&plan->maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i]);
@@ -360,8 +380,6 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.m_tiles_per_b = static_cast<int>((M + mg::kBlockM - 1) / mg::kBlockM);
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
-    prm.O = static_cast<__half *>(O);
-    prm.ws_o = plan->ws_o;
     prm.ws_l = plan->ws_l;
     prm.status = plan->status;
     prm.timeout_ns = plan->timeout_ns;
@@ -379,7 +397,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    void *fwd_args[4] = {&plan->maps[0], &plan->maps[1], &plan->maps[2], &prm};
+    void *fwd_args[6] = {&plan->maps[0], &plan->maps[1], &plan->maps[2], &plan->maps[3], &plan->maps[4], &prm};
     cudaError_t e;
     if (plan->ev_begin && (e = cudaEventRecord(plan->ev_begin, cfg.stream)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord(begin)");
@@ -531,14 +549,19 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
 
-    CUtensorMap maps[3];
-    const void *ptrs[3] = {Q, K, V};
+    CUtensorMap maps[5];
+    std::memset(maps, 0, sizeof(maps));
+    const void *ptrs[4] = {Q, K, V, O};
     const uint64_t uB = B, uM = M, uN = N, ud = d;
-    const uint64_t dims[3][3] = {{ud, uM, uB}, {uN, ud, uB}, {ud, uN, uB}};
-    const uint32_t box1[3] = {128u, static_cast<uint32_t>(d), 128u};
-    for (int i = 0; i < 3; ++i)
+    const uint64_t dims[4][3] = {{ud, uM, uB}, {uN, ud, uB}, {ud, uN, uB}, {ud, uM, uB}};
+    const uint32_t box1[4] = {128u, static_cast<uint32_t>(d), 128u, 128u};
+    for (int i = 0; i < 4; ++i)
         if ((st = encode_3d(&maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i])) != MG_OK)
             return st;
+    float *ws_o = in.n_split > 1 ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
+    if (ws_o && (st = encode_3d(&maps[4], ws_o, ud, uM, static_cast<uint64_t>(in.n_split) * uB, 32u, 128u, 4)) !=
+                    MG_OK)
+        return st;
 
     mg::FwdParams prm;
     prm.B = static_cast<int>(B);
@@ -547,10 +570,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.m_tiles_per_b = static_cast<int>((M + mg::kBlockM - 1) / mg::kBlockM);
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
-    prm.O = static_cast<__half *>(O);
     prm.status = reinterpret_cast<int *>(sd->scratch);
-    prm.ws_o = in.n_split > 1 ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
-    prm.ws_l = in.n_split > 1 ? prm.ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
+    prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
 
@@ -564,14 +585,14 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void *fwd_args[4] = {&maps[0], &maps[1], &maps[2], &prm};
+    void *fwd_args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4], &prm};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fwd), fwd_args);
     if (e != cudaSuccess)
         return cuda_fail(e, "launch mg_attn_fwd_partial");
     if (in.n_split > 1) {
         int rows = static_cast<int>(B * M);
         int n_split = in.n_split;
-        const float *wo = prm.ws_o;
+        const float *wo = ws_o;
         const float *wl = prm.ws_l;
         __half *out = static_cast<__half *>(O);
         const int rows_per_cta = d == 64 ? mg::CombineCfg<64>::kRows : mg::CombineCfg<128>::kRows;

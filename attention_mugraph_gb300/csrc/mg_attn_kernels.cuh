@@ -7,24 +7,33 @@
 // axis). The split owns a contiguous run of 128-column tiles of K/V and loops over them,
 // as the threadblock for-loop over N with a row-sum accumulator does in Mirage's attention
 // search space (blog "Reading Mirage's muGraph search and backend generation through the
-// GQA example", section 4.2-4.3: forloop dims and the REDTOX_LD_SUM accumulator). Per tile:
+// GQA example", sections 4.2-4.3: forloop dims and the REDTOX_LD_SUM accumulator). Per tile:
 //     S  = Q . K_tile                    tcgen05 MMA, fp32 in tensor memory
-//     P  = exp(S) (0 beyond N)           fp32, one thread per row; l += rowsum(P) in fp32
-//     O += fp16(P) . V_tile              tcgen05 MMA, fp32 in tensor memory
+//     P  = exp(S) (0 beyond N)           fp32; l += rowsum(P) in fp32; fp16 P to tensor memory
+//     O += fp16(P) . V_tile              tcgen05 MMA with A read from tensor memory
 // The divide by the row sum commutes with the second product, so it is deferred.
 // With one split the CTA divides and writes fp16 O; otherwise it writes the fp32 partial
-// numerator O_j and row sum l_j to the workspace.
+// numerator O_j and row sum l_j to the workspace. Both go out through shared memory and TMA
+// bulk stores.
 //
 // Kernel 2, mg_attn_combine: O = (sum_j O_j) / (sum_j l_j) -> fp16, the second threadblock
 // graph of the "attention" search configuration (blog, section 4.3). No max-subtraction
 // means the partials combine by plain sums.
 //
-// Warp roles of kernel 1 (192 threads):
-//   warp 0      TMA producer: Q once, then K/V tiles through a STAGES-deep mbarrier ring
-//   warp 1      tensor-memory allocator and MMA issuer (one thread)
-//   warps 2..5  softmax + epilogue, thread = row (tensor-memory lane), 128 rows
+// Warp roles of kernel 1 (320 threads):
+//   warp 0       TMA producer: Q once, then K/V tiles through a STAGES-deep mbarrier ring
+//   warp 1       tensor-memory allocator and MMA issuer (one thread)
+//   warps 2..9   softmax + epilogue. Warp w reads tensor-memory lanes 32*(w%4).. (its rows)
+//                and column half h = (w-2)/4 of each 128-column S tile: 64 columns per thread.
 // Tensor memory (512 columns): S double buffer at columns [0,128) and [128,256), O at
-// [256, 256 + d).
+// [256, 256 + d), the fp16 P double buffer (64 columns each, two fp16 per column) after O.
+// Keeping P in tensor memory spares shared memory 64 KB of traffic per tile (P written by the
+// softmax warps and read back by the MMA), which otherwise bounds the tile rate.
+//
+// Exponentials: 2 of every 8 columns go through a polynomial on the FMA pipe (exp_fma), the
+// rest through the MUFU unit (ex2.approx); both are fp32 with relative error near 2e-7. The
+// split balances MUFU time against instruction issue, since MUFU alone (16 per clock per SM)
+// would bound the kernel.
 //
 // Every wait is bounded by a global-timer deadline. A wait that runs out records
 // MG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag, and every role then
@@ -40,28 +49,37 @@ namespace mg {
 
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBuffers = 2;
+constexpr int kPolyOf8 = 2;        // columns (of every 8) whose exp runs on the FMA pipe
+constexpr uint32_t kTmemO = 256;   // tensor-memory column of O; P buffers follow it
 constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
+constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warps
 
 template <int D>
 struct TileCfg {
     static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
-    static constexpr int kChunks = D / 64;                  // 128-byte column chunks of a d-wide row
+    static constexpr int kChunks = D / 64;                  // 128-byte column chunks of a d-wide fp16 row
     static constexpr uint32_t kQBytes = kBlockM * D * 2;    // Q tile, K-major
     static constexpr uint32_t kKBytes = D * kBlockN * 2;    // K tile, N contiguous
     static constexpr uint32_t kVBytes = kBlockN * D * 2;    // V tile, d contiguous
     static constexpr uint32_t kStageBytes = kKBytes + kVBytes;
-    static constexpr uint32_t kPBytes = kBlockM * kBlockN * 2;  // P tile, K-major
     static constexpr uint32_t kChunkRows128 = 128 * 128;        // one 128-row x 128-byte chunk
+    static constexpr int kHalfCols = D / 2;                     // O columns per softmax thread
+    static constexpr uint32_t kTmemP = kTmemO + D;              // P buffer b at kTmemP + 64 b
+    static_assert(kTmemP + 64 * kPBuffers <= kTmemCols, "tensor memory overflow");
 };
 
-// Shared-memory bytes of kernel 1 for a head dim and pipeline depth (+1024 for alignment).
+// Shared-memory bytes of kernel 1 for a head dim and pipeline depth: alignment slack, Q, the
+// K/V ring (its first stage is reused as the output staging area), the row-sum exchange and
+// the barriers.
 __host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages)
 {
     return 1024u + static_cast<uint32_t>(128 * d * 2) + static_cast<uint32_t>(stages) * (2u * d * 128 * 2) +
-           static_cast<uint32_t>(kPBuffers) * (128u * 128 * 2) + 256u;
+           2u * 128 * 4 + 256u;
 }
 
 struct FwdParams {
@@ -69,8 +87,6 @@ struct FwdParams {
     int m_tiles_per_b;       // ceil(M / 128)
     int n_tiles;             // ceil(N / 128)
     int n_split;
-    __half *O;               // (B, M, d); written here when n_split == 1
-    float *ws_o;             // (n_split, B, M, d) partial numerators
     float *ws_l;             // (n_split, B, M) partial row sums
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
@@ -130,21 +146,54 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsign
     }
 }
 
+// Byte offset of 16-byte unit `unit` of row `row` inside a 128-row x 128-byte chunk written in
+// the TMA/UMMA 128-byte swizzle (unit index XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128_offset(int row, uint32_t unit)
+{
+    return static_cast<uint32_t>(row) * 128u + ((unit ^ static_cast<uint32_t>(row & 7)) << 4);
+}
+
+// The exponentials of one 32-column slice of a score row, packed as fp16 pairs into w[16]:
+// exp(s[i]) for columns below n_valid, 0 past N (MASK: only the last tile needs the test); the
+// fp32 values add into four partial row sums (fixed order).
+template <bool MASK>
+__device__ __forceinline__ void exp_slice(const uint32_t (&r)[32], int col0, int n_valid, uint32_t *w,
+                                          float (&acc)[4])
+{
+    constexpr float kLog2e = 1.4426950408889634f;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        float v[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float s = __uint_as_float(r[i + k]);
+            float x = ((i + k) & 7) < kPolyOf8 ? ptx::exp_fma(s) : ptx::ex2_approx(s * kLog2e);
+            if (MASK)
+                x = (col0 + i + k < n_valid) ? x : 0.f;
+            v[k] = x;
+            acc[(i + k) & 3] += x;
+        }
+        w[i / 2] = ptx::pack_half2(v[0], v[1]);
+    }
+}
+
 template <int D, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     mg_attn_fwd_partial(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const FwdParams p)
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                        const __grid_constant__ CUtensorMap tmW, const FwdParams p)
 {
     using C = TileCfg<D>;
     using BI = Bars<STAGES>;
     static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
+    static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = ptx::smem_u32(smem);
     const uint32_t sStage0 = sQ + C::kQBytes;
-    const uint32_t sP0 = sStage0 + STAGES * C::kStageBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kQBytes + STAGES * C::kStageBytes + kPBuffers * C::kPBytes);
+    float *l_xchg = reinterpret_cast<float *>(smem + C::kQBytes + STAGES * C::kStageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(l_xchg + 2 * kBlockM);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
@@ -171,10 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(bar(BI::kSFull + s), 1);
-            ptx::mbar_init(bar(BI::kSEmpty + s), 128);
+            ptx::mbar_init(bar(BI::kSEmpty + s), kSoftmaxThreads);
         }
         for (int s = 0; s < kPBuffers; ++s) {
-            ptx::mbar_init(bar(BI::kPFull + s), 128);
+            ptx::mbar_init(bar(BI::kPFull + s), kSoftmaxThreads);
             ptx::mbar_init(bar(BI::kPEmpty + s), 1);
         }
         ptx::mbar_init(bar(BI::kOFull), 1);
@@ -187,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmQ);
         ptx::prefetch_tensormap(&tmK);
         ptx::prefetch_tensormap(&tmV);
+        ptx::prefetch_tensormap(p.n_split == 1 ? &tmO : &tmW);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
@@ -262,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockM, kBlockN, false, true);
             constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
-            const uint32_t tmem_o = tmem + 256;
+            const uint32_t tmem_o = tmem + kTmemO;
             bool ok = wait_bounded(wc, bar(BI::kQFull), 0, BI::kQFull);
             if (ok)
                 ptx::tc_fence_after();
@@ -275,14 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 const int s = u % STAGES;
                 const uint32_t sV = sStage0 + s * C::kStageBytes + C::kKBytes;
-                const uint32_t sP = sP0 + pb * C::kPBytes;
+                const uint32_t tP = tmem + C::kTmemP + pb * 64;
 #pragma unroll
                 for (int k = 0; k < kBlockN / 16; ++k) {
-                    // A = P: K-major, 128 rows x 128 bytes per 64-column chunk, 8-row groups 1024 B apart.
-                    const uint64_t a = ptx::sdesc_sw128(sP + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
+                    // A = P in tensor memory: 16 K-columns per step are 8 tensor-memory columns.
                     // B = V: N(=d)-major, 16 rows of 128 B per step; d-chunks 128 rows x 128 B apart.
                     const uint64_t bd = ptx::sdesc_sw128(sV + k * 2048, C::kChunkRows128, 1024);
-                    ptx::mma_f16_ss(tmem_o, a, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
+                    ptx::mma_f16_ts(tmem_o, tP + k * 8, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
@@ -334,18 +383,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
+        const int sw = warp - 2;                 // 0..7
         const int q4 = warp & 3;                 // tensor-memory lane quarter this warp may access
+        const int h = sw >> 2;                   // column half of every S tile (and of O)
         const int row = q4 * 32 + lane;          // row inside the 128-row tile
         const bool warp_rows = (m0 + q4 * 32) < p.M;  // warp-uniform: any valid row in this warp
         const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
-        constexpr float kLog2e = 1.4426950408889634f;
         // The decision to go on is taken by the whole warp, so that no lane reaches a
         // warp-collective tcgen05.ld without the others.
         auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
             const bool r = wait_bounded(wc, b_, parity, where);
             return __all_sync(0xffffffffu, r);
         };
-        float l = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
         bool ok = true;
         for (int t = 0; t < T; ++t) {
             const int sb = t & 1;
@@ -355,85 +405,105 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
+            // Columns of this tile inside N, relative to this thread's half.
+            const int n_valid = p.N - (t_begin + t) * kBlockN - h * 64;
+            uint32_t r0[32], r1[32];
+            if (warp_rows) {
+                const uint32_t s_addr = tmem + lane_addr + sb * kBlockN + h * 64;
+                ptx::tmem_ld_32x32b_x32(s_addr, r0);
+                ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
+                ptx::tmem_ld_wait(r0);
+                ptx::tmem_ld_wait(r1);
+            }
+            // S is in registers: its tensor-memory buffer can take the next-but-one tile.
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(BI::kSEmpty + sb));
             if (t >= kPBuffers &&
                 !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
                            BI::kPEmpty + pb)) {
                 ok = false;
                 break;
             }
-            const int n_valid = p.N - (t_begin + t) * kBlockN;  // columns of this tile inside N
             if (warp_rows) {
-                const uint32_t p_row = sP0 + pb * C::kPBytes + row * 128;
-#pragma unroll 1
-                for (int c = 0; c < kBlockN / 32; ++c) {
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(tmem + lane_addr + sb * kBlockN + c * 32, r);
-                    ptx::tmem_ld_wait(r);
-                    float e[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float x = __uint_as_float(r[i]);
-                        const float v = ptx::ex2_approx(x * kLog2e);
-                        e[i] = (c * 32 + i < n_valid) ? v : 0.f;
-                        l += e[i];
-                    }
-                    // 32 columns = four 16-byte units of the 128-byte swizzled row of chunk c/2.
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t unit = static_cast<uint32_t>((c & 1) * 4 + q);
-                        const uint32_t addr =
-                            p_row + (c >> 1) * C::kChunkRows128 + ((unit ^ static_cast<uint32_t>(row & 7)) << 4);
-                        ptx::st_shared_v4(addr, ptx::pack_half2(e[8 * q + 0], e[8 * q + 1]),
-                                          ptx::pack_half2(e[8 * q + 2], e[8 * q + 3]),
-                                          ptx::pack_half2(e[8 * q + 4], e[8 * q + 5]),
-                                          ptx::pack_half2(e[8 * q + 6], e[8 * q + 7]));
-                    }
+                // This half's 64 columns of P are tensor-memory columns [32h, 32h + 32) of buffer pb.
+                uint32_t w[32];
+                if (n_valid >= 64) {
+                    exp_slice<false>(r0, 0, n_valid, w, acc);
+                    exp_slice<false>(r1, 32, n_valid, w + 16, acc);
+                } else {
+                    exp_slice<true>(r0, 0, n_valid, w, acc);
+                    exp_slice<true>(r1, 32, n_valid, w + 16, acc);
                 }
+                ptx::tmem_st_32x32b_x32(tmem + lane_addr + C::kTmemP + pb * 64 + h * 32, w);
+                ptx::tmem_st_wait();
             }
-            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(BI::kSEmpty + sb));
             ptx::mbar_arrive(bar(BI::kPFull + pb));
         }
 
-        if (ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull)) {
+        // ------------------------------------------------------------ epilogue
+        // Row sum: this thread's half, then the two halves added in a fixed order.
+        const float l_half = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        l_xchg[h * kBlockM + row] = l_half;
+        // One barrier publishes the half sums and makes "O is ready" a decision all eight softmax
+        // warps share (a warp that unwound from an abort votes no), so the barrier inside the
+        // branch below is reached by all of them or by none.
+        const bool o_ready = ptx::named_barrier_and(kSoftmaxBarrier, kSoftmaxThreads,
+                                                    ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull));
+        const float l = l_xchg[row] + l_xchg[kBlockM + row];
+        if (o_ready) {
             ptx::tc_fence_after();
-            const int grow = m0 + row;
+            // The K/V ring is idle (every PV has completed): stage this CTA's output in its first
+            // stage, in the 128-byte-swizzled layout the output tensor maps expect, then TMA-store it.
+            const uint32_t stage = sStage0;
             if (warp_rows) {
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                for (int c = 0; c < C::kHalfCols / 32; ++c) {
                     uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(tmem + lane_addr + 256 + c * 32, r);
+                    const int col = h * C::kHalfCols + c * 32;  // first O column of this slice
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, r);
                     ptx::tmem_ld_wait(r);
-                    if (grow < p.M) {
-                        if (p.n_split == 1) {
-                            __half *dst = p.O + (static_cast<size_t>(b) * p.M + grow) * D + c * 32;
+                    if (p.n_split == 1) {
+                        // fp16 O/l: chunk col/64 of a {64, 128} fp16 box; this slice is units (col%64)/8 .. +3.
+                        const uint32_t chunk = stage + (col / 64) * C::kChunkRows128;
+                        const uint32_t u0 = static_cast<uint32_t>((col % 64) / 8);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                uint4 w;
-                                w.x = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 0]), l),
-                                                      __fdiv_rn(__uint_as_float(r[8 * q + 1]), l));
-                                w.y = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 2]), l),
-                                                      __fdiv_rn(__uint_as_float(r[8 * q + 3]), l));
-                                w.z = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 4]), l),
-                                                      __fdiv_rn(__uint_as_float(r[8 * q + 5]), l));
-                                w.w = ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 6]), l),
-                                                      __fdiv_rn(__uint_as_float(r[8 * q + 7]), l));
-                                reinterpret_cast<uint4 *>(dst)[q] = w;
-                            }
-                        } else {
-                            float *dst =
-                                p.ws_o + ((static_cast<size_t>(j) * p.B + b) * p.M + grow) * D + c * 32;
+                        for (int q = 0; q < 4; ++q)
+                            ptx::st_shared_v4(chunk + sw128_offset(row, u0 + q),
+                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 0]), l),
+                                                              __fdiv_rn(__uint_as_float(r[8 * q + 1]), l)),
+                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 2]), l),
+                                                              __fdiv_rn(__uint_as_float(r[8 * q + 3]), l)),
+                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 4]), l),
+                                                              __fdiv_rn(__uint_as_float(r[8 * q + 5]), l)),
+                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 6]), l),
+                                                              __fdiv_rn(__uint_as_float(r[8 * q + 7]), l)));
+                    } else {
+                        // fp32 partial: chunk col/32 of {32, 128} fp32 boxes; this slice fills units 0..7.
+                        const uint32_t chunk = stage + (col / 32) * C::kChunkRows128;
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                reinterpret_cast<float4 *>(dst)[q] =
-                                    make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-                        }
+                        for (int q = 0; q < 8; ++q)
+                            ptx::st_shared_v4(chunk + sw128_offset(row, q), r[4 * q + 0], r[4 * q + 1], r[4 * q + 2],
+                                              r[4 * q + 3]);
                     }
                 }
-                if (grow < p.M && p.n_split > 1)
-                    p.ws_l[(static_cast<size_t>(j) * p.B + b) * p.M + grow] = l;
+            }
+            if (p.n_split > 1 && h == 0 && m0 + row < p.M)
+                p.ws_l[(static_cast<size_t>(j) * p.B + b) * p.M + m0 + row] = l;
+            ptx::fence_proxy_async_smem();
+            ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
+            if (sw == 0 && lane == 0) {
+                if (p.n_split == 1) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)  // O[b, m0:m0+128, 64c:64c+64]
+                        ptx::tma_store_3d(&tmO, stage + c * C::kChunkRows128, c * 64, m0, b);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)  // ws_o[j, b, m0:m0+128, 32c:32c+32]
+                        ptx::tma_store_3d(&tmW, stage + c * C::kChunkRows128, c * 32, m0, j * p.B + b);
+                }
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read0();
             }
         }
     }

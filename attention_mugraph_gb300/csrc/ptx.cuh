@@ -77,6 +77,49 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 3-D tiled copy shared -> global (rows past the tensor's extent are not written), tracked by
+// the issuing thread's bulk-async group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32), id 1..15 (0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also ANDs a predicate over its participants: every thread gets the same
+// answer, so a decision taken after it is uniform across them.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
 // (the tensor core reading an operand that threads wrote with st.shared).
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -132,6 +175,19 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], fp16 inputs, fp32 accumulate (kind::f16). A is M x K with
+// row i in tensor-memory lane i and two consecutive K elements per 32-bit column.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
@@ -164,6 +220,26 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 #pragma unroll
     for (int i = 0; i < 32; ++i)
         asm volatile("" : "+r"(r[i]));
+}
+
+// Warp-collective: lane i writes tensor-memory lane (taddr.lane + i), 32 consecutive 32-bit
+// columns starting at taddr.col. Complete (and the registers reusable) after tmem_st_wait().
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ descriptors
@@ -213,6 +289,24 @@ __device__ __forceinline__ float exp2_fma(float x)
     const float t = x + 12582912.0f;
     const float r = t - 12582912.0f;
     const float f = x - r;
+    float p = 0x1.5c08e6p-10f;
+    p = fmaf(p, f, 0x1.3d0c52p-7f);
+    p = fmaf(p, f, 0x1.c6b6e4p-5f);
+    p = fmaf(p, f, 0x1.ebf918p-3f);
+    p = fmaf(p, f, 0x1.62e428p-1f);
+    p = fmaf(p, f, 0x1.000002p+0f);
+    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// exp(s) on the FMA pipe: exp2_fma with the log2(e) scale folded into the range reduction
+// (t = s*log2e + shifter and f = s*log2e - r each take one fused multiply-add).
+__device__ __forceinline__ float exp_fma(float s)
+{
+    constexpr float kLog2e = 1.4426950408889634f;
+    s = fmaxf(s, -86.0f);  // s*log2e >= -124.07: the result stays a normal float
+    const float t = fmaf(s, kLog2e, 12582912.0f);
+    const float r = t - 12582912.0f;
+    const float f = fmaf(s, kLog2e, -r);
     float p = 0x1.5c08e6p-10f;
     p = fmaf(p, f, 0x1.3d0c52p-7f);
     p = fmaf(p, f, 0x1.c6b6e4p-5f);

@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
+    ap.add_argument("--per-config-steps", type=int, default=2000, help="graph-replayed calls per workload")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload table")
     return ap.parse_args()
 
 
@@ -107,6 +109,23 @@ def recorded_traffic():
         return float(fields["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's elapsed time (all_reduce MAX); the identity on one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps (weak scaling), timed by the slowest."""
+    return flops_per_step * world * steps / (max_ms * 1e-3) / 1e12
 
 
 class ClockSampler:
@@ -249,6 +268,76 @@ def workload_config(B, M, N, d, a, extra=None):
 
 # ------------------------------------------------------------------ GPU arm
 
+def measure_workload(name, steps, peaks, stream):
+    """Graph-replayed µs/call over rotating buffer sets (> 2x L2) and the fused kernel's own time for
+    one named workload; returns a dict for the JSON line's per_config field."""
+    import torch
+
+    import attention_mugraph_gb300 as mg
+    from attention_mugraph_gb300 import inputs
+
+    B, M, N, d, a = inputs.CONFIGS[name]
+    fl = flops_per_step(B, M, N, d)
+    by = bytes_per_step(B, M, N, d)
+    q, k, v = inputs.make_inputs(B, M, N, d, a, seed=0)
+    l2 = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0)
+             or 132 * 1024 * 1024)
+    n_sets = max(2, math.ceil(2 * l2 / by))
+    dev = [(q.cuda(), k.cuda(), v.cuda(), torch.empty((B, M, d), dtype=torch.float16, device="cuda"))
+           for _ in range(n_sets)]
+    plan = mg.Plan(B, M, N, d)
+    ptrs = [tuple(t.data_ptr() for t in s) for s in dev]
+    sh = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for i in range(max(3, n_sets)):
+            plan.run_ptr(*ptrs[i % n_sets], stream=sh)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        g.capture_begin()
+        for i in range(n_sets):
+            plan.run_ptr(*ptrs[i], stream=sh)
+        g.capture_end()
+    reps = max(1, steps // n_sets)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n_sets)
+    # Fused kernel alone (library-recorded events, host queue fed ahead of the GPU).
+    nk = min(200, max(n_sets, 20))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
+    for pair in evs:
+        for ev in pair:
+            ev.record(stream)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(20_000_000)
+        for i in range(nk):
+            plan.set_timing_events(*evs[i])
+            plan.run_ptr(*ptrs[i % n_sets], stream=sh)
+    plan.set_timing_events(None, None)
+    stream.synchronize()
+    k_us = statistics.median([b.elapsed_time(e) for b, e in evs]) * 1e3
+    t_tensor = fl / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    roof = max(t_tensor, t_hbm) * 1e6
+    st = plan.status()
+    info = plan.info
+    plan.destroy()
+    if st != mg.MG_OK:
+        raise SystemExit(f"{name}: device status {st}")
+    return {"B": B, "M": M, "N": N, "d": d, "us_per_call": us, "tflops": fl / (us * 1e-6) / 1e12,
+            "hbm_gbs": by / (us * 1e-6) / 1e9, "roofline_us": roof, "roofline_frac": roof / us,
+            "bound": "hbm" if t_hbm >= t_tensor else "tensor", "fused_kernel_us_median": k_us,
+            "n_split": info["n_split"], "buffer_sets": n_sets}
+
+
 def main():
     args = parse_args()
     if args.warmup < 3:
@@ -334,12 +423,7 @@ def main():
         ev1.synchronize()
         torch.cuda.synchronize()
         barrier()
-        ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(ev0.elapsed_time(ev1), world, device="cuda")
 
     def graph_steps():
         with torch.cuda.stream(stream):
@@ -423,7 +507,7 @@ def main():
         return
     us_graph = ms_graph * 1e3 / args.steps
     us_loop = ms_loop * 1e3 / args.steps
-    value = fl * world * args.steps / (ms_graph * 1e-3) / 1e12
+    value = job_tflops(fl, args.steps, world, ms_graph)
     roof_t = max(t_tensor, t_hbm)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -455,6 +539,11 @@ def main():
         "clocks": clk,
     }
     if world == 1:
+        if not args.no_per_config:
+            from attention_mugraph_gb300 import inputs as _inputs
+
+            line["per_config"] = {name: measure_workload(name, args.per_config_steps, peaks, stream)
+                                  for name in _inputs.CONFIG_ORDER}
         line["cpu_baseline"] = cpu_baseline(q, k, v, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     plan.destroy()

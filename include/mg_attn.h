@@ -71,7 +71,7 @@ typedef enum {
 
 typedef struct {
     int32_t n_split;    /* CTAs sharing one 128-row tile along N; 0 = automatic. 1 <= n_split <= ceil(N/128) */
-    int32_t stages;     /* K/V shared-memory pipeline depth; 0 = automatic; 2..4 (d = 128: 2 only) */
+    int32_t stages;     /* K/V shared-memory pipeline depth; 0 = automatic (the deepest); 2..6 (d = 128: 2..3) */
     int32_t flags;      /* MG_FLAG_* bits */
     int32_t reserved;   /* must be 0 */
     int64_t timeout_ns; /* bound on every in-kernel wait; 0 = 1 second; otherwise 1e3 .. 6e10 */

@@ -98,7 +98,8 @@ def test_query_decisions(B, M, N, d):
 def test_query_options():
     info = mg.mg_attn_query(2, 256, 4096, 64, 152, n_split=5, stages=2)
     assert info["n_split"] == 5 and info["stages"] == 2
-    assert mg.mg_attn_query(2, 256, 4096, 128, 152)["stages"] == 2
+    assert mg.mg_attn_query(2, 256, 4096, 128, 152)["stages"] == 3
+    assert mg.mg_attn_query(2, 256, 4096, 64, 152)["stages"] == 6
 
 
 @pytest.mark.parametrize("args,kw,code", [
@@ -107,10 +108,10 @@ def test_query_options():
     ((2, 256, 4096, 32), {}, mg.MG_ERR_UNSUPPORTED),
     ((2, 256, 4100, 64), {}, mg.MG_ERR_LAYOUT),
     ((2, 256, 4096, 64), {"n_split": 33}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 64), {"stages": 5}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x80}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 128), {"stages": 3}, mg.MG_ERR_INSUFFICIENT_SMEM),
+    ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 1 << 31, 4096, 64), {}, mg.MG_ERR_INVALID_ARG),
 ])

@@ -14,19 +14,42 @@ sys.path.insert(0, CSRC)
 import exp2_poly_fit as fit  # noqa: E402
 
 
-def kernel_coefficients():
+def kernel_coefficients(fn="float exp2_fma(float x)"):
     text = open(os.path.join(CSRC, "ptx.cuh")).read()
-    body = text[text.index("float exp2_fma(float x)"):]
+    body = text[text.index(fn):]
     body = body[:body.index("}")]
     return np.array([float.fromhex(h) for h in re.findall(r"(0x[0-9a-fA-F.]+p[-+]\d+)f", body)], dtype=np.float32)
 
 
 def test_kernel_constants_are_the_fit():
     c = fit.fit()
-    k = kernel_coefficients()
-    assert k.size == fit.DEGREE + 1
-    # Horner order in the kernel: highest degree first.
-    assert np.array_equal(k[::-1], c)
+    for fn in ("float exp2_fma(float x)", "float exp_fma(float s)"):
+        k = kernel_coefficients(fn)
+        assert k.size == fit.DEGREE + 1, fn
+        # Horner order in the kernel: highest degree first.
+        assert np.array_equal(k[::-1], c), fn
+
+
+def exp_emulated(s32, coef32):
+    """exp_fma's steps in fp32: t = fma(s, log2e, shifter), r = t - shifter, f = fma(s, log2e, -r)
+    (each fused multiply-add exact in double, rounded once), polynomial, exponent add."""
+    L = np.float64(np.float32(1.4426950408889634))
+    s32 = np.maximum(s32, np.float32(-86.0))
+    shifter = np.float64(12582912.0)
+    t = (s32.astype(np.float64) * L + shifter).astype(np.float32)
+    r = (t.astype(np.float64) - shifter).astype(np.float32)
+    f = (s32.astype(np.float64) * L - r.astype(np.float64)).astype(np.float32)
+    p = fit.horner_fp32(coef32, f)
+    return (p.view(np.int32) + (t.view(np.int32) << 23)).astype(np.int32).view(np.float32)
+
+
+def test_exp_with_folded_scale_error_bound():
+    c = fit.fit()
+    s = np.linspace(-20.0, 11.1, 2_000_001).astype(np.float32)
+    y = exp_emulated(s, c).astype(np.float64)
+    ref = np.exp(s.astype(np.float64))
+    # The fp32 rounding of log2(e) adds |s| * 2^-25 relative error to the argument.
+    assert np.max(np.abs(y / ref - 1.0)) < 6e-7
 
 
 def test_relative_error_bound():

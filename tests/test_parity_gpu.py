@@ -79,12 +79,20 @@ def test_shape_sweep(B, M, N, d, n_split):
     assert_parity(O, ref, f"{B, M, N, d, n_split}")
 
 
-@pytest.mark.parametrize("n_split,stages", [(1, 4), (2, 2), (3, 3), (5, 4), (32, 2), (31, 3)])
+@pytest.mark.parametrize("n_split,stages", [(1, 4), (2, 2), (3, 3), (5, 4), (32, 2), (31, 3), (7, 5), (4, 6)])
 def test_split_and_pipeline_depth(n_split, stages):
     q, k, v, _ = inputs.make_config("gqa")
     ref = oracle.attention(q, k, v)
     O, _ = run_gpu(q, k, v, n_split=n_split, stages=stages)
     assert_parity(O, ref, f"n_split={n_split} stages={stages}")
+
+
+@pytest.mark.parametrize("n_split,stages", [(1, 2), (3, 3), (9, 2)])
+def test_split_and_pipeline_depth_d128(n_split, stages):
+    q, k, v = inputs.make_inputs(4, 100, 4104, 128, 0.25, seed=12)
+    ref = oracle.attention(q, k, v)
+    O, _ = run_gpu(q, k, v, n_split=n_split, stages=stages)
+    assert_parity(O, ref, f"d=128 n_split={n_split} stages={stages}")
 
 
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
