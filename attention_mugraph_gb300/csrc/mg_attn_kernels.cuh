@@ -30,10 +30,10 @@
 // Keeping P in tensor memory spares shared memory 64 KB of traffic per tile (P written by the
 // softmax warps and read back by the MMA), which otherwise bounds the tile rate.
 //
-// Exponentials: 2 of every 8 columns go through a polynomial on the FMA pipe (exp_fma), the
-// rest through the MUFU unit (ex2.approx); both are fp32 with relative error near 2e-7. The
-// split balances MUFU time against instruction issue, since MUFU alone (16 per clock per SM)
-// would bound the kernel.
+// Exponentials: 4 of every 8 columns go through a polynomial on the FMA pipe (exp_pair_fma), the
+// rest through the MUFU unit (ex2.approx); both are fp32 with relative error near 2e-7, and both
+// use Blackwell's two-wide fp32 instructions. The split balances MUFU time against instruction
+// issue, since MUFU alone (16 per clock per SM) would bound the kernel.
 //
 // Every wait is bounded by a global-timer deadline. A wait that runs out records
 // MG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag, and every role then
@@ -54,7 +54,7 @@ constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBuffers = 2;
-constexpr int kPolyOf8 = 2;        // columns (of every 8) whose exp runs on the FMA pipe
+constexpr int kPolyOf8 = 4;        // columns (of every 8) whose exp runs on the FMA pipe (even)
 constexpr uint32_t kTmemO = 256;   // tensor-memory column of O; P buffers follow it
 constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
 constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warps
@@ -123,7 +123,8 @@ __device__ __forceinline__ bool wait_bounded(const WaitCtx &w, uint32_t bar, uin
         return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
-        if (ptx::mbar_try_wait(bar, parity))
+        // Suspended rather than spinning: waiting warps leave the issue slots to working ones.
+        if (ptx::mbar_try_wait_sleep(bar, parity, 100000u))
             return true;
         if (*w.abort_flag)
             return false;
@@ -154,26 +155,26 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, uint32_t unit)
 }
 
 // The exponentials of one 32-column slice of a score row, packed as fp16 pairs into w[16]:
-// exp(s[i]) for columns below n_valid, 0 past N (MASK: only the last tile needs the test); the
-// fp32 values add into four partial row sums (fixed order).
+// exp(s[i]) for columns below n_valid, 0 past N (MASK: only the last tile needs the test). Pairs
+// of columns go through the f32x2 pipe: columns 0-3 of every 8 by the polynomial, 4-7 by MUFU.
+// The fp32 values add into two packed partial row sums (fixed order).
 template <bool MASK>
 __device__ __forceinline__ void exp_slice(const uint32_t (&r)[32], int col0, int n_valid, uint32_t *w,
-                                          float (&acc)[4])
+                                          uint64_t (&acc)[2], const ptx::ExpPairConsts &k)
 {
-    constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-        float v[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const float s = __uint_as_float(r[i + k]);
-            float x = ((i + k) & 7) < kPolyOf8 ? ptx::exp_fma(s) : ptx::ex2_approx(s * kLog2e);
-            if (MASK)
-                x = (col0 + i + k < n_valid) ? x : 0.f;
-            v[k] = x;
-            acc[(i + k) & 3] += x;
+        uint32_t e0, e1;
+        if ((i & 7) < kPolyOf8)
+            ptx::exp_pair_fma(r[i], r[i + 1], k, e0, e1);
+        else
+            ptx::exp_pair_mufu(r[i], r[i + 1], k, e0, e1);
+        if (MASK) {
+            e0 = (col0 + i < n_valid) ? e0 : 0u;
+            e1 = (col0 + i + 1 < n_valid) ? e1 : 0u;
         }
-        w[i / 2] = ptx::pack_half2(v[0], v[1]);
+        acc[(i >> 1) & 1] = ptx::add_pair(acc[(i >> 1) & 1], e0, e1);
+        w[i / 2] = ptx::pack_half2(__uint_as_float(e0), __uint_as_float(e1));
     }
 }
 
@@ -313,6 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockM, kBlockN, false, true);
             constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
             const uint32_t tmem_o = tmem + kTmemO;
+            // Descriptors are computed once (Q) or once per tile (K, V); each k-step adds a
+            // constant to the start-address field, so the issuing thread spends almost no
+            // instructions between MMAs (it shares its scheduler with two softmax warps).
+            uint64_t a_q[D / 16];
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)  // A = Q: K-major; 16-column steps advance 32 B in a swizzle row
+                a_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
             bool ok = wait_bounded(wc, bar(BI::kQFull), 0, BI::kQFull);
             if (ok)
                 ptx::tc_fence_after();
@@ -324,15 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 ptx::tc_fence_after();
                 const int s = u % STAGES;
-                const uint32_t sV = sStage0 + s * C::kStageBytes + C::kKBytes;
                 const uint32_t tP = tmem + C::kTmemP + pb * 64;
+                // B = V: N(=d)-major, 16 rows (2048 B) per k-step; d-chunks 128 rows x 128 B apart.
+                const uint64_t v_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes + C::kKBytes, C::kChunkRows128, 1024);
+                // A = P in tensor memory: 16 K-columns per step are 8 tensor-memory columns.
+                ptx::mma_f16_ts(tmem_o, tP, v_desc, idesc_o, u > 0 ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < kBlockN / 16; ++k) {
-                    // A = P in tensor memory: 16 K-columns per step are 8 tensor-memory columns.
-                    // B = V: N(=d)-major, 16 rows of 128 B per step; d-chunks 128 rows x 128 B apart.
-                    const uint64_t bd = ptx::sdesc_sw128(sV + k * 2048, C::kChunkRows128, 1024);
-                    ptx::mma_f16_ts(tmem_o, tP + k * 8, bd, idesc_o, (u > 0 || k > 0) ? 1u : 0u);
-                }
+                for (int k = 1; k < kBlockN / 16; ++k)
+                    ptx::mma_f16_ts(tmem_o, tP + k * 8, v_desc + static_cast<uint64_t>(k * (2048 >> 4)), idesc_o, 1u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
                 return true;
@@ -352,15 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t sK = sStage0 + s * C::kStageBytes;
+                // B = K: N-major; 16 d-rows (2048 B) per k-step; the two 64-column halves D*128 B apart.
+                const uint64_t k_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes, D * 128, 1024);
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    // A = Q: K-major; 16-column steps advance 32 B inside a 128-byte swizzle row.
-                    const uint64_t a = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
-                    // B = K: N-major; 16 d-rows per step (2048 B); the two 64-column halves D*128 B apart.
-                    const uint64_t bd = ptx::sdesc_sw128(sK + k * 2048, D * 128, 1024);
-                    ptx::mma_f16_ss(tmem + sb * kBlockN, a, bd, idesc_s, k > 0 ? 1u : 0u);
-                }
+                for (int k = 0; k < D / 16; ++k)
+                    ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
+                                    idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
                 if (t >= 1 && !issue_pv(t - 1)) {
                     ok = false;
@@ -395,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool r = wait_bounded(wc, b_, parity, where);
             return __all_sync(0xffffffffu, r);
         };
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t acc[2] = {0, 0};  // packed fp32 partial row sums (+0.0 bit patterns)
+        const ptx::ExpPairConsts ek = ptx::exp_pair_consts();
         bool ok = true;
         for (int t = 0; t < T; ++t) {
             const int sb = t & 1;
@@ -428,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // This half's 64 columns of P are tensor-memory columns [32h, 32h + 32) of buffer pb.
                 uint32_t w[32];
                 if (n_valid >= 64) {
-                    exp_slice<false>(r0, 0, n_valid, w, acc);
-                    exp_slice<false>(r1, 32, n_valid, w + 16, acc);
+                    exp_slice<false>(r0, 0, n_valid, w, acc, ek);
+                    exp_slice<false>(r1, 32, n_valid, w + 16, acc, ek);
                 } else {
-                    exp_slice<true>(r0, 0, n_valid, w, acc);
-                    exp_slice<true>(r1, 32, n_valid, w + 16, acc);
+                    exp_slice<true>(r0, 0, n_valid, w, acc, ek);
+                    exp_slice<true>(r1, 32, n_valid, w + 16, acc, ek);
                 }
                 ptx::tmem_st_32x32b_x32(tmem + lane_addr + C::kTmemP + pb * 64 + h * 32, w);
                 ptx::tmem_st_wait();
@@ -443,7 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ------------------------------------------------------------ epilogue
         // Row sum: this thread's half, then the two halves added in a fixed order.
-        const float l_half = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        const float l_half = (__uint_as_float(static_cast<uint32_t>(acc[0])) +
+                              __uint_as_float(static_cast<uint32_t>(acc[0] >> 32))) +
+                             (__uint_as_float(static_cast<uint32_t>(acc[1])) +
+                              __uint_as_float(static_cast<uint32_t>(acc[1] >> 32)));
         l_xchg[h * kBlockM + row] = l_half;
         // One barrier publishes the half sums and makes "O is ready" a decision all eight softmax
         // warps share (a warp that unwound from an abort votes no), so the barrier inside the

@@ -59,6 +59,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended (off the scheduler) for up to `hint_ns`
+// while the phase is incomplete, so waiting threads do not take issue slots from working warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// One lane of a converged warp returns true (elect.sync over the full mask).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
@@ -277,24 +304,34 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// Degree-5 polynomial for 2^f on f in [-1/2, 1/2], coefficients chosen to minimise the maximum
+// relative error (Remez exchange, csrc/exp2_poly_fit.py), highest degree first. Evaluated in
+// fp32 with fused multiply-adds after the range reduction below, its relative error is <= 2.2e-7.
+constexpr float kExp2C5 = 0x1.5c08e6p-10f;
+constexpr float kExp2C4 = 0x1.3d0c52p-7f;
+constexpr float kExp2C3 = 0x1.c6b6e4p-5f;
+constexpr float kExp2C2 = 0x1.ebf918p-3f;
+constexpr float kExp2C1 = 0x1.62e428p-1f;
+constexpr float kExp2C0 = 0x1.000002p+0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kShifter = 12582912.0f;  // 1.5 * 2^23: x + shifter rounds x to an integer in the low bits
+
 // 2^x on the FMA pipe, for offloading part of the exponentials from the MUFU unit.
-// Range reduction x = r + f with r = round-to-nearest(x), taken with the 1.5 * 2^23 shifter
-// (exact for |x| < 2^22), and f in [-1/2, 1/2]; 2^f by a degree-5 polynomial whose coefficients
-// minimise the maximum relative error on [-1/2, 1/2] (csrc/exp2_poly_fit.py, Remez exchange);
-// r is added to the exponent field. Relative error <= 2.2e-7 for x >= -125; smaller inputs are
-// clamped to -125 (a result near 2^-125, negligible next to any row sum).
+// Range reduction x = r + f with r = round-to-nearest(x), taken with the shifter (exact for
+// |x| < 2^22), and f in [-1/2, 1/2]; 2^f by the polynomial above; r is added to the exponent
+// field. Inputs below -125 are clamped (a result near 2^-125, negligible next to any row sum).
 __device__ __forceinline__ float exp2_fma(float x)
 {
     x = fmaxf(x, -125.0f);
-    const float t = x + 12582912.0f;
-    const float r = t - 12582912.0f;
+    const float t = x + kShifter;
+    const float r = t - kShifter;
     const float f = x - r;
-    float p = 0x1.5c08e6p-10f;
-    p = fmaf(p, f, 0x1.3d0c52p-7f);
-    p = fmaf(p, f, 0x1.c6b6e4p-5f);
-    p = fmaf(p, f, 0x1.ebf918p-3f);
-    p = fmaf(p, f, 0x1.62e428p-1f);
-    p = fmaf(p, f, 0x1.000002p+0f);
+    float p = kExp2C5;
+    p = fmaf(p, f, kExp2C4);
+    p = fmaf(p, f, kExp2C3);
+    p = fmaf(p, f, kExp2C2);
+    p = fmaf(p, f, kExp2C1);
+    p = fmaf(p, f, kExp2C0);
     return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
@@ -302,18 +339,88 @@ __device__ __forceinline__ float exp2_fma(float x)
 // (t = s*log2e + shifter and f = s*log2e - r each take one fused multiply-add).
 __device__ __forceinline__ float exp_fma(float s)
 {
-    constexpr float kLog2e = 1.4426950408889634f;
     s = fmaxf(s, -86.0f);  // s*log2e >= -124.07: the result stays a normal float
-    const float t = fmaf(s, kLog2e, 12582912.0f);
-    const float r = t - 12582912.0f;
+    const float t = fmaf(s, kLog2e, kShifter);
+    const float r = t - kShifter;
     const float f = fmaf(s, kLog2e, -r);
-    float p = 0x1.5c08e6p-10f;
-    p = fmaf(p, f, 0x1.3d0c52p-7f);
-    p = fmaf(p, f, 0x1.c6b6e4p-5f);
-    p = fmaf(p, f, 0x1.ebf918p-3f);
-    p = fmaf(p, f, 0x1.62e428p-1f);
-    p = fmaf(p, f, 0x1.000002p+0f);
+    float p = kExp2C5;
+    p = fmaf(p, f, kExp2C4);
+    p = fmaf(p, f, kExp2C3);
+    p = fmaf(p, f, kExp2C2);
+    p = fmaf(p, f, kExp2C1);
+    p = fmaf(p, f, kExp2C0);
     return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// ------------------------------------------------------------------ packed pairs (f32x2)
+// Blackwell's two-wide fp32 instructions process a pair of values per thread per instruction,
+// halving the FMA-pipe issue cost of the exponentials.
+
+__host__ __device__ constexpr uint64_t pair_of(uint32_t bits) { return (static_cast<uint64_t>(bits) << 32) | bits; }
+
+// The constants of exp_fma, each duplicated into both halves of a 64-bit register.
+struct ExpPairConsts {
+    uint64_t log2e, shifter, c5, c4, c3, c2, c1, c0;
+};
+
+__device__ __forceinline__ ExpPairConsts exp_pair_consts()
+{
+    return ExpPairConsts{pair_of(__float_as_uint(kLog2e)), pair_of(__float_as_uint(kShifter)),
+                         pair_of(__float_as_uint(kExp2C5)), pair_of(__float_as_uint(kExp2C4)),
+                         pair_of(__float_as_uint(kExp2C3)), pair_of(__float_as_uint(kExp2C2)),
+                         pair_of(__float_as_uint(kExp2C1)), pair_of(__float_as_uint(kExp2C0))};
+}
+
+// (exp(s0), exp(s1)) by exp_fma's steps on f32x2 pairs; bit-identical to exp_fma per element.
+// The exponent add is one integer multiply-add per element: bits(p) + bits(t) * 2^23.
+__device__ __forceinline__ void exp_pair_fma(uint32_t s0, uint32_t s1, const ExpPairConsts &k, uint32_t &e0,
+                                             uint32_t &e1)
+{
+    asm("{\n\t.reg .b64 a, t, nr, f, p;\n\t.reg .f32 a0, a1;\n\t.reg .b32 t0, t1, p0, p1;\n\t"
+        "max.f32 a0, %2, 0fC2AC0000;\n\t"  // -86.0
+        "max.f32 a1, %3, 0fC2AC0000;\n\t"
+        "mov.b64 a, {a0, a1};\n\t"
+        "fma.rn.f32x2 t, a, %4, %5;\n\t"     // t = s*log2e + shifter
+        "sub.rn.f32x2 nr, %5, t;\n\t"        // -r, exactly
+        "fma.rn.f32x2 f, a, %4, nr;\n\t"     // f = s*log2e - r
+        "fma.rn.f32x2 p, %6, f, %7;\n\t"
+        "fma.rn.f32x2 p, p, f, %8;\n\t"
+        "fma.rn.f32x2 p, p, f, %9;\n\t"
+        "fma.rn.f32x2 p, p, f, %10;\n\t"
+        "fma.rn.f32x2 p, p, f, %11;\n\t"
+        "mov.b64 {t0, t1}, t;\n\t"
+        "mov.b64 {p0, p1}, p;\n\t"
+        "mad.lo.u32 %0, t0, 8388608, p0;\n\t"
+        "mad.lo.u32 %1, t1, 8388608, p1;\n\t}"
+        : "=r"(e0), "=r"(e1)
+        : "f"(__uint_as_float(s0)), "f"(__uint_as_float(s1)), "l"(k.log2e), "l"(k.shifter), "l"(k.c5), "l"(k.c4),
+          "l"(k.c3), "l"(k.c2), "l"(k.c1), "l"(k.c0));
+}
+
+// (exp(s0), exp(s1)) on the MUFU unit: one packed multiply by log2(e), then ex2.approx each.
+__device__ __forceinline__ void exp_pair_mufu(uint32_t s0, uint32_t s1, const ExpPairConsts &k, uint32_t &e0,
+                                              uint32_t &e1)
+{
+    asm("{\n\t.reg .b64 a, x;\n\t.reg .f32 x0, x1;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mul.rn.f32x2 x, a, %4;\n\t"
+        "mov.b64 {x0, x1}, x;\n\t"
+        "ex2.approx.ftz.f32 x0, x0;\n\t"
+        "ex2.approx.ftz.f32 x1, x1;\n\t"
+        "mov.b32 %0, x0;\n\t"
+        "mov.b32 %1, x1;\n\t}"
+        : "=r"(e0), "=r"(e1)
+        : "r"(s0), "r"(s1), "l"(k.log2e));
+}
+
+// acc + (e0, e1) on an f32x2 pair.
+__device__ __forceinline__ uint64_t add_pair(uint64_t acc, uint32_t e0, uint32_t e1)
+{
+    uint64_t d;
+    asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%2, %3};\n\tadd.rn.f32x2 %0, %1, x;\n\t}"
+        : "=l"(d)
+        : "l"(acc), "r"(e0), "r"(e1));
+    return d;
 }
 
 // Two fp32 values to one fp16x2 word, round-to-nearest-even; `lo` lands at the lower address.

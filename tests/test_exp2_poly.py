@@ -14,20 +14,17 @@ sys.path.insert(0, CSRC)
 import exp2_poly_fit as fit  # noqa: E402
 
 
-def kernel_coefficients(fn="float exp2_fma(float x)"):
+def kernel_coefficients():
     text = open(os.path.join(CSRC, "ptx.cuh")).read()
-    body = text[text.index(fn):]
-    body = body[:body.index("}")]
-    return np.array([float.fromhex(h) for h in re.findall(r"(0x[0-9a-fA-F.]+p[-+]\d+)f", body)], dtype=np.float32)
+    found = dict(re.findall(r"constexpr float kExp2C(\d) = (0x[0-9a-fA-F.]+p[-+]\d+)f;", text))
+    return np.array([float.fromhex(found[str(i)]) for i in range(len(found))], dtype=np.float32)
 
 
 def test_kernel_constants_are_the_fit():
     c = fit.fit()
-    for fn in ("float exp2_fma(float x)", "float exp_fma(float s)"):
-        k = kernel_coefficients(fn)
-        assert k.size == fit.DEGREE + 1, fn
-        # Horner order in the kernel: highest degree first.
-        assert np.array_equal(k[::-1], c), fn
+    k = kernel_coefficients()
+    assert k.size == fit.DEGREE + 1
+    assert np.array_equal(k, c)  # kExp2C0 .. kExp2C5, lowest degree first like the fit
 
 
 def exp_emulated(s32, coef32):
