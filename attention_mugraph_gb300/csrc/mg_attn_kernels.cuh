@@ -30,10 +30,10 @@
 // Keeping P in tensor memory spares shared memory 64 KB of traffic per tile (P written by the
 // softmax warps and read back by the MMA), which otherwise bounds the tile rate.
 //
-// Exponentials: 4 of every 8 columns go through a polynomial on the FMA pipe (exp_pair_fma), the
-// rest through the MUFU unit (ex2.approx); both are fp32 with relative error near 2e-7, and both
-// use Blackwell's two-wide fp32 instructions. The split balances MUFU time against instruction
-// issue, since MUFU alone (16 per clock per SM) would bound the kernel.
+// Exponentials: ex2.approx on the MUFU unit after one two-wide fp32 multiply by log2(e) per pair
+// of columns. A polynomial path on the FMA pipe (exp_pair_fma, same fp32 accuracy) can take
+// kPolyOf8 of every 8 columns; measured on GB300, MUFU ex2 sustains about 26 exponentials per
+// clock per SM, so every column taken off it only adds instructions, and the split is 0.
 //
 // Every wait is bounded by a global-timer deadline. A wait that runs out records
 // MG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag, and every role then
@@ -54,7 +54,7 @@ constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBuffers = 2;
-constexpr int kPolyOf8 = 4;        // columns (of every 8) whose exp runs on the FMA pipe (even)
+constexpr int kPolyOf8 = 0;        // columns (of every 8, even) whose exp runs on the FMA pipe
 constexpr uint32_t kTmemO = 256;   // tensor-memory column of O; P buffers follow it
 constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
 constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warps
@@ -325,7 +325,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok)
                 ptx::tc_fence_after();
 
-            // O += P_u . V_u for local tile u.
+            // S_u = Q . K_u into S buffer u % 2: needs K/V tile u in its stage and, for u >= 2, the
+            // softmax warps to have read S_{u-2} out of that buffer.
+            auto issue_qk = [&](int u) -> bool {
+                const int s = u % STAGES;
+                const int sb = u & 1;
+                if (!wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKvFull + s))
+                    return false;
+                if (u >= 2 && !wait_bounded(wc, bar(BI::kSEmpty + sb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u,
+                                            BI::kSEmpty + sb))
+                    return false;
+                ptx::tc_fence_after();
+                // B = K: N-major; 16 d-rows (2048 B) per k-step; the two 64-column halves D*128 B apart.
+                const uint64_t k_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes, D * 128, 1024);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
+                                    idesc_s, k > 0 ? 1u : 0u);
+                ptx::mma_commit(bar(BI::kSFull + sb));
+                return true;
+            };
+
+            // O += P_u . V_u: needs the softmax warps to have written P_u; releases K/V stage u and
+            // P buffer u % 2 when it completes.
             auto issue_pv = [&](int u) -> bool {
                 const int pb = u % kPBuffers;
                 if (!wait_bounded(wc, bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb))
@@ -345,34 +367,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
 
-            int t = 0;
-            for (; ok && t < T; ++t) {
-                const int s = t % STAGES;
-                if (!wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(t / STAGES) & 1u, BI::kKvFull + s)) {
+            // S runs two tiles ahead of P.V: S_{t+2} goes in as soon as the softmax warps have read
+            // S_t (early in their work on tile t), so they find every later S ready and never wait
+            // for the tensor core. With a ring of fewer than 4 stages, K/V tile t+2 is often still in
+            // flight then (its stage is freed only by P.V_{t-1} or P.V_t), and waiting for it would
+            // hold back P.V_t, so there S_{t+2} follows P.V_t.
+            constexpr bool kEarlyS = STAGES >= 4;
+            for (int u = 0; ok && u < 2 && u < T; ++u)
+                ok = issue_qk(u);
+            for (int t = 0; ok && t < T; ++t) {
+                if (kEarlyS && t + 2 < T && !issue_qk(t + 2)) {
                     ok = false;
                     break;
                 }
-                const int sb = t & 1;
-                if (t >= 2 &&
-                    !wait_bounded(wc, bar(BI::kSEmpty + sb), (static_cast<uint32_t>(t >> 1) & 1u) ^ 1u, BI::kSEmpty + sb)) {
+                if (!issue_pv(t)) {
                     ok = false;
                     break;
                 }
-                ptx::tc_fence_after();
-                // B = K: N-major; 16 d-rows (2048 B) per k-step; the two 64-column halves D*128 B apart.
-                const uint64_t k_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes, D * 128, 1024);
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k)
-                    ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
-                                    idesc_s, k > 0 ? 1u : 0u);
-                ptx::mma_commit(bar(BI::kSFull + sb));
-                if (t >= 1 && !issue_pv(t - 1)) {
+                if (!kEarlyS && t + 2 < T && !issue_qk(t + 2)) {
                     ok = false;
                     break;
                 }
             }
-            if (ok && T > 0)
-                ok = issue_pv(T - 1);
             if (ok) {
                 ptx::mma_commit(bar(BI::kOFull));
                 // Tail: the commits that release the last P buffers must land before the CTA exits.
