@@ -26,6 +26,7 @@ MG_ERR_TIMEOUT = 7
 
 MG_FLAG_NO_PDL = 0x1
 MG_FLAG_INJECT_TIMEOUT = 0x2
+MG_FLAG_NO_CLUSTER = 0x4
 
 # Every function include/mg_attn.h declares.
 EXPORTS = ("mg_attn_plan", "mg_attn_plan_ex", "mg_attn_run", "mg_attn_run_host", "mg_attn_destroy",
@@ -44,7 +45,7 @@ class MgAttnPlanInfo(ctypes.Structure):
                 ("n_tiles", ctypes.c_int32), ("n_split", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("grid_ctas", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("tmem_cols", ctypes.c_int32), ("kernels_per_run", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("cluster_ctas", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

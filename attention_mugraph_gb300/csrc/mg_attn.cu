@@ -45,6 +45,7 @@ mg_status cuda_fail(cudaError_t e, const char *what)
 constexpr int64_t kMaxDim = int64_t(1) << 30;
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
+constexpr int64_t kMaxCluster = 16;  // largest thread-block cluster (non-portable size)
 
 // The driver's tensor-map encoder, fetched through the runtime so that no libcuda link is needed.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -117,7 +118,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     mg_attn_options o{};
     if (opts)
         o = *opts;
-    if (o.reserved != 0 || (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT)) != 0)
+    if (o.reserved != 0 || (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -137,7 +138,13 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
             n_split = n_tiles;
         if (n_split < 1)
             n_split = 1;
+        // Small problems: rather than more than 16 splits and a second kernel, take the largest
+        // cluster (16) when that leaves at most 4 column tiles per CTA.
+        if (n_split > kMaxCluster && !(o.flags & MG_FLAG_NO_CLUSTER) &&
+            (n_tiles + kMaxCluster - 1) / kMaxCluster <= 4)
+            n_split = kMaxCluster;
     }
+    const bool cluster = !(o.flags & MG_FLAG_NO_CLUSTER) && n_split >= 2 && n_split <= kMaxCluster;
     if (m_tiles * n_split > 0x7fffffffLL)
         return fail(MG_ERR_INVALID_ARG, "grid too large");
 
@@ -164,10 +171,11 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->grid_ctas = static_cast<int32_t>(m_tiles * n_split);
     info->smem_bytes = static_cast<int32_t>(smem);
     info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
-    info->kernels_per_run = n_split > 1 ? 2 : 1;
+    info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
-    const int64_t partial_bytes = n_split > 1 ? (n_split * B * M * d + n_split * B * M) * 4 : 0;
+    const int64_t partial_bytes = (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M) * 4 : 0;
     info->workspace_bytes = 256 + partial_bytes;
+    info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
     if (timeout_ns)
         *timeout_ns = o.timeout_ns ? static_cast<unsigned long long>(o.timeout_ns) : kDefaultTimeoutNs;
     if (flags)
@@ -177,6 +185,54 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
 }
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// Whether the current device can hold all ctas / n clusters of n CTAs of the fused kernel at
+// once (one wave: a cluster left for a second wave would double the time). Sizes above 8 need
+// the non-portable opt-in. Clears any error it provokes.
+bool cluster_schedulable(FwdKernel fwd, int n, int ctas, int smem)
+{
+    if (n > 8 && cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd),
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(mg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = static_cast<unsigned>(n);
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(fwd), &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return clusters >= (ctas + n - 1) / n;
+}
+
+// Launch attributes of the fused kernel: programmatic dependent launch and the cluster shape.
+int fused_launch_attrs(cudaLaunchAttribute (&attr)[2], bool pdl, int cluster_ctas)
+{
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_ctas > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_ctas);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    return n;
+}
 
 // 3-D tensor map over a contiguous (d2, d1, d0) array (d0 innermost) of fp16 (elem = 2) or fp32
 // (elem = 4) with a box of box0 x box1 x 1 elements and 128-byte swizzle; out-of-range elements
@@ -285,6 +341,15 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
         return fail(MG_ERR_UNSUPPORTED, "no sm_103a kernel image for device %d", dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
+    if (info.cluster_ctas > 0 && !cluster_schedulable(fwd, info.cluster_ctas, info.grid_ctas, info.smem_bytes)) {
+        // The device cannot place the cluster: plan again with the second-kernel combine.
+        mg_attn_options o{};
+        if (opts)
+            o = *opts;
+        o.flags |= MG_FLAG_NO_CLUSTER;
+        if ((st = decide(B, M, N, d, &o, sms, smem_optin, &info, &timeout_ns, &flags)) != MG_OK)
+            return st;
+    }
 
     struct mg_attn_plan *p = new (std::nothrow) struct mg_attn_plan();
     if (!p)
@@ -303,7 +368,7 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     uint8_t *ws = static_cast<uint8_t *>(p->workspace);
     p->status = reinterpret_cast<int *>(ws);
     std::memset(p->maps, 0, sizeof(p->maps));
-    if (info.n_split > 1) {
+    if (info.n_split > 1 && info.cluster_ctas == 0) {
         p->ws_o = reinterpret_cast<float *>(ws + 256);
         p->ws_l = p->ws_o + static_cast<size_t>(info.n_split) * B * M * d;
         // ws_o as (n_split*B, M, d) fp32, stored in {32, 128} boxes.
@@ -380,14 +445,14 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.m_tiles_per_b = static_cast<int>((M + mg::kBlockM - 1) / mg::kBlockM);
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
+    prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
+    prm.O = static_cast<__half *>(O);
     prm.ws_l = plan->ws_l;
     prm.status = plan->status;
     prm.timeout_ns = plan->timeout_ns;
     prm.inject_timeout = (plan->flags & MG_FLAG_INJECT_TIMEOUT) ? 1 : 0;
 
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
     const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
 
     cudaLaunchConfig_t cfg = {};
@@ -396,7 +461,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     cfg.dynamicSmemBytes = static_cast<size_t>(in.smem_bytes);
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, pdl, in.cluster_ctas));
     void *fwd_args[6] = {&plan->maps[0], &plan->maps[1], &plan->maps[2], &plan->maps[3], &plan->maps[4], &prm};
     cudaError_t e;
     if (plan->ev_begin && (e = cudaEventRecord(plan->ev_begin, cfg.stream)) != cudaSuccess)
@@ -407,7 +472,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     if (plan->ev_end && (e = cudaEventRecord(plan->ev_end, cfg.stream)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord(end)");
 
-    if (in.n_split > 1) {
+    if (in.n_split > 1 && in.cluster_ctas == 0) {
         int rows = static_cast<int>(B * M);
         int n_split = in.n_split;
         const float *wo = plan->ws_o;
@@ -418,6 +483,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
         cc.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), 1, 1);
         cc.blockDim = dim3(256, 1, 1);
         cc.dynamicSmemBytes = 0;
+        cc.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, pdl, 0));
         void *cargs[5] = {&wo, &wl, &out, &rows, &n_split};
         e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(plan->combine), cargs);
         if (e != cudaSuccess)
@@ -538,6 +604,13 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     st = decide(B, M, N, d, nullptr, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags);
     if (st != MG_OK)
         return st;
+    if (in.cluster_ctas > 0 &&
+        !cluster_schedulable(fwd_kernel(d, in.stages), in.cluster_ctas, in.grid_ctas, in.smem_bytes)) {
+        mg_attn_options o{};
+        o.flags = MG_FLAG_NO_CLUSTER;
+        if ((st = decide(B, M, N, d, &o, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags)) != MG_OK)
+            return st;
+    }
     if (in.workspace_bytes > static_cast<int64_t>(MG_ATTN_STATIC_SCRATCH_BYTES))
         return fail(MG_ERR_INVALID_ARG,
                     "shape needs %lld bytes of split scratch; the static scratch holds %u bytes "
@@ -558,7 +631,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     for (int i = 0; i < 4; ++i)
         if ((st = encode_3d(&maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i])) != MG_OK)
             return st;
-    float *ws_o = in.n_split > 1 ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
+    float *ws_o = (in.n_split > 1 && in.cluster_ctas == 0) ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
     if (ws_o && (st = encode_3d(&maps[4], ws_o, ud, uM, static_cast<uint64_t>(in.n_split) * uB, 32u, 128u, 4)) !=
                     MG_OK)
         return st;
@@ -570,26 +643,26 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.m_tiles_per_b = static_cast<int>((M + mg::kBlockM - 1) / mg::kBlockM);
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
+    prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
+    prm.O = static_cast<__half *>(O);
     prm.status = reinterpret_cast<int *>(sd->scratch);
     prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
 
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(in.grid_ctas), 1, 1);
     cfg.blockDim = dim3(mg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(in.smem_bytes);
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, true, in.cluster_ctas));
     void *fwd_args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4], &prm};
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fwd), fwd_args);
     if (e != cudaSuccess)
         return cuda_fail(e, "launch mg_attn_fwd_partial");
-    if (in.n_split > 1) {
+    if (in.n_split > 1 && in.cluster_ctas == 0) {
         int rows = static_cast<int>(B * M);
         int n_split = in.n_split;
         const float *wo = ws_o;
@@ -600,6 +673,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         cc.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), 1, 1);
         cc.blockDim = dim3(256, 1, 1);
         cc.dynamicSmemBytes = 0;
+        cc.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, true, 0));
         void *cargs[5] = {&wo, &wl, &out, &rows, &n_split};
         e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(combine_kernel(d)), cargs);
         if (e != cudaSuccess)

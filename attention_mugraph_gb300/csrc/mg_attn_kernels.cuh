@@ -20,13 +20,16 @@
 // graph of the "attention" search configuration (blog, section 4.3). No max-subtraction
 // means the partials combine by plain sums.
 //
-// Warp roles of kernel 1 (320 threads):
+// Warp roles of kernel 1 (352 threads):
 //   warp 0       TMA producer: Q once, then K/V tiles through a STAGES-deep mbarrier ring
-//   warp 1       tensor-memory allocator and MMA issuer (one thread)
+//   warp 1       tensor-memory allocator; issues S = Q.K (one thread)
+//   warp 10      issues O += P.V (one thread); two issuing warps keep an S from waiting behind
+//                a P.V and the reverse
 //   warps 2..9   softmax + epilogue. Warp w reads tensor-memory lanes 32*(w%4).. (its rows)
 //                and column half h = (w-2)/4 of each 128-column S tile: 64 columns per thread.
 // Tensor memory (512 columns): S double buffer at columns [0,128) and [128,256), O at
-// [256, 256 + d), the fp16 P double buffer (64 columns each, two fp16 per column) after O.
+// [256, 256 + d), then the fp16 P buffers (64 columns each, two fp16 per column): three for
+// d = 64, two for d = 128, so the softmax warps can run ahead of the P.V products.
 // Keeping P in tensor memory spares shared memory 64 KB of traffic per tile (P written by the
 // softmax warps and read back by the MMA), which otherwise bounds the tile rate.
 //
@@ -51,9 +54,9 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kThreads = 64 + kSoftmaxThreads;
+constexpr int kThreads = 96 + kSoftmaxThreads;  // load warp, S warp, 8 softmax warps, P.V warp
+constexpr int kPvWarp = kThreads / 32 - 1;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPBuffers = 2;
 constexpr int kPolyOf8 = 0;        // columns (of every 8, even) whose exp runs on the FMA pipe
 constexpr uint32_t kTmemO = 256;   // tensor-memory column of O; P buffers follow it
 constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
@@ -70,6 +73,8 @@ struct TileCfg {
     static constexpr uint32_t kChunkRows128 = 128 * 128;        // one 128-row x 128-byte chunk
     static constexpr int kHalfCols = D / 2;                     // O columns per softmax thread
     static constexpr uint32_t kTmemP = kTmemO + D;              // P buffer b at kTmemP + 64 b
+    // P buffers: as many as tensor memory holds after S (2 x 128 columns) and O (d columns).
+    static constexpr int kPBuffers = D == 64 ? 3 : 2;
     static_assert(kTmemP + 64 * kPBuffers <= kTmemCols, "tensor memory overflow");
 };
 
@@ -87,6 +92,8 @@ struct FwdParams {
     int m_tiles_per_b;       // ceil(M / 128)
     int n_tiles;             // ceil(N / 128)
     int n_split;
+    int cluster_reduce;      // the n_split CTAs of a row tile form a cluster and combine on chip
+    __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
     float *ws_l;             // (n_split, B, M) partial row sums
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
@@ -94,7 +101,7 @@ struct FwdParams {
 };
 
 // Barrier indices inside the CTA's barrier array.
-template <int STAGES>
+template <int STAGES, int kPBuffers>
 struct Bars {
     static constexpr int kQFull = 0;
     static constexpr int kKvFull = 1;
@@ -104,8 +111,9 @@ struct Bars {
     static constexpr int kPFull = kSEmpty + 2;
     static constexpr int kPEmpty = kPFull + kPBuffers;
     static constexpr int kOFull = kPEmpty + kPBuffers;
-    static constexpr int kDrain = kOFull + 1;
-    static constexpr int kNever = kDrain + 1;
+    static constexpr int kDrain = kOFull + 1;      // unwinding: the S warp's MMAs
+    static constexpr int kDrainPv = kDrain + 1;    // unwinding: the P.V warp's MMAs
+    static constexpr int kNever = kDrainPv + 1;
     static constexpr int kCount = kNever + 1;
 };
 
@@ -119,7 +127,9 @@ struct WaitCtx {
 // the deadline passes; the first waiter to time out records where.
 __device__ __forceinline__ bool wait_bounded(const WaitCtx &w, uint32_t bar, uint32_t parity, int where)
 {
-    if (ptx::mbar_try_wait(bar, parity))
+    // Fast path: a phase that has already completed is seen by a plain test, without the
+    // potentially-suspending try_wait.
+    if (ptx::mbar_test_wait(bar, parity))
         return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
@@ -185,9 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmW, const FwdParams p)
 {
     using C = TileCfg<D>;
-    using BI = Bars<STAGES>;
+    constexpr int kPBuffers = C::kPBuffers;
+    using BI = Bars<STAGES, kPBuffers>;
     static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
+    static_assert((128 * (D + 4) + 128) * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -202,11 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // CTA -> (b, split j, row tile mt); consecutive CTAs share (b, j) and so read the same
-    // K/V tiles close together in time.
+    // CTA -> (b, split j, row tile mt). With the on-chip combine, the n_split CTAs of a row tile
+    // are consecutive (one cluster, rank j); otherwise consecutive CTAs share (b, j) and so read
+    // the same K/V tiles close together in time.
     const int cta = blockIdx.x;
-    const int mt = cta % p.m_tiles_per_b;
-    const int j = (cta / p.m_tiles_per_b) % p.n_split;
+    const int mt = p.cluster_reduce ? (cta / p.n_split) % p.m_tiles_per_b : cta % p.m_tiles_per_b;
+    const int j = p.cluster_reduce ? cta % p.n_split : (cta / p.m_tiles_per_b) % p.n_split;
     const int b = cta / (p.m_tiles_per_b * p.n_split);
     const int m0 = mt * kBlockM;
     const int t_begin = static_cast<int>((static_cast<long long>(j) * p.n_tiles) / p.n_split);
@@ -221,14 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(bar(BI::kSFull + s), 1);
-            ptx::mbar_init(bar(BI::kSEmpty + s), kSoftmaxThreads);
+            ptx::mbar_init(bar(BI::kSEmpty + s), kSoftmaxWarps);
         }
         for (int s = 0; s < kPBuffers; ++s) {
-            ptx::mbar_init(bar(BI::kPFull + s), kSoftmaxThreads);
+            ptx::mbar_init(bar(BI::kPFull + s), kSoftmaxWarps);
             ptx::mbar_init(bar(BI::kPEmpty + s), 1);
         }
         ptx::mbar_init(bar(BI::kOFull), 1);
         ptx::mbar_init(bar(BI::kDrain), 1);
+        ptx::mbar_init(bar(BI::kDrainPv), 1);
         ptx::mbar_init(bar(BI::kNever), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -237,7 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmQ);
         ptx::prefetch_tensormap(&tmK);
         ptx::prefetch_tensormap(&tmV);
-        ptx::prefetch_tensormap(p.n_split == 1 ? &tmO : &tmW);
+        if (p.n_split == 1)
+            ptx::prefetch_tensormap(&tmO);
+        else if (!p.cluster_reduce)
+            ptx::prefetch_tensormap(&tmW);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
@@ -309,32 +326,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
+        // ---------------------------------------------------------------- S = Q.K issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockM, kBlockN, false, true);
-            constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
-            const uint32_t tmem_o = tmem + kTmemO;
-            // Descriptors are computed once (Q) or once per tile (K, V); each k-step adds a
-            // constant to the start-address field, so the issuing thread spends almost no
-            // instructions between MMAs (it shares its scheduler with two softmax warps).
+            // Descriptors are computed once (Q) or once per tile (K); each k-step adds a constant
+            // to the start-address field, so the issuing thread spends almost no instructions
+            // between MMAs (it shares its scheduler with two softmax warps).
             uint64_t a_q[D / 16];
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)  // A = Q: K-major; 16-column steps advance 32 B in a swizzle row
                 a_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
             bool ok = wait_bounded(wc, bar(BI::kQFull), 0, BI::kQFull);
-            if (ok)
-                ptx::tc_fence_after();
-
-            // S_u = Q . K_u into S buffer u % 2: needs K/V tile u in its stage and, for u >= 2, the
-            // softmax warps to have read S_{u-2} out of that buffer.
-            auto issue_qk = [&](int u) -> bool {
+            // S_u = Q . K_u into S buffer u % 2, as soon as K/V tile u is in its stage and, for
+            // u >= 2, the softmax warps have read S_{u-2} out of that buffer (which they do first
+            // thing on tile u-2). The P.V products run from another warp, so an S never waits
+            // behind a P.V and the softmax warps find every S ready.
+            for (int u = 0; ok && u < T; ++u) {
                 const int s = u % STAGES;
                 const int sb = u & 1;
-                if (!wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKvFull + s))
-                    return false;
-                if (u >= 2 && !wait_bounded(wc, bar(BI::kSEmpty + sb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u,
-                                            BI::kSEmpty + sb))
-                    return false;
+                if (!wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKvFull + s) ||
+                    (u >= 2 && !wait_bounded(wc, bar(BI::kSEmpty + sb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u,
+                                             BI::kSEmpty + sb))) {
+                    ok = false;
+                    break;
+                }
                 ptx::tc_fence_after();
                 // B = K: N-major; 16 d-rows (2048 B) per k-step; the two 64-column halves D*128 B apart.
                 const uint64_t k_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes, D * 128, 1024);
@@ -343,17 +358,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
                                     idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
-                return true;
-            };
-
-            // O += P_u . V_u: needs the softmax warps to have written P_u; releases K/V stage u and
-            // P buffer u % 2 when it completes.
-            auto issue_pv = [&](int u) -> bool {
+            }
+            if (!ok) {
+                // Unwind: wait for the MMAs already issued before tensor memory is freed.
+                ptx::mma_commit(bar(BI::kDrain));
+                wait_drain(bar(BI::kDrain), 0, p.timeout_ns);
+            }
+        }
+    } else if (warp == kPvWarp) {
+        // ---------------------------------------------------------------- O += P.V issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
+            const uint32_t tmem_o = tmem + kTmemO;
+            bool ok = true;
+            // O += P_u . V_u once the softmax warps have written P_u (K/V tile u is in its stage
+            // long before: S_u, which precedes P_u, needed it). The completion releases K/V stage u
+            // and P buffer u % kPBuffers.
+            for (int u = 0; ok && u < T; ++u) {
                 const int pb = u % kPBuffers;
-                if (!wait_bounded(wc, bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb))
-                    return false;
-                ptx::tc_fence_after();
                 const int s = u % STAGES;
+                if (!wait_bounded(wc, bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb) ||
+                    !wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKvFull + s)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
                 const uint32_t tP = tmem + C::kTmemP + pb * 64;
                 // B = V: N(=d)-major, 16 rows (2048 B) per k-step; d-chunks 128 rows x 128 B apart.
                 const uint64_t v_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes + C::kKBytes, C::kChunkRows128, 1024);
@@ -364,30 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ts(tmem_o, tP + k * 8, v_desc + static_cast<uint64_t>(k * (2048 >> 4)), idesc_o, 1u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
-                return true;
-            };
-
-            // S runs two tiles ahead of P.V: S_{t+2} goes in as soon as the softmax warps have read
-            // S_t (early in their work on tile t), so they find every later S ready and never wait
-            // for the tensor core. With a ring of fewer than 4 stages, K/V tile t+2 is often still in
-            // flight then (its stage is freed only by P.V_{t-1} or P.V_t), and waiting for it would
-            // hold back P.V_t, so there S_{t+2} follows P.V_t.
-            constexpr bool kEarlyS = STAGES >= 4;
-            for (int u = 0; ok && u < 2 && u < T; ++u)
-                ok = issue_qk(u);
-            for (int t = 0; ok && t < T; ++t) {
-                if (kEarlyS && t + 2 < T && !issue_qk(t + 2)) {
-                    ok = false;
-                    break;
-                }
-                if (!issue_pv(t)) {
-                    ok = false;
-                    break;
-                }
-                if (!kEarlyS && t + 2 < T && !issue_qk(t + 2)) {
-                    ok = false;
-                    break;
-                }
             }
             if (ok) {
                 ptx::mma_commit(bar(BI::kOFull));
@@ -396,9 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_bounded(wc, bar(BI::kPEmpty + u % kPBuffers), static_cast<uint32_t>(u / kPBuffers) & 1u,
                                       BI::kPEmpty + u % kPBuffers);
             } else {
-                // Unwind: wait for the MMAs already issued before tensor memory is freed.
-                ptx::mma_commit(bar(BI::kDrain));
-                wait_drain(bar(BI::kDrain), 0, p.timeout_ns);
+                ptx::mma_commit(bar(BI::kDrainPv));
+                wait_drain(bar(BI::kDrainPv), 0, p.timeout_ns);
             }
         }
     } else {
@@ -437,8 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld_wait(r1);
             }
             // S is in registers: its tensor-memory buffer can take the next-but-one tile.
+            // One arrival per warp (after a warp barrier) rather than per thread: 256 arrivals on
+            // one barrier word would serialise as shared-memory atomics on every tile.
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(BI::kSEmpty + sb));
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(bar(BI::kSEmpty + sb));
             if (t >= kPBuffers &&
                 !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
                            BI::kPEmpty + pb)) {
@@ -459,7 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_st_wait();
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(BI::kPFull + pb));
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(bar(BI::kPFull + pb));
         }
 
         // ------------------------------------------------------------ epilogue
@@ -477,9 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l = l_xchg[row] + l_xchg[kBlockM + row];
         if (o_ready) {
             ptx::tc_fence_after();
-            // The K/V ring is idle (every PV has completed): stage this CTA's output in its first
-            // stage, in the 128-byte-swizzled layout the output tensor maps expect, then TMA-store it.
+            // The K/V ring is idle (every PV has completed): stage this CTA's output there. For the
+            // on-chip combine: fp32 rows of d + 4 floats (the pad keeps 8 consecutive rows on distinct
+            // banks) and the row sums after them, read by the cluster's CTAs at teardown. Otherwise
+            // the 128-byte-swizzled layout the output tensor maps expect, then a TMA store.
             const uint32_t stage = sStage0;
+            float *stage_f = reinterpret_cast<float *>(smem + C::kQBytes);
             if (warp_rows) {
 #pragma unroll
                 for (int c = 0; c < C::kHalfCols / 32; ++c) {
@@ -487,7 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int col = h * C::kHalfCols + c * 32;  // first O column of this slice
                     ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, r);
                     ptx::tmem_ld_wait(r);
-                    if (p.n_split == 1) {
+                    if (p.cluster_reduce) {
+                        float4 *dst = reinterpret_cast<float4 *>(stage_f + row * (D + 4) + col);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    } else if (p.n_split == 1) {
                         // fp16 O/l: chunk col/64 of a {64, 128} fp16 box; this slice is units (col%64)/8 .. +3.
                         const uint32_t chunk = stage + (col / 64) * C::kChunkRows128;
                         const uint32_t u0 = static_cast<uint32_t>((col % 64) / 8);
@@ -512,11 +531,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.n_split > 1 && h == 0 && m0 + row < p.M)
-                p.ws_l[(static_cast<size_t>(j) * p.B + b) * p.M + m0 + row] = l;
-            ptx::fence_proxy_async_smem();
-            ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
-            if (sw == 0 && lane == 0) {
+            if (p.cluster_reduce) {
+                if (h == 0)
+                    stage_f[kBlockM * (D + 4) + row] = l;
+            } else {
+                if (p.n_split > 1 && h == 0 && m0 + row < p.M)
+                    p.ws_l[(static_cast<size_t>(j) * p.B + b) * p.M + m0 + row] = l;
+                ptx::fence_proxy_async_smem();
+                ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
+            }
+            if (!p.cluster_reduce && sw == 0 && lane == 0) {
                 if (p.n_split == 1) {
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c)  // O[b, m0:m0+128, 64c:64c+64]
@@ -532,8 +556,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // Teardown: every tensor-memory access of the CTA is ordered before the free.
+    // On-chip combine of the split partials: after the first cluster barrier every CTA's staged
+    // (O_j, l_j) is visible; CTA rank j sums rows [128 j / n, 128 (j+1) / n) of its row tile over
+    // all n ranks in rank order (reproducible), divides and writes fp16 O. The second barrier
+    // keeps each CTA's shared memory alive until the others have read it. Every thread of every
+    // CTA reaches both barriers, on the unwinding path too.
     __syncwarp();
+    if (p.cluster_reduce) {
+        ptx::cluster_sync();
+        if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
+            constexpr int G = D / 4;  // float4 groups per row
+            const int n = p.n_split;
+            const int lo = j * kBlockM / n;
+            const int hi = (j + 1) * kBlockM / n;
+            const uint32_t st = ptx::smem_u32(smem + C::kQBytes);
+            const uint32_t ls = st + kBlockM * (D + 4) * 4;
+            for (int it = threadIdx.x - 64; it < (hi - lo) * G; it += kSoftmaxThreads) {
+                const int rr = lo + it / G;
+                const int g = it % G;
+                if (m0 + rr >= p.M)
+                    continue;
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lsum = 0.f;
+                const uint32_t off = static_cast<uint32_t>((rr * (D + 4) + g * 4) * 4);
+                for (int r = 0; r < n; ++r) {
+                    const float4 v = ptx::ld_cluster_v4(ptx::map_to_rank(st + off, r));
+                    a.x += v.x;
+                    a.y += v.y;
+                    a.z += v.z;
+                    a.w += v.w;
+                    lsum += ptx::ld_cluster_f32(ptx::map_to_rank(ls + rr * 4, r));
+                }
+                uint2 w;
+                w.x = ptx::pack_half2(__fdiv_rn(a.x, lsum), __fdiv_rn(a.y, lsum));
+                w.y = ptx::pack_half2(__fdiv_rn(a.z, lsum), __fdiv_rn(a.w, lsum));
+                *reinterpret_cast<uint2 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + g * 4) = w;
+            }
+        }
+        ptx::cluster_sync();
+    }
+
+    // Teardown: every tensor-memory access of the CTA is ordered before the free.
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -65,12 +65,15 @@ typedef enum {
 
 /* Flags for mg_attn_options.flags. */
 #define MG_FLAG_NO_PDL 0x1         /* launch without programmatic dependent launch */
+#define MG_FLAG_NO_CLUSTER 0x4     /* always combine split partials with the second kernel, never on chip */
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and
                                       the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */
 
 typedef struct {
-    int32_t n_split;    /* CTAs sharing one 128-row tile along N; 0 = automatic. 1 <= n_split <= ceil(N/128) */
+    int32_t n_split;    /* CTAs sharing one 128-row tile along N; 0 = automatic. 1 <= n_split <= ceil(N/128).
+                           2..16 splits combine on chip in a thread-block cluster when the device can
+                           schedule the cluster (unless MG_FLAG_NO_CLUSTER); more use the second kernel */
     int32_t stages;     /* K/V shared-memory pipeline depth; 0 = automatic (the deepest); 2..6 (d = 128: 2..3) */
     int32_t flags;      /* MG_FLAG_* bits */
     int32_t reserved;   /* must be 0 */
@@ -89,9 +92,13 @@ typedef struct {
     int32_t grid_ctas;       /* m_tiles * n_split */
     int32_t smem_bytes;      /* dynamic shared memory per CTA of the fused kernel */
     int32_t tmem_cols;       /* tensor-memory columns allocated per CTA */
-    int32_t kernels_per_run; /* 1 when n_split == 1 (the fused kernel writes O), else 2 */
+    int32_t kernels_per_run; /* 1 when the fused kernel writes O itself (n_split == 1 or cluster_ctas > 0), else 2 */
     int32_t num_sms;         /* streaming multiprocessors the plan was sized for */
     int64_t workspace_bytes; /* device bytes owned by the plan (split partials + status words) */
+    int32_t cluster_ctas;    /* > 0: the n_split CTAs of a row tile run as one thread-block cluster
+                                and combine their partials in distributed shared memory (no second
+                                kernel, no partials in global memory); 0: second kernel */
+    int32_t reserved0;
 } mg_attn_plan_info;
 
 /*

@@ -47,8 +47,9 @@ def test_struct_layout_matches_header(tmp_path):
 #include "mg_attn.h"
 int main(void) {
   printf("%zu %zu %zu\\n", sizeof(mg_attn_options), offsetof(mg_attn_options, timeout_ns), offsetof(mg_attn_options, flags));
-  printf("%zu %zu %zu %zu\\n", sizeof(mg_attn_plan_info), offsetof(mg_attn_plan_info, block_m),
-         offsetof(mg_attn_plan_info, num_sms), offsetof(mg_attn_plan_info, workspace_bytes));
+  printf("%zu %zu %zu %zu %zu\\n", sizeof(mg_attn_plan_info), offsetof(mg_attn_plan_info, block_m),
+         offsetof(mg_attn_plan_info, num_sms), offsetof(mg_attn_plan_info, workspace_bytes),
+         offsetof(mg_attn_plan_info, cluster_ctas));
   return 0;
 }
 """)
@@ -58,7 +59,7 @@ int main(void) {
     O, I = _lib.MgAttnOptions, _lib.MgAttnPlanInfo
     assert [int(x) for x in l1.split()] == [ctypes.sizeof(O), O.timeout_ns.offset, O.flags.offset]
     assert [int(x) for x in l2.split()] == [ctypes.sizeof(I), I.block_m.offset, I.num_sms.offset,
-                                            I.workspace_bytes.offset]
+                                            I.workspace_bytes.offset, I.cluster_ctas.offset]
 
 
 def test_status_strings_and_version(lib):
@@ -86,13 +87,28 @@ def test_query_decisions(B, M, N, d):
         assert info["n_split"] == 1
     else:
         assert info["grid_ctas"] <= 152  # one wave
-    assert info["kernels_per_run"] == (2 if info["n_split"] > 1 else 1)
+    cluster = info["cluster_ctas"]
+    assert cluster in (0, info["n_split"]) and cluster <= 16
+    if 2 <= info["n_split"] <= 16:
+        assert cluster == info["n_split"]  # small splits combine on chip
+    assert info["kernels_per_run"] == (2 if info["n_split"] > 1 and cluster == 0 else 1)
     assert info["smem_bytes"] <= 232448
     rng = tile_ranges(n_tiles, info["n_split"])
     assert rng[0][0] == 0 and rng[-1][1] == n_tiles
     assert all(a < b for a, b in rng) and all(rng[i][1] == rng[i + 1][0] for i in range(len(rng) - 1))
-    ws = 256 + (info["n_split"] * B * M * (d + 1) * 4 if info["n_split"] > 1 else 0)
+    ws = 256 + (info["n_split"] * B * M * (d + 1) * 4 if info["n_split"] > 1 and cluster == 0 else 0)
     assert info["workspace_bytes"] == ws
+
+
+def test_query_cluster_choices():
+    # The GQA tutorial shape takes a 16-CTA cluster (2 column tiles per CTA) instead of 32 splits.
+    assert mg.mg_attn_query(2, 256, 4096, 64, 152)["cluster_ctas"] == 16
+    # A long KV axis keeps one wave of splits and the second kernel.
+    lkv = mg.mg_attn_query(2, 256, 65536, 64, 152)
+    assert lkv["n_split"] == 38 and lkv["cluster_ctas"] == 0 and lkv["kernels_per_run"] == 2
+    # The flag forces the second kernel.
+    nc = mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_NO_CLUSTER)
+    assert nc["cluster_ctas"] == 0 and nc["n_split"] == 32 and nc["kernels_per_run"] == 2
 
 
 def test_query_options():

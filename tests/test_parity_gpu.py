@@ -95,6 +95,20 @@ def test_split_and_pipeline_depth_d128(n_split, stages):
     assert_parity(O, ref, f"d=128 n_split={n_split} stages={stages}")
 
 
+@pytest.mark.parametrize("B,M,N,d,n_split", [(2, 256, 4096, 64, 16), (1, 200, 2056, 64, 3), (4, 100, 4104, 128, 9),
+                                             (3, 129, 1032, 64, 8), (2, 17, 1024, 128, 2), (1, 384, 8192, 64, 13)])
+def test_cluster_combine_matches_second_kernel(B, M, N, d, n_split):
+    # The on-chip combine (thread-block cluster, distributed shared memory) against the oracle and
+    # against the second-kernel combine of the same split.
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=n_split * 7 + d)
+    ref = oracle.attention(q, k, v)
+    O_cl, plan = run_gpu(q, k, v, n_split=n_split)
+    O_k2, plan2 = run_gpu(q, k, v, n_split=n_split, flags=mg.MG_FLAG_NO_CLUSTER)
+    assert plan2.info["cluster_ctas"] == 0 and plan2.info["kernels_per_run"] == 2
+    assert_parity(O_cl, ref, f"cluster {plan.info['cluster_ctas']}")
+    assert_parity(O_k2, ref, "second kernel")
+
+
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
     # Scores 0 everywhere -> every weight is exp(0)=1: any column past N that leaked into the row
     # sum (zero-filled K gives exp(0)=1 too) would pull the mean toward 0.
