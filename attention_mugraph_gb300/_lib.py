@@ -32,6 +32,8 @@ MG_FLAG_NO_CLUSTER = 0x4
 EXPORTS = ("mg_attn_plan", "mg_attn_plan_ex", "mg_attn_run", "mg_attn_run_host", "mg_attn_destroy",
            "mg_attn_get_status", "mg_attn_get_info", "mg_attn_query", "mg_attn_status_string",
            "mg_attn_last_error", "mg_attn_version", "mg_attn_set_timing_events", "mg_attn_run_noalloc")
+# Every function include/mg_diag.h declares.
+DIAG_EXPORTS = ("mg_diag_launch_floor", "mg_diag_exp_rate", "mg_diag_last_error")
 
 
 class MgAttnOptions(ctypes.Structure):
@@ -98,6 +100,12 @@ def _bind(lib):
     lib.mg_attn_run_noalloc.restype = st
     lib.mg_attn_version.argtypes = []
     lib.mg_attn_version.restype = i32
+    lib.mg_diag_launch_floor.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_float)]
+    lib.mg_diag_launch_floor.restype = st
+    lib.mg_diag_exp_rate.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    lib.mg_diag_exp_rate.restype = st
+    lib.mg_diag_last_error.argtypes = []
+    lib.mg_diag_last_error.restype = ctypes.c_char_p
     return lib
 
 
@@ -216,6 +224,27 @@ class Plan:
                 self._lib.mg_attn_destroy(self._h)
         except Exception:
             pass
+
+
+def _check_diag(status: int, where: str):
+    if status != MG_OK:
+        raise MgAttnError(status, where, load_library().mg_diag_last_error().decode())
+
+
+def diag_launch_floor(ctas, cluster=1, smem_bytes=215296, pdl=True, launches=1000) -> float:
+    """µs per launch of a no-work kernel with this launch shape (``mg_diag_launch_floor``)."""
+    out = ctypes.c_float()
+    _check_diag(load_library().mg_diag_launch_floor(int(ctas), int(cluster), int(smem_bytes), 1 if pdl else 0,
+                                                    int(launches), ctypes.byref(out)), "mg_diag_launch_floor")
+    return float(out.value)
+
+
+def diag_exp_rate(iters=2000, poly=False) -> tuple:
+    """(exponentials per SM clock, per SM ns) of the fused kernel's exp (``mg_diag_exp_rate``)."""
+    clk, ns = ctypes.c_double(), ctypes.c_double()
+    _check_diag(load_library().mg_diag_exp_rate(int(iters), 1 if poly else 0, ctypes.byref(clk), ctypes.byref(ns)),
+                "mg_diag_exp_rate")
+    return float(clk.value), float(ns.value)
 
 
 def mg_attn_plan(B, M, N, d, **opts) -> Plan:

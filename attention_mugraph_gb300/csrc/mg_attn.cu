@@ -45,7 +45,7 @@ mg_status cuda_fail(cudaError_t e, const char *what)
 constexpr int64_t kMaxDim = int64_t(1) << 30;
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
-constexpr int64_t kMaxCluster = 16;  // largest thread-block cluster (non-portable size)
+constexpr int64_t kMaxCluster = mg::kMaxClusterRanks;  // largest thread-block cluster (non-portable size)
 
 // The driver's tensor-map encoder, fetched through the runtime so that no libcuda link is needed.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()

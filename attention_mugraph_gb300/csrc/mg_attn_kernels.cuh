@@ -61,6 +61,7 @@ constexpr int kPolyOf8 = 0;        // columns (of every 8, even) whose exp runs 
 constexpr uint32_t kTmemO = 256;   // tensor-memory column of O; P buffers follow it
 constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
 constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warps
+constexpr int kMaxClusterRanks = 16;     // largest cluster of the on-chip combine
 
 template <int D>
 struct TileCfg {
@@ -84,7 +85,7 @@ struct TileCfg {
 __host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages)
 {
     return 1024u + static_cast<uint32_t>(128 * d * 2) + static_cast<uint32_t>(stages) * (2u * d * 128 * 2) +
-           2u * 128 * 4 + 256u;
+           2u * 128 * 4 + 512u;
 }
 
 struct FwdParams {
@@ -104,8 +105,9 @@ struct FwdParams {
 template <int STAGES, int kPBuffers>
 struct Bars {
     static constexpr int kQFull = 0;
-    static constexpr int kKvFull = 1;
-    static constexpr int kKvEmpty = kKvFull + STAGES;
+    static constexpr int kKFull = 1;                // K tile of a stage landed (the S warp waits)
+    static constexpr int kVFull = kKFull + STAGES;  // V tile of a stage landed (the P.V warp waits)
+    static constexpr int kKvEmpty = kVFull + STAGES;
     static constexpr int kSFull = kKvEmpty + STAGES;
     static constexpr int kSEmpty = kSFull + 2;
     static constexpr int kPFull = kSEmpty + 2;
@@ -115,6 +117,7 @@ struct Bars {
     static constexpr int kDrainPv = kDrain + 1;    // unwinding: the P.V warp's MMAs
     static constexpr int kNever = kDrainPv + 1;
     static constexpr int kCount = kNever + 1;
+    static_assert(kCount * 8 + 8 <= 512, "barrier area overflow");
 };
 
 struct WaitCtx {
@@ -229,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(BI::kQFull), 1);
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bar(BI::kKvFull + s), 1);
+            ptx::mbar_init(bar(BI::kKFull + s), 1);
+            ptx::mbar_init(bar(BI::kVFull + s), 1);
             ptx::mbar_init(bar(BI::kKvEmpty + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -299,15 +303,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n0 = (t_begin + t) * kBlockN;
                 const uint32_t sK = sStage0 + s * C::kStageBytes;
                 const uint32_t sV = sK + C::kKBytes;
-                ptx::mbar_arrive_expect_tx(bar(BI::kKvFull + s), C::kStageBytes);
+                // K and V land on separate barriers: S = Q.K need not wait for V.
+                ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), C::kKBytes);
+                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
                 ++armed[s];
                 // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
-                ptx::tma_load_3d(sK, &tmK, bar(BI::kKvFull + s), n0, 0, b);
-                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKvFull + s), n0 + 64, 0, b);
+                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
+                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
                 // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kKvFull + s), c * 64, n0, b);
+                    ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
             }
             if (ok) {
                 // Tail: the commits that release the last stages must land before the CTA exits.
@@ -321,8 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_drain(bar(BI::kQFull), 0, p.timeout_ns);
 #pragma unroll
                 for (int s = 0; s < STAGES; ++s)
-                    if (armed[s] > 0)
-                        wait_drain(bar(BI::kKvFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
+                    if (armed[s] > 0) {
+                        wait_drain(bar(BI::kKFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
+                        wait_drain(bar(BI::kVFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
+                    }
             }
         }
     } else if (warp == 1) {
@@ -337,14 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < D / 16; ++k)  // A = Q: K-major; 16-column steps advance 32 B in a swizzle row
                 a_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
             bool ok = wait_bounded(wc, bar(BI::kQFull), 0, BI::kQFull);
-            // S_u = Q . K_u into S buffer u % 2, as soon as K/V tile u is in its stage and, for
+            // S_u = Q . K_u into S buffer u % 2, as soon as K tile u is in its stage and, for
             // u >= 2, the softmax warps have read S_{u-2} out of that buffer (which they do first
             // thing on tile u-2). The P.V products run from another warp, so an S never waits
             // behind a P.V and the softmax warps find every S ready.
             for (int u = 0; ok && u < T; ++u) {
                 const int s = u % STAGES;
                 const int sb = u & 1;
-                if (!wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKvFull + s) ||
+                if (!wait_bounded(wc, bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s) ||
                     (u >= 2 && !wait_bounded(wc, bar(BI::kSEmpty + sb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u,
                                              BI::kSEmpty + sb))) {
                     ok = false;
@@ -371,14 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
             const uint32_t tmem_o = tmem + kTmemO;
             bool ok = true;
-            // O += P_u . V_u once the softmax warps have written P_u (K/V tile u is in its stage
-            // long before: S_u, which precedes P_u, needed it). The completion releases K/V stage u
-            // and P buffer u % kPBuffers.
+            // O += P_u . V_u once the softmax warps have written P_u and V tile u has landed (K
+            // tile u, which S_u needed, shares its stage). The completion releases K/V stage u and
+            // P buffer u % kPBuffers.
             for (int u = 0; ok && u < T; ++u) {
                 const int pb = u % kPBuffers;
                 const int s = u % STAGES;
                 if (!wait_bounded(wc, bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb) ||
-                    !wait_bounded(wc, bar(BI::kKvFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKvFull + s)) {
+                    !wait_bounded(wc, bar(BI::kVFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kVFull + s)) {
                     ok = false;
                     break;
                 }
@@ -576,16 +584,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int g = it % G;
                 if (m0 + rr >= p.M)
                     continue;
+                const uint32_t off = static_cast<uint32_t>((rr * (D + 4) + g * 4) * 4);
+                // Every rank's values are requested before the first is used: the remote reads
+                // are then in flight together rather than one round trip after another.
+                float4 v[kMaxClusterRanks];
+                float lv[kMaxClusterRanks];
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r) {
+                    if (r < n) {
+                        v[r] = ptx::ld_cluster_v4(ptx::map_to_rank(st + off, r));
+                        lv[r] = ptx::ld_cluster_f32(ptx::map_to_rank(ls + rr * 4, r));
+                    }
+                }
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
                 float lsum = 0.f;
-                const uint32_t off = static_cast<uint32_t>((rr * (D + 4) + g * 4) * 4);
-                for (int r = 0; r < n; ++r) {
-                    const float4 v = ptx::ld_cluster_v4(ptx::map_to_rank(st + off, r));
-                    a.x += v.x;
-                    a.y += v.y;
-                    a.z += v.z;
-                    a.w += v.w;
-                    lsum += ptx::ld_cluster_f32(ptx::map_to_rank(ls + rr * 4, r));
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r) {
+                    if (r < n) {
+                        a.x += v[r].x;
+                        a.y += v[r].y;
+                        a.z += v[r].z;
+                        a.w += v[r].w;
+                        lsum += lv[r];
+                    }
                 }
                 uint2 w;
                 w.x = ptx::pack_half2(__fdiv_rn(a.x, lsum), __fdiv_rn(a.y, lsum));
@@ -593,7 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint2 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + g * 4) = w;
             }
         }
-        ptx::cluster_sync();
+        // Only "every CTA has finished reading the others' shared memory" is needed here; a
+        // release would also hold each CTA until its output stores had drained.
+        ptx::cluster_sync_relaxed();
     }
 
     // Teardown: every tensor-memory access of the CTA is ordered before the free.

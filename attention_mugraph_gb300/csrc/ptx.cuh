@@ -183,6 +183,15 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Cluster-wide barrier without release semantics: it says only that every thread of the cluster
+// has got here. A CTA's earlier loads from other CTAs' shared memory have returned by then (their
+// values were used), and its global stores need not drain first, which a release would make it
+// wait for.
+__device__ __forceinline__ void cluster_sync_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // The shared::cluster address of the same shared-memory location in the cluster's CTA `rank`.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
 {

@@ -13,8 +13,11 @@ with these additions:
     twice the L2 size, so each call reads its inputs from HBM, not L2;
   * the timed steps are replayed from a CUDA graph (host launch cost excluded); a plain
     stream loop is timed too and reported beside it;
-  * the fused kernel alone is timed with events the library records around it, for the
-    roofline fraction;
+  * the roofline fraction uses the fused kernel's average duration: the timed region / K
+    when a step is that one kernel, else events the library records around each launch;
+  * two floors outside the roofline formula are measured in the same run and reported
+    beside it (``ceilings``): the launch floor of the plan's launch shape and the time of the
+    B*M*N exponentials at the measured per-SM rate;
   * the end-to-end number runs the host-buffer entry point: host->device copies of Q, K, V,
     the kernels, and the device->host copy of O, every step.
 The CPU baseline is the fp64 oracle (test infrastructure) on the host cores.
@@ -80,6 +83,18 @@ def load_peaks():
             p = json.load(f)
         return p, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ceilings(info, B, M, N, exp_rate_ns, roof_us):
+    """The two floors outside the roofline formula, for one plan: the launch floor of its launch
+    shape (a no-work kernel with the fused kernel's prologue, measured now) and the time of its
+    B*M*N exponentials at the measured per-SM rate on every SM."""
+    import attention_mugraph_gb300 as mg
+
+    floor = mg.diag_launch_floor(info["grid_ctas"], max(1, info["cluster_ctas"]), info["smem_bytes"], True, 1000)
+    t_exp = B * M * N / (exp_rate_ns * info["num_sms"]) / 1e3
+    return {"launch_floor_us": floor, "exp_time_us": t_exp, "roofline_us": roof_us,
+            "floor_us": max(floor, t_exp, roof_us)}
 
 
 def kernel_source_digest():
@@ -268,7 +283,7 @@ def workload_config(B, M, N, d, a, extra=None):
 
 # ------------------------------------------------------------------ GPU arm
 
-def measure_workload(name, steps, peaks, stream):
+def measure_workload(name, steps, peaks, stream, exp_rate_ns):
     """Graph-replayed µs/call over rotating buffer sets (> 2x L2) and the fused kernel's own time for
     one named workload; returns a dict for the JSON line's per_config field."""
     import torch
@@ -329,13 +344,14 @@ def measure_workload(name, steps, peaks, stream):
     roof = max(t_tensor, t_hbm) * 1e6
     st = plan.status()
     info = plan.info
-    plan.destroy()
     if st != mg.MG_OK:
         raise SystemExit(f"{name}: device status {st}")
+    plan.destroy()
     return {"B": B, "M": M, "N": N, "d": d, "us_per_call": us, "tflops": fl / (us * 1e-6) / 1e12,
             "hbm_gbs": by / (us * 1e-6) / 1e9, "roofline_us": roof, "roofline_frac": roof / us,
             "bound": "hbm" if t_hbm >= t_tensor else "tensor", "fused_kernel_us_median": k_us,
-            "n_split": info["n_split"], "buffer_sets": n_sets}
+            "n_split": info["n_split"], "cluster_ctas": info["cluster_ctas"], "buffer_sets": n_sets,
+            "ceilings": ceilings(info, B, M, N, exp_rate_ns, roof)}
 
 
 def main():
@@ -494,14 +510,29 @@ def main():
     t_tensor = fl / (peaks["bf16_tflops"] * 1e12)
     t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
     bound = "hbm" if t_hbm >= t_tensor else "tensor"
+    # The fused kernel's average launch duration. When a step is that one kernel, the timed
+    # region itself (CUDA events on the launching stream around K back-to-back launches) gives it;
+    # events recorded around each single launch would add their own latency to a few-µs kernel.
+    # With a second (combine) kernel per step, the per-launch events bracket the fused kernel.
+    if info["kernels_per_run"] == 1:
+        dur_us = ms_graph * 1e3 / args.steps
+        dur_source = "timed region / steps (one kernel per step)"
+    else:
+        dur_us = fwd_us
+        dur_source = "mean of CUDA events recorded around each fused-kernel launch"
     if bound == "hbm":
-        achieved = alg_bytes / (fwd_us * 1e-6) / 1e9
+        achieved = alg_bytes / (dur_us * 1e-6) / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     else:
-        achieved = fl / (fwd_us * 1e-6) / 1e12
+        achieved = fl / (dur_us * 1e-6) / 1e12
         peak = peaks["bf16_tflops"]
         unit = "TFLOP/s"
+
+    # Exponential rate of the fused kernel's instruction sequence (MUFU), and of the FMA-pipe
+    # polynomial it can move columns to, per SM clock and per SM ns.
+    exp_clk, exp_ns = mg.diag_exp_rate(2000, poly=False)
+    poly_clk, poly_ns = mg.diag_exp_rate(2000, poly=True)
 
     if rank != 0:
         return
@@ -528,21 +559,25 @@ def main():
                         "unit": "TFLOP/s"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": recorded_traffic(), "kernel": "mg_attn_fwd_partial",
-                     "kernel_us_mean": fwd_us, "kernel_us_median": fwd_us_median,
+                     "kernel_us": dur_us, "kernel_us_source": dur_source,
+                     "event_bracketed_us_mean": fwd_us, "event_bracketed_us_median": fwd_us_median,
                      "algorithmic_bytes_per_launch": alg_bytes, "flops_per_launch": fl,
                      "peak_source": f"{peak_kind}: MEASURED_PEAKS.json "
                                     f"{'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'} (burst)",
-                     "tensor_frac": fl / (fwd_us * 1e-6) / 1e12 / peaks["bf16_tflops"]},
+                     "tensor_frac": fl / (dur_us * 1e-6) / 1e12 / peaks["bf16_tflops"]},
         "e2e": {"value": fl * n_e2e / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e, "us_per_call": ms_e2e * 1e3 / n_e2e},
         "gpu_launches": args.steps * info["kernels_per_run"],
         "clocks": clk,
+        "ceilings": dict(ceilings(info, B, M, N, exp_ns, roof_t * 1e6),
+                         exp_per_clk_per_sm_mufu=exp_clk, exp_per_ns_per_sm_mufu=exp_ns,
+                         exp_per_clk_per_sm_fma_poly=poly_clk, exp_per_ns_per_sm_fma_poly=poly_ns),
     }
     if world == 1:
         if not args.no_per_config:
             from attention_mugraph_gb300 import inputs as _inputs
 
-            line["per_config"] = {name: measure_workload(name, args.per_config_steps, peaks, stream)
+            line["per_config"] = {name: measure_workload(name, args.per_config_steps, peaks, stream, exp_ns)
                                   for name in _inputs.CONFIG_ORDER}
         line["cpu_baseline"] = cpu_baseline(q, k, v, args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -15,6 +15,7 @@ from attention_mugraph_gb300 import _lib, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "mg_attn.h")
+DIAG_HEADER = os.path.join(ROOT, "include", "mg_diag.h")
 
 
 @pytest.fixture(scope="module")
@@ -23,15 +24,18 @@ def lib():
     return _lib.load_library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:mg_status|const char \*|int32_t)\s*\*?\s*(mg_attn_\w+)\s*\(", text, re.M)))
+def declared_functions(header=HEADER, prefix="mg_attn_"):
+    text = open(header).read()
+    return sorted(set(re.findall(rf"^\s*(?:mg_status|const char \*|int32_t)\s*\*?\s*({prefix}\w+)\s*\(", text, re.M)))
 
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) >= 10
+    diag = declared_functions(DIAG_HEADER, "mg_diag_")
+    assert len(names) >= 10 and len(diag) == 3
     assert sorted(_lib.EXPORTS) == names
+    assert sorted(_lib.DIAG_EXPORTS) == diag
+    names = names + diag
     for name in names:
         assert hasattr(lib, name), f"{name} not exported"
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
@@ -161,3 +165,19 @@ def test_product_path_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "mg_oracle" not in text and "libmgoracle" not in text, f
+
+
+@pytest.mark.parametrize("args", [(0, 1, 215296, 1, 10), (64, 3, 215296, 1, 10), (64, 17, 215296, 1, 10),
+                                  (64, 16, 215296, 1, 0), (64, 16, 215296, 1, 100001)])
+def test_diag_launch_floor_rejects_bad_arguments_before_any_cuda_call(lib, args):
+    out = ctypes.c_float(-1.0)
+    assert lib.mg_diag_launch_floor(*args, ctypes.byref(out)) == mg.MG_ERR_INVALID_ARG
+    assert out.value == -1.0 and lib.mg_diag_last_error()
+    assert lib.mg_diag_launch_floor(64, 16, 215296, 1, 10, None) == mg.MG_ERR_INVALID_ARG
+
+
+def test_diag_exp_rate_rejects_bad_arguments_before_any_cuda_call(lib):
+    a, b = ctypes.c_double(), ctypes.c_double()
+    assert lib.mg_diag_exp_rate(0, 0, ctypes.byref(a), ctypes.byref(b)) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_diag_exp_rate(1000001, 1, ctypes.byref(a), ctypes.byref(b)) == mg.MG_ERR_INVALID_ARG
+    assert lib.mg_diag_exp_rate(10, 0, None, ctypes.byref(b)) == mg.MG_ERR_INVALID_ARG
