@@ -25,8 +25,10 @@
 //   warp 1       tensor-memory allocator; issues S = Q.K (one thread)
 //   warp 10      issues O += P.V (one thread); two issuing warps keep an S from waiting behind
 //                a P.V and the reverse
-//   warps 2..9   softmax + epilogue. Warp w reads tensor-memory lanes 32*(w%4).. (its rows)
-//                and column half h = (w-2)/4 of each 128-column S tile: 64 columns per thread.
+//   warps 2..9   softmax + epilogue, two groups of four: group g = (w-2)/4 takes the tiles
+//                t with t % 2 == g, in S buffer g, all 128 columns of its rows; warp w reads
+//                tensor-memory lanes 32*(w%4).. (its rows). In the epilogue group g takes
+//                O columns [g d/2, (g+1) d/2).
 // Tensor memory (512 columns): S double buffer at columns [0,128) and [128,256), O at
 // [256, 256 + d), then the fp16 P buffers (64 columns each, two fp16 per column): three for
 // d = 64, two for d = 128, so the softmax warps can run ahead of the P.V products.
@@ -35,8 +37,8 @@
 //
 // Exponentials: ex2.approx on the MUFU unit after one two-wide fp32 multiply by log2(e) per pair
 // of columns. A polynomial path on the FMA pipe (exp_pair_fma, same fp32 accuracy) can take
-// kPolyOf8 of every 8 columns; measured on GB300, MUFU ex2 sustains about 26 exponentials per
-// clock per SM, so every column taken off it only adds instructions, and the split is 0.
+// kPolyOf8 of every 8 columns; measured on GB300 (mg_diag_exp_rate), this sequence runs 32
+// exponentials per clock per SM on MUFU and 13 on the FMA pipe, so the split is 0.
 //
 // Every wait is bounded by a global-timer deadline. A wait that runs out records
 // MG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag, and every role then
@@ -54,6 +56,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kGroupWarps = kSoftmaxWarps / 2;  // softmax warps per group (one tile each)
 constexpr int kThreads = 96 + kSoftmaxThreads;  // load warp, S warp, 8 softmax warps, P.V warp
 constexpr int kPvWarp = kThreads / 32 - 1;
 constexpr uint32_t kTmemCols = 512;
@@ -238,10 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(bar(BI::kSFull + s), 1);
-            ptx::mbar_init(bar(BI::kSEmpty + s), kSoftmaxWarps);
+            ptx::mbar_init(bar(BI::kSEmpty + s), kGroupWarps);
         }
         for (int s = 0; s < kPBuffers; ++s) {
-            ptx::mbar_init(bar(BI::kPFull + s), kSoftmaxWarps);
+            ptx::mbar_init(bar(BI::kPFull + s), kGroupWarps);
             ptx::mbar_init(bar(BI::kPEmpty + s), 1);
         }
         ptx::mbar_init(bar(BI::kOFull), 1);
@@ -335,65 +338,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- S = Q.K issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockM, kBlockN, false, true);
-            // Descriptors are computed once (Q) or once per tile (K); each k-step adds a constant
-            // to the start-address field, so the issuing thread spends almost no instructions
-            // between MMAs (it shares its scheduler with two softmax warps).
-            uint64_t a_q[D / 16];
+        // The whole warp runs the loop and takes every wait together (the decision to go on is a
+        // warp vote); the lane elect.sync picks issues each tile's MMAs and their commit. Measured
+        // on GB300, an M=128, N=64 MMA issued this way occupies the tensor pipe 32 cycles (its
+        // arithmetic), against 45 from a lone thread looping on its own and 57 from "lane == 0"
+        // of a converged warp.
+        constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockM, kBlockN, false, true);
+        uint64_t a_q[D / 16];
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)  // A = Q: K-major; 16-column steps advance 32 B in a swizzle row
-                a_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
-            bool ok = wait_bounded(wc, bar(BI::kQFull), 0, BI::kQFull);
-            // S_u = Q . K_u into S buffer u % 2, as soon as K tile u is in its stage and, for
-            // u >= 2, the softmax warps have read S_{u-2} out of that buffer (which they do first
-            // thing on tile u-2). The P.V products run from another warp, so an S never waits
-            // behind a P.V and the softmax warps find every S ready.
-            for (int u = 0; ok && u < T; ++u) {
-                const int s = u % STAGES;
-                const int sb = u & 1;
-                if (!wait_bounded(wc, bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s) ||
-                    (u >= 2 && !wait_bounded(wc, bar(BI::kSEmpty + sb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u,
-                                             BI::kSEmpty + sb))) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                // B = K: N-major; 16 d-rows (2048 B) per k-step; the two 64-column halves D*128 B apart.
-                const uint64_t k_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes, D * 128, 1024);
+        for (int k = 0; k < D / 16; ++k)  // A = Q: K-major; 16-column steps advance 32 B in a swizzle row
+            a_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
+        auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+            return __all_sync(0xffffffffu, wait_bounded(wc, b_, parity, where));
+        };
+        bool ok = warp_wait(bar(BI::kQFull), 0, BI::kQFull);
+        // S_u = Q . K_u into S buffer u % 2, as soon as K tile u is in its stage and, for
+        // u >= 2, the softmax warps have read S_{u-2} out of that buffer (which they do first
+        // thing on tile u-2). The P.V products run from another warp, so an S never waits
+        // behind a P.V and the softmax warps find every S ready.
+        for (int u = 0; ok && u < T; ++u) {
+            const int s = u % STAGES;
+            const int sb = u & 1;
+            if (!warp_wait(bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s) ||
+                (u >= 2 &&
+                 !warp_wait(bar(BI::kSEmpty + sb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u, BI::kSEmpty + sb))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            // B = K: N-major; 16 d-rows (2048 B) per k-step; the two 64-column halves D*128 B apart.
+            const uint64_t k_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes, D * 128, 1024);
+            if (ptx::elect_one()) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
                     ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
                                     idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
             }
-            if (!ok) {
-                // Unwind: wait for the MMAs already issued before tensor memory is freed.
+            __syncwarp();
+        }
+        if (!ok) {
+            // Unwind: wait for the MMAs already issued before tensor memory is freed (elect.sync
+            // picks the same lane of the full warp every time).
+            if (ptx::elect_one()) {
                 ptx::mma_commit(bar(BI::kDrain));
                 wait_drain(bar(BI::kDrain), 0, p.timeout_ns);
             }
+            __syncwarp();
         }
     } else if (warp == kPvWarp) {
         // ---------------------------------------------------------------- O += P.V issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
-            const uint32_t tmem_o = tmem + kTmemO;
-            bool ok = true;
-            // O += P_u . V_u once the softmax warps have written P_u and V tile u has landed (K
-            // tile u, which S_u needed, shares its stage). The completion releases K/V stage u and
-            // P buffer u % kPBuffers.
-            for (int u = 0; ok && u < T; ++u) {
-                const int pb = u % kPBuffers;
-                const int s = u % STAGES;
-                if (!wait_bounded(wc, bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb) ||
-                    !wait_bounded(wc, bar(BI::kVFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kVFull + s)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t tP = tmem + C::kTmemP + pb * 64;
-                // B = V: N(=d)-major, 16 rows (2048 B) per k-step; d-chunks 128 rows x 128 B apart.
-                const uint64_t v_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes + C::kKBytes, C::kChunkRows128, 1024);
+        // Same pattern as the S issuer: warp-wide waits, the elected lane issues.
+        constexpr uint32_t idesc_o = ptx::idesc_f16_f32(kBlockM, D, false, true);
+        const uint32_t tmem_o = tmem + kTmemO;
+        auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+            return __all_sync(0xffffffffu, wait_bounded(wc, b_, parity, where));
+        };
+        bool ok = true;
+        // O += P_u . V_u once the softmax warps have written P_u and V tile u has landed (K
+        // tile u, which S_u needed, shares its stage). The completion releases K/V stage u and
+        // P buffer u % kPBuffers.
+        for (int u = 0; ok && u < T; ++u) {
+            const int pb = u % kPBuffers;
+            const int s = u % STAGES;
+            if (!warp_wait(bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb) ||
+                !warp_wait(bar(BI::kVFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kVFull + s)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t tP = tmem + C::kTmemP + pb * 64;
+            // B = V: N(=d)-major, 16 rows (2048 B) per k-step; d-chunks 128 rows x 128 B apart.
+            const uint64_t v_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes + C::kKBytes, C::kChunkRows128, 1024);
+            if (ptx::elect_one()) {
                 // A = P in tensor memory: 16 K-columns per step are 8 tensor-memory columns.
                 ptx::mma_f16_ts(tmem_o, tP, v_desc, idesc_o, u > 0 ? 1u : 0u);
 #pragma unroll
@@ -401,23 +418,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ts(tmem_o, tP + k * 8, v_desc + static_cast<uint64_t>(k * (2048 >> 4)), idesc_o, 1u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
+                if (u == T - 1)  // committed by the thread that issued every P.V
+                    ptx::mma_commit(bar(BI::kOFull));
             }
-            if (ok) {
-                ptx::mma_commit(bar(BI::kOFull));
-                // Tail: the commits that release the last P buffers must land before the CTA exits.
-                for (int u = T - kPBuffers > 0 ? T - kPBuffers : 0; ok && u < T; ++u)
-                    ok = wait_bounded(wc, bar(BI::kPEmpty + u % kPBuffers), static_cast<uint32_t>(u / kPBuffers) & 1u,
-                                      BI::kPEmpty + u % kPBuffers);
-            } else {
+            __syncwarp();
+        }
+        if (ok) {
+            // Tail: the commits that release the last P buffers must land before the CTA exits.
+            for (int u = T - kPBuffers > 0 ? T - kPBuffers : 0; ok && u < T; ++u)
+                ok = warp_wait(bar(BI::kPEmpty + u % kPBuffers), static_cast<uint32_t>(u / kPBuffers) & 1u,
+                               BI::kPEmpty + u % kPBuffers);
+        } else {
+            if (ptx::elect_one()) {
                 ptx::mma_commit(bar(BI::kDrainPv));
                 wait_drain(bar(BI::kDrainPv), 0, p.timeout_ns);
             }
+            __syncwarp();
         }
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
         const int sw = warp - 2;                 // 0..7
         const int q4 = warp & 3;                 // tensor-memory lane quarter this warp may access
-        const int h = sw >> 2;                   // column half of every S tile (and of O)
+        const int g = sw >> 2;                   // warp group: takes the tiles t with t % 2 == g
         const int row = q4 * 32 + lane;          // row inside the 128-row tile
         const bool warp_rows = (m0 + q4 * 32) < p.M;  // warp-uniform: any valid row in this warp
         const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
@@ -430,50 +452,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc[2] = {0, 0};  // packed fp32 partial row sums (+0.0 bit patterns)
         const ptx::ExpPairConsts ek = ptx::exp_pair_consts();
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
-            const int sb = t & 1;
+        // The two groups alternate tiles, each with its own S buffer (g): while one group's warps
+        // wait on tensor memory or a barrier, the other group's warps on the same scheduler keep
+        // the MUFU unit busy. A thread covers its row's 128 columns of a tile in two 64-column
+        // halves (64 fp32 registers at a time).
+        for (int t = g; t < T; t += 2) {
             const int pb = t % kPBuffers;
-            if (!warp_wait(bar(BI::kSFull + sb), static_cast<uint32_t>(t >> 1) & 1u, BI::kSFull + sb)) {
+            if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(t >> 1) & 1u, BI::kSFull + g)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            // Columns of this tile inside N, relative to this thread's half.
-            const int n_valid = p.N - (t_begin + t) * kBlockN - h * 64;
-            uint32_t r0[32], r1[32];
-            if (warp_rows) {
-                const uint32_t s_addr = tmem + lane_addr + sb * kBlockN + h * 64;
-                ptx::tmem_ld_32x32b_x32(s_addr, r0);
-                ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
-                ptx::tmem_ld_wait(r0);
-                ptx::tmem_ld_wait(r1);
-            }
-            // S is in registers: its tensor-memory buffer can take the next-but-one tile.
-            // One arrival per warp (after a warp barrier) rather than per thread: 256 arrivals on
-            // one barrier word would serialise as shared-memory atomics on every tile.
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(bar(BI::kSEmpty + sb));
-            if (t >= kPBuffers &&
-                !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
-                           BI::kPEmpty + pb)) {
-                ok = false;
-                break;
-            }
-            if (warp_rows) {
-                // This half's 64 columns of P are tensor-memory columns [32h, 32h + 32) of buffer pb.
-                uint32_t w[32];
-                if (n_valid >= 64) {
-                    exp_slice<false>(r0, 0, n_valid, w, acc, ek);
-                    exp_slice<false>(r1, 32, n_valid, w + 16, acc, ek);
-                } else {
-                    exp_slice<true>(r0, 0, n_valid, w, acc, ek);
-                    exp_slice<true>(r1, 32, n_valid, w + 16, acc, ek);
+            const int n_valid = p.N - (t_begin + t) * kBlockN;  // columns of this tile inside N
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r0[32], r1[32];
+                if (warp_rows) {
+                    const uint32_t s_addr = tmem + lane_addr + g * kBlockN + half * 64;
+                    ptx::tmem_ld_32x32b_x32(s_addr, r0);
+                    ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
+                    ptx::tmem_ld_wait(r0);
+                    ptx::tmem_ld_wait(r1);
                 }
-                ptx::tmem_st_32x32b_x32(tmem + lane_addr + C::kTmemP + pb * 64 + h * 32, w);
-                ptx::tmem_st_wait();
+                if (half == 1) {
+                    // All of S is in registers: the buffer can take this group's next tile. One
+                    // arrival per warp (after a warp barrier) rather than per thread.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bar(BI::kSEmpty + g));
+                } else if (t >= kPBuffers &&
+                           !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
+                                      BI::kPEmpty + pb)) {
+                    ok = false;
+                    break;
+                }
+                if (warp_rows) {
+                    // Columns [64 half, 64 half + 64) of P are tensor-memory columns
+                    // [32 half, 32 half + 32) of buffer pb (two fp16 per column).
+                    const int nv = n_valid - half * 64;
+                    uint32_t w[32];
+                    if (nv >= 64) {
+                        exp_slice<false>(r0, 0, nv, w, acc, ek);
+                        exp_slice<false>(r1, 32, nv, w + 16, acc, ek);
+                    } else {
+                        exp_slice<true>(r0, 0, nv, w, acc, ek);
+                        exp_slice<true>(r1, 32, nv, w + 16, acc, ek);
+                    }
+                    ptx::tmem_st_32x32b_x32(tmem + lane_addr + C::kTmemP + pb * 64 + half * 32, w);
+                    ptx::tmem_st_wait();
+                }
             }
+            if (!ok)
+                break;
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -481,12 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ------------------------------------------------------------ epilogue
-        // Row sum: this thread's half, then the two halves added in a fixed order.
-        const float l_half = (__uint_as_float(static_cast<uint32_t>(acc[0])) +
-                              __uint_as_float(static_cast<uint32_t>(acc[0] >> 32))) +
-                             (__uint_as_float(static_cast<uint32_t>(acc[1])) +
-                              __uint_as_float(static_cast<uint32_t>(acc[1] >> 32)));
-        l_xchg[h * kBlockM + row] = l_half;
+        // Row sum: this thread's tiles, then the two groups' sums added in a fixed order.
+        const float l_group = (__uint_as_float(static_cast<uint32_t>(acc[0])) +
+                               __uint_as_float(static_cast<uint32_t>(acc[0] >> 32))) +
+                              (__uint_as_float(static_cast<uint32_t>(acc[1])) +
+                               __uint_as_float(static_cast<uint32_t>(acc[1] >> 32)));
+        l_xchg[g * kBlockM + row] = l_group;
         // One barrier publishes the half sums and makes "O is ready" a decision all eight softmax
         // warps share (a warp that unwound from an abort votes no), so the barrier inside the
         // branch below is reached by all of them or by none.
@@ -505,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < C::kHalfCols / 32; ++c) {
                     uint32_t r[32];
-                    const int col = h * C::kHalfCols + c * 32;  // first O column of this slice
+                    const int col = g * C::kHalfCols + c * 32;  // first O column of this slice
                     ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, r);
                     ptx::tmem_ld_wait(r);
                     if (p.cluster_reduce) {
@@ -540,10 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (p.cluster_reduce) {
-                if (h == 0)
+                if (g == 0)
                     stage_f[kBlockM * (D + 4) + row] = l;
             } else {
-                if (p.n_split > 1 && h == 0 && m0 + row < p.M)
+                if (p.n_split > 1 && g == 0 && m0 + row < p.M)
                     p.ws_l[(static_cast<size_t>(j) * p.B + b) * p.M + m0 + row] = l;
                 ptx::fence_proxy_async_smem();
                 ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
