@@ -204,13 +204,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU (oracle) timing
 
-def time_oracle(q, k, v, seconds: float, rows_per_call=None):
+def time_oracle(q, k, v, seconds: float, rows_per_call=None, threads=None):
     """Run the fp64 oracle repeatedly for about `seconds`; returns (calls, elapsed, rows, threads).
-    rows_per_call=None runs the whole workload per call, else that many leading rows."""
+    rows_per_call=None runs the whole workload per call, else that many leading rows; threads=None
+    uses every host thread OpenMP offers."""
     import oracle
 
     lib = oracle.load_library()
-    threads = oracle.max_threads(lib)
+    threads = oracle.max_threads(lib) if threads is None else int(threads)
     B, M, d = q.shape
     rows = list(range(B * M if rows_per_call is None else min(rows_per_call, B * M)))
     calls, t0 = 0, time.perf_counter()
@@ -226,9 +227,14 @@ def cpu_baseline(q, k, v, seconds):
     B, M, N, d = q.shape[0], q.shape[1], k.shape[2], q.shape[2]
     calls, el, rows, threads = time_oracle(q, k, v, seconds)
     fl = 4.0 * rows * N * d * calls
+    # The same oracle on one thread, on a sample of leading rows (a third of the time budget).
+    c1, el1, rows1, _ = time_oracle(q, k, v, max(1.0, seconds / 3), rows_per_call=32, threads=1)
+    fl1 = 4.0 * rows1 * N * d * c1
     return {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{calls} full oracle evaluations of the {WORKLOAD} workload ({rows} rows x N={N} x d={d}, "
-                      f"fp64) in {el:.1f} s on {threads} host threads"}
+                      f"fp64) in {el:.1f} s on {threads} host threads",
+            "single_thread": {"value": fl1 / el1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"{c1} evaluations of the first {rows1} rows in {el1:.1f} s on 1 thread"}}
 
 
 def run_reference(args, rank, world):
