@@ -9,7 +9,7 @@
 #include <cstdio>
 #include <vector>
 
-#include "ptx.cuh"
+#include "mg_attn_kernels.cuh"
 
 namespace {
 
@@ -29,16 +29,19 @@ mg_status diag_cuda(cudaError_t e, const char *what)
     return diag_fail(MG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-constexpr int kFloorThreads = 352;  // the fused kernel's block size
+constexpr int kFloorThreads = mg::kThreads;  // the fused kernel's block size
 constexpr int kFloorMinSmem = 120 * 1024;
 constexpr int kExpThreads = 512;
 constexpr int kExpPairs = 8;  // independent pairs per thread and round
 
 // The fused kernel's prologue and teardown and nothing else: tensor-memory allocation by warp 1,
 // the dependent-launch handshake, one cluster barrier, the free.
+// The tensor-memory address lives in the dynamic shared memory, like the fused kernel's, so the
+// kernel accepts the same dynamic size (up to the opt-in limit, with no static shared memory).
 __global__ void __launch_bounds__(kFloorThreads, 1) floor_kernel(int use_cluster)
 {
-    __shared__ uint32_t holder;
+    extern __shared__ uint32_t dyn_smem[];
+    uint32_t &holder = dyn_smem[0];
     const int warp = threadIdx.x >> 5;
     if (warp == 1) {
         mg::ptx::tmem_alloc(mg::ptx::smem_u32(&holder), 512);

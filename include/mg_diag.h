@@ -40,7 +40,7 @@ extern "C" {
  *               at most the device's opt-in limit
  *   pdl         nonzero: programmatic dependent launch, as mg_attn_run uses by default
  *   launches    1 .. 100000
- * Each CTA has 352 threads, like the fused kernel. Errors: MG_ERR_INVALID_ARG (a NULL
+ * Each CTA has as many threads as the fused kernel. Errors: MG_ERR_INVALID_ARG (a NULL
  * output or a value out of range), MG_ERR_CONFIG (the cluster cannot be scheduled),
  * MG_ERR_CUDA. */
 mg_status mg_diag_launch_floor(int32_t ctas, int32_t cluster, int32_t smem_bytes, int32_t pdl, int32_t launches,
