@@ -27,6 +27,7 @@ MG_ERR_TIMEOUT = 7
 MG_FLAG_NO_PDL = 0x1
 MG_FLAG_INJECT_TIMEOUT = 0x2
 MG_FLAG_NO_CLUSTER = 0x4
+MG_FLAG_SAFE_SOFTMAX = 0x8
 
 # Every function include/mg_attn.h declares.
 EXPORTS = ("mg_attn_plan", "mg_attn_plan_ex", "mg_attn_run", "mg_attn_run_host", "mg_attn_destroy",

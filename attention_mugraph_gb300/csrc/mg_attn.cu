@@ -90,7 +90,7 @@ FwdKernel fwd_kernel(int64_t d, int stages)
     return nullptr;
 }
 
-using CombineKernel = void (*)(const float *, const float *, __half *, int, int);
+using CombineKernel = void (*)(const float *, const float *, const float *, __half *, int, int);
 
 CombineKernel combine_kernel(int64_t d)
 {
@@ -118,7 +118,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     mg_attn_options o{};
     if (opts)
         o = *opts;
-    if (o.reserved != 0 || (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER)) != 0)
+    if (o.reserved != 0 ||
+        (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -173,7 +174,10 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
     info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
-    const int64_t partial_bytes = (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M) * 4 : 0;
+    // Split partials for the second kernel: numerators, row sums and (max-subtracted variant) row maxima.
+    const int64_t row_words = (o.flags & MG_FLAG_SAFE_SOFTMAX) ? 2 : 1;
+    const int64_t partial_bytes =
+        (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M * row_words) * 4 : 0;
     info->workspace_bytes = 256 + partial_bytes;
     info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
     if (timeout_ns)
@@ -263,10 +267,11 @@ struct mg_attn_plan {
     mg_attn_plan_info info{};
     int flags = 0;
     unsigned long long timeout_ns = kDefaultTimeoutNs;
-    void *workspace = nullptr;  // [status words | ws_o | ws_l]
+    void *workspace = nullptr;  // [status words | ws_o | ws_l | ws_m (max-subtracted variant)]
     int *status = nullptr;
     float *ws_o = nullptr;
     float *ws_l = nullptr;
+    float *ws_m = nullptr;
     FwdKernel fwd = nullptr;
     CombineKernel combine = nullptr;
     // Tensor maps Q, K, V, O (re-encoded when a pointer changes) and the fp32 partial workspace
@@ -371,6 +376,8 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     if (info.n_split > 1 && info.cluster_ctas == 0) {
         p->ws_o = reinterpret_cast<float *>(ws + 256);
         p->ws_l = p->ws_o + static_cast<size_t>(info.n_split) * B * M * d;
+        if (flags & MG_FLAG_SAFE_SOFTMAX)
+            p->ws_m = p->ws_l + static_cast<size_t>(info.n_split) * B * M;
         // ws_o as (n_split*B, M, d) fp32, stored in {32, 128} boxes.
         st = encode_3d(&p->maps[4], p->ws_o, d, M, static_cast<uint64_t>(info.n_split) * B, 32u, 128u, 4);
         if (st != MG_OK) {
@@ -448,6 +455,8 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
     prm.O = static_cast<__half *>(O);
     prm.ws_l = plan->ws_l;
+    prm.ws_m = plan->ws_m;
+    prm.safe = (plan->flags & MG_FLAG_SAFE_SOFTMAX) ? 1 : 0;
     prm.status = plan->status;
     prm.timeout_ns = plan->timeout_ns;
     prm.inject_timeout = (plan->flags & MG_FLAG_INJECT_TIMEOUT) ? 1 : 0;
@@ -477,6 +486,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
         int n_split = in.n_split;
         const float *wo = plan->ws_o;
         const float *wl = plan->ws_l;
+        const float *wm = plan->ws_m;
         __half *out = static_cast<__half *>(O);
         const int rows_per_cta = d == 64 ? mg::CombineCfg<64>::kRows : mg::CombineCfg<128>::kRows;
         cudaLaunchConfig_t cc = cfg;
@@ -484,7 +494,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
         cc.blockDim = dim3(256, 1, 1);
         cc.dynamicSmemBytes = 0;
         cc.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, pdl, 0));
-        void *cargs[5] = {&wo, &wl, &out, &rows, &n_split};
+        void *cargs[6] = {&wo, &wl, &wm, &out, &rows, &n_split};
         e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(plan->combine), cargs);
         if (e != cudaSuccess)
             return cuda_fail(e, "launch mg_attn_combine");
@@ -647,6 +657,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.O = static_cast<__half *>(O);
     prm.status = reinterpret_cast<int *>(sd->scratch);
     prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
+    prm.ws_m = nullptr;
+    prm.safe = 0;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
 
@@ -674,7 +686,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         cc.blockDim = dim3(256, 1, 1);
         cc.dynamicSmemBytes = 0;
         cc.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, true, 0));
-        void *cargs[5] = {&wo, &wl, &out, &rows, &n_split};
+        const float *wm = nullptr;
+        void *cargs[6] = {&wo, &wl, &wm, &out, &rows, &n_split};
         e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(combine_kernel(d)), cargs);
         if (e != cudaSuccess)
             return cuda_fail(e, "launch mg_attn_combine");

@@ -45,6 +45,7 @@
 // stops, drains the copies/MMAs it issued (again bounded), frees tensor memory and returns.
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 #include <cuda_fp16.h>
 
@@ -99,6 +100,8 @@ struct FwdParams {
     int cluster_reduce;      // the n_split CTAs of a row tile form a cluster and combine on chip
     __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
     float *ws_l;             // (n_split, B, M) partial row sums
+    float *ws_m;             // (n_split, B, M) partial row maxima (max-subtracted variant only)
+    int safe;                // max-subtracted variant: a first pass finds each row's maximum score
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
     int inject_timeout;
@@ -171,12 +174,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, uint32_t unit)
 }
 
 // The exponentials of one 32-column slice of a score row, packed as fp16 pairs into w[16]:
-// exp(s[i]) for columns below n_valid, 0 past N (MASK: only the last tile needs the test). Pairs
-// of columns go through the f32x2 pipe: columns 0-3 of every 8 by the polynomial, 4-7 by MUFU.
+// exp(s[i] - m) for columns below n_valid, 0 past N (MASK: only the last tile needs the test);
+// `shift` holds -m*log2(e) twice (+0 for the graph as written, where m = 0). Pairs of columns go
+// through the f32x2 pipe: the first kPolyOf8 of every 8 by the polynomial, the rest by MUFU.
 // The fp32 values add into two packed partial row sums (fixed order).
 template <bool MASK>
 __device__ __forceinline__ void exp_slice(const uint32_t (&r)[32], int col0, int n_valid, uint32_t *w,
-                                          uint64_t (&acc)[2], const ptx::ExpPairConsts &k)
+                                          uint64_t (&acc)[2], const ptx::ExpPairConsts &k, uint64_t shift)
 {
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -184,7 +188,7 @@ __device__ __forceinline__ void exp_slice(const uint32_t (&r)[32], int col0, int
         if ((i & 7) < kPolyOf8)
             ptx::exp_pair_fma(r[i], r[i + 1], k, e0, e1);
         else
-            ptx::exp_pair_mufu(r[i], r[i + 1], k, e0, e1);
+            ptx::exp_pair_mufu(r[i], r[i + 1], k, shift, e0, e1);
         if (MASK) {
             e0 = (col0 + i < n_valid) ? e0 : 0u;
             e1 = (col0 + i + 1 < n_valid) ? e1 : 0u;
@@ -192,6 +196,19 @@ __device__ __forceinline__ void exp_slice(const uint32_t (&r)[32], int col0, int
         acc[(i >> 1) & 1] = ptx::add_pair(acc[(i >> 1) & 1], e0, e1);
         w[i / 2] = ptx::pack_half2(__uint_as_float(e0), __uint_as_float(e1));
     }
+}
+
+// Running maximum of the valid columns of a 32-column slice (MASK: columns at or past n_valid
+// are left out).
+template <bool MASK>
+__device__ __forceinline__ float max_slice(const uint32_t (&r)[32], int col0, int n_valid, float m)
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float v = __uint_as_float(r[i]);
+        m = (!MASK || col0 + i < n_valid) ? fmaxf(m, v) : m;
+    }
+    return m;
 }
 
 template <int D, int STAGES>
@@ -205,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using BI = Bars<STAGES, kPBuffers>;
     static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
-    static_assert((128 * (D + 4) + 128) * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
+    static_assert((128 * (D + 4) + 2 * 128) * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -231,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_begin = static_cast<int>((static_cast<long long>(j) * p.n_tiles) / p.n_split);
     const int t_end = static_cast<int>((static_cast<long long>(j + 1) * p.n_tiles) / p.n_split);
     const int T = t_end - t_begin;
+    // Steps of the K/V ring: with the max-subtracted variant, T steps that stream K alone (the
+    // row-maximum pass), then the T steps of the main pass.
+    const int T1 = p.safe ? T : 0;
+    const int U = T1 + T;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(BI::kQFull), 1);
@@ -296,31 +317,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::kChunks; ++c)  // Q[b, m0:m0+128, 64c:64c+64]
                     ptx::tma_load_3d(sQ + c * C::kChunkRows128, &tmQ, bar(BI::kQFull), c * 64, m0, b);
             }
-            for (int t = 0; ok && t < T; ++t) {
+            for (int t = 0; ok && t < U; ++t) {
                 const int s = t % STAGES;
                 const uint32_t round = static_cast<uint32_t>(t / STAGES);
                 if (t >= STAGES && !wait_bounded(wc, bar(BI::kKvEmpty + s), (round & 1u) ^ 1u, BI::kKvEmpty + s)) {
                     ok = false;
                     break;
                 }
-                const int n0 = (t_begin + t) * kBlockN;
+                const int n0 = (t_begin + (t < T1 ? t : t - T1)) * kBlockN;
                 const uint32_t sK = sStage0 + s * C::kStageBytes;
                 const uint32_t sV = sK + C::kKBytes;
-                // K and V land on separate barriers: S = Q.K need not wait for V.
+                // K and V land on separate barriers: S = Q.K need not wait for V. A step of the
+                // row-maximum pass loads no V; its V barrier phase completes on a plain arrival,
+                // so every step advances every barrier of its stage by one phase.
                 ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), C::kKBytes);
-                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
+                if (t < T1)
+                    ptx::mbar_arrive(bar(BI::kVFull + s));
+                else
+                    ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
                 ++armed[s];
                 // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
                 ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
                 ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
                 // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
+                if (t >= T1) {
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
+                }
             }
             if (ok) {
                 // Tail: the commits that release the last stages must land before the CTA exits.
-                for (int u = T - STAGES > 0 ? T - STAGES : 0; ok && u < T; ++u)
+                for (int u = U - STAGES > 0 ? U - STAGES : 0; ok && u < U; ++u)
                     ok = wait_bounded(wc, bar(BI::kKvEmpty + u % STAGES), static_cast<uint32_t>(u / STAGES) & 1u,
                                       BI::kKvEmpty + u % STAGES);
             }
@@ -356,7 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // u >= 2, the softmax warps have read S_{u-2} out of that buffer (which they do first
         // thing on tile u-2). The P.V products run from another warp, so an S never waits
         // behind a P.V and the softmax warps find every S ready.
-        for (int u = 0; ok && u < T; ++u) {
+        // With the max-subtracted variant the first T1 steps compute S for the row-maximum pass;
+        // their completion also frees the K stage (no P.V reads it).
+        for (int u = 0; ok && u < U; ++u) {
             const int s = u % STAGES;
             const int sb = u & 1;
             if (!warp_wait(bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s) ||
@@ -374,6 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
                                     idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
+                if (u < T1)
+                    ptx::mma_commit(bar(BI::kKvEmpty + s));
             }
             __syncwarp();
         }
@@ -398,10 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O += P_u . V_u once the softmax warps have written P_u and V tile u has landed (K
         // tile u, which S_u needed, shares its stage). The completion releases K/V stage u and
         // P buffer u % kPBuffers.
-        for (int u = 0; ok && u < T; ++u) {
-            const int pb = u % kPBuffers;
+        for (int v = 0; ok && v < T; ++v) {
+            const int u = T1 + v;  // step of the K/V ring
+            const int pb = v % kPBuffers;
             const int s = u % STAGES;
-            if (!warp_wait(bar(BI::kPFull + pb), static_cast<uint32_t>(u / kPBuffers) & 1u, BI::kPFull + pb) ||
+            if (!warp_wait(bar(BI::kPFull + pb), static_cast<uint32_t>(v / kPBuffers) & 1u, BI::kPFull + pb) ||
                 !warp_wait(bar(BI::kVFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kVFull + s)) {
                 ok = false;
                 break;
@@ -412,13 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t v_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes + C::kKBytes, C::kChunkRows128, 1024);
             if (ptx::elect_one()) {
                 // A = P in tensor memory: 16 K-columns per step are 8 tensor-memory columns.
-                ptx::mma_f16_ts(tmem_o, tP, v_desc, idesc_o, u > 0 ? 1u : 0u);
+                ptx::mma_f16_ts(tmem_o, tP, v_desc, idesc_o, v > 0 ? 1u : 0u);
 #pragma unroll
                 for (int k = 1; k < kBlockN / 16; ++k)
                     ptx::mma_f16_ts(tmem_o, tP + k * 8, v_desc + static_cast<uint64_t>(k * (2048 >> 4)), idesc_o, 1u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
-                if (u == T - 1)  // committed by the thread that issued every P.V
+                if (v == T - 1)  // committed by the thread that issued every P.V
                     ptx::mma_commit(bar(BI::kOFull));
             }
             __syncwarp();
@@ -452,13 +485,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc[2] = {0, 0};  // packed fp32 partial row sums (+0.0 bit patterns)
         const ptx::ExpPairConsts ek = ptx::exp_pair_consts();
         bool ok = true;
+        // Max-subtracted variant, first pass: each thread's running maximum of its row over the
+        // valid columns of its group's steps (S only; the buffer is released once read).
+        float m_row = -INFINITY;
+        int u = g;
+        for (; u < T1; u += 2) {
+            if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const int n_valid = p.N - (t_begin + u) * kBlockN;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                if (warp_rows) {
+                    uint32_t r0[32], r1[32];
+                    const uint32_t s_addr = tmem + lane_addr + g * kBlockN + half * 64;
+                    ptx::tmem_ld_32x32b_x32(s_addr, r0);
+                    ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
+                    ptx::tmem_ld_wait(r0);
+                    ptx::tmem_ld_wait(r1);
+                    const int nv = n_valid - half * 64;
+                    if (nv >= 64) {
+                        m_row = max_slice<false>(r0, 0, nv, m_row);
+                        m_row = max_slice<false>(r1, 32, nv, m_row);
+                    } else {
+                        m_row = max_slice<true>(r0, 0, nv, m_row);
+                        m_row = max_slice<true>(r1, 32, nv, m_row);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(bar(BI::kSEmpty + g));
+        }
+        // The two groups' maxima meet in shared memory (both reach both barriers, on the
+        // unwinding path too): m is the row's maximum over the split, and every exponential of
+        // the main pass is exp(s - m) <= 1. The second barrier keeps the exchange slots from
+        // being reused (by the row sums below) before every thread has read them.
+        uint64_t shift = 0;  // +0.0 twice: exp(s) unshifted, as the graph is written
+        float m = 0.f;
+        if (p.safe) {
+            l_xchg[g * kBlockM + row] = m_row;
+            ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
+            m = fmaxf(l_xchg[row], l_xchg[kBlockM + row]);
+            ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
+            const uint32_t nm = __float_as_uint(-m * ptx::kLog2e);
+            shift = ptx::pair_of(nm);
+        }
         // The two groups alternate tiles, each with its own S buffer (g): while one group's warps
         // wait on tensor memory or a barrier, the other group's warps on the same scheduler keep
         // the MUFU unit busy. A thread covers its row's 128 columns of a tile in two 64-column
-        // halves (64 fp32 registers at a time).
-        for (int t = g; t < T; t += 2) {
+        // halves (64 fp32 registers at a time). Step u of the ring is tile t = u - T1.
+        for (u = (T1 % 2 == g) ? T1 : T1 + 1; ok && u < U; u += 2) {
+            const int t = u - T1;
             const int pb = t % kPBuffers;
-            if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(t >> 1) & 1u, BI::kSFull + g)) {
+            if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
                 ok = false;
                 break;
             }
@@ -493,11 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nv = n_valid - half * 64;
                     uint32_t w[32];
                     if (nv >= 64) {
-                        exp_slice<false>(r0, 0, nv, w, acc, ek);
-                        exp_slice<false>(r1, 32, nv, w + 16, acc, ek);
+                        exp_slice<false>(r0, 0, nv, w, acc, ek, shift);
+                        exp_slice<false>(r1, 32, nv, w + 16, acc, ek, shift);
                     } else {
-                        exp_slice<true>(r0, 0, nv, w, acc, ek);
-                        exp_slice<true>(r1, 32, nv, w + 16, acc, ek);
+                        exp_slice<true>(r0, 0, nv, w, acc, ek, shift);
+                        exp_slice<true>(r1, 32, nv, w + 16, acc, ek, shift);
                     }
                     ptx::tmem_st_32x32b_x32(tmem + lane_addr + C::kTmemP + pb * 64 + half * 32, w);
                     ptx::tmem_st_wait();
@@ -571,11 +654,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (p.cluster_reduce) {
-                if (g == 0)
+                if (g == 0) {
                     stage_f[kBlockM * (D + 4) + row] = l;
+                    stage_f[kBlockM * (D + 4) + kBlockM + row] = m;
+                }
             } else {
-                if (p.n_split > 1 && g == 0 && m0 + row < p.M)
-                    p.ws_l[(static_cast<size_t>(j) * p.B + b) * p.M + m0 + row] = l;
+                if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
+                    const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
+                    p.ws_l[r] = l;
+                    if (p.safe)
+                        p.ws_m[r] = m;
+                }
                 ptx::fence_proxy_async_smem();
                 ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
             }
@@ -610,12 +699,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hi = (j + 1) * kBlockM / n;
             const uint32_t st = ptx::smem_u32(smem + C::kQBytes);
             const uint32_t ls = st + kBlockM * (D + 4) * 4;
+            const uint32_t ms = ls + kBlockM * 4;
             for (int it = threadIdx.x - 64; it < (hi - lo) * G; it += kSoftmaxThreads) {
                 const int rr = lo + it / G;
                 const int g = it % G;
                 if (m0 + rr >= p.M)
                     continue;
                 const uint32_t off = static_cast<uint32_t>((rr * (D + 4) + g * 4) * 4);
+                // Max-subtracted variant: rank r's partial was taken relative to its own row
+                // maximum m_r, so it enters the sum with weight exp(m_r - max_r m_r) (1 for the
+                // rank that holds the maximum); otherwise every weight is 1.
+                float wt[kMaxClusterRanks];
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r)
+                    wt[r] = 1.f;
+                if (p.safe) {
+                    float mr[kMaxClusterRanks];
+                    float mmax = -INFINITY;
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r) {
+                        if (r < n) {
+                            mr[r] = ptx::ld_cluster_f32(ptx::map_to_rank(ms + rr * 4, r));
+                            mmax = fmaxf(mmax, mr[r]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r)
+                        if (r < n)
+                            wt[r] = ptx::ex2_approx((mr[r] - mmax) * ptx::kLog2e);
+                }
                 // Every rank's values are requested before the first is used: the remote reads
                 // are then in flight together rather than one round trip after another.
                 float4 v[kMaxClusterRanks];
@@ -632,11 +744,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < kMaxClusterRanks; ++r) {
                     if (r < n) {
-                        a.x += v[r].x;
-                        a.y += v[r].y;
-                        a.z += v[r].z;
-                        a.w += v[r].w;
-                        lsum += lv[r];
+                        a.x += wt[r] * v[r].x;
+                        a.y += wt[r] * v[r].y;
+                        a.z += wt[r] * v[r].z;
+                        a.w += wt[r] * v[r].w;
+                        lsum += wt[r] * lv[r];
                     }
                 }
                 uint2 w;
@@ -673,8 +785,8 @@ struct CombineCfg {
 
 template <int D>
 __global__ void __launch_bounds__(256)
-    mg_attn_combine(const float *__restrict__ ws_o, const float *__restrict__ ws_l, __half *__restrict__ O,
-                    int rows, int n_split)
+    mg_attn_combine(const float *__restrict__ ws_o, const float *__restrict__ ws_l, const float *__restrict__ ws_m,
+                    __half *__restrict__ O, int rows, int n_split)
 {
     using CC = CombineCfg<D>;
     __shared__ float4 part_o[CC::kParts][CC::kRows][CC::kGroups];
@@ -690,17 +802,27 @@ __global__ void __launch_bounds__(256)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
     if (r < rows) {
+        // Max-subtracted variant (ws_m given): split j's partial is relative to its row maximum
+        // m_j and enters with weight exp(m_j - max_j m_j); otherwise every weight is 1.
+        float mmax = 0.f;
+        if (ws_m) {
+            mmax = -INFINITY;
+            for (int j = 0; j < n_split; ++j)
+                mmax = fmaxf(mmax, ws_m[static_cast<size_t>(j) * rows + r]);
+        }
         const float4 *src = reinterpret_cast<const float4 *>(ws_o) + static_cast<size_t>(r) * CC::kGroups + g;
         const size_t split_stride = static_cast<size_t>(rows) * CC::kGroups;
 #pragma unroll 4
         for (int j = part; j < n_split; j += CC::kParts) {
             const float4 a = src[static_cast<size_t>(j) * split_stride];
-            acc.x += a.x;
-            acc.y += a.y;
-            acc.z += a.z;
-            acc.w += a.w;
+            const float wt = ws_m ? ptx::ex2_approx((ws_m[static_cast<size_t>(j) * rows + r] - mmax) * ptx::kLog2e)
+                                  : 1.f;
+            acc.x += wt * a.x;
+            acc.y += wt * a.y;
+            acc.z += wt * a.z;
+            acc.w += wt * a.w;
             if (g == 0)
-                l += ws_l[static_cast<size_t>(j) * rows + r];
+                l += wt * ws_l[static_cast<size_t>(j) * rows + r];
         }
     }
     part_o[part][rl][g] = acc;

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
             if (POLY)
                 mg::ptx::exp_pair_fma(x[2 * p], x[2 * p + 1], k, x[2 * p], x[2 * p + 1]);
             else
-                mg::ptx::exp_pair_mufu(x[2 * p], x[2 * p + 1], k, x[2 * p], x[2 * p + 1]);
+                mg::ptx::exp_pair_mufu(x[2 * p], x[2 * p + 1], k, 0ull, x[2 * p], x[2 * p + 1]);
         }
     }
     __syncthreads();

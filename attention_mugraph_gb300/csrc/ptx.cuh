@@ -454,20 +454,22 @@ __device__ __forceinline__ void exp_pair_fma(uint32_t s0, uint32_t s1, const Exp
           "l"(k.c3), "l"(k.c2), "l"(k.c1), "l"(k.c0));
 }
 
-// (exp(s0), exp(s1)) on the MUFU unit: one packed multiply by log2(e), then ex2.approx each.
-__device__ __forceinline__ void exp_pair_mufu(uint32_t s0, uint32_t s1, const ExpPairConsts &k, uint32_t &e0,
-                                              uint32_t &e1)
+// (exp(s0 - m), exp(s1 - m)) on the MUFU unit: one packed fused multiply-add s*log2(e) + shift
+// with shift = -m*log2(e) in both halves (+0 gives exp(s) exactly as a plain multiply would),
+// then ex2.approx each.
+__device__ __forceinline__ void exp_pair_mufu(uint32_t s0, uint32_t s1, const ExpPairConsts &k, uint64_t shift,
+                                              uint32_t &e0, uint32_t &e1)
 {
     asm("{\n\t.reg .b64 a, x;\n\t.reg .f32 x0, x1;\n\t"
         "mov.b64 a, {%2, %3};\n\t"
-        "mul.rn.f32x2 x, a, %4;\n\t"
+        "fma.rn.f32x2 x, a, %4, %5;\n\t"
         "mov.b64 {x0, x1}, x;\n\t"
         "ex2.approx.ftz.f32 x0, x0;\n\t"
         "ex2.approx.ftz.f32 x1, x1;\n\t"
         "mov.b32 %0, x0;\n\t"
         "mov.b32 %1, x1;\n\t}"
         : "=r"(e0), "=r"(e1)
-        : "r"(s0), "r"(s1), "l"(k.log2e));
+        : "r"(s0), "r"(s1), "l"(k.log2e), "l"(shift));
 }
 
 // acc + (e0, e1) on an f32x2 pair.

@@ -289,7 +289,7 @@ def workload_config(B, M, N, d, a, extra=None):
 
 # ------------------------------------------------------------------ GPU arm
 
-def measure_workload(name, steps, peaks, stream, exp_rate_ns):
+def measure_workload(name, steps, peaks, stream, exp_rate_ns, flags=0):
     """Graph-replayed µs/call over rotating buffer sets (> 2x L2) and the fused kernel's own time for
     one named workload; returns a dict for the JSON line's per_config field."""
     import torch
@@ -306,7 +306,7 @@ def measure_workload(name, steps, peaks, stream, exp_rate_ns):
     n_sets = max(2, math.ceil(2 * l2 / by))
     dev = [(q.cuda(), k.cuda(), v.cuda(), torch.empty((B, M, d), dtype=torch.float16, device="cuda"))
            for _ in range(n_sets)]
-    plan = mg.Plan(B, M, N, d)
+    plan = mg.Plan(B, M, N, d, flags=flags)
     ptrs = [tuple(t.data_ptr() for t in s) for s in dev]
     sh = stream.cuda_stream
     with torch.cuda.stream(stream):
@@ -585,6 +585,10 @@ def main():
 
             line["per_config"] = {name: measure_workload(name, args.per_config_steps, peaks, stream, exp_ns)
                                   for name in _inputs.CONFIG_ORDER}
+            # The max-subtracted variant (MG_FLAG_SAFE_SOFTMAX) on the same workloads.
+            line["per_config_safe_softmax"] = {
+                name: measure_workload(name, args.per_config_steps, peaks, stream, exp_ns, flags=mg.MG_FLAG_SAFE_SOFTMAX)
+                for name in _inputs.CONFIG_ORDER}
         line["cpu_baseline"] = cpu_baseline(q, k, v, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     plan.destroy()

@@ -27,7 +27,9 @@
  * fp32; exp(A) is rounded to fp16 only as the operand of the second product; the final
  * divide is one IEEE fp32 division per element, then round-to-nearest-even to fp16.
  * Precondition: exp(A) must fit fp16, i.e. A <= ln(65504) ~ 11.09. Larger scores make the
- * fp16 graph itself overflow; the result is then inf/NaN and no error is reported.
+ * fp16 graph itself overflow; the result is then inf/NaN and no error is reported. The opt-in
+ * MG_FLAG_SAFE_SOFTMAX lifts it: each row's maximum score is subtracted before exp, which the
+ * normalisation cancels, so the result is the same function with every fp16 weight <= 1.
  *
  * Status codes: the first four mirror the error enum of Mirage's CUDA transpiler
  * (blog, section 5.1: success, insufficient shared memory, layout error, config error).
@@ -66,6 +68,12 @@ typedef enum {
 /* Flags for mg_attn_options.flags. */
 #define MG_FLAG_NO_PDL 0x1         /* launch without programmatic dependent launch */
 #define MG_FLAG_NO_CLUSTER 0x4     /* always combine split partials with the second kernel, never on chip */
+#define MG_FLAG_SAFE_SOFTMAX 0x8   /* max-subtracted evaluation: a first pass over K finds each row's
+                                      largest score m (per split), then P = exp(A - m) and the split
+                                      partials combine with weights exp(m_j - max_j m_j). The result is
+                                      the graph's (the normalisation cancels any per-row shift) without
+                                      the A <= ln(65504) precondition; the cost is Q.K computed twice and
+                                      K read twice. */
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and
                                       the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */

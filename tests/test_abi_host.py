@@ -115,6 +115,24 @@ def test_query_cluster_choices():
     assert nc["cluster_ctas"] == 0 and nc["n_split"] == 32 and nc["kernels_per_run"] == 2
 
 
+def test_query_safe_softmax_workspace():
+    # The max-subtracted variant adds one fp32 row maximum per split and row to the partials of
+    # the second kernel; the on-chip combine and single-split plans need no extra memory.
+    B, M, N, d = 2, 256, 65536, 64
+    plain = mg.mg_attn_query(B, M, N, d, 152)
+    safe = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX)
+    n = safe["n_split"]
+    assert n == plain["n_split"] and safe["kernels_per_run"] == 2
+    assert safe["workspace_bytes"] == 256 + n * B * M * (d + 2) * 4
+    assert safe["workspace_bytes"] - plain["workspace_bytes"] == n * B * M * 4
+    for shape in [(2, 256, 4096, 64), (16, 8, 32768, 128)]:
+        for kw in [{}, {"n_split": 1}]:
+            a = mg.mg_attn_query(*shape, 152, **kw)
+            b = mg.mg_attn_query(*shape, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX, **kw)
+            if a["kernels_per_run"] == 1:
+                assert b["workspace_bytes"] == a["workspace_bytes"] == 256
+
+
 def test_query_options():
     info = mg.mg_attn_query(2, 256, 4096, 64, 152, n_split=5, stages=2)
     assert info["n_split"] == 5 and info["stages"] == 2
@@ -130,6 +148,7 @@ def test_query_options():
     ((2, 256, 4096, 64), {"n_split": 33}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x80}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x10}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),
