@@ -63,6 +63,9 @@ def _bind(path: str):
                                              ctypes.POINTER(ctypes.c_int64), i64,
                                              ctypes.c_int, f64p]
     lib.mg_oracle_attention_rows.restype = ctypes.c_int
+    lib.mg_oracle_attention_qknorm_rows.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, ctypes.c_double,
+                                                    ctypes.POINTER(ctypes.c_int64), i64, ctypes.c_int, f64p]
+    lib.mg_oracle_attention_qknorm_rows.restype = ctypes.c_int
     lib.mg_oracle_max_threads.argtypes = []
     lib.mg_oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -135,3 +138,27 @@ def attention_rows(Q, K, V, rows, threads: int = 0, lib=None) -> np.ndarray:
     if rc != 0:
         raise RuntimeError(f"mg_oracle_attention_rows failed with code {rc}")
     return out
+
+
+QKNORM_EPS = 1e-6  # the library's fixed epsilon of rms_norm (MG_QKNORM_EPS in include/mg_attn.h)
+
+
+def attention_qknorm(Q, K, V, eps: float = QKNORM_EPS, rows=None, threads: int = 0, lib=None) -> np.ndarray:
+    """QK-norm attention: Q and K each rms-normalised over d (x / sqrt(mean(x^2) + eps)), then the
+    graph (documentation, tutorials/attention-with-kv-norm). Returns (B, M, d) float64, or
+    (len(rows), d) for the listed flat rows b*M + m."""
+    q, k, v = _as_half_bits(Q), _as_half_bits(K), _as_half_bits(V)
+    B, M, d = q.shape
+    N = k.shape[2]
+    if k.shape != (B, d, N) or v.shape != (B, N, d):
+        raise ValueError(f"shape mismatch: Q{q.shape} K{k.shape} V{v.shape}")
+    r = np.arange(B * M, dtype=np.int64) if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.empty((len(r), d), dtype=np.float64)
+    lib = lib or load_library()
+    rc = lib.mg_oracle_attention_qknorm_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                             _ptr(v, ctypes.c_uint16), B, M, N, d, float(eps),
+                                             _ptr(r, ctypes.c_int64), len(r), int(threads),
+                                             _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise RuntimeError(f"mg_oracle_attention_qknorm_rows failed with code {rc}")
+    return out.reshape(B, M, d) if rows is None else out

@@ -179,6 +179,112 @@ int mg_oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
     return rc;
 }
 
+/* ------------------------------------------------------------------------
+ * QK-norm attention (Mirage documentation, tutorials/attention-with-kv-norm,
+ * "Implement QK Normalization and Optimize Attention Kernel in Python"):
+ *
+ *     Q = rms_norm(Q); K = rms_norm(K); then the graph above.
+ *
+ * rms_norm takes no weight in that graph. Reading: it normalises each query
+ * row and each key vector over the head dimension d (for K, stored (B,d,N),
+ * that is over axis 1), x / sqrt(mean(x^2) + eps), computed here in double
+ * from the widened fp16 inputs and used unrounded.
+ * ------------------------------------------------------------------------ */
+
+/* One output row of QK-norm attention. A, E: scratch of N doubles; kn: scratch
+ * of d*N doubles for the normalised key vectors of batch b. */
+static void oracle_row_qknorm(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                              int64_t M, int64_t N, int64_t d, double eps, int64_t b,
+                              int64_t m, double *A, double *E, double *qn, double *kn,
+                              double *out)
+{
+    const uint16_t *q = Q + (b * M + m) * d;
+    const uint16_t *Kb = K + b * d * N;
+    const uint16_t *Vb = V + b * N * d;
+
+    /* Q = rms_norm(Q): this row over d */
+    double ss = 0.0;
+    for (int64_t k = 0; k < d; ++k)
+        ss += H(q[k]) * H(q[k]);
+    const double rq = 1.0 / sqrt(ss / (double)d + eps);
+    for (int64_t k = 0; k < d; ++k)
+        qn[k] = H(q[k]) * rq;
+
+    /* K = rms_norm(K): every key vector K[b][:][n] over d */
+    for (int64_t n = 0; n < N; ++n) {
+        double sk = 0.0;
+        for (int64_t k = 0; k < d; ++k)
+            sk += H(Kb[k * N + n]) * H(Kb[k * N + n]);
+        const double rk = 1.0 / sqrt(sk / (double)d + eps);
+        for (int64_t k = 0; k < d; ++k)
+            kn[k * N + n] = H(Kb[k * N + n]) * rk;
+    }
+
+    /* A = matmul(Q, K) */
+    for (int64_t n = 0; n < N; ++n)
+        A[n] = 0.0;
+    for (int64_t k = 0; k < d; ++k)
+        for (int64_t n = 0; n < N; ++n)
+            A[n] += qn[k] * kn[k * N + n];
+
+    /* E = exp(A); S = reduction(E, 2); D = div(E, S); O = matmul(D, V) */
+    for (int64_t n = 0; n < N; ++n)
+        E[n] = exp(A[n]);
+    double S = 0.0;
+    for (int64_t n = 0; n < N; ++n)
+        S += E[n];
+    for (int64_t n = 0; n < N; ++n)
+        E[n] = E[n] / S;
+    for (int64_t c = 0; c < d; ++c)
+        out[c] = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+        const double w = E[n];
+        const uint16_t *vrow = Vb + n * d;
+        for (int64_t c = 0; c < d; ++c)
+            out[c] += w * H(vrow[c]);
+    }
+}
+
+/* QK-norm attention for the listed rows (as mg_oracle_attention_rows); eps >= 0. */
+int mg_oracle_attention_qknorm_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                    int64_t B, int64_t M, int64_t N, int64_t d, double eps,
+                                    const int64_t *rows, int64_t nrows, int nthreads, double *O)
+{
+    if (!Q || !K || !V || !O || !rows || nrows < 0 || bad_shape(B, M, N, d) || !(eps >= 0.0))
+        return -1;
+    for (int64_t i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= B * M)
+            return -1;
+    pthread_once(&g_half_once, build_half_table);
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#else
+    nthreads = 1;
+#endif
+    int failed = 0;
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+    {
+        double *A = (double *)malloc((size_t)N * sizeof(double));
+        double *E = (double *)malloc((size_t)N * sizeof(double));
+        double *qn = (double *)malloc((size_t)d * sizeof(double));
+        double *kn = (double *)malloc((size_t)d * (size_t)N * sizeof(double));
+        if (!A || !E || !qn || !kn) {
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t i = 0; i < nrows; ++i)
+                oracle_row_qknorm(Q, K, V, M, N, d, eps, rows[i] / M, rows[i] % M, A, E, qn, kn,
+                                  O + i * d);
+        }
+        free(A);
+        free(E);
+        free(qn);
+        free(kn);
+    }
+    return failed ? -2 : 0;
+}
+
 /* Threads OpenMP would use by default (1 when built without OpenMP). */
 int mg_oracle_max_threads(void)
 {

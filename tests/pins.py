@@ -210,3 +210,97 @@ def pin_v_linearity(fn):
 PINS = [pin_k_zero, pin_q_zero, pin_v_constant, pin_single_key, pin_one_hot,
         pin_golden_worked_examples, pin_brute_force, pin_torch_softmax, pin_joint_permutation,
         pin_convex_hull, pin_batch_independence, pin_score_shift, pin_v_linearity]
+
+
+# ================================================================ QK-norm attention
+# Pins for ``fn(Q, K, V, eps) -> O`` of the QK-norm graph (Mirage documentation,
+# tutorials/attention-with-kv-norm): Q = rms_norm(Q), K = rms_norm(K), then the graph above,
+# rms_norm over the head dimension d: x / sqrt(mean(x^2) + eps).
+
+def qk_brute_force(q, k, v, eps):
+    """Pure-Python evaluation, one element at a time, exactly rounded sums."""
+    Q = q.double().tolist()
+    K = k.double().tolist()
+    V = v.double().tolist()
+    B, M, d = len(Q), len(Q[0]), len(Q[0][0])
+    N = len(K[0][0])
+    out = np.zeros((B, M, d))
+    for b in range(B):
+        kn = [[0.0] * N for _ in range(d)]
+        for n in range(N):
+            r = 1.0 / math.sqrt(math.fsum(K[b][kk][n] ** 2 for kk in range(d)) / d + eps)
+            for kk in range(d):
+                kn[kk][n] = K[b][kk][n] * r
+        for m in range(M):
+            rq = 1.0 / math.sqrt(math.fsum(x * x for x in Q[b][m]) / d + eps)
+            qn = [x * rq for x in Q[b][m]]
+            w = [math.exp(math.fsum(qn[kk] * kn[kk][n] for kk in range(d))) for n in range(N)]
+            tot = math.fsum(w)
+            for c in range(d):
+                out[b, m, c] = math.fsum(w[n] * V[b][n][c] for n in range(N)) / tot
+    return out
+
+
+def qk_pin_brute_force(fn):
+    for i, (B, M, N, d) in enumerate([(1, 2, 5, 3), (2, 3, 7, 4), (1, 5, 16, 8)]):
+        q, k, v = _rand_inputs(B, M, N, d, a=1.0, seed=80 + i)
+        _close(fn(q, k, v, 1e-6), qk_brute_force(q, k, v, 1e-6), 1e-12, 1e-14, f"qk brute {B,M,N,d}")
+
+
+def qk_pin_torch_rms_norm(fn):
+    """torch.nn.functional.rms_norm over d (K transposed to put d last), then softmax in float64."""
+    F = torch.nn.functional
+    for i, (B, M, N, d) in enumerate([(2, 16, 64, 64), (1, 9, 130, 128)]):
+        q, k, v = _rand_inputs(B, M, N, d, seed=90 + i)
+        qn = F.rms_norm(q.double(), (d,), eps=1e-6)
+        kn = F.rms_norm(k.double().transpose(1, 2), (d,), eps=1e-6).transpose(1, 2)
+        want = (torch.softmax(qn @ kn, dim=-1) @ v.double()).numpy()
+        _close(fn(q, k, v, 1e-6), want, 1e-11, 1e-13, f"qk torch {B,M,N,d}")
+
+
+def qk_pin_key_scale(fn):
+    """With eps = 0 a key vector's scale cancels in its normalisation: multiplying K[b,:,n*] by 4
+    (exact in fp16) leaves O unchanged. Normalising K over N instead of d would not."""
+    B, M, N, d = 2, 5, 13, 6
+    q, k, v = _rand_inputs(B, M, N, d, seed=95)
+    k2 = k.clone()
+    k2[:, :, 7] = (k[:, :, 7].float() * 4).half()
+    _close(fn(q, k2, v, 0.0), fn(q, k, v, 0.0), 1e-12, 1e-14, "key scale")
+
+
+def qk_pin_query_scale(fn):
+    """With eps = 0 scaling one query row by 8 leaves every output unchanged."""
+    B, M, N, d = 2, 6, 11, 5
+    q, k, v = _rand_inputs(B, M, N, d, seed=96)
+    q2 = q.clone()
+    q2[1, 3, :] = (q[1, 3, :].float() * 8).half()
+    _close(fn(q2, k, v, 0.0), fn(q, k, v, 0.0), 1e-12, 1e-14, "query scale")
+
+
+def qk_pin_d1_sign(fn):
+    """d = 1 and eps = 0: rms_norm(x) = sign(x), so A = sign(q) sign(k_n) = +-1 and
+    O = (e^{+-1} weighted mean of V) in closed form."""
+    q = torch.tensor([[[0.75], [-2.0]]], dtype=torch.float16)
+    k = torch.tensor([[[0.5, -0.25, 3.0, -1.0]]], dtype=torch.float16)
+    g = torch.Generator("cpu").manual_seed(97)
+    v = torch.randn((1, 4, 1), generator=g).half()
+    vv = [float(x) for x in v.double().flatten()]
+    sk = [1.0, -1.0, 1.0, -1.0]
+    want = []
+    for sq in (1.0, -1.0):
+        w = [math.exp(sq * s) for s in sk]
+        want.append(math.fsum(wi * x for wi, x in zip(w, vv)) / math.fsum(w))
+    _close(fn(q, k, v, 0.0), np.array(want).reshape(1, 2, 1), 1e-13, 1e-15, "d=1 sign")
+
+
+def qk_pin_zero_query_row(fn):
+    """A zero query row with eps > 0 normalises to zero: every score 0, O = mean of V."""
+    B, M, N, d = 1, 3, 9, 4
+    q, k, v = _rand_inputs(B, M, N, d, seed=98)
+    q[0, 1, :] = 0.0
+    o = np.asarray(fn(q, k, v, 1e-6))
+    _close(o[0, 1], v.double().numpy()[0].mean(axis=0), 1e-13, 1e-15, "zero query row")
+
+
+QK_PINS = [qk_pin_brute_force, qk_pin_torch_rms_norm, qk_pin_key_scale, qk_pin_query_scale,
+           qk_pin_d1_sign, qk_pin_zero_query_row]

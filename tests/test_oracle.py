@@ -78,3 +78,15 @@ def test_input_recipe_is_seeded_and_shaped():
     assert q.shape == (2, 3, 8) and k.shape == (2, 8, 16) and v.shape == (2, 16, 8)
     assert q.dtype == k.dtype == v.dtype == torch.float16
     assert float(q.abs().max()) <= 0.5 and float(k.abs().max()) <= 0.5
+
+
+@pytest.mark.parametrize("pin", pins.QK_PINS, ids=lambda p: p.__name__)
+def test_qknorm_oracle_pin(pin):
+    pin(lambda q, k, v, eps: oracle.attention_qknorm(q, k, v, eps=eps, threads=2))
+
+
+def test_qknorm_rows_match_full():
+    q, k, v = pins._rand_inputs(2, 7, 40, 16, seed=8)
+    full = oracle.attention_qknorm(q, k, v)
+    rows = [0, 6, 9, 13]
+    assert np.array_equal(oracle.attention_qknorm(q, k, v, rows=rows), full.reshape(-1, 16)[rows])

@@ -11,6 +11,15 @@ from tests import pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "mg_oracle.c")
 
+
+def mutate(text, start, end, old, new):
+    """Replace `old` (unique between the markers `start` and `end`) inside that span only."""
+    i = text.index(start)
+    j = text.index(end, i)
+    span = text[i:j]
+    assert span.count(old) == 1, f"mutation anchor not unique in its function: {old!r}"
+    return text[:i] + span.replace(old, new) + text[j:]
+
 # (name, text in the source, replacement). Every replacement keeps indices in bounds.
 MUTANTS = [
     ("exp of the negated score", "E[n] = exp(A[n]);", "E[n] = exp(-A[n]);"),
@@ -29,10 +38,9 @@ MUTANTS = [
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_pins_catch_planted_mistake(tmp_path, name, old, new):
-    text = open(SRC).read()
-    assert text.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    text = mutate(open(SRC).read(), "static void oracle_row(", "static int bad_shape(", old, new)
     mutant_src = tmp_path / "mutant.c"
-    mutant_src.write_text(text.replace(old, new))
+    mutant_src.write_text(text)
     lib_path = oracle.compile_library(str(mutant_src), str(tmp_path / "libmutant.so"))
     lib = oracle.load_library(lib_path)
 
@@ -44,5 +52,37 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
         try:
             pin(fn)
         except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake: {name}"
+
+
+QK_MUTANTS = [
+    ("key vectors normalised over N instead of d",
+     "sk += H(Kb[k * N + n]) * H(Kb[k * N + n]);", "sk += H(Kb[n % d * N + (k * 7 + n) % N]) * H(Kb[n % d * N + (k * 7 + n) % N]);"),
+    ("query not normalised", "qn[k] = H(q[k]) * rq;", "qn[k] = H(q[k]);"),
+    ("key not normalised", "kn[k * N + n] = H(Kb[k * N + n]) * rk;", "kn[k * N + n] = H(Kb[k * N + n]);"),
+    ("sum instead of mean of squares", "const double rq = 1.0 / sqrt(ss / (double)d + eps);",
+     "const double rq = 1.0 / sqrt(ss + eps);"),
+    ("eps dropped", "const double rk = 1.0 / sqrt(sk / (double)d + eps);", "const double rk = 1.0 / sqrt(sk / (double)d);"),
+    ("multiplied by the rms instead of divided", "const double rk = 1.0 / sqrt(sk / (double)d + eps);",
+     "const double rk = sqrt(sk / (double)d + eps);"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", QK_MUTANTS, ids=[m[0] for m in QK_MUTANTS])
+def test_qknorm_pins_catch_planted_mistake(tmp_path, name, old, new):
+    text = mutate(open(SRC).read(), "static void oracle_row_qknorm(", "int mg_oracle_attention_qknorm_rows(", old, new)
+    mutant_src = tmp_path / "mutant.c"
+    mutant_src.write_text(text)
+    lib = oracle.load_library(oracle.compile_library(str(mutant_src), str(tmp_path / "libmutant.so")))
+
+    def fn(q, k, v, eps):
+        return oracle.attention_qknorm(q, k, v, eps=eps, threads=1, lib=lib)
+
+    caught = []
+    for pin in pins.QK_PINS:
+        try:
+            pin(fn)
+        except (AssertionError, FloatingPointError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake: {name}"
