@@ -28,6 +28,8 @@ MG_FLAG_NO_PDL = 0x1
 MG_FLAG_INJECT_TIMEOUT = 0x2
 MG_FLAG_NO_CLUSTER = 0x4
 MG_FLAG_SAFE_SOFTMAX = 0x8
+MG_FLAG_QK_NORM = 0x10
+MG_QKNORM_EPS = 1e-6
 
 # Every function include/mg_attn.h declares.
 EXPORTS = ("mg_attn_plan", "mg_attn_plan_ex", "mg_attn_run", "mg_attn_run_host", "mg_attn_destroy",

@@ -63,31 +63,47 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-int auto_stages(int64_t d) { return d == 64 ? 6 : 3; }
+// The deepest K/V ring that fits (the QK-norm variant's 2 KB of key-vector scales leave d = 128
+// two stages).
+int auto_stages(int64_t d, bool qk_norm) { return d == 64 ? 6 : (qk_norm ? 2 : 3); }
 
 using FwdKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                            const CUtensorMap, const mg::FwdParams);
 
-FwdKernel fwd_kernel(int64_t d, int stages)
+template <int VAR>
+FwdKernel fwd_kernel_variant(int64_t d, int stages)
 {
     if (d == 64) {
         switch (stages) {
-        case 2: return mg::mg_attn_fwd_partial<64, 2>;
-        case 3: return mg::mg_attn_fwd_partial<64, 3>;
-        case 4: return mg::mg_attn_fwd_partial<64, 4>;
-        case 5: return mg::mg_attn_fwd_partial<64, 5>;
-        case 6: return mg::mg_attn_fwd_partial<64, 6>;
+        case 2: return mg::mg_attn_fwd_partial<64, 2, VAR>;
+        case 3: return mg::mg_attn_fwd_partial<64, 3, VAR>;
+        case 4: return mg::mg_attn_fwd_partial<64, 4, VAR>;
+        case 5: return mg::mg_attn_fwd_partial<64, 5, VAR>;
+        case 6: return mg::mg_attn_fwd_partial<64, 6, VAR>;
         default: return nullptr;
         }
     }
     if (d == 128) {
         switch (stages) {
-        case 2: return mg::mg_attn_fwd_partial<128, 2>;
-        case 3: return mg::mg_attn_fwd_partial<128, 3>;
+        case 2: return mg::mg_attn_fwd_partial<128, 2, VAR>;
+        case 3:  // the QK-norm variant's scales leave no room for a third 64 KB stage
+            if constexpr (VAR != mg::kQkNorm)
+                return mg::mg_attn_fwd_partial<128, 3, VAR>;
+            return nullptr;
         default: return nullptr;
         }
     }
     return nullptr;
+}
+
+// The fused kernel for a head dim, pipeline depth and the MG_FLAG_* evaluation flags.
+FwdKernel fwd_kernel(int64_t d, int stages, int flags)
+{
+    if (flags & MG_FLAG_QK_NORM)
+        return fwd_kernel_variant<mg::kQkNorm>(d, stages);
+    if (flags & MG_FLAG_SAFE_SOFTMAX)
+        return fwd_kernel_variant<mg::kSafe>(d, stages);
+    return fwd_kernel_variant<mg::kPlain>(d, stages);
 }
 
 using CombineKernel = void (*)(const float *, const float *, const float *, __half *, int, int);
@@ -119,7 +135,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     if (opts)
         o = *opts;
     if (o.reserved != 0 ||
-        (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX)) != 0)
+        (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX |
+                     MG_FLAG_QK_NORM)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -149,11 +166,12 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     if (m_tiles * n_split > 0x7fffffffLL)
         return fail(MG_ERR_INVALID_ARG, "grid too large");
 
-    int stages = o.stages == 0 ? auto_stages(d) : o.stages;
+    const bool qk_norm = (o.flags & MG_FLAG_QK_NORM) != 0;
+    int stages = o.stages == 0 ? auto_stages(d, qk_norm) : o.stages;
     if (stages < 2 || stages > 6)
         return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 6]", stages);
-    const uint32_t smem = mg::fwd_smem_bytes(static_cast<int>(d), stages);
-    if (!fwd_kernel(d, stages) || static_cast<int64_t>(smem) > max_smem)
+    const uint32_t smem = mg::fwd_smem_bytes(static_cast<int>(d), stages, qk_norm);
+    if (static_cast<int64_t>(smem) > max_smem || !fwd_kernel(d, stages, o.flags))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
 
@@ -175,7 +193,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
     // Split partials for the second kernel: numerators, row sums and (max-subtracted variant) row maxima.
-    const int64_t row_words = (o.flags & MG_FLAG_SAFE_SOFTMAX) ? 2 : 1;
+    const int64_t row_words = (o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) ? 2 : 1;
     const int64_t partial_bytes =
         (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M * row_words) * 4 : 0;
     info->workspace_bytes = 256 + partial_bytes;
@@ -339,7 +357,7 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     if (st != MG_OK)
         return st;
 
-    FwdKernel fwd = fwd_kernel(d, info.stages);
+    FwdKernel fwd = fwd_kernel(d, info.stages, flags);
     e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              info.smem_bytes);
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
@@ -376,7 +394,7 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     if (info.n_split > 1 && info.cluster_ctas == 0) {
         p->ws_o = reinterpret_cast<float *>(ws + 256);
         p->ws_l = p->ws_o + static_cast<size_t>(info.n_split) * B * M * d;
-        if (flags & MG_FLAG_SAFE_SOFTMAX)
+        if (flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM))
             p->ws_m = p->ws_l + static_cast<size_t>(info.n_split) * B * M;
         // ws_o as (n_split*B, M, d) fp32, stored in {32, 128} boxes.
         st = encode_3d(&p->maps[4], p->ws_o, d, M, static_cast<uint64_t>(info.n_split) * B, 32u, 128u, 4);
@@ -456,7 +474,6 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.O = static_cast<__half *>(O);
     prm.ws_l = plan->ws_l;
     prm.ws_m = plan->ws_m;
-    prm.safe = (plan->flags & MG_FLAG_SAFE_SOFTMAX) ? 1 : 0;
     prm.status = plan->status;
     prm.timeout_ns = plan->timeout_ns;
     prm.inject_timeout = (plan->flags & MG_FLAG_INJECT_TIMEOUT) ? 1 : 0;
@@ -615,7 +632,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     if (st != MG_OK)
         return st;
     if (in.cluster_ctas > 0 &&
-        !cluster_schedulable(fwd_kernel(d, in.stages), in.cluster_ctas, in.grid_ctas, in.smem_bytes)) {
+        !cluster_schedulable(fwd_kernel(d, in.stages, 0), in.cluster_ctas, in.grid_ctas, in.smem_bytes)) {
         mg_attn_options o{};
         o.flags = MG_FLAG_NO_CLUSTER;
         if ((st = decide(B, M, N, d, &o, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags)) != MG_OK)
@@ -626,7 +643,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
                     "shape needs %lld bytes of split scratch; the static scratch holds %u bytes "
                     "(use mg_attn_plan / mg_attn_run)",
                     (long long)in.workspace_bytes, MG_ATTN_STATIC_SCRATCH_BYTES);
-    FwdKernel fwd = fwd_kernel(d, in.stages);
+    FwdKernel fwd = fwd_kernel(d, in.stages, 0);
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, in.smem_bytes);
     if (e != cudaSuccess)
@@ -658,7 +675,6 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.status = reinterpret_cast<int *>(sd->scratch);
     prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
     prm.ws_m = nullptr;
-    prm.safe = 0;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
 

@@ -66,6 +66,8 @@ constexpr uint32_t kTmemO = 256;   // tensor-memory column of O; P buffers follo
 constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
 constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warps
 constexpr int kMaxClusterRanks = 16;     // largest cluster of the on-chip combine
+constexpr float kQkNormEps = 1e-6f;      // rms_norm epsilon of the QK-norm variant
+constexpr int kColScaleSlots = 4;        // QK-norm: key-vector scales of the last 4 ring steps
 
 template <int D>
 struct TileCfg {
@@ -84,12 +86,12 @@ struct TileCfg {
 };
 
 // Shared-memory bytes of kernel 1 for a head dim and pipeline depth: alignment slack, Q, the
-// K/V ring (its first stage is reused as the output staging area), the row-sum exchange and
-// the barriers.
-__host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages)
+// K/V ring (its first stage is reused as the output staging area), the row-sum exchange of the
+// two softmax groups, the barriers and (QK-norm variant) the key-vector scales.
+__host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages, bool qk_norm = false)
 {
     return 1024u + static_cast<uint32_t>(128 * d * 2) + static_cast<uint32_t>(stages) * (2u * d * 128 * 2) +
-           2u * 128 * 4 + 512u;
+           2u * 128 * 4 + 512u + (qk_norm ? static_cast<uint32_t>(kColScaleSlots) * 128 * 4 : 0u);
 }
 
 struct FwdParams {
@@ -101,7 +103,6 @@ struct FwdParams {
     __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
     float *ws_l;             // (n_split, B, M) partial row sums
     float *ws_m;             // (n_split, B, M) partial row maxima (max-subtracted variant only)
-    int safe;                // max-subtracted variant: a first pass finds each row's maximum score
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
     int inject_timeout;
@@ -211,16 +212,76 @@ __device__ __forceinline__ float max_slice(const uint32_t (&r)[32], int col0, in
     return m;
 }
 
-template <int D, int STAGES>
+// QK-norm variant: as exp_slice and max_slice for the scores s * c_col * a, where `cs` holds the
+// slice's 32 key-vector scales c (shared memory, the same for every row) and `arow` is
+// a*log2(e) twice (this row's query scale; for the maximum the caller applies a afterwards).
+template <bool MASK>
+__device__ __forceinline__ void exp_slice_scaled(const uint32_t (&r)[32], int col0, int n_valid, uint32_t *w,
+                                                 uint64_t (&acc)[2], const float *cs, uint64_t arow, uint64_t shift)
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const float2 c = *reinterpret_cast<const float2 *>(cs + i);
+        uint32_t e0, e1;
+        ptx::exp_pair_mufu_scaled(r[i], r[i + 1], c.x, c.y, arow, shift, e0, e1);
+        if (MASK) {
+            e0 = (col0 + i < n_valid) ? e0 : 0u;
+            e1 = (col0 + i + 1 < n_valid) ? e1 : 0u;
+        }
+        acc[(i >> 1) & 1] = ptx::add_pair(acc[(i >> 1) & 1], e0, e1);
+        w[i / 2] = ptx::pack_half2(__uint_as_float(e0), __uint_as_float(e1));
+    }
+}
+
+template <bool MASK>
+__device__ __forceinline__ float max_slice_scaled(const uint32_t (&r)[32], int col0, int n_valid, float m,
+                                                  const float *cs)
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 c = *reinterpret_cast<const float4 *>(cs + i);
+        const float cc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float v = __uint_as_float(r[i + q]) * cc[q];
+            m = (!MASK || col0 + i + q < n_valid) ? fmaxf(m, v) : m;
+        }
+    }
+    return m;
+}
+
+// QK-norm variant: 1 / sqrt(mean(x^2) + eps) of the d fp16 values x given as d/8 16-byte units.
+__device__ __forceinline__ float rms_scale_accumulate(float ss, uint4 u)
+{
+    const uint32_t words[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[q]));
+        ss = fmaf(f.x, f.x, ss);
+        ss = fmaf(f.y, f.y, ss);
+    }
+    return ss;
+}
+
+// Evaluation variants of kernel 1, compiled separately so that each carries only its own code.
+enum Variant : int {
+    kPlain = 0,    // the graph as written
+    kSafe = 1,     // each row's maximum subtracted before exp (a first pass over K finds it)
+    kQkNorm = 2,   // QK-norm: scores scaled by 1/rms of the query row and of the key vector; safe
+};
+
+template <int D, int STAGES, int VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     mg_attn_fwd_partial(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                         const __grid_constant__ CUtensorMap tmW, const FwdParams p)
 {
     using C = TileCfg<D>;
+    constexpr bool kSafeMax = VAR != kPlain;  // the row-maximum pass runs
+    constexpr bool kQk = VAR == kQkNorm;
     constexpr int kPBuffers = C::kPBuffers;
     using BI = Bars<STAGES, kPBuffers>;
-    static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
+    static_assert(fwd_smem_bytes(D, STAGES, kQk) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
     static_assert((128 * (D + 4) + 2 * 128) * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
 
@@ -230,6 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sStage0 = sQ + C::kQBytes;
     float *l_xchg = reinterpret_cast<float *>(smem + C::kQBytes + STAGES * C::kStageBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(l_xchg + 2 * kBlockM);
+    // QK-norm variant: key-vector scales of ring step u in slot u % kColScaleSlots (128 floats),
+    // after the 512-byte barrier area.
+    float *col_scale = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 512);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
@@ -250,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T = t_end - t_begin;
     // Steps of the K/V ring: with the max-subtracted variant, T steps that stream K alone (the
     // row-maximum pass), then the T steps of the main pass.
-    const int T1 = p.safe ? T : 0;
+    const int T1 = kSafeMax ? T : 0;
     const int U = T1 + T;
 
     if (threadIdx.x == 0) {
@@ -261,7 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(BI::kKvEmpty + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(bar(BI::kSFull + s), 1);
+            // QK-norm: S_u is complete when its MMAs are (commit) and the S warp has written the
+            // tile's key-vector scales (a second arrival).
+            ptx::mbar_init(bar(BI::kSFull + s), kQk ? 2 : 1);
             ptx::mbar_init(bar(BI::kSEmpty + s), kGroupWarps);
         }
         for (int s = 0; s < kPBuffers; ++s) {
@@ -404,10 +470,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
                                     idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
-                if (u < T1)
+                if (u < T1 && !kQk)
                     ptx::mma_commit(bar(BI::kKvEmpty + s));
             }
             __syncwarp();
+            if constexpr (kQk) {
+                // Key-vector scales 1/rms over d of this tile's 128 columns, lane l taking
+                // columns 4l..4l+3: one 8-byte load per d-row from the 128-byte-swizzled K tile.
+                const uint8_t *kt = smem + C::kQBytes + s * C::kStageBytes + (lane >> 4) * (D * 128);
+                const uint32_t unit = static_cast<uint32_t>(lane & 15) >> 1;
+                float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+                for (int k = 0; k < D; ++k) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(
+                        kt + k * 128 + ((unit ^ static_cast<uint32_t>(k & 7)) << 4) + (lane & 1) * 8);
+                    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+                    const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+                    ss[0] = fmaf(a.x, a.x, ss[0]);
+                    ss[1] = fmaf(a.y, a.y, ss[1]);
+                    ss[2] = fmaf(c.x, c.x, ss[2]);
+                    ss[3] = fmaf(c.y, c.y, ss[3]);
+                }
+                float4 cv;
+                cv.x = __frsqrt_rn(ss[0] * (1.f / D) + kQkNormEps);
+                cv.y = __frsqrt_rn(ss[1] * (1.f / D) + kQkNormEps);
+                cv.z = __frsqrt_rn(ss[2] * (1.f / D) + kQkNormEps);
+                cv.w = __frsqrt_rn(ss[3] * (1.f / D) + kQkNormEps);
+                *reinterpret_cast<float4 *>(col_scale + (u % kColScaleSlots) * kBlockN + 4 * lane) = cv;
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bar(BI::kSFull + sb));
+                // The row-maximum pass frees the K stage only now: its scales are read.
+                if (u < T1) {
+                    if (ptx::elect_one())
+                        ptx::mma_commit(bar(BI::kKvEmpty + s));
+                    __syncwarp();
+                }
+            }
         }
         if (!ok) {
             // Unwind: wait for the MMAs already issued before tensor memory is freed (elect.sync
@@ -485,11 +584,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc[2] = {0, 0};  // packed fp32 partial row sums (+0.0 bit patterns)
         const ptx::ExpPairConsts ek = ptx::exp_pair_consts();
         bool ok = true;
+        // QK-norm variant: this row's query scale 1/rms over d, from the Q tile in shared memory
+        // (rows past M are zero: their scale is finite and their scores stay 0).
+        float a_row = 1.f;
+        if constexpr (kQk) {
+            if (!warp_wait(bar(BI::kQFull), 0, BI::kQFull)) {
+                ok = false;
+            } else {
+                float ss = 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        ss = rms_scale_accumulate(ss, *reinterpret_cast<const uint4 *>(
+                                                          smem + c * C::kChunkRows128 + row * 128 +
+                                                          ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(row & 7)) << 4)));
+                a_row = __frsqrt_rn(ss * (1.f / D) + kQkNormEps);
+            }
+        }
+        const uint32_t a_log2e = __float_as_uint(a_row * ptx::kLog2e);
+        const uint64_t arow = ptx::pair_of(a_log2e);
         // Max-subtracted variant, first pass: each thread's running maximum of its row over the
         // valid columns of its group's steps (S only; the buffer is released once read).
         float m_row = -INFINITY;
         int u = g;
-        for (; u < T1; u += 2) {
+        for (; ok && u < T1; u += 2) {
             if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
                 ok = false;
                 break;
@@ -506,7 +625,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_wait(r0);
                     ptx::tmem_ld_wait(r1);
                     const int nv = n_valid - half * 64;
-                    if (nv >= 64) {
+                    if constexpr (kQk) {
+                        const float *cs = col_scale + (u % kColScaleSlots) * kBlockN + half * 64;
+                        if (nv >= 64) {
+                            m_row = max_slice_scaled<false>(r0, 0, nv, m_row, cs);
+                            m_row = max_slice_scaled<false>(r1, 32, nv, m_row, cs + 32);
+                        } else {
+                            m_row = max_slice_scaled<true>(r0, 0, nv, m_row, cs);
+                            m_row = max_slice_scaled<true>(r1, 32, nv, m_row, cs + 32);
+                        }
+                    } else if (nv >= 64) {
                         m_row = max_slice<false>(r0, 0, nv, m_row);
                         m_row = max_slice<false>(r1, 32, nv, m_row);
                     } else {
@@ -526,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // being reused (by the row sums below) before every thread has read them.
         uint64_t shift = 0;  // +0.0 twice: exp(s) unshifted, as the graph is written
         float m = 0.f;
-        if (p.safe) {
-            l_xchg[g * kBlockM + row] = m_row;
+        if constexpr (kSafeMax) {
+            l_xchg[g * kBlockM + row] = m_row * a_row;  // a_row > 0 (1 without QK-norm)
             ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
             m = fmaxf(l_xchg[row], l_xchg[kBlockM + row]);
             ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
@@ -575,7 +703,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // [32 half, 32 half + 32) of buffer pb (two fp16 per column).
                     const int nv = n_valid - half * 64;
                     uint32_t w[32];
-                    if (nv >= 64) {
+                    if constexpr (kQk) {
+                        const float *cs = col_scale + (u % kColScaleSlots) * kBlockN + half * 64;
+                        if (nv >= 64) {
+                            exp_slice_scaled<false>(r0, 0, nv, w, acc, cs, arow, shift);
+                            exp_slice_scaled<false>(r1, 32, nv, w + 16, acc, cs + 32, arow, shift);
+                        } else {
+                            exp_slice_scaled<true>(r0, 0, nv, w, acc, cs, arow, shift);
+                            exp_slice_scaled<true>(r1, 32, nv, w + 16, acc, cs + 32, arow, shift);
+                        }
+                    } else if (nv >= 64) {
                         exp_slice<false>(r0, 0, nv, w, acc, ek, shift);
                         exp_slice<false>(r1, 32, nv, w + 16, acc, ek, shift);
                     } else {
@@ -662,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
                     const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
                     p.ws_l[r] = l;
-                    if (p.safe)
+                    if (kSafeMax)
                         p.ws_m[r] = m;
                 }
                 ptx::fence_proxy_async_smem();
@@ -713,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < kMaxClusterRanks; ++r)
                     wt[r] = 1.f;
-                if (p.safe) {
+                if (kSafeMax) {
                     float mr[kMaxClusterRanks];
                     float mmax = -INFINITY;
 #pragma unroll

@@ -472,6 +472,26 @@ __device__ __forceinline__ void exp_pair_mufu(uint32_t s0, uint32_t s1, const Ex
         : "r"(s0), "r"(s1), "l"(k.log2e), "l"(shift));
 }
 
+// (exp(s0 c0 a - m), exp(s1 c1 a - m)) on the MUFU unit for scaled scores: one packed multiply
+// by the column scales (c0, c1), one packed fused multiply-add by `arow` = a*log2(e) (twice) plus
+// `shift` = -m*log2(e) (twice), then ex2.approx each.
+__device__ __forceinline__ void exp_pair_mufu_scaled(uint32_t s0, uint32_t s1, float c0, float c1, uint64_t arow,
+                                                     uint64_t shift, uint32_t &e0, uint32_t &e1)
+{
+    asm("{\n\t.reg .b64 a, c, t, x;\n\t.reg .f32 x0, x1;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 c, {%4, %5};\n\t"
+        "mul.rn.f32x2 t, a, c;\n\t"
+        "fma.rn.f32x2 x, t, %6, %7;\n\t"
+        "mov.b64 {x0, x1}, x;\n\t"
+        "ex2.approx.ftz.f32 x0, x0;\n\t"
+        "ex2.approx.ftz.f32 x1, x1;\n\t"
+        "mov.b32 %0, x0;\n\t"
+        "mov.b32 %1, x1;\n\t}"
+        : "=r"(e0), "=r"(e1)
+        : "r"(s0), "r"(s1), "f"(c0), "f"(c1), "l"(arow), "l"(shift));
+}
+
 // acc + (e0, e1) on an f32x2 pair.
 __device__ __forceinline__ uint64_t add_pair(uint64_t acc, uint32_t e0, uint32_t e1)
 {

@@ -589,6 +589,10 @@ def main():
             line["per_config_safe_softmax"] = {
                 name: measure_workload(name, args.per_config_steps, peaks, stream, exp_ns, flags=mg.MG_FLAG_SAFE_SOFTMAX)
                 for name in _inputs.CONFIG_ORDER}
+            # QK-norm attention (MG_FLAG_QK_NORM, which implies the max-subtracted evaluation).
+            line["per_config_qk_norm"] = {
+                name: measure_workload(name, args.per_config_steps, peaks, stream, exp_ns, flags=mg.MG_FLAG_QK_NORM)
+                for name in _inputs.CONFIG_ORDER}
         line["cpu_baseline"] = cpu_baseline(q, k, v, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     plan.destroy()
