@@ -63,9 +63,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// The deepest K/V ring that fits (the QK-norm variant's 2 KB of key-vector scales leave d = 128
-// two stages).
-int auto_stages(int64_t d, bool qk_norm) { return d == 64 ? 6 : (qk_norm ? 2 : 3); }
+// The deepest K/V ring that fits.
+int auto_stages(int64_t d) { return d == 64 ? 6 : 3; }
 
 using FwdKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                            const CUtensorMap, const mg::FwdParams);
@@ -86,10 +85,7 @@ FwdKernel fwd_kernel_variant(int64_t d, int stages)
     if (d == 128) {
         switch (stages) {
         case 2: return mg::mg_attn_fwd_partial<128, 2, VAR>;
-        case 3:  // the QK-norm variant's scales leave no room for a third 64 KB stage
-            if constexpr (VAR != mg::kQkNorm)
-                return mg::mg_attn_fwd_partial<128, 3, VAR>;
-            return nullptr;
+        case 3: return mg::mg_attn_fwd_partial<128, 3, VAR>;
         default: return nullptr;
         }
     }
@@ -167,10 +163,10 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         return fail(MG_ERR_INVALID_ARG, "grid too large");
 
     const bool qk_norm = (o.flags & MG_FLAG_QK_NORM) != 0;
-    int stages = o.stages == 0 ? auto_stages(d, qk_norm) : o.stages;
+    int stages = o.stages == 0 ? auto_stages(d) : o.stages;
     if (stages < 2 || stages > 6)
         return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 6]", stages);
-    const uint32_t smem = mg::fwd_smem_bytes(static_cast<int>(d), stages, qk_norm);
+    const uint32_t smem = mg::fwd_smem_bytes(static_cast<int>(d), stages);
     if (static_cast<int64_t>(smem) > max_smem || !fwd_kernel(d, stages, o.flags))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
@@ -190,13 +186,17 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->grid_ctas = static_cast<int32_t>(m_tiles * n_split);
     info->smem_bytes = static_cast<int32_t>(smem);
     info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
-    info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
+    // The QK-norm variant runs its scale kernel first.
+    info->kernels_per_run = ((n_split > 1 && !cluster) ? 2 : 1) + (qk_norm ? 1 : 0);
     info->num_sms = num_sms;
     // Split partials for the second kernel: numerators, row sums and (max-subtracted variant) row maxima.
     const int64_t row_words = (o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) ? 2 : 1;
     const int64_t partial_bytes =
         (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M * row_words) * 4 : 0;
-    info->workspace_bytes = 256 + partial_bytes;
+    // QK-norm: key-vector scales (B*N floats, then 128 more that reads of a last tile past N may
+    // touch) and query-row scales (B*M floats), from a 256-byte boundary.
+    const int64_t scale_bytes = qk_norm ? 256 + (B * N + 128 + B * M) * 4 : 0;
+    info->workspace_bytes = 256 + partial_bytes + scale_bytes;
     info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
     if (timeout_ns)
         *timeout_ns = o.timeout_ns ? static_cast<unsigned long long>(o.timeout_ns) : kDefaultTimeoutNs;
@@ -290,6 +290,8 @@ struct mg_attn_plan {
     float *ws_o = nullptr;
     float *ws_l = nullptr;
     float *ws_m = nullptr;
+    float *col_scale = nullptr;  // QK-norm: (B, N) key-vector scales, 128 spare floats, then (B, M) row scales
+    float *row_scale = nullptr;
     FwdKernel fwd = nullptr;
     CombineKernel combine = nullptr;
     // Tensor maps Q, K, V, O (re-encoded when a pointer changes) and the fp32 partial workspace
@@ -404,6 +406,18 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
             return st;
         }
     }
+    if (flags & MG_FLAG_QK_NORM) {
+        const size_t scale_floats = static_cast<size_t>(B) * N + 128 + static_cast<size_t>(B) * M;
+        const uintptr_t at = reinterpret_cast<uintptr_t>(ws + info.workspace_bytes - scale_floats * 4 - 256);
+        p->col_scale = reinterpret_cast<float *>((at + 255) & ~uintptr_t(255));
+        p->row_scale = p->col_scale + static_cast<size_t>(B) * N + 128;
+        e = cudaMemset(p->col_scale, 0, scale_floats * 4);
+        if (e != cudaSuccess) {
+            cudaFree(p->workspace);
+            delete p;
+            return cuda_fail(e, "cudaMemset(scales)");
+        }
+    }
     e = cudaMemset(p->workspace, 0, 256);
     if (e == cudaSuccess)
         e = cudaDeviceSynchronize();
@@ -474,6 +488,8 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.O = static_cast<__half *>(O);
     prm.ws_l = plan->ws_l;
     prm.ws_m = plan->ws_m;
+    prm.col_scale = plan->col_scale;
+    prm.row_scale = plan->row_scale;
     prm.status = plan->status;
     prm.timeout_ns = plan->timeout_ns;
     prm.inject_timeout = (plan->flags & MG_FLAG_INJECT_TIMEOUT) ? 1 : 0;
@@ -490,6 +506,29 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     cfg.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, pdl, in.cluster_ctas));
     void *fwd_args[6] = {&plan->maps[0], &plan->maps[1], &plan->maps[2], &plan->maps[3], &plan->maps[4], &prm};
     cudaError_t e;
+    if (plan->col_scale) {
+        // QK-norm: the key-vector and query-row scales first (PDL lets the fused kernel's prologue
+        // overlap it).
+        const __half *q = static_cast<const __half *>(Q);
+        const __half *k = static_cast<const __half *>(K);
+        float *cs = plan->col_scale;
+        float *rs = plan->row_scale;
+        int b = prm.B, m = prm.M, n = prm.N;
+        // Blocks of 32 key vectors, then blocks of 256 query rows.
+        const long long blocks = (static_cast<long long>(B) * N + 31) / 32 + (static_cast<long long>(B) * M + 255) / 256;
+        cudaLaunchConfig_t sc = cfg;
+        sc.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+        sc.blockDim = dim3(256, 1, 1);
+        sc.dynamicSmemBytes = 0;
+        cudaLaunchAttribute sattr[2];
+        sc.attrs = sattr;
+        sc.numAttrs = static_cast<unsigned>(fused_launch_attrs(sattr, pdl, 0));
+        void *sargs[7] = {&q, &k, &cs, &rs, &b, &m, &n};
+        const void *sk = d == 64 ? reinterpret_cast<const void *>(mg::mg_qknorm_scales<64>)
+                                 : reinterpret_cast<const void *>(mg::mg_qknorm_scales<128>);
+        if ((e = cudaLaunchKernelExC(&sc, sk, sargs)) != cudaSuccess)
+            return cuda_fail(e, "launch mg_qknorm_scales");
+    }
     if (plan->ev_begin && (e = cudaEventRecord(plan->ev_begin, cfg.stream)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord(begin)");
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(plan->fwd), fwd_args);
@@ -675,6 +714,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.status = reinterpret_cast<int *>(sd->scratch);
     prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
     prm.ws_m = nullptr;
+    prm.col_scale = nullptr;
+    prm.row_scale = nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
 

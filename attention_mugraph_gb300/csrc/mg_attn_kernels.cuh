@@ -67,7 +67,6 @@ constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
 constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warps
 constexpr int kMaxClusterRanks = 16;     // largest cluster of the on-chip combine
 constexpr float kQkNormEps = 1e-6f;      // rms_norm epsilon of the QK-norm variant
-constexpr int kColScaleSlots = 4;        // QK-norm: key-vector scales of the last 4 ring steps
 
 template <int D>
 struct TileCfg {
@@ -87,11 +86,11 @@ struct TileCfg {
 
 // Shared-memory bytes of kernel 1 for a head dim and pipeline depth: alignment slack, Q, the
 // K/V ring (its first stage is reused as the output staging area), the row-sum exchange of the
-// two softmax groups, the barriers and (QK-norm variant) the key-vector scales.
-__host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages, bool qk_norm = false)
+// two softmax groups and the barriers.
+__host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages)
 {
     return 1024u + static_cast<uint32_t>(128 * d * 2) + static_cast<uint32_t>(stages) * (2u * d * 128 * 2) +
-           2u * 128 * 4 + 512u + (qk_norm ? static_cast<uint32_t>(kColScaleSlots) * 128 * 4 : 0u);
+           2u * 128 * 4 + 512u;
 }
 
 struct FwdParams {
@@ -103,6 +102,8 @@ struct FwdParams {
     __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
     float *ws_l;             // (n_split, B, M) partial row sums
     float *ws_m;             // (n_split, B, M) partial row maxima (max-subtracted variant only)
+    const float *col_scale;  // QK-norm: (B, N) key-vector scales 1/rms (+128 readable floats past the end)
+    const float *row_scale;  // QK-norm: (B, M) query-row scales 1/rms
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
     int inject_timeout;
@@ -213,7 +214,7 @@ __device__ __forceinline__ float max_slice(const uint32_t (&r)[32], int col0, in
 }
 
 // QK-norm variant: as exp_slice and max_slice for the scores s * c_col * a, where `cs` holds the
-// slice's 32 key-vector scales c (shared memory, the same for every row) and `arow` is
+// slice's 32 key-vector scales c (16-byte aligned, the same for every row) and `arow` is
 // a*log2(e) twice (this row's query scale; for the maximum the caller applies a afterwards).
 template <bool MASK>
 __device__ __forceinline__ void exp_slice_scaled(const uint32_t (&r)[32], int col0, int n_valid, uint32_t *w,
@@ -221,7 +222,8 @@ __device__ __forceinline__ void exp_slice_scaled(const uint32_t (&r)[32], int co
 {
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-        const float2 c = *reinterpret_cast<const float2 *>(cs + i);
+        const float4 c4 = *reinterpret_cast<const float4 *>(cs + (i & ~3));
+        const float2 c = (i & 2) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
         uint32_t e0, e1;
         ptx::exp_pair_mufu_scaled(r[i], r[i + 1], c.x, c.y, arow, shift, e0, e1);
         if (MASK) {
@@ -250,19 +252,6 @@ __device__ __forceinline__ float max_slice_scaled(const uint32_t (&r)[32], int c
     return m;
 }
 
-// QK-norm variant: 1 / sqrt(mean(x^2) + eps) of the d fp16 values x given as d/8 16-byte units.
-__device__ __forceinline__ float rms_scale_accumulate(float ss, uint4 u)
-{
-    const uint32_t words[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[q]));
-        ss = fmaf(f.x, f.x, ss);
-        ss = fmaf(f.y, f.y, ss);
-    }
-    return ss;
-}
-
 // Evaluation variants of kernel 1, compiled separately so that each carries only its own code.
 enum Variant : int {
     kPlain = 0,    // the graph as written
@@ -281,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kQk = VAR == kQkNorm;
     constexpr int kPBuffers = C::kPBuffers;
     using BI = Bars<STAGES, kPBuffers>;
-    static_assert(fwd_smem_bytes(D, STAGES, kQk) <= 232448u, "tile configuration exceeds 227 KB");
+    static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
     static_assert((128 * (D + 4) + 2 * 128) * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
 
@@ -291,9 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sStage0 = sQ + C::kQBytes;
     float *l_xchg = reinterpret_cast<float *>(smem + C::kQBytes + STAGES * C::kStageBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(l_xchg + 2 * kBlockM);
-    // QK-norm variant: key-vector scales of ring step u in slot u % kColScaleSlots (128 floats),
-    // after the 512-byte barrier area.
-    float *col_scale = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 512);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
@@ -325,9 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(BI::kKvEmpty + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
-            // QK-norm: S_u is complete when its MMAs are (commit) and the S warp has written the
-            // tile's key-vector scales (a second arrival).
-            ptx::mbar_init(bar(BI::kSFull + s), kQk ? 2 : 1);
+            ptx::mbar_init(bar(BI::kSFull + s), 1);
             ptx::mbar_init(bar(BI::kSEmpty + s), kGroupWarps);
         }
         for (int s = 0; s < kPBuffers; ++s) {
@@ -470,43 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
                                     idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
-                if (u < T1 && !kQk)
+                if (u < T1)
                     ptx::mma_commit(bar(BI::kKvEmpty + s));
             }
             __syncwarp();
-            if constexpr (kQk) {
-                // Key-vector scales 1/rms over d of this tile's 128 columns, lane l taking
-                // columns 4l..4l+3: one 8-byte load per d-row from the 128-byte-swizzled K tile.
-                const uint8_t *kt = smem + C::kQBytes + s * C::kStageBytes + (lane >> 4) * (D * 128);
-                const uint32_t unit = static_cast<uint32_t>(lane & 15) >> 1;
-                float ss[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-                for (int k = 0; k < D; ++k) {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(
-                        kt + k * 128 + ((unit ^ static_cast<uint32_t>(k & 7)) << 4) + (lane & 1) * 8);
-                    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-                    const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-                    ss[0] = fmaf(a.x, a.x, ss[0]);
-                    ss[1] = fmaf(a.y, a.y, ss[1]);
-                    ss[2] = fmaf(c.x, c.x, ss[2]);
-                    ss[3] = fmaf(c.y, c.y, ss[3]);
-                }
-                float4 cv;
-                cv.x = __frsqrt_rn(ss[0] * (1.f / D) + kQkNormEps);
-                cv.y = __frsqrt_rn(ss[1] * (1.f / D) + kQkNormEps);
-                cv.z = __frsqrt_rn(ss[2] * (1.f / D) + kQkNormEps);
-                cv.w = __frsqrt_rn(ss[3] * (1.f / D) + kQkNormEps);
-                *reinterpret_cast<float4 *>(col_scale + (u % kColScaleSlots) * kBlockN + 4 * lane) = cv;
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(bar(BI::kSFull + sb));
-                // The row-maximum pass frees the K stage only now: its scales are read.
-                if (u < T1) {
-                    if (ptx::elect_one())
-                        ptx::mma_commit(bar(BI::kKvEmpty + s));
-                    __syncwarp();
-                }
-            }
         }
         if (!ok) {
             // Unwind: wait for the MMAs already issued before tensor memory is freed (elect.sync
@@ -584,23 +535,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc[2] = {0, 0};  // packed fp32 partial row sums (+0.0 bit patterns)
         const ptx::ExpPairConsts ek = ptx::exp_pair_consts();
         bool ok = true;
-        // QK-norm variant: this row's query scale 1/rms over d, from the Q tile in shared memory
-        // (rows past M are zero: their scale is finite and their scores stay 0).
+        // QK-norm variant: this row's query scale and the key-vector scales of the split's columns
+        // come from the scale kernel (rows past M take 1: their scores are 0 anyway).
         float a_row = 1.f;
+        const float *col_scale = nullptr;
         if constexpr (kQk) {
-            if (!warp_wait(bar(BI::kQFull), 0, BI::kQFull)) {
-                ok = false;
-            } else {
-                float ss = 0.f;
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        ss = rms_scale_accumulate(ss, *reinterpret_cast<const uint4 *>(
-                                                          smem + c * C::kChunkRows128 + row * 128 +
-                                                          ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(row & 7)) << 4)));
-                a_row = __frsqrt_rn(ss * (1.f / D) + kQkNormEps);
-            }
+            if (m0 + row < p.M)
+                a_row = p.row_scale[static_cast<size_t>(b) * p.M + m0 + row];
+            col_scale = p.col_scale + static_cast<size_t>(b) * p.N + static_cast<size_t>(t_begin) * kBlockN;
         }
         const uint32_t a_log2e = __float_as_uint(a_row * ptx::kLog2e);
         const uint64_t arow = ptx::pair_of(a_log2e);
@@ -626,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_wait(r1);
                     const int nv = n_valid - half * 64;
                     if constexpr (kQk) {
-                        const float *cs = col_scale + (u % kColScaleSlots) * kBlockN + half * 64;
+                        const float *cs = col_scale + static_cast<size_t>(u) * kBlockN + half * 64;
                         if (nv >= 64) {
                             m_row = max_slice_scaled<false>(r0, 0, nv, m_row, cs);
                             m_row = max_slice_scaled<false>(r1, 32, nv, m_row, cs + 32);
@@ -704,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nv = n_valid - half * 64;
                     uint32_t w[32];
                     if constexpr (kQk) {
-                        const float *cs = col_scale + (u % kColScaleSlots) * kBlockN + half * 64;
+                        const float *cs = col_scale + static_cast<size_t>(t) * kBlockN + half * 64;
                         if (nv >= 64) {
                             exp_slice_scaled<false>(r0, 0, nv, w, acc, cs, arow, shift);
                             exp_slice_scaled<false>(r1, 32, nv, w + 16, acc, cs + 32, arow, shift);
@@ -905,6 +847,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// QK-norm scales (the graph's Q = rms_norm(Q), K = rms_norm(K) over the head dimension, applied
+// by kernel 1 as scales of the scores): col_scale[b, n] = 1/sqrt(mean_k K[b,k,n]^2 + eps) and
+// row_scale[b, m] = 1/sqrt(mean_k Q[b,m,k]^2 + eps), sums of squares in fp32.
+// Blocks [0, key_blocks) take 32 consecutive key vectors each: warp w sums rows
+// [w D/8, (w+1) D/8) of every column (a coalesced 64-byte read per row, all rows of a warp in
+// flight together), and the eight partial sums meet in shared memory in a fixed order. The
+// remaining blocks take 256 query rows each, one per thread.
+template <int D>
+__global__ void __launch_bounds__(256)
+    mg_qknorm_scales(const __half *__restrict__ Q, const __half *__restrict__ K, float *__restrict__ col_scale,
+                     float *__restrict__ row_scale, int B, int M, int N)
+{
+    constexpr int kRowsPerWarp = D / 8;
+    __shared__ float part[8][32];
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    const long long keys = static_cast<long long>(B) * N;
+    const long long key_blocks = (keys + 31) / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (blockIdx.x < key_blocks) {
+        const long long i = static_cast<long long>(blockIdx.x) * 32 + lane;  // key index b*N + n
+        float ss = 0.f;
+        if (i < keys) {
+            const int b = static_cast<int>(i / N);
+            const int n = static_cast<int>(i % N);
+            const __half *k = K + (static_cast<size_t>(b) * D + static_cast<size_t>(warp) * kRowsPerWarp) * N + n;
+            float x[kRowsPerWarp];
+#pragma unroll
+            for (int c = 0; c < kRowsPerWarp; ++c)
+                x[c] = __half2float(k[static_cast<size_t>(c) * N]);
+#pragma unroll
+            for (int c = 0; c < kRowsPerWarp; ++c)
+                ss = fmaf(x[c], x[c], ss);
+        }
+        part[warp][lane] = ss;
+        __syncthreads();
+        if (warp == 0 && i < keys) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                t += part[w][lane];
+            col_scale[i] = __frsqrt_rn(t * (1.f / D) + kQkNormEps);
+        }
+    } else {
+        const long long r = (blockIdx.x - key_blocks) * 256 + threadIdx.x;
+        if (r < static_cast<long long>(B) * M) {
+            const uint4 *q = reinterpret_cast<const uint4 *>(Q + static_cast<size_t>(r) * D);
+            uint4 w[D / 8];
+#pragma unroll
+            for (int u = 0; u < D / 8; ++u)
+                w[u] = q[u];
+            float ss = 0.f;
+#pragma unroll
+            for (int u = 0; u < D / 8; ++u) {
+                const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[h]));
+                    ss = fmaf(f.x, f.x, ss);
+                    ss = fmaf(f.y, f.y, ss);
+                }
+            }
+            row_scale[r] = __frsqrt_rn(ss * (1.f / D) + kQkNormEps);
+        }
     }
 }
 

@@ -134,16 +134,20 @@ def test_query_safe_softmax_workspace():
 
 
 def test_query_qk_norm_plan():
-    # QK-norm keeps 2 KB of key-vector scales in shared memory (d = 128 then takes 2 stages) and,
-    # as it implies the max-subtracted evaluation, one row maximum per split and row.
+    # QK-norm adds its scale kernel (one more launch) and the scales to the workspace: B*N key
+    # scales, 128 spare floats and B*M query scales; as it implies the max-subtracted evaluation,
+    # also one row maximum per split and row. Shared memory and stages are unchanged.
     plain = mg.mg_attn_query(2, 256, 4096, 64, 152)
     qk = mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_QK_NORM)
-    assert qk["smem_bytes"] == plain["smem_bytes"] + 2048 and qk["stages"] == 6
-    assert mg.mg_attn_query(2, 256, 4096, 128, 152, flags=mg.MG_FLAG_QK_NORM)["stages"] == 2
+    assert qk["smem_bytes"] == plain["smem_bytes"] and qk["stages"] == 6
+    assert qk["kernels_per_run"] == plain["kernels_per_run"] + 1
+    assert qk["workspace_bytes"] == plain["workspace_bytes"] + 256 + (2 * 4096 + 128 + 2 * 256) * 4
+    assert mg.mg_attn_query(2, 256, 4096, 128, 152, flags=mg.MG_FLAG_QK_NORM)["stages"] == 3
     B, M, N, d = 2, 256, 65536, 64
     a = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_QK_NORM)
     b = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX)
-    assert a["workspace_bytes"] == b["workspace_bytes"] == 256 + a["n_split"] * B * M * (d + 2) * 4
+    assert a["workspace_bytes"] == b["workspace_bytes"] + 256 + (B * N + 128 + B * M) * 4
+    assert b["workspace_bytes"] == 256 + b["n_split"] * B * M * (d + 2) * 4
 
 
 def test_query_options():
@@ -162,7 +166,6 @@ def test_query_options():
     ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x80}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x20}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 128), {"flags": 0x10, "stages": 3}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),
