@@ -206,7 +206,72 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     return MG_OK;
 }
 
+// Host-buffer entry point: copies between the caller's pinned host buffers (read and written
+// through their device-mapped addresses over the CPU-GPU link) and the plan's device staging, in
+// 16-byte units. Up to three (src, dst, units) jobs per launch; each CTA walks all of them with a
+// grid stride, keeping several loads in flight per thread.
+struct CopyJobs {
+    const uint4 *src[3];
+    uint4 *dst[3];
+    unsigned long long units[3];
+};
+
+__global__ void __launch_bounds__(512) mg_copy_units(const CopyJobs jobs)
+{
+    mg::ptx::griddep_wait();  // the staging buffers may still be read by the previous call's kernels
+    mg::ptx::griddep_launch_dependents();
+    const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
+#pragma unroll 1
+    for (int j = 0; j < 3; ++j) {
+        const uint4 *src = jobs.src[j];
+        uint4 *dst = jobs.dst[j];
+        const unsigned long long n = jobs.units[j];
+        unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+        for (; i + 3 * stride < n; i += 4 * stride) {
+            const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+            dst[i] = a;
+            dst[i + stride] = b;
+            dst[i + 2 * stride] = c;
+            dst[i + 3 * stride] = d;
+        }
+        for (; i < n; i += stride)
+            dst[i] = src[i];
+    }
+}
+
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// Whether a host pointer is page-locked host memory the device can address (its device address in
+// *dev); false for pageable memory or on any query error (which is cleared).
+bool device_mapped(const void *p, void **dev)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr || misaligned(a.devicePointer))
+        return false;
+    *dev = a.devicePointer;
+    return true;
+}
+
+// One launch of the 16-byte copy kernel: two CTAs of 512 threads per SM, PDL when allowed.
+cudaError_t launch_copy(const CopyJobs &jobs, int num_sms, bool pdl, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * num_sms), 1, 1);
+    cfg.blockDim = dim3(512, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, mg_copy_units, jobs);
+}
 
 // Whether the current device can hold all ctas / n clusters of n CTAs of the fused kernel at
 // once (one wave: a cluster left for a second wave would double the time). Sizes above 8 need
@@ -579,15 +644,43 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
     }
     uint8_t *s = static_cast<uint8_t *>(plan->staging);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((e = cudaMemcpyAsync(s + oq, hQ, bq, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(s + ok, hK, bk, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(s + ov, hV, bv, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+
+    // Pinned (page-locked, device-mapped) 16-byte-aligned host buffers are read and written by
+    // copy kernels through their device addresses, chained to the attention kernels with PDL;
+    // any other host memory goes through the copy engines.
+    void *dQ = nullptr, *dK = nullptr, *dV = nullptr, *dO = nullptr;
+    bool direct = device_mapped(hQ, &dQ) && device_mapped(hK, &dK) && device_mapped(hV, &dV) && device_mapped(hO, &dO);
+    const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
+    if (direct) {
+        CopyJobs in_jobs{};
+        const void *src[3] = {dQ, dK, dV};
+        const size_t off[3] = {oq, ok, ov};
+        const size_t bytes[3] = {bq, bk, bv};
+        for (int i = 0; i < 3; ++i) {
+            in_jobs.src[i] = static_cast<const uint4 *>(src[i]);
+            in_jobs.dst[i] = reinterpret_cast<uint4 *>(s + off[i]);
+            in_jobs.units[i] = bytes[i] / 16;
+        }
+        if ((e = launch_copy(in_jobs, plan->info.num_sms, pdl, st)) != cudaSuccess)
+            return cuda_fail(e, "launch mg_copy_units (host to device)");
+    } else if ((e = cudaMemcpyAsync(s + oq, hQ, bq, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+               (e = cudaMemcpyAsync(s + ok, hK, bk, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+               (e = cudaMemcpyAsync(s + ov, hV, bv, cudaMemcpyHostToDevice, st)) != cudaSuccess) {
         return cuda_fail(e, "cudaMemcpyAsync(host to device)");
+    }
     mg_status r = mg_attn_run(plan, s + oq, s + ok, s + ov, s + oo, stream);
     if (r != MG_OK)
         return r;
-    if ((e = cudaMemcpyAsync(hO, s + oo, bq, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    if (direct) {
+        CopyJobs out_jobs{};
+        out_jobs.src[0] = reinterpret_cast<const uint4 *>(s + oo);
+        out_jobs.dst[0] = static_cast<uint4 *>(dO);
+        out_jobs.units[0] = bq / 16;
+        if ((e = launch_copy(out_jobs, plan->info.num_sms, pdl, st)) != cudaSuccess)
+            return cuda_fail(e, "launch mg_copy_units (device to host)");
+    } else if ((e = cudaMemcpyAsync(hO, s + oo, bq, cudaMemcpyDeviceToHost, st)) != cudaSuccess) {
         return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    }
     return MG_OK;
 }
 

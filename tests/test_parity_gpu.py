@@ -206,6 +206,22 @@ def test_host_buffer_entry_point():
         assert_parity(ho, ref, "run_host")
 
 
+def test_host_buffer_entry_point_pageable_and_large():
+    # Pageable host tensors take the copy-engine path; pinned ones the mapped-copy kernels. Both
+    # on a shape with a split combine and several copy rounds per thread.
+    q, k, v, _ = inputs.make_config("long_kv")
+    ref = oracle.attention(q, k, v)
+    B, M, N, d = 2, 256, 65536, 64
+    plan = mg.Plan(B, M, N, d)
+    for pinned in (False, True):
+        hq, hk, hv = ((t.pin_memory() if pinned else t.clone()) for t in (q, k, v))
+        ho = torch.full((B, M, d), float("nan"), dtype=torch.float16)
+        ho = ho.pin_memory() if pinned else ho
+        plan.run_host(hq, hk, hv, ho)
+        torch.cuda.synchronize()
+        assert_parity(ho, ref, f"run_host pinned={pinned}")
+
+
 def test_misaligned_pointer_rejected():
     plan = mg.Plan(1, 128, 1024, 64)
     buf = torch.zeros(1 * 128 * 64 + 8, dtype=torch.float16, device="cuda")
