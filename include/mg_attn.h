@@ -149,9 +149,13 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
 /*
  * End-to-end variant for host buffers: copies Q, K, V from host memory into device
  * buffers owned by the plan, runs as mg_attn_run, and copies O back into host memory,
- * all enqueued on `stream` (pinned host memory makes the copies asynchronous; the caller
- * synchronises the stream before reading hO). The plan's device staging buffers (the
- * size of Q, K, V and O) are allocated by the first call on that plan and reused after.
+ * all enqueued on `stream`; the caller synchronises the stream before reading hO.
+ * Page-locked host buffers that the device can address (cudaHostAlloc / pinned tensors,
+ * 16-byte aligned) are read and written by copy kernels through their device addresses,
+ * chained to the attention kernels with programmatic dependent launch; other host memory
+ * (pageable) goes through cudaMemcpyAsync. The plan's device staging buffers (the size of
+ * Q, K, V and O) are allocated by the first call on that plan and reused after, so one
+ * plan must not run two such calls at once on different streams.
  * Errors: as mg_attn_run, plus MG_ERR_CUDA if the staging allocation fails.
  */
 mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, const void *hV,
