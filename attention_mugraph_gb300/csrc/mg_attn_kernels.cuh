@@ -12,31 +12,37 @@
 //     P  = exp(S) (0 beyond N)           fp32; l += rowsum(P) in fp32; fp16 P to tensor memory
 //     O += fp16(P) . V_tile              tcgen05 MMA with A read from tensor memory
 // The divide by the row sum commutes with the second product, so it is deferred.
-// With one split the CTA divides and writes fp16 O; otherwise it writes the fp32 partial
-// numerator O_j and row sum l_j to the workspace. Both go out through shared memory and TMA
-// bulk stores.
+// With one split the CTA divides and writes fp16 O (TMA store). With 2..16 splits that fit one
+// wave, the splits of a row tile form a thread-block cluster and combine on chip (distributed
+// shared memory, fixed rank order). Otherwise each writes the fp32 partial numerator O_j and row
+// sum l_j to the workspace (TMA store) for kernel 2.
 //
 // Kernel 2, mg_attn_combine: O = (sum_j O_j) / (sum_j l_j) -> fp16, the second threadblock
 // graph of the "attention" search configuration (blog, section 4.3). No max-subtraction
-// means the partials combine by plain sums.
+// means the partials combine by plain sums (weights exp(m_j - max m) in the max-subtracted
+// variant).
+//
+// Variants (template parameter VAR): the graph as written; max-subtracted (a first pass over
+// the split's K tiles finds each row's maximum score m, then P = exp(S - m)); QK-norm (scores
+// scaled by query-row and key-vector scales from kernel mg_qknorm_scales, max-subtracted).
 //
 // Warp roles of kernel 1 (352 threads):
 //   warp 0       TMA producer: Q once, then K/V tiles through a STAGES-deep mbarrier ring
-//   warp 1       tensor-memory allocator; issues S = Q.K (one thread)
-//   warp 10      issues O += P.V (one thread); two issuing warps keep an S from waiting behind
-//                a P.V and the reverse
+//   warp 1       tensor-memory allocator; issues S = Q.K (elected lane)
+//   warp 10      issues O += P.V (elected lane); two issuing warps keep an S from waiting
+//                behind a P.V and the reverse
 //   warps 2..9   softmax + epilogue, two groups of four: group g = (w-2)/4 takes the tiles
 //                t with t % 2 == g, in S buffer g, all 128 columns of its rows; warp w reads
 //                tensor-memory lanes 32*(w%4).. (its rows). In the epilogue group g takes
 //                O columns [g d/2, (g+1) d/2).
-// Tensor memory (512 columns): S double buffer at columns [0,128) and [128,256), O at
-// [256, 256 + d), then the fp16 P buffers (64 columns each, two fp16 per column): three for
-// d = 64, two for d = 128, so the softmax warps can run ahead of the P.V products.
+// Tensor memory (512 columns): S buffers at columns [0,128) (group 0) and [128,256) (group 1),
+// O at [256, 256 + d), then the fp16 P buffers (64 columns each, two fp16 per column): three
+// for d = 64, two for d = 128, so the softmax warps can run ahead of the P.V products.
 // Keeping P in tensor memory spares shared memory 64 KB of traffic per tile (P written by the
-// softmax warps and read back by the MMA), which otherwise bounds the tile rate.
+// softmax warps and read back by the MMA).
 //
-// Exponentials: ex2.approx on the MUFU unit after one two-wide fp32 multiply by log2(e) per pair
-// of columns. A polynomial path on the FMA pipe (exp_pair_fma, same fp32 accuracy) can take
+// Exponentials: ex2.approx on the MUFU unit after one two-wide fp32 fused multiply-add
+// s*log2(e) - m*log2(e) per pair of columns (m = 0 for the graph as written). A polynomial path on the FMA pipe (exp_pair_fma, same fp32 accuracy) can take
 // kPolyOf8 of every 8 columns; measured on GB300 (mg_diag_exp_rate), this sequence runs 32
 // exponentials per clock per SM on MUFU and 13 on the FMA pipe, so the split is 0.
 //
@@ -77,7 +83,7 @@ struct TileCfg {
     static constexpr uint32_t kVBytes = kBlockN * D * 2;    // V tile, d contiguous
     static constexpr uint32_t kStageBytes = kKBytes + kVBytes;
     static constexpr uint32_t kChunkRows128 = 128 * 128;        // one 128-row x 128-byte chunk
-    static constexpr int kHalfCols = D / 2;                     // O columns per softmax thread
+    static constexpr int kHalfCols = D / 2;                     // O columns per epilogue thread
     static constexpr uint32_t kTmemP = kTmemO + D;              // P buffer b at kTmemP + 64 b
     // P buffers: as many as tensor memory holds after S (2 x 128 columns) and O (d columns).
     static constexpr int kPBuffers = D == 64 ? 3 : 2;
@@ -430,10 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             return __all_sync(0xffffffffu, wait_bounded(wc, b_, parity, where));
         };
         bool ok = warp_wait(bar(BI::kQFull), 0, BI::kQFull);
-        // S_u = Q . K_u into S buffer u % 2, as soon as K tile u is in its stage and, for
-        // u >= 2, the softmax warps have read S_{u-2} out of that buffer (which they do first
-        // thing on tile u-2). The P.V products run from another warp, so an S never waits
-        // behind a P.V and the softmax warps find every S ready.
+        // S_u = Q . K_u into S buffer u % 2 (softmax group u % 2), as soon as K tile u is in its
+        // stage and, for u >= 2, that group has read S_{u-2} out of the buffer (which it does in
+        // the first half of tile u-2). The P.V products run from another warp, so an S never
+        // waits behind a P.V.
         // With the max-subtracted variant the first T1 steps compute S for the row-maximum pass;
         // their completion also frees the K stage (no P.V reads it).
         for (int u = 0; ok && u < U; ++u) {
