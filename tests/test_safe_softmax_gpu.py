@@ -107,3 +107,17 @@ def test_matches_plain_path_on_small_scores():
     b, _ = run_gpu(q, k, v, flags=SAFE)
     assert_parity(a, ref, "plain")
     assert_parity(b, ref, "safe")
+
+
+@pytest.mark.parametrize("flags", [SAFE, mg.MG_FLAG_QK_NORM, SAFE | mg.MG_FLAG_NO_CLUSTER])
+def test_bounded_wait_in_variants(flags):
+    # The load warp waits on a barrier nothing arrives on; every role of the variant (row-maximum
+    # pass, maximum exchange, cluster or second-kernel combine) unwinds within the bound and the
+    # context stays usable.
+    q, k, v, _ = inputs.make_config("gqa")
+    plan = mg.Plan(2, 256, 4096, 64, flags=flags | mg.MG_FLAG_INJECT_TIMEOUT, timeout_ns=2_000_000)
+    O = torch.zeros((2, 256, 64), dtype=torch.float16, device="cuda")
+    plan.run(q.cuda(), k.cuda(), v.cuda(), O)
+    assert plan.status() == mg.MG_ERR_TIMEOUT
+    O2, _ = run_gpu(q, k, v, flags=SAFE)
+    assert_parity(O2, oracle.attention(q, k, v), "after timeout")
