@@ -561,7 +561,7 @@ def main():
         "us_per_call": us_graph,
         "roofline_time_us": roof_t * 1e6,
         "roofline_fraction_of_step": roof_t * 1e6 / us_graph,
-        "stream_loop": {"us_per_call": us_loop, "value": fl * args.steps / (ms_loop * 1e-3) / 1e12,
+        "stream_loop": {"us_per_call": us_loop, "value": job_tflops(fl, args.steps, world, ms_loop),
                         "unit": "TFLOP/s"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": recorded_traffic(), "kernel": "mg_attn_fwd_partial",
@@ -571,7 +571,7 @@ def main():
                      "peak_source": f"{peak_kind}: MEASURED_PEAKS.json "
                                     f"{'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'} (burst)",
                      "tensor_frac": fl / (dur_us * 1e-6) / 1e12 / peaks["bf16_tflops"]},
-        "e2e": {"value": fl * n_e2e / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tflops(fl, n_e2e, world, ms_e2e), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e, "us_per_call": ms_e2e * 1e3 / n_e2e},
         "gpu_launches": args.steps * info["kernels_per_run"],
         "clocks": clk,
