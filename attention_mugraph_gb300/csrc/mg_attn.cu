@@ -187,7 +187,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->smem_bytes = static_cast<int32_t>(smem);
     info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
     // The QK-norm variant runs its scale kernel first.
-    info->kernels_per_run = ((n_split > 1 && !cluster) ? 2 : 1) + (qk_norm ? 1 : 0);
+    info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
     // Split partials for the second kernel: numerators, row sums and (max-subtracted variant) row maxima.
     const int64_t row_words = (o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) ? 2 : 1;
@@ -195,7 +195,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M * row_words) * 4 : 0;
     // QK-norm: key-vector scales (B*N floats, then 128 more that reads of a last tile past N may
     // touch) and query-row scales (B*M floats), from a 256-byte boundary.
-    const int64_t scale_bytes = qk_norm ? 256 + (B * N + 128 + B * M) * 4 : 0;
+    const int64_t scale_bytes = qk_norm ? 256 + (B * N + 128) * 4 : 0;
     info->workspace_bytes = 256 + partial_bytes + scale_bytes;
     info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
     if (timeout_ns)
@@ -355,8 +355,7 @@ struct mg_attn_plan {
     float *ws_o = nullptr;
     float *ws_l = nullptr;
     float *ws_m = nullptr;
-    float *col_scale = nullptr;  // QK-norm: (B, N) key-vector scales, 128 spare floats, then (B, M) row scales
-    float *row_scale = nullptr;
+    float *col_scale = nullptr;  // QK-norm: (B, N) key-vector scales, then 128 spare floats
     FwdKernel fwd = nullptr;
     CombineKernel combine = nullptr;
     // Tensor maps Q, K, V, O (re-encoded when a pointer changes) and the fp32 partial workspace
@@ -472,10 +471,9 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
         }
     }
     if (flags & MG_FLAG_QK_NORM) {
-        const size_t scale_floats = static_cast<size_t>(B) * N + 128 + static_cast<size_t>(B) * M;
+        const size_t scale_floats = static_cast<size_t>(B) * N + 128;
         const uintptr_t at = reinterpret_cast<uintptr_t>(ws + info.workspace_bytes - scale_floats * 4 - 256);
         p->col_scale = reinterpret_cast<float *>((at + 255) & ~uintptr_t(255));
-        p->row_scale = p->col_scale + static_cast<size_t>(B) * N + 128;
         e = cudaMemset(p->col_scale, 0, scale_floats * 4);
         if (e != cudaSuccess) {
             cudaFree(p->workspace);
@@ -554,7 +552,6 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.ws_l = plan->ws_l;
     prm.ws_m = plan->ws_m;
     prm.col_scale = plan->col_scale;
-    prm.row_scale = plan->row_scale;
     prm.status = plan->status;
     prm.timeout_ns = plan->timeout_ns;
     prm.inject_timeout = (plan->flags & MG_FLAG_INJECT_TIMEOUT) ? 1 : 0;
@@ -571,29 +568,6 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     cfg.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, pdl, in.cluster_ctas));
     void *fwd_args[6] = {&plan->maps[0], &plan->maps[1], &plan->maps[2], &plan->maps[3], &plan->maps[4], &prm};
     cudaError_t e;
-    if (plan->col_scale) {
-        // QK-norm: the key-vector and query-row scales first (PDL lets the fused kernel's prologue
-        // overlap it).
-        const __half *q = static_cast<const __half *>(Q);
-        const __half *k = static_cast<const __half *>(K);
-        float *cs = plan->col_scale;
-        float *rs = plan->row_scale;
-        int b = prm.B, m = prm.M, n = prm.N;
-        // Blocks of 32 key vectors, then blocks of 256 query rows.
-        const long long blocks = (static_cast<long long>(B) * N + 31) / 32 + (static_cast<long long>(B) * M + 255) / 256;
-        cudaLaunchConfig_t sc = cfg;
-        sc.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-        sc.blockDim = dim3(256, 1, 1);
-        sc.dynamicSmemBytes = 0;
-        cudaLaunchAttribute sattr[2];
-        sc.attrs = sattr;
-        sc.numAttrs = static_cast<unsigned>(fused_launch_attrs(sattr, pdl, 0));
-        void *sargs[7] = {&q, &k, &cs, &rs, &b, &m, &n};
-        const void *sk = d == 64 ? reinterpret_cast<const void *>(mg::mg_qknorm_scales<64>)
-                                 : reinterpret_cast<const void *>(mg::mg_qknorm_scales<128>);
-        if ((e = cudaLaunchKernelExC(&sc, sk, sargs)) != cudaSuccess)
-            return cuda_fail(e, "launch mg_qknorm_scales");
-    }
     if (plan->ev_begin && (e = cudaEventRecord(plan->ev_begin, cfg.stream)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord(begin)");
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(plan->fwd), fwd_args);
@@ -808,7 +782,6 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
     prm.ws_m = nullptr;
     prm.col_scale = nullptr;
-    prm.row_scale = nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
 

@@ -24,7 +24,9 @@
 //
 // Variants (template parameter VAR): the graph as written; max-subtracted (a first pass over
 // the split's K tiles finds each row's maximum score m, then P = exp(S - m)); QK-norm (scores
-// scaled by query-row and key-vector scales from kernel mg_qknorm_scales, max-subtracted).
+// scaled by query-row and key-vector scales 1/rms, max-subtracted; the softmax warps compute the
+// key-vector scales in the first pass from the K tiles it streams, and the query-row scales from
+// the Q tile).
 //
 // Warp roles of kernel 1 (352 threads):
 //   warp 0       TMA producer: Q once, then K/V tiles through a STAGES-deep mbarrier ring
@@ -73,6 +75,7 @@ constexpr int kStatusTimeout = 7;  // MG_ERR_TIMEOUT
 constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warps
 constexpr int kMaxClusterRanks = 16;     // largest cluster of the on-chip combine
 constexpr float kQkNormEps = 1e-6f;      // rms_norm epsilon of the QK-norm variant
+constexpr uint32_t kGroupBarrier0 = 2;   // named barrier ids 2, 3: the four warps of softmax group 0, 1
 
 template <int D>
 struct TileCfg {
@@ -108,8 +111,8 @@ struct FwdParams {
     __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
     float *ws_l;             // (n_split, B, M) partial row sums
     float *ws_m;             // (n_split, B, M) partial row maxima (max-subtracted variant only)
-    const float *col_scale;  // QK-norm: (B, N) key-vector scales 1/rms (+128 readable floats past the end)
-    const float *row_scale;  // QK-norm: (B, M) query-row scales 1/rms
+    float *col_scale;        // QK-norm: (B, N) key-vector scales 1/rms, written by the row-maximum
+                             // pass and read by the main pass (+128 readable floats past the end)
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
     int inject_timeout;
@@ -256,6 +259,46 @@ __device__ __forceinline__ float max_slice_scaled(const uint32_t (&r)[32], int c
         }
     }
     return m;
+}
+
+// QK-norm sums of squares (fp32) of eight fp16 values, one 16-byte unit of shared memory: into
+// two running sums (a Q row), or column by column (eight key vectors, one d-row of each).
+__device__ __forceinline__ void sum_sq_unit(const uint4 &w, float (&ss)[2])
+{
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[h]));
+        ss[0] = fmaf(f.x, f.x, ss[0]);
+        ss[1] = fmaf(f.y, f.y, ss[1]);
+    }
+}
+
+__device__ __forceinline__ void sum_sq_cols(const uint4 &w, float (&sq)[8])
+{
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[h]));
+        sq[2 * h] = fmaf(f.x, f.x, sq[2 * h]);
+        sq[2 * h + 1] = fmaf(f.y, f.y, sq[2 * h + 1]);
+    }
+}
+
+// Sums a[e] over the eight lanes that share lane % 4 (lane bits 2..4) and leaves element
+// e = 4 bit4 + 2 bit3 + bit2 of the total on each lane: a reduce-scatter in three exchange steps
+// (7 shuffles instead of 24 for eight full reductions), in a fixed order.
+__device__ __forceinline__ float reduce_scatter8(const float (&a)[8], int lane)
+{
+    float b4[4], b2[2];
+    const bool h4 = (lane & 16) != 0, h3 = (lane & 8) != 0, h2 = (lane & 4) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        b4[e] = (h4 ? a[e + 4] : a[e]) + __shfl_xor_sync(0xffffffffu, h4 ? a[e] : a[e + 4], 16);
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+        b2[e] = (h3 ? b4[e + 2] : b4[e]) + __shfl_xor_sync(0xffffffffu, h3 ? b4[e] : b4[e + 2], 8);
+    return (h2 ? b2[1] : b2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? b2[0] : b2[1], 4);
 }
 
 // Evaluation variants of kernel 1, compiled separately so that each carries only its own code.
@@ -441,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the first half of tile u-2). The P.V products run from another warp, so an S never
         // waits behind a P.V.
         // With the max-subtracted variant the first T1 steps compute S for the row-maximum pass;
-        // their completion also frees the K stage (no P.V reads it).
+        // their completion also frees the K stage (no P.V reads it), except with QK-norm, where
+        // the softmax group also reads the K tile (the key-vector scales) and frees the stage.
         for (int u = 0; ok && u < U; ++u) {
             const int s = u % STAGES;
             const int sb = u & 1;
@@ -460,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
                                     idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
-                if (u < T1)
+                if (!kQk && u < T1)
                     ptx::mma_commit(bar(BI::kKvEmpty + s));
             }
             __syncwarp();
@@ -541,14 +585,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc[2] = {0, 0};  // packed fp32 partial row sums (+0.0 bit patterns)
         const ptx::ExpPairConsts ek = ptx::exp_pair_consts();
         bool ok = true;
-        // QK-norm variant: this row's query scale and the key-vector scales of the split's columns
-        // come from the scale kernel (rows past M take 1: their scores are 0 anyway).
+        // QK-norm variant: a is this row's query scale, 1/rms of the Q tile's row (read from shared
+        // memory once; rows past M take 1, their scores are 0 anyway); the key-vector scales c of
+        // the split's columns are computed by the row-maximum pass below and kept in global
+        // memory (L2) for the main pass.
         float a_row = 1.f;
-        const float *col_scale = nullptr;
+        float *col_scale = nullptr;
         if constexpr (kQk) {
-            if (m0 + row < p.M)
-                a_row = p.row_scale[static_cast<size_t>(b) * p.M + m0 + row];
             col_scale = p.col_scale + static_cast<size_t>(b) * p.N + static_cast<size_t>(t_begin) * kBlockN;
+            ok = warp_wait(bar(BI::kQFull), 0, BI::kQFull);
+            if (ok && m0 + row < p.M) {
+                // The row's 16-byte units in swizzled order (a permutation of the row: the sum is
+                // the same), so the eight lanes of a quarter-warp hit eight distinct bank groups.
+                float ss[2] = {0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        sum_sq_unit(*reinterpret_cast<const uint4 *>(
+                                        smem + c * C::kChunkRows128 + row * 128 + ((k ^ (row & 7)) << 4)),
+                                    ss);
+                a_row = __frsqrt_rn((ss[0] + ss[1]) * (1.f / D) + kQkNormEps);
+            }
         }
         const uint32_t a_log2e = __float_as_uint(a_row * ptx::kLog2e);
         const uint64_t arow = ptx::pair_of(a_log2e);
@@ -556,25 +614,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         // valid columns of its group's steps (S only; the buffer is released once read).
         float m_row = -INFINITY;
         int u = g;
-        for (; ok && u < T1; u += 2) {
-            if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const int n_valid = p.N - (t_begin + u) * kBlockN;
+        if constexpr (kQk) {
+            // Each tile's 128 key-vector scales first, from the K tile in shared memory: warp gw of
+            // the group sums the squares of columns [32 gw, 32 gw + 32), a lane taking one 16-byte
+            // unit (8 columns) of every eighth d-row (rows kr, kr + 8, ...; kr alternates between
+            // the two halves of the swizzle pattern so that a quarter-warp's eight loads hit eight
+            // distinct bank groups); a reduce-scatter over the eight lanes of a unit then leaves one
+            // column's sum per lane. The scales meet in this group's half of l_xchg (free until the
+            // maxima are exchanged); the group's two barriers per tile publish them and keep the
+            // next tile's from overwriting them early. All four warps of the group run every
+            // iteration and vote at the first barrier, so an abort leaves them together.
+            const int gw = sw & 3;
+            const int rs = lane >> 2;
+            const int kr = ((rs & 1) << 2) | (rs >> 1);
+            const uint32_t unit_phys = (static_cast<uint32_t>(((gw & 1) << 2) | (lane & 3))) ^ static_cast<uint32_t>(kr);
+            const int my_col = 32 * gw + 8 * (lane & 3) + ((((lane >> 4) & 1) << 2) | (((lane >> 3) & 1) << 1) | ((lane >> 2) & 1));
+            float *cs_tile = l_xchg + g * kBlockM;
+            // Barrier ids stay compile-time constants (one branch per group).
+            auto group_barrier_and = [&](bool pred) {
+                return g == 0 ? ptx::named_barrier_and(kGroupBarrier0, kGroupWarps * 32, pred)
+                              : ptx::named_barrier_and(kGroupBarrier0 + 1, kGroupWarps * 32, pred);
+            };
+            for (; u < T1; u += 2) {
+                const int s = u % STAGES;
+                bool w_ok = ok && warp_wait(bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s) &&
+                            warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);
+                if (w_ok) {
+                    const uint8_t *kp = smem + C::kQBytes + s * C::kStageBytes + (gw >> 1) * (D * 128) + kr * 128 +
+                                        (unit_phys << 4);
+                    float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                if (warp_rows) {
-                    uint32_t r0[32], r1[32];
-                    const uint32_t s_addr = tmem + lane_addr + g * kBlockN + half * 64;
-                    ptx::tmem_ld_32x32b_x32(s_addr, r0);
-                    ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
-                    ptx::tmem_ld_wait(r0);
-                    ptx::tmem_ld_wait(r1);
-                    const int nv = n_valid - half * 64;
-                    if constexpr (kQk) {
-                        const float *cs = col_scale + static_cast<size_t>(u) * kBlockN + half * 64;
+                    for (int k = 0; k < D / 8; ++k)  // d-row kr + 8k
+                        sum_sq_cols(*reinterpret_cast<const uint4 *>(kp + k * 1024), sq);
+                    const float c = __frsqrt_rn(reduce_scatter8(sq, lane) * (1.f / D) + kQkNormEps);
+                    cs_tile[my_col] = c;
+                    if ((t_begin + u) * kBlockN + my_col < p.N)
+                        col_scale[static_cast<size_t>(u) * kBlockN + my_col] = c;
+                }
+                w_ok = group_barrier_and(w_ok);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                // The group is done with the K tile (the S product that read it has completed).
+                if (gw == 0 && lane == 0)
+                    ptx::mbar_arrive(bar(BI::kKvEmpty + s));
+                ptx::tc_fence_after();
+                const int n_valid = p.N - (t_begin + u) * kBlockN;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (warp_rows) {
+                        uint32_t r0[32], r1[32];
+                        const uint32_t s_addr = tmem + lane_addr + g * kBlockN + half * 64;
+                        ptx::tmem_ld_32x32b_x32(s_addr, r0);
+                        ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
+                        ptx::tmem_ld_wait(r0);
+                        ptx::tmem_ld_wait(r1);
+                        const int nv = n_valid - half * 64;
+                        const float *cs = cs_tile + half * 64;
                         if (nv >= 64) {
                             m_row = max_slice_scaled<false>(r0, 0, nv, m_row, cs);
                             m_row = max_slice_scaled<false>(r1, 32, nv, m_row, cs + 32);
@@ -582,19 +679,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                             m_row = max_slice_scaled<true>(r0, 0, nv, m_row, cs);
                             m_row = max_slice_scaled<true>(r1, 32, nv, m_row, cs + 32);
                         }
-                    } else if (nv >= 64) {
-                        m_row = max_slice<false>(r0, 0, nv, m_row);
-                        m_row = max_slice<false>(r1, 32, nv, m_row);
-                    } else {
-                        m_row = max_slice<true>(r0, 0, nv, m_row);
-                        m_row = max_slice<true>(r1, 32, nv, m_row);
                     }
                 }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bar(BI::kSEmpty + g));
+                group_barrier_and(true);
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(bar(BI::kSEmpty + g));
+        } else {
+            for (; ok && u < T1; u += 2) {
+                if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int n_valid = p.N - (t_begin + u) * kBlockN;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (warp_rows) {
+                        uint32_t r0[32], r1[32];
+                        const uint32_t s_addr = tmem + lane_addr + g * kBlockN + half * 64;
+                        ptx::tmem_ld_32x32b_x32(s_addr, r0);
+                        ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
+                        ptx::tmem_ld_wait(r0);
+                        ptx::tmem_ld_wait(r1);
+                        const int nv = n_valid - half * 64;
+                        if (nv >= 64) {
+                            m_row = max_slice<false>(r0, 0, nv, m_row);
+                            m_row = max_slice<false>(r1, 32, nv, m_row);
+                        } else {
+                            m_row = max_slice<true>(r0, 0, nv, m_row);
+                            m_row = max_slice<true>(r1, 32, nv, m_row);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bar(BI::kSEmpty + g));
+            }
         }
         // The two groups' maxima meet in shared memory (both reach both barriers, on the
         // unwinding path too): m is the row's maximum over the split, and every exponential of
@@ -853,74 +977,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-// QK-norm scales (the graph's Q = rms_norm(Q), K = rms_norm(K) over the head dimension, applied
-// by kernel 1 as scales of the scores): col_scale[b, n] = 1/sqrt(mean_k K[b,k,n]^2 + eps) and
-// row_scale[b, m] = 1/sqrt(mean_k Q[b,m,k]^2 + eps), sums of squares in fp32.
-// Blocks [0, key_blocks) take 32 consecutive key vectors each: warp w sums rows
-// [w D/8, (w+1) D/8) of every column (a coalesced 64-byte read per row, all rows of a warp in
-// flight together), and the eight partial sums meet in shared memory in a fixed order. The
-// remaining blocks take 256 query rows each, one per thread.
-template <int D>
-__global__ void __launch_bounds__(256)
-    mg_qknorm_scales(const __half *__restrict__ Q, const __half *__restrict__ K, float *__restrict__ col_scale,
-                     float *__restrict__ row_scale, int B, int M, int N)
-{
-    constexpr int kRowsPerWarp = D / 8;
-    __shared__ float part[8][32];
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
-    const long long keys = static_cast<long long>(B) * N;
-    const long long key_blocks = (keys + 31) / 32;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    if (blockIdx.x < key_blocks) {
-        const long long i = static_cast<long long>(blockIdx.x) * 32 + lane;  // key index b*N + n
-        float ss = 0.f;
-        if (i < keys) {
-            const int b = static_cast<int>(i / N);
-            const int n = static_cast<int>(i % N);
-            const __half *k = K + (static_cast<size_t>(b) * D + static_cast<size_t>(warp) * kRowsPerWarp) * N + n;
-            float x[kRowsPerWarp];
-#pragma unroll
-            for (int c = 0; c < kRowsPerWarp; ++c)
-                x[c] = __half2float(k[static_cast<size_t>(c) * N]);
-#pragma unroll
-            for (int c = 0; c < kRowsPerWarp; ++c)
-                ss = fmaf(x[c], x[c], ss);
-        }
-        part[warp][lane] = ss;
-        __syncthreads();
-        if (warp == 0 && i < keys) {
-            float t = 0.f;
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-                t += part[w][lane];
-            col_scale[i] = __frsqrt_rn(t * (1.f / D) + kQkNormEps);
-        }
-    } else {
-        const long long r = (blockIdx.x - key_blocks) * 256 + threadIdx.x;
-        if (r < static_cast<long long>(B) * M) {
-            const uint4 *q = reinterpret_cast<const uint4 *>(Q + static_cast<size_t>(r) * D);
-            uint4 w[D / 8];
-#pragma unroll
-            for (int u = 0; u < D / 8; ++u)
-                w[u] = q[u];
-            float ss = 0.f;
-#pragma unroll
-            for (int u = 0; u < D / 8; ++u) {
-                const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[h]));
-                    ss = fmaf(f.x, f.x, ss);
-                    ss = fmaf(f.y, f.y, ss);
-                }
-            }
-            row_scale[r] = __frsqrt_rn(ss * (1.f / D) + kQkNormEps);
-        }
     }
 }
 

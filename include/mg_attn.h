@@ -77,11 +77,13 @@ typedef enum {
 #define MG_FLAG_QK_NORM 0x10       /* QK-norm attention (Mirage documentation, tutorials/attention-with-kv-norm):
                                       Q = rms_norm(Q), K = rms_norm(K) before the graph, each query row and
                                       each key vector K[b,:,n] normalised over d: x / sqrt(mean(x^2) + eps),
-                                      eps = MG_QKNORM_EPS, no weight. A small kernel computes the scales
-                                      1/rms of every key vector and query row (fp32, in the plan's
-                                      workspace); the fused kernel applies them to the scores in fp32, so
-                                      Q and K stay the fp16 MMA operands. Normalised scores reach +-d, past
-                                      the fp16 range of exp, so the flag implies MG_FLAG_SAFE_SOFTMAX. */
+                                      eps = MG_QKNORM_EPS, no weight. The fused kernel computes the scales
+                                      1/rms in fp32 (a query row's from the Q tile it holds, a key vector's
+                                      in the row-maximum pass from the K tile it streams, kept in the plan's
+                                      workspace for the main pass) and applies them to the scores in fp32,
+                                      so Q and K stay the fp16 MMA operands and K is read twice, as without
+                                      the flag. Normalised scores reach +-d, past the fp16 range of exp, so
+                                      the flag implies MG_FLAG_SAFE_SOFTMAX. */
 #define MG_QKNORM_EPS 1e-6
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and

@@ -134,19 +134,19 @@ def test_query_safe_softmax_workspace():
 
 
 def test_query_qk_norm_plan():
-    # QK-norm adds its scale kernel (one more launch) and the scales to the workspace: B*N key
-    # scales, 128 spare floats and B*M query scales; as it implies the max-subtracted evaluation,
-    # also one row maximum per split and row. Shared memory and stages are unchanged.
+    # QK-norm computes its scales inside the fused kernel (no extra launch) and keeps the key
+    # scales in the workspace: B*N of them and 128 spare floats; as it implies the max-subtracted
+    # evaluation, also one row maximum per split and row. Shared memory and stages are unchanged.
     plain = mg.mg_attn_query(2, 256, 4096, 64, 152)
     qk = mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_QK_NORM)
     assert qk["smem_bytes"] == plain["smem_bytes"] and qk["stages"] == 6
-    assert qk["kernels_per_run"] == plain["kernels_per_run"] + 1
-    assert qk["workspace_bytes"] == plain["workspace_bytes"] + 256 + (2 * 4096 + 128 + 2 * 256) * 4
+    assert qk["kernels_per_run"] == plain["kernels_per_run"]
+    assert qk["workspace_bytes"] == plain["workspace_bytes"] + 256 + (2 * 4096 + 128) * 4
     assert mg.mg_attn_query(2, 256, 4096, 128, 152, flags=mg.MG_FLAG_QK_NORM)["stages"] == 3
     B, M, N, d = 2, 256, 65536, 64
     a = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_QK_NORM)
     b = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX)
-    assert a["workspace_bytes"] == b["workspace_bytes"] + 256 + (B * N + 128 + B * M) * 4
+    assert a["workspace_bytes"] == b["workspace_bytes"] + 256 + (B * N + 128) * 4
     assert b["workspace_bytes"] == 256 + b["n_split"] * B * M * (d + 2) * 4
 
 
