@@ -637,8 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (; u < T1; u += 2) {
                 const int s = u % STAGES;
-                bool w_ok = ok && warp_wait(bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s) &&
-                            warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);
+                // The sums need only the K tile; they run while the tensor core computes S.
+                bool w_ok = ok && warp_wait(bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s);
                 if (w_ok) {
                     const uint8_t *kp = smem + C::kQBytes + s * C::kStageBytes + (gw >> 1) * (D * 128) + kr * 128 +
                                         (unit_phys << 4);
@@ -651,6 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if ((t_begin + u) * kBlockN + my_col < p.N)
                         col_scale[static_cast<size_t>(u) * kBlockN + my_col] = c;
                 }
+                w_ok = w_ok && warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);
                 w_ok = group_barrier_and(w_ok);
                 if (!w_ok) {
                     ok = false;
