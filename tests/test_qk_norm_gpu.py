@@ -66,7 +66,7 @@ def test_workloads(name):
     (3, 129, 136, 64, 0, 0), (2, 300, 1000, 64, 3, 0), (2, 300, 1000, 64, 3, mg.MG_FLAG_NO_CLUSTER),
     (1, 127, 4104, 128, 0, 0), (4, 64, 6216, 64, 7, 0), (1, 513, 256, 128, 2, 0), (2, 17, 65544, 64, 0, 0),
     (7, 3, 1024, 128, 8, mg.MG_FLAG_NO_CLUSTER), (1, 128, 128, 64, 1, 0), (2, 200, 2056, 64, 1, 0),
-    (1, 1, 8, 128, 0, 0), (2, 64, 1024, 128, 1, 0)])
+    (1, 1, 8, 128, 0, 0), (2, 64, 1024, 128, 1, 0), (16, 8, 4096, 128, 9, mg.MG_FLAG_NO_CLUSTER)])
 def test_shapes_and_combines(B, M, N, d, n_split, flags):
     q, k, v = inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=11 * B + M + N)
     O, plan = run_gpu(q, k, v, n_split=n_split, flags=QK | flags)

@@ -61,7 +61,7 @@ def test_workloads(name):
     (3, 129, 136, 64, 0, 0), (2, 300, 1000, 64, 3, 0), (2, 300, 1000, 64, 3, mg.MG_FLAG_NO_CLUSTER),
     (1, 127, 4104, 128, 0, 0), (4, 64, 6216, 64, 7, 0), (1, 513, 256, 128, 2, 0), (2, 17, 65544, 64, 0, 0),
     (7, 3, 1024, 128, 8, mg.MG_FLAG_NO_CLUSTER), (1, 128, 128, 64, 1, 0), (2, 200, 2056, 64, 1, 0),
-    (1, 256, 2048, 64, 5, 0), (1, 1, 8, 128, 0, 0)])
+    (1, 256, 2048, 64, 5, 0), (1, 1, 8, 128, 0, 0), (16, 8, 32768, 128, 9, mg.MG_FLAG_NO_CLUSTER)])
 def test_shapes_and_combines(B, M, N, d, n_split, flags):
     q, k, v = inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=7 * B + M + N)
     O, plan = run_gpu(q, k, v, n_split=n_split, flags=SAFE | flags)
@@ -109,13 +109,14 @@ def test_matches_plain_path_on_small_scores():
     assert_parity(b, ref, "safe")
 
 
-@pytest.mark.parametrize("flags", [SAFE, mg.MG_FLAG_QK_NORM, SAFE | mg.MG_FLAG_NO_CLUSTER])
-def test_bounded_wait_in_variants(flags):
+@pytest.mark.parametrize("flags,n_split", [(SAFE, 0), (mg.MG_FLAG_QK_NORM, 0), (SAFE | mg.MG_FLAG_NO_CLUSTER, 0),
+                                           (mg.MG_FLAG_QK_NORM | mg.MG_FLAG_NO_CLUSTER, 4)])
+def test_bounded_wait_in_variants(flags, n_split):
     # The load warp waits on a barrier nothing arrives on; every role of the variant (row-maximum
     # pass, maximum exchange, cluster or second-kernel combine) unwinds within the bound and the
     # context stays usable.
     q, k, v, _ = inputs.make_config("gqa")
-    plan = mg.Plan(2, 256, 4096, 64, flags=flags | mg.MG_FLAG_INJECT_TIMEOUT, timeout_ns=2_000_000)
+    plan = mg.Plan(2, 256, 4096, 64, n_split=n_split, flags=flags | mg.MG_FLAG_INJECT_TIMEOUT, timeout_ns=2_000_000)
     O = torch.zeros((2, 256, 64), dtype=torch.float16, device="cuda")
     plan.run(q.cuda(), k.cuda(), v.cuda(), O)
     assert plan.status() == mg.MG_ERR_TIMEOUT
