@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using BI = Bars<STAGES, kPBuffers>;
     static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
-    static_assert((128 * (D + 4) + 2 * 128) * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
+    static_assert(128 * (D + 8) * 2 + 2 * 128 * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -820,11 +820,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (o_ready) {
             ptx::tc_fence_after();
             // The K/V ring is idle (every PV has completed): stage this CTA's output there. For the
-            // on-chip combine: fp32 rows of d + 4 floats (the pad keeps 8 consecutive rows on distinct
-            // banks) and the row sums after them, read by the cluster's CTAs at teardown. Otherwise
-            // the 128-byte-swizzled layout the output tensor maps expect, then a TMA store.
+            // on-chip combine: the normalised partial O_j / l_j as fp16 rows of d + 8 halves (the
+            // pad keeps 8 consecutive rows on distinct banks), then the fp32 row sums l_j and
+            // maxima m_j, read by the cluster's CTAs at teardown. The normalised values are convex
+            // combinations of V rows, so fp16 holds them to half an ulp of max |V|, and the
+            // exchange moves half the bytes of fp32 numerators. Otherwise the 128-byte-swizzled
+            // layout the output tensor maps expect, then a TMA store.
             const uint32_t stage = sStage0;
-            float *stage_f = reinterpret_cast<float *>(smem + C::kQBytes);
+            __half *stage_h = reinterpret_cast<__half *>(smem + C::kQBytes);
+            float *stage_lm = reinterpret_cast<float *>(smem + C::kQBytes + kBlockM * (D + 8) * 2);
             if (warp_rows) {
 #pragma unroll
                 for (int c = 0; c < C::kHalfCols / 32; ++c) {
@@ -833,11 +837,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, r);
                     ptx::tmem_ld_wait(r);
                     if (p.cluster_reduce) {
-                        float4 *dst = reinterpret_cast<float4 *>(stage_f + row * (D + 4) + col);
+                        // The split's normalised partial O_j / l_j in fp16 (every value a convex
+                        // combination of V rows), rows of d + 8 halves.
+                        // One correctly rounded reciprocal, then products (l = 0 only if every
+                        // exponential of the split underflowed; its partial is then 0).
+                        const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
+                        uint4 *dst = reinterpret_cast<uint4 *>(stage_h + row * (D + 8) + col);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h)
+                                w4[h] = ptx::pack_half2(__uint_as_float(r[8 * q + 2 * h]) * inv,
+                                                        __uint_as_float(r[8 * q + 2 * h + 1]) * inv);
+                            dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
                     } else if (p.n_split == 1) {
                         // fp16 O/l: chunk col/64 of a {64, 128} fp16 box; this slice is units (col%64)/8 .. +3.
                         const uint32_t chunk = stage + (col / 64) * C::kChunkRows128;
@@ -865,8 +879,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (p.cluster_reduce) {
                 if (g == 0) {
-                    stage_f[kBlockM * (D + 4) + row] = l;
-                    stage_f[kBlockM * (D + 4) + kBlockM + row] = m;
+                    stage_lm[row] = l;
+                    stage_lm[kBlockM + row] = m;
                 }
             } else {
                 if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
@@ -895,30 +909,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // On-chip combine of the split partials: after the first cluster barrier every CTA's staged
-    // (O_j, l_j) is visible; CTA rank j sums rows [128 j / n, 128 (j+1) / n) of its row tile over
-    // all n ranks in rank order (reproducible), divides and writes fp16 O. The second barrier
+    // (O_j / l_j, l_j, m_j) is visible; CTA rank j forms rows [128 j / n, 128 (j+1) / n) of its row
+    // tile as sum_r c_r (O_r / l_r) / sum_r c_r with c_r = l_r (times exp(m_r - max m) in the
+    // max-subtracted variant), over all n ranks in rank order (reproducible), and writes fp16 O. The second barrier
     // keeps each CTA's shared memory alive until the others have read it. Every thread of every
     // CTA reaches both barriers, on the unwinding path too.
     __syncwarp();
     if (p.cluster_reduce) {
         ptx::cluster_sync();
         if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
-            constexpr int G = D / 4;  // float4 groups per row
+            constexpr int G = D / 8;  // 16-byte groups (8 fp16 columns) per row
             const int n = p.n_split;
             const int lo = j * kBlockM / n;
             const int hi = (j + 1) * kBlockM / n;
             const uint32_t st = ptx::smem_u32(smem + C::kQBytes);
-            const uint32_t ls = st + kBlockM * (D + 4) * 4;
+            const uint32_t ls = st + kBlockM * (D + 8) * 2;
             const uint32_t ms = ls + kBlockM * 4;
             for (int it = threadIdx.x - 64; it < (hi - lo) * G; it += kSoftmaxThreads) {
                 const int rr = lo + it / G;
                 const int g = it % G;
                 if (m0 + rr >= p.M)
                     continue;
-                const uint32_t off = static_cast<uint32_t>((rr * (D + 4) + g * 4) * 4);
-                // Max-subtracted variant: rank r's partial was taken relative to its own row
-                // maximum m_r, so it enters the sum with weight exp(m_r - max_r m_r) (1 for the
-                // rank that holds the maximum); otherwise every weight is 1.
+                const uint32_t off = static_cast<uint32_t>((rr * (D + 8) + g * 8) * 2);
+                // Rank r's normalised partial enters with weight c_r = l_r (times exp(m_r - max_r m_r)
+                // in the max-subtracted variant, where l_r was taken relative to m_r).
                 float wt[kMaxClusterRanks];
 #pragma unroll
                 for (int r = 0; r < kMaxClusterRanks; ++r)
@@ -949,22 +963,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lv[r] = ptx::ld_cluster_f32(ptx::map_to_rank(ls + rr * 4, r));
                     }
                 }
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 float lsum = 0.f;
 #pragma unroll
                 for (int r = 0; r < kMaxClusterRanks; ++r) {
                     if (r < n) {
-                        a.x += wt[r] * v[r].x;
-                        a.y += wt[r] * v[r].y;
-                        a.z += wt[r] * v[r].z;
-                        a.w += wt[r] * v[r].w;
-                        lsum += wt[r] * lv[r];
+                        const float c = wt[r] * lv[r];
+                        const uint32_t words[4] = {__float_as_uint(v[r].x), __float_as_uint(v[r].y),
+                                                   __float_as_uint(v[r].z), __float_as_uint(v[r].w)};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[h]));
+                            a[2 * h] = fmaf(c, f.x, a[2 * h]);
+                            a[2 * h + 1] = fmaf(c, f.y, a[2 * h + 1]);
+                        }
+                        lsum += c;
                     }
                 }
-                uint2 w;
-                w.x = ptx::pack_half2(__fdiv_rn(a.x, lsum), __fdiv_rn(a.y, lsum));
-                w.y = ptx::pack_half2(__fdiv_rn(a.z, lsum), __fdiv_rn(a.w, lsum));
-                *reinterpret_cast<uint2 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + g * 4) = w;
+                uint4 w;
+                w.x = ptx::pack_half2(__fdiv_rn(a[0], lsum), __fdiv_rn(a[1], lsum));
+                w.y = ptx::pack_half2(__fdiv_rn(a[2], lsum), __fdiv_rn(a[3], lsum));
+                w.z = ptx::pack_half2(__fdiv_rn(a[4], lsum), __fdiv_rn(a[5], lsum));
+                w.w = ptx::pack_half2(__fdiv_rn(a[6], lsum), __fdiv_rn(a[7], lsum));
+                *reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + g * 8) = w;
             }
         }
         // Only "every CTA has finished reading the others' shared memory" is needed here; a

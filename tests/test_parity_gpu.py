@@ -109,6 +109,29 @@ def test_cluster_combine_matches_second_kernel(B, M, N, d, n_split):
     assert_parity(O_k2, ref, "second kernel")
 
 
+@pytest.mark.parametrize("n_split,flags", [(2, 0), (16, 0), (16, mg.MG_FLAG_SAFE_SOFTMAX)])
+def test_cluster_combine_of_cancelling_splits(n_split, flags):
+    # Two splits each dominated by one V row, of opposite signs: O is the small difference of two
+    # large partials. The on-chip exchange carries each split's O_j / l_j in fp16, so this is
+    # where it loses the most (half an ulp of |V| ~ 4 per partial, against a bound of 2e-3).
+    B, M, N, d = 1, 3, 2048, 64
+    q = torch.zeros((B, M, d))
+    q[0, :, 0] = torch.tensor([1.0, 1.25, 1.5])
+    k = torch.zeros((B, d, N))
+    k[0, 0, :] = -5.0
+    k[0, 0, 0] = 5.0      # split 0
+    k[0, 0, N // 2] = 5.0  # split n_split / 2
+    v = torch.randn((B, N, d), generator=torch.Generator().manual_seed(9)) * 0.01
+    v[0, 0, :] = 3.9
+    v[0, N // 2, :] = -3.7
+    q, k, v = q.half(), k.half(), v.half()
+    ref = oracle.attention(q, k, v)
+    assert np.abs(ref).max() < 0.2  # the partials (~3.8) nearly cancel
+    O, plan = run_gpu(q, k, v, n_split=n_split, flags=flags)
+    assert plan.info["cluster_ctas"] == n_split
+    assert_parity(O, ref, f"cancelling splits, cluster {n_split}, flags {flags}")
+
+
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
     # Scores 0 everywhere -> every weight is exp(0)=1: any column past N that leaked into the row
     # sum (zero-filled K gives exp(0)=1 too) would pull the mean toward 0.
