@@ -14,6 +14,7 @@
 #include <new>
 
 #include "mg_attn_kernels.cuh"
+#include "mg_combine.cuh"
 
 namespace {
 
@@ -104,9 +105,24 @@ FwdKernel fwd_kernel(int64_t d, int stages, int flags)
 
 using CombineKernel = void (*)(const float *, const float *, const float *, __half *, int, int);
 
-CombineKernel combine_kernel(int64_t d)
+template <int D>
+CombineKernel combine_kernel_d(int n_split)
 {
-    return d == 64 ? mg::mg_attn_combine<64> : mg::mg_attn_combine<128>;
+    if (n_split <= mg::CombineCfg<D>::kMaxSplits)
+        return mg::mg_attn_combine<D>;
+    return mg::WideCombineCfg<D>::batch(n_split) == 4 ? mg::mg_attn_combine_wide<D, 4> : mg::mg_attn_combine_wide<D, 8>;
+}
+
+template <int D>
+int combine_rows_per_cta(int n_split)
+{
+    return n_split <= mg::CombineCfg<D>::kMaxSplits ? mg::CombineCfg<D>::kRows : mg::WideCombineCfg<D>::kRows;
+}
+
+// The second kernel for a head dim and split count (its load batch depends on the split count).
+CombineKernel combine_kernel(int64_t d, int n_split)
+{
+    return d == 64 ? combine_kernel_d<64>(n_split) : combine_kernel_d<128>(n_split);
 }
 
 // Validation and tiling decisions; touches no GPU.
@@ -448,7 +464,7 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     p->flags = flags;
     p->timeout_ns = timeout_ns;
     p->fwd = fwd;
-    p->combine = combine_kernel(d);
+    p->combine = combine_kernel(d, info.n_split);
     e = cudaMalloc(&p->workspace, static_cast<size_t>(info.workspace_bytes));
     if (e != cudaSuccess) {
         delete p;
@@ -583,7 +599,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
         const float *wl = plan->ws_l;
         const float *wm = plan->ws_m;
         __half *out = static_cast<__half *>(O);
-        const int rows_per_cta = d == 64 ? mg::CombineCfg<64>::kRows : mg::CombineCfg<128>::kRows;
+        const int rows_per_cta = d == 64 ? combine_rows_per_cta<64>(n_split) : combine_rows_per_cta<128>(n_split);
         cudaLaunchConfig_t cc = cfg;
         cc.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), 1, 1);
         cc.blockDim = dim3(256, 1, 1);
@@ -803,7 +819,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         const float *wo = ws_o;
         const float *wl = prm.ws_l;
         __half *out = static_cast<__half *>(O);
-        const int rows_per_cta = d == 64 ? mg::CombineCfg<64>::kRows : mg::CombineCfg<128>::kRows;
+        const int rows_per_cta = d == 64 ? combine_rows_per_cta<64>(n_split) : combine_rows_per_cta<128>(n_split);
         cudaLaunchConfig_t cc = cfg;
         cc.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), 1, 1);
         cc.blockDim = dim3(256, 1, 1);
@@ -811,7 +827,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         cc.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, true, 0));
         const float *wm = nullptr;
         void *cargs[6] = {&wo, &wl, &wm, &out, &rows, &n_split};
-        e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(combine_kernel(d)), cargs);
+        e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(combine_kernel(d, n_split)), cargs);
         if (e != cudaSuccess)
             return cuda_fail(e, "launch mg_attn_combine");
     }

@@ -1,4 +1,4 @@
-// mg_attn_kernels.cuh -- the two device kernels of the exp-normalised GQA graph.
+// mg_attn_kernels.cuh -- the fused device kernel of the exp-normalised GQA graph.
 //
 // Graph (Mirage documentation, tutorials/group-query-attention, "Define GQA Computation
 // Graph"): A = matmul(Q,K); E = exp(A); S = reduction(E,2); D = div(E,S); O = matmul(D,V).
@@ -17,7 +17,7 @@
 // shared memory, fixed rank order). Otherwise each writes the fp32 partial numerator O_j and row
 // sum l_j to the workspace (TMA store) for kernel 2.
 //
-// Kernel 2, mg_attn_combine: O = (sum_j O_j) / (sum_j l_j) -> fp16, the second threadblock
+// Kernel 2 (mg_combine.cuh): O = (sum_j O_j) / (sum_j l_j) -> fp16, the second threadblock
 // graph of the "attention" search configuration (blog, section 4.3). No max-subtraction
 // means the partials combine by plain sums (weights exp(m_j - max m) in the max-subtracted
 // variant).
@@ -999,83 +999,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-// O[r, c] = (sum_j ws_o[j, r, c]) / (sum_j ws_l[j, r]) -> fp16, r = b*M + m.
-// A CTA of 256 threads covers kRows rows. Thread (row, part, g) sums float4 column group g of its
-// row over the splits j = part, part + kParts, ... (independent loads, all in flight together);
-// the kParts partial sums then meet in shared memory in a fixed order, so the result is
-// reproducible run to run.
-template <int D>
-struct CombineCfg {
-    static constexpr int kGroups = D / 4;                  // float4 groups per row
-    static constexpr int kParts = 4;                       // split-index residues per row
-    static constexpr int kRows = 256 / (kGroups * kParts); // rows per CTA: 4 (d=64) or 2 (d=128)
-};
-
-template <int D>
-__global__ void __launch_bounds__(256)
-    mg_attn_combine(const float *__restrict__ ws_o, const float *__restrict__ ws_l, const float *__restrict__ ws_m,
-                    __half *__restrict__ O, int rows, int n_split)
-{
-    using CC = CombineCfg<D>;
-    __shared__ float4 part_o[CC::kParts][CC::kRows][CC::kGroups];
-    __shared__ float part_l[CC::kParts][CC::kRows];
-
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
-
-    const int g = threadIdx.x % CC::kGroups;
-    const int part = (threadIdx.x / CC::kGroups) % CC::kParts;
-    const int rl = threadIdx.x / (CC::kGroups * CC::kParts);
-    const int r = blockIdx.x * CC::kRows + rl;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float l = 0.f;
-    if (r < rows) {
-        // Max-subtracted variant (ws_m given): split j's partial is relative to its row maximum
-        // m_j and enters with weight exp(m_j - max_j m_j); otherwise every weight is 1.
-        float mmax = 0.f;
-        if (ws_m) {
-            mmax = -INFINITY;
-            for (int j = 0; j < n_split; ++j)
-                mmax = fmaxf(mmax, ws_m[static_cast<size_t>(j) * rows + r]);
-        }
-        const float4 *src = reinterpret_cast<const float4 *>(ws_o) + static_cast<size_t>(r) * CC::kGroups + g;
-        const size_t split_stride = static_cast<size_t>(rows) * CC::kGroups;
-#pragma unroll 4
-        for (int j = part; j < n_split; j += CC::kParts) {
-            const float4 a = src[static_cast<size_t>(j) * split_stride];
-            const float wt = ws_m ? ptx::ex2_approx((ws_m[static_cast<size_t>(j) * rows + r] - mmax) * ptx::kLog2e)
-                                  : 1.f;
-            acc.x += wt * a.x;
-            acc.y += wt * a.y;
-            acc.z += wt * a.z;
-            acc.w += wt * a.w;
-            if (g == 0)
-                l += wt * ws_l[static_cast<size_t>(j) * rows + r];
-        }
-    }
-    part_o[part][rl][g] = acc;
-    if (g == 0)
-        part_l[part][rl] = l;
-    __syncthreads();
-    if (part == 0 && r < rows) {
-        float4 s = part_o[0][rl][g];
-        float ls = part_l[0][rl];
-#pragma unroll
-        for (int q = 1; q < CC::kParts; ++q) {
-            const float4 t = part_o[q][rl][g];
-            s.x += t.x;
-            s.y += t.y;
-            s.z += t.z;
-            s.w += t.w;
-            ls += part_l[q][rl];
-        }
-        uint2 w;
-        w.x = ptx::pack_half2(__fdiv_rn(s.x, ls), __fdiv_rn(s.y, ls));
-        w.y = ptx::pack_half2(__fdiv_rn(s.z, ls), __fdiv_rn(s.w, ls));
-        *reinterpret_cast<uint2 *>(O + static_cast<size_t>(r) * D + g * 4) = w;
     }
 }
 
