@@ -105,7 +105,7 @@ typedef struct {
     int32_t block_n;         /* columns of K per pipeline step (128) */
     int32_t m_tiles;         /* B * ceil(M / block_m) */
     int32_t n_tiles;         /* ceil(N / block_n) */
-    int32_t n_split;         /* CTAs per row tile; each takes a contiguous run of column tiles */
+    int32_t n_split;         /* CTAs per row tile; CTA j takes the column tiles j, j + n_split, ... */
     int32_t stages;          /* K/V pipeline depth */
     int32_t threads;         /* threads per CTA of the fused kernel */
     int32_t grid_ctas;       /* m_tiles * n_split */

@@ -73,9 +73,9 @@ def test_status_strings_and_version(lib):
     assert lib.mg_attn_version() == 10000
 
 
-def tile_ranges(n_tiles, n_split):
-    # The fused kernel's split j owns tiles [j*T/S, (j+1)*T/S).
-    return [(j * n_tiles // n_split, (j + 1) * n_tiles // n_split) for j in range(n_split)]
+def split_tiles(n_tiles, n_split):
+    # The fused kernel's split j owns the column tiles j, j + n_split, j + 2 n_split, ...
+    return [list(range(j, n_tiles, n_split)) for j in range(n_split)]
 
 
 @pytest.mark.parametrize("B,M,N,d", [(2, 64, 1024, 64), (2, 256, 4096, 64), (16, 256, 4096, 64),
@@ -97,9 +97,12 @@ def test_query_decisions(B, M, N, d):
         assert cluster == info["n_split"]  # small splits combine on chip
     assert info["kernels_per_run"] == (2 if info["n_split"] > 1 and cluster == 0 else 1)
     assert info["smem_bytes"] <= 232448
-    rng = tile_ranges(n_tiles, info["n_split"])
-    assert rng[0][0] == 0 and rng[-1][1] == n_tiles
-    assert all(a < b for a, b in rng) and all(rng[i][1] == rng[i + 1][0] for i in range(len(rng) - 1))
+    # Every column tile belongs to exactly one split, every split has one (n_split <= n_tiles),
+    # and the splits' counts differ by at most one.
+    own = split_tiles(n_tiles, info["n_split"])
+    assert sorted(t for ts in own for t in ts) == list(range(n_tiles))
+    counts = [len(ts) for ts in own]
+    assert min(counts) >= 1 and max(counts) - min(counts) <= 1
     ws = 256 + (info["n_split"] * B * M * (d + 1) * 4 if info["n_split"] > 1 and cluster == 0 else 0)
     assert info["workspace_bytes"] == ws
 
