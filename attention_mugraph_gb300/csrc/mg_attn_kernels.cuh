@@ -153,8 +153,11 @@ __device__ __forceinline__ bool wait_bounded(const WaitCtx &w, uint32_t bar, uin
         return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
-        // Suspended rather than spinning: waiting warps leave the issue slots to working ones.
-        if (ptx::mbar_try_wait_sleep(bar, parity, 100000u))
+        // try_wait may suspend the thread for a hardware-chosen time while the phase is
+        // incomplete, so waiting warps leave the issue slots to working ones. Measured on GB300
+        // (µs per call): 1-2 % faster than with a 100 µs suspend-time hint (gqa 6.65 against
+        // 6.77), and a test_wait spin is slower than both (it competes for issue slots).
+        if (ptx::mbar_try_wait(bar, parity))
             return true;
         if (*w.abort_flag)
             return false;

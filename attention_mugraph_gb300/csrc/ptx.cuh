@@ -45,7 +45,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// True once the phase with the given parity has completed.
+// True once the phase with the given parity has completed; while it is incomplete the thread may
+// be suspended for a hardware-chosen time before the call returns false.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -69,21 +70,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// As mbar_try_wait, but the thread may be suspended (off the scheduler) for up to `hint_ns`
-// while the phase is incomplete, so waiting threads do not take issue slots from working warps.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
