@@ -202,7 +202,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->grid_ctas = static_cast<int32_t>(m_tiles * n_split);
     info->smem_bytes = static_cast<int32_t>(smem);
     info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
-    // The QK-norm variant runs its scale kernel first.
+    // The fused kernel writes O itself unless split partials go through the second kernel.
     info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
     // Split partials for the second kernel: numerators, row sums and (max-subtracted variant) row maxima.
@@ -210,7 +210,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     const int64_t partial_bytes =
         (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M * row_words) * 4 : 0;
     // QK-norm: key-vector scales (B*N floats, then 128 more that reads of a last tile past N may
-    // touch) and query-row scales (B*M floats), from a 256-byte boundary.
+    // touch), from a 256-byte boundary.
     const int64_t scale_bytes = qk_norm ? 256 + (B * N + 128) * 4 : 0;
     info->workspace_bytes = 256 + partial_bytes + scale_bytes;
     info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
