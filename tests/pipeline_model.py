@@ -1,0 +1,382 @@
+"""Protocol model of the fused kernel's mbarrier pipeline (mg_attn_fwd_partial), for CPU tests.
+
+The kernel's roles and every barrier operation they perform are restated here as Python
+coroutines, in the kernel's order: the TMA producer, the S-issuing warp, the P.V-issuing warp
+and the two groups of four softmax warps, for the graph as written, the max-subtracted variant
+(a row-maximum pass over K first) and the QK-norm variant (whose softmax warps also read the K
+tiles in that pass). Copies and tensor-core work complete asynchronously: a TMA copy at any
+later moment, the tensor pipe's operations in issue order, a commit once every operation issued
+before it has completed.
+
+A scheduler runs the roles under random interleavings and checks, at every step:
+
+* parity waits: an mbarrier wait passes only when the phase its caller means has just
+  completed. The hardware test compares the barrier's current phase bit with the parity, so a
+  wait on phase k while phase k-1 is still open passes early; a wait that falls two phases
+  behind never passes (reported as a deadlock);
+* data hazards: a copy lands in a K or V stage only when no operation still reads it; an MMA
+  reads K, V and P only once the step's data is there and writes an S buffer only when its
+  softmax group has finished reading it; the softmax warps read S only after its MMA and write
+  a P buffer only after the P.V product of three (d = 64) or two (d = 128) tiles earlier;
+  the epilogue reads O only after the last P.V product.
+
+The model is a restatement, not the kernel: a change to the kernel's barrier protocol has to
+be made here too. The mutations in tests/test_pipeline_protocol.py show that it catches the
+hazards it is meant to (for example, the P.V warp waiting for V before P in the two-pass
+variants).
+"""
+
+from __future__ import annotations
+
+import random
+
+PLAIN, SAFE, QKNORM = 0, 1, 2
+GROUP_WARPS = 4
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class Barrier:
+    """An mbarrier: arrival count, transaction bytes and the number of completed phases."""
+
+    def __init__(self, name: str, count: int):
+        self.name = name
+        self.count = count
+        self.pending = count
+        self.tx = 0
+        self.completed = 0  # completed phases; the open phase has index `completed`
+
+    def arrive(self, expect_tx: int = 0):
+        self.tx += expect_tx
+        self.pending -= 1
+        if self.pending < 0:
+            raise ProtocolError(f"{self.name}: more arrivals than its count in phase {self.completed}")
+        self._maybe_complete()
+
+    def complete_tx(self, nbytes: int):
+        self.tx -= nbytes
+        if self.tx < 0:
+            raise ProtocolError(f"{self.name}: transaction bytes below zero in phase {self.completed}")
+        self._maybe_complete()
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.completed += 1
+            self.pending = self.count
+
+    def test(self, parity: int) -> bool:
+        # What the hardware's parity test sees: the open phase's parity differs from `parity`.
+        return (self.completed & 1) != parity
+
+
+class Sim:
+    def __init__(self, T: int, stages: int, pbufs: int, variant: int, seed: int, mutations=()):
+        if T < 1 or stages < 2 or pbufs < 2:
+            raise ValueError("T >= 1, stages >= 2, pbufs >= 2")
+        self.T, self.S, self.P, self.var = T, stages, pbufs, variant
+        self.safe = variant != PLAIN
+        self.qk = variant == QKNORM
+        self.T1 = T if self.safe else 0
+        self.U = self.T1 + T
+        self.mut = set(mutations)
+        self.rng = random.Random(seed)
+        self.bars = {}
+
+        def mk(name, count):
+            self.bars[name] = Barrier(name, count)
+
+        mk("QFull", 1)
+        for s in range(stages):
+            mk(f"KFull{s}", 1)
+            mk(f"VFull{s}", 1)
+            mk(f"KvEmpty{s}", 1)
+        for g in range(2):
+            mk(f"SFull{g}", 1)
+            mk(f"SEmpty{g}", GROUP_WARPS)
+        for p in range(pbufs):
+            mk(f"PFull{p}", GROUP_WARPS)
+            mk(f"PEmpty{p}", 1)
+        mk("OFull", 1)
+        # Buffer contents (the step or tile held, None while undefined) and their live readers.
+        self.q_loaded = False
+        self.kst = [None] * stages
+        self.vst = [None] * stages
+        self.k_readers = [0] * stages
+        self.v_readers = [0] * stages
+        self.sbuf = [None, None]
+        self.s_readers = [0, 0]
+        self.s_pending_write = [False, False]
+        self.pbuf = [None] * pbufs          # tile whose P is complete in the buffer
+        self.pieces = [set() for _ in range(pbufs)]
+        self.p_tile_writing = [None] * pbufs
+        self.p_readers = [0] * pbufs
+        self.pv_done = 0
+        self.pv_issued = 0
+        self.tma = []                       # in-flight copies: (barrier, bytes, effect)
+        self.pipe = []                      # tensor pipe FIFO: ("mma", effect) or ("commit", barrier)
+        self.gbar = {}                      # named barriers: id -> {"gen": n, "arrived": set()}
+        self.gbar_wait = {}                 # actor -> (barrier id, generation it waits to end)
+        self.actors = {}
+        self._make_actors()
+
+    # ------------------------------------------------------------------ checks
+    def fail(self, msg):
+        raise ProtocolError(msg)
+
+    def wait(self, bar, parity, k, who):
+        return ("wait", bar, parity, k, who)
+
+    # ------------------------------------------------------------------ roles
+    def _producer(self):
+        S = self.S
+        yield ("do", lambda: self._tma_q())
+        for t in range(self.U):
+            s = t % S
+            rnd = t // S
+            if t >= S and "producer_no_kvempty_wait" not in self.mut:
+                yield self.wait(f"KvEmpty{s}", (rnd & 1) ^ 1, rnd - 1, f"producer step {t}")
+            yield ("do", lambda t=t, s=s: self._issue_step(t, s))
+        for u in range(max(self.U - S, 0), self.U):
+            yield self.wait(f"KvEmpty{u % S}", (u // S) & 1, u // S, f"producer tail {u}")
+
+    def _tma_q(self):
+        self.bars["QFull"].arrive(expect_tx=1)
+        self.tma.append(("QFull", 1, lambda: setattr(self, "q_loaded", True)))
+
+    def _issue_step(self, t, s):
+        if self.k_readers[s]:
+            self.fail(f"K stage {s} overwritten for step {t} while still read")
+        self.kst[s] = None
+        kb = self.bars[f"KFull{s}"]
+        kb.arrive(expect_tx=1)
+        self.tma.append((f"KFull{s}", 1, lambda: self.kst.__setitem__(s, t)))
+        vb = self.bars[f"VFull{s}"]
+        if t < self.T1:
+            vb.arrive()  # a row-maximum step loads no V
+        else:
+            if self.v_readers[s]:
+                self.fail(f"V stage {s} overwritten for step {t} while still read")
+            self.vst[s] = None
+            vb.arrive(expect_tx=1)
+            self.tma.append((f"VFull{s}", 1, lambda: self.vst.__setitem__(s, t)))
+
+    def _s_warp(self):
+        S = self.S
+        yield self.wait("QFull", 0, 0, "S warp Q")
+        for u in range(self.U):
+            s, sb = u % S, u & 1
+            yield self.wait(f"KFull{s}", (u // S) & 1, u // S, f"S warp K {u}")
+            if u >= 2 and "s_no_sempty_wait" not in self.mut:
+                yield self.wait(f"SEmpty{sb}", ((u >> 1) & 1) ^ 1, (u >> 1) - 1, f"S warp S buffer {u}")
+            yield ("do", lambda u=u, s=s, sb=sb: self._issue_s(u, s, sb))
+
+    def _issue_s(self, u, s, sb):
+        if not self.q_loaded:
+            self.fail(f"S MMA {u} issued before Q landed")
+        if self.kst[s] != u:
+            self.fail(f"S MMA {u} reads K stage {s} holding step {self.kst[s]}")
+        if self.s_readers[sb]:
+            self.fail(f"S MMA {u} writes S buffer {sb} while softmax warps read it")
+        self.k_readers[s] += 1
+        self.s_pending_write[sb] = True
+
+        def done():
+            self.k_readers[s] -= 1
+            self.sbuf[sb] = u
+            self.s_pending_write[sb] = False
+
+        self.pipe.append(("mma", done))
+        self.pipe.append(("commit", f"SFull{sb}"))
+        if not self.qk and u < self.T1:
+            self.pipe.append(("commit", f"KvEmpty{s}"))
+
+    def _pv_warp(self):
+        S, P = self.S, self.P
+        for v in range(self.T):
+            u = self.T1 + v
+            pb, s = v % P, u % S
+            w_p = self.wait(f"PFull{pb}", (v // P) & 1, v // P, f"PV warp P {v}")
+            w_v = self.wait(f"VFull{s}", (u // S) & 1, u // S, f"PV warp V {v}")
+            for w in ((w_v, w_p) if "pv_waits_v_first" in self.mut else (w_p, w_v)):
+                yield w
+            yield ("do", lambda v=v, u=u, pb=pb, s=s: self._issue_pv(v, u, pb, s))
+        for t in range(max(self.T - P, 0), self.T):
+            yield self.wait(f"PEmpty{t % P}", (t // P) & 1, t // P, f"PV warp tail {t}")
+
+    def _issue_pv(self, v, u, pb, s):
+        if self.pbuf[pb] != v:
+            self.fail(f"P.V MMA {v} reads P buffer {pb} holding tile {self.pbuf[pb]}")
+        if self.vst[s] != u:
+            self.fail(f"P.V MMA {v} reads V stage {s} holding step {self.vst[s]}")
+        self.p_readers[pb] += 1
+        self.v_readers[s] += 1
+        self.pv_issued += 1
+
+        def done():
+            self.p_readers[pb] -= 1
+            self.v_readers[s] -= 1
+            self.pv_done += 1
+
+        self.pipe.append(("mma", done))
+        self.pipe.append(("commit", f"KvEmpty{s}"))
+        self.pipe.append(("commit", f"PEmpty{pb}"))
+        if v == self.T - 1:
+            self.pipe.append(("commit", "OFull"))
+
+    def _softmax_warp(self, g, gw):
+        S, P = self.S, self.P
+        who = f"softmax g{g}w{gw}"
+        if self.qk:
+            yield self.wait("QFull", 0, 0, who + " Q")
+        # Row-maximum pass.
+        for u in range(g, self.T1, 2):
+            s = u % S
+            if self.qk:
+                yield self.wait(f"KFull{s}", (u // S) & 1, u // S, f"{who} K {u}")
+                yield ("do", lambda s=s, u=u: self._read_k(s, u, +1))
+                yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")
+                yield ("do", lambda s=s: self._read_k(s, None, -1))
+                if gw == 0 and "qk_kvempty_before_barrier" in self.mut:
+                    # Mutation: the stage is released before the other warps have read K.
+                    yield ("do", lambda s=s: self.bars[f"KvEmpty{s}"].arrive())
+                yield ("gbar", f"group{g}", GROUP_WARPS)
+                if gw == 0 and "qk_kvempty_before_barrier" not in self.mut:
+                    yield ("do", lambda s=s: self.bars[f"KvEmpty{s}"].arrive())
+                yield ("do", lambda u=u: self._read_s(g, u, +1))
+                yield ("do", lambda u=u: self._read_s(g, u, -1))
+                yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
+                yield ("gbar", f"group{g}", GROUP_WARPS)
+            else:
+                yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")
+                yield ("do", lambda u=u: self._read_s(g, u, +1))
+                yield ("do", lambda u=u: self._read_s(g, u, -1))
+                yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
+        if self.safe:
+            yield ("gbar", "softmax", 2 * GROUP_WARPS)
+            yield ("gbar", "softmax", 2 * GROUP_WARPS)
+        # Main pass.
+        start = self.T1 if (self.T1 % 2 == g) else self.T1 + 1
+        for u in range(start, self.U, 2):
+            t = u - self.T1
+            pb = t % P
+            yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")
+            yield ("do", lambda u=u: self._read_s(g, u, +1))            # half 0 loaded
+            if t >= P:
+                yield self.wait(f"PEmpty{pb}", ((t // P) & 1) ^ 1, t // P - 1, f"{who} P buffer {t}")
+            yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 0)))
+            yield ("do", lambda u=u: self._read_s(g, u, -1))            # half 1 loaded: S released
+            yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
+            yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 1)))
+            yield ("do", lambda pb=pb: self.bars[f"PFull{pb}"].arrive())
+        # Epilogue: every softmax warp waits for O, then all meet.
+        yield self.wait("OFull", 0, 0, f"{who} O")
+        yield ("gbar", "softmax", 2 * GROUP_WARPS)
+        yield ("do", lambda: self._read_o())
+
+    def _read_k(self, s, u, delta):
+        if delta > 0 and self.kst[s] != u:
+            self.fail(f"QK-norm softmax reads K stage {s} holding step {self.kst[s]}, expected {u}")
+        self.k_readers[s] += delta
+
+    def _read_s(self, g, u, delta):
+        if delta > 0 and (self.sbuf[g] != u or self.s_pending_write[g]):
+            self.fail(f"softmax group {g} reads S buffer holding step {self.sbuf[g]}, expected {u}")
+        self.s_readers[g] += delta
+
+    def _write_p(self, pb, t, piece):
+        if self.p_readers[pb]:
+            self.fail(f"P buffer {pb} written for tile {t} while a P.V MMA reads it")
+        if self.p_tile_writing[pb] != t:
+            if self.pbuf[pb] is not None and self.pv_done <= self.pbuf[pb]:
+                self.fail(f"P buffer {pb} overwritten for tile {t} before P.V of tile {self.pbuf[pb]}")
+            self.p_tile_writing[pb] = t
+            self.pieces[pb] = set()
+            self.pbuf[pb] = None
+        self.pieces[pb].add(piece)
+        if len(self.pieces[pb]) == 2 * GROUP_WARPS:
+            self.pbuf[pb] = t
+
+    def _read_o(self):
+        if self.pv_done != self.T:
+            self.fail(f"O read after {self.pv_done} of {self.T} P.V products")
+
+    def _make_actors(self):
+        self.actors["producer"] = self._producer()
+        self.actors["s_warp"] = self._s_warp()
+        self.actors["pv_warp"] = self._pv_warp()
+        for g in range(2):
+            for gw in range(GROUP_WARPS):
+                self.actors[f"softmax{g}.{gw}"] = self._softmax_warp(g, gw)
+
+    # ------------------------------------------------------------------ scheduler
+    def run(self, max_steps: int = 200000):
+        nxt = {name: next(gen) for name, gen in self.actors.items()}
+        waiting_gbar = {}
+        steps = 0
+        while nxt or self.tma or self.pipe:
+            steps += 1
+            if steps > max_steps:
+                self.fail("step limit")
+            options = []
+            for name, op in nxt.items():
+                kind = op[0]
+                if kind == "do":
+                    options.append(("actor", name))
+                elif kind == "wait":
+                    _, bar, parity, k, who = op
+                    if self.bars[bar].test(parity):
+                        options.append(("actor", name))
+                elif kind == "gbar":
+                    _, gid, n = op
+                    g = self.gbar.setdefault(gid, {"gen": 0, "arrived": set()})
+                    if name not in self.gbar_wait or g["gen"] > self.gbar_wait[name][1]:
+                        options.append(("actor", name))
+            for i in range(len(self.tma)):
+                options.append(("tma", i))
+            if self.pipe:
+                options.append(("pipe", 0))
+            if not options:
+                self.fail("deadlock: " + ", ".join(f"{n} at {op[0]} {op[1:3] if op[0] != 'do' else ''}"
+                                                    for n, op in nxt.items()))
+            kind, key = self.rng.choice(options)
+            if kind == "tma":
+                bar, nbytes, effect = self.tma.pop(key)
+                effect()
+                self.bars[bar].complete_tx(nbytes)
+                continue
+            if kind == "pipe":
+                op = self.pipe.pop(0)
+                if op[0] == "mma":
+                    op[1]()
+                else:
+                    self.bars[op[1]].arrive()
+                continue
+            name = key
+            op = nxt[name]
+            if op[0] == "do":
+                op[1]()
+            elif op[0] == "wait":
+                _, bar, parity, k, who = op
+                b = self.bars[bar]
+                if b.completed != k + 1:
+                    self.fail(f"{who}: wait on {bar} for phase {k} passed with {b.completed} phases complete")
+            elif op[0] == "gbar":
+                _, gid, n = op
+                g = self.gbar[gid]
+                if name not in self.gbar_wait:
+                    # Arrive; the last arrival ends this generation of the barrier.
+                    self.gbar_wait[name] = (gid, g["gen"])
+                    g["arrived"].add(name)
+                    if len(g["arrived"]) == n:
+                        g["gen"] += 1
+                        g["arrived"] = set()
+                    if g["gen"] == self.gbar_wait[name][1]:
+                        continue  # stays at the barrier until the others arrive
+                del self.gbar_wait[name]
+            try:
+                nxt[name] = next(self.actors[name])
+            except StopIteration:
+                del nxt[name]
+        return steps

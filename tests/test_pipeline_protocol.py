@@ -1,0 +1,71 @@
+"""CPU checks of the fused kernel's mbarrier protocol through its model (tests/pipeline_model.py).
+
+The model restates, role by role, every barrier wait, arrival, commit and copy of
+mg_attn_fwd_partial, and explores random interleavings of the roles with asynchronous copy and
+tensor-pipe completion. The protocol as built must pass for every variant and for the ring
+depths and P-buffer counts the plans use; each planted reordering must be caught in some
+interleaving. One of them is the ordering that faulted a GPU when an A/B copy of the kernel
+tried it: the P.V warp waiting for V before P in the two-pass variants.
+"""
+
+import itertools
+
+import pytest
+
+from tests import pipeline_model as pm
+
+VARIANTS = {"plain": pm.PLAIN, "max-subtracted": pm.SAFE, "qk-norm": pm.QKNORM}
+# (stages, P buffers): d = 64 plans use 2..6 stages and 3 P buffers, d = 128 plans 2..3 and 2.
+RINGS = [(6, 3), (5, 3), (4, 3), (3, 3), (2, 3), (3, 2), (2, 2)]
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("stages,pbufs", RINGS)
+def test_protocol_as_built_is_clean(variant, stages, pbufs):
+    for T, seed in itertools.product((1, 2, 3, 4, 7, 12), range(12)):
+        pm.Sim(T, stages, pbufs, VARIANTS[variant], seed).run()
+
+
+def caught(mutation, variant, tries=40):
+    for T, (stages, pbufs), seed in itertools.product((2, 3, 5, 8), [(6, 3), (3, 2)], range(tries)):
+        try:
+            pm.Sim(T, stages, pbufs, variant, seed, mutations=(mutation,)).run()
+        except pm.ProtocolError as e:
+            return str(e)
+    return None
+
+
+@pytest.mark.parametrize("variant", ["max-subtracted", "qk-norm"])
+def test_pv_warp_waiting_for_v_first_passes_a_parity_wait_early(variant):
+    msg = caught("pv_waits_v_first", VARIANTS[variant])
+    assert msg is not None and "VFull" in msg and "passed with" in msg
+
+
+def test_pv_warp_waiting_for_v_first_is_harmless_without_the_row_maximum_pass():
+    # Without the row-maximum steps every V phase completes on a copy the P.V warp has waited
+    # for in order, so the reordering is only slower, not wrong.
+    assert caught("pv_waits_v_first", pm.PLAIN, tries=20) is None
+
+
+@pytest.mark.parametrize("mutation,variant", [
+    ("s_no_sempty_wait", pm.PLAIN),             # S written while the softmax group reads it
+    ("producer_no_kvempty_wait", pm.PLAIN),     # K/V stage refilled while an MMA reads it
+    ("qk_kvempty_before_barrier", pm.QKNORM),   # K stage released before every warp summed it
+])
+def test_planted_hazards_are_caught(mutation, variant):
+    assert caught(mutation, variant) is not None
+
+
+def test_barrier_parity_semantics():
+    # The model's parity test is the hardware's: phase k is seen as complete when the open
+    # phase's parity differs from k's, which is also true while phase k - 1 is still open.
+    b = pm.Barrier("x", 1)
+    assert not b.test(0)          # phase 0 open
+    b.arrive()
+    assert b.test(0) and not b.test(1)
+    b.arrive()
+    assert b.test(1) and not b.test(0)
+    with pytest.raises(pm.ProtocolError):
+        c = pm.Barrier("y", 1)
+        c.arrive(expect_tx=4)
+        c.complete_tx(8)
