@@ -540,8 +540,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int u = T1 + v;  // step of the K/V ring
             const int pb = v % kPBuffers;
             const int s = u % STAGES;
-            if (!warp_wait(bar(BI::kPFull + pb), static_cast<uint32_t>(v / kPBuffers) & 1u, BI::kPFull + pb) ||
-                !warp_wait(bar(BI::kVFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kVFull + s)) {
+            // The graph as written waits for V first: it has usually landed long before P, and
+            // its test then costs nothing after P's. In the two-pass variants the V barrier of a
+            // stage also completes phases for the row-maximum steps, on the producer's plain
+            // arrival when it issues them. A wait for V before P could test the barrier while
+            // the phase before the awaited one is still open, and a parity wait would then pass
+            // early. There P comes first: P of step u exists only once K of step u has landed, so
+            // every earlier phase of that V barrier has completed.
+            bool waited;
+            if constexpr (!kSafeMax)
+                waited = warp_wait(bar(BI::kVFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kVFull + s) &&
+                         warp_wait(bar(BI::kPFull + pb), static_cast<uint32_t>(v / kPBuffers) & 1u, BI::kPFull + pb);
+            else
+                waited = warp_wait(bar(BI::kPFull + pb), static_cast<uint32_t>(v / kPBuffers) & 1u, BI::kPFull + pb) &&
+                         warp_wait(bar(BI::kVFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kVFull + s);
+            if (!waited) {
                 ok = false;
                 break;
             }

@@ -199,7 +199,9 @@ class Sim:
             pb, s = v % P, u % S
             w_p = self.wait(f"PFull{pb}", (v // P) & 1, v // P, f"PV warp P {v}")
             w_v = self.wait(f"VFull{s}", (u // S) & 1, u // S, f"PV warp V {v}")
-            for w in ((w_v, w_p) if "pv_waits_v_first" in self.mut else (w_p, w_v)):
+            # As built: V first for the graph as written, P first in the two-pass variants.
+            v_first = (not self.safe) or "pv_waits_v_first" in self.mut
+            for w in ((w_v, w_p) if v_first else (w_p, w_v)):
                 yield w
             yield ("do", lambda v=v, u=u, pb=pb, s=s: self._issue_pv(v, u, pb, s))
         for t in range(max(self.T - P, 0), self.T):

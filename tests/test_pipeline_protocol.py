@@ -41,9 +41,10 @@ def test_pv_warp_waiting_for_v_first_passes_a_parity_wait_early(variant):
     assert msg is not None and "VFull" in msg and "passed with" in msg
 
 
-def test_pv_warp_waiting_for_v_first_is_harmless_without_the_row_maximum_pass():
-    # Without the row-maximum steps every V phase completes on a copy the P.V warp has waited
-    # for in order, so the reordering is only slower, not wrong.
+def test_pv_warp_waits_for_v_first_only_without_the_row_maximum_pass():
+    # As built, the graph as written waits for V first (every V phase completes on a copy the
+    # P.V warp has waited for in order); the clean runs above cover it. The two-pass variants
+    # wait for P first, and forcing V first there is caught (the test above).
     assert caught("pv_waits_v_first", pm.PLAIN, tries=20) is None
 
 
