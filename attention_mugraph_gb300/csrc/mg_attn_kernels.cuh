@@ -515,15 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
-        if (!ok) {
-            // Unwind: wait for the MMAs already issued before tensor memory is freed (elect.sync
-            // picks the same lane of the full warp every time).
-            if (ptx::elect_one()) {
-                ptx::mma_commit(bar(BI::kDrain));
-                wait_drain(bar(BI::kDrain), 0, p.timeout_ns);
-            }
-            __syncwarp();
+        // Every S product issued completes before tensor memory is freed, on the unwinding path
+        // and also when another role aborts after this loop has ended (then nobody else may wait
+        // for the last S buffers). elect.sync picks the same lane of the full warp every time.
+        if (ptx::elect_one()) {
+            ptx::mma_commit(bar(BI::kDrain));
+            wait_drain(bar(BI::kDrain), 0, p.timeout_ns);
         }
+        __syncwarp();
     } else if (warp == kPvWarp) {
         // ---------------------------------------------------------------- O += P.V issuer
         // Same pattern as the S issuer: warp-wide waits, the elected lane issues.
@@ -580,7 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = T - kPBuffers > 0 ? T - kPBuffers : 0; ok && u < T; ++u)
                 ok = warp_wait(bar(BI::kPEmpty + u % kPBuffers), static_cast<uint32_t>(u / kPBuffers) & 1u,
                                BI::kPEmpty + u % kPBuffers);
-        } else {
+        }
+        if (!ok) {
+            // Unwinding, from the loop or from the tail: the P.V products issued complete before
+            // tensor memory is freed.
             if (ptx::elect_one()) {
                 ptx::mma_commit(bar(BI::kDrainPv));
                 wait_drain(bar(BI::kDrainPv), 0, p.timeout_ns);

@@ -14,7 +14,11 @@ A scheduler runs the roles under random interleavings and checks, at every step:
   completed. The hardware test compares the barrier's current phase bit with the parity, so a
   wait on phase k while phase k-1 is still open passes early; a wait that falls two phases
   behind never passes (reported as a deadlock);
-* data hazards: a copy lands in a K or V stage only when no operation still reads it; an MMA
+* unwinding: with `abort_rate`, a blocked wait may run out at any moment; every later wait
+  whose phase has not completed then fails, as the kernel's bounded waits do once the CTA's
+  abort flag is up, and the roles unwind as the kernel's do. No role may deadlock, and no copy
+  or tensor-core operation may still be in flight when the CTA tears down;
+* data hazards (when no abort): a copy lands in a K or V stage only when no operation still reads it; an MMA
   reads K, V and P only once the step's data is there and writes an S buffer only when its
   softmax group has finished reading it; the softmax warps read S only after its MMA and write
   a P buffer only after the P.V product of three (d = 64) or two (d = 128) tiles earlier;
@@ -72,7 +76,8 @@ class Barrier:
 
 
 class Sim:
-    def __init__(self, T: int, stages: int, pbufs: int, variant: int, seed: int, mutations=()):
+    def __init__(self, T: int, stages: int, pbufs: int, variant: int, seed: int, mutations=(),
+                 abort_rate: float = 0.0):
         if T < 1 or stages < 2 or pbufs < 2:
             raise ValueError("T >= 1, stages >= 2, pbufs >= 2")
         self.T, self.S, self.P, self.var = T, stages, pbufs, variant
@@ -82,6 +87,8 @@ class Sim:
         self.U = self.T1 + T
         self.mut = set(mutations)
         self.rng = random.Random(seed)
+        self.abort_rate = abort_rate  # chance per step that a blocked wait runs out (0: never)
+        self.abort = False
         self.bars = {}
 
         def mk(name, count):
@@ -129,24 +136,38 @@ class Sim:
         return ("wait", bar, parity, k, who)
 
     # ------------------------------------------------------------------ roles
+    # A role yields ("wait", ...) and receives True, or False once the CTA is aborting and the
+    # phase has not completed (the kernel's bounded wait); ("gbar", id, n, pred) receives the AND
+    # of the participants' predicates; ("drain", kind) waits, ignoring the abort, until the
+    # role's copies ("tma") or tensor-core operations ("pipe") have completed.
     def _producer(self):
         S = self.S
+        ok = True
         yield ("do", lambda: self._tma_q())
-        for t in range(self.U):
+        t = 0
+        while ok and t < self.U:
             s = t % S
             rnd = t // S
             if t >= S and "producer_no_kvempty_wait" not in self.mut:
-                yield self.wait(f"KvEmpty{s}", (rnd & 1) ^ 1, rnd - 1, f"producer step {t}")
+                if not (yield self.wait(f"KvEmpty{s}", (rnd & 1) ^ 1, rnd - 1, f"producer step {t}")):
+                    ok = False
+                    break
             yield ("do", lambda t=t, s=s: self._issue_step(t, s))
-        for u in range(max(self.U - S, 0), self.U):
-            yield self.wait(f"KvEmpty{u % S}", (u // S) & 1, u // S, f"producer tail {u}")
+            t += 1
+        if ok:
+            for u in range(max(self.U - S, 0), self.U):
+                ok = yield self.wait(f"KvEmpty{u % S}", (u // S) & 1, u // S, f"producer tail {u}")
+                if not ok:
+                    break
+        if self.abort:
+            yield ("drain", "tma")
 
     def _tma_q(self):
         self.bars["QFull"].arrive(expect_tx=1)
         self.tma.append(("QFull", 1, lambda: setattr(self, "q_loaded", True)))
 
     def _issue_step(self, t, s):
-        if self.k_readers[s]:
+        if self.k_readers[s] and not self.abort:
             self.fail(f"K stage {s} overwritten for step {t} while still read")
         self.kst[s] = None
         kb = self.bars[f"KFull{s}"]
@@ -156,7 +177,7 @@ class Sim:
         if t < self.T1:
             vb.arrive()  # a row-maximum step loads no V
         else:
-            if self.v_readers[s]:
+            if self.v_readers[s] and not self.abort:
                 self.fail(f"V stage {s} overwritten for step {t} while still read")
             self.vst[s] = None
             vb.arrive(expect_tx=1)
@@ -164,21 +185,30 @@ class Sim:
 
     def _s_warp(self):
         S = self.S
-        yield self.wait("QFull", 0, 0, "S warp Q")
-        for u in range(self.U):
+        ok = yield self.wait("QFull", 0, 0, "S warp Q")
+        u = 0
+        while ok and u < self.U:
             s, sb = u % S, u & 1
-            yield self.wait(f"KFull{s}", (u // S) & 1, u // S, f"S warp K {u}")
+            if not (yield self.wait(f"KFull{s}", (u // S) & 1, u // S, f"S warp K {u}")):
+                ok = False
+                break
             if u >= 2 and "s_no_sempty_wait" not in self.mut:
-                yield self.wait(f"SEmpty{sb}", ((u >> 1) & 1) ^ 1, (u >> 1) - 1, f"S warp S buffer {u}")
+                if not (yield self.wait(f"SEmpty{sb}", ((u >> 1) & 1) ^ 1, (u >> 1) - 1, f"S warp S buffer {u}")):
+                    ok = False
+                    break
             yield ("do", lambda u=u, s=s, sb=sb: self._issue_s(u, s, sb))
+            u += 1
+        if not ok or "drain_only_on_failure" not in self.mut:
+            yield ("drain", "pipe")
 
     def _issue_s(self, u, s, sb):
-        if not self.q_loaded:
-            self.fail(f"S MMA {u} issued before Q landed")
-        if self.kst[s] != u:
-            self.fail(f"S MMA {u} reads K stage {s} holding step {self.kst[s]}")
-        if self.s_readers[sb]:
-            self.fail(f"S MMA {u} writes S buffer {sb} while softmax warps read it")
+        if not self.abort:
+            if not self.q_loaded:
+                self.fail(f"S MMA {u} issued before Q landed")
+            if self.kst[s] != u:
+                self.fail(f"S MMA {u} reads K stage {s} holding step {self.kst[s]}")
+            if self.s_readers[sb]:
+                self.fail(f"S MMA {u} writes S buffer {sb} while softmax warps read it")
         self.k_readers[s] += 1
         self.s_pending_write[sb] = True
 
@@ -194,7 +224,9 @@ class Sim:
 
     def _pv_warp(self):
         S, P = self.S, self.P
-        for v in range(self.T):
+        ok = True
+        v = 0
+        while ok and v < self.T:
             u = self.T1 + v
             pb, s = v % P, u % S
             w_p = self.wait(f"PFull{pb}", (v // P) & 1, v // P, f"PV warp P {v}")
@@ -202,16 +234,29 @@ class Sim:
             # As built: V first for the graph as written, P first in the two-pass variants.
             v_first = (not self.safe) or "pv_waits_v_first" in self.mut
             for w in ((w_v, w_p) if v_first else (w_p, w_v)):
-                yield w
+                if not (yield w):
+                    ok = False
+                    break
+            if not ok:
+                break
             yield ("do", lambda v=v, u=u, pb=pb, s=s: self._issue_pv(v, u, pb, s))
-        for t in range(max(self.T - P, 0), self.T):
-            yield self.wait(f"PEmpty{t % P}", (t // P) & 1, t // P, f"PV warp tail {t}")
+            v += 1
+        if ok:
+            for t in range(max(self.T - P, 0), self.T):
+                ok = yield self.wait(f"PEmpty{t % P}", (t // P) & 1, t // P, f"PV warp tail {t}")
+                if not ok:
+                    break
+            if not ok and "drain_only_on_failure" not in self.mut:
+                yield ("drain", "pipe")
+        else:
+            yield ("drain", "pipe")
 
     def _issue_pv(self, v, u, pb, s):
-        if self.pbuf[pb] != v:
-            self.fail(f"P.V MMA {v} reads P buffer {pb} holding tile {self.pbuf[pb]}")
-        if self.vst[s] != u:
-            self.fail(f"P.V MMA {v} reads V stage {s} holding step {self.vst[s]}")
+        if not self.abort:
+            if self.pbuf[pb] != v:
+                self.fail(f"P.V MMA {v} reads P buffer {pb} holding tile {self.pbuf[pb]}")
+            if self.vst[s] != u:
+                self.fail(f"P.V MMA {v} reads V stage {s} holding step {self.vst[s]}")
         self.p_readers[pb] += 1
         self.v_readers[s] += 1
         self.pv_issued += 1
@@ -230,64 +275,83 @@ class Sim:
     def _softmax_warp(self, g, gw):
         S, P = self.S, self.P
         who = f"softmax g{g}w{gw}"
+        ok = True
         if self.qk:
-            yield self.wait("QFull", 0, 0, who + " Q")
+            ok = yield self.wait("QFull", 0, 0, who + " Q")
         # Row-maximum pass.
-        for u in range(g, self.T1, 2):
-            s = u % S
-            if self.qk:
-                yield self.wait(f"KFull{s}", (u // S) & 1, u // S, f"{who} K {u}")
-                yield ("do", lambda s=s, u=u: self._read_k(s, u, +1))
-                yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")
-                yield ("do", lambda s=s: self._read_k(s, None, -1))
-                if gw == 0 and "qk_kvempty_before_barrier" in self.mut:
-                    # Mutation: the stage is released before the other warps have read K.
-                    yield ("do", lambda s=s: self.bars[f"KvEmpty{s}"].arrive())
-                yield ("gbar", f"group{g}", GROUP_WARPS)
+        if self.qk:
+            # All four warps of the group run every iteration and vote at the first barrier.
+            for u in range(g, self.T1, 2):
+                s = u % S
+                w_ok = ok and (yield self.wait(f"KFull{s}", (u // S) & 1, u // S, f"{who} K {u}"))
+                if w_ok:
+                    yield ("do", lambda s=s, u=u: self._read_k(s, u, +1))
+                    yield ("do", lambda s=s: self._read_k(s, None, -1))
+                    if gw == 0 and "qk_kvempty_before_barrier" in self.mut:
+                        # Mutation: the stage is released before the other warps have read K.
+                        yield ("do", lambda s=s: self.bars[f"KvEmpty{s}"].arrive())
+                w_ok = w_ok and (yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}"))
+                w_ok = yield ("gbar", f"group{g}", GROUP_WARPS, w_ok)
+                if not w_ok:
+                    ok = False
+                    break
                 if gw == 0 and "qk_kvempty_before_barrier" not in self.mut:
                     yield ("do", lambda s=s: self.bars[f"KvEmpty{s}"].arrive())
                 yield ("do", lambda u=u: self._read_s(g, u, +1))
                 yield ("do", lambda u=u: self._read_s(g, u, -1))
                 yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
-                yield ("gbar", f"group{g}", GROUP_WARPS)
-            else:
-                yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")
+                yield ("gbar", f"group{g}", GROUP_WARPS, True)
+        else:
+            u = g
+            while ok and u < self.T1:
+                if not (yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")):
+                    ok = False
+                    break
                 yield ("do", lambda u=u: self._read_s(g, u, +1))
                 yield ("do", lambda u=u: self._read_s(g, u, -1))
                 yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
+                u += 2
         if self.safe:
-            yield ("gbar", "softmax", 2 * GROUP_WARPS)
-            yield ("gbar", "softmax", 2 * GROUP_WARPS)
+            yield ("gbar", "softmax", 2 * GROUP_WARPS, True)
+            yield ("gbar", "softmax", 2 * GROUP_WARPS, True)
         # Main pass.
-        start = self.T1 if (self.T1 % 2 == g) else self.T1 + 1
-        for u in range(start, self.U, 2):
+        u = self.T1 if (self.T1 % 2 == g) else self.T1 + 1
+        while ok and u < self.U:
             t = u - self.T1
             pb = t % P
-            yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")
+            if not (yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")):
+                ok = False
+                break
             yield ("do", lambda u=u: self._read_s(g, u, +1))            # half 0 loaded
             if t >= P:
-                yield self.wait(f"PEmpty{pb}", ((t // P) & 1) ^ 1, t // P - 1, f"{who} P buffer {t}")
+                if not (yield self.wait(f"PEmpty{pb}", ((t // P) & 1) ^ 1, t // P - 1, f"{who} P buffer {t}")):
+                    ok = False
+                    break
             yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 0)))
             yield ("do", lambda u=u: self._read_s(g, u, -1))            # half 1 loaded: S released
             yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
             yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 1)))
             yield ("do", lambda pb=pb: self.bars[f"PFull{pb}"].arrive())
-        # Epilogue: every softmax warp waits for O, then all meet.
-        yield self.wait("OFull", 0, 0, f"{who} O")
-        yield ("gbar", "softmax", 2 * GROUP_WARPS)
-        yield ("do", lambda: self._read_o())
+            u += 2
+        # Epilogue: a vote on "O is ready" that every softmax warp takes part in.
+        o_ok = ok and (yield self.wait("OFull", 0, 0, f"{who} O"))
+        o_ready = yield ("gbar", "softmax", 2 * GROUP_WARPS, o_ok)
+        if o_ready:
+            yield ("do", lambda: self._read_o())
 
     def _read_k(self, s, u, delta):
-        if delta > 0 and self.kst[s] != u:
+        if delta > 0 and self.kst[s] != u and not self.abort:
             self.fail(f"QK-norm softmax reads K stage {s} holding step {self.kst[s]}, expected {u}")
         self.k_readers[s] += delta
 
     def _read_s(self, g, u, delta):
-        if delta > 0 and (self.sbuf[g] != u or self.s_pending_write[g]):
+        if delta > 0 and (self.sbuf[g] != u or self.s_pending_write[g]) and not self.abort:
             self.fail(f"softmax group {g} reads S buffer holding step {self.sbuf[g]}, expected {u}")
         self.s_readers[g] += delta
 
     def _write_p(self, pb, t, piece):
+        if self.abort:
+            return
         if self.p_readers[pb]:
             self.fail(f"P buffer {pb} written for tile {t} while a P.V MMA reads it")
         if self.p_tile_writing[pb] != t:
@@ -313,30 +377,51 @@ class Sim:
                 self.actors[f"softmax{g}.{gw}"] = self._softmax_warp(g, gw)
 
     # ------------------------------------------------------------------ scheduler
-    def run(self, max_steps: int = 200000):
-        nxt = {name: next(gen) for name, gen in self.actors.items()}
-        waiting_gbar = {}
+    def _runnable(self, name, op):
+        """(runnable, value sent back) for an actor's pending operation."""
+        kind = op[0]
+        if kind == "do":
+            return True, None
+        if kind == "wait":
+            _, bar, parity, k, who = op
+            if self.bars[bar].test(parity):
+                return True, True
+            return (True, False) if self.abort else (False, None)
+        if kind == "gbar":
+            _, gid, n, pred = op
+            g = self.gbar.setdefault(gid, {"gen": 0, "arrived": {}, "result": {}})
+            if name not in self.gbar_wait:
+                return True, None
+            gen = self.gbar_wait[name][1]
+            return (g["gen"] > gen), g["result"].get(gen)
+        if kind == "drain":
+            return (not self.tma) if op[1] == "tma" else (not self.pipe), None
+        raise ValueError(kind)
+
+    def run(self, max_steps: int = 400000):
+        gens = dict(self.actors)
+        nxt = {name: next(gen) for name, gen in gens.items()}
         steps = 0
         while nxt or self.tma or self.pipe:
             steps += 1
             if steps > max_steps:
                 self.fail("step limit")
+            if not nxt:
+                # Every role has finished: the CTA tears down (tensor memory freed, shared
+                # memory released). Nothing may still be in flight.
+                self.fail(f"teardown with {len(self.tma)} copies and {len(self.pipe)} tensor-pipe "
+                          "operations in flight")
+            # A bounded wait that runs out: some blocked wait times out and the CTA aborts.
+            if self.abort_rate and not self.abort and self.rng.random() < self.abort_rate:
+                blocked = [n for n, op in nxt.items() if op[0] == "wait" and not self._runnable(n, op)[0]]
+                if blocked:
+                    self.abort = True
             options = []
             for name, op in nxt.items():
-                kind = op[0]
-                if kind == "do":
+                ready, _ = self._runnable(name, op)
+                if ready:
                     options.append(("actor", name))
-                elif kind == "wait":
-                    _, bar, parity, k, who = op
-                    if self.bars[bar].test(parity):
-                        options.append(("actor", name))
-                elif kind == "gbar":
-                    _, gid, n = op
-                    g = self.gbar.setdefault(gid, {"gen": 0, "arrived": set()})
-                    if name not in self.gbar_wait or g["gen"] > self.gbar_wait[name][1]:
-                        options.append(("actor", name))
-            for i in range(len(self.tma)):
-                options.append(("tma", i))
+            options += [("tma", i) for i in range(len(self.tma))]
             if self.pipe:
                 options.append(("pipe", 0))
             if not options:
@@ -357,28 +442,35 @@ class Sim:
                 continue
             name = key
             op = nxt[name]
+            _, value = self._runnable(name, op)
             if op[0] == "do":
                 op[1]()
-            elif op[0] == "wait":
+            elif op[0] == "wait" and value:
                 _, bar, parity, k, who = op
                 b = self.bars[bar]
                 if b.completed != k + 1:
                     self.fail(f"{who}: wait on {bar} for phase {k} passed with {b.completed} phases complete")
             elif op[0] == "gbar":
-                _, gid, n = op
+                _, gid, n, pred = op
                 g = self.gbar[gid]
                 if name not in self.gbar_wait:
-                    # Arrive; the last arrival ends this generation of the barrier.
-                    self.gbar_wait[name] = (gid, g["gen"])
-                    g["arrived"].add(name)
+                    # Arrive with a predicate; the last arrival ends this generation of the
+                    # barrier and fixes the AND of the predicates.
+                    gen = g["gen"]
+                    self.gbar_wait[name] = (gid, gen)
+                    g["arrived"][name] = bool(pred)
                     if len(g["arrived"]) == n:
+                        g["result"][gen] = all(g["arrived"].values())
                         g["gen"] += 1
-                        g["arrived"] = set()
-                    if g["gen"] == self.gbar_wait[name][1]:
+                        g["arrived"] = {}
+                    if g["gen"] == gen:
                         continue  # stays at the barrier until the others arrive
+                    value = g["result"][gen]
+                else:
+                    value = g["result"][self.gbar_wait[name][1]]
                 del self.gbar_wait[name]
             try:
-                nxt[name] = next(self.actors[name])
+                nxt[name] = gens[name].send(value)
             except StopIteration:
                 del nxt[name]
         return steps

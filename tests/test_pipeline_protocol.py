@@ -57,6 +57,29 @@ def test_planted_hazards_are_caught(mutation, variant):
     assert caught(mutation, variant) is not None
 
 
+@pytest.mark.parametrize("variant", list(VARIANTS))
+def test_unwinding_from_any_wait_is_clean(variant):
+    # A bounded wait may run out anywhere (here: a random blocked wait at a random moment).
+    # Every role must then unwind without waiting on a peer that left, and nothing the CTA
+    # issued (copies, MMAs, commits) may still be in flight when it tears down.
+    for T, (stages, pbufs), seed in itertools.product((1, 2, 3, 5, 8), [(6, 3), (3, 2), (2, 2)], range(12)):
+        pm.Sim(T, stages, pbufs, VARIANTS[variant], seed, abort_rate=0.02).run()
+
+
+def test_draining_only_after_a_failed_loop_leaves_mmas_in_flight():
+    # The S warp once drained its MMAs only when its own loop failed, and the P.V warp not when
+    # its tail waits failed: an abort raised elsewhere after those loops could free tensor
+    # memory under a running MMA.
+    hit = None
+    for T, (stages, pbufs), seed in itertools.product((2, 3, 5, 8), [(6, 3), (3, 2)], range(60)):
+        try:
+            pm.Sim(T, stages, pbufs, pm.PLAIN, seed, mutations=("drain_only_on_failure",), abort_rate=0.01).run()
+        except pm.ProtocolError as e:
+            hit = str(e)
+            break
+    assert hit is not None and "in flight" in hit
+
+
 def test_barrier_parity_semantics():
     # The model's parity test is the hardware's: phase k is seen as complete when the open
     # phase's parity differs from k's, which is also true while phase k - 1 is still open.
