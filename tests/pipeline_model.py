@@ -22,7 +22,8 @@ A scheduler runs the roles under random interleavings and checks, at every step:
   reads K, V and P only once the step's data is there and writes an S buffer only when its
   softmax group has finished reading it; the softmax warps read S only after its MMA and write
   a P buffer only after the P.V product of three (d = 64) or two (d = 128) tiles earlier;
-  the epilogue reads O only after the last P.V product.
+  the epilogue reads O only after the last P.V product, and stages its output in the K/V
+  ring only when no copy into it or MMA reading it is still in flight.
 
 The model is a restatement, not the kernel: a change to the kernel's barrier protocol has to
 be made here too. The mutations in tests/test_pipeline_protocol.py show that it catches the
@@ -367,6 +368,12 @@ class Sim:
     def _read_o(self):
         if self.pv_done != self.T:
             self.fail(f"O read after {self.pv_done} of {self.T} P.V products")
+        # The epilogue stages its output in the K/V ring: no copy may still be landing there and
+        # no MMA may still read it.
+        if any(bar.startswith(("KFull", "VFull")) for bar, _, _ in self.tma):
+            self.fail("output staged in the K/V ring while a copy into it is in flight")
+        if any(self.k_readers) or any(self.v_readers):
+            self.fail("output staged in the K/V ring while an MMA reads it")
 
     def _make_actors(self):
         self.actors["producer"] = self._producer()
