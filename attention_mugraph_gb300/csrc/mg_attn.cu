@@ -635,9 +635,9 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
     uint8_t *s = static_cast<uint8_t *>(plan->staging);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-    // Pinned (page-locked, device-mapped) 16-byte-aligned host buffers are read and written by
-    // copy kernels through their device addresses, chained to the attention kernels with PDL;
-    // any other host memory goes through the copy engines.
+    // Pinned (page-locked, device-mapped) 16-byte-aligned host buffers are read by a copy kernel
+    // through their device addresses, chained to the attention kernels with PDL, and O is written
+    // back the same way (or directly, below); any other host memory goes through the copy engines.
     void *dQ = nullptr, *dK = nullptr, *dV = nullptr, *dO = nullptr;
     bool direct = device_mapped(hQ, &dQ) && device_mapped(hK, &dK) && device_mapped(hV, &dV) && device_mapped(hO, &dO);
     const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
@@ -658,9 +658,15 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
                (e = cudaMemcpyAsync(s + ov, hV, bv, cudaMemcpyHostToDevice, st)) != cudaSuccess) {
         return cuda_fail(e, "cudaMemcpyAsync(host to device)");
     }
-    mg_status r = mg_attn_run(plan, s + oq, s + ok, s + ov, s + oo, stream);
+    // With split partials (the on-chip combine or the second kernel) O is written by plain stores,
+    // which reach the pinned host buffer through its device address directly: no staging of O
+    // and no copy back. One split writes O with a TMA store, which takes the staging path.
+    const bool o_direct = direct && in.n_split > 1;
+    mg_status r = mg_attn_run(plan, s + oq, s + ok, s + ov, o_direct ? dO : s + oo, stream);
     if (r != MG_OK)
         return r;
+    if (o_direct)
+        return MG_OK;
     if (direct) {
         CopyJobs out_jobs{};
         out_jobs.src[0] = reinterpret_cast<const uint4 *>(s + oo);

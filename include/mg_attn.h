@@ -153,9 +153,10 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
  * buffers owned by the plan, runs as mg_attn_run, and copies O back into host memory,
  * all enqueued on `stream`; the caller synchronises the stream before reading hO.
  * Page-locked host buffers that the device can address (cudaHostAlloc / pinned tensors,
- * 16-byte aligned) are read and written by copy kernels through their device addresses,
- * chained to the attention kernels with programmatic dependent launch; other host memory
- * (pageable) goes through cudaMemcpyAsync. The plan's device staging buffers (the size of
+ * 16-byte aligned) are read by a copy kernel through their device addresses, chained to the
+ * attention kernels with programmatic dependent launch; when the plan splits N
+ * (info.n_split > 1) the kernels write O straight into such a host buffer, and otherwise a
+ * second copy kernel writes it back. Other host memory (pageable) goes through cudaMemcpyAsync. The plan's device staging buffers (the size of
  * Q, K, V and O) are allocated by the first call on that plan and reused after, so one
  * plan must not run two such calls at once on different streams.
  * Errors: as mg_attn_run, plus MG_ERR_CUDA if the staging allocation fails.

@@ -217,10 +217,13 @@ def test_cuda_graph_capture_replay():
     assert_parity(O, ref, "graph replay")
 
 
-def test_host_buffer_entry_point():
+@pytest.mark.parametrize("kw", [{}, {"n_split": 1}, {"flags": mg.MG_FLAG_NO_CLUSTER}])
+def test_host_buffer_entry_point(kw):
+    # Pinned buffers: O is written straight to the host buffer when N is split (the cluster
+    # combine, the second kernel), and staged and copied back with one split.
     q, k, v, _ = inputs.make_config("tiny")
     ref = oracle.attention(q, k, v)
-    plan = mg.Plan(2, 64, 1024, 64)
+    plan = mg.Plan(2, 64, 1024, 64, **kw)
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     ho = torch.empty((2, 64, 64), dtype=torch.float16).pin_memory()
     for _ in range(2):
