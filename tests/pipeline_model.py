@@ -122,6 +122,7 @@ class Sim:
         self.p_readers = [0] * pbufs
         self.pv_done = 0
         self.pv_issued = 0
+        self.scale_parts = {}               # QK-norm: tile -> softmax warps that wrote its key scales
         self.tma = []                       # in-flight copies: (barrier, bytes, effect)
         self.pipe = []                      # tensor pipe FIFO: ("mma", effect) or ("commit", barrier)
         self.gbar = {}                      # named barriers: id -> {"gen": n, "arrived": set()}
@@ -288,6 +289,7 @@ class Sim:
                 if w_ok:
                     yield ("do", lambda s=s, u=u: self._read_k(s, u, +1))
                     yield ("do", lambda s=s: self._read_k(s, None, -1))
+                    yield ("do", lambda u=u: self.scale_parts.setdefault(u, set()).add(gw))
                     if gw == 0 and "qk_kvempty_before_barrier" in self.mut:
                         # Mutation: the stage is released before the other warps have read K.
                         yield ("do", lambda s=s: self.bars[f"KvEmpty{s}"].arrive())
@@ -312,7 +314,7 @@ class Sim:
                 yield ("do", lambda u=u: self._read_s(g, u, -1))
                 yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
                 u += 2
-        if self.safe:
+        if self.safe and "no_max_exchange" not in self.mut:
             yield ("gbar", "softmax", 2 * GROUP_WARPS, True)
             yield ("gbar", "softmax", 2 * GROUP_WARPS, True)
         # Main pass.
@@ -328,6 +330,8 @@ class Sim:
                 if not (yield self.wait(f"PEmpty{pb}", ((t // P) & 1) ^ 1, t // P - 1, f"{who} P buffer {t}")):
                     ok = False
                     break
+            if self.qk:
+                yield ("do", lambda t=t: self._read_scales(t))
             yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 0)))
             yield ("do", lambda u=u: self._read_s(g, u, -1))            # half 1 loaded: S released
             yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
@@ -364,6 +368,12 @@ class Sim:
         self.pieces[pb].add(piece)
         if len(self.pieces[pb]) == 2 * GROUP_WARPS:
             self.pbuf[pb] = t
+
+    def _read_scales(self, t):
+        # QK-norm main pass: tile t's key-vector scales were written to global memory in the
+        # row-maximum pass (step t), by the four warps of whichever group took that step.
+        if not self.abort and len(self.scale_parts.get(t, ())) != GROUP_WARPS:
+            self.fail(f"main pass reads tile {t}'s key scales before all four warps wrote them")
 
     def _read_o(self):
         if self.pv_done != self.T:

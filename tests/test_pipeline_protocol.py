@@ -27,7 +27,7 @@ def test_protocol_as_built_is_clean(variant, stages, pbufs):
 
 
 def caught(mutation, variant, tries=40):
-    for T, (stages, pbufs), seed in itertools.product((2, 3, 5, 8), [(6, 3), (3, 2)], range(tries)):
+    for T, (stages, pbufs), seed in itertools.product((1, 2, 3, 5, 8), [(6, 3), (3, 2)], range(tries)):
         try:
             pm.Sim(T, stages, pbufs, variant, seed, mutations=(mutation,)).run()
         except pm.ProtocolError as e:
@@ -52,6 +52,10 @@ def test_pv_warp_waits_for_v_first_only_without_the_row_maximum_pass():
     ("s_no_sempty_wait", pm.PLAIN),             # S written while the softmax group reads it
     ("producer_no_kvempty_wait", pm.PLAIN),     # K/V stage refilled while an MMA reads it
     ("qk_kvempty_before_barrier", pm.QKNORM),   # K stage released before every warp summed it
+    # Key scales read before the other group wrote them. With several tiles per split the
+    # in-order S issue orders this hand-off as well; with one tile per split (a row-maximum
+    # step for group 0, the main-pass step for group 1) only the maximum exchange's barriers do.
+    ("no_max_exchange", pm.QKNORM),
 ])
 def test_planted_hazards_are_caught(mutation, variant):
     assert caught(mutation, variant) is not None
