@@ -207,9 +207,57 @@ def pin_v_linearity(fn):
     assert np.array_equal(np.asarray(fn(q, k, (v.float() * 2).half())), 2 * np.asarray(fn(q, k, v)))
 
 
+
+# ---------------------------------------------------------------- the fp16 decode, every bit pattern
+
+def _all_half_patterns():
+    return np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+
+
+def pin_half_decode_exhaustive(fn):
+    # Every IEEE binary16 bit pattern (subnormals, both zeros, infinities, NaNs included) as V with
+    # M = N = d = 1 and Q = K = 0: the weight is exp(0) / exp(0) = 1, so O = V exactly. numpy's
+    # float16 -> float64 widening is the independent reference.
+    v16 = _all_half_patterns()
+    B = v16.size
+    q = torch.zeros((B, 1, 1), dtype=torch.float16)
+    k = torch.zeros((B, 1, 1), dtype=torch.float16)
+    v = torch.from_numpy(v16.copy()).reshape(B, 1, 1)
+    got = np.asarray(fn(q, k, v), dtype=np.float64).reshape(-1)
+    want = v16.astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan), "NaN patterns must decode to NaN and nothing else"
+    assert np.array_equal(got[~nan], want[~nan]), (
+        f"{int((got[~nan] != want[~nan]).sum())} finite or infinite patterns decode wrongly")
+
+
+def pin_half_decode_scores(fn):
+    # The same decode on the score side: Q = x (or K = x) with d = 1, N = 2, K = [1, 0] (or Q = 1,
+    # K = [x, 0]) and V = [1, 0] gives O = e^x / (e^x + 1), the logistic function of the decoded x.
+    # Every finite pattern with |x| <= 30 (where the logistic still resolves x), subnormals included.
+    x16 = _all_half_patterns()
+    x64 = x16.astype(np.float64)
+    keep = np.isfinite(x64) & (np.abs(x64) <= 30.0)
+    x16, x64 = x16[keep], x64[keep]
+    B = x16.size
+    want = np.exp(x64) / (np.exp(x64) + 1.0)
+    xs = torch.from_numpy(x16.copy())
+    v = torch.zeros((B, 2, 1), dtype=torch.float16)
+    v[:, 0, 0] = 1.0
+    one = torch.ones((B, 1, 1), dtype=torch.float16)
+    k_side = torch.zeros((B, 1, 2), dtype=torch.float16)
+    k_side[:, 0, 0] = 1.0
+    got_q = np.asarray(fn(xs.reshape(B, 1, 1), k_side, v), dtype=np.float64).reshape(-1)
+    k_x = torch.zeros((B, 1, 2), dtype=torch.float16)
+    k_x[:, 0, 0] = xs
+    got_k = np.asarray(fn(one, k_x, v), dtype=np.float64).reshape(-1)
+    _close(got_q, want, 1e-13, 0.0, "Q decode through the logistic")
+    _close(got_k, want, 1e-13, 0.0, "K decode through the logistic")
+
 PINS = [pin_k_zero, pin_q_zero, pin_v_constant, pin_single_key, pin_one_hot,
         pin_golden_worked_examples, pin_brute_force, pin_torch_softmax, pin_joint_permutation,
-        pin_convex_hull, pin_batch_independence, pin_score_shift, pin_v_linearity]
+        pin_convex_hull, pin_batch_independence, pin_score_shift, pin_v_linearity,
+        pin_half_decode_exhaustive, pin_half_decode_scores]
 
 
 # ================================================================ QK-norm attention

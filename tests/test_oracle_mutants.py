@@ -86,3 +86,35 @@ def test_qknorm_pins_catch_planted_mistake(tmp_path, name, old, new):
         except (AssertionError, FloatingPointError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake: {name}"
+
+
+# Slips in the binary16 widening. The subnormal branch is reached only by the exhaustive decode
+# pins (random draws almost never produce an fp16 subnormal).
+DECODE_MUTANTS = [
+    ("subnormal exponent -14 instead of -24", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -14);"),
+    ("subnormals flushed to zero", "v = ldexp((double)f, -24);", "v = 0.0 * f;"),
+    ("normal exponent bias off by one", "v = ldexp((double)(f | 0x400), e - 25);",
+     "v = ldexp((double)(f | 0x400), e - 24);"),
+    ("implicit leading bit dropped", "v = ldexp((double)(f | 0x400), e - 25);", "v = ldexp((double)f, e - 25);"),
+    ("infinity and NaN swapped", "v = f ? NAN : INFINITY;", "v = f ? INFINITY : NAN;"),
+    ("sign bit ignored", "return sign ? -v : v;", "return v + 0.0 * sign;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", DECODE_MUTANTS, ids=[m[0] for m in DECODE_MUTANTS])
+def test_pins_catch_planted_decode_mistake(tmp_path, name, old, new):
+    text = mutate(open(SRC).read(), "static double half_bits_to_double(", "static double g_half[", old, new)
+    mutant_src = tmp_path / "mutant.c"
+    mutant_src.write_text(text)
+    lib = oracle.load_library(oracle.compile_library(str(mutant_src), str(tmp_path / "libmutant.so")))
+
+    def fn(q, k, v):
+        return oracle.attention(q, k, v, threads=1, lib=lib)
+
+    caught = []
+    for pin in (pins.pin_half_decode_exhaustive, pins.pin_half_decode_scores):
+        try:
+            pin(fn)
+        except (AssertionError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no decode pin caught the planted mistake: {name}"
