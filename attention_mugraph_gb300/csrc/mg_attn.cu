@@ -759,23 +759,30 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     st = decide(B, M, N, d, nullptr, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags);
     if (st != MG_OK)
         return st;
-    if (in.cluster_ctas > 0 &&
-        !cluster_schedulable(fwd_kernel(d, in.stages, 0), in.cluster_ctas, in.grid_ctas, in.smem_bytes)) {
+    // The kernel's shared-memory limit is raised before the cluster occupancy query, as
+    // mg_attn_plan_ex does: at the default 48 KB limit the query would refuse the cluster, and a
+    // first call in a process would then take another combine than later calls.
+    FwdKernel fwd = fwd_kernel(d, in.stages, 0);
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, in.smem_bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute");
+    if (in.cluster_ctas > 0 && !cluster_schedulable(fwd, in.cluster_ctas, in.grid_ctas, in.smem_bytes)) {
         mg_attn_options o{};
         o.flags = MG_FLAG_NO_CLUSTER;
         if ((st = decide(B, M, N, d, &o, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags)) != MG_OK)
             return st;
+        // The fallback keeps the pipeline depth, hence the kernel; its limit is set again anyway.
+        fwd = fwd_kernel(d, in.stages, 0);
+        if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      in.smem_bytes)) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute");
     }
     if (in.workspace_bytes > static_cast<int64_t>(MG_ATTN_STATIC_SCRATCH_BYTES))
         return fail(MG_ERR_INVALID_ARG,
                     "shape needs %lld bytes of split scratch; the static scratch holds %u bytes "
                     "(use mg_attn_plan / mg_attn_run)",
                     (long long)in.workspace_bytes, MG_ATTN_STATIC_SCRATCH_BYTES);
-    FwdKernel fwd = fwd_kernel(d, in.stages, 0);
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, in.smem_bytes);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute");
 
     CUtensorMap maps[5];
     std::memset(maps, 0, sizeof(maps));
