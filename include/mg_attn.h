@@ -121,7 +121,10 @@ typedef struct {
 } mg_attn_plan_info;
 
 /*
- * Make a plan for one problem shape on the current CUDA device. Validates the shape,
+ * Make a plan for one problem shape on the current CUDA device. This is the step the pages take
+ * before a graph's first launch: the optimized graph is transpiled and compiled for its fixed
+ * input shapes (documentation, tutorials/group-query-attention, "Launch Mirage-Generated GQA
+ * Kernel"; blog, section 5: compile and profile after the search). Validates the shape,
  * chooses the tiling and the N split from the device's SM count, and allocates the
  * plan's device workspace (fp32 partial numerators n_split*B*M*d and row sums
  * n_split*B*M, plus two status words). Synchronous. On success *out owns the plan.
@@ -136,7 +139,12 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d,
                           const mg_attn_options *opts, mg_attn_plan_t *out);
 
 /*
- * Enqueue O = attention(Q, K, V) on `stream`. Asynchronous and stream-ordered: no
+ * Enqueue O = attention(Q, K, V) on `stream`. Restates the generated host entry point of the
+ * CUDA transpiler, _execute_mugraph(input_tensors, output_tensors, buf) (documentation,
+ * cuda-transpiler, "Generated CUDA Code Example"), called as optimized_graph(input_tensors) in
+ * the GQA tutorial ("Launch Mirage-Generated GQA Kernel"): the inputs are (Q, K, V) and the
+ * output O, as device pointers; the scratch buffer `buf` is the plan's workspace, so it is not an
+ * argument here. Asynchronous and stream-ordered: no
  * synchronisation, no allocation. Q, K, V, O are device pointers with the plan's shape
  * (see the top of this file), 16-byte aligned; O must not overlap the inputs. The caller
  * keeps ownership of all four. With programmatic dependent launch (the default) the
@@ -189,11 +197,19 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
 mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const void *Q, const void *K,
                               const void *V, void *O, mg_stream_t stream);
 
-/* Synchronise the device, free the plan's workspace and the plan. NULL is MG_ERR_INVALID_ARG. */
+/*
+ * Synchronise the device, then free the plan's workspace (the scratch buffer `buf` that the
+ * generated entry point takes from its caller: documentation, cuda-transpiler, "Generated CUDA
+ * Code Example"), its host staging and the plan. NULL is MG_ERR_INVALID_ARG; MG_ERR_CUDA if the
+ * synchronisation reports an error (the memory is freed all the same).
+ */
 mg_status mg_attn_destroy(mg_attn_plan_t plan);
 
 /*
- * Sticky device-side status of the plan: MG_OK, or MG_ERR_TIMEOUT once any in-kernel wait
+ * Sticky device-side status of the plan, reported in the codes above, whose first four restate
+ * the CUDA transpiler's error enum (blog, section 5.1: CUDA_T_SUCCESS, CUDA_T_INSUFFICIENT_SMEM,
+ * CUDA_T_LAYOUT_ERROR, CUDA_T_CONFIG_ERROR); the pages have no in-kernel timeout, so
+ * MG_ERR_TIMEOUT is this library's. MG_OK, or MG_ERR_TIMEOUT once any in-kernel wait
  * of any run of this plan ran out (the kernels then stop early and O is undefined).
  * Synchronises the device to read it. MG_ERR_CUDA if the read itself fails.
  */
