@@ -48,6 +48,7 @@ WORKLOAD = "gqa"  # Q (2,256,64), K (2,64,4096), V (2,4096,64)
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "mg_attn_fwd_partial_gqa.md")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+QUEUE_FILL_CYCLES = 2_000_000  # device-side sleep ahead of a timed region (~1 ms at 2 GHz)
 
 
 def parse_args():
@@ -148,7 +149,7 @@ class ClockSampler:
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -182,7 +183,7 @@ class ClockSampler:
                 self.thread.join(timeout=2)
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
+        sm, smax, loaded, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -193,13 +194,19 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                if len(parts) > 9 and float(parts[9]) >= 50.0:
+                    loaded.append(sm[-1])
+            except ValueError:
+                pass
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": len(loaded),
+                "sm_mhz_median_all": statistics.median(sm)}
 
 
 # ------------------------------------------------------------------ CPU (oracle) timing
@@ -324,6 +331,8 @@ def measure_workload(name, steps, peaks, stream, exp_rate_ns, flags=0):
         g.replay()
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(QUEUE_FILL_CYCLES)  # the GPU waits while the host queues the replays
     e0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(reps):
@@ -358,6 +367,19 @@ def measure_workload(name, steps, peaks, stream, exp_rate_ns, flags=0):
             "bound": "hbm" if t_hbm >= t_tensor else "tensor", "fused_kernel_us_median": k_us,
             "n_split": info["n_split"], "cluster_ctas": info["cluster_ctas"], "buffer_sets": n_sets,
             "ceilings": ceilings(info, B, M, N, exp_rate_ns, roof)}
+
+
+def per_config_summary(line):
+    """Compact table as the line's last key: for every workload, [µs per call, % of roofline] of the
+    graph as written and of the two opt-in variants, plus the headline step."""
+    out = {"gqa_headline": [round(line["us_per_call"], 3), round(100 * line["roofline_fraction_of_step"], 2)]}
+    for key, tag in (("per_config", "plain"), ("per_config_safe_softmax", "safe_softmax"),
+                     ("per_config_qk_norm", "qk_norm")):
+        if key in line:
+            out[tag] = {name: [round(r["us_per_call"], 2), round(100 * r["roofline_frac"], 1)]
+                        for name, r in line[key].items()}
+    out["format"] = "[us per call, % of roofline]"
+    return out
 
 
 def main():
@@ -404,6 +426,9 @@ def main():
     plan = mg.Plan(B, M, N, d)
     info = plan.info
     stream = torch.cuda.Stream()
+    # Clocks are sampled over the whole GPU arm (warm-up, the timed regions, the per-workload
+    # tables): the headline region alone is shorter than one 200 ms sample.
+    arm_clocks = ClockSampler(local_rank).__enter__()
     sh = stream.cuda_stream
 
     def step(i):
@@ -439,6 +464,11 @@ def main():
         torch.cuda.synchronize()
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
+        # The stream sleeps on the device (~1 ms) before the first event, so that the host has
+        # queued the timed launches by the time the GPU reaches it: the events then time the
+        # GPU's execution of the K steps, not the host's submission of the first of them.
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(QUEUE_FILL_CYCLES)
         ev0.record(stream)
         fn()
         ev1.record(stream)
@@ -454,10 +484,8 @@ def main():
             if g_rem:
                 g_rem.replay()
 
-    # Timed region 1 (the value): K steps replayed from CUDA graphs, clocks sampled meanwhile.
-    with ClockSampler(local_rank) as clocks:
-        ms_graph = timed(graph_steps)
-    clk = clocks.summary()
+    # Timed region 1 (the value): K steps replayed from CUDA graphs.
+    ms_graph = timed(graph_steps)
 
     # Timed region 2: the same K steps as a plain host loop of mg_attn_run calls.
     def loop_steps():
@@ -541,6 +569,10 @@ def main():
     poly_clk, poly_ns = mg.diag_exp_rate(2000, poly=True)
 
     if rank != 0:
+        arm_clocks.__exit__(None, None, None)
+        plan.destroy()
+        if world > 1:
+            dist.destroy_process_group()
         return
     us_graph = ms_graph * 1e3 / args.steps
     us_loop = ms_loop * 1e3 / args.steps
@@ -574,7 +606,6 @@ def main():
         "e2e": {"value": job_tflops(fl, n_e2e, world, ms_e2e), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e, "us_per_call": ms_e2e * 1e3 / n_e2e},
         "gpu_launches": args.steps * info["kernels_per_run"],
-        "clocks": clk,
         "ceilings": dict(ceilings(info, B, M, N, exp_ns, roof_t * 1e6),
                          exp_per_clk_per_sm_mufu=exp_clk, exp_per_ns_per_sm_mufu=exp_ns,
                          exp_per_clk_per_sm_fma_poly=poly_clk, exp_per_ns_per_sm_fma_poly=poly_ns),
@@ -593,7 +624,12 @@ def main():
             line["per_config_qk_norm"] = {
                 name: measure_workload(name, args.per_config_steps, peaks, stream, exp_ns, flags=mg.MG_FLAG_QK_NORM)
                 for name in _inputs.CONFIG_ORDER}
+    arm_clocks.__exit__(None, None, None)
+    line["clocks"] = dict(arm_clocks.summary(), window="the whole GPU arm: warm-up, timed regions, "
+                                                      "per-workload tables")
+    if world == 1:
         line["cpu_baseline"] = cpu_baseline(q, k, v, args.cpu_seconds)
+        line["summary"] = per_config_summary(line)
     print(json.dumps(line), flush=True)
     plan.destroy()
     if world > 1:
