@@ -125,6 +125,12 @@ CombineKernel combine_kernel(int64_t d, int n_split)
     return d == 64 ? combine_kernel_d<64>(n_split) : combine_kernel_d<128>(n_split);
 }
 
+// Rows of partials per split: B*M for the second kernel, whole 128-row tiles for the cluster combine.
+int64_t partial_rows(int64_t B, int64_t M, bool cluster)
+{
+    return cluster ? B * ((M + mg::kBlockM - 1) / mg::kBlockM) * mg::kBlockM : B * M;
+}
+
 // Validation and tiling decisions; touches no GPU.
 mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int32_t num_sms,
                  int32_t max_smem, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags)
@@ -205,10 +211,10 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     // The fused kernel writes O itself unless split partials go through the second kernel.
     info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
-    // Split partials for the second kernel: numerators, row sums and (max-subtracted variant) row maxima.
+    // Split partials: numerators, row sums and (max-subtracted variant) row maxima, for every split
+    // and row; the cluster combine keeps whole 128-row tiles (rows past M included).
     const int64_t row_words = (o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) ? 2 : 1;
-    const int64_t partial_bytes =
-        (n_split > 1 && !cluster) ? (n_split * B * M * d + n_split * B * M * row_words) * 4 : 0;
+    const int64_t partial_bytes = n_split > 1 ? n_split * partial_rows(B, M, cluster) * (d + row_words) * 4 : 0;
     // QK-norm: key-vector scales (B*N floats, then 128 more that reads of a last tile past N may
     // touch), from a 256-byte boundary.
     const int64_t scale_bytes = qk_norm ? 256 + (B * N + 128) * 4 : 0;
@@ -473,12 +479,15 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     uint8_t *ws = static_cast<uint8_t *>(p->workspace);
     p->status = reinterpret_cast<int *>(ws);
     std::memset(p->maps, 0, sizeof(p->maps));
-    if (info.n_split > 1 && info.cluster_ctas == 0) {
+    if (info.n_split > 1) {
+        const size_t rows = static_cast<size_t>(info.n_split) * partial_rows(B, M, info.cluster_ctas > 0);
         p->ws_o = reinterpret_cast<float *>(ws + 256);
-        p->ws_l = p->ws_o + static_cast<size_t>(info.n_split) * B * M * d;
+        p->ws_l = p->ws_o + rows * d;
         if (flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM))
-            p->ws_m = p->ws_l + static_cast<size_t>(info.n_split) * B * M;
-        // ws_o as (n_split*B, M, d) fp32, stored in {32, 128} boxes.
+            p->ws_m = p->ws_l + rows;
+    }
+    if (info.n_split > 1 && info.cluster_ctas == 0) {
+        // ws_o as (n_split*B, M, d) fp32, stored in {32, 128} boxes by the TMA.
         st = encode_3d(&p->maps[4], p->ws_o, d, M, static_cast<uint64_t>(info.n_split) * B, 32u, 128u, 4);
         if (st != MG_OK) {
             cudaFree(p->workspace);
@@ -565,6 +574,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.n_split = in.n_split;
     prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
     prm.O = static_cast<__half *>(O);
+    prm.ws_o = plan->ws_o;
     prm.ws_l = plan->ws_l;
     prm.ws_m = plan->ws_m;
     prm.col_scale = plan->col_scale;
@@ -793,9 +803,9 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     for (int i = 0; i < 4; ++i)
         if ((st = encode_3d(&maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i])) != MG_OK)
             return st;
-    float *ws_o = (in.n_split > 1 && in.cluster_ctas == 0) ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
-    if (ws_o && (st = encode_3d(&maps[4], ws_o, ud, uM, static_cast<uint64_t>(in.n_split) * uB, 32u, 128u, 4)) !=
-                    MG_OK)
+    float *ws_o = in.n_split > 1 ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
+    if (ws_o && in.cluster_ctas == 0 &&
+        (st = encode_3d(&maps[4], ws_o, ud, uM, static_cast<uint64_t>(in.n_split) * uB, 32u, 128u, 4)) != MG_OK)
         return st;
 
     mg::FwdParams prm;
@@ -808,7 +818,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
     prm.O = static_cast<__half *>(O);
     prm.status = reinterpret_cast<int *>(sd->scratch);
-    prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * B * M * d : nullptr;
+    prm.ws_o = ws_o;
+    prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * partial_rows(B, M, in.cluster_ctas > 0) * d : nullptr;
     prm.ws_m = nullptr;
     prm.col_scale = nullptr;
     prm.timeout_ns = timeout_ns;

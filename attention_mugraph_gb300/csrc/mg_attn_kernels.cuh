@@ -109,6 +109,7 @@ struct FwdParams {
     int n_split;
     int cluster_reduce;      // the n_split CTAs of a row tile form a cluster and combine on chip
     __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
+    float *ws_o;             // (n_split, B, M, d) partial numerators (the cluster combine's plain stores)
     float *ws_l;             // (n_split, B, M) partial row sums
     float *ws_m;             // (n_split, B, M) partial row maxima (max-subtracted variant only)
     float *col_scale;        // QK-norm: (B, N) key-vector scales 1/rms, written by the row-maximum
@@ -304,6 +305,96 @@ __device__ __forceinline__ float reduce_scatter8(const float (&a)[8], int lane)
     return (h2 ? b2[1] : b2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? b2[0] : b2[1], 4);
 }
 
+// Index of the (split j, batch b, row tile mt) tile among the cluster combine's partial tiles.
+__device__ __forceinline__ size_t cluster_tile(const FwdParams &p, int j, int b, int mt)
+{
+    return (static_cast<size_t>(j) * p.B + b) * p.m_tiles_per_b + mt;
+}
+
+// The reading side of the cluster combine, for CTA rank j of row tile (b, mt): rows
+// [128 j / n, 128 (j+1) / n) of the tile as (sum_r w_r O_r) / (sum_r w_r l_r) over the n ranks,
+// w_r = 1 (exp(m_r - max_r m_r) when SAFE), written as fp16 O. Partial tiles are tile-major
+// (float4 column group outermost, 128 rows innermost). An element is (column group, row); the two
+// lanes of a pair take the same elements, lane h the ranks [h RPL, h RPL + RPL), and a pair takes
+// 8 / RPL elements at a time, so that each thread has its 8 loads in flight together. The pair then
+// adds its two sums in a fixed order (lower ranks first) and each lane writes two of the element's
+// four columns: the result does not depend on timing.
+template <int D, bool SAFE, int RPL>
+__device__ __forceinline__ void cluster_combine_rows(const FwdParams &p, int b, int mt, int m0, int j, int tid)
+{
+    constexpr int G = D / 4;          // float4 column groups per row
+    constexpr int EPP = 8 / RPL;      // elements per pair per batch of loads
+    constexpr int kPairs = kSoftmaxThreads / 2;
+    const int n = p.n_split;
+    const int lo = j * kBlockM / n;
+    // Rows this rank combines: its share of the tile, cut at M (rows past M hold no partials).
+    const int R = max(0, min((j + 1) * kBlockM / n, p.M - m0) - lo);
+    const int E = R * G;
+    const int pair = tid >> 1;
+    const int h = tid & 1;
+    const unsigned pair_mask = 3u << (tid & 30);
+    const size_t tiles_per_rank = static_cast<size_t>(p.B) * p.m_tiles_per_b;
+    const size_t tile0 = static_cast<size_t>(b) * p.m_tiles_per_b + mt;
+    const float4 *ws4 = reinterpret_cast<const float4 *>(p.ws_o);
+    for (int base = pair; base < E; base += kPairs * EPP) {
+        // All loads first (L1 is bypassed: the partials were written by other SMs).
+        float4 v[8];
+        float lv[8], mr[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int e = base + (s / RPL) * kPairs;
+            const int r = h * RPL + s % RPL;
+            if (e < E && r < n) {
+                const size_t t = r * tiles_per_rank + tile0;
+                const int rr = lo + e % R;
+                v[s] = __ldcg(ws4 + (t * G + e / R) * kBlockM + rr);
+                lv[s] = __ldcg(p.ws_l + t * kBlockM + rr);
+                if (SAFE)
+                    mr[s] = __ldcg(p.ws_m + t * kBlockM + rr);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < EPP; ++k) {
+            const int e = base + k * kPairs;  // the same on both lanes of the pair
+            if (e >= E)
+                break;
+            float mmax = 0.f;
+            if (SAFE) {
+                mmax = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < RPL; ++q)
+                    if (h * RPL + q < n)
+                        mmax = fmaxf(mmax, mr[k * RPL + q]);
+                mmax = fmaxf(mmax, __shfl_xor_sync(pair_mask, mmax, 1));
+            }
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+            float lsum = 0.f;
+#pragma unroll
+            for (int q = 0; q < RPL; ++q) {
+                if (h * RPL + q < n) {
+                    const int s = k * RPL + q;
+                    const float w = SAFE ? ptx::ex2_approx((mr[s] - mmax) * ptx::kLog2e) : 1.f;
+                    a[0] = fmaf(w, v[s].x, a[0]);
+                    a[1] = fmaf(w, v[s].y, a[1]);
+                    a[2] = fmaf(w, v[s].z, a[2]);
+                    a[3] = fmaf(w, v[s].w, a[3]);
+                    lsum = fmaf(w, lv[s], lsum);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float other = __shfl_xor_sync(pair_mask, a[c], 1);
+                a[c] = h == 0 ? a[c] + other : other + a[c];
+            }
+            const float lother = __shfl_xor_sync(pair_mask, lsum, 1);
+            lsum = h == 0 ? lsum + lother : lother + lsum;
+            const int rr = lo + e % R;
+            const uint32_t o = ptx::pack_half2(__fdiv_rn(a[2 * h], lsum), __fdiv_rn(a[2 * h + 1], lsum));
+            *reinterpret_cast<uint32_t *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + (e / R) * 4 + 2 * h) = o;
+        }
+    }
+}
+
 // Evaluation variants of kernel 1, compiled separately so that each carries only its own code.
 enum Variant : int {
     kPlain = 0,    // the graph as written
@@ -324,7 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     using BI = Bars<STAGES, kPBuffers>;
     static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
-    static_assert(128 * (D + 8) * 2 + 2 * 128 * 4 <= STAGES * C::kStageBytes, "cluster staging must fit in the K/V ring");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -840,16 +930,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l = l_xchg[row] + l_xchg[kBlockM + row];
         if (o_ready) {
             ptx::tc_fence_after();
-            // The K/V ring is idle (every PV has completed): stage this CTA's output there. For the
-            // on-chip combine: the normalised partial O_j / l_j as fp16 rows of d + 8 halves (the
-            // pad keeps 8 consecutive rows on distinct banks), then the fp32 row sums l_j and
-            // maxima m_j, read by the cluster's CTAs at teardown. The normalised values are convex
-            // combinations of V rows, so fp16 holds them to half an ulp of max |V|, and the
-            // exchange moves half the bytes of fp32 numerators. Otherwise the 128-byte-swizzled
-            // layout the output tensor maps expect, then a TMA store.
+            // The K/V ring is idle (every PV has completed). With one split, or with partials for
+            // the second kernel, this CTA's output is staged there in the 128-byte-swizzled layout
+            // the output tensor maps expect, then written by a TMA store. With the cluster combine,
+            // each thread stores its row's fp32 partial numerator straight from registers to the
+            // workspace (plain stores, which the cluster barrier below publishes).
             const uint32_t stage = sStage0;
-            __half *stage_h = reinterpret_cast<__half *>(smem + C::kQBytes);
-            float *stage_lm = reinterpret_cast<float *>(smem + C::kQBytes + kBlockM * (D + 8) * 2);
             if (warp_rows) {
 #pragma unroll
                 for (int c = 0; c < C::kHalfCols / 32; ++c) {
@@ -858,20 +944,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, r);
                     ptx::tmem_ld_wait(r);
                     if (p.cluster_reduce) {
-                        // The split's normalised partial O_j / l_j in fp16 (every value a convex
-                        // combination of V rows), rows of d + 8 halves.
-                        // One correctly rounded reciprocal, then products (l = 0 only if every
-                        // exponential of the split underflowed; its partial is then 0).
-                        const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
-                        uint4 *dst = reinterpret_cast<uint4 *>(stage_h + row * (D + 8) + col);
+                        // Tile-major: float4 column group outermost, the tile's 128 rows innermost,
+                        // so the 32 lanes of a warp (32 consecutive rows) store 512 contiguous bytes.
+                        float4 *dst = reinterpret_cast<float4 *>(p.ws_o) +
+                                      cluster_tile(p, j, b, mt) * (D / 4) * kBlockM + (col / 4) * kBlockM + row;
+                        if (m0 + row < p.M) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t w4[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h)
-                                w4[h] = ptx::pack_half2(__uint_as_float(r[8 * q + 2 * h]) * inv,
-                                                        __uint_as_float(r[8 * q + 2 * h + 1]) * inv);
-                            dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            for (int q = 0; q < 8; ++q)
+                                dst[q * kBlockM] =
+                                    make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
                         }
                     } else if (p.n_split == 1) {
                         // fp16 O/l: chunk col/64 of a {64, 128} fp16 box; this slice is units (col%64)/8 .. +3.
@@ -898,120 +980,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.cluster_reduce) {
-                if (g == 0) {
-                    stage_lm[row] = l;
-                    stage_lm[kBlockM + row] = m;
-                }
-            } else {
-                if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
-                    const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
-                    p.ws_l[r] = l;
-                    if (kSafeMax)
-                        p.ws_m[r] = m;
-                }
+            if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
+                // Cluster combine: 128-row tiles (rows past M unwritten); second kernel: rows of M.
+                const size_t r = p.cluster_reduce ? cluster_tile(p, j, b, mt) * kBlockM + row
+                                                  : (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
+                p.ws_l[r] = l;
+                if (kSafeMax)
+                    p.ws_m[r] = m;
+            }
+            if (!p.cluster_reduce) {
                 ptx::fence_proxy_async_smem();
                 ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
-            }
-            if (!p.cluster_reduce && sw == 0 && lane == 0) {
-                if (p.n_split == 1) {
+                if (sw == 0 && lane == 0) {
+                    if (p.n_split == 1) {
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c)  // O[b, m0:m0+128, 64c:64c+64]
-                        ptx::tma_store_3d(&tmO, stage + c * C::kChunkRows128, c * 64, m0, b);
-                } else {
+                        for (int c = 0; c < D / 64; ++c)  // O[b, m0:m0+128, 64c:64c+64]
+                            ptx::tma_store_3d(&tmO, stage + c * C::kChunkRows128, c * 64, m0, b);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c)  // ws_o[j, b, m0:m0+128, 32c:32c+32]
-                        ptx::tma_store_3d(&tmW, stage + c * C::kChunkRows128, c * 32, m0, j * p.B + b);
+                        for (int c = 0; c < D / 32; ++c)  // ws_o[j, b, m0:m0+128, 32c:32c+32]
+                            ptx::tma_store_3d(&tmW, stage + c * C::kChunkRows128, c * 32, m0, j * p.B + b);
+                    }
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_group_read0();
                 }
-                ptx::bulk_commit_group();
-                ptx::bulk_wait_group_read0();
             }
         }
     }
 
-    // On-chip combine of the split partials: after the first cluster barrier every CTA's staged
-    // (O_j / l_j, l_j, m_j) is visible; CTA rank j forms rows [128 j / n, 128 (j+1) / n) of its row
-    // tile as sum_r c_r (O_r / l_r) / sum_r c_r with c_r = l_r (times exp(m_r - max m) in the
-    // max-subtracted variant), over all n ranks in rank order (reproducible), and writes fp16 O. The second barrier
-    // keeps each CTA's shared memory alive until the others have read it. Every thread of every
-    // CTA reaches both barriers, on the unwinding path too.
+    // Cluster combine of the split partials. The cluster only co-schedules the n_split CTAs of a
+    // row tile and gives them one hardware barrier: the partials themselves go through L2 (each
+    // CTA's fp32 numerators, row sums and, max-subtracted, row maxima, stored above). After the
+    // barrier (release/acquire at cluster scope) CTA rank j forms rows [128 j / n, 128 (j+1) / n)
+    // of its row tile as (sum_r w_r O_r) / (sum_r w_r l_r), w_r = 1 (exp(m_r - max m) when
+    // max-subtracted), over the n ranks in rank order (reproducible), and writes fp16 O. Nothing
+    // reads another CTA's shared memory, so no CTA waits for the others after that. Every thread
+    // of every CTA reaches the barrier, on the unwinding path too. (Measured on GB300: moving the
+    // partials through distributed shared memory instead took ~1.3-1.7 us per exchange, in fp16.)
     __syncwarp();
     if (p.cluster_reduce) {
         ptx::cluster_sync();
         if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
-            constexpr int G = D / 8;  // 16-byte groups (8 fp16 columns) per row
+            const int tid = threadIdx.x - 64;
             const int n = p.n_split;
-            const int lo = j * kBlockM / n;
-            const int hi = (j + 1) * kBlockM / n;
-            const uint32_t st = ptx::smem_u32(smem + C::kQBytes);
-            const uint32_t ls = st + kBlockM * (D + 8) * 2;
-            const uint32_t ms = ls + kBlockM * 4;
-            for (int it = threadIdx.x - 64; it < (hi - lo) * G; it += kSoftmaxThreads) {
-                const int rr = lo + it / G;
-                const int g = it % G;
-                if (m0 + rr >= p.M)
-                    continue;
-                const uint32_t off = static_cast<uint32_t>((rr * (D + 8) + g * 8) * 2);
-                // Rank r's normalised partial enters with weight c_r = l_r (times exp(m_r - max_r m_r)
-                // in the max-subtracted variant, where l_r was taken relative to m_r).
-                float wt[kMaxClusterRanks];
-#pragma unroll
-                for (int r = 0; r < kMaxClusterRanks; ++r)
-                    wt[r] = 1.f;
-                if (kSafeMax) {
-                    float mr[kMaxClusterRanks];
-                    float mmax = -INFINITY;
-#pragma unroll
-                    for (int r = 0; r < kMaxClusterRanks; ++r) {
-                        if (r < n) {
-                            mr[r] = ptx::ld_cluster_f32(ptx::map_to_rank(ms + rr * 4, r));
-                            mmax = fmaxf(mmax, mr[r]);
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < kMaxClusterRanks; ++r)
-                        if (r < n)
-                            wt[r] = ptx::ex2_approx((mr[r] - mmax) * ptx::kLog2e);
-                }
-                // Every rank's values are requested before the first is used: the remote reads
-                // are then in flight together rather than one round trip after another.
-                float4 v[kMaxClusterRanks];
-                float lv[kMaxClusterRanks];
-#pragma unroll
-                for (int r = 0; r < kMaxClusterRanks; ++r) {
-                    if (r < n) {
-                        v[r] = ptx::ld_cluster_v4(ptx::map_to_rank(st + off, r));
-                        lv[r] = ptx::ld_cluster_f32(ptx::map_to_rank(ls + rr * 4, r));
-                    }
-                }
-                float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                float lsum = 0.f;
-#pragma unroll
-                for (int r = 0; r < kMaxClusterRanks; ++r) {
-                    if (r < n) {
-                        const float c = wt[r] * lv[r];
-                        const uint32_t words[4] = {__float_as_uint(v[r].x), __float_as_uint(v[r].y),
-                                                   __float_as_uint(v[r].z), __float_as_uint(v[r].w)};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[h]));
-                            a[2 * h] = fmaf(c, f.x, a[2 * h]);
-                            a[2 * h + 1] = fmaf(c, f.y, a[2 * h + 1]);
-                        }
-                        lsum += c;
-                    }
-                }
-                uint4 w;
-                w.x = ptx::pack_half2(__fdiv_rn(a[0], lsum), __fdiv_rn(a[1], lsum));
-                w.y = ptx::pack_half2(__fdiv_rn(a[2], lsum), __fdiv_rn(a[3], lsum));
-                w.z = ptx::pack_half2(__fdiv_rn(a[4], lsum), __fdiv_rn(a[5], lsum));
-                w.w = ptx::pack_half2(__fdiv_rn(a[6], lsum), __fdiv_rn(a[7], lsum));
-                *reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + g * 8) = w;
-            }
+            if (n <= 2)
+                cluster_combine_rows<D, kSafeMax, 1>(p, b, mt, m0, j, tid);
+            else if (n <= 4)
+                cluster_combine_rows<D, kSafeMax, 2>(p, b, mt, m0, j, tid);
+            else if (n <= 8)
+                cluster_combine_rows<D, kSafeMax, 4>(p, b, mt, m0, j, tid);
+            else
+                cluster_combine_rows<D, kSafeMax, 8>(p, b, mt, m0, j, tid);
         }
-        // Only "every CTA has finished reading the others' shared memory" is needed here; a
-        // release would also hold each CTA until its output stores had drained.
-        ptx::cluster_sync_relaxed();
     }
 
     // Teardown: every tensor-memory access of the CTA is ordered before the free.

@@ -132,6 +132,32 @@ def test_cluster_combine_of_cancelling_splits(n_split, flags):
     assert_parity(O, ref, f"cancelling splits, cluster {n_split}, flags {flags}")
 
 
+@pytest.mark.parametrize("n_split", [2, 16])
+@pytest.mark.parametrize("flags", [0, mg.MG_FLAG_SAFE_SOFTMAX])
+def test_cluster_combine_of_cancelling_splits_large_v(n_split, flags):
+    # Two splits each dominated by one V row of magnitude ~30, of opposite signs: O (~0.8) is the
+    # small difference of two large partials, and the bound 2e-3 * (1 + |O|) does not grow with
+    # them. Split j takes column tiles j, j + n_split, ..., so the dominant columns sit in tiles 0
+    # and 1: splits 0 and 1 for every n_split >= 2. V is the earlier test's values times 8, which
+    # fp16 holds exactly.
+    B, M, N, d = 1, 3, 2048, 64
+    q = torch.zeros((B, M, d))
+    q[0, :, 0] = torch.tensor([1.0, 1.25, 1.5])
+    k = torch.zeros((B, d, N))
+    k[0, 0, :] = -5.0
+    k[0, 0, 0] = 5.0    # column tile 0: split 0
+    k[0, 0, 128] = 5.0  # column tile 1: split 1
+    v = torch.randn((B, N, d), generator=torch.Generator().manual_seed(9)) * 0.01
+    v[0, 0, :] = 3.9
+    v[0, 128, :] = -3.7
+    q, k, v = q.half(), k.half(), (v.half() * 8)
+    ref = oracle.attention(q, k, v)
+    assert np.abs(ref).max() < 1.2  # the partials (~30) nearly cancel
+    O, plan = run_gpu(q, k, v, n_split=n_split, flags=flags)
+    assert plan.info["cluster_ctas"] == n_split
+    assert_parity(O, ref, f"cancelling splits |V| ~ 30, cluster {n_split}, flags {flags}")
+
+
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
     # Scores 0 everywhere -> every weight is exp(0)=1: any column past N that leaked into the row
     # sum (zero-filled K gives exp(0)=1 too) would pull the mean toward 0.
