@@ -491,3 +491,155 @@ class Sim:
             except StopIteration:
                 del nxt[name]
         return steps
+
+
+class PairSim(Sim):
+    """The two-Q-tile kernel (mg_attn_fwd_pair): each CTA holds two 128-row Q tiles of one batch
+    and streams every K/V tile once for both. Softmax group g owns Q tile g, its S buffer g, its
+    single P buffer g and its accumulator O_g; no row data passes between the groups. Per step t:
+    the S warp issues S_0 and S_1 (each once its group has read the previous S out of its buffer),
+    the P.V warp issues O_0 += P_0 V_t and O_1 += P_1 V_t (each once its group has written P), and
+    the commit after the second one releases the K/V stage. Graph as written only (no row-maximum
+    pass).
+
+    Mutations: "pair_s_no_sempty_wait", "pair_no_pempty_wait" (P written before the previous P.V
+    read it), "pair_kvempty_after_pv0" (the stage released after the first P.V), plus the base
+    class's "producer_no_kvempty_wait" and "drain_only_on_failure"."""
+
+    def __init__(self, T: int, stages: int, seed: int, mutations=(), abort_rate: float = 0.0):
+        super().__init__(T, stages, 2, PLAIN, seed, mutations, abort_rate)
+        self.pv_done_g = [0, 0]
+
+    def _s_warp(self):
+        S = self.S
+        ok = yield self.wait("QFull", 0, 0, "S warp Q")
+        t = 0
+        while ok and t < self.T:
+            s = t % S
+            if not (yield self.wait(f"KFull{s}", (t // S) & 1, t // S, f"S warp K {t}")):
+                ok = False
+                break
+            for g in range(2):
+                if t >= 1 and "pair_s_no_sempty_wait" not in self.mut:
+                    if not (yield self.wait(f"SEmpty{g}", (t - 1) & 1, t - 1, f"S warp S{g} buffer {t}")):
+                        ok = False
+                        break
+                yield ("do", lambda t=t, s=s, g=g: self._issue_s_pair(t, s, g))
+            t += 1
+        if not ok or "drain_only_on_failure" not in self.mut:
+            yield ("drain", "pipe")
+
+    def _issue_s_pair(self, t, s, g):
+        if not self.abort:
+            if not self.q_loaded:
+                self.fail(f"S MMA {t} issued before Q landed")
+            if self.kst[s] != t:
+                self.fail(f"S{g} MMA {t} reads K stage {s} holding step {self.kst[s]}")
+            if self.s_readers[g]:
+                self.fail(f"S{g} MMA {t} writes S buffer {g} while softmax warps read it")
+        self.k_readers[s] += 1
+        self.s_pending_write[g] = True
+
+        def done():
+            self.k_readers[s] -= 1
+            self.sbuf[g] = t
+            self.s_pending_write[g] = False
+
+        self.pipe.append(("mma", done))
+        self.pipe.append(("commit", f"SFull{g}"))
+
+    def _pv_warp(self):
+        S = self.S
+        ok = True
+        t = 0
+        while ok and t < self.T:
+            s = t % S
+            if not (yield self.wait(f"VFull{s}", (t // S) & 1, t // S, f"PV warp V {t}")):
+                ok = False
+                break
+            for g in range(2):
+                if not (yield self.wait(f"PFull{g}", t & 1, t, f"PV warp P{g} {t}")):
+                    ok = False
+                    break
+                yield ("do", lambda t=t, s=s, g=g: self._issue_pv_pair(t, s, g))
+            t += 1
+        if ok:
+            for g in range(2):
+                ok = yield self.wait(f"PEmpty{g}", (self.T - 1) & 1, self.T - 1, f"PV warp tail P{g}")
+                if not ok:
+                    break
+            if not ok and "drain_only_on_failure" not in self.mut:
+                yield ("drain", "pipe")
+        else:
+            yield ("drain", "pipe")
+
+    def _issue_pv_pair(self, t, s, g):
+        if not self.abort:
+            if self.pbuf[g] != t:
+                self.fail(f"P.V{g} MMA {t} reads P buffer {g} holding tile {self.pbuf[g]}")
+            if self.vst[s] != t:
+                self.fail(f"P.V{g} MMA {t} reads V stage {s} holding step {self.vst[s]}")
+        self.p_readers[g] += 1
+        self.v_readers[s] += 1
+        self.pv_issued += 1
+
+        def done():
+            self.p_readers[g] -= 1
+            self.v_readers[s] -= 1
+            self.pv_done += 1
+            self.pv_done_g[g] += 1
+
+        self.pipe.append(("mma", done))
+        self.pipe.append(("commit", f"PEmpty{g}"))
+        if g == 1 or "pair_kvempty_after_pv0" in self.mut:
+            if g == 0 or "pair_kvempty_after_pv0" not in self.mut:
+                self.pipe.append(("commit", f"KvEmpty{s}"))
+        if g == 1 and t == self.T - 1:
+            self.pipe.append(("commit", "OFull"))
+
+    def _softmax_warp(self, g, gw):
+        who = f"softmax g{g}w{gw}"
+        ok = True
+        t = 0
+        while ok and t < self.T:
+            if not (yield self.wait(f"SFull{g}", t & 1, t, f"{who} S {t}")):
+                ok = False
+                break
+            yield ("do", lambda t=t: self._read_s(g, t, +1))             # half 0 loaded
+            if t >= 1 and "pair_no_pempty_wait" not in self.mut:
+                if not (yield self.wait(f"PEmpty{g}", (t - 1) & 1, t - 1, f"{who} P buffer {t}")):
+                    ok = False
+                    break
+            yield ("do", lambda t=t: self._write_p_pair(g, t, (gw, 0)))
+            yield ("do", lambda t=t: self._read_s(g, t, -1))             # half 1 loaded: S released
+            yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
+            yield ("do", lambda t=t: self._write_p_pair(g, t, (gw, 1)))
+            yield ("do", lambda: self.bars[f"PFull{g}"].arrive())
+            t += 1
+        o_ok = ok and (yield self.wait("OFull", 0, 0, f"{who} O"))
+        o_ready = yield ("gbar", "softmax", 2 * GROUP_WARPS, o_ok)
+        if o_ready:
+            yield ("do", lambda: self._read_o())
+
+    def _write_p_pair(self, g, t, piece):
+        if self.abort:
+            return
+        if self.p_readers[g]:
+            self.fail(f"P buffer {g} written for tile {t} while a P.V MMA reads it")
+        if self.p_tile_writing[g] != t:
+            if self.pbuf[g] is not None and self.pv_done_g[g] <= self.pbuf[g]:
+                self.fail(f"P buffer {g} overwritten for tile {t} before P.V of tile {self.pbuf[g]}")
+            self.p_tile_writing[g] = t
+            self.pieces[g] = set()
+            self.pbuf[g] = None
+        self.pieces[g].add(piece)
+        if len(self.pieces[g]) == 2 * GROUP_WARPS:
+            self.pbuf[g] = t
+
+    def _read_o(self):
+        if self.pv_done != 2 * self.T:
+            self.fail(f"O read after {self.pv_done} of {2 * self.T} P.V products")
+        if any(bar.startswith(("KFull", "VFull")) for bar, _, _ in self.tma):
+            self.fail("output staged in the K/V ring while a copy into it is in flight")
+        if any(self.k_readers) or any(self.v_readers):
+            self.fail("output staged in the K/V ring while an MMA reads it")

@@ -97,3 +97,47 @@ def test_barrier_parity_semantics():
         c = pm.Barrier("y", 1)
         c.arrive(expect_tx=4)
         c.complete_tx(8)
+
+
+# ------------------------------------------------------------------ two-Q-tile kernel
+
+@pytest.mark.parametrize("stages", [2, 3, 4, 5, 6])
+def test_pair_protocol_as_built_is_clean(stages):
+    for T, seed in itertools.product((1, 2, 3, 4, 7, 12), range(12)):
+        pm.PairSim(T, stages, seed).run()
+
+
+def caught_pair(mutation, tries=40):
+    for T, stages, seed in itertools.product((1, 2, 3, 5, 8), (6, 3, 2), range(tries)):
+        try:
+            pm.PairSim(T, stages, seed, mutations=(mutation,)).run()
+        except pm.ProtocolError as e:
+            return str(e)
+    return None
+
+
+@pytest.mark.parametrize("mutation,expect", [
+    ("pair_s_no_sempty_wait", "writes S buffer"),       # S of the next tile over the one being read
+    ("pair_no_pempty_wait", "overwritten"),             # P rewritten before the previous P.V read it
+    ("pair_kvempty_after_pv0", "overwritten"),          # stage released while the second P.V reads V
+    ("producer_no_kvempty_wait", "stage"),
+])
+def test_pair_planted_hazards_are_caught(mutation, expect):
+    msg = caught_pair(mutation)
+    assert msg is not None and expect in msg, msg
+
+
+def test_pair_unwinding_from_any_wait_is_clean():
+    for T, stages, seed in itertools.product((1, 2, 3, 5, 8), (6, 3, 2), range(12)):
+        pm.PairSim(T, stages, seed, abort_rate=0.02).run()
+
+
+def test_pair_draining_only_after_a_failed_loop_leaves_mmas_in_flight():
+    hit = None
+    for T, stages, seed in itertools.product((1, 2, 3, 5, 8), (6, 3, 2), range(60)):
+        try:
+            pm.PairSim(T, stages, seed, mutations=("drain_only_on_failure",), abort_rate=0.1).run()
+        except pm.ProtocolError as e:
+            hit = str(e)
+            break
+    assert hit is not None and "in flight" in hit
