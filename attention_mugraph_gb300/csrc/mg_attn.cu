@@ -14,6 +14,7 @@
 #include <new>
 
 #include "mg_attn_kernels.cuh"
+#include "mg_attn_pair.cuh"
 #include "mg_combine.cuh"
 
 namespace {
@@ -93,6 +94,19 @@ FwdKernel fwd_kernel_variant(int64_t d, int stages)
     return nullptr;
 }
 
+// The two-Q-tile kernel (head dim 64, the graph as written) for a pipeline depth.
+FwdKernel pair_kernel(int stages)
+{
+    switch (stages) {
+    case 2: return mg::mg_attn_fwd_pair<2>;
+    case 3: return mg::mg_attn_fwd_pair<3>;
+    case 4: return mg::mg_attn_fwd_pair<4>;
+    case 5: return mg::mg_attn_fwd_pair<5>;
+    case 6: return mg::mg_attn_fwd_pair<6>;
+    default: return nullptr;
+    }
+}
+
 // The fused kernel for a head dim, pipeline depth and the MG_FLAG_* evaluation flags.
 FwdKernel fwd_kernel(int64_t d, int stages, int flags)
 {
@@ -125,10 +139,12 @@ CombineKernel combine_kernel(int64_t d, int n_split)
     return d == 64 ? combine_kernel_d<64>(n_split) : combine_kernel_d<128>(n_split);
 }
 
-// Rows of partials per split: B*M for the second kernel, whole 128-row tiles for the cluster combine.
+// Rows of partials per split: B*M for the second kernel; for the cluster combine, whole tiles of
+// min(M, 128) rows.
 int64_t partial_rows(int64_t B, int64_t M, bool cluster)
 {
-    return cluster ? B * ((M + mg::kBlockM - 1) / mg::kBlockM) * mg::kBlockM : B * M;
+    const int64_t tile_rows = M < mg::kBlockM ? M : mg::kBlockM;
+    return cluster ? B * ((M + mg::kBlockM - 1) / mg::kBlockM) * tile_rows : B * M;
 }
 
 // Validation and tiling decisions; touches no GPU.
@@ -154,7 +170,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         o = *opts;
     if (o.reserved != 0 ||
         (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX |
-                     MG_FLAG_QK_NORM)) != 0)
+                     MG_FLAG_QK_NORM | MG_FLAG_Q_PAIRS | MG_FLAG_NO_Q_PAIRS)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -162,18 +178,29 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     const int64_t m_tiles_per_b = (M + mg::kBlockM - 1) / mg::kBlockM;
     const int64_t m_tiles = B * m_tiles_per_b;
     const int64_t n_tiles = (N + mg::kBlockN - 1) / mg::kBlockN;
+    if ((o.flags & MG_FLAG_Q_PAIRS) && (o.flags & MG_FLAG_NO_Q_PAIRS))
+        return fail(MG_ERR_CONFIG, "MG_FLAG_Q_PAIRS and MG_FLAG_NO_Q_PAIRS together");
+
+    // One wave: as many splits per unit (a row tile, or a pair of them) as keep every SM busy,
+    // never fewer than one column tile per split.
+    auto one_wave = [&](int64_t units) {
+        int64_t n = units >= num_sms ? 1 : num_sms / units;
+        return n > n_tiles ? n_tiles : (n < 1 ? 1 : n);
+    };
+    // The two-Q-tile kernel applies to head dim 64, the graph as written and an even number of
+    // row tiles per batch, and only on request: measured on GB300 it is slower than the one-tile
+    // kernel on every workload (its per-tile loop is no faster, and it needs twice the splits for
+    // one wave).
+    const bool pair_applies = d == 64 && !(o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) &&
+                              m_tiles_per_b % 2 == 0;
+    const bool pair = pair_applies && (o.flags & MG_FLAG_Q_PAIRS);
+    const int64_t units = pair ? m_tiles / 2 : m_tiles;  // CTAs per split
 
     int64_t n_split = o.n_split;
     if (n_split < 0 || n_split > n_tiles)
         return fail(MG_ERR_CONFIG, "n_split=%lld out of range [0, %lld]", (long long)n_split, (long long)n_tiles);
     if (n_split == 0) {
-        // One wave: as many splits per row tile as keep every SM busy, never fewer than one
-        // column tile per split.
-        n_split = m_tiles >= num_sms ? 1 : num_sms / m_tiles;
-        if (n_split > n_tiles)
-            n_split = n_tiles;
-        if (n_split < 1)
-            n_split = 1;
+        n_split = one_wave(units);
         // Small problems: rather than more than 16 splits and a second kernel, take the largest
         // cluster (16) when that leaves at most 4 column tiles per CTA.
         if (n_split > kMaxCluster && !(o.flags & MG_FLAG_NO_CLUSTER) &&
@@ -181,15 +208,15 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
             n_split = kMaxCluster;
     }
     const bool cluster = !(o.flags & MG_FLAG_NO_CLUSTER) && n_split >= 2 && n_split <= kMaxCluster;
-    if (m_tiles * n_split > 0x7fffffffLL)
+    if (units * n_split > 0x7fffffffLL)
         return fail(MG_ERR_INVALID_ARG, "grid too large");
 
     const bool qk_norm = (o.flags & MG_FLAG_QK_NORM) != 0;
     int stages = o.stages == 0 ? auto_stages(d) : o.stages;
     if (stages < 2 || stages > 6)
         return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 6]", stages);
-    const uint32_t smem = mg::fwd_smem_bytes(static_cast<int>(d), stages);
-    if (static_cast<int64_t>(smem) > max_smem || !fwd_kernel(d, stages, o.flags))
+    const uint32_t smem = pair ? mg::pair_smem_bytes(stages) : mg::fwd_smem_bytes(static_cast<int>(d), stages);
+    if (static_cast<int64_t>(smem) > max_smem || !(pair ? pair_kernel(stages) : fwd_kernel(d, stages, o.flags)))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
 
@@ -205,14 +232,14 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->n_split = static_cast<int32_t>(n_split);
     info->stages = stages;
     info->threads = mg::kThreads;
-    info->grid_ctas = static_cast<int32_t>(m_tiles * n_split);
+    info->grid_ctas = static_cast<int32_t>(units * n_split);
     info->smem_bytes = static_cast<int32_t>(smem);
     info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
     // The fused kernel writes O itself unless split partials go through the second kernel.
     info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
     // Split partials: numerators, row sums and (max-subtracted variant) row maxima, for every split
-    // and row; the cluster combine keeps whole 128-row tiles (rows past M included).
+    // and row; the cluster combine keeps whole row tiles (rows past M included).
     const int64_t row_words = (o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) ? 2 : 1;
     const int64_t partial_bytes = n_split > 1 ? n_split * partial_rows(B, M, cluster) * (d + row_words) * 4 : 0;
     // QK-norm: key-vector scales (B*N floats, then 128 more that reads of a last tile past N may
@@ -220,12 +247,19 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     const int64_t scale_bytes = qk_norm ? 256 + (B * N + 128) * 4 : 0;
     info->workspace_bytes = 256 + partial_bytes + scale_bytes;
     info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
+    info->q_tiles_per_cta = pair ? 2 : 1;
     if (timeout_ns)
         *timeout_ns = o.timeout_ns ? static_cast<unsigned long long>(o.timeout_ns) : kDefaultTimeoutNs;
     if (flags)
         *flags = o.flags;
     g_last_error[0] = '\0';
     return MG_OK;
+}
+
+// The fused kernel a plan's decisions call for.
+FwdKernel plan_kernel(const mg_attn_plan_info &info, int flags)
+{
+    return info.q_tiles_per_cta == 2 ? pair_kernel(info.stages) : fwd_kernel(info.d, info.stages, flags);
 }
 
 // Host-buffer entry point: copies between the caller's pinned host buffers (read and written
@@ -445,7 +479,7 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     if (st != MG_OK)
         return st;
 
-    FwdKernel fwd = fwd_kernel(d, info.stages, flags);
+    FwdKernel fwd = plan_kernel(info, flags);
     e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              info.smem_bytes);
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
@@ -460,6 +494,10 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
         o.flags |= MG_FLAG_NO_CLUSTER;
         if ((st = decide(B, M, N, d, &o, sms, smem_optin, &info, &timeout_ns, &flags)) != MG_OK)
             return st;
+        fwd = plan_kernel(info, flags);
+        if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      info.smem_bytes)) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute");
     }
 
     struct mg_attn_plan *p = new (std::nothrow) struct mg_attn_plan();
@@ -772,7 +810,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     // The kernel's shared-memory limit is raised before the cluster occupancy query, as
     // mg_attn_plan_ex does: at the default 48 KB limit the query would refuse the cluster, and a
     // first call in a process would then take another combine than later calls.
-    FwdKernel fwd = fwd_kernel(d, in.stages, 0);
+    FwdKernel fwd = plan_kernel(in, 0);
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, in.smem_bytes);
     if (e != cudaSuccess)
@@ -782,8 +820,9 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         o.flags = MG_FLAG_NO_CLUSTER;
         if ((st = decide(B, M, N, d, &o, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags)) != MG_OK)
             return st;
-        // The fallback keeps the pipeline depth, hence the kernel; its limit is set again anyway.
-        fwd = fwd_kernel(d, in.stages, 0);
+        // The fallback keeps the kernel (its choice does not depend on the cluster); its limit is
+        // set again anyway.
+        fwd = plan_kernel(in, 0);
         if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       in.smem_bytes)) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute");

@@ -311,86 +311,97 @@ __device__ __forceinline__ size_t cluster_tile(const FwdParams &p, int j, int b,
     return (static_cast<size_t>(j) * p.B + b) * p.m_tiles_per_b + mt;
 }
 
-// The reading side of the cluster combine, for CTA rank j of row tile (b, mt): rows
-// [128 j / n, 128 (j+1) / n) of the tile as (sum_r w_r O_r) / (sum_r w_r l_r) over the n ranks,
-// w_r = 1 (exp(m_r - max_r m_r) when SAFE), written as fp16 O. Partial tiles are tile-major
-// (float4 column group outermost, 128 rows innermost). An element is (column group, row); the two
-// lanes of a pair take the same elements, lane h the ranks [h RPL, h RPL + RPL), and a pair takes
-// 8 / RPL elements at a time, so that each thread has its 8 loads in flight together. The pair then
-// adds its two sums in a fixed order (lower ranks first) and each lane writes two of the element's
-// four columns: the result does not depend on timing.
+// Rows per partial tile of the cluster combine: 128, or M when a batch has fewer rows.
+__device__ __forceinline__ int cluster_tile_rows(const FwdParams &p) { return p.M < kBlockM ? p.M : kBlockM; }
+
+// The reading side of the cluster combine, for CTA rank j and the row tiles (b, mt_first) ..
+// (b, mt_first + ntiles - 1) of its CTA: rows [128 j / n, 128 (j+1) / n) of each tile as
+// (sum_r w_r O_r) / (sum_r w_r l_r) over the n ranks, w_r = 1 (exp(m_r - max_r m_r) when SAFE),
+// written as fp16 O. Partial tiles are tile-major (float4 column group outermost, the tile's
+// cluster_tile_rows rows innermost). An element is (column group, row); the two lanes of a pair take the same elements,
+// lane h the ranks [h RPL, h RPL + RPL), and a pair takes 8 / RPL elements at a time, so that each
+// thread has its 8 loads in flight together. The pair then adds its two sums in a fixed order
+// (lower ranks first) and each lane writes two of the element's four columns: the result does not
+// depend on timing. (One call loops over the tiles: a call site per tile costs registers.)
 template <int D, bool SAFE, int RPL>
-__device__ __forceinline__ void cluster_combine_rows(const FwdParams &p, int b, int mt, int m0, int j, int tid)
+__device__ __forceinline__ void cluster_combine_rows(const FwdParams &p, int b, int mt_first, int ntiles, int j,
+                                                     int tid)
 {
     constexpr int G = D / 4;          // float4 column groups per row
     constexpr int EPP = 8 / RPL;      // elements per pair per batch of loads
     constexpr int kPairs = kSoftmaxThreads / 2;
     const int n = p.n_split;
-    const int lo = j * kBlockM / n;
-    // Rows this rank combines: its share of the tile, cut at M (rows past M hold no partials).
-    const int R = max(0, min((j + 1) * kBlockM / n, p.M - m0) - lo);
-    const int E = R * G;
     const int pair = tid >> 1;
     const int h = tid & 1;
     const unsigned pair_mask = 3u << (tid & 30);
     const size_t tiles_per_rank = static_cast<size_t>(p.B) * p.m_tiles_per_b;
-    const size_t tile0 = static_cast<size_t>(b) * p.m_tiles_per_b + mt;
+    const int TR = cluster_tile_rows(p);
     const float4 *ws4 = reinterpret_cast<const float4 *>(p.ws_o);
-    for (int base = pair; base < E; base += kPairs * EPP) {
-        // All loads first (L1 is bypassed: the partials were written by other SMs).
-        float4 v[8];
-        float lv[8], mr[8];
+#pragma unroll 1
+    for (int mt = mt_first; mt < mt_first + ntiles; ++mt) {
+        const int m0 = mt * kBlockM;
+        const int lo = j * kBlockM / n;
+        // Rows this rank combines: its share of the tile, cut at M (rows past M hold no partials).
+        const int R = max(0, min((j + 1) * kBlockM / n, p.M - m0) - lo);
+        const int E = R * G;
+        const size_t tile0 = static_cast<size_t>(b) * p.m_tiles_per_b + mt;
+        for (int base = pair; base < E; base += kPairs * EPP) {
+            // All loads first (L1 is bypassed: the partials were written by other SMs).
+            float4 v[8];
+            float lv[8], mr[8];
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const int e = base + (s / RPL) * kPairs;
-            const int r = h * RPL + s % RPL;
-            if (e < E && r < n) {
-                const size_t t = r * tiles_per_rank + tile0;
-                const int rr = lo + e % R;
-                v[s] = __ldcg(ws4 + (t * G + e / R) * kBlockM + rr);
-                lv[s] = __ldcg(p.ws_l + t * kBlockM + rr);
-                if (SAFE)
-                    mr[s] = __ldcg(p.ws_m + t * kBlockM + rr);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < EPP; ++k) {
-            const int e = base + k * kPairs;  // the same on both lanes of the pair
-            if (e >= E)
-                break;
-            float mmax = 0.f;
-            if (SAFE) {
-                mmax = -INFINITY;
-#pragma unroll
-                for (int q = 0; q < RPL; ++q)
-                    if (h * RPL + q < n)
-                        mmax = fmaxf(mmax, mr[k * RPL + q]);
-                mmax = fmaxf(mmax, __shfl_xor_sync(pair_mask, mmax, 1));
-            }
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-            float lsum = 0.f;
-#pragma unroll
-            for (int q = 0; q < RPL; ++q) {
-                if (h * RPL + q < n) {
-                    const int s = k * RPL + q;
-                    const float w = SAFE ? ptx::ex2_approx((mr[s] - mmax) * ptx::kLog2e) : 1.f;
-                    a[0] = fmaf(w, v[s].x, a[0]);
-                    a[1] = fmaf(w, v[s].y, a[1]);
-                    a[2] = fmaf(w, v[s].z, a[2]);
-                    a[3] = fmaf(w, v[s].w, a[3]);
-                    lsum = fmaf(w, lv[s], lsum);
+            for (int s = 0; s < 8; ++s) {
+                const int e = base + (s / RPL) * kPairs;
+                const int r = h * RPL + s % RPL;
+                if (e < E && r < n) {
+                    const size_t t = r * tiles_per_rank + tile0;
+                    const int rr = lo + e % R;
+                    v[s] = __ldcg(ws4 + (t * G + e / R) * TR + rr);
+                    lv[s] = __ldcg(p.ws_l + t * TR + rr);
+                    if (SAFE)
+                        mr[s] = __ldcg(p.ws_m + t * TR + rr);
                 }
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float other = __shfl_xor_sync(pair_mask, a[c], 1);
-                a[c] = h == 0 ? a[c] + other : other + a[c];
+            for (int k = 0; k < EPP; ++k) {
+                const int e = base + k * kPairs;  // the same on both lanes of the pair
+                if (e >= E)
+                    break;
+                float mmax = 0.f;
+                if (SAFE) {
+                    mmax = -INFINITY;
+#pragma unroll
+                    for (int q = 0; q < RPL; ++q)
+                        if (h * RPL + q < n)
+                            mmax = fmaxf(mmax, mr[k * RPL + q]);
+                    mmax = fmaxf(mmax, __shfl_xor_sync(pair_mask, mmax, 1));
+                }
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+                float lsum = 0.f;
+#pragma unroll
+                for (int q = 0; q < RPL; ++q) {
+                    if (h * RPL + q < n) {
+                        const int s = k * RPL + q;
+                        const float w = SAFE ? ptx::ex2_approx((mr[s] - mmax) * ptx::kLog2e) : 1.f;
+                        a[0] = fmaf(w, v[s].x, a[0]);
+                        a[1] = fmaf(w, v[s].y, a[1]);
+                        a[2] = fmaf(w, v[s].z, a[2]);
+                        a[3] = fmaf(w, v[s].w, a[3]);
+                        lsum = fmaf(w, lv[s], lsum);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float other = __shfl_xor_sync(pair_mask, a[c], 1);
+                    a[c] = h == 0 ? a[c] + other : other + a[c];
+                }
+                const float lother = __shfl_xor_sync(pair_mask, lsum, 1);
+                lsum = h == 0 ? lsum + lother : lother + lsum;
+                const int rr = lo + e % R;
+                const uint32_t o = ptx::pack_half2(__fdiv_rn(a[2 * h], lsum), __fdiv_rn(a[2 * h + 1], lsum));
+                *reinterpret_cast<uint32_t *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + (e / R) * 4 +
+                                              2 * h) = o;
             }
-            const float lother = __shfl_xor_sync(pair_mask, lsum, 1);
-            lsum = h == 0 ? lsum + lother : lother + lsum;
-            const int rr = lo + e % R;
-            const uint32_t o = ptx::pack_half2(__fdiv_rn(a[2 * h], lsum), __fdiv_rn(a[2 * h + 1], lsum));
-            *reinterpret_cast<uint32_t *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + (e / R) * 4 + 2 * h) = o;
         }
     }
 }
@@ -876,17 +887,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0)
                         ptx::mbar_arrive(bar(BI::kSEmpty + g));
-                } else if (t >= kPBuffers &&
-                           !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
-                                      BI::kPEmpty + pb)) {
-                    ok = false;
-                    break;
                 }
+                // The exponentials go to registers first; only their store into the P buffer waits
+                // for the P.V product that last read it, so that product's latency hides behind them.
+                uint32_t w[32];
                 if (warp_rows) {
                     // Columns [64 half, 64 half + 64) of P are tensor-memory columns
                     // [32 half, 32 half + 32) of buffer pb (two fp16 per column).
                     const int nv = n_valid - half * 64;
-                    uint32_t w[32];
                     if constexpr (kQk) {
                         const float *cs = col_scale + static_cast<size_t>(tile_of(t)) * kBlockN + half * 64;
                         if (nv >= 64) {
@@ -903,6 +911,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         exp_slice<true>(r0, 0, nv, w, acc, ek, shift);
                         exp_slice<true>(r1, 32, nv, w + 16, acc, ek, shift);
                     }
+                }
+                if (half == 0 && t >= kPBuffers &&
+                    !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
+                               BI::kPEmpty + pb)) {
+                    ok = false;
+                    break;
+                }
+                if (warp_rows) {
                     ptx::tmem_st_32x32b_x32(tmem + lane_addr + C::kTmemP + pb * 64 + half * 32, w);
                     ptx::tmem_st_wait();
                 }
@@ -946,12 +962,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.cluster_reduce) {
                         // Tile-major: float4 column group outermost, the tile's 128 rows innermost,
                         // so the 32 lanes of a warp (32 consecutive rows) store 512 contiguous bytes.
+                        const int TR = cluster_tile_rows(p);
                         float4 *dst = reinterpret_cast<float4 *>(p.ws_o) +
-                                      cluster_tile(p, j, b, mt) * (D / 4) * kBlockM + (col / 4) * kBlockM + row;
+                                      (cluster_tile(p, j, b, mt) * (D / 4) + col / 4) * TR + row;
                         if (m0 + row < p.M) {
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
-                                dst[q * kBlockM] =
+                                dst[q * TR] =
                                     make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
                         }
@@ -982,7 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
                 // Cluster combine: 128-row tiles (rows past M unwritten); second kernel: rows of M.
-                const size_t r = p.cluster_reduce ? cluster_tile(p, j, b, mt) * kBlockM + row
+                const size_t r = p.cluster_reduce ? cluster_tile(p, j, b, mt) * cluster_tile_rows(p) + row
                                                   : (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
                 p.ws_l[r] = l;
                 if (kSafeMax)
@@ -1024,13 +1041,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tid = threadIdx.x - 64;
             const int n = p.n_split;
             if (n <= 2)
-                cluster_combine_rows<D, kSafeMax, 1>(p, b, mt, m0, j, tid);
+                cluster_combine_rows<D, kSafeMax, 1>(p, b, mt, 1, j, tid);
             else if (n <= 4)
-                cluster_combine_rows<D, kSafeMax, 2>(p, b, mt, m0, j, tid);
+                cluster_combine_rows<D, kSafeMax, 2>(p, b, mt, 1, j, tid);
             else if (n <= 8)
-                cluster_combine_rows<D, kSafeMax, 4>(p, b, mt, m0, j, tid);
+                cluster_combine_rows<D, kSafeMax, 4>(p, b, mt, 1, j, tid);
             else
-                cluster_combine_rows<D, kSafeMax, 8>(p, b, mt, m0, j, tid);
+                cluster_combine_rows<D, kSafeMax, 8>(p, b, mt, 1, j, tid);
         }
     }
 

@@ -85,6 +85,13 @@ typedef enum {
                                       the flag. Normalised scores reach +-d, past the fp16 range of exp, so
                                       the flag implies MG_FLAG_SAFE_SOFTMAX. */
 #define MG_QKNORM_EPS 1e-6
+#define MG_FLAG_Q_PAIRS 0x20       /* use the two-Q-tile kernel wherever it applies (head dim 64, the graph as
+                                      written, an even number of 128-row tiles per batch): each CTA holds
+                                      two Q tiles of one batch, streams each K/V tile once for both, and
+                                      each softmax warp group owns one tile's S, P and O. Opt-in: measured
+                                      on GB300 it is slower than the default one-tile kernel (see
+                                      info.q_tiles_per_cta) */
+#define MG_FLAG_NO_Q_PAIRS 0x40    /* always use the one-tile kernel (the default) */
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and
                                       the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */
@@ -108,16 +115,17 @@ typedef struct {
     int32_t n_split;         /* CTAs per row tile; CTA j takes the column tiles j, j + n_split, ... */
     int32_t stages;          /* K/V pipeline depth */
     int32_t threads;         /* threads per CTA of the fused kernel */
-    int32_t grid_ctas;       /* m_tiles * n_split */
+    int32_t grid_ctas;       /* m_tiles / q_tiles_per_cta * n_split */
     int32_t smem_bytes;      /* dynamic shared memory per CTA of the fused kernel */
     int32_t tmem_cols;       /* tensor-memory columns allocated per CTA */
     int32_t kernels_per_run; /* 1 when the fused kernel writes O itself (n_split == 1 or cluster_ctas > 0), else 2 */
     int32_t num_sms;         /* streaming multiprocessors the plan was sized for */
     int64_t workspace_bytes; /* device bytes owned by the plan (split partials + status words) */
-    int32_t cluster_ctas;    /* > 0: the n_split CTAs of a row tile run as one thread-block cluster
-                                and combine their partials in distributed shared memory (no second
-                                kernel, no partials in global memory); 0: second kernel */
-    int32_t reserved0;
+    int32_t cluster_ctas;    /* > 0: the n_split CTAs of a row tile (or row-tile pair) run as one
+                                thread-block cluster and combine their partials themselves after
+                                one cluster barrier (no second kernel); 0: second kernel */
+    int32_t q_tiles_per_cta; /* 128-row Q tiles per CTA: 1 (one-tile kernel) or 2 (two-Q-tile
+                                kernel; m_tiles / 2 row-tile pairs, each split n_split ways) */
 } mg_attn_plan_info;
 
 /*

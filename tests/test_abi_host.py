@@ -86,8 +86,13 @@ def test_query_decisions(B, M, N, d):
     n_tiles = -(-N // 128)
     assert info["m_tiles"] == m_tiles and info["n_tiles"] == n_tiles
     assert 1 <= info["n_split"] <= n_tiles
-    assert info["grid_ctas"] == m_tiles * info["n_split"]
-    if m_tiles >= 152:
+    q = info["q_tiles_per_cta"]
+    # Two Q tiles per CTA only where the two-tile kernel applies (d = 64, the graph as written, an
+    # even number of row tiles per batch), and then only for throughput-bound shapes.
+    assert q in (1, 2) and (q == 1 or (d == 64 and -(-M // 128) % 2 == 0))
+    units = m_tiles // q
+    assert info["grid_ctas"] == units * info["n_split"]
+    if units >= 152:
         assert info["n_split"] == 1
     else:
         assert info["grid_ctas"] <= 152  # one wave
@@ -105,9 +110,25 @@ def test_query_decisions(B, M, N, d):
     assert min(counts) >= 1 and max(counts) - min(counts) <= 1
     # Every split plan keeps its fp32 partials in the workspace (read by the cluster's CTAs through
     # L2, or by the second kernel); one split needs only the status words.
-    rows = B * -(-M // 128) * 128 if cluster else B * M  # the cluster combine keeps whole row tiles
+    rows = B * -(-M // 128) * min(M, 128) if cluster else B * M  # the cluster combine keeps whole tiles
     ws = 256 + (info["n_split"] * rows * (d + 1) * 4 if info["n_split"] > 1 else 0)
     assert info["workspace_bytes"] == ws
+
+
+def test_query_pair_choices():
+    # The two-Q-tile kernel is opt-in: by default every workload takes the one-tile kernel.
+    for shape in [(16, 256, 4096, 64), (2, 256, 65536, 64), (2, 256, 4096, 64), (16, 256, 4096, 128)]:
+        assert mg.mg_attn_query(*shape, 152)["q_tiles_per_cta"] == 1
+    lkv = mg.mg_attn_query(2, 256, 65536, 64, 152, flags=mg.MG_FLAG_Q_PAIRS)
+    assert lkv["q_tiles_per_cta"] == 2 and lkv["n_split"] == 76 and lkv["grid_ctas"] == 152
+    assert mg.mg_attn_query(16, 256, 4096, 128, 152, flags=mg.MG_FLAG_Q_PAIRS)["q_tiles_per_cta"] == 1
+    # Flags force either kernel; variants and odd row-tile counts keep the one-tile kernel.
+    assert mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_Q_PAIRS)["q_tiles_per_cta"] == 2
+    assert mg.mg_attn_query(16, 256, 4096, 64, 152, flags=mg.MG_FLAG_NO_Q_PAIRS)["q_tiles_per_cta"] == 1
+    assert mg.mg_attn_query(16, 256, 4096, 64, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX)["q_tiles_per_cta"] == 1
+    assert mg.mg_attn_query(16, 384, 4096, 64, 152, flags=mg.MG_FLAG_Q_PAIRS)["q_tiles_per_cta"] == 1
+    with pytest.raises(mg.MgAttnError):
+        mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_Q_PAIRS | mg.MG_FLAG_NO_Q_PAIRS)
 
 
 def test_query_cluster_choices():
@@ -139,7 +160,7 @@ def test_query_safe_softmax_workspace():
                 assert b["workspace_bytes"] == a["workspace_bytes"] == 256
             else:
                 n = a["n_split"]
-                rows = shape[0] * -(-shape[1] // 128) * 128 if a["cluster_ctas"] else shape[0] * shape[1]
+                rows = shape[0] * -(-shape[1] // 128) * min(shape[1], 128) if a["cluster_ctas"] else shape[0] * shape[1]
                 assert b["workspace_bytes"] - a["workspace_bytes"] == n * rows * 4
 
 
@@ -176,7 +197,7 @@ def test_query_options():
     ((2, 256, 4096, 64), {"n_split": 33}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x80}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 64), {"flags": 0x20}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x100}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),

@@ -1,9 +1,10 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the same seeded
 fp16 inputs, elementwise within max|O_gpu - O_ref| <= 2e-3 * (1 + |O_ref|).
 
-Covers the five workloads at full size, a shape sweep with ragged M and N tails over both head
-dims, every N split and pipeline depth, degenerate inputs with closed forms, the largest N,
-determinism, the host-buffer entry point, CUDA-graph capture and the bounded-wait status path.
+Covers the six workloads at full size, a shape sweep with ragged M and N tails over both head
+dims, every N split and pipeline depth, both combines, the two-Q-tile kernel, degenerate inputs
+with closed forms, the largest N, determinism, the host-buffer entry point, CUDA-graph capture and
+the bounded-wait status path.
 """
 
 import ctypes
@@ -98,8 +99,9 @@ def test_split_and_pipeline_depth_d128(n_split, stages):
 @pytest.mark.parametrize("B,M,N,d,n_split", [(2, 256, 4096, 64, 16), (1, 200, 2056, 64, 3), (4, 100, 4104, 128, 9),
                                              (3, 129, 1032, 64, 8), (2, 17, 1024, 128, 2), (1, 384, 8192, 64, 13)])
 def test_cluster_combine_matches_second_kernel(B, M, N, d, n_split):
-    # The on-chip combine (thread-block cluster, distributed shared memory) against the oracle and
-    # against the second-kernel combine of the same split.
+    # The cluster combine (the split CTAs of a row tile in one thread-block cluster, partials
+    # through L2 after one cluster barrier) and the second-kernel combine of the same split, each
+    # against the oracle.
     q, k, v = inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=n_split * 7 + d)
     ref = oracle.attention(q, k, v)
     O_cl, plan = run_gpu(q, k, v, n_split=n_split)
@@ -112,8 +114,7 @@ def test_cluster_combine_matches_second_kernel(B, M, N, d, n_split):
 @pytest.mark.parametrize("n_split,flags", [(2, 0), (16, 0), (16, mg.MG_FLAG_SAFE_SOFTMAX)])
 def test_cluster_combine_of_cancelling_splits(n_split, flags):
     # Two splits each dominated by one V row, of opposite signs: O is the small difference of two
-    # large partials. The on-chip exchange carries each split's O_j / l_j in fp16, so this is
-    # where it loses the most (half an ulp of |V| ~ 4 per partial, against a bound of 2e-3).
+    # large partials, where any rounding of the exchanged partials shows most.
     B, M, N, d = 1, 3, 2048, 64
     q = torch.zeros((B, M, d))
     q[0, :, 0] = torch.tensor([1.0, 1.25, 1.5])
@@ -156,6 +157,45 @@ def test_cluster_combine_of_cancelling_splits_large_v(n_split, flags):
     O, plan = run_gpu(q, k, v, n_split=n_split, flags=flags)
     assert plan.info["cluster_ctas"] == n_split
     assert_parity(O, ref, f"cancelling splits |V| ~ 30, cluster {n_split}, flags {flags}")
+
+
+PAIR_SHAPES = [  # (B, M, N, d, n_split, stages): the two-Q-tile kernel forced (MG_FLAG_Q_PAIRS)
+    (1, 256, 1024, 64, 1, 0),      # one split: TMA store of both tiles
+    (2, 200, 2056, 64, 0, 0),      # ragged M (tile 1 holds rows 128..199) and ragged N
+    (1, 129, 8, 64, 0, 0),         # tile 1 holds one row; one ragged column tile
+    (3, 512, 1032, 64, 3, 0),      # two pairs per batch, cluster of 3
+    (1, 256, 8192, 64, 16, 0),     # cluster of 16
+    (2, 256, 4096, 64, 2, 0),      # cluster of 2
+    (2, 256, 4096, 64, 20, 0),     # 20 splits: second kernel
+    (4, 256, 520, 64, 5, 2),       # two-stage ring
+    (1, 256, 3072, 64, 1, 3),      # one split, 24 tiles through a three-stage ring
+    (2, 384, 2048, 64, 4, 0),      # three row tiles: odd, so the one-tile kernel serves it
+]
+
+
+@pytest.mark.parametrize("B,M,N,d,n_split,stages", PAIR_SHAPES)
+def test_two_q_tile_kernel(B, M, N, d, n_split, stages):
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.5, seed=B * 31 + M + N + n_split)
+    ref = oracle.attention(q, k, v)
+    O, plan = run_gpu(q, k, v, n_split=n_split, stages=stages, flags=mg.MG_FLAG_Q_PAIRS)
+    want_pairs = (-(-M // 128)) % 2 == 0
+    assert plan.info["q_tiles_per_cta"] == (2 if want_pairs else 1)
+    assert_parity(O, ref, f"pairs {B, M, N, d} n_split={plan.info['n_split']} cluster={plan.info['cluster_ctas']}")
+
+
+@pytest.mark.parametrize("flags", [0, mg.MG_FLAG_NO_CLUSTER])
+def test_two_q_tile_kernel_matches_one_tile_kernel(flags):
+    # The batch-8 GQA shape through both kernels, each against the oracle; the two-tile kernel is
+    # reproducible bit for bit, run to run.
+    q, k, v, _ = inputs.make_config("gqa_b8")
+    ref = oracle.attention(q, k, v)
+    O2, p2 = run_gpu(q, k, v, flags=flags | mg.MG_FLAG_Q_PAIRS)
+    O2b, _ = run_gpu(q, k, v, flags=flags | mg.MG_FLAG_Q_PAIRS)
+    O1, p1 = run_gpu(q, k, v, flags=flags | mg.MG_FLAG_NO_Q_PAIRS)
+    assert p2.info["q_tiles_per_cta"] == 2 and p1.info["q_tiles_per_cta"] == 1
+    assert_parity(O2, ref, "two-tile")
+    assert_parity(O1, ref, "one-tile")
+    assert torch.equal(O2, O2b)
 
 
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
