@@ -238,10 +238,14 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     // The fused kernel writes O itself unless split partials go through the second kernel.
     info->kernels_per_run = (n_split > 1 && !cluster) ? 2 : 1;
     info->num_sms = num_sms;
-    // Split partials: numerators, row sums and (max-subtracted variant) row maxima, for every split
-    // and row; the cluster combine keeps whole row tiles (rows past M included).
+    // Split partials in the workspace: numerators, row sums and (max-subtracted variant) row maxima,
+    // for every split and row, for the second kernel and for the two-Q-tile kernel's cluster
+    // combine (which keeps whole row tiles); the one-tile kernel's cluster combine exchanges them
+    // on chip.
     const int64_t row_words = (o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) ? 2 : 1;
-    const int64_t partial_bytes = n_split > 1 ? n_split * partial_rows(B, M, cluster) * (d + row_words) * 4 : 0;
+    const bool ws_partials = n_split > 1 && (!cluster || pair);
+    const int64_t partial_bytes =
+        ws_partials ? n_split * partial_rows(B, M, cluster && pair) * (d + row_words) * 4 : 0;
     // QK-norm: key-vector scales (B*N floats, then 128 more that reads of a last tile past N may
     // touch), from a 256-byte boundary.
     const int64_t scale_bytes = qk_norm ? 256 + (B * N + 128) * 4 : 0;
@@ -517,8 +521,9 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     uint8_t *ws = static_cast<uint8_t *>(p->workspace);
     p->status = reinterpret_cast<int *>(ws);
     std::memset(p->maps, 0, sizeof(p->maps));
-    if (info.n_split > 1) {
-        const size_t rows = static_cast<size_t>(info.n_split) * partial_rows(B, M, info.cluster_ctas > 0);
+    const bool l2_cluster = info.cluster_ctas > 0 && info.q_tiles_per_cta == 2;
+    if (info.n_split > 1 && (info.cluster_ctas == 0 || l2_cluster)) {
+        const size_t rows = static_cast<size_t>(info.n_split) * partial_rows(B, M, l2_cluster);
         p->ws_o = reinterpret_cast<float *>(ws + 256);
         p->ws_l = p->ws_o + rows * d;
         if (flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM))
@@ -842,7 +847,9 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     for (int i = 0; i < 4; ++i)
         if ((st = encode_3d(&maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i])) != MG_OK)
             return st;
-    float *ws_o = in.n_split > 1 ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
+    const bool l2_cluster = in.cluster_ctas > 0 && in.q_tiles_per_cta == 2;
+    float *ws_o =
+        in.n_split > 1 && (in.cluster_ctas == 0 || l2_cluster) ? reinterpret_cast<float *>(sd->scratch + 256) : nullptr;
     if (ws_o && in.cluster_ctas == 0 &&
         (st = encode_3d(&maps[4], ws_o, ud, uM, static_cast<uint64_t>(in.n_split) * uB, 32u, 128u, 4)) != MG_OK)
         return st;
@@ -858,7 +865,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.O = static_cast<__half *>(O);
     prm.status = reinterpret_cast<int *>(sd->scratch);
     prm.ws_o = ws_o;
-    prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * partial_rows(B, M, in.cluster_ctas > 0) * d : nullptr;
+    prm.ws_l = ws_o ? ws_o + static_cast<size_t>(in.n_split) * partial_rows(B, M, l2_cluster) * d : nullptr;
     prm.ws_m = nullptr;
     prm.col_scale = nullptr;
     prm.timeout_ns = timeout_ns;

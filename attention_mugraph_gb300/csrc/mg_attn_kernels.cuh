@@ -76,6 +76,11 @@ constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier id of the softmax warp
 constexpr int kMaxClusterRanks = 16;     // largest cluster of the on-chip combine
 constexpr float kQkNormEps = 1e-6f;      // rms_norm epsilon of the QK-norm variant
 constexpr uint32_t kGroupBarrier0 = 2;   // named barrier ids 2, 3: the four warps of softmax group 0, 1
+// On-chip combine: a normalised partial value |x| below this is exchanged as fp16 alone (its rounding,
+// at most 2^-10 here, is half the 2e-3 error bound); for a 32-column slice of a row with any larger
+// value the reader also adds each value's fp16 remainder x - fp16(x), which restores close to fp32
+// precision.
+constexpr float kHiOnlyBelow = 4.0f;
 
 template <int D>
 struct TileCfg {
@@ -305,107 +310,6 @@ __device__ __forceinline__ float reduce_scatter8(const float (&a)[8], int lane)
     return (h2 ? b2[1] : b2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? b2[0] : b2[1], 4);
 }
 
-// Index of the (split j, batch b, row tile mt) tile among the cluster combine's partial tiles.
-__device__ __forceinline__ size_t cluster_tile(const FwdParams &p, int j, int b, int mt)
-{
-    return (static_cast<size_t>(j) * p.B + b) * p.m_tiles_per_b + mt;
-}
-
-// Rows per partial tile of the cluster combine: 128, or M when a batch has fewer rows.
-__device__ __forceinline__ int cluster_tile_rows(const FwdParams &p) { return p.M < kBlockM ? p.M : kBlockM; }
-
-// The reading side of the cluster combine, for CTA rank j and the row tiles (b, mt_first) ..
-// (b, mt_first + ntiles - 1) of its CTA: rows [128 j / n, 128 (j+1) / n) of each tile as
-// (sum_r w_r O_r) / (sum_r w_r l_r) over the n ranks, w_r = 1 (exp(m_r - max_r m_r) when SAFE),
-// written as fp16 O. Partial tiles are tile-major (float4 column group outermost, the tile's
-// cluster_tile_rows rows innermost). An element is (column group, row); the two lanes of a pair take the same elements,
-// lane h the ranks [h RPL, h RPL + RPL), and a pair takes 8 / RPL elements at a time, so that each
-// thread has its 8 loads in flight together. The pair then adds its two sums in a fixed order
-// (lower ranks first) and each lane writes two of the element's four columns: the result does not
-// depend on timing. (One call loops over the tiles: a call site per tile costs registers.)
-template <int D, bool SAFE, int RPL>
-__device__ __forceinline__ void cluster_combine_rows(const FwdParams &p, int b, int mt_first, int ntiles, int j,
-                                                     int tid)
-{
-    constexpr int G = D / 4;          // float4 column groups per row
-    constexpr int EPP = 8 / RPL;      // elements per pair per batch of loads
-    constexpr int kPairs = kSoftmaxThreads / 2;
-    const int n = p.n_split;
-    const int pair = tid >> 1;
-    const int h = tid & 1;
-    const unsigned pair_mask = 3u << (tid & 30);
-    const size_t tiles_per_rank = static_cast<size_t>(p.B) * p.m_tiles_per_b;
-    const int TR = cluster_tile_rows(p);
-    const float4 *ws4 = reinterpret_cast<const float4 *>(p.ws_o);
-#pragma unroll 1
-    for (int mt = mt_first; mt < mt_first + ntiles; ++mt) {
-        const int m0 = mt * kBlockM;
-        const int lo = j * kBlockM / n;
-        // Rows this rank combines: its share of the tile, cut at M (rows past M hold no partials).
-        const int R = max(0, min((j + 1) * kBlockM / n, p.M - m0) - lo);
-        const int E = R * G;
-        const size_t tile0 = static_cast<size_t>(b) * p.m_tiles_per_b + mt;
-        for (int base = pair; base < E; base += kPairs * EPP) {
-            // All loads first (L1 is bypassed: the partials were written by other SMs).
-            float4 v[8];
-            float lv[8], mr[8];
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int e = base + (s / RPL) * kPairs;
-                const int r = h * RPL + s % RPL;
-                if (e < E && r < n) {
-                    const size_t t = r * tiles_per_rank + tile0;
-                    const int rr = lo + e % R;
-                    v[s] = __ldcg(ws4 + (t * G + e / R) * TR + rr);
-                    lv[s] = __ldcg(p.ws_l + t * TR + rr);
-                    if (SAFE)
-                        mr[s] = __ldcg(p.ws_m + t * TR + rr);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < EPP; ++k) {
-                const int e = base + k * kPairs;  // the same on both lanes of the pair
-                if (e >= E)
-                    break;
-                float mmax = 0.f;
-                if (SAFE) {
-                    mmax = -INFINITY;
-#pragma unroll
-                    for (int q = 0; q < RPL; ++q)
-                        if (h * RPL + q < n)
-                            mmax = fmaxf(mmax, mr[k * RPL + q]);
-                    mmax = fmaxf(mmax, __shfl_xor_sync(pair_mask, mmax, 1));
-                }
-                float a[4] = {0.f, 0.f, 0.f, 0.f};
-                float lsum = 0.f;
-#pragma unroll
-                for (int q = 0; q < RPL; ++q) {
-                    if (h * RPL + q < n) {
-                        const int s = k * RPL + q;
-                        const float w = SAFE ? ptx::ex2_approx((mr[s] - mmax) * ptx::kLog2e) : 1.f;
-                        a[0] = fmaf(w, v[s].x, a[0]);
-                        a[1] = fmaf(w, v[s].y, a[1]);
-                        a[2] = fmaf(w, v[s].z, a[2]);
-                        a[3] = fmaf(w, v[s].w, a[3]);
-                        lsum = fmaf(w, lv[s], lsum);
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float other = __shfl_xor_sync(pair_mask, a[c], 1);
-                    a[c] = h == 0 ? a[c] + other : other + a[c];
-                }
-                const float lother = __shfl_xor_sync(pair_mask, lsum, 1);
-                lsum = h == 0 ? lsum + lother : lother + lsum;
-                const int rr = lo + e % R;
-                const uint32_t o = ptx::pack_half2(__fdiv_rn(a[2 * h], lsum), __fdiv_rn(a[2 * h + 1], lsum));
-                *reinterpret_cast<uint32_t *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + (e / R) * 4 +
-                                              2 * h) = o;
-            }
-        }
-    }
-}
-
 // Evaluation variants of kernel 1, compiled separately so that each carries only its own code.
 enum Variant : int {
     kPlain = 0,    // the graph as written
@@ -426,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using BI = Bars<STAGES, kPBuffers>;
     static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
+    static_assert(2 * 128 * (D + 8) * 2 + (D / 32 + 1) * 128 * 4 <= STAGES * C::kStageBytes,
+                  "on-chip combine staging must fit in the K/V ring");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -887,14 +793,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0)
                         ptx::mbar_arrive(bar(BI::kSEmpty + g));
+                } else if (t >= kPBuffers &&
+                           !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
+                                      BI::kPEmpty + pb)) {
+                    ok = false;
+                    break;
                 }
-                // The exponentials go to registers first; only their store into the P buffer waits
-                // for the P.V product that last read it, so that product's latency hides behind them.
-                uint32_t w[32];
                 if (warp_rows) {
                     // Columns [64 half, 64 half + 64) of P are tensor-memory columns
                     // [32 half, 32 half + 32) of buffer pb (two fp16 per column).
                     const int nv = n_valid - half * 64;
+                    uint32_t w[32];
                     if constexpr (kQk) {
                         const float *cs = col_scale + static_cast<size_t>(tile_of(t)) * kBlockN + half * 64;
                         if (nv >= 64) {
@@ -911,14 +820,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         exp_slice<true>(r0, 0, nv, w, acc, ek, shift);
                         exp_slice<true>(r1, 32, nv, w + 16, acc, ek, shift);
                     }
-                }
-                if (half == 0 && t >= kPBuffers &&
-                    !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(t / kPBuffers) & 1u) ^ 1u,
-                               BI::kPEmpty + pb)) {
-                    ok = false;
-                    break;
-                }
-                if (warp_rows) {
                     ptx::tmem_st_32x32b_x32(tmem + lane_addr + C::kTmemP + pb * 64 + half * 32, w);
                     ptx::tmem_st_wait();
                 }
@@ -946,12 +847,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l = l_xchg[row] + l_xchg[kBlockM + row];
         if (o_ready) {
             ptx::tc_fence_after();
-            // The K/V ring is idle (every PV has completed). With one split, or with partials for
-            // the second kernel, this CTA's output is staged there in the 128-byte-swizzled layout
-            // the output tensor maps expect, then written by a TMA store. With the cluster combine,
-            // each thread stores its row's fp32 partial numerator straight from registers to the
-            // workspace (plain stores, which the cluster barrier below publishes).
+            // The K/V ring is idle (every PV has completed): stage this CTA's output there. For the
+            // on-chip combine: the normalised partial x = O_j / l_j as fp16 rows of d + 8 halves
+            // (the pad keeps 8 consecutive rows on distinct banks); for a 32-column slice of a row
+            // with any |x| >= kHiOnlyBelow also the remainders x - fp16(x), in the same layout;
+            // then the fp32 row sum l_j once per slice (each copy carries, in its sign bit, whether
+            // that slice's remainders are staged; l_j >= 0) and the row maxima m_j, read by the
+            // cluster's CTAs after the cluster barrier. Otherwise the 128-byte-swizzled layout the
+            // output tensor maps expect, then a TMA store.
             const uint32_t stage = sStage0;
+            __half *stage_hi = reinterpret_cast<__half *>(smem + C::kQBytes);
+            __half *stage_lo = stage_hi + kBlockM * (D + 8);
+            float *stage_lm = reinterpret_cast<float *>(stage_lo + kBlockM * (D + 8));  // [D/32 + 1][128]
             if (warp_rows) {
 #pragma unroll
                 for (int c = 0; c < C::kHalfCols / 32; ++c) {
@@ -960,18 +867,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, r);
                     ptx::tmem_ld_wait(r);
                     if (p.cluster_reduce) {
-                        // Tile-major: float4 column group outermost, the tile's 128 rows innermost,
-                        // so the 32 lanes of a warp (32 consecutive rows) store 512 contiguous bytes.
-                        const int TR = cluster_tile_rows(p);
-                        float4 *dst = reinterpret_cast<float4 *>(p.ws_o) +
-                                      (cluster_tile(p, j, b, mt) * (D / 4) + col / 4) * TR + row;
-                        if (m0 + row < p.M) {
+                        // One correctly rounded reciprocal, then products (l = 0 only if every
+                        // exponential of the split underflowed; its partial is then 0).
+                        const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
+                        uint4 *dhi = reinterpret_cast<uint4 *>(stage_hi + row * (D + 8) + col);
+                        uint4 *dlo = reinterpret_cast<uint4 *>(stage_lo + row * (D + 8) + col);
+                        bool wide = false;
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                dst[q * TR] =
-                                    make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                                __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t h4[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const float x0 = __uint_as_float(r[8 * q + 2 * h]) * inv;
+                                const float x1 = __uint_as_float(r[8 * q + 2 * h + 1]) * inv;
+                                h4[h] = ptx::pack_half2(x0, x1);
+                                wide = wide || fabsf(x0) >= kHiOnlyBelow || fabsf(x1) >= kHiOnlyBelow;
+                            }
+                            dhi[q] = make_uint4(h4[0], h4[1], h4[2], h4[3]);
                         }
+                        if (wide) {
+                            // Second pass, only for a slice that needs it: the same products again,
+                            // minus their fp16 roundings (exact differences).
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t l4[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const float x0 = __uint_as_float(r[8 * q + 2 * h]) * inv;
+                                    const float x1 = __uint_as_float(r[8 * q + 2 * h + 1]) * inv;
+                                    const uint32_t hw = ptx::pack_half2(x0, x1);
+                                    const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hw));
+                                    l4[h] = ptx::pack_half2(x0 - hf.x, x1 - hf.y);
+                                }
+                                dlo[q] = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                            }
+                        }
+                        stage_lm[(col / 32) * kBlockM + row] = wide ? -l : l;  // -0.0 when l = 0
                     } else if (p.n_split == 1) {
                         // fp16 O/l: chunk col/64 of a {64, 128} fp16 box; this slice is units (col%64)/8 .. +3.
                         const uint32_t chunk = stage + (col / 64) * C::kChunkRows128;
@@ -997,10 +928,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
-                // Cluster combine: 128-row tiles (rows past M unwritten); second kernel: rows of M.
-                const size_t r = p.cluster_reduce ? cluster_tile(p, j, b, mt) * cluster_tile_rows(p) + row
-                                                  : (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
+            if (p.cluster_reduce) {
+                if (g == 0)
+                    stage_lm[(D / 32) * kBlockM + row] = m;
+            } else if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
+                const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
                 p.ws_l[r] = l;
                 if (kSafeMax)
                     p.ws_m[r] = m;
@@ -1025,30 +957,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // Cluster combine of the split partials. The cluster only co-schedules the n_split CTAs of a
-    // row tile and gives them one hardware barrier: the partials themselves go through L2 (each
-    // CTA's fp32 numerators, row sums and, max-subtracted, row maxima, stored above). After the
-    // barrier (release/acquire at cluster scope) CTA rank j forms rows [128 j / n, 128 (j+1) / n)
-    // of its row tile as (sum_r w_r O_r) / (sum_r w_r l_r), w_r = 1 (exp(m_r - max m) when
-    // max-subtracted), over the n ranks in rank order (reproducible), and writes fp16 O. Nothing
-    // reads another CTA's shared memory, so no CTA waits for the others after that. Every thread
-    // of every CTA reaches the barrier, on the unwinding path too. (Measured on GB300: moving the
-    // partials through distributed shared memory instead took ~1.3-1.7 us per exchange, in fp16.)
+    // On-chip combine of the split partials: after the first cluster barrier every CTA's staged
+    // (O_j / l_j, remainders, l_j, m_j) is visible; CTA rank j forms rows [128 j / n, 128 (j+1) / n)
+    // of its row tile as sum_r c_r x_r / sum_r c_r with c_r = l_r (times exp(m_r - max m) in the
+    // max-subtracted variant), x_r = the fp16 value plus, where rank r flagged the half-row, its
+    // fp16 remainder, over all n ranks in rank order (reproducible), and writes fp16 O. The second
+    // barrier keeps each CTA's shared memory alive until the others have read it. Every thread of
+    // every CTA reaches both barriers, on the unwinding path too.
     __syncwarp();
     if (p.cluster_reduce) {
         ptx::cluster_sync();
         if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
-            const int tid = threadIdx.x - 64;
+            constexpr int G = D / 8;  // 16-byte groups (8 fp16 columns) per row
             const int n = p.n_split;
-            if (n <= 2)
-                cluster_combine_rows<D, kSafeMax, 1>(p, b, mt, 1, j, tid);
-            else if (n <= 4)
-                cluster_combine_rows<D, kSafeMax, 2>(p, b, mt, 1, j, tid);
-            else if (n <= 8)
-                cluster_combine_rows<D, kSafeMax, 4>(p, b, mt, 1, j, tid);
-            else
-                cluster_combine_rows<D, kSafeMax, 8>(p, b, mt, 1, j, tid);
+            const int lo_row = j * kBlockM / n;
+            const int hi_row = (j + 1) * kBlockM / n;
+            const uint32_t sh = ptx::smem_u32(smem + C::kQBytes);
+            const uint32_t sl = sh + kBlockM * (D + 8) * 2;
+            const uint32_t ls = sl + kBlockM * (D + 8) * 2;  // l per 32-column slice: [D / 32][128]
+            const uint32_t ms = ls + (D / 32) * kBlockM * 4;
+            for (int it = threadIdx.x - 64; it < (hi_row - lo_row) * G; it += kSoftmaxThreads) {
+                const int rr = lo_row + it / G;
+                const int gq = it % G;
+                if (m0 + rr >= p.M)
+                    continue;
+                const uint32_t off = static_cast<uint32_t>((rr * (D + 8) + gq * 8) * 2);
+                const uint32_t lrow = ls + static_cast<uint32_t>(((gq * 8) / 32) * kBlockM + rr) * 4;
+                // Max-subtracted variant: every rank's row maximum first, then the weights
+                // exp(m_r - max m) (measured faster than requesting them with the values: fewer
+                // registers live at once).
+                float wt[kMaxClusterRanks];
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r)
+                    wt[r] = 1.f;
+                if (kSafeMax) {
+                    float mr[kMaxClusterRanks];
+                    float mmax = -INFINITY;
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r) {
+                        if (r < n) {
+                            mr[r] = ptx::ld_cluster_f32(ptx::map_to_rank(ms + rr * 4, r));
+                            mmax = fmaxf(mmax, mr[r]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r)
+                        if (r < n)
+                            wt[r] = ptx::ex2_approx((mr[r] - mmax) * ptx::kLog2e);
+                }
+                // Every rank's values and row sums are requested before the first is used: the
+                // remote reads are in flight together rather than one round trip after another.
+                float4 v[kMaxClusterRanks];
+                float c[kMaxClusterRanks];
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r) {
+                    if (r < n) {
+                        v[r] = ptx::ld_cluster_v4(ptx::map_to_rank(sh + off, r));
+                        c[r] = ptx::ld_cluster_f32(ptx::map_to_rank(lrow, r));
+                    }
+                }
+                uint32_t flags = 0;  // ranks that staged remainders for this slice of the row
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r) {
+                    if (r < n) {
+                        flags |= (signbit(c[r]) ? 1u : 0u) << r;
+                        c[r] = fabsf(c[r]) * wt[r];
+                    }
+                }
+                float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float lsum = 0.f;
+                auto add_halves = [&](const float4 &w, float cr) {
+                    const uint32_t words[4] = {__float_as_uint(w.x), __float_as_uint(w.y), __float_as_uint(w.z),
+                                               __float_as_uint(w.w)};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&words[h]));
+                        a[2 * h] = fmaf(cr, f.x, a[2 * h]);
+                        a[2 * h + 1] = fmaf(cr, f.y, a[2 * h + 1]);
+                    }
+                };
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r) {
+                    if (r < n) {
+                        add_halves(v[r], c[r]);
+                        lsum += c[r];
+                    }
+                }
+                if (flags) {
+                    // Remainders of the flagged ranks: one more round of remote reads, all in flight.
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r)
+                        if (r < n && ((flags >> r) & 1u))
+                            v[r] = ptx::ld_cluster_v4(ptx::map_to_rank(sl + off, r));
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r)
+                        if (r < n && ((flags >> r) & 1u))
+                            add_halves(v[r], c[r]);
+                }
+                uint4 w;
+                w.x = ptx::pack_half2(__fdiv_rn(a[0], lsum), __fdiv_rn(a[1], lsum));
+                w.y = ptx::pack_half2(__fdiv_rn(a[2], lsum), __fdiv_rn(a[3], lsum));
+                w.z = ptx::pack_half2(__fdiv_rn(a[4], lsum), __fdiv_rn(a[5], lsum));
+                w.w = ptx::pack_half2(__fdiv_rn(a[6], lsum), __fdiv_rn(a[7], lsum));
+                *reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + gq * 8) = w;
+            }
         }
+        // Only "every CTA has finished reading the others' shared memory" is needed here; a
+        // release would also hold each CTA until its output stores had drained.
+        ptx::cluster_sync_relaxed();
     }
 
     // Teardown: every tensor-memory access of the CTA is ordered before the free.

@@ -14,9 +14,9 @@
 // alternate K/V tiles of the same rows), a K/V tile also costs half the shared-memory and L2 reads
 // per unit of work.
 //
-// The division by the row sum, the split partials and the combines are the one-tile kernel's
-// (mg_attn_kernels.cuh): one split writes fp16 O by TMA store; 2..16 splits of one wave combine in
-// a cluster through L2; more go to the second kernel. The barrier protocol is restated on the CPU by
+// The division by the row sum and the split partials follow the one-tile kernel (mg_attn_kernels.cuh):
+// one split writes fp16 O by TMA store; 2..16 splits of one wave combine in a cluster through L2
+// (below); more go to the second kernel. The barrier protocol is restated on the CPU by
 // tests/pipeline_model.py (PairSim), which a change here must follow.
 //
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,320), O_1 [320,384), P_0
@@ -38,6 +38,111 @@ constexpr uint32_t kPairTmemP = 384;                            // P_g at kPairT
 __host__ __device__ constexpr uint32_t pair_smem_bytes(int stages)
 {
     return 1024u + 2u * kPairQBytes + static_cast<uint32_t>(stages) * kPairStageBytes + 2u * 128 * 4 + 512u;
+}
+
+// The cluster combine of the two-tile kernel moves the split partials through L2: each CTA stores
+// its fp32 numerators and row sums, one cluster barrier publishes them, and each rank combines its
+// rows from L2. (The one-tile kernel exchanges them on chip instead.)
+
+// Index of the (split j, batch b, row tile mt) tile among the cluster combine's partial tiles.
+__device__ __forceinline__ size_t cluster_tile(const FwdParams &p, int j, int b, int mt)
+{
+    return (static_cast<size_t>(j) * p.B + b) * p.m_tiles_per_b + mt;
+}
+
+// Rows per partial tile of the cluster combine: 128, or M when a batch has fewer rows.
+__device__ __forceinline__ int cluster_tile_rows(const FwdParams &p) { return p.M < kBlockM ? p.M : kBlockM; }
+
+// The reading side of the cluster combine, for CTA rank j and the row tiles (b, mt_first) ..
+// (b, mt_first + ntiles - 1) of its CTA: rows [128 j / n, 128 (j+1) / n) of each tile as
+// (sum_r w_r O_r) / (sum_r w_r l_r) over the n ranks, w_r = 1 (exp(m_r - max_r m_r) when SAFE),
+// written as fp16 O. Partial tiles are tile-major (float4 column group outermost, the tile's
+// cluster_tile_rows rows innermost). An element is (column group, row); the two lanes of a pair take the same elements,
+// lane h the ranks [h RPL, h RPL + RPL), and a pair takes 8 / RPL elements at a time, so that each
+// thread has its 8 loads in flight together. The pair then adds its two sums in a fixed order
+// (lower ranks first) and each lane writes two of the element's four columns: the result does not
+// depend on timing. (One call loops over the tiles: a call site per tile costs registers.)
+template <int D, bool SAFE, int RPL>
+__device__ __forceinline__ void cluster_combine_rows(const FwdParams &p, int b, int mt_first, int ntiles, int j,
+                                                     int tid)
+{
+    constexpr int G = D / 4;          // float4 column groups per row
+    constexpr int EPP = 8 / RPL;      // elements per pair per batch of loads
+    constexpr int kPairs = kSoftmaxThreads / 2;
+    const int n = p.n_split;
+    const int pair = tid >> 1;
+    const int h = tid & 1;
+    const unsigned pair_mask = 3u << (tid & 30);
+    const size_t tiles_per_rank = static_cast<size_t>(p.B) * p.m_tiles_per_b;
+    const int TR = cluster_tile_rows(p);
+    const float4 *ws4 = reinterpret_cast<const float4 *>(p.ws_o);
+#pragma unroll 1
+    for (int mt = mt_first; mt < mt_first + ntiles; ++mt) {
+        const int m0 = mt * kBlockM;
+        const int lo = j * kBlockM / n;
+        // Rows this rank combines: its share of the tile, cut at M (rows past M hold no partials).
+        const int R = max(0, min((j + 1) * kBlockM / n, p.M - m0) - lo);
+        const int E = R * G;
+        const size_t tile0 = static_cast<size_t>(b) * p.m_tiles_per_b + mt;
+        for (int base = pair; base < E; base += kPairs * EPP) {
+            // All loads first (L1 is bypassed: the partials were written by other SMs).
+            float4 v[8];
+            float lv[8], mr[8];
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int e = base + (s / RPL) * kPairs;
+                const int r = h * RPL + s % RPL;
+                if (e < E && r < n) {
+                    const size_t t = r * tiles_per_rank + tile0;
+                    const int rr = lo + e % R;
+                    v[s] = __ldcg(ws4 + (t * G + e / R) * TR + rr);
+                    lv[s] = __ldcg(p.ws_l + t * TR + rr);
+                    if (SAFE)
+                        mr[s] = __ldcg(p.ws_m + t * TR + rr);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < EPP; ++k) {
+                const int e = base + k * kPairs;  // the same on both lanes of the pair
+                if (e >= E)
+                    break;
+                float mmax = 0.f;
+                if (SAFE) {
+                    mmax = -INFINITY;
+#pragma unroll
+                    for (int q = 0; q < RPL; ++q)
+                        if (h * RPL + q < n)
+                            mmax = fmaxf(mmax, mr[k * RPL + q]);
+                    mmax = fmaxf(mmax, __shfl_xor_sync(pair_mask, mmax, 1));
+                }
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+                float lsum = 0.f;
+#pragma unroll
+                for (int q = 0; q < RPL; ++q) {
+                    if (h * RPL + q < n) {
+                        const int s = k * RPL + q;
+                        const float w = SAFE ? ptx::ex2_approx((mr[s] - mmax) * ptx::kLog2e) : 1.f;
+                        a[0] = fmaf(w, v[s].x, a[0]);
+                        a[1] = fmaf(w, v[s].y, a[1]);
+                        a[2] = fmaf(w, v[s].z, a[2]);
+                        a[3] = fmaf(w, v[s].w, a[3]);
+                        lsum = fmaf(w, lv[s], lsum);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float other = __shfl_xor_sync(pair_mask, a[c], 1);
+                    a[c] = h == 0 ? a[c] + other : other + a[c];
+                }
+                const float lother = __shfl_xor_sync(pair_mask, lsum, 1);
+                lsum = h == 0 ? lsum + lother : lother + lsum;
+                const int rr = lo + e % R;
+                const uint32_t o = ptx::pack_half2(__fdiv_rn(a[2 * h], lsum), __fdiv_rn(a[2 * h + 1], lsum));
+                *reinterpret_cast<uint32_t *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + (e / R) * 4 +
+                                              2 * h) = o;
+            }
+        }
+    }
 }
 
 template <int STAGES>

@@ -147,6 +147,21 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
     return r != 0;
 }
 
+// Named barrier that also ORs a predicate over its participants (the same answer on every thread).
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
 // (the tensor core reading an operand that threads wrote with st.shared).
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -200,6 +215,13 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
 {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 

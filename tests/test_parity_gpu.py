@@ -159,6 +159,29 @@ def test_cluster_combine_of_cancelling_splits_large_v(n_split, flags):
     assert_parity(O, ref, f"cancelling splits |V| ~ 30, cluster {n_split}, flags {flags}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_cluster_combine_mixed_slices(d):
+    # As above, but only some 32-column slices of the dominant V rows are large: in one row, the
+    # on-chip exchange adds the fp16 remainders of those slices and not of the others.
+    B, M, N = 2, 40, 1024
+    g = torch.Generator().manual_seed(17)
+    q = torch.zeros((B, M, d))
+    q[:, :, 0] = torch.rand((B, M), generator=g) * 0.5 + 1.0
+    k = torch.full((B, d, N), -5.0)
+    k[:, 1:, :] = 0.0
+    k[:, 0, 0] = 5.0
+    k[:, 0, 128] = 5.0
+    v = torch.randn((B, N, d), generator=g) * 0.5
+    wide = [c for c in range(d) if (c // 32) % 2 == 0]  # slices 0, 2: large; 1, 3: small
+    v[:, 0, wide] = 29.5
+    v[:, 128, wide] = -31.25
+    q, k, v = q.half(), k.half(), v.half()
+    ref = oracle.attention(q, k, v)
+    O, plan = run_gpu(q, k, v, n_split=4)
+    assert plan.info["cluster_ctas"] == 4
+    assert_parity(O, ref, f"mixed slices d={d}")
+
+
 PAIR_SHAPES = [  # (B, M, N, d, n_split, stages): the two-Q-tile kernel forced (MG_FLAG_Q_PAIRS)
     (1, 256, 1024, 64, 1, 0),      # one split: TMA store of both tiles
     (2, 200, 2056, 64, 0, 0),      # ragged M (tile 1 holds rows 128..199) and ragged N
