@@ -132,6 +132,18 @@ def test_query_pair_choices():
         mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_Q_PAIRS | mg.MG_FLAG_NO_Q_PAIRS)
 
 
+def test_query_split_fills_its_tiles_when_hbm_bound():
+    # Few query rows (HBM-bound): among split counts down to 4/5 of one wave, the plan takes the one
+    # that leaves the fewest idle tile slots. Decode-like (16, 8, 32768, 128): 16 row tiles, one wave
+    # is 9 splits (28 or 29 of 256 tiles each); 8 splits give every CTA 32.
+    info = mg.mg_attn_query(16, 8, 32768, 128, 152)
+    assert info["n_split"] == 8 and info["grid_ctas"] == 128
+    # A shape whose one-wave split already divides its tiles evenly keeps it.
+    assert mg.mg_attn_query(64, 1, 4096, 128, 152)["n_split"] == 2
+    # Many query rows per batch: every SM is used (one wave, 38 splits of 13 or 14 tiles).
+    assert mg.mg_attn_query(2, 256, 65536, 64, 152)["n_split"] == 38
+
+
 def test_query_cluster_choices():
     # The GQA tutorial shape takes a 16-CTA cluster (2 column tiles per CTA) instead of 32 splits.
     assert mg.mg_attn_query(2, 256, 4096, 64, 152)["cluster_ctas"] == 16
