@@ -89,6 +89,7 @@ class Sim:
         self.mut = set(mutations)
         self.rng = random.Random(seed)
         self.abort_rate = abort_rate  # chance per step that a blocked wait runs out (0: never)
+        self.slow = ()                # prefixes of actors the scheduler seldom picks (see run)
         self.abort = False
         self.bars = {}
 
@@ -444,7 +445,13 @@ class Sim:
             if not options:
                 self.fail("deadlock: " + ", ".join(f"{n} at {op[0]} {op[1:3] if op[0] != 'do' else ''}"
                                                     for n, op in nxt.items()))
-            kind, key = self.rng.choice(options)
+            if self.slow:
+                # Actors named with a prefix in `slow` are picked rarely: an adversarial schedule in
+                # which those roles lag far behind the others.
+                w = [0.02 if k == "actor" and any(n.startswith(p) for p in self.slow) else 1.0 for k, n in options]
+                kind, key = self.rng.choices(options, weights=w)[0]
+            else:
+                kind, key = self.rng.choice(options)
             if kind == "tma":
                 bar, nbytes, effect = self.tma.pop(key)
                 effect()
@@ -643,3 +650,128 @@ class PairSim(Sim):
             self.fail("output staged in the K/V ring while a copy into it is in flight")
         if any(self.k_readers) or any(self.v_readers):
             self.fail("output staged in the K/V ring while an MMA reads it")
+
+
+class SegmentSim(Sim):
+    """The one-tile kernel under a stream-K schedule (the graph as written): the CTA's steps form
+    consecutive segments, each a run of column tiles of one row tile with its own Q tile (all loaded
+    at the start, one barrier), its own row sums and its own partial. The two softmax groups still
+    take alternate steps; after its last step of a segment each group joins that segment's epilogue,
+    which waits for OFull's phase k (committed after the segment's last P.V), reads O, and ends with
+    a barrier of all eight softmax warps. The first P.V of segment k+1 overwrites O (no accumulate):
+    it needs P of that tile, which its group writes only after that barrier, so it cannot overtake
+    the epilogue's reads and needs no barrier of its own.
+
+    Mutations: "seg_no_read_barrier" (no barrier after the epilogue's reads), "seg_no_ofull_per_segment"
+    (OFull committed only after the last segment), plus the base class's."""
+
+    def __init__(self, seg_lengths, stages: int, pbufs: int, seed: int, mutations=(), abort_rate: float = 0.0):
+        if not seg_lengths or min(seg_lengths) < 1:
+            raise ValueError("segments of at least one step")
+        self.segs = list(seg_lengths)
+        super().__init__(sum(seg_lengths), stages, pbufs, PLAIN, seed, mutations, abort_rate)
+        self.seg_of = []
+        for k, n in enumerate(self.segs):
+            self.seg_of += [k] * n
+        self.seg_start = [sum(self.segs[:k]) for k in range(len(self.segs))]
+        self.seg_last = [self.seg_start[k] + self.segs[k] - 1 for k in range(len(self.segs))]
+        self.pv_done_seg = [0] * len(self.segs)
+        self.o_reads = [0] * len(self.segs)   # softmax warps that finished reading segment k's O
+        self.o_readers = 0                   # softmax warps reading O right now
+
+    def _pv_warp(self):
+        S, P = self.S, self.P
+        ok = True
+        v = 0
+        while ok and v < self.T:
+            k = self.seg_of[v]
+            pb, s = v % P, v % S
+            if not (yield self.wait(f"VFull{s}", (v // S) & 1, v // S, f"PV warp V {v}")):
+                ok = False
+                break
+            if not (yield self.wait(f"PFull{pb}", (v // P) & 1, v // P, f"PV warp P {v}")):
+                ok = False
+                break
+            yield ("do", lambda v=v, pb=pb, s=s, k=k: self._issue_pv_seg(v, pb, s, k))
+            v += 1
+        if ok:
+            for t in range(max(self.T - P, 0), self.T):
+                ok = yield self.wait(f"PEmpty{t % P}", (t // P) & 1, t // P, f"PV warp tail {t}")
+                if not ok:
+                    break
+            if not ok and "drain_only_on_failure" not in self.mut:
+                yield ("drain", "pipe")
+        else:
+            yield ("drain", "pipe")
+
+    def _issue_pv_seg(self, v, pb, s, k):
+        if not self.abort:
+            if self.pbuf[pb] != v:
+                self.fail(f"P.V MMA {v} reads P buffer {pb} holding tile {self.pbuf[pb]}")
+            if self.vst[s] != v:
+                self.fail(f"P.V MMA {v} reads V stage {s} holding step {self.vst[s]}")
+            if v == self.seg_start[k] and k >= 1 and (self.o_readers or self.o_reads[k - 1] != 2 * GROUP_WARPS):
+                self.fail(f"segment {k}'s first P.V overwrites O while segment {k - 1}'s epilogue reads it")
+        self.p_readers[pb] += 1
+        self.v_readers[s] += 1
+        self.pv_issued += 1
+
+        def done():
+            self.p_readers[pb] -= 1
+            self.v_readers[s] -= 1
+            self.pv_done += 1
+            self.pv_done_seg[k] += 1
+
+        self.pipe.append(("mma", done))
+        self.pipe.append(("commit", f"KvEmpty{s}"))
+        self.pipe.append(("commit", f"PEmpty{pb}"))
+        if v == self.seg_last[k] and ("seg_no_ofull_per_segment" not in self.mut or v == self.T - 1):
+            n = 1 if "seg_no_ofull_per_segment" not in self.mut else len(self.segs)
+            for _ in range(n):
+                self.pipe.append(("commit", "OFull"))
+
+    def _softmax_warp(self, g, gw):
+        P = self.P
+        who = f"softmax g{g}w{gw}"
+        ok = True
+        for k in range(len(self.segs)):
+            for u in range(self.seg_start[k], self.seg_last[k] + 1):
+                if u % 2 != g or not ok:
+                    continue
+                t = u
+                pb = t % P
+                if not (yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")):
+                    ok = False
+                    continue
+                yield ("do", lambda u=u: self._read_s(g, u, +1))
+                if t >= P:
+                    if not (yield self.wait(f"PEmpty{pb}", ((t // P) & 1) ^ 1, t // P - 1, f"{who} P buffer {t}")):
+                        ok = False
+                        continue
+                yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 0)))
+                yield ("do", lambda u=u: self._read_s(g, u, -1))
+                yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
+                yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 1)))
+                yield ("do", lambda pb=pb: self.bars[f"PFull{pb}"].arrive())
+            # Segment k's epilogue: every softmax warp votes (an unwound warp votes no).
+            o_ok = ok and (yield self.wait("OFull", k & 1, k, f"{who} O of segment {k}"))
+            o_ready = yield ("gbar", "softmax", 2 * GROUP_WARPS, o_ok)
+            if o_ready:
+                yield ("do", lambda k=k: self._read_o_seg(k, +1))
+                yield ("do", lambda k=k: self._read_o_seg(k, -1))
+                if "seg_no_read_barrier" not in self.mut:
+                    yield ("gbar", "softmax", 2 * GROUP_WARPS, True)
+            else:
+                ok = False
+
+    def _read_o_seg(self, k, delta):
+        if self.abort:
+            return
+        if delta > 0 and self.pv_done_seg[k] != self.segs[k]:
+            self.fail(f"segment {k}'s O read after {self.pv_done_seg[k]} of {self.segs[k]} P.V products")
+        self.o_readers += delta
+        if delta < 0:
+            self.o_reads[k] += 1
+
+    def _read_o(self):  # not used: each segment has its own epilogue
+        pass

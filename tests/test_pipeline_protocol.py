@@ -141,3 +141,53 @@ def test_pair_draining_only_after_a_failed_loop_leaves_mmas_in_flight():
             hit = str(e)
             break
     assert hit is not None and "in flight" in hit
+
+
+# ------------------------------------------------------------------ stream-K segments
+
+SEGMENTS = [[1], [3], [1, 1], [2, 1], [1, 2], [5, 4], [7, 9], [1, 12], [13, 1], [3, 3]]
+
+
+@pytest.mark.parametrize("stages,pbufs", [(6, 3), (3, 3), (3, 2), (2, 2)])
+def test_segment_protocol_as_built_is_clean(stages, pbufs):
+    for segs, seed in itertools.product(SEGMENTS, range(10)):
+        pm.SegmentSim(segs, stages, pbufs, seed).run()
+
+
+def test_segment_protocol_is_clean_when_any_role_lags():
+    # Adversarial schedules: one role is seldom picked, so the others run far ahead of it.
+    for segs, seed in itertools.product(([1, 1], [2, 2], [3, 1], [5, 4]), range(12)):
+        for slow in ("softmax0", "softmax1", "pv_warp", "s_warp", "producer"):
+            sim = pm.SegmentSim(segs, 3, 2, seed)
+            sim.slow = (slow,)
+            sim.run()
+
+
+def test_segment_epilogue_needs_its_read_barrier():
+    # Without the barrier that ends a segment's epilogue, the group that takes the next segment's
+    # first tile can write its P, and that tile's P.V overwrite O, while the other group still
+    # reads O: caught once that other group lags.
+    hit = None
+    for segs, seed in itertools.product(([1, 1], [2, 2], [3, 1]), range(10)):
+        for slow in ("softmax0", "softmax1"):
+            sim = pm.SegmentSim(segs, 3, 2, seed, mutations=("seg_no_read_barrier",))
+            sim.slow = (slow,)
+            try:
+                sim.run()
+            except pm.ProtocolError as e:
+                hit = str(e)
+                break
+        if hit:
+            break
+    assert hit is not None and "overwrites O" in hit
+
+
+def test_segment_needs_ofull_per_segment():
+    with pytest.raises(pm.ProtocolError, match="deadlock"):
+        pm.SegmentSim([2, 2], 3, 2, 0, mutations=("seg_no_ofull_per_segment",)).run()
+
+
+def test_segment_unwinding_from_any_wait_is_clean():
+    for segs, (stages, pbufs), seed in itertools.product(([2, 1], [1, 2], [3, 4], [1, 1], [4]), [(6, 3), (3, 2)],
+                                                         range(12)):
+        pm.SegmentSim(segs, stages, pbufs, seed, abort_rate=0.02).run()
