@@ -9,6 +9,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -107,6 +108,9 @@ FwdKernel pair_kernel(int stages)
     }
 }
 
+// The one-tile kernel under the stream-K schedule (the graph as written).
+FwdKernel sk_kernel(int64_t d, int stages) { return fwd_kernel_variant<mg::kStreamK>(d, stages); }
+
 // The fused kernel for a head dim, pipeline depth and the MG_FLAG_* evaluation flags.
 FwdKernel fwd_kernel(int64_t d, int stages, int flags)
 {
@@ -137,6 +141,16 @@ int combine_rows_per_cta(int n_split)
 CombineKernel combine_kernel(int64_t d, int n_split)
 {
     return d == 64 ? combine_kernel_d<64>(n_split) : combine_kernel_d<128>(n_split);
+}
+
+// Stream-K partial slots per row tile: the most CTAs whose runs touch one row tile.
+int64_t sk_slots(int64_t rows, int64_t n_tiles, int64_t G)
+{
+    const int64_t U = rows * n_tiles;
+    int64_t most = 1;
+    for (int64_t r = 0; r < rows; ++r)
+        most = std::max<int64_t>(most, mg::sk_cta_of((r + 1) * n_tiles - 1, U, G) - mg::sk_cta_of(r * n_tiles, U, G) + 1);
+    return most;
 }
 
 // Rows of partials per split: B*M for the second kernel; for the cluster combine, whole tiles of
@@ -170,7 +184,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         o = *opts;
     if (o.reserved != 0 ||
         (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX |
-                     MG_FLAG_QK_NORM | MG_FLAG_Q_PAIRS | MG_FLAG_NO_Q_PAIRS)) != 0)
+                     MG_FLAG_QK_NORM | MG_FLAG_Q_PAIRS | MG_FLAG_NO_Q_PAIRS | MG_FLAG_STREAM_K |
+                     MG_FLAG_NO_STREAM_K)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -180,6 +195,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     const int64_t n_tiles = (N + mg::kBlockN - 1) / mg::kBlockN;
     if ((o.flags & MG_FLAG_Q_PAIRS) && (o.flags & MG_FLAG_NO_Q_PAIRS))
         return fail(MG_ERR_CONFIG, "MG_FLAG_Q_PAIRS and MG_FLAG_NO_Q_PAIRS together");
+    if ((o.flags & MG_FLAG_STREAM_K) && (o.flags & MG_FLAG_NO_STREAM_K))
+        return fail(MG_ERR_CONFIG, "MG_FLAG_STREAM_K and MG_FLAG_NO_STREAM_K together");
 
     // One wave: as many splits per unit (a row tile, or a pair of them) as keep every SM busy,
     // never fewer than one column tile per split.
@@ -224,8 +241,31 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
             (n_tiles + kMaxCluster - 1) / kMaxCluster <= 4)
             n_split = kMaxCluster;
     }
-    const bool cluster = !(o.flags & MG_FLAG_NO_CLUSTER) && n_split >= 2 && n_split <= kMaxCluster;
-    if (units * n_split > 0x7fffffffLL)
+    // Stream-K applies to the graph as written with at most 16 query rows per batch (one compact
+    // Q tile per segment, a batch being one row tile), no explicit split, and runs of at most
+    // n_tiles units (so a CTA touches at most two batches), and only on request: measured on
+    // GB300 it is not faster on the decode shapes, which are bound by DRAM throughput (both
+    // schedules stream ~5.4 TB/s there) rather than by uneven CTAs, and its contiguous runs give
+    // concurrent CTAs K rows far apart where the split schedule's interleaved tiles keep them in
+    // neighbouring DRAM locations; (16, 8, 32768, 128): 49.3 against 48.3 us per call,
+    // (64, 1, 4096, 128): 28.2 against 26.7 (there also the second kernel against the cluster).
+    bool stream_k = false;
+    int64_t sk_ctas = 0;
+    if (!pair && M <= mg::kSkQRows && o.n_split == 0 && !(o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) &&
+        !(o.flags & MG_FLAG_NO_STREAM_K)) {
+        const int64_t U = m_tiles * n_tiles;
+        sk_ctas = U < num_sms ? U : num_sms;
+        const int64_t run = (U + sk_ctas - 1) / sk_ctas;
+        const int64_t split_run = (n_tiles + n_split - 1) / n_split;
+        stream_k = run <= n_tiles && sk_ctas >= 2 && (o.flags & MG_FLAG_STREAM_K) && run <= split_run;
+    }
+    if (stream_k) {
+        n_split = sk_slots(m_tiles, n_tiles, sk_ctas);
+        if (n_split < 2)  // every run within one batch and every batch in one run: nothing to combine
+            stream_k = false, n_split = one_wave(units);
+    }
+    const bool cluster = !stream_k && !(o.flags & MG_FLAG_NO_CLUSTER) && n_split >= 2 && n_split <= kMaxCluster;
+    if (!stream_k && units * n_split > 0x7fffffffLL)
         return fail(MG_ERR_INVALID_ARG, "grid too large");
 
     const bool qk_norm = (o.flags & MG_FLAG_QK_NORM) != 0;
@@ -233,7 +273,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     if (stages < 2 || stages > 6)
         return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 6]", stages);
     const uint32_t smem = pair ? mg::pair_smem_bytes(stages) : mg::fwd_smem_bytes(static_cast<int>(d), stages);
-    if (static_cast<int64_t>(smem) > max_smem || !(pair ? pair_kernel(stages) : fwd_kernel(d, stages, o.flags)))
+    if (static_cast<int64_t>(smem) > max_smem ||
+        !(pair ? pair_kernel(stages) : stream_k ? sk_kernel(d, stages) : fwd_kernel(d, stages, o.flags)))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
 
@@ -249,7 +290,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->n_split = static_cast<int32_t>(n_split);
     info->stages = stages;
     info->threads = mg::kThreads;
-    info->grid_ctas = static_cast<int32_t>(units * n_split);
+    info->grid_ctas = static_cast<int32_t>(stream_k ? sk_ctas : units * n_split);
     info->smem_bytes = static_cast<int32_t>(smem);
     info->tmem_cols = static_cast<int32_t>(mg::kTmemCols);
     // The fused kernel writes O itself unless split partials go through the second kernel.
@@ -269,6 +310,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->workspace_bytes = 256 + partial_bytes + scale_bytes;
     info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
     info->q_tiles_per_cta = pair ? 2 : 1;
+    info->schedule = stream_k ? 1 : 0;
     if (timeout_ns)
         *timeout_ns = o.timeout_ns ? static_cast<unsigned long long>(o.timeout_ns) : kDefaultTimeoutNs;
     if (flags)
@@ -280,8 +322,11 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
 // The fused kernel a plan's decisions call for.
 FwdKernel plan_kernel(const mg_attn_plan_info &info, int flags)
 {
+    if (info.schedule == 1)
+        return sk_kernel(info.d, info.stages);
     return info.q_tiles_per_cta == 2 ? pair_kernel(info.stages) : fwd_kernel(info.d, info.stages, flags);
 }
+
 
 // Host-buffer entry point: copies between the caller's pinned host buffers (read and written
 // through their device-mapped addresses over the CPU-GPU link) and the plan's device staging, in
@@ -614,7 +659,9 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     // rows; O (B, M, d): box 64 x 128 rows.
     const void *ptrs[4] = {Q, K, V, O};
     const uint64_t dims[4][3] = {{d, M, B}, {N, d, B}, {d, N, B}, {d, M, B}};
-    const uint32_t box1[4] = {128u, static_cast<uint32_t>(d), 128u, 128u};
+    // Under the stream-K schedule the Q box is kSkQRows rows high (a compact tile per segment).
+    const uint32_t qrows = in.schedule == 1 ? static_cast<uint32_t>(mg::kSkQRows) : 128u;
+    const uint32_t box1[4] = {qrows, static_cast<uint32_t>(d), 128u, 128u};
     for (int i = 0; i < 4; ++i) {
         if (plan->map_ptr[i] != ptrs[i]) {
             plan->map_ptr[i] = nullptr;
@@ -641,6 +688,9 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.status = plan->status;
     prm.timeout_ns = plan->timeout_ns;
     prm.inject_timeout = (plan->flags & MG_FLAG_INJECT_TIMEOUT) ? 1 : 0;
+    prm.sk_units = static_cast<long long>(in.m_tiles) * in.n_tiles;
+    prm.sk_ctas = in.grid_ctas;
+    prm.sk_slots = in.n_split;
 
     cudaLaunchAttribute attr[2];
     const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
@@ -860,7 +910,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     const void *ptrs[4] = {Q, K, V, O};
     const uint64_t uB = B, uM = M, uN = N, ud = d;
     const uint64_t dims[4][3] = {{ud, uM, uB}, {uN, ud, uB}, {ud, uN, uB}, {ud, uM, uB}};
-    const uint32_t box1[4] = {128u, static_cast<uint32_t>(d), 128u, 128u};
+    const uint32_t qrows = in.schedule == 1 ? static_cast<uint32_t>(mg::kSkQRows) : 128u;
+    const uint32_t box1[4] = {qrows, static_cast<uint32_t>(d), 128u, 128u};
     for (int i = 0; i < 4; ++i)
         if ((st = encode_3d(&maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i])) != MG_OK)
             return st;
@@ -887,6 +938,9 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.col_scale = nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
+    prm.sk_units = static_cast<long long>(in.m_tiles) * in.n_tiles;
+    prm.sk_ctas = in.grid_ctas;
+    prm.sk_slots = in.n_split;
 
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};

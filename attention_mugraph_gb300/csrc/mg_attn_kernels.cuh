@@ -22,11 +22,12 @@
 // means the partials combine by plain sums (weights exp(m_j - max m) in the max-subtracted
 // variant).
 //
-// Variants (template parameter VAR): the graph as written; max-subtracted (a first pass over
-// the split's K tiles finds each row's maximum score m, then P = exp(S - m)); QK-norm (scores
-// scaled by query-row and key-vector scales 1/rms, max-subtracted; the softmax warps compute the
-// key-vector scales in the first pass from the K tiles it streams, and the query-row scales from
-// the Q tile).
+// Variants (template parameter VAR): the graph as written, under the split schedule or under the
+// stream-K schedule (CTAs share the (batch, column tile) units in equal runs; see kStreamK);
+// max-subtracted (a first pass over the split's K tiles finds each row's maximum score m, then
+// P = exp(S - m)); QK-norm (scores scaled by query-row and key-vector scales 1/rms,
+// max-subtracted; the softmax warps compute the key-vector scales in the first pass from the K
+// tiles it streams, and the query-row scales from the Q tile).
 //
 // Warp roles of kernel 1 (352 threads):
 //   warp 0       TMA producer: Q once, then K/V tiles through a STAGES-deep mbarrier ring
@@ -122,6 +123,9 @@ struct FwdParams {
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
     int inject_timeout;
+    long long sk_units;      // stream-K: B * n_tiles units (row tile, column tile)
+    int sk_ctas;             // stream-K: G, the grid
+    int sk_slots;            // stream-K: partial slots per row tile (the second kernel's split count)
 };
 
 // Barrier indices inside the CTA's barrier array.
@@ -315,7 +319,21 @@ enum Variant : int {
     kPlain = 0,    // the graph as written
     kSafe = 1,     // each row's maximum subtracted before exp (a first pass over K finds it)
     kQkNorm = 2,   // QK-norm: scores scaled by 1/rms of the query row and of the key vector; safe
+    kStreamK = 3,  // the graph as written under a stream-K schedule (batches of at most 16 rows)
 };
+
+// Stream-K schedule: the B row tiles x n_tiles column tiles form one sequence of units u = r n_tiles
+// + column tile; CTA c takes units [c U / G, (c+1) U / G) (U units, G CTAs), which span at most
+// kMaxSegments row tiles ("segments"). Each segment's partial goes to slot c - c_first(r) of its row
+// tile r, c_first(r) being the CTA that holds the row tile's first unit.
+constexpr int kMaxSegments = 2;
+constexpr int kSkQRows = 16;  // Q rows loaded per segment (batches of at most 16 rows)
+
+// The CTA holding unit u: the largest c with floor(c U / G) <= u.
+__host__ __device__ __forceinline__ long long sk_cta_of(long long u, long long U, long long G)
+{
+    return ((u + 1) * G - 1) / U;
+}
 
 template <int D, int STAGES, int VAR>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -324,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmW, const FwdParams p)
 {
     using C = TileCfg<D>;
-    constexpr bool kSafeMax = VAR != kPlain;  // the row-maximum pass runs
+    constexpr bool kSafeMax = VAR == kSafe || VAR == kQkNorm;  // the row-maximum pass runs
     constexpr bool kQk = VAR == kQkNorm;
     constexpr int kPBuffers = C::kPBuffers;
     using BI = Bars<STAGES, kPBuffers>;
@@ -350,16 +368,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // are consecutive (one cluster, rank j); otherwise consecutive CTAs share (b, j) and so read
     // the same K/V tiles close together in time.
     const int cta = blockIdx.x;
-    const int mt = p.cluster_reduce ? (cta / p.n_split) % p.m_tiles_per_b : cta % p.m_tiles_per_b;
-    const int j = p.cluster_reduce ? cta % p.n_split : (cta / p.m_tiles_per_b) % p.n_split;
-    const int b = cta / (p.m_tiles_per_b * p.n_split);
+    constexpr bool kSK = VAR == kStreamK;
+    const int mt = kSK ? 0 : p.cluster_reduce ? (cta / p.n_split) % p.m_tiles_per_b : cta % p.m_tiles_per_b;
+    const int j = kSK ? 0 : p.cluster_reduce ? cta % p.n_split : (cta / p.m_tiles_per_b) % p.n_split;
+    const int b = kSK ? 0 : cta / (p.m_tiles_per_b * p.n_split);
     const int m0 = mt * kBlockM;
+    // Stream-K: this CTA's units [u0, u1) and their segments (one per row tile touched; a batch is
+    // one row tile here). Segment 1, when there is one, starts at step t1.
+    const long long u0 = kSK ? static_cast<long long>(cta) * p.sk_units / p.sk_ctas : 0;
+    const long long u1 = kSK ? static_cast<long long>(cta + 1) * p.sk_units / p.sk_ctas : 0;
+    const int r0 = kSK ? static_cast<int>(u0 / p.n_tiles) : 0;
+    const int nseg = kSK ? static_cast<int>((u1 - 1) / p.n_tiles) - r0 + 1 : 1;  // <= kMaxSegments (plan)
+    const int t1 = kSK ? static_cast<int>(static_cast<long long>(r0 + 1) * p.n_tiles - u0) : 0;
     // Split j takes every n_split-th column tile, starting at tile j: the splits of a row tile
     // then read neighbouring K/V tiles at the same time, each row of K in one run of DRAM rather
     // than n_split runs far apart (measured on GB300 against contiguous runs of tiles: long_kv
     // 15.0 against 15.6 us per call, gqa 6.75 against 6.88, decode unchanged).
-    const int T = (p.n_tiles - j + p.n_split - 1) / p.n_split;  // >= 1: n_split <= n_tiles
-    auto tile_of = [&](int t) { return j + t * p.n_split; };   // column tile of the split's step t
+    const int T = kSK ? static_cast<int>(u1 - u0) : (p.n_tiles - j + p.n_split - 1) / p.n_split;  // >= 1
+    auto tile_of = [&](int t) {  // column tile of step t
+        return kSK ? static_cast<int>((u0 + t) % p.n_tiles) : j + t * p.n_split;
+    };
+    auto batch_of = [&](int t) { return kSK ? static_cast<int>((u0 + t) / p.n_tiles) : b; };
+    auto seg_of = [&](int t) { return kSK && t >= t1 ? 1 : 0; };
     // Steps of the K/V ring: with the max-subtracted variant, T steps that stream K alone (the
     // row-maximum pass), then the T steps of the main pass.
     const int T1 = kSafeMax ? T : 0;
@@ -423,11 +453,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.inject_timeout)
                 ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
             if (ok) {
-                ptx::mbar_arrive_expect_tx(bar(BI::kQFull), C::kQBytes);
-                q_armed = true;
+                if constexpr (kSK) {
+                    // One compact Q tile per segment (kSkQRows rows of 128-byte chunks: the tensor
+                    // map's box is kSkQRows high), all on one barrier.
+                    ptx::mbar_arrive_expect_tx(bar(BI::kQFull), nseg * C::kChunks * kSkQRows * 128);
+                    q_armed = true;
+                    for (int k = 0; k < nseg; ++k)
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)  // Q[b, m0:m0+128, 64c:64c+64]
-                    ptx::tma_load_3d(sQ + c * C::kChunkRows128, &tmQ, bar(BI::kQFull), c * 64, m0, b);
+                        for (int c = 0; c < C::kChunks; ++c)  // Q[r0 + k, 0:16, 64c:64c+64]
+                            ptx::tma_load_3d(sQ + (k * C::kChunks + c) * kSkQRows * 128, &tmQ, bar(BI::kQFull),
+                                             c * 64, 0, r0 + k);
+                } else {
+                    ptx::mbar_arrive_expect_tx(bar(BI::kQFull), C::kQBytes);
+                    q_armed = true;
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)  // Q[b, m0:m0+128, 64c:64c+64]
+                        ptx::tma_load_3d(sQ + c * C::kChunkRows128, &tmQ, bar(BI::kQFull), c * 64, m0, b);
+                }
             }
             for (int t = 0; ok && t < U; ++t) {
                 const int s = t % STAGES;
@@ -437,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int n0 = tile_of(t < T1 ? t : t - T1) * kBlockN;
+                const int bt = batch_of(t < T1 ? t : t - T1);
                 const uint32_t sK = sStage0 + s * C::kStageBytes;
                 const uint32_t sV = sK + C::kKBytes;
                 // K and V land on separate barriers: S = Q.K need not wait for V. A step of the
@@ -449,13 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
                 ++armed[s];
                 // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
-                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
-                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
+                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, bt);
+                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, bt);
                 // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
                 if (t >= T1) {
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
+                        ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, bt);
                 }
             }
             if (ok) {
@@ -484,10 +527,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // arithmetic), against 45 from a lone thread looping on its own and 57 from "lane == 0"
         // of a converged warp.
         constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockM, kBlockN, false, true);
+        // A = Q: K-major; 16-column steps advance 32 B in a swizzle row; 8-row groups 1024 B apart.
+        // A stream-K segment's compact Q tile has its 64-column chunks kSkQRows rows apart: the
+        // product reads 128 rows from there, and rows past the tile's (past M here) are never
+        // stored, whatever they hold.
+        const uint32_t q_chunk = kSK ? kSkQRows * 128 : C::kChunkRows128;
         uint64_t a_q[D / 16];
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)  // A = Q: K-major; 16-column steps advance 32 B in a swizzle row
-            a_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * C::kChunkRows128 + (k & 3) * 32, 16, 1024);
+        for (int k = 0; k < D / 16; ++k)
+            a_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * q_chunk + (k & 3) * 32, 16, 1024);
+        // Segment 1's Q tile follows segment 0's: the same descriptors, start address moved on.
+        const uint64_t q_seg_step = static_cast<uint64_t>((C::kChunks * kSkQRows * 128) >> 4);
         auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
             return __all_sync(0xffffffffu, wait_bounded(wc, b_, parity, where));
         };
@@ -514,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ptx::elect_one()) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k], k_desc + static_cast<uint64_t>(k * (2048 >> 4)),
-                                    idesc_s, k > 0 ? 1u : 0u);
+                    ptx::mma_f16_ss(tmem + sb * kBlockN, a_q[k] + (kSK ? seg_of(u) * q_seg_step : 0),
+                                    k_desc + static_cast<uint64_t>(k * (2048 >> 4)), idesc_s, k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
                 if (!kQk && u < T1)
                     ptx::mma_commit(bar(BI::kKvEmpty + s));
@@ -568,15 +618,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tP = tmem + C::kTmemP + pb * 64;
             // B = V: N(=d)-major, 16 rows (2048 B) per k-step; d-chunks 128 rows x 128 B apart.
             const uint64_t v_desc = ptx::sdesc_sw128(sStage0 + s * C::kStageBytes + C::kKBytes, C::kChunkRows128, 1024);
+            // A stream-K segment's first product starts O afresh. It cannot overtake the previous
+            // segment's epilogue, which reads O: it needs P of its tile, and the softmax group writes
+            // that only after the epilogue's closing barrier.
+            const bool fresh = v == 0 || (kSK && v == t1);
             if (ptx::elect_one()) {
                 // A = P in tensor memory: 16 K-columns per step are 8 tensor-memory columns.
-                ptx::mma_f16_ts(tmem_o, tP, v_desc, idesc_o, v > 0 ? 1u : 0u);
+                ptx::mma_f16_ts(tmem_o, tP, v_desc, idesc_o, fresh ? 0u : 1u);
 #pragma unroll
                 for (int k = 1; k < kBlockN / 16; ++k)
                     ptx::mma_f16_ts(tmem_o, tP + k * 8, v_desc + static_cast<uint64_t>(k * (2048 >> 4)), idesc_o, 1u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
-                if (v == T - 1)  // committed by the thread that issued every P.V
+                // Committed by the thread that issued every P.V: O of the last step (of each
+                // stream-K segment) is complete, one OFull phase per segment.
+                if (v == T - 1 || (kSK && v == t1 - 1))
                     ptx::mma_commit(bar(BI::kOFull));
             }
             __syncwarp();
@@ -767,7 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // wait on tensor memory or a barrier, the other group's warps on the same scheduler keep
         // the MUFU unit busy. A thread covers its row's 128 columns of a tile in two 64-column
         // halves (64 fp32 registers at a time). Step u of the ring is tile t = u - T1.
-        for (u = (T1 % 2 == g) ? T1 : T1 + 1; ok && u < U; u += 2) {
+        // Stream-K: each segment's steps, then that segment's epilogue; otherwise one segment.
+        for (int k = 0; k < nseg; ++k) {
+        const int t_beg = k == 0 ? 0 : t1;
+        const int t_end = k + 1 < nseg ? t1 : T;
+        for (u = T1 + t_beg + ((T1 + t_beg) % 2 == g ? 0 : 1); ok && u < T1 + t_end; u += 2) {
             const int t = u - T1;
             const int pb = t % kPBuffers;
             if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
@@ -831,7 +891,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0)
                 ptx::mbar_arrive(bar(BI::kPFull + pb));
         }
+        if constexpr (kSK) {
+            // -------------------------------------------------------- stream-K segment epilogue
+            // The segment's partial (fp32 numerators and the row sum, rows < M) goes to slot
+            // c - c_first(r) of its row tile r = r0 + k (a batch: one row tile each), for the second
+            // kernel; the row tile's last contributor also zeroes its unused slots, so each call
+            // leaves every slot the second kernel reads defined. A barrier of all eight softmax
+            // warps closes the epilogue: O and the row-sum exchange are free again after it.
+            const float lg = (__uint_as_float(static_cast<uint32_t>(acc[0])) +
+                              __uint_as_float(static_cast<uint32_t>(acc[0] >> 32))) +
+                             (__uint_as_float(static_cast<uint32_t>(acc[1])) +
+                              __uint_as_float(static_cast<uint32_t>(acc[1] >> 32)));
+            acc[0] = 0;
+            acc[1] = 0;
+            l_xchg[g * kBlockM + row] = lg;
+            const bool seg_ready = ptx::named_barrier_and(
+                kSoftmaxBarrier, kSoftmaxThreads,
+                ok && warp_wait(bar(BI::kOFull), static_cast<uint32_t>(k) & 1u, BI::kOFull));
+            const float ls = l_xchg[row] + l_xchg[kBlockM + row];
+            if (!seg_ready) {
+                ok = false;
+            } else {
+                ptx::tc_fence_after();
+                const int r = r0 + k;
+                const int c_first = static_cast<int>(sk_cta_of(static_cast<long long>(r) * p.n_tiles, p.sk_units, p.sk_ctas));
+                const int c_last = static_cast<int>(
+                    sk_cta_of(static_cast<long long>(r + 1) * p.n_tiles - 1, p.sk_units, p.sk_ctas));
+                const int slot = cta - c_first;
+                const int zero_from = cta == c_last ? c_last - c_first + 1 : p.sk_slots;
+                const bool mine = row < p.M;
+                if (warp_rows) {
+#pragma unroll
+                    for (int c = 0; c < C::kHalfCols / 32; ++c) {
+                        uint32_t rv[32];
+                        const int col = g * C::kHalfCols + c * 32;
+                        ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, rv);
+                        ptx::tmem_ld_wait(rv);
+                        if (mine) {
+                            float4 *dst = reinterpret_cast<float4 *>(
+                                p.ws_o + ((static_cast<size_t>(slot) * p.B + r) * p.M + row) * D + col);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                dst[q] = make_float4(__uint_as_float(rv[4 * q]), __uint_as_float(rv[4 * q + 1]),
+                                                     __uint_as_float(rv[4 * q + 2]), __uint_as_float(rv[4 * q + 3]));
+                            for (int z = zero_from; z < p.sk_slots; ++z) {
+                                float4 *zd = reinterpret_cast<float4 *>(
+                                    p.ws_o + ((static_cast<size_t>(z) * p.B + r) * p.M + row) * D + col);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q)
+                                    zd[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+                    }
+                }
+                if (g == 0 && mine) {
+                    p.ws_l[(static_cast<size_t>(slot) * p.B + r) * p.M + row] = ls;
+                    for (int z = zero_from; z < p.sk_slots; ++z)
+                        p.ws_l[(static_cast<size_t>(z) * p.B + r) * p.M + row] = 0.f;
+                }
+                ptx::tc_fence_before();
+                ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
+            }
+        }
+        }  // segments
 
+        if constexpr (!kSK) {
         // ------------------------------------------------------------ epilogue
         // Row sum: this thread's tiles, then the two groups' sums added in a fixed order.
         const float l_group = (__uint_as_float(static_cast<uint32_t>(acc[0])) +
@@ -955,6 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        }  // !kSK
     }
 
     // On-chip combine of the split partials: after the first cluster barrier every CTA's staged

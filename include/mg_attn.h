@@ -92,6 +92,15 @@ typedef enum {
                                       on GB300 it is slower than the default one-tile kernel (see
                                       info.q_tiles_per_cta) */
 #define MG_FLAG_NO_Q_PAIRS 0x40    /* always use the one-tile kernel (the default) */
+#define MG_FLAG_STREAM_K 0x80      /* use the stream-K schedule where it applies (the graph as written, at
+                                      most 16 query rows per batch, no explicit n_split, runs of at most
+                                      ceil(N/128) units, and no more tiles for the busiest CTA than the split
+                                      schedule gives): the B x ceil(N/128) (batch, column tile) units form one
+                                      sequence that the grid's CTAs share in equal contiguous runs, one CTA
+                                      per SM; each run's part of a batch is a partial that the second kernel
+                                      sums in a fixed order. Opt-in: measured on GB300 it is not faster than
+                                      the default split schedule on the decode shapes; see info.schedule */
+#define MG_FLAG_NO_STREAM_K 0x100  /* the split schedule (N split n_split ways per row tile; the default) */
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and
                                       the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */
@@ -126,6 +135,10 @@ typedef struct {
                                 one cluster barrier (no second kernel); 0: second kernel */
     int32_t q_tiles_per_cta; /* 128-row Q tiles per CTA: 1 (one-tile kernel) or 2 (two-Q-tile
                                 kernel; m_tiles / 2 row-tile pairs, each split n_split ways) */
+    int32_t schedule;        /* 0: split (CTA j of a row tile takes column tiles j, j + n_split, ...);
+                                1: stream-K (grid_ctas CTAs share the m_tiles x n_tiles units in equal
+                                contiguous runs; n_split is then the second kernel's partials per row) */
+    int32_t reserved1;
 } mg_attn_plan_info;
 
 /*

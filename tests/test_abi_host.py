@@ -51,9 +51,9 @@ def test_struct_layout_matches_header(tmp_path):
 #include "mg_attn.h"
 int main(void) {
   printf("%zu %zu %zu\\n", sizeof(mg_attn_options), offsetof(mg_attn_options, timeout_ns), offsetof(mg_attn_options, flags));
-  printf("%zu %zu %zu %zu %zu\\n", sizeof(mg_attn_plan_info), offsetof(mg_attn_plan_info, block_m),
+  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(mg_attn_plan_info), offsetof(mg_attn_plan_info, block_m),
          offsetof(mg_attn_plan_info, num_sms), offsetof(mg_attn_plan_info, workspace_bytes),
-         offsetof(mg_attn_plan_info, cluster_ctas));
+         offsetof(mg_attn_plan_info, cluster_ctas), offsetof(mg_attn_plan_info, schedule));
   return 0;
 }
 """)
@@ -63,7 +63,7 @@ int main(void) {
     O, I = _lib.MgAttnOptions, _lib.MgAttnPlanInfo
     assert [int(x) for x in l1.split()] == [ctypes.sizeof(O), O.timeout_ns.offset, O.flags.offset]
     assert [int(x) for x in l2.split()] == [ctypes.sizeof(I), I.block_m.offset, I.num_sms.offset,
-                                            I.workspace_bytes.offset, I.cluster_ctas.offset]
+                                            I.workspace_bytes.offset, I.cluster_ctas.offset, I.schedule.offset]
 
 
 def test_status_strings_and_version(lib):
@@ -91,6 +91,9 @@ def test_query_decisions(B, M, N, d):
     # even number of row tiles per batch), and then only for throughput-bound shapes.
     assert q in (1, 2) and (q == 1 or (d == 64 and -(-M // 128) % 2 == 0))
     units = m_tiles // q
+    if info["schedule"] == 1:  # stream-K: one CTA per SM (or per unit), n_split partial slots per row
+        assert info["grid_ctas"] == min(152, m_tiles * n_tiles) and M <= 16
+        return
     assert info["grid_ctas"] == units * info["n_split"]
     if units >= 152:
         assert info["n_split"] == 1
@@ -136,12 +139,51 @@ def test_query_split_fills_its_tiles_when_hbm_bound():
     # Few query rows (HBM-bound): among split counts down to 4/5 of one wave, the plan takes the one
     # that leaves the fewest idle tile slots. Decode-like (16, 8, 32768, 128): 16 row tiles, one wave
     # is 9 splits (28 or 29 of 256 tiles each); 8 splits give every CTA 32.
-    info = mg.mg_attn_query(16, 8, 32768, 128, 152)
+    info = mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_NO_STREAM_K)
     assert info["n_split"] == 8 and info["grid_ctas"] == 128
     # A shape whose one-wave split already divides its tiles evenly keeps it.
-    assert mg.mg_attn_query(64, 1, 4096, 128, 152)["n_split"] == 2
+    assert mg.mg_attn_query(64, 1, 4096, 128, 152, flags=mg.MG_FLAG_NO_STREAM_K)["n_split"] == 2
     # Many query rows per batch: every SM is used (one wave, 38 splits of 13 or 14 tiles).
     assert mg.mg_attn_query(2, 256, 65536, 64, 152)["n_split"] == 38
+
+
+def _sk_slots(rows, n_tiles, G):
+    # Restated from the schedule's definition: CTA c takes units [c U / G, (c+1) U / G).
+    U = rows * n_tiles
+    owner = [0] * U
+    for c in range(G):
+        for u in range(c * U // G, (c + 1) * U // G):
+            owner[u] = c
+    return max(owner[(r + 1) * n_tiles - 1] - owner[r * n_tiles] + 1 for r in range(rows))
+
+
+@pytest.mark.parametrize("B,M,N,d", [(16, 8, 32768, 128), (64, 1, 4096, 128), (20, 5, 3000, 64), (37, 16, 1032, 64)])
+def test_query_stream_k(B, M, N, d):
+    info = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_STREAM_K)
+    n_tiles = -(-N // 128)
+    U = B * n_tiles
+    G = min(U, 152)
+    assert info["schedule"] == 1 and info["grid_ctas"] == G and info["cluster_ctas"] == 0
+    assert info["kernels_per_run"] == 2 and info["n_split"] == _sk_slots(B, n_tiles, G)
+    assert info["workspace_bytes"] == 256 + info["n_split"] * B * M * (d + 1) * 4
+    assert -(-U // G) <= n_tiles  # a run touches at most two batches
+
+
+def test_query_stream_k_choices():
+    # Opt-in: the default plans keep the split schedule.
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152)["schedule"] == 0
+    assert mg.mg_attn_query(64, 1, 4096, 128, 152)["schedule"] == 0
+    assert mg.mg_attn_query(64, 1, 4096, 128, 152, flags=mg.MG_FLAG_STREAM_K)["schedule"] == 1
+    # Not where it does not apply: more than 16 rows per batch, the variants, an explicit split.
+    assert mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_STREAM_K)["schedule"] == 0
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX)["schedule"] == 0
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152, n_split=8)["schedule"] == 0
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_NO_STREAM_K)["schedule"] == 0
+    # Where the runs would exceed one batch's tiles (more batches than SMs), it does not apply.
+    assert mg.mg_attn_query(5, 16, 40000, 64, 152, flags=mg.MG_FLAG_STREAM_K)["schedule"] == 1
+    assert mg.mg_attn_query(400, 4, 1024, 64, 152, flags=mg.MG_FLAG_STREAM_K)["schedule"] == 0
+    with pytest.raises(mg.MgAttnError):
+        mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_STREAM_K | mg.MG_FLAG_NO_STREAM_K)
 
 
 def test_query_cluster_choices():
@@ -204,8 +246,8 @@ def test_query_options():
     ((2, 256, 4100, 64), {}, mg.MG_ERR_LAYOUT),
     ((2, 256, 4096, 64), {"n_split": 33}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 64), {"flags": 0x80}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 64), {"flags": 0x100}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x200}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x400}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),

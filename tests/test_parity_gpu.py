@@ -221,6 +221,40 @@ def test_two_q_tile_kernel_matches_one_tile_kernel(flags):
     assert torch.equal(O2, O2b)
 
 
+SK_SHAPES = [  # (B, M, N, d): the stream-K schedule forced (MG_FLAG_STREAM_K)
+    (20, 5, 3000, 64),     # runs of 3-4 units crossing batches; ragged N
+    (37, 16, 1032, 64),    # 16 rows; runs of 2-3 units; ragged N
+    (7, 3, 1000, 128),     # fewer units than SMs: one unit per CTA
+    (64, 1, 4096, 128),    # the launch example's shapes
+    (16, 8, 32768, 128),   # decode-like
+    (3, 9, 262144, 64),    # long runs: 1536 units over 152 CTAs, 2 batches touched by many
+]
+
+
+@pytest.mark.parametrize("B,M,N,d", SK_SHAPES)
+def test_stream_k_schedule(B, M, N, d):
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=B + M + N)
+    ref = oracle.attention(q, k, v)
+    O, plan = run_gpu(q, k, v, flags=mg.MG_FLAG_STREAM_K)
+    assert plan.info["schedule"] == 1
+    assert_parity(O, ref, f"stream-K {B, M, N, d} slots={plan.info['n_split']} ctas={plan.info['grid_ctas']}")
+    # Reproducible bit for bit, and on a second call (every partial slot rewritten or re-zeroed).
+    O2 = torch.full_like(O, float("nan"))
+    plan.run(q.cuda(), k.cuda(), v.cuda(), O2)
+    torch.cuda.synchronize()
+    assert torch.equal(O, O2)
+
+
+def test_stream_k_matches_split_schedule():
+    q, k, v, _ = inputs.make_config("decode_m1")
+    ref = oracle.attention(q, k, v)
+    O_sk, p_sk = run_gpu(q, k, v, flags=mg.MG_FLAG_STREAM_K)
+    O_sp, p_sp = run_gpu(q, k, v, flags=mg.MG_FLAG_NO_STREAM_K)
+    assert p_sk.info["schedule"] == 1 and p_sp.info["schedule"] == 0
+    assert_parity(O_sk, ref, "stream-K")
+    assert_parity(O_sp, ref, "split")
+
+
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
     # Scores 0 everywhere -> every weight is exp(0)=1: any column past N that leaked into the row
     # sum (zero-filled K gives exp(0)=1 too) would pull the mean toward 0.
