@@ -13,7 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(_HERE)
 SOURCES = [os.path.join(_HERE, "csrc", "mg_attn.cu"), os.path.join(_HERE, "csrc", "mg_diag.cu")]
 DEPS = SOURCES + [os.path.join(_HERE, "csrc", "mg_attn_kernels.cuh"), os.path.join(_HERE, "csrc", "mg_combine.cuh"),
-                  os.path.join(_HERE, "csrc", "mg_attn_pair.cuh"),
+                  os.path.join(_HERE, "csrc", "mg_attn_pair.cuh"), os.path.join(_HERE, "csrc", "mg_attn_swap.cuh"),
                   os.path.join(_HERE, "csrc", "ptx.cuh"),
                   os.path.join(ROOT, "include", "mg_attn.h"), os.path.join(ROOT, "include", "mg_diag.h")]
 OUT = os.path.join(_HERE, "libmgattn.so")

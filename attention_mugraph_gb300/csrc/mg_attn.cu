@@ -16,6 +16,7 @@
 
 #include "mg_attn_kernels.cuh"
 #include "mg_attn_pair.cuh"
+#include "mg_attn_swap.cuh"
 #include "mg_combine.cuh"
 
 namespace {
@@ -108,6 +109,16 @@ FwdKernel pair_kernel(int stages)
     }
 }
 
+// The few-row specialisation (head dim 128, transposed products) for a pipeline depth.
+FwdKernel swap_kernel(int stages)
+{
+    switch (stages) {
+    case 2: return mg::mg_attn_fwd_swap<2>;
+    case 3: return mg::mg_attn_fwd_swap<3>;
+    default: return nullptr;
+    }
+}
+
 // The one-tile kernel under the stream-K schedule (the graph as written).
 FwdKernel sk_kernel(int64_t d, int stages) { return fwd_kernel_variant<mg::kStreamK>(d, stages); }
 
@@ -185,7 +196,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     if (o.reserved != 0 ||
         (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX |
                      MG_FLAG_QK_NORM | MG_FLAG_Q_PAIRS | MG_FLAG_NO_Q_PAIRS | MG_FLAG_STREAM_K |
-                     MG_FLAG_NO_STREAM_K)) != 0)
+                     MG_FLAG_NO_STREAM_K | MG_FLAG_SWAP_AB | MG_FLAG_NO_SWAP_AB)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -197,6 +208,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         return fail(MG_ERR_CONFIG, "MG_FLAG_Q_PAIRS and MG_FLAG_NO_Q_PAIRS together");
     if ((o.flags & MG_FLAG_STREAM_K) && (o.flags & MG_FLAG_NO_STREAM_K))
         return fail(MG_ERR_CONFIG, "MG_FLAG_STREAM_K and MG_FLAG_NO_STREAM_K together");
+    if ((o.flags & MG_FLAG_SWAP_AB) && (o.flags & MG_FLAG_NO_SWAP_AB))
+        return fail(MG_ERR_CONFIG, "MG_FLAG_SWAP_AB and MG_FLAG_NO_SWAP_AB together");
 
     // One wave: as many splits per unit (a row tile, or a pair of them) as keep every SM busy,
     // never fewer than one column tile per split.
@@ -264,7 +277,13 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         if (n_split < 2)  // every run within one batch and every batch in one run: nothing to combine
             stream_k = false, n_split = one_wave(units);
     }
-    const bool cluster = !stream_k && !(o.flags & MG_FLAG_NO_CLUSTER) && n_split >= 2 && n_split <= kMaxCluster;
+    // The few-row specialisation: head dim 128, at most 16 query rows per batch, the graph as
+    // written under the split schedule; the default there (measured on GB300, us per call against
+    // the one-tile kernel: (16, 8, 32768, 128) 45.8 against 48.2, (64, 1, 4096, 128) 25.2 against 26.9).
+    const bool swap = !pair && !stream_k && d == 128 && M <= mg::kSwapNQ &&
+                      !(o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) && !(o.flags & MG_FLAG_NO_SWAP_AB);
+    const bool cluster =
+        !stream_k && !swap && !(o.flags & MG_FLAG_NO_CLUSTER) && n_split >= 2 && n_split <= kMaxCluster;
     if (!stream_k && units * n_split > 0x7fffffffLL)
         return fail(MG_ERR_INVALID_ARG, "grid too large");
 
@@ -272,9 +291,12 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     int stages = o.stages == 0 ? auto_stages(d) : o.stages;
     if (stages < 2 || stages > 6)
         return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 6]", stages);
-    const uint32_t smem = pair ? mg::pair_smem_bytes(stages) : mg::fwd_smem_bytes(static_cast<int>(d), stages);
+    const uint32_t smem = pair   ? mg::pair_smem_bytes(stages)
+                          : swap ? mg::swap_smem_bytes(stages)
+                                 : mg::fwd_smem_bytes(static_cast<int>(d), stages);
     if (static_cast<int64_t>(smem) > max_smem ||
-        !(pair ? pair_kernel(stages) : stream_k ? sk_kernel(d, stages) : fwd_kernel(d, stages, o.flags)))
+        !(pair ? pair_kernel(stages)
+               : swap ? swap_kernel(stages) : stream_k ? sk_kernel(d, stages) : fwd_kernel(d, stages, o.flags)))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
 
@@ -311,6 +333,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->cluster_ctas = cluster ? static_cast<int32_t>(n_split) : 0;
     info->q_tiles_per_cta = pair ? 2 : 1;
     info->schedule = stream_k ? 1 : 0;
+    info->swap_ab = swap ? 1 : 0;
     if (timeout_ns)
         *timeout_ns = o.timeout_ns ? static_cast<unsigned long long>(o.timeout_ns) : kDefaultTimeoutNs;
     if (flags)
@@ -322,6 +345,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
 // The fused kernel a plan's decisions call for.
 FwdKernel plan_kernel(const mg_attn_plan_info &info, int flags)
 {
+    if (info.swap_ab == 1)
+        return swap_kernel(info.stages);
     if (info.schedule == 1)
         return sk_kernel(info.d, info.stages);
     return info.q_tiles_per_cta == 2 ? pair_kernel(info.stages) : fwd_kernel(info.d, info.stages, flags);
@@ -660,7 +685,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     const void *ptrs[4] = {Q, K, V, O};
     const uint64_t dims[4][3] = {{d, M, B}, {N, d, B}, {d, N, B}, {d, M, B}};
     // Under the stream-K schedule the Q box is kSkQRows rows high (a compact tile per segment).
-    const uint32_t qrows = in.schedule == 1 ? static_cast<uint32_t>(mg::kSkQRows) : 128u;
+    const uint32_t qrows = in.schedule == 1 || in.swap_ab == 1 ? static_cast<uint32_t>(mg::kSkQRows) : 128u;
     const uint32_t box1[4] = {qrows, static_cast<uint32_t>(d), 128u, 128u};
     for (int i = 0; i < 4; ++i) {
         if (plan->map_ptr[i] != ptrs[i]) {
@@ -910,7 +935,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     const void *ptrs[4] = {Q, K, V, O};
     const uint64_t uB = B, uM = M, uN = N, ud = d;
     const uint64_t dims[4][3] = {{ud, uM, uB}, {uN, ud, uB}, {ud, uN, uB}, {ud, uM, uB}};
-    const uint32_t qrows = in.schedule == 1 ? static_cast<uint32_t>(mg::kSkQRows) : 128u;
+    const uint32_t qrows = in.schedule == 1 || in.swap_ab == 1 ? static_cast<uint32_t>(mg::kSkQRows) : 128u;
     const uint32_t box1[4] = {qrows, static_cast<uint32_t>(d), 128u, 128u};
     for (int i = 0; i < 4; ++i)
         if ((st = encode_3d(&maps[i], ptrs[i], dims[i][0], dims[i][1], dims[i][2], 64u, box1[i])) != MG_OK)

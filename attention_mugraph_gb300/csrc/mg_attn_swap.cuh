@@ -1,0 +1,373 @@
+// mg_attn_swap.cuh -- the fused kernel specialised for few query rows (at most 16 per batch, head
+// dim 128, the graph as written; Mirage documentation, tutorials/group-query-attention, "Define
+// GQA Computation Graph", and its launch example "Launch Mirage-Generated GQA Kernel" with one query
+// row per head).
+//
+// The one-tile kernel puts the query rows on the MMA's 128-row M axis, so a decode batch of 8 rows
+// leaves 120 of them zero. Here the operands swap roles ("swap-AB"): per K/V tile of 128 keys,
+//     S^T = K^T . Q^T     M = 128 keys, N = 16 query rows, K = d      (tcgen05, fp32 in tensor memory)
+//     P^T = exp(S^T)      fp32; l[q] += sum over the tile's keys; fp16 P^T to shared memory
+//     O^T += V^T . P^T    M = d = 128, N = 16 query rows, K = 128 keys
+// so every MMA row is a key (or an output column) and nothing is padded but the N axis (16 columns
+// for up to 16 rows). K and V serve as A operands in the layouts their TMA tiles already have (keys,
+// resp. d, contiguous), Q^T and P^T as K-major B operands. S^T and O^T take 16 tensor-memory
+// columns each; the row sum of query q is a sum over keys, i.e. over tensor-memory lanes, so each
+// thread keeps one per query for its keys and the CTA reduces them once at the end.
+//
+// Roles, ring, bounded waits and unwinding are the one-tile kernel's (mg_attn_kernels.cuh): a TMA
+// producer warp, an S-issuing warp, a P.V-issuing warp and two groups of four softmax warps that take
+// alternate tiles, with the same barrier protocol (tests/pipeline_model.py, Sim, graph as written);
+// P lives in shared memory, written by the softmax warps and read by the tensor core after a proxy
+// fence. Split partials (fp32 O^T columns and row sums) go to the second kernel.
+#pragma once
+
+#include "mg_attn_kernels.cuh"
+
+namespace mg {
+
+constexpr int kSwapD = 128;
+constexpr int kSwapNQ = 16;                                      // query rows per tile (MMA N)
+constexpr uint32_t kSwapQBytes = kSwapNQ * kSwapD * 2;           // two 64-column chunks of 16 rows
+constexpr uint32_t kSwapChunk = kSwapNQ * 128;                   // one such chunk (2 KB)
+constexpr uint32_t kSwapStageBytes = 2u * kSwapD * kBlockN * 2;  // K + V tile
+constexpr uint32_t kSwapPBytes = kSwapNQ * kBlockN * 2;          // P^T: two 64-key chunks of 16 rows
+constexpr int kSwapPBuffers = 3;
+constexpr uint32_t kSwapTmemCols = 64;                           // S^T buffers at 0 and 16, O^T at 32
+constexpr uint32_t kSwapTmemO = 32;
+
+// Shared-memory bytes: alignment slack, Q^T, the P^T ring, the K/V ring, the per-warp row sums and
+// the barriers.
+__host__ __device__ constexpr uint32_t swap_smem_bytes(int stages)
+{
+    return 1024u + kSwapQBytes + kSwapPBuffers * kSwapPBytes + static_cast<uint32_t>(stages) * kSwapStageBytes +
+           kSoftmaxWarps * kSwapNQ * 4 + 512u;
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    mg_attn_fwd_swap(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const __grid_constant__ CUtensorMap tmW, const FwdParams p)
+{
+    constexpr int D = kSwapD;
+    using BI = Bars<STAGES, kSwapPBuffers>;
+    static_assert(swap_smem_bytes(STAGES) <= 232448u, "tile configuration exceeds 227 KB");
+    (void)tmO;
+    (void)tmW;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = ptx::smem_u32(smem);
+    const uint32_t sP0 = sQ + kSwapQBytes;                        // P^T buffer pb at sP0 + pb * kSwapPBytes
+    const uint32_t sStage0 = sP0 + kSwapPBuffers * kSwapPBytes;   // 1024-aligned: 4 KB steps so far
+    float *l_red = reinterpret_cast<float *>(smem + kSwapQBytes + kSwapPBuffers * kSwapPBytes + STAGES * kSwapStageBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(l_red + kSoftmaxWarps * kSwapNQ);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // CTA -> (b, split j): one row tile per batch (M <= 16); split j takes the column tiles j,
+    // j + n_split, ... as in the one-tile kernel.
+    const int cta = blockIdx.x;
+    const int j = cta % p.n_split;
+    const int b = cta / p.n_split;
+    const int T = (p.n_tiles - j + p.n_split - 1) / p.n_split;  // >= 1
+    auto tile_of = [&](int t) { return j + t * p.n_split; };
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(BI::kQFull), 1);
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(bar(BI::kKFull + s), 1);
+            ptx::mbar_init(bar(BI::kVFull + s), 1);
+            ptx::mbar_init(bar(BI::kKvEmpty + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(bar(BI::kSFull + s), 1);
+            ptx::mbar_init(bar(BI::kSEmpty + s), kGroupWarps);
+        }
+        for (int s = 0; s < kSwapPBuffers; ++s) {
+            ptx::mbar_init(bar(BI::kPFull + s), kGroupWarps);
+            ptx::mbar_init(bar(BI::kPEmpty + s), 1);
+        }
+        ptx::mbar_init(bar(BI::kOFull), 1);
+        ptx::mbar_init(bar(BI::kDrain), 1);
+        ptx::mbar_init(bar(BI::kDrainPv), 1);
+        ptx::mbar_init(bar(BI::kNever), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmQ);
+        ptx::prefetch_tensormap(&tmK);
+        ptx::prefetch_tensormap(&tmV);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kSwapTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+
+    const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            bool q_armed = false;
+            int armed[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s)
+                armed[s] = 0;
+            bool ok = true;
+            if (p.inject_timeout)
+                ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
+            if (ok) {
+                // Q[b, 0:16, 64c:64c+64] (the tensor map's box is 16 rows; rows past M read as zero).
+                ptx::mbar_arrive_expect_tx(bar(BI::kQFull), kSwapQBytes);
+                q_armed = true;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_load_3d(sQ + c * kSwapChunk, &tmQ, bar(BI::kQFull), c * 64, 0, b);
+            }
+            for (int t = 0; ok && t < T; ++t) {
+                const int s = t % STAGES;
+                const uint32_t round = static_cast<uint32_t>(t / STAGES);
+                if (t >= STAGES && !wait_bounded(wc, bar(BI::kKvEmpty + s), (round & 1u) ^ 1u, BI::kKvEmpty + s)) {
+                    ok = false;
+                    break;
+                }
+                const int n0 = tile_of(t) * kBlockN;
+                const uint32_t sK = sStage0 + s * kSwapStageBytes;
+                const uint32_t sV = sK + D * kBlockN * 2;
+                ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), D * kBlockN * 2);
+                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), kBlockN * D * 2);
+                ++armed[s];
+                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
+                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_load_3d(sV + c * TileCfg<D>::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
+            }
+            if (ok) {
+                for (int u = T - STAGES > 0 ? T - STAGES : 0; ok && u < T; ++u)
+                    ok = wait_bounded(wc, bar(BI::kKvEmpty + u % STAGES), static_cast<uint32_t>(u / STAGES) & 1u,
+                                      BI::kKvEmpty + u % STAGES);
+            }
+            if (*abort_flag) {
+                if (q_armed)
+                    wait_drain(bar(BI::kQFull), 0, p.timeout_ns);
+#pragma unroll
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed[s] > 0) {
+                        wait_drain(bar(BI::kKFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
+                        wait_drain(bar(BI::kVFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- S^T = K^T . Q^T issuer
+        // A = K^T: M-major (keys contiguous), the two 64-key halves D*128 B apart, 8-row groups
+        // along d 1024 B apart, 16 d-rows (2048 B) per k-step. B = Q^T: K-major (d contiguous), 16
+        // query rows, 64-column chunks kSwapChunk apart, 16-column steps 32 B inside a swizzle row.
+        constexpr uint32_t idesc_s = ptx::idesc_f16_f32(kBlockN, kSwapNQ, true, false);
+        uint64_t b_q[D / 16];
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+            b_q[k] = ptx::sdesc_sw128(sQ + (k >> 2) * kSwapChunk + (k & 3) * 32, 16, 1024);
+        auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+            return __all_sync(0xffffffffu, wait_bounded(wc, b_, parity, where));
+        };
+        bool ok = warp_wait(bar(BI::kQFull), 0, BI::kQFull);
+        for (int u = 0; ok && u < T; ++u) {
+            const int s = u % STAGES;
+            const int sb = u & 1;
+            if (!warp_wait(bar(BI::kKFull + s), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + s) ||
+                (u >= 2 &&
+                 !warp_wait(bar(BI::kSEmpty + sb), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u, BI::kSEmpty + sb))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t a_k = ptx::sdesc_sw128(sStage0 + s * kSwapStageBytes, D * 128, 1024);
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    ptx::mma_f16_ss(tmem + sb * kSwapNQ, a_k + static_cast<uint64_t>(k * (2048 >> 4)), b_q[k], idesc_s,
+                                    k > 0 ? 1u : 0u);
+                ptx::mma_commit(bar(BI::kSFull + sb));
+            }
+            __syncwarp();
+        }
+        if (ptx::elect_one()) {
+            ptx::mma_commit(bar(BI::kDrain));
+            wait_drain(bar(BI::kDrain), 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ---------------------------------------------------------------- O^T += V^T . P^T issuer
+        // A = V^T: M-major (d contiguous), the two 64-column halves 128 rows x 128 B apart, 16 keys
+        // (2048 B) per k-step. B = P^T: K-major (keys contiguous), 16 query rows, 64-key chunks
+        // kSwapChunk apart.
+        constexpr uint32_t idesc_o = ptx::idesc_f16_f32(D, kSwapNQ, true, false);
+        auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+            return __all_sync(0xffffffffu, wait_bounded(wc, b_, parity, where));
+        };
+        bool ok = true;
+        for (int v = 0; ok && v < T; ++v) {
+            const int pb = v % kSwapPBuffers;
+            const int s = v % STAGES;
+            if (!(warp_wait(bar(BI::kVFull + s), static_cast<uint32_t>(v / STAGES) & 1u, BI::kVFull + s) &&
+                  warp_wait(bar(BI::kPFull + pb), static_cast<uint32_t>(v / kSwapPBuffers) & 1u, BI::kPFull + pb))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t a_v =
+                ptx::sdesc_sw128(sStage0 + s * kSwapStageBytes + D * kBlockN * 2, TileCfg<D>::kChunkRows128, 1024);
+            const uint32_t sP = sP0 + pb * kSwapPBytes;
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int k = 0; k < kBlockN / 16; ++k)
+                    ptx::mma_f16_ss(tmem + kSwapTmemO, a_v + static_cast<uint64_t>(k * (2048 >> 4)),
+                                    ptx::sdesc_sw128(sP + (k >> 2) * kSwapChunk + (k & 3) * 32, 16, 1024), idesc_o,
+                                    (v > 0 || k > 0) ? 1u : 0u);
+                ptx::mma_commit(bar(BI::kKvEmpty + s));
+                ptx::mma_commit(bar(BI::kPEmpty + pb));
+                if (v == T - 1)
+                    ptx::mma_commit(bar(BI::kOFull));
+            }
+            __syncwarp();
+        }
+        if (ok) {
+            for (int u = T - kSwapPBuffers > 0 ? T - kSwapPBuffers : 0; ok && u < T; ++u)
+                ok = warp_wait(bar(BI::kPEmpty + u % kSwapPBuffers), static_cast<uint32_t>(u / kSwapPBuffers) & 1u,
+                               BI::kPEmpty + u % kSwapPBuffers);
+        }
+        if (!ok) {
+            if (ptx::elect_one()) {
+                ptx::mma_commit(bar(BI::kDrainPv));
+                wait_drain(bar(BI::kDrainPv), 0, p.timeout_ns);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax + epilogue
+        const int sw = warp - 2;
+        const int q4 = warp & 3;
+        const int g = sw >> 2;
+        const int key = q4 * 32 + lane;  // this thread's key (tensor-memory lane) within a tile
+        const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
+        auto warp_wait = [&](uint32_t b_, uint32_t parity, int where) -> bool {
+            return __all_sync(0xffffffffu, wait_bounded(wc, b_, parity, where));
+        };
+        const ptx::ExpPairConsts ek = ptx::exp_pair_consts();
+        float lq[kSwapNQ];  // this thread's part of each query row's sum (its keys, fp32)
+#pragma unroll
+        for (int q = 0; q < kSwapNQ; ++q)
+            lq[q] = 0.f;
+        // P^T element (query q, key) in its buffer: 64-key chunk, row q, the 128-byte swizzle.
+        const uint32_t p_off = (key / 64) * kSwapChunk + (((static_cast<uint32_t>(key % 64) / 8) << 4) | ((key % 8) * 2));
+        bool ok = true;
+        for (int u = g; ok && u < T; u += 2) {
+            const int pb = u % kSwapPBuffers;
+            if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t r[kSwapNQ];
+            ptx::tmem_ld_32x32b_x16(tmem + lane_addr + g * kSwapNQ, r);
+            ptx::tmem_ld_wait16(r);
+            // S^T is in registers: the buffer can take this group's next tile.
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(bar(BI::kSEmpty + g));
+            if (u >= kSwapPBuffers &&
+                !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(u / kSwapPBuffers) & 1u) ^ 1u, BI::kPEmpty + pb)) {
+                ok = false;
+                break;
+            }
+            const bool valid = tile_of(u) * kBlockN + key < p.N;  // keys past N weigh 0
+            uint8_t *pt = smem + kSwapQBytes + pb * kSwapPBytes;
+#pragma unroll
+            for (int q = 0; q < kSwapNQ; q += 2) {
+                uint32_t e0, e1;
+                ptx::exp_pair_mufu(r[q], r[q + 1], ek, 0, e0, e1);
+                e0 = valid ? e0 : 0u;
+                e1 = valid ? e1 : 0u;
+                lq[q] += __uint_as_float(e0);
+                lq[q + 1] += __uint_as_float(e1);
+                // Rows q and q + 1 of the 128-byte swizzle: unit index XOR row mod 8.
+                *reinterpret_cast<__half *>(pt + (p_off ^ ((q & 7) << 4)) + q * 128) = __float2half_rn(__uint_as_float(e0));
+                *reinterpret_cast<__half *>(pt + (p_off ^ (((q + 1) & 7) << 4)) + (q + 1) * 128) =
+                    __float2half_rn(__uint_as_float(e1));
+            }
+            ptx::fence_proxy_async_smem();  // the tensor core reads P^T through the async proxy
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(bar(BI::kPFull + pb));
+        }
+
+        // ------------------------------------------------------------ epilogue
+        // Row sums: each warp adds its 32 keys' parts (the same butterfly order on every lane), the
+        // eight warps' sums meet in shared memory and add in warp order.
+#pragma unroll
+        for (int q = 0; q < kSwapNQ; ++q) {
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                lq[q] += __shfl_xor_sync(0xffffffffu, lq[q], o);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < kSwapNQ; ++q)
+                l_red[sw * kSwapNQ + q] = lq[q];
+        }
+        const bool o_ready = ptx::named_barrier_and(kSoftmaxBarrier, kSoftmaxThreads,
+                                                    ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull));
+        if (o_ready && g == 0) {
+            // O^T lanes are output columns: the four warps of group 0 cover all 128.
+            ptx::tc_fence_after();
+            uint32_t o[kSwapNQ];
+            ptx::tmem_ld_32x32b_x16(tmem + lane_addr + kSwapTmemO, o);
+            ptx::tmem_ld_wait16(o);
+            const int c = q4 * 32 + lane;  // output column
+            const int mq = p.M < kSwapNQ ? p.M : kSwapNQ;
+#pragma unroll
+            for (int q = 0; q < kSwapNQ; ++q) {
+                if (q < mq) {
+                    float l = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kSoftmaxWarps; ++w)
+                        l += l_red[w * kSwapNQ + q];
+                    if (p.n_split == 1) {
+                        p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(__fdiv_rn(__uint_as_float(o[q]), l));
+                    } else {
+                        const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + q;
+                        p.ws_o[r * D + c] = __uint_as_float(o[q]);
+                        if (c == 0)
+                            p.ws_l[r] = l;
+                    }
+                }
+            }
+        }
+    }
+
+    // Teardown: every tensor-memory access of the CTA is ordered before the free.
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kSwapTmemCols);
+    }
+}
+
+}  // namespace mg

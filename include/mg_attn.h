@@ -101,6 +101,13 @@ typedef enum {
                                       sums in a fixed order. Opt-in: measured on GB300 it is not faster than
                                       the default split schedule on the decode shapes; see info.schedule */
 #define MG_FLAG_NO_STREAM_K 0x100  /* the split schedule (N split n_split ways per row tile; the default) */
+#define MG_FLAG_SWAP_AB 0x200      /* few-row specialisation (the graph as written, head dim 128, at most 16
+                                      query rows per batch, the split schedule): per K/V tile the products run
+                                      transposed, S^T = K^T Q^T and O^T += V^T P^T, so the MMA's 128 rows are
+                                      keys (resp. output columns) instead of mostly-empty query rows; split
+                                      partials always go to the second kernel. The default where it applies
+                                      (this flag only states it); see info.swap_ab */
+#define MG_FLAG_NO_SWAP_AB 0x400   /* never use the few-row specialisation (the one-tile kernel instead) */
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and
                                       the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */
@@ -138,7 +145,7 @@ typedef struct {
     int32_t schedule;        /* 0: split (CTA j of a row tile takes column tiles j, j + n_split, ...);
                                 1: stream-K (grid_ctas CTAs share the m_tiles x n_tiles units in equal
                                 contiguous runs; n_split is then the second kernel's partials per row) */
-    int32_t reserved1;
+    int32_t swap_ab;         /* 1: the few-row specialisation (transposed products, MG_FLAG_SWAP_AB) */
 } mg_attn_plan_info;
 
 /*

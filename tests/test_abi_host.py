@@ -101,8 +101,8 @@ def test_query_decisions(B, M, N, d):
         assert info["grid_ctas"] <= 152  # one wave
     cluster = info["cluster_ctas"]
     assert cluster in (0, info["n_split"]) and cluster <= 16
-    if 2 <= info["n_split"] <= 16:
-        assert cluster == info["n_split"]  # small splits combine on chip
+    if 2 <= info["n_split"] <= 16 and not info["swap_ab"]:
+        assert cluster == info["n_split"]  # small splits combine on chip (the few-row kernel: second kernel)
     assert info["kernels_per_run"] == (2 if info["n_split"] > 1 and cluster == 0 else 1)
     assert info["smem_bytes"] <= 232448
     # Every column tile belongs to exactly one split, every split has one (n_split <= n_tiles),
@@ -186,6 +186,23 @@ def test_query_stream_k_choices():
         mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_STREAM_K | mg.MG_FLAG_NO_STREAM_K)
 
 
+def test_query_swap_ab():
+    info = mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_SWAP_AB)
+    assert info["swap_ab"] == 1 and info["cluster_ctas"] == 0 and info["schedule"] == 0
+    assert info["kernels_per_run"] == (2 if info["n_split"] > 1 else 1)
+    assert info["smem_bytes"] < mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_NO_SWAP_AB)["smem_bytes"]
+    # The default where it applies: head dim 128, at most 16 rows, the graph as written.
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152)["swap_ab"] == 1
+    assert mg.mg_attn_query(64, 1, 4096, 128, 152)["swap_ab"] == 1
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_NO_SWAP_AB)["swap_ab"] == 0
+    assert mg.mg_attn_query(16, 8, 32768, 64, 152, flags=mg.MG_FLAG_SWAP_AB)["swap_ab"] == 0
+    assert mg.mg_attn_query(16, 17, 32768, 128, 152, flags=mg.MG_FLAG_SWAP_AB)["swap_ab"] == 0
+    flags = mg.MG_FLAG_SWAP_AB | mg.MG_FLAG_SAFE_SOFTMAX
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152, flags=flags)["swap_ab"] == 0
+    with pytest.raises(mg.MgAttnError):
+        mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_SWAP_AB | mg.MG_FLAG_NO_SWAP_AB)
+
+
 def test_query_cluster_choices():
     # The GQA tutorial shape takes a 16-CTA cluster (2 column tiles per CTA) instead of 32 splits.
     assert mg.mg_attn_query(2, 256, 4096, 64, 152)["cluster_ctas"] == 16
@@ -246,8 +263,8 @@ def test_query_options():
     ((2, 256, 4100, 64), {}, mg.MG_ERR_LAYOUT),
     ((2, 256, 4096, 64), {"n_split": 33}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 64), {"flags": 0x200}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 64), {"flags": 0x400}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x800}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x1000}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),

@@ -255,6 +255,36 @@ def test_stream_k_matches_split_schedule():
     assert_parity(O_sp, ref, "split")
 
 
+SWAP_SHAPES = [  # (B, M, N, d, n_split): the few-row specialisation forced (MG_FLAG_SWAP_AB)
+    (16, 8, 32768, 128, 0),    # decode-like, the second kernel
+    (64, 1, 4096, 128, 0),     # the launch example's shapes
+    (3, 16, 1032, 128, 1),     # 16 rows, one split: O written directly; ragged N
+    (5, 3, 5000, 128, 7),      # 3 rows; ragged N; 7 splits
+    (2, 1, 8, 128, 0),         # one query row, one ragged column tile
+]
+
+
+@pytest.mark.parametrize("B,M,N,d,n_split", SWAP_SHAPES)
+def test_swap_ab_specialisation(B, M, N, d, n_split):
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.25, seed=B * 7 + M + N)
+    ref = oracle.attention(q, k, v)
+    O, plan = run_gpu(q, k, v, n_split=n_split, flags=mg.MG_FLAG_SWAP_AB)
+    assert plan.info["swap_ab"] == 1
+    assert_parity(O, ref, f"swap-AB {B, M, N, d} n_split={plan.info['n_split']}")
+
+
+def test_swap_ab_matches_one_tile_kernel_and_is_reproducible():
+    q, k, v, _ = inputs.make_config("decode")
+    ref = oracle.attention(q, k, v)
+    O1, _ = run_gpu(q, k, v, flags=mg.MG_FLAG_SWAP_AB)
+    O2, _ = run_gpu(q, k, v, flags=mg.MG_FLAG_SWAP_AB)
+    O3, p3 = run_gpu(q, k, v, flags=mg.MG_FLAG_NO_SWAP_AB)
+    assert p3.info["swap_ab"] == 0
+    assert torch.equal(O1, O2)
+    assert_parity(O1, ref, "swap-AB")
+    assert_parity(O3, ref, "one-tile")
+
+
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
     # Scores 0 everywhere -> every weight is exp(0)=1: any column past N that leaked into the row
     # sum (zero-filled K gives exp(0)=1 too) would pull the mean toward 0.
