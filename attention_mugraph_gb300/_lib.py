@@ -35,6 +35,7 @@ MG_FLAG_STREAM_K = 0x80
 MG_FLAG_NO_STREAM_K = 0x100
 MG_FLAG_SWAP_AB = 0x200
 MG_FLAG_NO_SWAP_AB = 0x400
+MG_FLAG_PUSH_COMBINE = 0x800
 MG_QKNORM_EPS = 1e-6
 
 # Every function include/mg_attn.h declares.
@@ -57,7 +58,8 @@ class MgAttnPlanInfo(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("grid_ctas", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("tmem_cols", ctypes.c_int32), ("kernels_per_run", ctypes.c_int32), ("num_sms", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("cluster_ctas", ctypes.c_int32),
-                ("q_tiles_per_cta", ctypes.c_int32), ("schedule", ctypes.c_int32), ("swap_ab", ctypes.c_int32)]
+                ("q_tiles_per_cta", ctypes.c_int32), ("schedule", ctypes.c_int32), ("swap_ab", ctypes.c_int32),
+                ("xchg_push", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -50,6 +50,9 @@ constexpr int64_t kMaxDim = int64_t(1) << 30;
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
 constexpr int64_t kMaxCluster = mg::kMaxClusterRanks;  // largest thread-block cluster (non-portable size)
+// Deepest d = 64 K/V ring beside the pushed combine's receive area (227 KB of shared memory).
+constexpr int kPushMaxStages = 5;
+static_assert(mg::fwd_smem_bytes(64, kPushMaxStages, true) <= 232448u, "pushed combine exceeds shared memory");
 
 // The driver's tensor-map encoder, fetched through the runtime so that no libcuda link is needed.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -196,7 +199,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     if (o.reserved != 0 ||
         (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX |
                      MG_FLAG_QK_NORM | MG_FLAG_Q_PAIRS | MG_FLAG_NO_Q_PAIRS | MG_FLAG_STREAM_K |
-                     MG_FLAG_NO_STREAM_K | MG_FLAG_SWAP_AB | MG_FLAG_NO_SWAP_AB)) != 0)
+                     MG_FLAG_NO_STREAM_K | MG_FLAG_SWAP_AB | MG_FLAG_NO_SWAP_AB | MG_FLAG_PUSH_COMBINE)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -291,9 +294,22 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     int stages = o.stages == 0 ? auto_stages(d) : o.stages;
     if (stages < 2 || stages > 6)
         return fail(MG_ERR_CONFIG, "stages=%d out of range [2, 6]", stages);
+    // The pushed on-chip combine applies to the graph as written at head dim 64 (its receive area
+    // takes the place of one K/V stage; d = 128 has no room for it) unless an explicit depth leaves
+    // no room, and only on request: measured on GB300 it is slower than the pulled form, us per
+    // call (2, 256, 4096, 64) 7.34 against 6.72, (2, 64, 1024, 64) 5.94 against 5.45,
+    // (16, 256, 4096, 64) 11.26 against 10.12 (the pulled form at 5 stages: 6.73, 5.41, 10.28).
+    bool push = cluster && !pair && d == 64 && !(o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) &&
+                (o.flags & MG_FLAG_PUSH_COMBINE);
+    if (push && stages > kPushMaxStages) {
+        if (o.stages == 0)
+            stages = kPushMaxStages;
+        else
+            push = false;
+    }
     const uint32_t smem = pair   ? mg::pair_smem_bytes(stages)
                           : swap ? mg::swap_smem_bytes(stages)
-                                 : mg::fwd_smem_bytes(static_cast<int>(d), stages);
+                                 : mg::fwd_smem_bytes(static_cast<int>(d), stages, push);
     if (static_cast<int64_t>(smem) > max_smem ||
         !(pair ? pair_kernel(stages)
                : swap ? swap_kernel(stages) : stream_k ? sk_kernel(d, stages) : fwd_kernel(d, stages, o.flags)))
@@ -334,6 +350,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     info->q_tiles_per_cta = pair ? 2 : 1;
     info->schedule = stream_k ? 1 : 0;
     info->swap_ab = swap ? 1 : 0;
+    info->xchg_push = push ? 1 : 0;
     if (timeout_ns)
         *timeout_ns = o.timeout_ns ? static_cast<unsigned long long>(o.timeout_ns) : kDefaultTimeoutNs;
     if (flags)
@@ -705,6 +722,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
     prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
+    prm.push_combine = in.cluster_ctas > 0 && in.xchg_push ? 1 : 0;
     prm.O = static_cast<__half *>(O);
     prm.ws_o = plan->ws_o;
     prm.ws_l = plan->ws_l;
@@ -955,6 +973,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
     prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
+    prm.push_combine = in.cluster_ctas > 0 && in.xchg_push ? 1 : 0;
     prm.O = static_cast<__half *>(O);
     prm.status = reinterpret_cast<int *>(sd->scratch);
     prm.ws_o = ws_o;

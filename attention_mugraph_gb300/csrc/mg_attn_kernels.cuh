@@ -56,6 +56,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
@@ -97,15 +98,25 @@ struct TileCfg {
     // P buffers: as many as tensor memory holds after S (2 x 128 columns) and O (d columns).
     static constexpr int kPBuffers = D == 64 ? 3 : 2;
     static_assert(kTmemP + 64 * kPBuffers <= kTmemCols, "tensor memory overflow");
+    // On-chip combine staging, per row: fp16 x = O_j / l_j and its remainders (d + 8 halves each,
+    // the pad keeping 8 consecutive rows on distinct banks), then kLmw floats: the row sum once per
+    // 32-column slice (its sign bit says whether that slice's remainders are staged), the row
+    // maximum, padding to 16 bytes.
+    static constexpr int kRowHalves = D + 8;
+    static constexpr int kLmw = D == 64 ? 4 : 8;
+    // Receive area of the pushed exchange: a slot of ceil(128 / n) rows for each of the n ranks
+    // (at most 140 rows in all for n <= 16), each row as staged.
+    static constexpr uint32_t kRecvRows = 144;
+    static constexpr uint32_t kRecvBytes = kRecvRows * (2u * kRowHalves * 2 + kLmw * 4);
 };
 
 // Shared-memory bytes of kernel 1 for a head dim and pipeline depth: alignment slack, Q, the
-// K/V ring (its first stage is reused as the output staging area), the row-sum exchange of the
-// two softmax groups and the barriers.
-__host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages)
+// K/V ring (its first stages are reused as the output staging area), the receive area of the
+// pushed exchange (only with it), the row-sum exchange of the two softmax groups and the barriers.
+__host__ __device__ constexpr uint32_t fwd_smem_bytes(int d, int stages, bool push = false)
 {
     return 1024u + static_cast<uint32_t>(128 * d * 2) + static_cast<uint32_t>(stages) * (2u * d * 128 * 2) +
-           2u * 128 * 4 + 512u;
+           (push ? (d == 64 ? TileCfg<64>::kRecvBytes : TileCfg<128>::kRecvBytes) : 0u) + 2u * 128 * 4 + 512u;
 }
 
 struct FwdParams {
@@ -114,6 +125,7 @@ struct FwdParams {
     int n_tiles;             // ceil(N / 128)
     int n_split;
     int cluster_reduce;      // the n_split CTAs of a row tile form a cluster and combine on chip
+    int push_combine;        // on-chip combine by bulk copies into each owner's receive area
     __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
     float *ws_o;             // (n_split, B, M, d) partial numerators (the cluster combine's plain stores)
     float *ws_l;             // (n_split, B, M) partial row sums
@@ -143,8 +155,10 @@ struct Bars {
     static constexpr int kDrain = kOFull + 1;      // unwinding: the S warp's MMAs
     static constexpr int kDrainPv = kDrain + 1;    // unwinding: the P.V warp's MMAs
     static constexpr int kNever = kDrainPv + 1;
-    static constexpr int kCount = kNever + 1;
-    static_assert(kCount * 8 + 8 <= 512, "barrier area overflow");
+    static constexpr int kXRecv = kNever + 1;      // pushed exchange: every rank's rows have landed here
+    static constexpr int kCount = kXRecv + 1;
+    // + the tensor-memory address, the abort flag and 16 per-owner remainder flags
+    static_assert(kCount * 8 + 8 + 64 <= 512, "barrier area overflow");
 };
 
 struct WaitCtx {
@@ -348,17 +362,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     using BI = Bars<STAGES, kPBuffers>;
     static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
-    static_assert(2 * 128 * (D + 8) * 2 + (D / 32 + 1) * 128 * 4 <= STAGES * C::kStageBytes,
+    static_assert(2 * 128 * C::kRowHalves * 2 + 128 * C::kLmw * 4 <= STAGES * C::kStageBytes,
                   "on-chip combine staging must fit in the K/V ring");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = ptx::smem_u32(smem);
     const uint32_t sStage0 = sQ + C::kQBytes;
-    float *l_xchg = reinterpret_cast<float *>(smem + C::kQBytes + STAGES * C::kStageBytes);
+    uint8_t *recv = smem + C::kQBytes + STAGES * C::kStageBytes;
+    float *l_xchg = reinterpret_cast<float *>(recv + (p.push_combine ? C::kRecvBytes : 0u));
     uint64_t *bars = reinterpret_cast<uint64_t *>(l_xchg + 2 * kBlockM);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    // Pushed exchange: whether owner o gets remainders from this CTA (written 1 by any thread that
+    // staged one of o's rows with remainders).
+    volatile uint32_t *lo_need = reinterpret_cast<volatile uint32_t *>(tmem_holder + 2);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
 
     const int warp = threadIdx.x >> 5;
@@ -414,7 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(BI::kDrain), 1);
         ptx::mbar_init(bar(BI::kDrainPv), 1);
         ptx::mbar_init(bar(BI::kNever), 1);
+        // One arrival per rank of the cluster (its expected bytes, then its copies land).
+        ptx::mbar_init(bar(BI::kXRecv), p.n_split);
         *abort_flag = 0;
+        for (int o = 0; o < kMaxClusterRanks; ++o)
+            lo_need[o] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -434,12 +456,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // Pushed exchange: the first half of a cluster barrier whose wait, just before the first copy
+    // to another CTA, says that every CTA's receive barrier is initialised.
+    if (VAR == kPlain && p.cluster_reduce && p.push_combine)
+        ptx::cluster_arrive_release();
 
     // Everything above touched only on-chip state; global memory waits for the previous grid.
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
 
     const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+    bool staged_ok = false;  // softmax warps: this CTA staged its output (its O was complete)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
@@ -969,6 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool o_ready = ptx::named_barrier_and(kSoftmaxBarrier, kSoftmaxThreads,
                                                     ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull));
         const float l = l_xchg[row] + l_xchg[kBlockM + row];
+        staged_ok = o_ready;
         if (o_ready) {
             ptx::tc_fence_after();
             // The K/V ring is idle (every PV has completed): stage this CTA's output there. For the
@@ -976,13 +1004,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the pad keeps 8 consecutive rows on distinct banks); for a 32-column slice of a row
             // with any |x| >= kHiOnlyBelow also the remainders x - fp16(x), in the same layout;
             // then the fp32 row sum l_j once per slice (each copy carries, in its sign bit, whether
-            // that slice's remainders are staged; l_j >= 0) and the row maxima m_j, read by the
-            // cluster's CTAs after the cluster barrier. Otherwise the 128-byte-swizzled layout the
-            // output tensor maps expect, then a TMA store.
+            // that slice's remainders are staged; l_j >= 0) and the row maximum m_j, kLmw floats per
+            // row, read by the cluster's CTAs after the cluster barrier or copied into their receive
+            // areas. Otherwise the 128-byte-swizzled layout the output tensor maps expect, then a
+            // TMA store.
             const uint32_t stage = sStage0;
             __half *stage_hi = reinterpret_cast<__half *>(smem + C::kQBytes);
-            __half *stage_lo = stage_hi + kBlockM * (D + 8);
-            float *stage_lm = reinterpret_cast<float *>(stage_lo + kBlockM * (D + 8));  // [D/32 + 1][128]
+            __half *stage_lo = stage_hi + kBlockM * C::kRowHalves;
+            float *stage_lm = reinterpret_cast<float *>(stage_lo + kBlockM * C::kRowHalves);  // [128][kLmw]
             if (warp_rows) {
 #pragma unroll
                 for (int c = 0; c < C::kHalfCols / 32; ++c) {
@@ -994,8 +1023,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // One correctly rounded reciprocal, then products (l = 0 only if every
                         // exponential of the split underflowed; its partial is then 0).
                         const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
-                        uint4 *dhi = reinterpret_cast<uint4 *>(stage_hi + row * (D + 8) + col);
-                        uint4 *dlo = reinterpret_cast<uint4 *>(stage_lo + row * (D + 8) + col);
+                        uint4 *dhi = reinterpret_cast<uint4 *>(stage_hi + row * C::kRowHalves + col);
+                        uint4 *dlo = reinterpret_cast<uint4 *>(stage_lo + row * C::kRowHalves + col);
                         bool wide = false;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -1026,22 +1055,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 dlo[q] = make_uint4(l4[0], l4[1], l4[2], l4[3]);
                             }
                         }
-                        stage_lm[(col / 32) * kBlockM + row] = wide ? -l : l;  // -0.0 when l = 0
+                        stage_lm[row * C::kLmw + col / 32] = wide ? -l : l;  // -0.0 when l = 0
+                        if (wide)  // its owner (rank o holds rows [128 o / n, 128 (o + 1) / n))
+                            lo_need[(row * p.n_split + p.n_split - 1) / kBlockM] = 1u;
                     } else if (p.n_split == 1) {
                         // fp16 O/l: chunk col/64 of a {64, 128} fp16 box; this slice is units (col%64)/8 .. +3.
+                        // One correctly rounded reciprocal, then products: within 1.5 fp32 ulps of
+                        // the quotient, far below the fp16 rounding that follows (0 and inf give
+                        // the quotient's NaN / 0 as well). Measured on GB300: 32 IEEE divisions per
+                        // thread took ~1 us of a one-tile call's epilogue.
+                        const float inv = __frcp_rn(l);
                         const uint32_t chunk = stage + (col / 64) * C::kChunkRows128;
                         const uint32_t u0 = static_cast<uint32_t>((col % 64) / 8);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             ptx::st_shared_v4(chunk + sw128_offset(row, u0 + q),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 0]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 1]), l)),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 2]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 3]), l)),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 4]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 5]), l)),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 6]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 7]), l)));
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 0]) * inv,
+                                                              __uint_as_float(r[8 * q + 1]) * inv),
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 2]) * inv,
+                                                              __uint_as_float(r[8 * q + 3]) * inv),
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 4]) * inv,
+                                                              __uint_as_float(r[8 * q + 5]) * inv),
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 6]) * inv,
+                                                              __uint_as_float(r[8 * q + 7]) * inv));
                     } else {
                         // fp32 partial: chunk col/32 of {32, 128} fp32 boxes; this slice fills units 0..7.
                         const uint32_t chunk = stage + (col / 32) * C::kChunkRows128;
@@ -1054,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (p.cluster_reduce) {
                 if (g == 0)
-                    stage_lm[(D / 32) * kBlockM + row] = m;
+                    stage_lm[row * C::kLmw + D / 32] = m;
             } else if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
                 const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
                 p.ws_l[r] = l;
@@ -1082,32 +1118,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }  // !kSK
     }
 
-    // On-chip combine of the split partials: after the first cluster barrier every CTA's staged
-    // (O_j / l_j, remainders, l_j, m_j) is visible; CTA rank j forms rows [128 j / n, 128 (j+1) / n)
-    // of its row tile as sum_r c_r x_r / sum_r c_r with c_r = l_r (times exp(m_r - max m) in the
-    // max-subtracted variant), x_r = the fp16 value plus, where rank r flagged the half-row, its
-    // fp16 remainder, over all n ranks in rank order (reproducible), and writes fp16 O. The second
-    // barrier keeps each CTA's shared memory alive until the others have read it. Every thread of
-    // every CTA reaches both barriers, on the unwinding path too.
+    // On-chip combine of the split partials. CTA rank j forms rows [128 j / n, 128 (j+1) / n) of
+    // its row tile as sum_r c_r x_r / sum_r c_r with c_r = l_r (times exp(m_r - max m) in the
+    // max-subtracted variant), x_r = the fp16 value plus, where rank r flagged the slice, its fp16
+    // remainder, over all n ranks in rank order (reproducible), and writes fp16 O. The staged rows
+    // reach their owner in one of two ways:
+    //  * pulled: after a cluster barrier every owner reads its rows out of the n CTAs' staging
+    //    (distributed shared memory), and a second barrier keeps each CTA's shared memory alive
+    //    until the others have read it;
+    //  * pushed (on request): as soon as a CTA has staged, one thread per owner copies that
+    //    owner's rows into the owner's receive area (bulk copies counted on the owner's receive
+    //    barrier), so an owner waits for its own rows only, not for a cluster-wide barrier, and
+    //    reads them locally. A closing cluster barrier, which each CTA reaches only once the copies
+    //    into it have landed, keeps every CTA's staging alive until its copies are done. Measured
+    //    on GB300 the pulled form is faster (0.5-1.1 us per call): the copies between CTAs take
+    //    longer than the owners' loads, and the early start does not make up for it.
+    // Every thread of every CTA reaches every cluster barrier, on the unwinding path too.
     __syncwarp();
     if (p.cluster_reduce) {
-        ptx::cluster_sync();
-        if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
+        const bool softmax_warp = warp >= 2 && warp < 2 + kSoftmaxWarps;
+        const int n = p.n_split;
+        const int lo_row = j * kBlockM / n;
+        const int hi_row = (j + 1) * kBlockM / n;
+        const int R = (kBlockM + n - 1) / n;  // rows of a receive slot
+        const uint32_t sh = ptx::smem_u32(smem + C::kQBytes);  // staged x: [128][kRowHalves] fp16
+        const uint32_t sl = sh + kBlockM * C::kRowHalves * 2;  // staged remainders, same layout
+        const uint32_t slm = sl + kBlockM * C::kRowHalves * 2; // staged row sums, maxima: [128][kLmw]
+        const uint32_t rh = ptx::smem_u32(recv);                  // received x: [kRecvRows][kRowHalves]
+        const uint32_t rl = rh + C::kRecvRows * C::kRowHalves * 2;  // received remainders
+        const uint32_t rlm = rl + C::kRecvRows * C::kRowHalves * 2; // received [kRecvRows][kLmw]
+
+        // One owner's rows from every rank; kPush: out of the receive area (slot r, row i at
+        // r * R + i), else out of each rank's staging.
+        auto combine = [&](auto push_tag) {
+            constexpr bool kPush = decltype(push_tag)::value;
             constexpr int G = D / 8;  // 16-byte groups (8 fp16 columns) per row
-            const int n = p.n_split;
-            const int lo_row = j * kBlockM / n;
-            const int hi_row = (j + 1) * kBlockM / n;
-            const uint32_t sh = ptx::smem_u32(smem + C::kQBytes);
-            const uint32_t sl = sh + kBlockM * (D + 8) * 2;
-            const uint32_t ls = sl + kBlockM * (D + 8) * 2;  // l per 32-column slice: [D / 32][128]
-            const uint32_t ms = ls + (D / 32) * kBlockM * 4;
+            auto ld4 = [&](uint32_t local, int r) {
+                return kPush ? ptx::ld_shared_v4(local) : ptx::ld_cluster_v4(ptx::map_to_rank(local, r));
+            };
+            auto ld1 = [&](uint32_t local, int r) {
+                return kPush ? ptx::ld_shared_f32(local) : ptx::ld_cluster_f32(ptx::map_to_rank(local, r));
+            };
             for (int it = threadIdx.x - 64; it < (hi_row - lo_row) * G; it += kSoftmaxThreads) {
                 const int rr = lo_row + it / G;
                 const int gq = it % G;
                 if (m0 + rr >= p.M)
                     continue;
-                const uint32_t off = static_cast<uint32_t>((rr * (D + 8) + gq * 8) * 2);
-                const uint32_t lrow = ls + static_cast<uint32_t>(((gq * 8) / 32) * kBlockM + rr) * 4;
+                // Rank r's copy of row rr: its index in the staging (pulled) or the receive area.
+                auto row_of = [&](int r) { return static_cast<uint32_t>(kPush ? r * R + (rr - lo_row) : rr); };
+                const uint32_t xh = kPush ? rh : sh;
+                const uint32_t xl = kPush ? rl : sl;
+                const uint32_t xlm = kPush ? rlm : slm;
+                const uint32_t col_off = static_cast<uint32_t>(gq * 8 * 2);
+                const uint32_t slice = static_cast<uint32_t>((gq * 8) / 32);
                 // Max-subtracted variant: every rank's row maximum first, then the weights
                 // exp(m_r - max m) (measured faster than requesting them with the values: fewer
                 // registers live at once).
@@ -1121,7 +1184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int r = 0; r < kMaxClusterRanks; ++r) {
                         if (r < n) {
-                            mr[r] = ptx::ld_cluster_f32(ptx::map_to_rank(ms + rr * 4, r));
+                            mr[r] = ld1(xlm + (row_of(r) * C::kLmw + D / 32) * 4, r);
                             mmax = fmaxf(mmax, mr[r]);
                         }
                     }
@@ -1131,14 +1194,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             wt[r] = ptx::ex2_approx((mr[r] - mmax) * ptx::kLog2e);
                 }
                 // Every rank's values and row sums are requested before the first is used: the
-                // remote reads are in flight together rather than one round trip after another.
+                // loads are in flight together rather than one round trip after another.
                 float4 v[kMaxClusterRanks];
                 float c[kMaxClusterRanks];
 #pragma unroll
                 for (int r = 0; r < kMaxClusterRanks; ++r) {
                     if (r < n) {
-                        v[r] = ptx::ld_cluster_v4(ptx::map_to_rank(sh + off, r));
-                        c[r] = ptx::ld_cluster_f32(ptx::map_to_rank(lrow, r));
+                        v[r] = ld4(xh + row_of(r) * C::kRowHalves * 2 + col_off, r);
+                        c[r] = ld1(xlm + (row_of(r) * C::kLmw + slice) * 4, r);
                     }
                 }
                 uint32_t flags = 0;  // ranks that staged remainders for this slice of the row
@@ -1169,27 +1232,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (flags) {
-                    // Remainders of the flagged ranks: one more round of remote reads, all in flight.
+                    // Remainders of the flagged ranks: one more round of loads, all in flight.
 #pragma unroll
                     for (int r = 0; r < kMaxClusterRanks; ++r)
                         if (r < n && ((flags >> r) & 1u))
-                            v[r] = ptx::ld_cluster_v4(ptx::map_to_rank(sl + off, r));
+                            v[r] = ld4(xl + row_of(r) * C::kRowHalves * 2 + col_off, r);
 #pragma unroll
                     for (int r = 0; r < kMaxClusterRanks; ++r)
                         if (r < n && ((flags >> r) & 1u))
                             add_halves(v[r], c[r]);
                 }
+                const float inv = __frcp_rn(lsum);  // reciprocal, then products (as in the staging)
                 uint4 w;
-                w.x = ptx::pack_half2(__fdiv_rn(a[0], lsum), __fdiv_rn(a[1], lsum));
-                w.y = ptx::pack_half2(__fdiv_rn(a[2], lsum), __fdiv_rn(a[3], lsum));
-                w.z = ptx::pack_half2(__fdiv_rn(a[4], lsum), __fdiv_rn(a[5], lsum));
-                w.w = ptx::pack_half2(__fdiv_rn(a[6], lsum), __fdiv_rn(a[7], lsum));
+                w.x = ptx::pack_half2(a[0] * inv, a[1] * inv);
+                w.y = ptx::pack_half2(a[2] * inv, a[3] * inv);
+                w.z = ptx::pack_half2(a[4] * inv, a[5] * inv);
+                w.w = ptx::pack_half2(a[6] * inv, a[7] * inv);
                 *reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + gq * 8) = w;
             }
+        };
+
+        // The pushed form serves the graph as written (the host plans it only there): in the two-pass
+        // variants a second copy of the combine loop would push the main loop's registers to spills.
+        if (VAR == kPlain && p.push_combine) {
+            ptx::cluster_wait_acquire();  // every CTA's receive barrier is initialised
+            if (softmax_warp) {
+                ptx::fence_proxy_async_smem();  // this thread's staging writes, before the copies read them
+                ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
+                const int t = threadIdx.x - 64;
+                if (t < n) {
+                    // Thread t sends owner t its rows: x, the row sums and maxima, and the
+                    // remainders when any of those rows has some. A CTA that unwound sends only
+                    // its arrival, so that no owner waits for it in vain.
+                    const int o = t;
+                    const int o_lo = o * kBlockM / n;
+                    const uint32_t rows = static_cast<uint32_t>((o + 1) * kBlockM / n - o_lo);
+                    const bool lo = lo_need[o] != 0u;
+                    const uint32_t x_bytes = rows * C::kRowHalves * 2;
+                    const uint32_t lm_bytes = rows * C::kLmw * 4;
+                    const uint32_t rbar = ptx::map_to_rank(bar(BI::kXRecv), static_cast<uint32_t>(o));
+                    if (staged_ok) {
+                        const uint32_t slot = static_cast<uint32_t>(j * R);
+                        ptx::mbar_arrive_expect_tx_cluster(rbar, x_bytes + lm_bytes + (lo ? x_bytes : 0u));
+                        ptx::bulk_copy_to_cluster(ptx::map_to_rank(rh + slot * C::kRowHalves * 2, o),
+                                                  sh + o_lo * C::kRowHalves * 2, x_bytes, rbar);
+                        ptx::bulk_copy_to_cluster(ptx::map_to_rank(rlm + slot * C::kLmw * 4, o),
+                                                  slm + o_lo * C::kLmw * 4, lm_bytes, rbar);
+                        if (lo)
+                            ptx::bulk_copy_to_cluster(ptx::map_to_rank(rl + slot * C::kRowHalves * 2, o),
+                                                      sl + o_lo * C::kRowHalves * 2, x_bytes, rbar);
+                    } else {
+                        ptx::mbar_arrive_expect_tx_cluster(rbar, 0u);
+                    }
+                }
+                // (A CTA that is unwinding does not wait here; wait_bounded returns at once.)
+                if (wait_bounded(wc, bar(BI::kXRecv), 0, BI::kXRecv)) {
+                    if constexpr (VAR == kPlain)
+                        combine(std::true_type{});
+                } else {
+                    // Even so, the copies on their way in land before this CTA passes the closing
+                    // barrier (after which their senders may release the staging they read): every
+                    // rank issued its copies and arrivals before any wait of its own.
+                    wait_drain(bar(BI::kXRecv), 0, p.timeout_ns);
+                }
+            }
+            ptx::cluster_sync_relaxed();
+        } else {
+            ptx::cluster_sync();  // every CTA's staging is visible
+            if (softmax_warp)
+                combine(std::false_type{});
+            // Only "every CTA has finished reading the others' shared memory" is needed here; a
+            // release would also hold each CTA until its output stores had drained.
+            ptx::cluster_sync_relaxed();
         }
-        // Only "every CTA has finished reading the others' shared memory" is needed here; a
-        // release would also hold each CTA until its output stores had drained.
-        ptx::cluster_sync_relaxed();
     }
 
     // Teardown: every tensor-memory access of the CTA is ordered before the free.

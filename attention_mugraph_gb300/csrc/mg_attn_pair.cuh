@@ -137,7 +137,8 @@ __device__ __forceinline__ void cluster_combine_rows(const FwdParams &p, int b, 
                 const float lother = __shfl_xor_sync(pair_mask, lsum, 1);
                 lsum = h == 0 ? lsum + lother : lother + lsum;
                 const int rr = lo + e % R;
-                const uint32_t o = ptx::pack_half2(__fdiv_rn(a[2 * h], lsum), __fdiv_rn(a[2 * h + 1], lsum));
+                const float inv = __frcp_rn(lsum);
+                const uint32_t o = ptx::pack_half2(a[2 * h] * inv, a[2 * h + 1] * inv);
                 *reinterpret_cast<uint32_t *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + (e / R) * 4 +
                                               2 * h) = o;
             }
@@ -484,17 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else if (p.n_split == 1) {
                         const uint32_t chunk = stage + g * (kBlockM * D * 2);
                         const uint32_t u0 = static_cast<uint32_t>(col / 8);
+                        const float inv = __frcp_rn(l);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             ptx::st_shared_v4(chunk + sw128_offset(row, u0 + q),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 0]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 1]), l)),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 2]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 3]), l)),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 4]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 5]), l)),
-                                              ptx::pack_half2(__fdiv_rn(__uint_as_float(r[8 * q + 6]), l),
-                                                              __fdiv_rn(__uint_as_float(r[8 * q + 7]), l)));
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 0]) * inv,
+                                                              __uint_as_float(r[8 * q + 1]) * inv),
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 2]) * inv,
+                                                              __uint_as_float(r[8 * q + 3]) * inv),
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 4]) * inv,
+                                                              __uint_as_float(r[8 * q + 5]) * inv),
+                                              ptx::pack_half2(__uint_as_float(r[8 * q + 6]) * inv,
+                                                              __uint_as_float(r[8 * q + 7]) * inv));
                     } else {
                         // fp32 partial: {32, 128} fp32 boxes; tile g's two boxes follow each other.
                         const uint32_t chunk = stage + g * (kBlockM * D * 4) + c * TileCfg<D>::kChunkRows128;

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int w = 0; w < kSoftmaxWarps; ++w)
                         l += l_red[w * kSwapNQ + q];
                     if (p.n_split == 1) {
-                        p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(__fdiv_rn(__uint_as_float(o[q]), l));
+                        p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(__uint_as_float(o[q]) * __frcp_rn(l));
                     } else {
                         const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + q;
                         p.ws_o[r * D + c] = __uint_as_float(o[q]);

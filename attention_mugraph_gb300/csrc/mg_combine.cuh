@@ -90,9 +90,10 @@ __global__ void __launch_bounds__(256)
             s.w += t.w;
             ls += part_l[q][rl];
         }
+        const float inv = __frcp_rn(ls);  // one reciprocal, then products
         uint2 w;
-        w.x = ptx::pack_half2(__fdiv_rn(s.x, ls), __fdiv_rn(s.y, ls));
-        w.y = ptx::pack_half2(__fdiv_rn(s.z, ls), __fdiv_rn(s.w, ls));
+        w.x = ptx::pack_half2(s.x * inv, s.y * inv);
+        w.y = ptx::pack_half2(s.z * inv, s.w * inv);
         *reinterpret_cast<uint2 *>(O + static_cast<size_t>(r) * D + g * 4) = w;
     }
 }
@@ -190,9 +191,10 @@ __global__ void __launch_bounds__(256, BATCH == 4 ? 4 : 3)
             s.w += wq * t.w;
             ls += wq * part_l[q][rl];
         }
+        const float inv = __frcp_rn(ls);  // one reciprocal, then products
         uint2 w;
-        w.x = ptx::pack_half2(__fdiv_rn(s.x, ls), __fdiv_rn(s.y, ls));
-        w.y = ptx::pack_half2(__fdiv_rn(s.z, ls), __fdiv_rn(s.w, ls));
+        w.x = ptx::pack_half2(s.x * inv, s.y * inv);
+        w.y = ptx::pack_half2(s.z * inv, s.w * inv);
         *reinterpret_cast<uint2 *>(O + static_cast<size_t>(r) * D + g * 4) = w;
     }
 }

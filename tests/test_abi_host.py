@@ -54,16 +54,18 @@ int main(void) {
   printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(mg_attn_plan_info), offsetof(mg_attn_plan_info, block_m),
          offsetof(mg_attn_plan_info, num_sms), offsetof(mg_attn_plan_info, workspace_bytes),
          offsetof(mg_attn_plan_info, cluster_ctas), offsetof(mg_attn_plan_info, schedule));
+  printf("%zu\\n", offsetof(mg_attn_plan_info, xchg_push));
   return 0;
 }
 """)
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
-    l1, l2 = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")[:2]
+    l1, l2, l3 = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")[:3]
     O, I = _lib.MgAttnOptions, _lib.MgAttnPlanInfo
     assert [int(x) for x in l1.split()] == [ctypes.sizeof(O), O.timeout_ns.offset, O.flags.offset]
     assert [int(x) for x in l2.split()] == [ctypes.sizeof(I), I.block_m.offset, I.num_sms.offset,
                                             I.workspace_bytes.offset, I.cluster_ctas.offset, I.schedule.offset]
+    assert int(l3) == I.xchg_push.offset
 
 
 def test_status_strings_and_version(lib):
@@ -256,6 +258,36 @@ def test_query_options():
     assert mg.mg_attn_query(2, 256, 4096, 64, 152)["stages"] == 6
 
 
+def fwd_smem(d, stages, push):
+    # Restated from the kernel's layout: alignment slack, Q, the ring, the pushed combine's receive
+    # area (144 rows of x, remainders and kLmw floats), the row-sum exchange, the barrier area.
+    lmw = 4 if d == 64 else 8
+    recv = 144 * (2 * (d + 8) * 2 + lmw * 4) if push else 0
+    return 1024 + 128 * d * 2 + stages * 2 * d * 128 * 2 + recv + 2 * 128 * 4 + 512
+
+
+def test_query_push_combine():
+    # On request, the graph as written at head dim 64 with an on-chip combine pushes each owner's
+    # rows into its receive area, which takes the place of one K/V stage; everything else pulls.
+    P = mg.MG_FLAG_PUSH_COMBINE
+    for shape in [(2, 256, 4096, 64), (2, 64, 1024, 64), (16, 256, 4096, 64), (1, 128, 2048, 64)]:
+        info = mg.mg_attn_query(*shape, 152, flags=P)
+        assert info["cluster_ctas"] > 0 and info["xchg_push"] == 1 and info["stages"] == 5
+        assert info["smem_bytes"] == fwd_smem(64, 5, True) <= 232448
+        pull = mg.mg_attn_query(*shape, 152)
+        assert pull["xchg_push"] == 0 and pull["stages"] == 6 and pull["smem_bytes"] == fwd_smem(64, 6, False)
+        assert pull["n_split"] == info["n_split"] and pull["cluster_ctas"] == info["cluster_ctas"]
+    q = dict(num_sms=152)
+    assert mg.mg_attn_query(2, 256, 4096, 64, stages=6, flags=P, **q)["xchg_push"] == 0  # no room at this depth
+    assert mg.mg_attn_query(2, 256, 4096, 64, stages=3, flags=P, **q)["xchg_push"] == 1
+    assert mg.mg_attn_query(2, 256, 4096, 64, stages=3, flags=P, **q)["stages"] == 3
+    for flags in (mg.MG_FLAG_SAFE_SOFTMAX, mg.MG_FLAG_QK_NORM, mg.MG_FLAG_NO_CLUSTER, mg.MG_FLAG_Q_PAIRS):
+        assert mg.mg_attn_query(2, 256, 4096, 64, flags=flags | P, **q)["xchg_push"] == 0
+    assert mg.mg_attn_query(2, 256, 4096, 128, flags=P, **q)["xchg_push"] == 0            # d = 128: no room
+    assert mg.mg_attn_query(2, 256, 65536, 64, flags=P, **q)["xchg_push"] == 0            # second kernel
+    assert mg.mg_attn_query(2, 256, 4096, 64, n_split=1, flags=P, **q)["xchg_push"] == 0  # nothing to combine
+
+
 @pytest.mark.parametrize("args,kw,code", [
     ((0, 256, 4096, 64), {}, mg.MG_ERR_INVALID_ARG),
     ((2, -1, 4096, 64), {}, mg.MG_ERR_INVALID_ARG),
@@ -263,7 +295,7 @@ def test_query_options():
     ((2, 256, 4100, 64), {}, mg.MG_ERR_LAYOUT),
     ((2, 256, 4096, 64), {"n_split": 33}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
-    ((2, 256, 4096, 64), {"flags": 0x800}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x2000}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x1000}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),

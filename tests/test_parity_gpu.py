@@ -182,6 +182,43 @@ def test_cluster_combine_mixed_slices(d):
     assert_parity(O, ref, f"mixed slices d={d}")
 
 
+PUSH_SHAPES = [  # (B, M, N, n_split, large V slices): head dim 64, cluster combine
+    (2, 256, 4096, 16, False),   # the GQA graph's own split
+    (1, 200, 2056, 3, True),     # ragged M and N; 3 owners of 42, 43, 43 rows
+    (3, 129, 1032, 8, False),    # the second row tile holds one row
+    (1, 384, 8192, 13, True),    # 13 owners of 9 or 10 rows
+    (2, 17, 1024, 2, True),      # one partial row tile
+    (1, 128, 3072, 7, False),    # 7 owners, 24 column tiles
+    (2, 64, 1024, 5, True),
+    (1, 256, 2048, 11, False),
+]
+
+
+@pytest.mark.parametrize("B,M,N,n_split,large", PUSH_SHAPES)
+def test_pushed_combine_matches_pulled_bit_for_bit(B, M, N, n_split, large):
+    # The pushed exchange (opt-in: each CTA copies every owner's rows into that owner's receive
+    # area) and the pulled one (owners read every CTA's staging) combine the same staged values in the same
+    # rank order, so their outputs agree bit for bit; both match the oracle. With large V slices,
+    # some rows carry fp16 remainders (pushed only to the owners of those rows).
+    d = 64
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.5, seed=n_split * 11 + M)
+    if large:
+        # Batch 0: slice 0 of V around 6, so every partial x there has |x| >= 4 (remainders);
+        # other slices and batches stay small (none).
+        v = v.float()
+        v[0, :, :32] = v[0, :, :32] * 0.5 + 6.0
+        v = v.half()
+    ref = oracle.attention(q, k, v)
+    O_push, plan = run_gpu(q, k, v, n_split=n_split, flags=mg.MG_FLAG_PUSH_COMBINE)
+    O_pull, plan2 = run_gpu(q, k, v, n_split=n_split)
+    assert plan.info["cluster_ctas"] == n_split and plan.info["xchg_push"] == 1
+    assert plan2.info["cluster_ctas"] == n_split and plan2.info["xchg_push"] == 0
+    assert_parity(O_push, ref, f"pushed, {n_split} ranks")
+    assert torch.equal(O_push, O_pull)
+    O_again, _ = run_gpu(q, k, v, n_split=n_split, flags=mg.MG_FLAG_PUSH_COMBINE)
+    assert torch.equal(O_push, O_again)
+
+
 PAIR_SHAPES = [  # (B, M, N, d, n_split, stages): the two-Q-tile kernel forced (MG_FLAG_Q_PAIRS)
     (1, 256, 1024, 64, 1, 0),      # one split: TMA store of both tiles
     (2, 200, 2056, 64, 0, 0),      # ragged M (tile 1 holds rows 128..199) and ragged N
@@ -411,11 +448,14 @@ def test_misaligned_pointer_rejected():
     assert e.value.status == mg.MG_ERR_LAYOUT
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("flags", [0, mg.MG_FLAG_PUSH_COMBINE, mg.MG_FLAG_NO_CLUSTER])
+def test_bounded_wait_reports_timeout_and_context_survives(flags):
     # The load warp waits on a barrier nothing arrives on (before issuing any copy); the wait
-    # runs out after 2 ms, every role unwinds, and the plan's sticky status says so.
+    # runs out after 2 ms, every role unwinds (with each on-chip exchange form, and without one),
+    # and the plan's sticky status says so.
     q, k, v, _ = inputs.make_config("tiny")
-    plan = mg.Plan(2, 64, 1024, 64, flags=mg.MG_FLAG_INJECT_TIMEOUT, timeout_ns=2_000_000)
+    plan = mg.Plan(2, 64, 1024, 64, flags=mg.MG_FLAG_INJECT_TIMEOUT | flags, timeout_ns=2_000_000)
+    assert plan.info["xchg_push"] == (1 if flags == mg.MG_FLAG_PUSH_COMBINE else 0)
     Q, K, V = q.cuda(), k.cuda(), v.cuda()
     O = torch.zeros((2, 64, 64), dtype=torch.float16, device="cuda")
     plan.run(Q, K, V, O)
