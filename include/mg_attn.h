@@ -198,7 +198,12 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
  * all enqueued on `stream`; the caller synchronises the stream before reading hO.
  * Page-locked host buffers that the device can address (cudaHostAlloc / pinned tensors,
  * 16-byte aligned) are read by a copy kernel through their device addresses, chained to the
- * attention kernels with programmatic dependent launch; when the plan splits N
+ * attention kernels with programmatic dependent launch. That kernel loads the inputs as soon as
+ * it starts, which can be while the previous kernels on `stream` still run (this library's
+ * kernels release their dependents early), and stores them into the staging only after those
+ * kernels end: so the inputs must hold their final values when the call is made, and no kernel
+ * enqueued before it may write them (O of an earlier call may: when hO shares bytes with an
+ * input, the loads wait for the earlier kernels). When the plan splits N
  * (info.n_split > 1) the kernels write O straight into such a host buffer, and otherwise a
  * second copy kernel writes it back. Other host memory (pageable) goes through cudaMemcpyAsync. The plan's device staging buffers (the size of
  * Q, K, V and O) are allocated by the first call on that plan and reused after, so one

@@ -422,6 +422,40 @@ def test_host_buffer_entry_point(kw):
         assert_parity(ho, ref, "run_host")
 
 
+@pytest.mark.parametrize("kw", [{}, {"n_split": 1}])
+def test_host_buffer_back_to_back_calls(kw):
+    # Calls enqueued back to back without synchronising: each call's copy kernel loads its pinned
+    # inputs while the previous call's kernels may still run (and stores them only after those
+    # end). Distinct inputs per call, each result checked; then calls chained in place (O of one
+    # call is Q of the next, one host buffer), where the loads must wait for the previous call.
+    B, M, N, d = 2, 64, 1024, 64
+    plan = mg.Plan(B, M, N, d, **kw)
+    sets = [inputs.make_inputs(B, M, N, d, 0.5, seed=40 + i) for i in range(4)]
+    pinned = [tuple(t.pin_memory() for t in s) for s in sets]
+    outs = [torch.full((B, M, d), float("nan"), dtype=torch.float16).pin_memory() for _ in sets]
+    for (hq, hk, hv), ho in zip(pinned, outs):
+        plan.run_host(hq, hk, hv, ho)
+    torch.cuda.synchronize()
+    for (q, k, v), ho in zip(sets, outs):
+        assert_parity(ho, oracle.attention(q, k, v), "back to back")
+    q, k, v = sets[0]
+    h = q.clone().pin_memory()
+    hk, hv = k.pin_memory(), v.pin_memory()
+    for _ in range(3):
+        plan.run_host(h, hk, hv, h)
+    torch.cuda.synchronize()
+    cur = q.clone()
+    for i in range(3):  # the same chain, one synchronised call at a time, separate buffers
+        o = torch.full((B, M, d), float("nan"), dtype=torch.float16).pin_memory()
+        hc = cur.pin_memory()
+        plan.run_host(hc, hk, hv, o)
+        torch.cuda.synchronize()
+        if i == 0:
+            assert_parity(o, oracle.attention(cur, k, v), "chain, first call")
+        cur = o.clone()
+    assert torch.equal(h, cur)
+
+
 def test_host_buffer_entry_point_pageable_and_large():
     # Pageable host tensors take the copy-engine path; pinned ones the mapped-copy kernels. Both
     # on a shape with a split combine and several copy rounds per thread.
