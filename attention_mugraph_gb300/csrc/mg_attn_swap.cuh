@@ -18,7 +18,8 @@
 // producer warp, an S-issuing warp, a P.V-issuing warp and two groups of four softmax warps that take
 // alternate tiles, with the same barrier protocol (tests/pipeline_model.py, Sim, graph as written);
 // P lives in shared memory, written by the softmax warps and read by the tensor core after a proxy
-// fence. Split partials (fp32 O^T columns and row sums) go to the second kernel.
+// fence. Split partials (fp32 O^T columns and row sums) are combined on chip when the n_split CTAs
+// of a batch run as one thread-block cluster, else by the second kernel.
 #pragma once
 
 #include "mg_attn_kernels.cuh"
@@ -333,6 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool o_ready = ptx::named_barrier_and(kSoftmaxBarrier, kSoftmaxThreads,
                                                     ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull));
+        float *stage_o = reinterpret_cast<float *>(smem + (sStage0 - sQ));  // [16][128]
+        float *stage_l = stage_o + kSwapNQ * D;                                // [16]
         if (o_ready && g == 0) {
             // O^T lanes are output columns: the four warps of group 0 cover all 128.
             ptx::tc_fence_after();
@@ -350,6 +353,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         l += l_red[w * kSwapNQ + q];
                     if (p.n_split == 1) {
                         p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(__uint_as_float(o[q]) * __frcp_rn(l));
+                    } else if (p.cluster_reduce) {
+                        // Staged for the cluster's owners (the K/V ring is idle): O^T column c of
+                        // query q, fp32, and the row sum of q.
+                        stage_o[q * D + c] = __uint_as_float(o[q]);
+                        if (c == 0)
+                            stage_l[q] = l;
                     } else {
                         const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + q;
                         p.ws_o[r * D + c] = __uint_as_float(o[q]);
@@ -359,6 +368,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    }
+
+    // On-chip combine (the n_split CTAs of a batch in one thread-block cluster, rank j): after a
+    // cluster barrier every CTA's staged fp32 O^T and row sums are visible; rank j forms columns
+    // [128 j / n, 128 (j + 1) / n) of every query row as sum_r O_r / sum_r l_r over the ranks in
+    // rank order and writes fp16 O; a second barrier keeps each CTA's shared memory alive until
+    // the others have read it. Every thread of every CTA reaches both barriers, on the unwinding
+    // path too (a CTA that unwound staged nothing: O is then undefined, as the status says).
+    __syncwarp();
+    if (p.cluster_reduce) {
+        ptx::cluster_sync();
+        if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
+            const int n = p.n_split;
+            const int c_lo = j * D / n;
+            const int cols = (j + 1) * D / n - c_lo;
+            const int mq = p.M < kSwapNQ ? p.M : kSwapNQ;
+            const uint32_t so = ptx::smem_u32(smem) + (sStage0 - sQ);
+            const uint32_t sl = so + kSwapNQ * D * 4;
+            for (int it = threadIdx.x - 64; it < mq * cols; it += kSoftmaxThreads) {
+                const int q = it / cols;
+                const int c = c_lo + it % cols;
+                float ov[kMaxClusterRanks], lv[kMaxClusterRanks];
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r) {  // every load in flight before the sums
+                    if (r < n) {
+                        ov[r] = ptx::ld_cluster_f32(ptx::map_to_rank(so + static_cast<uint32_t>(q * D + c) * 4, r));
+                        lv[r] = ptx::ld_cluster_f32(ptx::map_to_rank(sl + static_cast<uint32_t>(q) * 4, r));
+                    }
+                }
+                float os = 0.f, ls = 0.f;
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r) {
+                    if (r < n) {
+                        os += ov[r];
+                        ls += lv[r];
+                    }
+                }
+                p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(os * __frcp_rn(ls));
+            }
+        }
+        ptx::cluster_sync_relaxed();
     }
 
     // Teardown: every tensor-memory access of the CTA is ordered before the free.

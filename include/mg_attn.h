@@ -105,7 +105,8 @@ typedef enum {
                                       query rows per batch, the split schedule): per K/V tile the products run
                                       transposed, S^T = K^T Q^T and O^T += V^T P^T, so the MMA's 128 rows are
                                       keys (resp. output columns) instead of mostly-empty query rows; split
-                                      partials always go to the second kernel. The default where it applies
+                                      partials combine on chip (fp32) when the cluster fits, else in the
+                                      second kernel. The default where it applies
                                       (this flag only states it); see info.swap_ab */
 #define MG_FLAG_NO_SWAP_AB 0x400   /* never use the few-row specialisation (the one-tile kernel instead) */
 #define MG_FLAG_PUSH_COMBINE 0x800 /* on-chip combine, pushed form (the graph as written, head dim 64): each

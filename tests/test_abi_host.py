@@ -103,8 +103,8 @@ def test_query_decisions(B, M, N, d):
         assert info["grid_ctas"] <= 152  # one wave
     cluster = info["cluster_ctas"]
     assert cluster in (0, info["n_split"]) and cluster <= 16
-    if 2 <= info["n_split"] <= 16 and not info["swap_ab"]:
-        assert cluster == info["n_split"]  # small splits combine on chip (the few-row kernel: second kernel)
+    if 2 <= info["n_split"] <= 16:
+        assert cluster == info["n_split"]  # small splits combine on chip (where the device fits the cluster)
     assert info["kernels_per_run"] == (2 if info["n_split"] > 1 and cluster == 0 else 1)
     assert info["smem_bytes"] <= 232448
     # Every column tile belongs to exactly one split, every split has one (n_split <= n_tiles),
@@ -190,8 +190,13 @@ def test_query_stream_k_choices():
 
 def test_query_swap_ab():
     info = mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_SWAP_AB)
-    assert info["swap_ab"] == 1 and info["cluster_ctas"] == 0 and info["schedule"] == 0
-    assert info["kernels_per_run"] == (2 if info["n_split"] > 1 else 1)
+    assert info["swap_ab"] == 1 and info["schedule"] == 0
+    # Its split partials combine on chip like the one-tile kernel's (the query cannot see whether
+    # the device fits the cluster; a plan falls back to the second kernel when it does not).
+    assert info["cluster_ctas"] == info["n_split"] == 8 and info["kernels_per_run"] == 1
+    k2 = mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_NO_CLUSTER)
+    assert k2["swap_ab"] == 1 and k2["cluster_ctas"] == 0 and k2["kernels_per_run"] == 2
+    assert k2["workspace_bytes"] == 256 + 8 * 16 * 8 * (128 + 1) * 4 and info["workspace_bytes"] == 256
     assert info["smem_bytes"] < mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_NO_SWAP_AB)["smem_bytes"]
     # The default where it applies: head dim 128, at most 16 rows, the graph as written.
     assert mg.mg_attn_query(16, 8, 32768, 128, 152)["swap_ab"] == 1

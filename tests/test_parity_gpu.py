@@ -310,6 +310,32 @@ def test_swap_ab_specialisation(B, M, N, d, n_split):
     assert_parity(O, ref, f"swap-AB {B, M, N, d} n_split={plan.info['n_split']}")
 
 
+SWAP_CLUSTER_SHAPES = [  # (B, M, N, n_split): head dim 128, few rows, split partials
+    (64, 1, 4096, 2),     # the launch example's shapes, as planned
+    (4, 8, 8192, 16),     # 16 ranks of 8 columns each
+    (5, 3, 5000, 7),      # 7 ranks of 18 or 19 columns; 3 rows; ragged N
+    (3, 16, 2048, 3),     # 16 rows
+    (2, 5, 1032, 9),      # ragged N (9 column tiles, one per rank)
+]
+
+
+@pytest.mark.parametrize("B,M,N,n_split", SWAP_CLUSTER_SHAPES)
+def test_swap_ab_cluster_combine(B, M, N, n_split):
+    # The few-row kernel's split partials combined on chip (fp32 O^T columns and row sums across
+    # the cluster) and by the second kernel: each against the oracle, and each reproducible.
+    d = 128
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.25, seed=B * 13 + M + n_split)
+    ref = oracle.attention(q, k, v)
+    O_cl, plan = run_gpu(q, k, v, n_split=n_split)
+    O_k2, plan2 = run_gpu(q, k, v, n_split=n_split, flags=mg.MG_FLAG_NO_CLUSTER)
+    assert plan.info["swap_ab"] == 1 and plan2.info["swap_ab"] == 1
+    assert plan2.info["cluster_ctas"] == 0 and plan2.info["kernels_per_run"] == 2
+    assert_parity(O_cl, ref, f"swap-AB cluster {plan.info['cluster_ctas']} of {n_split}")
+    assert_parity(O_k2, ref, "swap-AB second kernel")
+    O_again, _ = run_gpu(q, k, v, n_split=n_split)
+    assert torch.equal(O_cl, O_again)
+
+
 def test_swap_ab_matches_one_tile_kernel_and_is_reproducible():
     q, k, v, _ = inputs.make_config("decode")
     ref = oracle.attention(q, k, v)
