@@ -125,6 +125,18 @@ FwdKernel swap_kernel(int stages)
 // The one-tile kernel under the stream-K schedule (the graph as written).
 FwdKernel sk_kernel(int64_t d, int stages) { return fwd_kernel_variant<mg::kStreamK>(d, stages); }
 
+// The pushed on-chip combine: head dim 64, at most kPushMaxStages stages.
+FwdKernel push_kernel(int stages)
+{
+    switch (stages) {
+    case 2: return mg::mg_attn_fwd_partial<64, 2, mg::kPush>;
+    case 3: return mg::mg_attn_fwd_partial<64, 3, mg::kPush>;
+    case 4: return mg::mg_attn_fwd_partial<64, 4, mg::kPush>;
+    case 5: return mg::mg_attn_fwd_partial<64, 5, mg::kPush>;
+    default: return nullptr;
+    }
+}
+
 // The fused kernel for a head dim, pipeline depth and the MG_FLAG_* evaluation flags.
 FwdKernel fwd_kernel(int64_t d, int stages, int flags)
 {
@@ -314,7 +326,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
                                  : mg::fwd_smem_bytes(static_cast<int>(d), stages, push);
     if (static_cast<int64_t>(smem) > max_smem ||
         !(pair ? pair_kernel(stages)
-               : swap ? swap_kernel(stages) : stream_k ? sk_kernel(d, stages) : fwd_kernel(d, stages, o.flags)))
+               : swap ? swap_kernel(stages)
+                      : stream_k ? sk_kernel(d, stages) : push ? push_kernel(stages) : fwd_kernel(d, stages, o.flags)))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
 
@@ -368,6 +381,8 @@ FwdKernel plan_kernel(const mg_attn_plan_info &info, int flags)
         return swap_kernel(info.stages);
     if (info.schedule == 1)
         return sk_kernel(info.d, info.stages);
+    if (info.xchg_push == 1)
+        return push_kernel(info.stages);
     return info.q_tiles_per_cta == 2 ? pair_kernel(info.stages) : fwd_kernel(info.d, info.stages, flags);
 }
 
@@ -758,7 +773,6 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
     prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
-    prm.push_combine = in.cluster_ctas > 0 && in.xchg_push ? 1 : 0;
     prm.O = static_cast<__half *>(O);
     prm.ws_o = plan->ws_o;
     prm.ws_l = plan->ws_l;
@@ -982,8 +996,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         o.flags = MG_FLAG_NO_CLUSTER;
         if ((st = decide(B, M, N, d, &o, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags)) != MG_OK)
             return st;
-        // The fallback keeps the kernel (its choice does not depend on the cluster); its limit is
-        // set again anyway.
+        // The fallback's kernel carries the second kernel's epilogue: its limit is set as well.
         fwd = plan_kernel(in, 0);
         if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       in.smem_bytes)) != cudaSuccess)
@@ -1020,7 +1033,6 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.n_tiles = in.n_tiles;
     prm.n_split = in.n_split;
     prm.cluster_reduce = in.cluster_ctas > 0 ? 1 : 0;
-    prm.push_combine = in.cluster_ctas > 0 && in.xchg_push ? 1 : 0;
     prm.O = static_cast<__half *>(O);
     prm.status = reinterpret_cast<int *>(sd->scratch);
     prm.ws_o = ws_o;

@@ -125,7 +125,6 @@ struct FwdParams {
     int n_tiles;             // ceil(N / 128)
     int n_split;
     int cluster_reduce;      // the n_split CTAs of a row tile form a cluster and combine on chip
-    int push_combine;        // on-chip combine by bulk copies into each owner's receive area
     __half *O;               // (B, M, d) fp16 output (written directly by the cluster reduction)
     float *ws_o;             // (n_split, B, M, d) partial numerators (the cluster combine's plain stores)
     float *ws_l;             // (n_split, B, M) partial row sums
@@ -334,6 +333,7 @@ enum Variant : int {
     kSafe = 1,     // each row's maximum subtracted before exp (a first pass over K finds it)
     kQkNorm = 2,   // QK-norm: scores scaled by 1/rms of the query row and of the key vector; safe
     kStreamK = 3,  // the graph as written under a stream-K schedule (batches of at most 16 rows)
+    kPush = 4,     // the graph as written, split partials pushed into each owner's receive area
 };
 
 // Stream-K schedule: the B row tiles x n_tiles column tiles form one sequence of units u = r n_tiles
@@ -358,9 +358,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = TileCfg<D>;
     constexpr bool kSafeMax = VAR == kSafe || VAR == kQkNorm;  // the row-maximum pass runs
     constexpr bool kQk = VAR == kQkNorm;
+    constexpr bool kPushX = VAR == kPush;  // the pushed on-chip combine (its receive area after the ring)
+    // The pushed variant always combines on chip and carries no code for the other epilogues (one
+    // split's TMA store of O, the second kernel's partials). (A plain variant cut down the same
+    // way measured no faster on GB300: GQA 6.64 against 6.60 us per call.)
+    constexpr bool kClusterOnly = VAR == kPush;
+    const bool cluster = kClusterOnly || p.cluster_reduce != 0;
     constexpr int kPBuffers = C::kPBuffers;
     using BI = Bars<STAGES, kPBuffers>;
-    static_assert(fwd_smem_bytes(D, STAGES) <= 232448u, "tile configuration exceeds 227 KB");
+    static_assert(fwd_smem_bytes(D, STAGES, VAR == kPush) <= 232448u, "tile configuration exceeds 227 KB");
     static_assert(128 * D * 4 <= C::kStageBytes, "output staging must fit in one K/V stage");
     static_assert(2 * 128 * C::kRowHalves * 2 + 128 * C::kLmw * 4 <= STAGES * C::kStageBytes,
                   "on-chip combine staging must fit in the K/V ring");
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = ptx::smem_u32(smem);
     const uint32_t sStage0 = sQ + C::kQBytes;
     uint8_t *recv = smem + C::kQBytes + STAGES * C::kStageBytes;
-    float *l_xchg = reinterpret_cast<float *>(recv + (p.push_combine ? C::kRecvBytes : 0u));
+    float *l_xchg = reinterpret_cast<float *>(recv + (kPushX ? C::kRecvBytes : 0u));
     uint64_t *bars = reinterpret_cast<uint64_t *>(l_xchg + 2 * kBlockM);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -387,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the same K/V tiles close together in time.
     const int cta = blockIdx.x;
     constexpr bool kSK = VAR == kStreamK;
-    const int mt = kSK ? 0 : p.cluster_reduce ? (cta / p.n_split) % p.m_tiles_per_b : cta % p.m_tiles_per_b;
-    const int j = kSK ? 0 : p.cluster_reduce ? cta % p.n_split : (cta / p.m_tiles_per_b) % p.n_split;
+    const int mt = kSK ? 0 : cluster ? (cta / p.n_split) % p.m_tiles_per_b : cta % p.m_tiles_per_b;
+    const int j = kSK ? 0 : cluster ? cta % p.n_split : (cta / p.m_tiles_per_b) % p.n_split;
     const int b = kSK ? 0 : cta / (p.m_tiles_per_b * p.n_split);
     const int m0 = mt * kBlockM;
     // Stream-K: this CTA's units [u0, u1) and their segments (one per row tile touched; a batch is
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmV);
         if (p.n_split == 1)
             ptx::prefetch_tensormap(&tmO);
-        else if (!p.cluster_reduce)
+        else if (!cluster)
             ptx::prefetch_tensormap(&tmW);
     }
     if (warp == 1) {
@@ -458,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     // Pushed exchange: the first half of a cluster barrier whose wait, just before the first copy
     // to another CTA, says that every CTA's receive barrier is initialised.
-    if (VAR == kPlain && p.cluster_reduce && p.push_combine)
+    if (kPushX && cluster)
         ptx::cluster_arrive_release();
 
     // Everything above touched only on-chip state; global memory waits for the previous grid.
@@ -1019,7 +1025,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int col = g * C::kHalfCols + c * 32;  // first O column of this slice
                     ptx::tmem_ld_32x32b_x32(tmem + lane_addr + kTmemO + col, r);
                     ptx::tmem_ld_wait(r);
-                    if (p.cluster_reduce) {
+                    if (cluster) {
                         // One correctly rounded reciprocal, then products (l = 0 only if every
                         // exponential of the split underflowed; its partial is then 0).
                         const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
@@ -1088,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.cluster_reduce) {
+            if (cluster) {
                 if (g == 0)
                     stage_lm[row * C::kLmw + D / 32] = m;
             } else if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
@@ -1097,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kSafeMax)
                     p.ws_m[r] = m;
             }
-            if (!p.cluster_reduce) {
+            if (!cluster) {
                 ptx::fence_proxy_async_smem();
                 ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
                 if (sw == 0 && lane == 0) {
@@ -1135,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     //    longer than the owners' loads, and the early start does not make up for it.
     // Every thread of every CTA reaches every cluster barrier, on the unwinding path too.
     __syncwarp();
-    if (p.cluster_reduce) {
+    if (cluster) {
         const bool softmax_warp = warp >= 2 && warp < 2 + kSoftmaxWarps;
         const int n = p.n_split;
         const int lo_row = j * kBlockM / n;
@@ -1252,9 +1258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        // The pushed form serves the graph as written (the host plans it only there): in the two-pass
-        // variants a second copy of the combine loop would push the main loop's registers to spills.
-        if (VAR == kPlain && p.push_combine) {
+        // The pushed form is a kernel variant of its own (the graph as written), so that the
+        // default kernels carry neither its code nor its receive area.
+        if constexpr (kPushX) {
             ptx::cluster_wait_acquire();  // every CTA's receive barrier is initialised
             if (softmax_warp) {
                 ptx::fence_proxy_async_smem();  // this thread's staging writes, before the copies read them
@@ -1287,8 +1293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // (A CTA that is unwinding does not wait here; wait_bounded returns at once.)
                 if (wait_bounded(wc, bar(BI::kXRecv), 0, BI::kXRecv)) {
-                    if constexpr (VAR == kPlain)
-                        combine(std::true_type{});
+                    combine(std::true_type{});
                 } else {
                     // Even so, the copies on their way in land before this CTA passes the closing
                     // barrier (after which their senders may release the staging they read): every
