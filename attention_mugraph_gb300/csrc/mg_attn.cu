@@ -311,8 +311,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     // The pushed on-chip combine applies to the graph as written at head dim 64 (its receive area
     // takes the place of one K/V stage; d = 128 has no room for it) unless an explicit depth leaves
     // no room, and only on request: measured on GB300 it is slower than the pulled form, us per
-    // call (2, 256, 4096, 64) 7.31 against 6.64, (2, 64, 1024, 64) 5.83 against 5.29,
-    // (16, 256, 4096, 64) 11.02 against 9.86 (the pulled form at 5 stages: 6.64, 5.29, 10.04).
+    // call (2, 256, 4096, 64) 7.55 against 6.56, (2, 64, 1024, 64) 5.79 against 5.28,
+    // (16, 256, 4096, 64) 11.40 against 10.00 (the pulled form at 5 stages: 6.60, 5.29, 10.22).
     bool push = cluster && !pair && d == 64 && !(o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) &&
                 (o.flags & MG_FLAG_PUSH_COMBINE);
     if (push && stages > kPushMaxStages) {

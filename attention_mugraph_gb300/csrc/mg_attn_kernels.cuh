@@ -156,8 +156,8 @@ struct Bars {
     static constexpr int kNever = kDrainPv + 1;
     static constexpr int kXRecv = kNever + 1;      // pushed exchange: every rank's rows have landed here
     static constexpr int kCount = kXRecv + 1;
-    // + the tensor-memory address, the abort flag and 16 per-owner remainder flags
-    static_assert(kCount * 8 + 8 + 64 <= 512, "barrier area overflow");
+    // + the tensor-memory address and the abort flag
+    static_assert(kCount * 8 + 8 <= 512, "barrier area overflow");
 };
 
 struct WaitCtx {
@@ -349,6 +349,20 @@ __host__ __device__ __forceinline__ long long sk_cta_of(long long u, long long U
     return ((u + 1) * G - 1) / U;
 }
 
+// Pushed exchange: the 32-row quarters of a row tile (one softmax warp per group each) that hold
+// rows inside M and of CTA rank j's share [128 j / n, 128 (j + 1) / n). Every rank's warps of
+// those quarters arrive once each on rank j's receive barrier.
+__device__ __forceinline__ int push_quarters(const FwdParams &p, int m0, int j)
+{
+    const int n = p.n_split;
+    const int lo = j * kBlockM / n, hi = (j + 1) * kBlockM / n;
+    int quarters = 0;
+    for (int q = 0; q < 4; ++q)
+        if (m0 + 32 * q < p.M && 32 * q < hi && lo < 32 * q + 32)
+            ++quarters;
+    return quarters;
+}
+
 template <int D, int STAGES, int VAR>
 __global__ void __launch_bounds__(kThreads, 1)
     mg_attn_fwd_partial(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -380,9 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(l_xchg + 2 * kBlockM);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-    // Pushed exchange: whether owner o gets remainders from this CTA (written 1 by any thread that
-    // staged one of o's rows with remainders).
-    volatile uint32_t *lo_need = reinterpret_cast<volatile uint32_t *>(tmem_holder + 2);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
 
     const int warp = threadIdx.x >> 5;
@@ -438,11 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(BI::kDrain), 1);
         ptx::mbar_init(bar(BI::kDrainPv), 1);
         ptx::mbar_init(bar(BI::kNever), 1);
-        // One arrival per rank of the cluster (its expected bytes, then its copies land).
-        ptx::mbar_init(bar(BI::kXRecv), p.n_split);
+        // Pushed exchange: one arrival (the bytes it sends) per rank and per softmax warp with rows
+        // of this CTA's share and inside M; a CTA whose share lies past M gets nothing and waits
+        // for nothing.
+        const int pq = kPushX ? push_quarters(p, m0, j) : 0;
+        ptx::mbar_init(bar(BI::kXRecv), pq > 0 ? static_cast<uint32_t>(p.n_split * 2 * pq) : 1u);
         *abort_flag = 0;
-        for (int o = 0; o < kMaxClusterRanks; ++o)
-            lo_need[o] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -1003,6 +1015,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull));
         const float l = l_xchg[row] + l_xchg[kBlockM + row];
         staged_ok = o_ready;
+        uint32_t push_bytes = 0;  // pushed exchange: bytes this thread sent its rows' owner
+        if constexpr (kPushX)
+            ptx::cluster_wait_acquire();  // every CTA's receive barrier is initialised
         if (o_ready) {
             ptx::tc_fence_after();
             // The K/V ring is idle (every PV has completed): stage this CTA's output there. For the
@@ -1031,6 +1046,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
                         uint4 *dhi = reinterpret_cast<uint4 *>(stage_hi + row * C::kRowHalves + col);
                         uint4 *dlo = reinterpret_cast<uint4 *>(stage_lo + row * C::kRowHalves + col);
+                        // Pushed exchange: this row's slot in its owner's receive area (rank o holds
+                        // rows [128 o / n, 128 (o + 1) / n); sender j's rows start at row j * R).
+                        const int po = (row * p.n_split + p.n_split - 1) / kBlockM;
+                        const uint32_t prow = static_cast<uint32_t>(j * ((kBlockM + p.n_split - 1) / p.n_split) + row -
+                                                                    po * kBlockM / p.n_split);
+                        const uint32_t pbar = kPushX ? ptx::map_to_rank(bar(BI::kXRecv), po) : 0u;
+                        const uint32_t precv = ptx::smem_u32(recv);
                         bool wide = false;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -1042,7 +1064,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 h4[h] = ptx::pack_half2(x0, x1);
                                 wide = wide || fabsf(x0) >= kHiOnlyBelow || fabsf(x1) >= kHiOnlyBelow;
                             }
-                            dhi[q] = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                            if constexpr (kPushX)
+                                ptx::st_async_v4(ptx::map_to_rank(precv + (prow * C::kRowHalves + col) * 2 + q * 16, po),
+                                                 h4[0], h4[1], h4[2], h4[3], pbar);
+                            else
+                                dhi[q] = make_uint4(h4[0], h4[1], h4[2], h4[3]);
                         }
                         if (wide) {
                             // Second pass, only for a slice that needs it: the same products again,
@@ -1058,12 +1084,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hw));
                                     l4[h] = ptx::pack_half2(x0 - hf.x, x1 - hf.y);
                                 }
-                                dlo[q] = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                                if constexpr (kPushX)
+                                    ptx::st_async_v4(
+                                        ptx::map_to_rank(precv + (C::kRecvRows + prow) * C::kRowHalves * 2 + col * 2 + q * 16, po),
+                                        l4[0], l4[1], l4[2], l4[3], pbar);
+                                else
+                                    dlo[q] = make_uint4(l4[0], l4[1], l4[2], l4[3]);
                             }
                         }
-                        stage_lm[row * C::kLmw + col / 32] = wide ? -l : l;  // -0.0 when l = 0
-                        if (wide)  // its owner (rank o holds rows [128 o / n, 128 (o + 1) / n))
-                            lo_need[(row * p.n_split + p.n_split - 1) / kBlockM] = 1u;
+                        if constexpr (kPushX) {
+                            ptx::st_async_b32(ptx::map_to_rank(precv + 2 * C::kRecvRows * C::kRowHalves * 2 +
+                                                                   (prow * C::kLmw + col / 32) * 4, po),
+                                              __float_as_uint(wide ? -l : l), pbar);
+                            push_bytes += 64u + 4u + (wide ? 64u : 0u);
+                        } else {
+                            stage_lm[row * C::kLmw + col / 32] = wide ? -l : l;  // -0.0 when l = 0
+                        }
                     } else if (p.n_split == 1) {
                         // fp16 O/l: chunk col/64 of a {64, 128} fp16 box; this slice is units (col%64)/8 .. +3.
                         // One correctly rounded reciprocal, then products: within 1.5 fp32 ulps of
@@ -1121,6 +1157,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if constexpr (kPushX) {
+            // Pushed exchange: one arrival per warp and owner, with the bytes its lanes sent that
+            // owner (0 from a CTA that unwound and sent nothing). An arrival and the stores it
+            // counts may land in either order.
+            if (cluster && warp_rows) {
+                const int po = (row * p.n_split + p.n_split - 1) / kBlockM;
+                const unsigned peers = __match_any_sync(0xffffffffu, po);
+                const unsigned total = __reduce_add_sync(peers, push_bytes);
+                if (lane == __ffs(peers) - 1)
+                    ptx::mbar_arrive_expect_tx_cluster(ptx::map_to_rank(bar(BI::kXRecv), po), total);
+            }
+        }
         }  // !kSK
     }
 
@@ -1132,13 +1180,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     //  * pulled: after a cluster barrier every owner reads its rows out of the n CTAs' staging
     //    (distributed shared memory), and a second barrier keeps each CTA's shared memory alive
     //    until the others have read it;
-    //  * pushed (on request): as soon as a CTA has staged, one thread per owner copies that
-    //    owner's rows into the owner's receive area (bulk copies counted on the owner's receive
-    //    barrier), so an owner waits for its own rows only, not for a cluster-wide barrier, and
-    //    reads them locally. A closing cluster barrier, which each CTA reaches only once the copies
-    //    into it have landed, keeps every CTA's staging alive until its copies are done. Measured
-    //    on GB300 the pulled form is faster (0.5-1.1 us per call): the copies between CTAs take
-    //    longer than the owners' loads, and the early start does not make up for it.
+    //  * pushed (on request): as each thread forms its row's values it stores them, from
+    //    registers, into the row owner's receive area (st.async, each store counted on the owner's
+    //    receive barrier, with one arrival per warp and owner), so an owner waits for its own rows
+    //    only, not for a cluster-wide barrier, and reads them locally. A closing cluster barrier,
+    //    which each CTA reaches only once the stores into it have landed (or, unwinding, after a
+    //    bounded drain), keeps every receive area alive until nothing more can land in it.
+    //    Measured on GB300 the pulled form is faster (0.5-1.4 us per call): a CTA-to-CTA store
+    //    takes longer to land than an owner's load takes to return, and the early start does not
+    //    make up for it; bulk copies of the staged rows instead of stores did no better.
     // Every thread of every CTA reaches every cluster barrier, on the unwinding path too.
     __syncwarp();
     if (cluster) {
@@ -1261,43 +1311,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The pushed form is a kernel variant of its own (the graph as written), so that the
         // default kernels carry neither its code nor its receive area.
         if constexpr (kPushX) {
-            ptx::cluster_wait_acquire();  // every CTA's receive barrier is initialised
-            if (softmax_warp) {
-                ptx::fence_proxy_async_smem();  // this thread's staging writes, before the copies read them
-                ptx::named_barrier(kSoftmaxBarrier, kSoftmaxThreads);
-                const int t = threadIdx.x - 64;
-                if (t < n) {
-                    // Thread t sends owner t its rows: x, the row sums and maxima, and the
-                    // remainders when any of those rows has some. A CTA that unwound sends only
-                    // its arrival, so that no owner waits for it in vain.
-                    const int o = t;
-                    const int o_lo = o * kBlockM / n;
-                    const uint32_t rows = static_cast<uint32_t>((o + 1) * kBlockM / n - o_lo);
-                    const bool lo = lo_need[o] != 0u;
-                    const uint32_t x_bytes = rows * C::kRowHalves * 2;
-                    const uint32_t lm_bytes = rows * C::kLmw * 4;
-                    const uint32_t rbar = ptx::map_to_rank(bar(BI::kXRecv), static_cast<uint32_t>(o));
-                    if (staged_ok) {
-                        const uint32_t slot = static_cast<uint32_t>(j * R);
-                        ptx::mbar_arrive_expect_tx_cluster(rbar, x_bytes + lm_bytes + (lo ? x_bytes : 0u));
-                        ptx::bulk_copy_to_cluster(ptx::map_to_rank(rh + slot * C::kRowHalves * 2, o),
-                                                  sh + o_lo * C::kRowHalves * 2, x_bytes, rbar);
-                        ptx::bulk_copy_to_cluster(ptx::map_to_rank(rlm + slot * C::kLmw * 4, o),
-                                                  slm + o_lo * C::kLmw * 4, lm_bytes, rbar);
-                        if (lo)
-                            ptx::bulk_copy_to_cluster(ptx::map_to_rank(rl + slot * C::kRowHalves * 2, o),
-                                                      sl + o_lo * C::kRowHalves * 2, x_bytes, rbar);
-                    } else {
-                        ptx::mbar_arrive_expect_tx_cluster(rbar, 0u);
-                    }
-                }
+            // (The softmax warps passed the first barrier's wait before their first store.)
+            if (!softmax_warp)
+                ptx::cluster_wait_acquire();
+            if (softmax_warp && push_quarters(p, m0, j) > 0) {
                 // (A CTA that is unwinding does not wait here; wait_bounded returns at once.)
                 if (wait_bounded(wc, bar(BI::kXRecv), 0, BI::kXRecv)) {
                     combine(std::true_type{});
                 } else {
-                    // Even so, the copies on their way in land before this CTA passes the closing
-                    // barrier (after which their senders may release the staging they read): every
-                    // rank issued its copies and arrivals before any wait of its own.
+                    // Even so, the stores on their way in land before this CTA passes the closing
+                    // barrier and releases its shared memory: every rank has issued its stores
+                    // and arrivals before any wait of its own.
                     wait_drain(bar(BI::kXRecv), 0, p.timeout_ns);
                 }
             }

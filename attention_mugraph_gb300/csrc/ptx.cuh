@@ -233,16 +233,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_b
                  : "memory");
 }
 
-// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
-// memory into the shared memory of a CTA of this cluster; completion counts the bytes on that
-// CTA's mbarrier `cluster_bar`. The source must stay unchanged until the destination CTA has seen
-// that barrier's phase complete.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                     uint32_t cluster_bar)
+// Asynchronous stores into the shared memory of a CTA of this cluster (shared::cluster addresses
+// from map_to_rank), each counting its bytes on that CTA's mbarrier `cluster_bar` when it lands.
+// The data leaves from registers: nothing of the sender's has to stay alive for it.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cluster_bar)
 {
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      dst_cluster),
-                 "r"(src), "r"(bytes), "r"(cluster_bar)
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t dst_cluster, uint32_t v, uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster), "r"(v),
+                 "r"(cluster_bar)
                  : "memory");
 }
 

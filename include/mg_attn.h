@@ -110,11 +110,11 @@ typedef enum {
                                       (this flag only states it); see info.swap_ab */
 #define MG_FLAG_NO_SWAP_AB 0x400   /* never use the few-row specialisation (the one-tile kernel instead) */
 #define MG_FLAG_PUSH_COMBINE 0x800 /* on-chip combine, pushed form (the graph as written, head dim 64): each
-                                      CTA copies every owner's rows into that owner's receive area as soon as
-                                      it has staged them (bulk copies counted on the owner's barrier; one
-                                      pipeline stage fewer), instead of the owners reading them out of every
-                                      CTA's shared memory after a cluster barrier (the default, pulled form).
-                                      Opt-in: measured on GB300 it is slower; see info.xchg_push */
+                                      thread stores its row's values into the row owner's receive area as
+                                      soon as it has formed them (asynchronous stores counted on the owner's
+                                      barrier; one pipeline stage fewer), instead of the owners reading them
+                                      out of every CTA's shared memory after a cluster barrier (the default,
+                                      pulled form). Opt-in: measured on GB300 it is slower; see info.xchg_push */
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and
                                       the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */

@@ -8,19 +8,21 @@ every cluster barrier, mbarrier operation and copy they perform, as coroutines p
 * pulled (the default): a cluster barrier (release/acquire) after staging, the owners' loads
   from every CTA's staging, a closing cluster barrier before any CTA exits;
 * pushed (opt-in): the first half of a cluster barrier at the start (receive barriers
-  initialised), its wait before the first copy; per owner one sender thread that arrives on the
-  owner's receive mbarrier with the bytes it will send and issues bulk copies into the owner's
-  receive slot (completing those bytes on that barrier asynchronously, at any later moment); the
+  initialised), its wait before the first store; asynchronous stores (st.async, from registers)
+  of each row into its owner's receive slot, each completing its bytes on the owner's receive
+  mbarrier at any later moment, and per warp and owner one arrival with the bytes sent (the
+  model lumps a rank's warps into one arrival per owner: the barrier's count differs, its
+  protocol does not); the
   owner's bounded wait on its receive barrier, its combine from the receive area, and a closing
   cluster barrier that each owner reaches only once its rows have landed (or, unwinding, after a
-  bounded drain of the copies still on their way).
+  bounded drain of the stores still on their way).
 
 A CTA may be unwinding (its output was never complete: it stages nothing and sends only its
 arrivals), and a bounded wait may run out at any moment once `abort_rate` is set. The scheduler
 runs the roles of all CTAs under random interleavings and checks:
 
-* a copy reads its source staging and writes its destination only while both CTAs are alive
-  (neither has passed the closing barrier and torn down);
+* a store writes its destination only while that CTA is alive (it has not passed the closing
+  barrier and torn down); its data leaves from the sender's registers, so the sender may be gone;
 * an owner reads a sender's slot (pushed) or staging (pulled) only once those bytes are there,
   and, when no CTA is unwinding and no wait ran out, every owner combines;
 * nothing deadlocks: every role finishes.
@@ -106,8 +108,6 @@ class ExchangeSim:
             yield "cbar"
 
     def _copy_lands(self, src, dst):
-        if not self.alive[src]:
-            raise ProtocolError(f"copy {src}->{dst} reads the staging of CTA {src} after it tore down")
         if not self.alive[dst]:
             raise ProtocolError(f"copy {src}->{dst} writes into CTA {dst} after it tore down")
         self.landed[dst][src] = True
