@@ -45,7 +45,7 @@ def _call(lib, shape, Q, K, V, O, stream):
                                    ctypes.c_void_p(stream.cuda_stream))
 
 
-@pytest.mark.parametrize("name", ["gqa", "decode", "tiny"])
+@pytest.mark.parametrize("name", ["gqa", "decode", "tiny", "decode_m1"])
 def test_noalloc_matches_planned_entry_point_on_two_calls(lib, name):
     q, k, v, shape = inputs.make_config(name)
     B, M, N, d = shape
