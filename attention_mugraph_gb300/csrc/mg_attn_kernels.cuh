@@ -1026,9 +1026,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // with any |x| >= kHiOnlyBelow also the remainders x - fp16(x), in the same layout;
             // then the fp32 row sum l_j once per slice (each copy carries, in its sign bit, whether
             // that slice's remainders are staged; l_j >= 0) and the row maximum m_j, kLmw floats per
-            // row, read by the cluster's CTAs after the cluster barrier or copied into their receive
-            // areas. Otherwise the 128-byte-swizzled layout the output tensor maps expect, then a
-            // TMA store.
+            // row, read by the cluster's CTAs after the cluster barrier (the pushed variant stores
+            // the same values straight into their owners' receive areas instead). Otherwise the
+            // 128-byte-swizzled layout the output tensor maps expect, then a TMA store.
             const uint32_t stage = sStage0;
             __half *stage_hi = reinterpret_cast<__half *>(smem + C::kQBytes);
             __half *stage_lo = stage_hi + kBlockM * C::kRowHalves;

@@ -98,13 +98,24 @@ def ceilings(info, B, M, N, exp_rate_ns, roof_us):
             "floor_us": max(floor, t_exp, roof_us)}
 
 
+def source_code_text(text: str) -> str:
+    """C++ source without its comments and blank lines: what a digest of the code should see."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_digest():
+    """Digest of the fused kernel's code (its two headers, comments left out), recorded beside the
+    ncu counters in the committed summary; a change of code invalidates the recorded traffic."""
     import hashlib
 
     h = hashlib.sha256()
     for rel in ("attention_mugraph_gb300/csrc/mg_attn_kernels.cuh", "attention_mugraph_gb300/csrc/ptx.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(source_code_text(f.read()).encode())
     return h.hexdigest()[:16]
 
 
