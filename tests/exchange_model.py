@@ -3,7 +3,7 @@
 The fused kernels (mg_attn_fwd_partial, mg_attn_fwd_swap) combine the n split partials of a row
 tile inside one cluster. Each CTA stages its partial in its own shared memory; rank o owns a
 slice of the rows (or columns) and writes that slice of O. Two forms are restated here, with
-every cluster barrier, mbarrier operation and copy they perform, as coroutines per CTA role:
+every cluster barrier, mbarrier operation and store they perform, as coroutines per CTA role:
 
 * pulled (the default): a cluster barrier (release/acquire) after staging, the owners' loads
   from every CTA's staging, a closing cluster barrier before any CTA exits;
@@ -27,7 +27,7 @@ runs the roles of all CTAs under random interleavings and checks:
   and, when no CTA is unwinding and no wait ran out, every owner combines;
 * nothing deadlocks: every role finishes.
 
-The transaction count of an mbarrier may go below zero for a while (a copy's bytes can land
+The transaction count of an mbarrier may go below zero for a while (a store's bytes can land
 before its sender's expect-tx arrival is counted); the phase completes when both the pending
 arrivals and the count are zero. The mutations in tests/test_exchange_protocol.py show that the
 model catches the hazards it is meant to.
@@ -95,7 +95,7 @@ class ExchangeSim:
         self.staged = [False] * n      # staging written (sender side)
         self.alive = [True] * n        # not yet torn down
         self.landed = [[False] * n for _ in range(n)]  # landed[o][r]: r's rows in o's receive slot
-        self.copies = []               # in flight: (src, dst)
+        self.stores = []               # in flight: (src, dst)
         self.combined = [False] * n
         self.timed_out = [False] * n
         self.bytes = lambda r, o: 3 + (r + o) % 2  # a sender's bytes for an owner (varies)
@@ -107,9 +107,9 @@ class ExchangeSim:
         while self.cbar.phase < k:
             yield "cbar"
 
-    def _copy_lands(self, src, dst):
+    def _store_lands(self, src, dst):
         if not self.alive[dst]:
-            raise ProtocolError(f"copy {src}->{dst} writes into CTA {dst} after it tore down")
+            raise ProtocolError(f"store {src}->{dst} lands in CTA {dst} after it tore down")
         self.landed[dst][src] = True
         self.recv[dst].complete_tx(self.bytes(src, dst))
 
@@ -130,13 +130,13 @@ class ExchangeSim:
             if r in self.unwound:
                 if "no_zero_arrival" not in self.mut:
                     self.recv[o].arrive(0)
-            elif "copies_before_arrival" in self.mut:
-                self.copies.append((r, o))
+            elif "stores_before_arrival" in self.mut:
+                self.stores.append((r, o))
                 yield "send"
                 self.recv[o].arrive(self.bytes(r, o))
             else:
                 self.recv[o].arrive(self.bytes(r, o))
-                self.copies.append((r, o))
+                self.stores.append((r, o))
             yield "send"
 
     # -------------------------------------------------------------- roles
@@ -147,7 +147,7 @@ class ExchangeSim:
         yield "staged"
         if self.push:
             # The prologue's arrival (receive barriers initialised) was made at the start; its
-            # wait comes before the first copy.
+            # wait comes before the first store.
             while self.cbar.phase < 1:
                 yield "cbar"
             yield from self._send(r)
@@ -162,8 +162,8 @@ class ExchangeSim:
                     yield "combine"
                 self.combined[r] = True
             elif "no_drain_on_abort" not in self.mut:
-                # the bounded drain of the copies still on their way in: every rank has issued
-                # its copies and arrivals before any wait of its own
+                # the bounded drain of the stores still on their way in: every rank has issued
+                # its stores and arrivals before any wait of its own
                 while not self.recv[r].done:
                     yield "drain"
             if "arrive_before_recv_wait" in self.mut:
@@ -211,20 +211,20 @@ class ExchangeSim:
         actors = {f"softmax{r}": self.softmax(r) for r in range(self.n)}
         actors.update({f"others{r}": self.others(r) for r in range(self.n)})
         for _ in range(max_steps):
-            if not actors and not self.copies:
+            if not actors and not self.stores:
                 break
-            choices = list(actors) + (["copy"] if self.copies else [])
+            choices = list(actors) + (["store"] if self.stores else [])
             pick = self.rng.choice(choices)
-            if pick == "copy":
-                src, dst = self.copies.pop(self.rng.randrange(len(self.copies)))
-                self._copy_lands(src, dst)
+            if pick == "store":
+                src, dst = self.stores.pop(self.rng.randrange(len(self.stores)))
+                self._store_lands(src, dst)
                 continue
             try:
                 next(actors[pick])
             except StopIteration:
                 del actors[pick]
         else:
-            raise ProtocolError(f"deadlock: {sorted(actors)} still waiting, {len(self.copies)} copies in flight")
+            raise ProtocolError(f"deadlock: {sorted(actors)} still waiting, {len(self.stores)} stores in flight")
         if not self.unwound and not any(self.timed_out) and not all(self.combined):
             raise ProtocolError("an owner did not combine although no CTA unwound")
         return self

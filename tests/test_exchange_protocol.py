@@ -24,10 +24,10 @@ def test_exchange_as_built_is_clean(push):
 
 
 def test_pushed_bytes_may_land_before_their_arrival():
-    # A copy's bytes can be counted before its sender's expect-tx arrival (the transaction count
+    # A store's bytes can be counted before its sender's expect-tx arrival (the transaction count
     # dips below zero): the phase still completes only once every arrival and byte is in.
     for n, seed in itertools.product(SIZES, range(25)):
-        em.ExchangeSim(n, True, seed, mutations=("copies_before_arrival",)).run()
+        em.ExchangeSim(n, True, seed, mutations=("stores_before_arrival",)).run()
 
 
 def caught(mutation, push, **kw):
