@@ -11,9 +11,10 @@ from ._lib import (MG_ERR_CONFIG, MG_ERR_CUDA, MG_ERR_INSUFFICIENT_SMEM, MG_ERR_
                    MG_FLAG_STREAM_K, MG_FLAG_SWAP_AB,
                    MG_FLAG_QK_NORM, MG_FLAG_SAFE_SOFTMAX, MG_OK,
                    MG_QKNORM_EPS, MgAttnError,
-                   Plan, attention, diag_exp_rate, diag_launch_floor, load_library, mg_attn_plan, mg_attn_query)
+                   Plan, attention, diag_exp_rate, diag_launch_floor, load_library, mg_attn_plan, mg_attn_query,
+                   run_noalloc)
 
-__all__ = ["Plan", "attention", "load_library", "mg_attn_plan", "mg_attn_query", "MgAttnError", "MG_OK",
+__all__ = ["Plan", "attention", "run_noalloc", "load_library", "mg_attn_plan", "mg_attn_query", "MgAttnError", "MG_OK",
            "MG_ERR_INSUFFICIENT_SMEM", "MG_ERR_LAYOUT", "MG_ERR_CONFIG", "MG_ERR_INVALID_ARG", "MG_ERR_UNSUPPORTED",
            "MG_ERR_CUDA", "MG_ERR_TIMEOUT", "MG_FLAG_NO_PDL", "MG_FLAG_INJECT_TIMEOUT", "MG_FLAG_NO_CLUSTER",
            "MG_FLAG_SAFE_SOFTMAX", "MG_FLAG_QK_NORM", "MG_FLAG_Q_PAIRS", "MG_FLAG_NO_Q_PAIRS",

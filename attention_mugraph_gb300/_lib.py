@@ -162,6 +162,23 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def run_noalloc(Q, K, V, O, stream=None):
+    """mg_attn_run_noalloc: O = attention(Q, K, V) with no plan and no device allocation (the split
+    partials go to the library's fixed 8 MiB array; calls that overlap on the GPU share it and
+    must be serialised). Q (B,M,d), K (B,d,N), V (B,N,d), O (B,M,d): contiguous fp16 CUDA tensors."""
+    import torch
+
+    B, M, d = (int(x) for x in Q.shape)
+    N = int(K.shape[2])
+    for t, shape, name in ((Q, (B, M, d), "Q"), (K, (B, d, N), "K"), (V, (B, N, d), "V"), (O, (B, M, d), "O")):
+        if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous fp16 CUDA tensor of shape {shape}")
+    lib = load_library()
+    _check(lib.mg_attn_run_noalloc(B, M, N, d, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                   _stream_handle(stream)), "mg_attn_run_noalloc")
+    return O
+
+
 class Plan:
     """Owns one ``mg_attn_plan_t`` for a fixed (B, M, N, d) on the current CUDA device."""
 
