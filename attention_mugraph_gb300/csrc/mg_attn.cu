@@ -738,6 +738,63 @@ mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info)
     return MG_OK;
 }
 
+// The output ranges of the last call enqueued on each stream (O as passed to mg_attn_run; hO and
+// its device address for mg_attn_run_host). A host-buffer call's copy kernel may load its inputs
+// before the previous kernel on its stream has finished, and only that kernel: every earlier one
+// has completed by the time the copy kernel can start (each of this library's kernels releases its
+// dependents only after its own wait). So the loads are early unless an input shares bytes with
+// the previous call's output on that stream (a chain of calls) or with the call's own output.
+struct OutRanges {
+    cudaStream_t stream = nullptr;
+    uintptr_t lo[2] = {0, 0}, hi[2] = {0, 0};  // [lo, hi) ranges; empty when lo == hi
+    unsigned long long age = 0;
+    bool used = false;
+};
+constexpr int kStreamSlots = 64;
+std::mutex g_out_mu;
+OutRanges g_out[kStreamSlots];
+unsigned long long g_out_clock = 0;
+
+OutRanges *find_slot(cudaStream_t stream, bool claim)
+{
+    OutRanges *oldest = &g_out[0];
+    for (auto &r : g_out) {
+        if (r.used && r.stream == stream)
+            return &r;
+        if (!r.used || (oldest->used && r.age < oldest->age))
+            oldest = &r;
+    }
+    return claim ? oldest : nullptr;
+}
+
+// The output ranges of the last call enqueued on `stream` (none if unknown).
+OutRanges last_outputs(cudaStream_t stream)
+{
+    std::lock_guard<std::mutex> lock(g_out_mu);
+    const OutRanges *r = find_slot(stream, false);
+    return r ? *r : OutRanges{};
+}
+
+// Records the output ranges of the call just enqueued on `stream`.
+void record_outputs(cudaStream_t stream, const void *a, size_t na, const void *b, size_t nb)
+{
+    std::lock_guard<std::mutex> lock(g_out_mu);
+    OutRanges *slot = find_slot(stream, true);
+    slot->used = true;
+    slot->stream = stream;
+    slot->age = ++g_out_clock;
+    slot->lo[0] = reinterpret_cast<uintptr_t>(a);
+    slot->hi[0] = slot->lo[0] + (a ? na : 0);
+    slot->lo[1] = reinterpret_cast<uintptr_t>(b);
+    slot->hi[1] = slot->lo[1] + (b ? nb : 0);
+}
+
+bool overlaps_range(const void *p, size_t n, uintptr_t lo, uintptr_t hi)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(p);
+    return lo < hi && x < hi && lo < x + n;
+}
+
 mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const void *V, void *O,
                       mg_stream_t stream)
 {
@@ -823,6 +880,7 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
         if (e != cudaSuccess)
             return cuda_fail(e, "launch mg_attn_combine");
     }
+    record_outputs(cfg.stream, O, static_cast<size_t>(B * M * d) * 2, nullptr, 0);
     return MG_OK;
 }
 
@@ -864,17 +922,24 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
             in_jobs.dst[i] = reinterpret_cast<uint4 *>(s + off[i]);
             in_jobs.units[i] = bytes[i] / 16;
         }
-        // The inputs are read as soon as the copy kernel starts, possibly while this stream's
-        // previous kernels still run; none of this library's kernels writes them, unless O (which
-        // the previous call on this plan may still be writing) shares bytes with one of them: then
-        // the loads wait as well. Measured on GB300 (GQA graph, back-to-back calls): 13.9 us per
-        // call, against 19.3 with every load after the wait (the link's transfer then overlaps
-        // the previous call's attention kernel).
-        auto overlaps = [&](const void *a, size_t na, const void *b, size_t nb) {
-            const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-            return x < y + nb && y < x + na;
+        // The inputs are loaded as soon as the copy kernel starts, possibly while the previous
+        // kernel on this stream still runs (only that one: each of this library's kernels releases
+        // its dependents after its own wait). So the loads wait as well when an input shares bytes
+        // with what that kernel may still be writing: the previous call's output on this stream
+        // (a chain of calls), or this call's own output (which a call before it on this plan may
+        // be writing). Measured on GB300 (GQA graph, back-to-back calls): 13.5 us per call, against
+        // 19.3 with every load after the wait (the link's transfer then overlaps the previous
+        // call's attention kernel).
+        const OutRanges prev = last_outputs(st);
+        auto clashes = [&](const void *host, const void *dev, size_t n) {
+            if (overlaps_range(host, n, reinterpret_cast<uintptr_t>(hO), reinterpret_cast<uintptr_t>(hO) + bq))
+                return true;
+            for (int r = 0; r < 2; ++r)
+                if (overlaps_range(host, n, prev.lo[r], prev.hi[r]) || overlaps_range(dev, n, prev.lo[r], prev.hi[r]))
+                    return true;
+            return false;
         };
-        in_jobs.early = !(overlaps(hO, bq, hQ, bq) || overlaps(hO, bq, hK, bk) || overlaps(hO, bq, hV, bv));
+        in_jobs.early = !(clashes(hQ, dQ, bq) || clashes(hK, dK, bk) || clashes(hV, dV, bv));
         if ((e = launch_copy(in_jobs, plan->info.num_sms, pdl, st)) != cudaSuccess)
             return cuda_fail(e, "launch mg_copy_units (host to device)");
     } else if ((e = cudaMemcpyAsync(s + oq, hQ, bq, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
@@ -889,18 +954,20 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
     mg_status r = mg_attn_run(plan, s + oq, s + ok, s + ov, o_direct ? dO : s + oo, stream);
     if (r != MG_OK)
         return r;
-    if (o_direct)
-        return MG_OK;
-    if (direct) {
-        CopyJobs out_jobs{};
-        out_jobs.src[0] = reinterpret_cast<const uint4 *>(s + oo);
-        out_jobs.dst[0] = static_cast<uint4 *>(dO);
-        out_jobs.units[0] = bq / 16;
-        if ((e = launch_copy(out_jobs, plan->info.num_sms, pdl, st)) != cudaSuccess)
-            return cuda_fail(e, "launch mg_copy_units (device to host)");
-    } else if ((e = cudaMemcpyAsync(hO, s + oo, bq, cudaMemcpyDeviceToHost, st)) != cudaSuccess) {
-        return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    if (!o_direct) {
+        if (direct) {
+            CopyJobs out_jobs{};
+            out_jobs.src[0] = reinterpret_cast<const uint4 *>(s + oo);
+            out_jobs.dst[0] = static_cast<uint4 *>(dO);
+            out_jobs.units[0] = bq / 16;
+            if ((e = launch_copy(out_jobs, plan->info.num_sms, pdl, st)) != cudaSuccess)
+                return cuda_fail(e, "launch mg_copy_units (device to host)");
+        } else if ((e = cudaMemcpyAsync(hO, s + oo, bq, cudaMemcpyDeviceToHost, st)) != cudaSuccess) {
+            return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+        }
     }
+    // What the next call on this stream must not load early: hO, by its host and device addresses.
+    record_outputs(st, hO, bq, direct ? dO : nullptr, bq);
     return MG_OK;
 }
 
@@ -1075,6 +1142,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         if (e != cudaSuccess)
             return cuda_fail(e, "launch mg_attn_combine");
     }
+    record_outputs(cfg.stream, O, static_cast<size_t>(B * M * d) * 2, nullptr, 0);
     return MG_OK;
 }
 

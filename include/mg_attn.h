@@ -200,11 +200,13 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
  * Page-locked host buffers that the device can address (cudaHostAlloc / pinned tensors,
  * 16-byte aligned) are read by a copy kernel through their device addresses, chained to the
  * attention kernels with programmatic dependent launch. That kernel loads the inputs as soon as
- * it starts, which can be while the previous kernels on `stream` still run (this library's
- * kernels release their dependents early), and stores them into the staging only after those
- * kernels end: so the inputs must hold their final values when the call is made, and no kernel
- * enqueued before it may write them (O of an earlier call may: when hO shares bytes with an
- * input, the loads wait for the earlier kernels). When the plan splits N
+ * it starts, which can be while the previous kernel on `stream` still runs (this library's
+ * kernels release their dependents early), and stores them into the staging only after that
+ * kernel ends. So the inputs must hold their final values when the call is made, and no kernel
+ * enqueued before it may write them, except as the output of an earlier call of this library on
+ * the same stream (O of mg_attn_run or mg_attn_run_noalloc, hO of mg_attn_run_host): when an
+ * input shares bytes with the previous call's output on that stream, or with this call's hO, the
+ * loads wait for the previous kernel. When the plan splits N
  * (info.n_split > 1) the kernels write O straight into such a host buffer, and otherwise a
  * second copy kernel writes it back. Other host memory (pageable) goes through cudaMemcpyAsync. The plan's device staging buffers (the size of
  * Q, K, V and O) are allocated by the first call on that plan and reused after, so one

@@ -1,0 +1,144 @@
+"""Protocol model of the host-buffer entry point's launches (mg_attn_run_host), for CPU tests.
+
+Each call enqueues on one stream a copy kernel (pinned host inputs -> the plan's device staging)
+and the attention kernel (staging -> O, written straight into the pinned output). Both are
+launched with programmatic dependent launch: a kernel may start once every CTA of the kernel
+before it has released its dependents (griddepcontrol.launch_dependents), and it passes its own
+griddepcontrol.wait only once that kernel has completed, with its memory visible; a kernel
+completes only after its own wait, so the completions stay in stream order.
+
+    copy kernel, early form:  load the inputs; wait; release dependents; store them into staging
+    copy kernel, late form:   wait; release dependents; load the inputs; store them into staging
+    attention kernel:         wait; release dependents; read staging; write O
+
+The early form is used unless an input shares bytes with the call's own O or with the previous
+call's O on the stream (what the previous kernel may still be writing). The host writes a call's inputs
+before it enqueues the call. The scheduler interleaves the kernels' steps at random within those
+rules and checks every read: staging is read only after the copy that filled it for this call
+has completed, staging is not overwritten while an earlier call still reads it, and every input
+read sees the value the host wrote for that call (an input that is an earlier call's O must be
+read after that call's attention kernel wrote it).
+"""
+
+from __future__ import annotations
+
+import random
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class StreamSim:
+    def __init__(self, calls, seed: int, mutations=()):
+        """calls: list of (inputs, output) buffer names, e.g. [("x0", "o0"), ("o0", "o1")] (the
+        second call reads the first call's output: in place)."""
+        self.calls = calls
+        self.rng = random.Random(seed)
+        self.mut = set(mutations)
+        self.version = {}        # buffer -> which call's value it holds ("host" for host-written inputs)
+        self.staging = None      # (call, complete) of the staged inputs
+        self.staging_readers = set()
+        self.kernels = []        # in stream order: dicts with name, state
+        for k, (inp, out) in enumerate(calls):
+            # The entry point's rule: load early unless the input is this call's output or the
+            # previous call's output on the stream (mutations: no rule, or the own output only).
+            prev_out = calls[k - 1][1] if k > 0 else None
+            if "early_despite_alias" in self.mut:
+                early = True
+            elif "alias_own_only" in self.mut:
+                early = inp != out
+            else:
+                early = inp != out and inp != prev_out
+            self.kernels.append({"name": f"copy{k}", "call": k, "kind": "copy", "early": early,
+                                 "inp": inp, "out": out})
+            self.kernels.append({"name": f"attn{k}", "call": k, "kind": "attn", "inp": inp, "out": out})
+        for kern in self.kernels:
+            kern.update(started=False, triggered=False, waited=False, done=False)
+        # the host wrote every call's inputs before enqueueing it; an input that is an earlier call's
+        # output is expected to hold that call's value
+        self.expect = {}
+        writer = {}
+        for k, (inp, out) in enumerate(calls):
+            self.expect[k] = writer.get(inp, "host")
+            writer[out] = k
+        for inp, _ in calls:
+            self.version.setdefault(inp, "host")
+
+    # ---------------------------------------------------------------- kernel bodies
+    def _prev(self, i):
+        return self.kernels[i - 1] if i > 0 else None
+
+    def _may_start(self, i):
+        prev = self._prev(i)
+        return prev is None or prev["triggered"] or prev["done"]
+
+    def _may_pass_wait(self, i):
+        prev = self._prev(i)
+        return prev is None or prev["done"]
+
+    def _store(self, k, loaded):
+        if loaded != self.expect[k]:
+            raise ProtocolError(f"copy{k} loaded an input holding {loaded!r}, not {self.expect[k]!r}")
+        if self.staging_readers:
+            raise ProtocolError(f"copy{k} overwrites staging while {sorted(self.staging_readers)} read it")
+        self.staging = (k, False)
+
+    def body(self, i):
+        kern = self.kernels[i]
+        while not self._may_start(i):
+            yield
+        kern["started"] = True
+        k = kern["call"]
+        if kern["kind"] == "copy":
+            loaded = None
+            if kern["early"]:
+                loaded = self.version.get(kern["inp"])
+                yield
+            if "store_before_wait" in self.mut and loaded is not None:
+                self._store(k, loaded)
+                yield
+            while not self._may_pass_wait(i):
+                yield
+            kern["waited"] = True
+            kern["triggered"] = True
+            yield
+            if loaded is None:
+                loaded = self.version.get(kern["inp"])
+                yield
+            if "store_before_wait" not in self.mut or not kern["early"]:
+                self._store(k, loaded)
+                yield
+            self.staging = (k, True)
+        else:
+            if "attn_no_wait" in self.mut:
+                kern["triggered"] = True
+            else:
+                while not self._may_pass_wait(i):
+                    yield
+                kern["waited"] = True
+                kern["triggered"] = True
+            yield
+            if self.staging != (k, True):
+                raise ProtocolError(f"attn{k} reads staging holding {self.staging!r}")
+            self.staging_readers.add(k)
+            yield
+            self.staging_readers.discard(k)
+            self.version[kern["out"]] = k
+        if "attn_no_wait" in self.mut and kern["kind"] == "attn":
+            while not self._may_pass_wait(i):  # completion still in stream order
+                yield
+        kern["done"] = True
+
+    # ---------------------------------------------------------------- scheduler
+    def run(self, max_steps: int = 100000):
+        actors = {i: self.body(i) for i in range(len(self.kernels))}
+        for _ in range(max_steps):
+            if not actors:
+                return self
+            i = self.rng.choice(list(actors))
+            try:
+                next(actors[i])
+            except StopIteration:
+                del actors[i]
+        raise ProtocolError(f"deadlock: {sorted(self.kernels[i]['name'] for i in actors)}")

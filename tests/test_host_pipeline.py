@@ -1,0 +1,56 @@
+"""CPU checks of the host-buffer entry point's launch protocol through its model
+(tests/stream_model.py): back-to-back calls, in-place chains, and planted orderings that break it."""
+
+import itertools
+
+import pytest
+
+from tests import stream_model as sm
+
+CHAINS = {
+    "distinct": [("x0", "o0"), ("x1", "o1"), ("x2", "o2"), ("x3", "o3")],
+    "same_buffers": [("x", "o")] * 4,
+    "in_place": [("h", "h")] * 4,
+    "chained": [("x", "a"), ("a", "b"), ("b", "c"), ("c", "d")],
+}
+
+
+@pytest.mark.parametrize("chain", list(CHAINS))
+def test_launch_protocol_as_built_is_clean(chain):
+    for seed in range(300):
+        sm.StreamSim(CHAINS[chain], seed).run()
+
+
+def caught(chain, mutation, tries=600):
+    for seed in range(tries):
+        try:
+            sm.StreamSim(CHAINS[chain], seed, mutations=(mutation,)).run()
+        except sm.ProtocolError as e:
+            return str(e)
+    return None
+
+
+def test_early_loads_need_the_alias_rule():
+    # The next call's copy kernel loads its inputs before the previous call's attention kernel has
+    # finished: an input that is that call's output (O fed back in place) would be read stale.
+    # The entry point therefore keeps the loads after the wait when O shares bytes with an input.
+    msg = caught("in_place", "early_despite_alias")
+    assert msg is not None and "loaded an input" in msg
+
+
+def test_chains_need_the_previous_output_in_the_rule():
+    # A call whose input is the previous call's output (O of call k as Q of call k + 1, in other
+    # buffers than its own O) is read stale if only the call's own O is compared with its inputs;
+    # the entry point also compares them with the previous call's output on the stream.
+    msg = caught("chained", "alias_own_only")
+    assert msg is not None and "loaded an input" in msg
+    assert caught("chained", "early_despite_alias") is not None
+
+
+@pytest.mark.parametrize("mutation,expect", [
+    ("attn_no_wait", "reads staging"),            # attention before its copy completed
+    ("store_before_wait", "staging"),   # staging rewritten under (or before) the previous call's read
+])
+def test_planted_orderings_are_caught(mutation, expect):
+    msg = caught("distinct", mutation)
+    assert msg is not None and expect in msg, msg

@@ -482,6 +482,31 @@ def test_host_buffer_back_to_back_calls(kw):
     assert torch.equal(h, cur)
 
 
+@pytest.mark.parametrize("kw", [{}, {"n_split": 1}])
+def test_host_buffer_chained_calls(kw):
+    # Back to back without synchronising, each call's Q is the previous call's O in another
+    # pinned buffer: the copy kernel must not load that input before the previous call has
+    # written it (the entry point compares its inputs with the previous call's output on the
+    # stream). Compared bit for bit with the same chain run one synchronised call at a time.
+    B, M, N, d = 2, 64, 1024, 64
+    plan = mg.Plan(B, M, N, d, **kw)
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.5, seed=71)
+    hk, hv = k.pin_memory(), v.pin_memory()
+    bufs = [q.clone().pin_memory()] + [torch.full((B, M, d), float("nan"), dtype=torch.float16).pin_memory()
+                                       for _ in range(4)]
+    for i in range(4):
+        plan.run_host(bufs[i], hk, hv, bufs[i + 1])
+    torch.cuda.synchronize()
+    cur = q.clone()
+    for i in range(4):
+        hc = cur.pin_memory()
+        o = torch.full((B, M, d), float("nan"), dtype=torch.float16).pin_memory()
+        plan.run_host(hc, hk, hv, o)
+        torch.cuda.synchronize()
+        assert torch.equal(o, bufs[i + 1]), f"call {i} of the chain"
+        cur = o.clone()
+
+
 def test_host_buffer_entry_point_pageable_and_large():
     # Pageable host tensors take the copy-engine path; pinned ones the mapped-copy kernels. Both
     # on a shape with a split combine and several copy rounds per thread.
