@@ -35,7 +35,11 @@ from __future__ import annotations
 
 import random
 
-PLAIN, SAFE, QKNORM = 0, 1, 2
+PLAIN, SAFE, QKNORM, ONLINE = 0, 1, 2, 3
+# ONLINE: the few-row kernel's max-subtracted form, in one pass. The protocol is the graph as
+# written's, plus per tile t a rescale of the group's own O accumulator (O_g, g = t % 2) by the
+# change of its running maxima, after the P.V product of the group's previous tile (t - 2) has
+# completed and before P of tile t is announced.
 GROUP_WARPS = 4
 
 
@@ -82,8 +86,9 @@ class Sim:
         if T < 1 or stages < 2 or pbufs < 2:
             raise ValueError("T >= 1, stages >= 2, pbufs >= 2")
         self.T, self.S, self.P, self.var = T, stages, pbufs, variant
-        self.safe = variant != PLAIN
+        self.safe = variant in (SAFE, QKNORM)
         self.qk = variant == QKNORM
+        self.online = variant == ONLINE
         self.T1 = T if self.safe else 0
         self.U = self.T1 + T
         self.mut = set(mutations)
@@ -122,6 +127,8 @@ class Sim:
         self.p_tile_writing = [None] * pbufs
         self.p_readers = [0] * pbufs
         self.pv_done = 0
+        self.pv_completed = set()           # tiles whose P.V product has completed
+        self.o_rescaled = {0: set(), 1: set()}  # group -> tiles at which its O was rescaled
         self.pv_issued = 0
         self.scale_parts = {}               # QK-norm: tile -> softmax warps that wrote its key scales
         self.tma = []                       # in-flight copies: (barrier, bytes, effect)
@@ -268,6 +275,7 @@ class Sim:
             self.p_readers[pb] -= 1
             self.v_readers[s] -= 1
             self.pv_done += 1
+            self.pv_completed.add(v)
 
         self.pipe.append(("mma", done))
         self.pipe.append(("commit", f"KvEmpty{s}"))
@@ -337,6 +345,14 @@ class Sim:
             yield ("do", lambda u=u: self._read_s(g, u, -1))            # half 1 loaded: S released
             yield ("do", lambda: self.bars[f"SEmpty{g}"].arrive())
             yield ("do", lambda t=t, pb=pb: self._write_p(pb, t, (gw, 1)))
+            if self.online and t >= 2:
+                # Rescale O_g once P.V of this group's previous tile has completed.
+                q = t - 2
+                if "online_no_rescale_wait" not in self.mut:
+                    if not (yield self.wait(f"PEmpty{q % P}", (q // P) & 1, q // P, f"{who} O rescale {t}")):
+                        ok = False
+                        break
+                yield ("do", lambda g=g, t=t: self._rescale_o(g, t))
             yield ("do", lambda pb=pb: self.bars[f"PFull{pb}"].arrive())
             u += 2
         # Epilogue: a vote on "O is ready" that every softmax warp takes part in.
@@ -344,6 +360,14 @@ class Sim:
         o_ready = yield ("gbar", "softmax", 2 * GROUP_WARPS, o_ok)
         if o_ready:
             yield ("do", lambda: self._read_o())
+
+    def _rescale_o(self, g, t):
+        if self.abort:
+            return
+        missing = [q for q in range(g, t, 2) if q not in self.pv_completed]
+        if missing:
+            self.fail(f"group {g} rescales its O at tile {t} while P.V of tile {missing[0]} is in flight")
+        self.o_rescaled[g].add(t)
 
     def _read_k(self, s, u, delta):
         if delta > 0 and self.kst[s] != u and not self.abort:

@@ -191,3 +191,29 @@ def test_segment_unwinding_from_any_wait_is_clean():
     for segs, (stages, pbufs), seed in itertools.product(([2, 1], [1, 2], [3, 4], [1, 1], [4]), [(6, 3), (3, 2)],
                                                          range(12)):
         pm.SegmentSim(segs, stages, pbufs, seed, abort_rate=0.02).run()
+
+
+# ------------------------------------------------------------------ few-row kernel, one-pass max-subtracted
+
+@pytest.mark.parametrize("stages,pbufs", [(3, 3), (2, 3)])
+def test_online_protocol_as_built_is_clean(stages, pbufs):
+    # The graph as written's protocol plus, per tile, the group's rescale of its own O after the
+    # P.V product of its previous tile (a wait on that tile's P-buffer barrier).
+    for T, seed in itertools.product((1, 2, 3, 4, 7, 12), range(12)):
+        pm.Sim(T, stages, pbufs, pm.ONLINE, seed).run()
+
+
+def test_online_rescale_needs_its_wait():
+    hit = None
+    for T, (stages, pbufs), seed in itertools.product((3, 5, 8), [(3, 3), (2, 3)], range(60)):
+        try:
+            pm.Sim(T, stages, pbufs, pm.ONLINE, seed, mutations=("online_no_rescale_wait",)).run()
+        except pm.ProtocolError as e:
+            hit = str(e)
+            break
+    assert hit is not None and "rescales its O" in hit
+
+
+def test_online_unwinding_from_any_wait_is_clean():
+    for T, (stages, pbufs), seed in itertools.product((1, 2, 3, 5, 8), [(3, 3), (2, 3)], range(12)):
+        pm.Sim(T, stages, pbufs, pm.ONLINE, seed, abort_rate=0.02).run()
