@@ -112,12 +112,13 @@ FwdKernel pair_kernel(int stages)
     }
 }
 
-// The few-row specialisation (head dim 128, transposed products) for a pipeline depth.
-FwdKernel swap_kernel(int stages)
+// The few-row specialisation (head dim 128, transposed products) for a pipeline depth; `online`:
+// its one-pass max-subtracted form.
+FwdKernel swap_kernel(int stages, bool online)
 {
     switch (stages) {
-    case 2: return mg::mg_attn_fwd_swap<2>;
-    case 3: return mg::mg_attn_fwd_swap<3>;
+    case 2: return online ? mg::mg_attn_fwd_swap<2, true> : mg::mg_attn_fwd_swap<2>;
+    case 3: return online ? mg::mg_attn_fwd_swap<3, true> : mg::mg_attn_fwd_swap<3>;
     default: return nullptr;
     }
 }
@@ -293,10 +294,12 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
             stream_k = false, n_split = one_wave(units);
     }
     // The few-row specialisation: head dim 128, at most 16 query rows per batch, the graph as
-    // written under the split schedule; the default there (measured on GB300, us per call against
-    // the one-tile kernel: (16, 8, 32768, 128) 45.8 against 48.2, (64, 1, 4096, 128) 25.2 against 26.9).
-    const bool swap = !pair && !stream_k && d == 128 && M <= mg::kSwapNQ &&
-                      !(o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) && !(o.flags & MG_FLAG_NO_SWAP_AB);
+    // written or its max-subtracted evaluation (in one pass there), under the split schedule; the
+    // default there (measured on GB300, us per call against the one-tile kernel: (16, 8, 32768,
+    // 128) 45.8 against 48.2, (64, 1, 4096, 128) 25.2 against 26.9).
+    const bool swap = !pair && !stream_k && d == 128 && M <= mg::kSwapNQ && !(o.flags & MG_FLAG_QK_NORM) &&
+                      !(o.flags & MG_FLAG_NO_SWAP_AB);
+    const bool safe = (o.flags & MG_FLAG_SAFE_SOFTMAX) != 0;
     // The few-row kernel combines on chip too (fp32 partials; measured on GB300 for (64, 1, 4096,
     // 128), 2 splits: 24.3 us per call against 25.1 with the second kernel).
     const bool cluster =
@@ -322,11 +325,11 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
             push = false;
     }
     const uint32_t smem = pair   ? mg::pair_smem_bytes(stages)
-                          : swap ? mg::swap_smem_bytes(stages)
+                          : swap ? mg::swap_smem_bytes(stages, safe)
                                  : mg::fwd_smem_bytes(static_cast<int>(d), stages, push);
     if (static_cast<int64_t>(smem) > max_smem ||
         !(pair ? pair_kernel(stages)
-               : swap ? swap_kernel(stages)
+               : swap ? swap_kernel(stages, safe)
                       : stream_k ? sk_kernel(d, stages) : push ? push_kernel(stages) : fwd_kernel(d, stages, o.flags)))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
@@ -378,7 +381,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
 FwdKernel plan_kernel(const mg_attn_plan_info &info, int flags)
 {
     if (info.swap_ab == 1)
-        return swap_kernel(info.stages);
+        return swap_kernel(info.stages, (flags & MG_FLAG_SAFE_SOFTMAX) != 0);
     if (info.schedule == 1)
         return sk_kernel(info.d, info.stages);
     if (info.xchg_push == 1)

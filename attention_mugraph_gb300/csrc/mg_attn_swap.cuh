@@ -20,6 +20,19 @@
 // P lives in shared memory, written by the softmax warps and read by the tensor core after a proxy
 // fence. Split partials (fp32 O^T columns and row sums) are combined on chip when the n_split CTAs
 // of a batch run as one thread-block cluster, else by the second kernel.
+//
+// ONLINE: the max-subtracted evaluation in one pass over K and V (each query row's maximum is not
+// known before the last tile, so it is kept running). Each softmax group keeps its own running
+// maximum m[q] and its own O^T accumulator (tensor-memory columns 32 and 48). Per tile the group
+// finds the tile's maximum of every query over its 128 keys (a warp reduction, then the four warps'
+// results through shared memory and a group barrier). Where some query's tile maximum exceeds m[q]
+// by more than kSwapRescaleSlack, it raises every m[q] to its tile maximum (if larger) and scales
+// its partial sums by alpha[q] = exp(m_old - m_new), and also its O^T accumulator, in tensor memory,
+// once the tensor core has finished the group's previous P.V (its P buffer released) and before it
+// publishes the new P^T. It writes P^T = exp(S^T - m); the CPU model of this
+// protocol is tests/pipeline_model.py's ONLINE variant. The epilogue merges the two groups (weights
+// exp(m_g - max m)); split partials carry their maximum to the combine, which weights them the same
+// way. The result equals the graph as written, exp(S) / rowsum(exp(S)) . V, up to rounding.
 #pragma once
 
 #include "mg_attn_kernels.cuh"
@@ -33,18 +46,55 @@ constexpr uint32_t kSwapChunk = kSwapNQ * 128;                   // one such chu
 constexpr uint32_t kSwapStageBytes = 2u * kSwapD * kBlockN * 2;  // K + V tile
 constexpr uint32_t kSwapPBytes = kSwapNQ * kBlockN * 2;          // P^T: two 64-key chunks of 16 rows
 constexpr int kSwapPBuffers = 3;
-constexpr uint32_t kSwapTmemCols = 64;                           // S^T buffers at 0 and 16, O^T at 32
+constexpr uint32_t kSwapTmemCols = 64;                           // S^T buffers at 0 and 16, O^T at 32 (and 48)
 constexpr uint32_t kSwapTmemO = 32;
+// ONLINE: per group, two buffers of the four warps' tile maxima, and group 1's final maxima.
+constexpr uint32_t kSwapOnlineBytes = (2 * 2 * kGroupWarps * kSwapNQ + kSwapNQ) * 4;
+// ONLINE: a group keeps the maximum it subtracts until some query's tile maximum exceeds it by
+// more than this; any per-row shift cancels in the normalisation, and the scores stay at most 8
+// above the subtracted value, so P <= e^8 ~ 2981 (fp16 keeps its relative precision up to 65504).
+// The rescale then runs on a group's first tiles and on jumps, not on every small rise.
+constexpr float kSwapRescaleSlack = 8.0f;
 
-// Shared-memory bytes: alignment slack, Q^T, the P^T ring, the K/V ring, the per-warp row sums and
-// the barriers.
-__host__ __device__ constexpr uint32_t swap_smem_bytes(int stages)
+// Shared-memory bytes: alignment slack, Q^T, the P^T ring, the K/V ring, the per-warp row sums,
+// (ONLINE) the maxima exchanged between warps, and the barriers.
+__host__ __device__ constexpr uint32_t swap_smem_bytes(int stages, bool online = false)
 {
     return 1024u + kSwapQBytes + kSwapPBuffers * kSwapPBytes + static_cast<uint32_t>(stages) * kSwapStageBytes +
-           kSoftmaxWarps * kSwapNQ * 4 + 512u;
+           kSoftmaxWarps * kSwapNQ * 4 + (online ? kSwapOnlineBytes : 0u) + 512u;
 }
 
-template <int STAGES>
+// Warp-collective: lane i writes tensor-memory lane (taddr.lane + i), 16 consecutive 32-bit
+// columns starting at taddr.col. Complete (and the registers reusable) after tmem_st_wait().
+__device__ __forceinline__ void swap_tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+// The maximum over the warp's 32 lanes of each of 16 values v[0..15], in 16 shuffles: at each step
+// a lane keeps the half of its values that its lane bit selects and takes the maximum with the
+// partner lane's copy of that half (the other half is what it sends). Lane L returns the maximum
+// of value (L >> 1) & 15. v is overwritten.
+__device__ __forceinline__ float warp_max16(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int w = 8, bit = 16; w >= 1; w >>= 1, bit >>= 1) {
+        const bool hi = (lane & bit) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = hi ? v[i] : v[i + w];
+            const float keep = hi ? v[i + w] : v[i];
+            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, bit));
+        }
+    }
+    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+}
+
+template <int STAGES, bool ONLINE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     mg_attn_fwd_swap(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -52,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     constexpr int D = kSwapD;
     using BI = Bars<STAGES, kSwapPBuffers>;
-    static_assert(swap_smem_bytes(STAGES) <= 232448u, "tile configuration exceeds 227 KB");
+    static_assert(swap_smem_bytes(STAGES, ONLINE) <= 232448u, "tile configuration exceeds 227 KB");
     (void)tmO;
     (void)tmW;
 
@@ -62,7 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sP0 = sQ + kSwapQBytes;                        // P^T buffer pb at sP0 + pb * kSwapPBytes
     const uint32_t sStage0 = sP0 + kSwapPBuffers * kSwapPBytes;   // 1024-aligned: 4 KB steps so far
     float *l_red = reinterpret_cast<float *>(smem + kSwapQBytes + kSwapPBuffers * kSwapPBytes + STAGES * kSwapStageBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(l_red + kSoftmaxWarps * kSwapNQ);
+    float *m_red = l_red + kSoftmaxWarps * kSwapNQ;           // ONLINE: [group][buffer][warp][query]
+    float *m_fin = m_red + 2 * 2 * kGroupWarps * kSwapNQ;     // ONLINE: group 1's final maxima
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ONLINE ? m_fin + kSwapNQ : m_red);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
@@ -234,12 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t a_v =
                 ptx::sdesc_sw128(sStage0 + s * kSwapStageBytes + D * kBlockN * 2, TileCfg<D>::kChunkRows128, 1024);
             const uint32_t sP = sP0 + pb * kSwapPBytes;
+            // ONLINE: tile v accumulates into its group's O^T (columns 32 + 16 (v mod 2)), from its
+            // group's first tile on.
+            const uint32_t o_col = ONLINE ? kSwapTmemO + (v & 1) * kSwapNQ : kSwapTmemO;
+            const int first = ONLINE ? 2 : 1;
             if (ptx::elect_one()) {
 #pragma unroll
                 for (int k = 0; k < kBlockN / 16; ++k)
-                    ptx::mma_f16_ss(tmem + kSwapTmemO, a_v + static_cast<uint64_t>(k * (2048 >> 4)),
+                    ptx::mma_f16_ss(tmem + o_col, a_v + static_cast<uint64_t>(k * (2048 >> 4)),
                                     ptx::sdesc_sw128(sP + (k >> 2) * kSwapChunk + (k & 3) * 32, 16, 1024), idesc_o,
-                                    (v > 0 || k > 0) ? 1u : 0u);
+                                    (v >= first || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
                 if (v == T - 1)
@@ -277,6 +333,153 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T element (query q, key) in its buffer: 64-key chunk, row q, the 128-byte swizzle.
         const uint32_t p_off = (key / 64) * kSwapChunk + (((static_cast<uint32_t>(key % 64) / 8) << 4) | ((key % 8) * 2));
         bool ok = true;
+        float mrun[kSwapNQ];  // ONLINE: the group's running maximum of each query row
+#pragma unroll
+        for (int q = 0; q < kSwapNQ; ++q)
+            mrun[q] = -INFINITY;
+        if constexpr (ONLINE) {
+            const int wq = sw & 3;  // warp within the group
+            float *m_red_g = m_red + g * 2 * kGroupWarps * kSwapNQ;
+            // Barrier ids stay compile-time constants (one branch per group).
+            auto group_barrier_and = [&](bool pred) {
+                return g == 0 ? ptx::named_barrier_and(kGroupBarrier0, kGroupWarps * 32, pred)
+                              : ptx::named_barrier_and(kGroupBarrier0 + 1, kGroupWarps * 32, pred);
+            };
+            auto group_barrier_or = [&](bool pred) {
+                return g == 0 ? ptx::named_barrier_or(kGroupBarrier0, kGroupWarps * 32, pred)
+                              : ptx::named_barrier_or(kGroupBarrier0 + 1, kGroupWarps * 32, pred);
+            };
+            // exp(s - m) for queries q and q + 1 as one packed multiply-add: -m log2(e) in each half.
+            uint64_t shift[kSwapNQ / 2];
+#pragma unroll
+            for (int q = 0; q < kSwapNQ / 2; ++q)
+                shift[q] = 0;
+            // Every warp of the group takes the same group barriers per tile, so all run the same
+            // iterations: a failed wait clears `ok`, and the next barriers (or the epilogue's) stop
+            // the others too.
+            for (int u = g; u < T; u += 2) {
+                const int pb = u % kSwapPBuffers;
+                const int mb = (u >> 1) & 1;  // buffer of the tile maxima
+                const bool valid = tile_of(u) * kBlockN + key < p.N;  // keys past N weigh 0
+                uint32_t r[kSwapNQ];
+                bool w_ok = ok && warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);
+                bool over = false;  // a score of this warp past its row's maximum by more than the slack
+                if (w_ok) {
+                    ptx::tc_fence_after();
+                    ptx::tmem_ld_32x32b_x16(tmem + lane_addr + g * kSwapNQ, r);
+                    ptx::tmem_ld_wait16(r);
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bar(BI::kSEmpty + g));
+#pragma unroll
+                    for (int q = 0; q < kSwapNQ; ++q)
+                        over |= valid && __uint_as_float(r[q]) > mrun[q] + kSwapRescaleSlack;
+                    over = __any_sync(0xffffffffu, over);
+                }
+                // One group barrier per tile tells every warp whether some warp failed a wait or
+                // must raise the maximum (always on the group's first tile: m = -inf). Only then
+                // do the tile's maxima go through shared memory, behind a second barrier.
+                float alpha[kSwapNQ];
+                bool changed = false;
+                if (group_barrier_or(!w_ok || over)) {
+                    if (w_ok) {
+                        float t[kSwapNQ];
+#pragma unroll
+                        for (int q = 0; q < kSwapNQ; ++q)
+                            t[q] = valid ? __uint_as_float(r[q]) : -INFINITY;
+                        const float wmax = warp_max16(t, lane);
+                        if ((lane & 1) == 0)
+                            m_red_g[(mb * kGroupWarps + wq) * kSwapNQ + (lane >> 1)] = wmax;
+                    }
+                    if (!group_barrier_and(w_ok)) {
+                        ok = false;
+                        break;
+                    }
+                    // The tile's maximum of every query over the group's 128 keys (at least one key
+                    // of a tile is below N, so it is finite), and the new maxima.
+#pragma unroll
+                    for (int q = 0; q < kSwapNQ; ++q)
+                        alpha[q] = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < kGroupWarps; ++w) {
+                        const float4 *row =
+                            reinterpret_cast<const float4 *>(m_red_g + (mb * kGroupWarps + w) * kSwapNQ);
+#pragma unroll
+                        for (int k = 0; k < kSwapNQ / 4; ++k) {
+                            const float4 x = row[k];
+                            alpha[4 * k + 0] = fmaxf(alpha[4 * k + 0], x.x);
+                            alpha[4 * k + 1] = fmaxf(alpha[4 * k + 1], x.y);
+                            alpha[4 * k + 2] = fmaxf(alpha[4 * k + 2], x.z);
+                            alpha[4 * k + 3] = fmaxf(alpha[4 * k + 3], x.w);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < kSwapNQ; ++q)
+                        changed |= alpha[q] > mrun[q] + kSwapRescaleSlack;
+                    if (changed) {  // the same on every thread of the group
+#pragma unroll
+                        for (int q = 0; q < kSwapNQ; ++q) {
+                            const float mn = fmaxf(mrun[q], alpha[q]);
+                            alpha[q] = ptx::ex2_approx((mrun[q] - mn) * ptx::kLog2e);  // 0 on the first tile
+                            lq[q] *= alpha[q];
+                            mrun[q] = mn;
+                        }
+#pragma unroll
+                        for (int q = 0; q < kSwapNQ; q += 2)
+                            shift[q / 2] = (static_cast<uint64_t>(__float_as_uint(-mrun[q + 1] * ptx::kLog2e)) << 32) |
+                                           __float_as_uint(-mrun[q] * ptx::kLog2e);
+                    }
+                }
+                if (u >= kSwapPBuffers &&
+                    !warp_wait(bar(BI::kPEmpty + pb), (static_cast<uint32_t>(u / kSwapPBuffers) & 1u) ^ 1u,
+                               BI::kPEmpty + pb))
+                    ok = false;
+                if (ok) {
+                    uint8_t *pt = smem + kSwapQBytes + pb * kSwapPBytes;
+#pragma unroll
+                    for (int q = 0; q < kSwapNQ; q += 2) {
+                        uint32_t e0, e1;
+                        ptx::exp_pair_mufu(r[q], r[q + 1], ek, shift[q / 2], e0, e1);
+                        e0 = valid ? e0 : 0u;
+                        e1 = valid ? e1 : 0u;
+                        lq[q] += __uint_as_float(e0);
+                        lq[q + 1] += __uint_as_float(e1);
+                        *reinterpret_cast<__half *>(pt + (p_off ^ ((q & 7) << 4)) + q * 128) =
+                            __float2half_rn(__uint_as_float(e0));
+                        *reinterpret_cast<__half *>(pt + (p_off ^ (((q + 1) & 7) << 4)) + (q + 1) * 128) =
+                            __float2half_rn(__uint_as_float(e1));
+                    }
+                }
+                // Rescale the group's O^T (its lanes = output columns, its columns = queries) once
+                // the tensor core has finished the group's previous P.V, before this tile's P.V.
+                if (ok && changed && u >= 2) {
+                    const int q2 = u - 2;
+                    if (warp_wait(bar(BI::kPEmpty + q2 % kSwapPBuffers),
+                                  static_cast<uint32_t>(q2 / kSwapPBuffers) & 1u, BI::kPEmpty + q2 % kSwapPBuffers)) {
+                        ptx::tc_fence_after();
+                        uint32_t o[kSwapNQ];
+                        const uint32_t taddr = tmem + lane_addr + kSwapTmemO + g * kSwapNQ;
+                        ptx::tmem_ld_32x32b_x16(taddr, o);
+                        ptx::tmem_ld_wait16(o);
+#pragma unroll
+                        for (int q = 0; q < kSwapNQ; ++q)
+                            o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha[q]);
+                        swap_tmem_st_x16(taddr, o);
+                        ptx::tmem_st_wait();
+                    } else {
+                        ok = false;
+                    }
+                }
+                if (ok) {
+                    ptx::fence_proxy_async_smem();  // the tensor core reads P^T through the async proxy
+                    ptx::tc_fence_before();         // and the rescaled O^T after the arrival
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bar(BI::kPFull + pb));
+                }
+            }
+        } else {
         for (int u = g; ok && u < T; u += 2) {
             const int pb = u % kSwapPBuffers;
             if (!warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g)) {
@@ -317,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0)
                 ptx::mbar_arrive(bar(BI::kPFull + pb));
         }
+        }
 
         // ------------------------------------------------------------ epilogue
         // Row sums: each warp adds its 32 keys' parts (the same butterfly order on every lane), the
@@ -331,39 +535,79 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < kSwapNQ; ++q)
                 l_red[sw * kSwapNQ + q] = lq[q];
+            if (ONLINE && sw == kGroupWarps) {  // group 1's maxima, for group 0's merge
+#pragma unroll
+                for (int q = 0; q < kSwapNQ; ++q)
+                    m_fin[q] = mrun[q];
+            }
         }
         const bool o_ready = ptx::named_barrier_and(kSoftmaxBarrier, kSoftmaxThreads,
                                                     ok && warp_wait(bar(BI::kOFull), 0, BI::kOFull));
         float *stage_o = reinterpret_cast<float *>(smem + (sStage0 - sQ));  // [16][128]
         float *stage_l = stage_o + kSwapNQ * D;                                // [16]
+        float *stage_m = stage_l + kSwapNQ;                                    // [16] (ONLINE)
         if (o_ready && g == 0) {
             // O^T lanes are output columns: the four warps of group 0 cover all 128.
             ptx::tc_fence_after();
             uint32_t o[kSwapNQ];
             ptx::tmem_ld_32x32b_x16(tmem + lane_addr + kSwapTmemO, o);
             ptx::tmem_ld_wait16(o);
+            // ONLINE: group 1's accumulator (written only when the CTA has a second tile).
+            const bool two = ONLINE && T >= 2;
+            uint32_t o1[kSwapNQ];
+            if (two) {
+                ptx::tmem_ld_32x32b_x16(tmem + lane_addr + kSwapTmemO + kSwapNQ, o1);
+                ptx::tmem_ld_wait16(o1);
+            }
             const int c = q4 * 32 + lane;  // output column
             const int mq = p.M < kSwapNQ ? p.M : kSwapNQ;
 #pragma unroll
             for (int q = 0; q < kSwapNQ; ++q) {
                 if (q < mq) {
                     float l = 0.f;
+                    float ov = __uint_as_float(o[q]);
+                    float m = 0.f;
+                    if constexpr (ONLINE) {
+                        // Both groups' parts relative to the larger of their maxima.
+                        float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kSoftmaxWarps; ++w)
-                        l += l_red[w * kSwapNQ + q];
+                        for (int w = 0; w < kGroupWarps; ++w) {
+                            l0 += l_red[w * kSwapNQ + q];
+                            l1 += l_red[(kGroupWarps + w) * kSwapNQ + q];
+                        }
+                        m = two ? fmaxf(mrun[q], m_fin[q]) : mrun[q];
+                        const float w0 = ptx::ex2_approx((mrun[q] - m) * ptx::kLog2e);
+                        l = l0 * w0;
+                        ov *= w0;
+                        if (two) {
+                            const float w1 = ptx::ex2_approx((m_fin[q] - m) * ptx::kLog2e);
+                            l = fmaf(l1, w1, l);
+                            ov = fmaf(__uint_as_float(o1[q]), w1, ov);
+                        }
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < kSoftmaxWarps; ++w)
+                            l += l_red[w * kSwapNQ + q];
+                    }
                     if (p.n_split == 1) {
-                        p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(__uint_as_float(o[q]) * __frcp_rn(l));
+                        p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(ov * __frcp_rn(l));
                     } else if (p.cluster_reduce) {
                         // Staged for the cluster's owners (the K/V ring is idle): O^T column c of
-                        // query q, fp32, and the row sum of q.
-                        stage_o[q * D + c] = __uint_as_float(o[q]);
-                        if (c == 0)
+                        // query q, fp32, the row sum of q and (ONLINE) the maximum they are relative to.
+                        stage_o[q * D + c] = ov;
+                        if (c == 0) {
                             stage_l[q] = l;
+                            if (ONLINE)
+                                stage_m[q] = m;
+                        }
                     } else {
                         const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + q;
-                        p.ws_o[r * D + c] = __uint_as_float(o[q]);
-                        if (c == 0)
+                        p.ws_o[r * D + c] = ov;
+                        if (c == 0) {
                             p.ws_l[r] = l;
+                            if (ONLINE)
+                                p.ws_m[r] = m;
+                        }
                     }
                 }
             }
@@ -386,9 +630,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int mq = p.M < kSwapNQ ? p.M : kSwapNQ;
             const uint32_t so = ptx::smem_u32(smem) + (sStage0 - sQ);
             const uint32_t sl = so + kSwapNQ * D * 4;
+            const uint32_t sm = sl + kSwapNQ * 4;
             for (int it = threadIdx.x - 64; it < mq * cols; it += kSoftmaxThreads) {
                 const int q = it / cols;
                 const int c = c_lo + it % cols;
+                // ONLINE: rank r's partial is relative to its maximum m_r; weights exp(m_r - max m).
+                float wt[kMaxClusterRanks];
+#pragma unroll
+                for (int r = 0; r < kMaxClusterRanks; ++r)
+                    wt[r] = 1.f;
+                if constexpr (ONLINE) {
+                    float mmax = -INFINITY;
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r) {
+                        if (r < n) {
+                            wt[r] = ptx::ld_cluster_f32(ptx::map_to_rank(sm + static_cast<uint32_t>(q) * 4, r));
+                            mmax = fmaxf(mmax, wt[r]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < kMaxClusterRanks; ++r)
+                        if (r < n)
+                            wt[r] = ptx::ex2_approx((wt[r] - mmax) * ptx::kLog2e);
+                }
                 float ov[kMaxClusterRanks], lv[kMaxClusterRanks];
 #pragma unroll
                 for (int r = 0; r < kMaxClusterRanks; ++r) {  // every load in flight before the sums
@@ -401,8 +665,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < kMaxClusterRanks; ++r) {
                     if (r < n) {
-                        os += ov[r];
-                        ls += lv[r];
+                        if constexpr (ONLINE) {
+                            os = fmaf(ov[r], wt[r], os);
+                            ls = fmaf(lv[r], wt[r], ls);
+                        } else {
+                            os += ov[r];
+                            ls += lv[r];
+                        }
                     }
                 }
                 p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(os * __frcp_rn(ls));

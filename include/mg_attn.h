@@ -68,12 +68,16 @@ typedef enum {
 /* Flags for mg_attn_options.flags. */
 #define MG_FLAG_NO_PDL 0x1         /* launch without programmatic dependent launch */
 #define MG_FLAG_NO_CLUSTER 0x4     /* always combine split partials with the second kernel, never on chip */
-#define MG_FLAG_SAFE_SOFTMAX 0x8   /* max-subtracted evaluation: a first pass over K finds each row's
-                                      largest score m (per split), then P = exp(A - m) and the split
+#define MG_FLAG_SAFE_SOFTMAX 0x8   /* max-subtracted evaluation: P = exp(A - m) with m a per-row shift
+                                      no smaller than the row's largest score minus 8, and the split
                                       partials combine with weights exp(m_j - max_j m_j). The result is
                                       the graph's (the normalisation cancels any per-row shift) without
-                                      the A <= ln(65504) precondition; the cost is Q.K computed twice and
-                                      K read twice. */
+                                      the A <= ln(65504) precondition. The one-tile kernel finds m (each
+                                      row's largest score per split) in a first pass over K: Q.K computed
+                                      twice and K read twice. The few-row specialisation (MG_FLAG_SWAP_AB)
+                                      keeps m running in one pass: whenever a tile's score exceeds m by
+                                      more than 8, m rises to the tile's maximum and the row's partial sum
+                                      and O accumulator are scaled by exp(m_old - m_new). */
 #define MG_FLAG_QK_NORM 0x10       /* QK-norm attention (Mirage documentation, tutorials/attention-with-kv-norm):
                                       Q = rms_norm(Q), K = rms_norm(K) before the graph, each query row and
                                       each key vector K[b,:,n] normalised over d: x / sqrt(mean(x^2) + eps),
@@ -101,7 +105,8 @@ typedef enum {
                                       sums in a fixed order. Opt-in: measured on GB300 it is not faster than
                                       the default split schedule on the decode shapes; see info.schedule */
 #define MG_FLAG_NO_STREAM_K 0x100  /* the split schedule (N split n_split ways per row tile; the default) */
-#define MG_FLAG_SWAP_AB 0x200      /* few-row specialisation (the graph as written, head dim 128, at most 16
+#define MG_FLAG_SWAP_AB 0x200      /* few-row specialisation (the graph as written or its max-subtracted
+                                      evaluation in one pass, head dim 128, at most 16
                                       query rows per batch, the split schedule): per K/V tile the products run
                                       transposed, S^T = K^T Q^T and O^T += V^T P^T, so the MMA's 128 rows are
                                       keys (resp. output columns) instead of mostly-empty query rows; split

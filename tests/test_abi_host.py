@@ -204,8 +204,14 @@ def test_query_swap_ab():
     assert mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_NO_SWAP_AB)["swap_ab"] == 0
     assert mg.mg_attn_query(16, 8, 32768, 64, 152, flags=mg.MG_FLAG_SWAP_AB)["swap_ab"] == 0
     assert mg.mg_attn_query(16, 17, 32768, 128, 152, flags=mg.MG_FLAG_SWAP_AB)["swap_ab"] == 0
-    flags = mg.MG_FLAG_SWAP_AB | mg.MG_FLAG_SAFE_SOFTMAX
-    assert mg.mg_attn_query(16, 8, 32768, 128, 152, flags=flags)["swap_ab"] == 0
+    # The max-subtracted evaluation runs there in one pass (its running maxima exchanged between
+    # warps: 1088 more bytes of shared memory); QK-norm keeps the one-tile kernel.
+    safe = mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX)
+    assert safe["swap_ab"] == 1 and safe["smem_bytes"] == info["smem_bytes"] + 1088
+    assert safe["cluster_ctas"] == 8 and safe["workspace_bytes"] == 256
+    k2s = mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX | mg.MG_FLAG_NO_CLUSTER)
+    assert k2s["swap_ab"] == 1 and k2s["workspace_bytes"] == 256 + 8 * 16 * 8 * (128 + 2) * 4
+    assert mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_QK_NORM)["swap_ab"] == 0
     with pytest.raises(mg.MgAttnError):
         mg.mg_attn_query(16, 8, 32768, 128, 152, flags=mg.MG_FLAG_SWAP_AB | mg.MG_FLAG_NO_SWAP_AB)
 

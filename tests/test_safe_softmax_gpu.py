@@ -122,3 +122,87 @@ def test_bounded_wait_in_variants(flags, n_split):
     assert plan.status() == mg.MG_ERR_TIMEOUT
     O2, _ = run_gpu(q, k, v, flags=SAFE)
     assert_parity(O2, oracle.attention(q, k, v), "after timeout")
+
+
+# ---------------------------------------------------------------------------------------------
+# The few-row kernel's one-pass form (head dim 128, at most 16 rows per batch): the running
+# maximum per softmax group, the rescale of the partial sums and of the O^T accumulator when it
+# grows, the merge of the two groups, and split partials that carry their maximum.
+
+ONLINE_SHAPES = [  # (B, M, N, n_split, flags, normal draws)
+    (16, 8, 32768, 0, 0, False),                        # decode: 8-CTA clusters
+    (16, 8, 32768, 0, mg.MG_FLAG_NO_CLUSTER, False),    # the second kernel, with the maxima
+    (64, 1, 4096, 0, 0, True),                          # the launch example's draws: |A| ~ 45
+    (64, 1, 4096, 0, mg.MG_FLAG_NO_CLUSTER, True),
+    (3, 16, 1032, 1, 0, True),                          # one split: O written directly; ragged N
+    (3, 16, 384, 1, 0, False),                          # 3 tiles: group 0 takes two, group 1 one
+    (2, 1, 8, 0, 0, True),                              # one ragged tile: group 1 has none
+    (5, 3, 5000, 7, 0, True),                           # 7 ranks; ragged N
+    (5, 3, 5000, 7, mg.MG_FLAG_NO_CLUSTER, True),
+    (4, 8, 8192, 16, 0, True),                          # 16 ranks
+    (2, 5, 1032, 9, 0, False),                          # one tile per rank: no group 1 anywhere
+]
+
+
+@pytest.mark.parametrize("B,M,N,n_split,flags,normal", ONLINE_SHAPES)
+def test_online_few_row_kernel(B, M, N, n_split, flags, normal):
+    d = 128
+    if normal:
+        q, k, v = inputs.make_inputs_normal(B, M, N, d, seed=B * 11 + M + N)
+    else:
+        q, k, v = inputs.make_inputs(B, M, N, d, 0.25, seed=B * 11 + M + N)
+    O, plan = run_gpu(q, k, v, n_split=n_split, flags=SAFE | flags)
+    assert plan.info["swap_ab"] == 1
+    assert_parity(O, oracle.attention(q, k, v), f"{B, M, N, d} n_split={plan.info['n_split']} "
+                                                f"cluster={plan.info['cluster_ctas']}")
+    O2, _ = run_gpu(q, k, v, n_split=n_split, flags=SAFE | flags)
+    assert torch.equal(O, O2)
+
+
+def ramped_keys(B, M, N, rising, seed):
+    # N(0, 1) draws with key n scaled by 0.25 + 6 n / N (rising) or its reverse: the rows' maxima
+    # climb from ~13 to ~320 across the tiles, so a group's maximum jumps past the kernel's
+    # rescale slack (8) on most of its tiles (O^T rescaled in tensor memory), or on none after the
+    # first. exp(A) stays finite in the fp64 oracle (A < 709).
+    q, k, v = inputs.make_inputs_normal(B, M, N, 128, seed=seed)
+    ramp = 0.25 + 6.0 * torch.arange(N, dtype=torch.float32) / N
+    if not rising:
+        ramp = ramp.flip(0)
+    return q, (k.float() * ramp).half().contiguous(), v
+
+
+@pytest.mark.parametrize("rising", [True, False])
+@pytest.mark.parametrize("n_split,flags", [(1, 0), (0, 0), (4, mg.MG_FLAG_NO_CLUSTER)])
+def test_online_running_maximum(rising, n_split, flags):
+    B, M, N = 4, 16, 4104
+    q, k, v = ramped_keys(B, M, N, rising, seed=5)
+    ref = oracle.attention(q, k, v)
+    O, plan = run_gpu(q, k, v, n_split=n_split, flags=SAFE | flags)
+    assert plan.info["swap_ab"] == 1
+    assert_parity(O, ref, f"ramp rising={rising} n_split={plan.info['n_split']}")
+
+
+def test_online_matches_two_pass_kernel():
+    # The one-tile kernel's two-pass form (MG_FLAG_NO_SWAP_AB) on the same inputs: both within the
+    # bound of the oracle.
+    q, k, v, _ = inputs.make_config("decode_m1")
+    ref = oracle.attention(q, k, v)
+    a, pa = run_gpu(q, k, v, flags=SAFE)
+    b, pb = run_gpu(q, k, v, flags=SAFE | mg.MG_FLAG_NO_SWAP_AB)
+    assert pa.info["swap_ab"] == 1 and pb.info["swap_ab"] == 0
+    assert_parity(a, ref, "one pass")
+    assert_parity(b, ref, "two passes")
+
+
+@pytest.mark.parametrize("flags", [0, mg.MG_FLAG_NO_CLUSTER])
+def test_online_bounded_wait(flags):
+    # The load warp waits on a barrier nothing arrives on: the group barriers, the rescale's wait
+    # and the combine unwind within the bound, and the context stays usable.
+    q, k, v, (B, M, N, d) = inputs.make_config("decode")
+    plan = mg.Plan(B, M, N, d, flags=SAFE | flags | mg.MG_FLAG_INJECT_TIMEOUT, timeout_ns=2_000_000)
+    assert plan.info["swap_ab"] == 1
+    O = torch.zeros((B, M, d), dtype=torch.float16, device="cuda")
+    plan.run(q.cuda(), k.cuda(), v.cuda(), O)
+    assert plan.status() == mg.MG_ERR_TIMEOUT
+    O2, _ = run_gpu(q, k, v, flags=SAFE | flags)
+    assert_parity(O2, oracle.attention(q, k, v), "after timeout")
