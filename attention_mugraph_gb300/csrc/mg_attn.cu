@@ -112,13 +112,24 @@ FwdKernel pair_kernel(int stages)
     }
 }
 
-// The few-row specialisation (head dim 128, transposed products) for a pipeline depth; `online`:
-// its one-pass max-subtracted form.
-FwdKernel swap_kernel(int stages, bool online)
+// The few-row specialisation (head dim 128, transposed products) for a pipeline depth and form
+// (the graph as written, its one-pass max-subtracted evaluation, QK-norm on that).
+template <int STAGES>
+FwdKernel swap_kernel_form(int form)
 {
+    return form == mg::kSwapQkNormForm   ? mg::mg_attn_fwd_swap<STAGES, mg::kSwapQkNormForm>
+           : form == mg::kSwapOnlineForm ? mg::mg_attn_fwd_swap<STAGES, mg::kSwapOnlineForm>
+                                         : mg::mg_attn_fwd_swap<STAGES, mg::kSwapPlainForm>;
+}
+
+FwdKernel swap_kernel(int stages, int flags)
+{
+    const int form = (flags & MG_FLAG_QK_NORM)        ? mg::kSwapQkNormForm
+                     : (flags & MG_FLAG_SAFE_SOFTMAX) ? mg::kSwapOnlineForm
+                                                      : mg::kSwapPlainForm;
     switch (stages) {
-    case 2: return online ? mg::mg_attn_fwd_swap<2, true> : mg::mg_attn_fwd_swap<2>;
-    case 3: return online ? mg::mg_attn_fwd_swap<3, true> : mg::mg_attn_fwd_swap<3>;
+    case 2: return swap_kernel_form<2>(form);
+    case 3: return swap_kernel_form<3>(form);
     default: return nullptr;
     }
 }
@@ -294,12 +305,11 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
             stream_k = false, n_split = one_wave(units);
     }
     // The few-row specialisation: head dim 128, at most 16 query rows per batch, the graph as
-    // written or its max-subtracted evaluation (in one pass there), under the split schedule; the
-    // default there (measured on GB300, us per call against the one-tile kernel: (16, 8, 32768,
-    // 128) 45.8 against 48.2, (64, 1, 4096, 128) 25.2 against 26.9).
-    const bool swap = !pair && !stream_k && d == 128 && M <= mg::kSwapNQ && !(o.flags & MG_FLAG_QK_NORM) &&
-                      !(o.flags & MG_FLAG_NO_SWAP_AB);
-    const bool safe = (o.flags & MG_FLAG_SAFE_SOFTMAX) != 0;
+    // written, its max-subtracted evaluation or QK-norm (both in one pass there), under the split
+    // schedule; the default there (measured on GB300, us per call against the one-tile kernel:
+    // (16, 8, 32768, 128) 45.8 against 48.2, (64, 1, 4096, 128) 25.2 against 26.9).
+    const bool swap = !pair && !stream_k && d == 128 && M <= mg::kSwapNQ && !(o.flags & MG_FLAG_NO_SWAP_AB);
+    const bool safe = (o.flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) != 0;
     // The few-row kernel combines on chip too (fp32 partials; measured on GB300 for (64, 1, 4096,
     // 128), 2 splits: 24.3 us per call against 25.1 with the second kernel).
     const bool cluster =
@@ -329,7 +339,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
                                  : mg::fwd_smem_bytes(static_cast<int>(d), stages, push);
     if (static_cast<int64_t>(smem) > max_smem ||
         !(pair ? pair_kernel(stages)
-               : swap ? swap_kernel(stages, safe)
+               : swap ? swap_kernel(stages, o.flags)
                       : stream_k ? sk_kernel(d, stages) : push ? push_kernel(stages) : fwd_kernel(d, stages, o.flags)))
         return fail(MG_ERR_INSUFFICIENT_SMEM, "d=%lld with %d stages needs %u bytes of shared memory (limit %d)",
                     (long long)d, stages, smem, max_smem);
@@ -381,7 +391,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
 FwdKernel plan_kernel(const mg_attn_plan_info &info, int flags)
 {
     if (info.swap_ab == 1)
-        return swap_kernel(info.stages, (flags & MG_FLAG_SAFE_SOFTMAX) != 0);
+        return swap_kernel(info.stages, flags);
     if (info.schedule == 1)
         return sk_kernel(info.d, info.stages);
     if (info.xchg_push == 1)

@@ -33,6 +33,13 @@
 // protocol is tests/pipeline_model.py's ONLINE variant. The epilogue merges the two groups (weights
 // exp(m_g - max m)); split partials carry their maximum to the combine, which weights them the same
 // way. The result equals the graph as written, exp(S) / rowsum(exp(S)) . V, up to rounding.
+//
+// QK-norm (Mirage documentation, tutorials/attention-with-kv-norm: Q and K rms-normalised over d
+// before the graph) runs on the ONLINE form with the scores scaled in fp32, S^T[n, q] a_q c_n:
+// the query scales a_q = 1/rms(Q[q, :]) once per CTA from Q^T in shared memory (all softmax
+// warps, one barrier), and per tile each thread's key scale c_n = 1/rms(K[:, n]) from the K tile
+// in shared memory (a lane sums one 16-byte unit of every eighth d-row, then a reduce-scatter over
+// the eight lanes of a unit), while the tensor core computes S^T. K is read once.
 #pragma once
 
 #include "mg_attn_kernels.cuh"
@@ -48,8 +55,14 @@ constexpr uint32_t kSwapPBytes = kSwapNQ * kBlockN * 2;          // P^T: two 64-
 constexpr int kSwapPBuffers = 3;
 constexpr uint32_t kSwapTmemCols = 64;                           // S^T buffers at 0 and 16, O^T at 32 (and 48)
 constexpr uint32_t kSwapTmemO = 32;
-// ONLINE: per group, two buffers of the four warps' tile maxima, and group 1's final maxima.
-constexpr uint32_t kSwapOnlineBytes = (2 * 2 * kGroupWarps * kSwapNQ + kSwapNQ) * 4;
+// Forms of the few-row kernel: the graph as written; ONLINE (max-subtracted, one pass); ONLINE
+// with QK-norm scales.
+constexpr int kSwapPlainForm = 0;
+constexpr int kSwapOnlineForm = 1;
+constexpr int kSwapQkNormForm = 2;
+// ONLINE: per group, two buffers of the four warps' tile maxima; group 1's final maxima; the
+// query scales (QK-norm).
+constexpr uint32_t kSwapOnlineBytes = (2 * 2 * kGroupWarps * kSwapNQ + 2 * kSwapNQ) * 4;
 // ONLINE: a group keeps the maximum it subtracts until some query's tile maximum exceeds it by
 // more than this; any per-row shift cancels in the normalisation, and the scores stay at most 8
 // above the subtracted value, so P <= e^8 ~ 2981 (fp16 keeps its relative precision up to 65504).
@@ -94,13 +107,15 @@ __device__ __forceinline__ float warp_max16(float (&v)[16], int lane)
     return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
 }
 
-template <int STAGES, bool ONLINE = false>
+template <int STAGES, int FORM = kSwapPlainForm>
 __global__ void __launch_bounds__(kThreads, 1)
     mg_attn_fwd_swap(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                      const __grid_constant__ CUtensorMap tmW, const FwdParams p)
 {
     constexpr int D = kSwapD;
+    constexpr bool ONLINE = FORM != kSwapPlainForm;
+    constexpr bool QKN = FORM == kSwapQkNormForm;
     using BI = Bars<STAGES, kSwapPBuffers>;
     static_assert(swap_smem_bytes(STAGES, ONLINE) <= 232448u, "tile configuration exceeds 227 KB");
     (void)tmO;
@@ -114,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *l_red = reinterpret_cast<float *>(smem + kSwapQBytes + kSwapPBuffers * kSwapPBytes + STAGES * kSwapStageBytes);
     float *m_red = l_red + kSoftmaxWarps * kSwapNQ;           // ONLINE: [group][buffer][warp][query]
     float *m_fin = m_red + 2 * 2 * kGroupWarps * kSwapNQ;     // ONLINE: group 1's final maxima
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ONLINE ? m_fin + kSwapNQ : m_red);
+    float *a_sc = m_fin + kSwapNQ;                            // QK-norm: the query scales
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ONLINE ? a_sc + kSwapNQ : m_red);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
@@ -354,6 +370,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < kSwapNQ / 2; ++q)
                 shift[q] = 0;
+            // QK-norm: the query scales a_q = 1/rms(Q[q, :]), 16 threads of the softmax warps per
+            // query row, one 16-byte unit (8 columns) each, a 4-step sum over those 16 lanes; one
+            // barrier of all softmax warps publishes them in shared memory (and ANDs the wait for
+            // Q), where each tile reads them again (fewer registers live in the loop).
+            // QK-norm, key scales: this lane's unit (8 keys) of the warp's 32 and its d-rows kr,
+            // kr + 8, ... (kr alternates between the swizzle pattern's halves, so a quarter-warp's
+            // eight loads hit eight distinct bank groups); after the reduce-scatter a lane holds
+            // key 8 (lane & 3) + 4 bit4 + 2 bit3 + bit2 of the warp's, and one shuffle brings each
+            // lane its own key's (key q4 * 32 + lane).
+            const int kr = (((lane >> 2) & 1) << 2) | (lane >> 3);
+            const uint32_t unit_phys = (static_cast<uint32_t>(((q4 & 1) << 2) | (lane & 3))) ^ static_cast<uint32_t>(kr);
+            const int c_src = (lane >> 3) | ((lane & 1) << 2) | (((lane >> 1) & 1) << 3) | (((lane >> 2) & 1) << 4);
+            if constexpr (QKN) {
+                const int i = threadIdx.x - 64;  // 0 .. 255
+                const int qr = i >> 4, part = i & 15;
+                bool q_ok = warp_wait(bar(BI::kQFull), 0, BI::kQFull);
+                float ss[2] = {0.f, 0.f};
+                if (q_ok)
+                    sum_sq_unit(*reinterpret_cast<const uint4 *>(smem + (part >> 3) * kSwapChunk + qr * 128 +
+                                                                 (((part & 7) ^ (qr & 7)) << 4)),
+                                ss);
+                float t = ss[0] + ss[1];
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1)
+                    t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (part == 0)
+                    a_sc[qr] = __frsqrt_rn(t * (1.f / D) + kQkNormEps);
+                if (!ptx::named_barrier_and(kSoftmaxBarrier, kSoftmaxThreads, q_ok))
+                    ok = false;
+            }
             // Every warp of the group takes the same group barriers per tile, so all run the same
             // iterations: a failed wait clears `ok`, and the next barriers (or the epilogue's) stop
             // the others too.
@@ -362,7 +408,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int mb = (u >> 1) & 1;  // buffer of the tile maxima
                 const bool valid = tile_of(u) * kBlockN + key < p.N;  // keys past N weigh 0
                 uint32_t r[kSwapNQ];
-                bool w_ok = ok && warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);
+                bool w_ok = ok;
+                float cn = 1.f;  // QK-norm: this thread's key scale c_n = 1/rms(K[:, n])
+                if constexpr (QKN) {
+                    // From the K tile in shared memory, while the tensor core computes S^T (the K
+                    // stage is released only after this tile's P.V, which waits for this group).
+                    const int st = u % STAGES;
+                    w_ok = w_ok && warp_wait(bar(BI::kKFull + st), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + st);
+                    if (w_ok) {
+                        const uint8_t *kp = smem + (sStage0 - sQ) + st * kSwapStageBytes + (q4 >> 1) * (D * 128) +
+                                            kr * 128 + (unit_phys << 4);
+                        float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int k = 0; k < D / 8; ++k)  // d-row kr + 8k
+                            sum_sq_cols(*reinterpret_cast<const uint4 *>(kp + k * 1024), sq);
+                        const float c = __frsqrt_rn(reduce_scatter8(sq, lane) * (1.f / D) + kQkNormEps);
+                        cn = __shfl_sync(0xffffffffu, c, c_src);
+                    }
+                }
+                w_ok = w_ok && warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);
                 bool over = false;  // a score of this warp past its row's maximum by more than the slack
                 if (w_ok) {
                     ptx::tc_fence_after();
@@ -372,6 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0)
                         ptx::mbar_arrive(bar(BI::kSEmpty + g));
+                    if constexpr (QKN) {
+#pragma unroll
+                        for (int k = 0; k < kSwapNQ / 4; ++k) {  // the normalised scores, a_q c_n S^T[n, q]
+                            const float4 a = reinterpret_cast<const float4 *>(a_sc)[k];
+                            r[4 * k + 0] = __float_as_uint(__uint_as_float(r[4 * k + 0]) * (cn * a.x));
+                            r[4 * k + 1] = __float_as_uint(__uint_as_float(r[4 * k + 1]) * (cn * a.y));
+                            r[4 * k + 2] = __float_as_uint(__uint_as_float(r[4 * k + 2]) * (cn * a.z));
+                            r[4 * k + 3] = __float_as_uint(__uint_as_float(r[4 * k + 3]) * (cn * a.w));
+                        }
+                    }
 #pragma unroll
                     for (int q = 0; q < kSwapNQ; ++q)
                         over |= valid && __uint_as_float(r[q]) > mrun[q] + kSwapRescaleSlack;

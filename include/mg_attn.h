@@ -87,7 +87,9 @@ typedef enum {
                                       workspace for the main pass) and applies them to the scores in fp32,
                                       so Q and K stay the fp16 MMA operands and K is read twice, as without
                                       the flag. Normalised scores reach +-d, past the fp16 range of exp, so
-                                      the flag implies MG_FLAG_SAFE_SOFTMAX. */
+                                      the flag implies MG_FLAG_SAFE_SOFTMAX. Under the few-row
+                                      specialisation (MG_FLAG_SWAP_AB) it runs in one pass (K read once):
+                                      the key scales come from each K tile in shared memory. */
 #define MG_QKNORM_EPS 1e-6
 #define MG_FLAG_Q_PAIRS 0x20       /* use the two-Q-tile kernel wherever it applies (head dim 64, the graph as
                                       written, an even number of 128-row tiles per batch): each CTA holds
@@ -105,8 +107,8 @@ typedef enum {
                                       sums in a fixed order. Opt-in: measured on GB300 it is not faster than
                                       the default split schedule on the decode shapes; see info.schedule */
 #define MG_FLAG_NO_STREAM_K 0x100  /* the split schedule (N split n_split ways per row tile; the default) */
-#define MG_FLAG_SWAP_AB 0x200      /* few-row specialisation (the graph as written or its max-subtracted
-                                      evaluation in one pass, head dim 128, at most 16
+#define MG_FLAG_SWAP_AB 0x200      /* few-row specialisation (the graph as written, or its max-subtracted
+                                      or QK-norm evaluation in one pass; head dim 128, at most 16
                                       query rows per batch, the split schedule): per K/V tile the products run
                                       transposed, S^T = K^T Q^T and O^T += V^T P^T, so the MMA's 128 rows are
                                       keys (resp. output columns) instead of mostly-empty query rows; split

@@ -96,3 +96,72 @@ def test_deterministic_and_combines_agree():
     assert p1.info["cluster_ctas"] > 0 and p3.info["cluster_ctas"] == 0
     assert torch.equal(O1, O2)
     assert_parity(O3, ref, "second-kernel combine")
+
+
+# ---------------------------------------------------------------------------------------------
+# The few-row kernel's QK-norm form (head dim 128, at most 16 rows per batch): one pass, the
+# query scales once per CTA and each tile's key scales from the K tile in shared memory.
+
+QK_SWAP_SHAPES = [  # (B, M, N, n_split, flags)
+    (16, 8, 32768, 0, 0),                        # decode
+    (16, 8, 32768, 0, mg.MG_FLAG_NO_CLUSTER),
+    (64, 1, 4096, 0, 0),                         # the launch example's shapes: 2-CTA clusters
+    (3, 16, 1032, 1, 0),                         # one split; ragged N
+    (2, 1, 8, 0, 0),                             # one ragged tile
+    (5, 3, 5000, 7, 0),
+    (5, 3, 5000, 7, mg.MG_FLAG_NO_CLUSTER),
+    (4, 8, 8192, 16, 0),
+]
+
+
+@pytest.mark.parametrize("B,M,N,n_split,flags", QK_SWAP_SHAPES)
+def test_few_row_kernel(B, M, N, n_split, flags):
+    q, k, v = inputs.make_inputs_normal(B, M, N, 128, seed=3 * B + M + N)
+    O, plan = run_gpu(q, k, v, n_split=n_split, flags=QK | flags)
+    assert plan.info["swap_ab"] == 1
+    assert_parity(O, qk_ref(q, k, v), f"{B, M, N} n_split={plan.info['n_split']} "
+                                      f"cluster={plan.info['cluster_ctas']}")
+    O2, _ = run_gpu(q, k, v, n_split=n_split, flags=QK | flags)
+    assert torch.equal(O, O2)
+
+
+@pytest.mark.parametrize("n_split", [1, 0])
+def test_few_row_kernel_scales_per_key_and_row(n_split):
+    # Every key vector and query row multiplied by its own power of two (exact in fp16), from
+    # 2^-3 to 2^3: the normalisation removes each factor, so the result is the unscaled inputs'
+    # up to eps. A key scale applied to the wrong key (or a query scale to the wrong row) is off
+    # by up to 2^6 and fails the bound.
+    B, M, N = 4, 13, 2056
+    q, k, v = inputs.make_inputs_normal(B, M, N, 128, seed=17)
+    ref = qk_ref(q, k, v)
+    kf = 2.0 ** (torch.arange(N) % 7 - 3).float()
+    qf = 2.0 ** (torch.arange(M) % 5 - 2).float()
+    ks = (k.float() * kf).half().contiguous()
+    qs = (q.float() * qf[:, None]).half().contiguous()
+    O, plan = run_gpu(qs, ks, v, n_split=n_split, flags=QK)
+    assert plan.info["swap_ab"] == 1
+    assert_parity(O, ref, f"per-key and per-row factors n_split={plan.info['n_split']}")
+
+
+def test_few_row_kernel_matches_one_tile_kernel():
+    q, k, v, _ = inputs.make_config("decode_m1")
+    ref = qk_ref(q, k, v)
+    a, pa = run_gpu(q, k, v, flags=QK)
+    b, pb = run_gpu(q, k, v, flags=QK | mg.MG_FLAG_NO_SWAP_AB)
+    assert pa.info["swap_ab"] == 1 and pb.info["swap_ab"] == 0
+    assert_parity(a, ref, "few-row kernel")
+    assert_parity(b, ref, "one-tile kernel")
+
+
+@pytest.mark.parametrize("flags", [0, mg.MG_FLAG_NO_CLUSTER])
+def test_few_row_kernel_bounded_wait(flags):
+    # The load warp waits on a barrier nothing arrives on: the wait for Q behind the query scales'
+    # barrier, the key-scale waits and the group barriers unwind within the bound.
+    q, k, v, (B, M, N, d) = inputs.make_config("decode")
+    plan = mg.Plan(B, M, N, d, flags=QK | flags | mg.MG_FLAG_INJECT_TIMEOUT, timeout_ns=2_000_000)
+    assert plan.info["swap_ab"] == 1
+    O = torch.zeros((B, M, d), dtype=torch.float16, device="cuda")
+    plan.run(q.cuda(), k.cuda(), v.cuda(), O)
+    assert plan.status() == mg.MG_ERR_TIMEOUT
+    O2, _ = run_gpu(q, k, v, flags=QK | flags)
+    assert_parity(O2, qk_ref(q, k, v), "after timeout")
