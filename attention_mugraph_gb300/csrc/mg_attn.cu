@@ -223,7 +223,8 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
     if (o.reserved != 0 ||
         (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX |
                      MG_FLAG_QK_NORM | MG_FLAG_Q_PAIRS | MG_FLAG_NO_Q_PAIRS | MG_FLAG_STREAM_K |
-                     MG_FLAG_NO_STREAM_K | MG_FLAG_SWAP_AB | MG_FLAG_NO_SWAP_AB | MG_FLAG_PUSH_COMBINE)) != 0)
+                     MG_FLAG_NO_STREAM_K | MG_FLAG_SWAP_AB | MG_FLAG_NO_SWAP_AB | MG_FLAG_PUSH_COMBINE |
+                     MG_FLAG_NO_EARLY_LOADS)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -752,13 +753,19 @@ mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info)
 }
 
 // The output ranges of the last call enqueued on each stream (O as passed to mg_attn_run; hO and
-// its device address for mg_attn_run_host). A host-buffer call's copy kernel may load its inputs
-// before the previous kernel on its stream has finished, and only that kernel: every earlier one
-// has completed by the time the copy kernel can start (each of this library's kernels releases its
-// dependents only after its own wait). So the loads are early unless an input shares bytes with
-// the previous call's output on that stream (a chain of calls) or with the call's own output.
+// its device address for mg_attn_run_host). A call's first kernel (the host-buffer call's copy
+// kernel, or the fused kernel) may load its inputs before the previous kernel on its stream has
+// finished, and only that kernel: every earlier one has completed by the time it can start (each
+// of this library's kernels releases its dependents only after its own wait, and a kernel of
+// another origin releases them when it completes). So the loads are early unless an input shares
+// bytes with the previous call's output on that stream (a chain of calls) or with the call's own
+// output, or the previous call is unknown: the first call on a stream (or one whose record was
+// displaced by 64 newer streams), and the first call of a stream capture. Calls enqueued under
+// capture are recorded apart from the stream's eager calls (keyed by the capture's id), since
+// the captured kernels run later, as one graph.
 struct OutRanges {
     cudaStream_t stream = nullptr;
+    unsigned long long capture = 0;            // the capture's id, 0 for eager calls
     uintptr_t lo[2] = {0, 0}, hi[2] = {0, 0};  // [lo, hi) ranges; empty when lo == hi
     unsigned long long age = 0;
     bool used = false;
@@ -768,11 +775,23 @@ std::mutex g_out_mu;
 OutRanges g_out[kStreamSlots];
 unsigned long long g_out_clock = 0;
 
-OutRanges *find_slot(cudaStream_t stream, bool claim)
+// The id of the capture in progress on `stream`, 0 if none; ~0 if the query failed.
+unsigned long long capture_of(cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    unsigned long long id = 0;
+    if (cudaStreamGetCaptureInfo(stream, &cs, &id) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ~0ull;
+    }
+    return cs == cudaStreamCaptureStatusActive ? id : 0;
+}
+
+OutRanges *find_slot(cudaStream_t stream, unsigned long long capture, bool claim)
 {
     OutRanges *oldest = &g_out[0];
     for (auto &r : g_out) {
-        if (r.used && r.stream == stream)
+        if (r.used && r.stream == stream && r.capture == capture)
             return &r;
         if (!r.used || (oldest->used && r.age < oldest->age))
             oldest = &r;
@@ -780,21 +799,27 @@ OutRanges *find_slot(cudaStream_t stream, bool claim)
     return claim ? oldest : nullptr;
 }
 
-// The output ranges of the last call enqueued on `stream` (none if unknown).
+// The output ranges of the last call enqueued on `stream` under the same capture (or none);
+// `used` is false when that call is unknown.
 OutRanges last_outputs(cudaStream_t stream)
 {
+    const unsigned long long capture = capture_of(stream);
+    if (capture == ~0ull)
+        return OutRanges{};
     std::lock_guard<std::mutex> lock(g_out_mu);
-    const OutRanges *r = find_slot(stream, false);
+    const OutRanges *r = find_slot(stream, capture, false);
     return r ? *r : OutRanges{};
 }
 
 // Records the output ranges of the call just enqueued on `stream`.
 void record_outputs(cudaStream_t stream, const void *a, size_t na, const void *b, size_t nb)
 {
+    const unsigned long long capture = capture_of(stream);
     std::lock_guard<std::mutex> lock(g_out_mu);
-    OutRanges *slot = find_slot(stream, true);
+    OutRanges *slot = find_slot(stream, capture, true);
     slot->used = true;
     slot->stream = stream;
+    slot->capture = capture;
     slot->age = ++g_out_clock;
     slot->lo[0] = reinterpret_cast<uintptr_t>(a);
     slot->hi[0] = slot->lo[0] + (a ? na : 0);
@@ -808,8 +833,32 @@ bool overlaps_range(const void *p, size_t n, uintptr_t lo, uintptr_t hi)
     return lo < hi && x < hi && lo < x + n;
 }
 
-mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const void *V, void *O,
-                      mg_stream_t stream)
+// Whether a call's first kernel may load its inputs before the previous grid on `stream` has
+// completed: the previous call is known and no input (n[i] bytes at p[i], host or device address)
+// shares bytes with its outputs or with this call's own output [o, o + no).
+bool may_load_early(cudaStream_t stream, const void *const *p, const size_t *n, int count, const void *o, size_t no)
+{
+    const OutRanges prev = last_outputs(stream);
+    if (!prev.used)
+        return false;
+    const uintptr_t ol = reinterpret_cast<uintptr_t>(o);
+    for (int i = 0; i < count; ++i) {
+        if (!p[i])
+            continue;
+        if (overlaps_range(p[i], n[i], ol, ol + no))
+            return false;
+        for (int r = 0; r < 2; ++r)
+            if (overlaps_range(p[i], n[i], prev.lo[r], prev.hi[r]))
+                return false;
+    }
+    return true;
+}
+
+// mg_attn_run's work; `allow_early`: the fused kernel may load Q, K and V before the previous
+// grid on the stream completes, where may_load_early allows it (the host-buffer entry point's
+// staged inputs are written by the copy kernel just before: never).
+static mg_status run_fused(mg_attn_plan_t plan, const void *Q, const void *K, const void *V, void *O,
+                           mg_stream_t stream, bool allow_early)
 {
     if (!plan || !Q || !K || !V || !O)
         return fail(MG_ERR_INVALID_ARG, "NULL plan or tensor pointer");
@@ -857,6 +906,19 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
 
     cudaLaunchAttribute attr[2];
     const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
+    // Early loads (the one-tile and few-row kernels; not with the injected timeout, whose wait
+    // comes before the loads). Measured on GB300 (us per call, back to back, against
+    // MG_FLAG_NO_EARLY_LOADS): gqa 6.17 against 6.50, tiny 4.56 against 5.44, gqa_b8 9.86
+    // against 10.03, long_kv 14.52 against 14.82, decode 46.0 against 46.7, decode_m1 24.6
+    // against 25.0.
+    prm.early_loads = 0;
+    if (allow_early && pdl && !prm.inject_timeout && in.q_tiles_per_cta == 1 &&
+        !(plan->flags & MG_FLAG_NO_EARLY_LOADS)) {
+        const size_t bq = static_cast<size_t>(B * M * d) * 2, bk = static_cast<size_t>(B * d * N) * 2;
+        const void *inp[3] = {Q, K, V};
+        const size_t nb[3] = {bq, bk, bk};
+        prm.early_loads = may_load_early(reinterpret_cast<cudaStream_t>(stream), inp, nb, 3, O, bq) ? 1 : 0;
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(in.grid_ctas), 1, 1);
@@ -895,6 +957,12 @@ mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const v
     }
     record_outputs(cfg.stream, O, static_cast<size_t>(B * M * d) * 2, nullptr, 0);
     return MG_OK;
+}
+
+mg_status mg_attn_run(mg_attn_plan_t plan, const void *Q, const void *K, const void *V, void *O,
+                      mg_stream_t stream)
+{
+    return run_fused(plan, Q, K, V, O, stream, true);
 }
 
 mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, const void *hV, void *hO,
@@ -943,16 +1011,9 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
         // be writing). Measured on GB300 (GQA graph, back-to-back calls): 13.5 us per call, against
         // 19.3 with every load after the wait (the link's transfer then overlaps the previous
         // call's attention kernel).
-        const OutRanges prev = last_outputs(st);
-        auto clashes = [&](const void *host, const void *dev, size_t n) {
-            if (overlaps_range(host, n, reinterpret_cast<uintptr_t>(hO), reinterpret_cast<uintptr_t>(hO) + bq))
-                return true;
-            for (int r = 0; r < 2; ++r)
-                if (overlaps_range(host, n, prev.lo[r], prev.hi[r]) || overlaps_range(dev, n, prev.lo[r], prev.hi[r]))
-                    return true;
-            return false;
-        };
-        in_jobs.early = !(clashes(hQ, dQ, bq) || clashes(hK, dK, bk) || clashes(hV, dV, bv));
+        const void *inp[6] = {hQ, hK, hV, dQ, dK, dV};
+        const size_t nb[6] = {bq, bk, bv, bq, bk, bv};
+        in_jobs.early = may_load_early(st, inp, nb, 6, hO, bq) ? 1 : 0;
         if ((e = launch_copy(in_jobs, plan->info.num_sms, pdl, st)) != cudaSuccess)
             return cuda_fail(e, "launch mg_copy_units (host to device)");
     } else if ((e = cudaMemcpyAsync(s + oq, hQ, bq, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
@@ -964,7 +1025,7 @@ mg_status mg_attn_run_host(mg_attn_plan_t plan, const void *hQ, const void *hK, 
     // which reach the pinned host buffer through its device address directly: no staging of O
     // and no copy back. One split writes O with a TMA store, which takes the staging path.
     const bool o_direct = direct && in.n_split > 1;
-    mg_status r = mg_attn_run(plan, s + oq, s + ok, s + ov, o_direct ? dO : s + oo, stream);
+    mg_status r = run_fused(plan, s + oq, s + ok, s + ov, o_direct ? dO : s + oo, stream, false);
     if (r != MG_OK)
         return r;
     if (!o_direct) {
@@ -1121,6 +1182,12 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.col_scale = nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
+    {
+        const size_t bq = static_cast<size_t>(B * M * d) * 2, bk = static_cast<size_t>(B * d * N) * 2;
+        const void *inp[3] = {Q, K, V};
+        const size_t nb[3] = {bq, bk, bk};
+        prm.early_loads = may_load_early(reinterpret_cast<cudaStream_t>(stream), inp, nb, 3, O, bq) ? 1 : 0;
+    }
     prm.sk_units = static_cast<long long>(in.m_tiles) * in.n_tiles;
     prm.sk_ctas = in.grid_ctas;
     prm.sk_slots = in.n_split;

@@ -134,6 +134,8 @@ struct FwdParams {
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
     int inject_timeout;
+    int early_loads;         // the load warp issues Q and the first STAGES K/V tiles before it waits
+                             // for the previous grid (the host found that grid writes none of them)
     long long sk_units;      // stream-K: B * n_tiles units (row tile, column tile)
     int sk_ctas;             // stream-K: G, the grid
     int sk_slots;            // stream-K: partial slots per row tile (the second kernel's split count)
@@ -479,22 +481,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPushX && cluster)
         ptx::cluster_arrive_release();
 
-    // Everything above touched only on-chip state; global memory waits for the previous grid.
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
+    // Everything above touched only on-chip state; global memory waits for the previous grid,
+    // except the early loads of the load warp (below). Every thread releases the dependents only
+    // after its own wait, so a grid launched after this one never starts before the one before
+    // this one has completed.
+    if (!(warp == 0 && p.early_loads)) {
+        ptx::griddep_wait();
+        ptx::griddep_launch_dependents();
+    }
 
     const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
     bool staged_ok = false;  // softmax warps: this CTA staged its output (its O was complete)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            bool q_armed = false;
-            int armed[STAGES];
+        // Lane 0 issues every copy. Early loads: Q and the first STAGES steps' tiles go out before
+        // the wait for the previous grid (the host allows it only when that grid writes none of
+        // Q, K and V), so their DRAM latency overlaps the previous call's end; the whole warp then
+        // waits (after lane 0's issues: a lane blocked in the wait would hold back the others).
+        bool q_armed = false;
+        int armed[STAGES];
 #pragma unroll
-            for (int s = 0; s < STAGES; ++s)
-                armed[s] = 0;
-            bool ok = true;
+        for (int s = 0; s < STAGES; ++s)
+            armed[s] = 0;
+        bool ok = true;
+        int t = 0;  // the next step to issue (lane 0)
+        // One step's copies into stage t % STAGES, once that stage is free.
+        auto issue = [&](int t) {
+            const int s = t % STAGES;
+            const int n0 = tile_of(t < T1 ? t : t - T1) * kBlockN;
+            const int bt = batch_of(t < T1 ? t : t - T1);
+            const uint32_t sK = sStage0 + s * C::kStageBytes;
+            const uint32_t sV = sK + C::kKBytes;
+            // K and V land on separate barriers: S = Q.K need not wait for V. A step of the
+            // row-maximum pass loads no V; its V barrier phase completes on a plain arrival,
+            // so every step advances every barrier of its stage by one phase.
+            ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), C::kKBytes);
+            if (t < T1)
+                ptx::mbar_arrive(bar(BI::kVFull + s));
+            else
+                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
+            ++armed[s];
+            // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
+            ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, bt);
+            ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, bt);
+            // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
+            if (t >= T1) {
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, bt);
+            }
+        };
+        if (lane == 0) {
             if (p.inject_timeout)
                 ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
             if (ok) {
@@ -515,36 +553,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < C::kChunks; ++c)  // Q[b, m0:m0+128, 64c:64c+64]
                         ptx::tma_load_3d(sQ + c * C::kChunkRows128, &tmQ, bar(BI::kQFull), c * 64, m0, b);
                 }
+                if (p.early_loads)
+                    for (; t < U && t < STAGES; ++t)  // the stages are free: no wait
+                        issue(t);
             }
-            for (int t = 0; ok && t < U; ++t) {
+        }
+        if (p.early_loads) {
+            __syncwarp();
+            ptx::griddep_wait();
+            ptx::griddep_launch_dependents();
+        }
+        if (lane == 0) {
+            for (; ok && t < U; ++t) {
                 const int s = t % STAGES;
                 const uint32_t round = static_cast<uint32_t>(t / STAGES);
                 if (t >= STAGES && !wait_bounded(wc, bar(BI::kKvEmpty + s), (round & 1u) ^ 1u, BI::kKvEmpty + s)) {
                     ok = false;
                     break;
                 }
-                const int n0 = tile_of(t < T1 ? t : t - T1) * kBlockN;
-                const int bt = batch_of(t < T1 ? t : t - T1);
-                const uint32_t sK = sStage0 + s * C::kStageBytes;
-                const uint32_t sV = sK + C::kKBytes;
-                // K and V land on separate barriers: S = Q.K need not wait for V. A step of the
-                // row-maximum pass loads no V; its V barrier phase completes on a plain arrival,
-                // so every step advances every barrier of its stage by one phase.
-                ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), C::kKBytes);
-                if (t < T1)
-                    ptx::mbar_arrive(bar(BI::kVFull + s));
-                else
-                    ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
-                ++armed[s];
-                // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
-                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, bt);
-                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, bt);
-                // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
-                if (t >= T1) {
-#pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, bt);
-                }
+                issue(t);
             }
             if (ok) {
                 // Tail: the commits that release the last stages must land before the CTA exits.

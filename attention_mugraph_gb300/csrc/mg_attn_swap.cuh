@@ -182,20 +182,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
+    // Global memory waits for the previous grid, except the load warp's early loads (as in the
+    // one-tile kernel); every thread releases the dependents only after its own wait.
+    if (!(warp == 0 && p.early_loads)) {
+        ptx::griddep_wait();
+        ptx::griddep_launch_dependents();
+    }
 
     const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            bool q_armed = false;
-            int armed[STAGES];
+        // Lane 0 issues every copy; early loads as in the one-tile kernel (Q and the first STAGES
+        // tiles before the warp's wait for the previous grid).
+        bool q_armed = false;
+        int armed[STAGES];
 #pragma unroll
-            for (int s = 0; s < STAGES; ++s)
-                armed[s] = 0;
-            bool ok = true;
+        for (int s = 0; s < STAGES; ++s)
+            armed[s] = 0;
+        bool ok = true;
+        int t = 0;  // the next tile to issue (lane 0)
+        auto issue = [&](int t) {
+            const int s = t % STAGES;
+            const int n0 = tile_of(t) * kBlockN;
+            const uint32_t sK = sStage0 + s * kSwapStageBytes;
+            const uint32_t sV = sK + D * kBlockN * 2;
+            ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), D * kBlockN * 2);
+            ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), kBlockN * D * 2);
+            ++armed[s];
+            ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
+            ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                ptx::tma_load_3d(sV + c * TileCfg<D>::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
+        };
+        if (lane == 0) {
             if (p.inject_timeout)
                 ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
             if (ok) {
@@ -205,25 +226,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d(sQ + c * kSwapChunk, &tmQ, bar(BI::kQFull), c * 64, 0, b);
+                if (p.early_loads)
+                    for (; t < T && t < STAGES; ++t)
+                        issue(t);
             }
-            for (int t = 0; ok && t < T; ++t) {
+        }
+        if (p.early_loads) {
+            __syncwarp();
+            ptx::griddep_wait();
+            ptx::griddep_launch_dependents();
+        }
+        if (lane == 0) {
+            for (; ok && t < T; ++t) {
                 const int s = t % STAGES;
                 const uint32_t round = static_cast<uint32_t>(t / STAGES);
                 if (t >= STAGES && !wait_bounded(wc, bar(BI::kKvEmpty + s), (round & 1u) ^ 1u, BI::kKvEmpty + s)) {
                     ok = false;
                     break;
                 }
-                const int n0 = tile_of(t) * kBlockN;
-                const uint32_t sK = sStage0 + s * kSwapStageBytes;
-                const uint32_t sV = sK + D * kBlockN * 2;
-                ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), D * kBlockN * 2);
-                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), kBlockN * D * 2);
-                ++armed[s];
-                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
-                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d(sV + c * TileCfg<D>::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
+                issue(t);
             }
             if (ok) {
                 for (int u = T - STAGES > 0 ? T - STAGES : 0; ok && u < T; ++u)

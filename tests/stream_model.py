@@ -1,23 +1,29 @@
-"""Protocol model of the host-buffer entry point's launches (mg_attn_run_host), for CPU tests.
+"""Protocol model of the launches of the library's calls on one stream, for CPU tests.
 
-Each call enqueues on one stream a copy kernel (pinned host inputs -> the plan's device staging)
-and the attention kernel (staging -> O, written straight into the pinned output). Both are
-launched with programmatic dependent launch: a kernel may start once every CTA of the kernel
-before it has released its dependents (griddepcontrol.launch_dependents), and it passes its own
-griddepcontrol.wait only once that kernel has completed, with its memory visible; a kernel
-completes only after its own wait, so the completions stay in stream order.
+A host-buffer call (mg_attn_run_host) enqueues a copy kernel (pinned host inputs -> the plan's
+device staging) and the attention kernel (staging -> O, written straight into the pinned
+output). A device call (mg_attn_run) enqueues the attention kernel alone, reading its inputs
+where the caller keeps them. Every kernel is launched with programmatic dependent launch: a
+kernel may start once every CTA of the kernel before it has released its dependents
+(griddepcontrol.launch_dependents), and it passes its own griddepcontrol.wait only once that
+kernel has completed, with its memory visible; every thread releases the dependents only after
+its own wait, so a kernel completes only after its wait and the completions stay in stream order.
 
-    copy kernel, early form:  load the inputs; wait; release dependents; store them into staging
-    copy kernel, late form:   wait; release dependents; load the inputs; store them into staging
-    attention kernel:         wait; release dependents; read staging; write O
+    copy kernel, early form:    load the inputs; wait; release dependents; store them into staging
+    copy kernel, late form:     wait; release dependents; load the inputs; store them into staging
+    attention kernel (host):    wait; release dependents; read staging; write O
+    attention kernel (device),
+      early form:               load the inputs; wait; release dependents; write O
+      late form:                wait; release dependents; load the inputs; write O
 
-The early form is used unless an input shares bytes with the call's own O or with the previous
-call's O on the stream (what the previous kernel may still be writing). The host writes a call's inputs
-before it enqueues the call. The scheduler interleaves the kernels' steps at random within those
-rules and checks every read: staging is read only after the copy that filled it for this call
-has completed, staging is not overwritten while an earlier call still reads it, and every input
-read sees the value the host wrote for that call (an input that is an earlier call's O must be
-read after that call's attention kernel wrote it).
+The early forms are used unless an input shares bytes with the call's own O or with the previous
+call's O on the stream (what the previous kernel may still be writing), or the call is the
+first on the stream (its previous kernel unknown). The caller writes a call's inputs before it
+enqueues the call. The scheduler interleaves the kernels' steps at random within those rules and
+checks every read: staging is read only after the copy that filled it for this call has
+completed, staging is not overwritten while an earlier call still reads it, and every input read
+sees the value written for that call (an input that is an earlier call's O must be read after
+that call's attention kernel wrote it).
 """
 
 from __future__ import annotations
@@ -31,8 +37,10 @@ class ProtocolError(AssertionError):
 
 class StreamSim:
     def __init__(self, calls, seed: int, mutations=()):
-        """calls: list of (inputs, output) buffer names, e.g. [("x0", "o0"), ("o0", "o1")] (the
-        second call reads the first call's output: in place)."""
+        """calls: list of (inputs, output) or (inputs, output, kind) buffer names, kind "host"
+        (the default) or "device", e.g. [("x0", "o0"), ("o0", "o1", "device")] (the second call
+        reads the first call's output)."""
+        calls = [c if len(c) == 3 else (c[0], c[1], "host") for c in calls]
         self.calls = calls
         self.rng = random.Random(seed)
         self.mut = set(mutations)
@@ -40,29 +48,34 @@ class StreamSim:
         self.staging = None      # (call, complete) of the staged inputs
         self.staging_readers = set()
         self.kernels = []        # in stream order: dicts with name, state
-        for k, (inp, out) in enumerate(calls):
-            # The entry point's rule: load early unless the input is this call's output or the
-            # previous call's output on the stream (mutations: no rule, or the own output only).
+        for k, (inp, out, kind) in enumerate(calls):
+            # The entry points' rule: load early unless the input is this call's output or the
+            # previous call's output on the stream, or the call is the stream's first (mutations:
+            # no rule, or the own output only).
             prev_out = calls[k - 1][1] if k > 0 else None
             if "early_despite_alias" in self.mut:
                 early = True
             elif "alias_own_only" in self.mut:
                 early = inp != out
             else:
-                early = inp != out and inp != prev_out
-            self.kernels.append({"name": f"copy{k}", "call": k, "kind": "copy", "early": early,
-                                 "inp": inp, "out": out})
-            self.kernels.append({"name": f"attn{k}", "call": k, "kind": "attn", "inp": inp, "out": out})
+                early = k > 0 and inp != out and inp != prev_out
+            if kind == "host":
+                self.kernels.append({"name": f"copy{k}", "call": k, "kind": "copy", "early": early,
+                                     "inp": inp, "out": out})
+                self.kernels.append({"name": f"attn{k}", "call": k, "kind": "attn", "inp": inp, "out": out})
+            else:
+                self.kernels.append({"name": f"dattn{k}", "call": k, "kind": "dattn", "early": early,
+                                     "inp": inp, "out": out})
         for kern in self.kernels:
             kern.update(started=False, triggered=False, waited=False, done=False)
         # the host wrote every call's inputs before enqueueing it; an input that is an earlier call's
         # output is expected to hold that call's value
         self.expect = {}
         writer = {}
-        for k, (inp, out) in enumerate(calls):
+        for k, (inp, out, _) in enumerate(calls):
             self.expect[k] = writer.get(inp, "host")
             writer[out] = k
-        for inp, _ in calls:
+        for inp, _, _ in calls:
             self.version.setdefault(inp, "host")
 
     # ---------------------------------------------------------------- kernel bodies
@@ -90,7 +103,23 @@ class StreamSim:
             yield
         kern["started"] = True
         k = kern["call"]
-        if kern["kind"] == "copy":
+        if kern["kind"] == "dattn":
+            loaded = None
+            if kern["early"]:
+                loaded = self.version.get(kern["inp"])
+                yield
+            while not self._may_pass_wait(i):
+                yield
+            kern["waited"] = True
+            kern["triggered"] = True
+            yield
+            if loaded is None:
+                loaded = self.version.get(kern["inp"])
+                yield
+            if loaded != self.expect[k]:
+                raise ProtocolError(f"dattn{k} loaded an input holding {loaded!r}, not {self.expect[k]!r}")
+            self.version[kern["out"]] = k
+        elif kern["kind"] == "copy":
             loaded = None
             if kern["early"]:
                 loaded = self.version.get(kern["inp"])

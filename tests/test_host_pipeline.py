@@ -1,5 +1,6 @@
-"""CPU checks of the host-buffer entry point's launch protocol through its model
-(tests/stream_model.py): back-to-back calls, in-place chains, and planted orderings that break it."""
+"""CPU checks of the launch protocol of the library's calls on one stream through its model
+(tests/stream_model.py): back-to-back host-buffer and device calls, in-place chains, mixed
+sequences, and planted orderings that break them."""
 
 import itertools
 
@@ -12,6 +13,11 @@ CHAINS = {
     "same_buffers": [("x", "o")] * 4,
     "in_place": [("h", "h")] * 4,
     "chained": [("x", "a"), ("a", "b"), ("b", "c"), ("c", "d")],
+    # device calls (mg_attn_run): the fused kernel loads its inputs early
+    "device_distinct": [("x0", "o0", "device"), ("x1", "o1", "device"), ("x2", "o2", "device")],
+    "device_chained": [("x", "a", "device"), ("a", "b", "device"), ("b", "c", "device"), ("c", "d", "device")],
+    "device_in_place": [("h", "h", "device")] * 4,
+    "mixed_chained": [("x", "a"), ("a", "b", "device"), ("b", "c"), ("c", "d", "device"), ("d", "e", "device")],
 }
 
 
@@ -54,3 +60,22 @@ def test_chains_need_the_previous_output_in_the_rule():
 def test_planted_orderings_are_caught(mutation, expect):
     msg = caught("distinct", mutation)
     assert msg is not None and expect in msg, msg
+
+
+@pytest.mark.parametrize("chain", ["device_chained", "device_in_place", "mixed_chained"])
+def test_device_calls_need_the_alias_rule(chain):
+    # The fused kernel of a device call loads Q, K and V before the previous kernel on the stream
+    # has completed; a call that reads the previous call's output (or its own, in place) would
+    # read it stale without the rule.
+    msg = caught(chain, "early_despite_alias")
+    assert msg is not None and "loaded an input" in msg, msg
+
+
+def test_device_chains_need_the_previous_output_in_the_rule():
+    msg = caught("device_chained", "alias_own_only")
+    assert msg is not None and "loaded an input" in msg
+
+
+def test_first_call_is_not_early():
+    sim = sm.StreamSim(CHAINS["device_distinct"], 0)
+    assert [k["early"] for k in sim.kernels] == [False, True, True]

@@ -507,6 +507,131 @@ def test_host_buffer_chained_calls(kw):
         cur = o.clone()
 
 
+EARLY_OFF = mg.MG_FLAG_NO_EARLY_LOADS | mg.MG_FLAG_NO_PDL
+
+
+def chain_inputs(q, k, v, which, prev):
+    # The call's (Q, K, V), with the one named by `which` replaced by the previous call's O (the
+    # same bytes, viewed in that input's shape).
+    x = {"q": q, "k": k, "v": v}
+    if prev is not None:
+        x[which] = prev.view(x[which].shape)
+    return x["q"], x["k"], x["v"]
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v"])
+@pytest.mark.parametrize("kw", [{}, {"n_split": 1}, {"flags": mg.MG_FLAG_NO_CLUSTER}])
+def test_device_chained_calls(which, kw):
+    # Back to back on one stream without synchronising, each call's Q (or K, or V) is the previous
+    # call's O: the fused kernel may load its inputs before the previous kernel on the stream has
+    # completed, and must not do so here (its inputs share bytes with the previous call's output).
+    # Compared bit for bit with the same chain run one synchronised call at a time with the early
+    # loads and dependent launch off. M = N so that O has the shape of Q, V and (viewed) K.
+    B, M, N, d = 2, 256, 256, 64
+    plan = mg.Plan(B, M, N, d, **kw)
+    q, k, v = (t.cuda() for t in inputs.make_inputs(B, M, N, d, 0.5, seed=83))
+    outs = [torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda") for _ in range(6)]
+    prev = None
+    for o in outs:
+        plan.run(*chain_inputs(q, k, v, which, prev), o)
+        prev = o
+    torch.cuda.synchronize()
+    ref_plan = mg.Plan(B, M, N, d, n_split=kw.get("n_split", 0), flags=kw.get("flags", 0) | EARLY_OFF)
+    prev = None
+    for i, o in enumerate(outs):
+        r = torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda")
+        ref_plan.run(*chain_inputs(q, k, v, which, prev), r)
+        torch.cuda.synchronize()
+        assert torch.equal(r, o), f"call {i} of the {which} chain"
+        prev = r
+
+
+def test_device_chain_in_captured_graph():
+    # Two calls captured into one graph, the second reading the first's O as Q, replayed three
+    # times: within the capture the first call has no known predecessor (no early loads) and the
+    # second sees the first's output.
+    B, M, N, d = 2, 256, 256, 64
+    plan = mg.Plan(B, M, N, d)
+    q, k, v = (t.cuda() for t in inputs.make_inputs(B, M, N, d, 0.5, seed=89))
+    o1 = torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda")
+    o2 = torch.full_like(o1, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.run(q, k, v, torch.empty_like(o1))  # an eager call on the stream first
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        plan.run(q, k, v, o1)
+        plan.run(o1, k, v, o2)
+        g.capture_end()
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            o1.fill_(float("nan"))
+            o2.fill_(float("nan"))
+            g.replay()
+    s.synchronize()
+    ref_plan = mg.Plan(B, M, N, d, flags=EARLY_OFF)
+    r1 = torch.empty_like(o1)
+    r2 = torch.empty_like(o1)
+    ref_plan.run(q, k, v, r1)
+    torch.cuda.synchronize()
+    ref_plan.run(r1, k, v, r2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, r1) and torch.equal(o2, r2)
+
+
+def test_eager_call_after_a_capture():
+    # An eager call X, a capture of an unrelated call on the same stream, then an eager call Z
+    # whose Q is X's O: Z's predecessor on the stream is X (the captured call has not run), so Z
+    # must compare its inputs with X's output, not with the captured call's. X is long (~30 us)
+    # so that Z, if it loaded early, would read Q before X wrote it.
+    d = 64
+    px = mg.Plan(16, 256, 16384, d)
+    pz = mg.Plan(16, 256, 4096, d)
+    qx, kx, vx = (t.cuda() for t in inputs.make_inputs(16, 256, 16384, d, 0.5, seed=97))
+    qz, kz, vz = (t.cuda() for t in inputs.make_inputs(16, 256, 4096, d, 0.5, seed=98))
+    ox = torch.full((16, 256, d), float("nan"), dtype=torch.float16, device="cuda")
+    oy = torch.empty_like(ox)
+    oz = torch.full_like(ox, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        px.run(qx, kx, vx, ox)
+        g.capture_begin()
+        pz.run(qz, kz, vz, oy)
+        g.capture_end()
+        pz.run(ox, kz, vz, oz)
+    s.synchronize()
+    rx = torch.empty_like(ox)
+    rz = torch.empty_like(ox)
+    mg.Plan(16, 256, 16384, d, flags=EARLY_OFF).run(qx, kx, vx, rx)
+    torch.cuda.synchronize()
+    mg.Plan(16, 256, 4096, d, flags=EARLY_OFF).run(rx, kz, vz, rz)
+    torch.cuda.synchronize()
+    assert torch.equal(ox, rx) and torch.equal(oz, rz)
+
+
+def test_early_loads_leave_results_unchanged():
+    # Distinct buffers back to back (the early loads taken) against the same calls with them off.
+    q, k, v, (B, M, N, d) = inputs.make_config("gqa")
+    sets = [tuple(t.cuda() for t in inputs.make_inputs(B, M, N, d, 0.5, seed=100 + i)) for i in range(4)]
+    for flags in (0, mg.MG_FLAG_NO_CLUSTER):
+        a = mg.Plan(B, M, N, d, flags=flags)
+        b = mg.Plan(B, M, N, d, flags=flags | EARLY_OFF)
+        oa = [torch.empty((B, M, d), dtype=torch.float16, device="cuda") for _ in sets]
+        ob = [torch.empty_like(x) for x in oa]
+        for x, o in zip(sets, oa):
+            a.run(*x, o)
+        torch.cuda.synchronize()
+        for x, o in zip(sets, ob):
+            b.run(*x, o)
+        torch.cuda.synchronize()
+        assert all(torch.equal(x, y) for x, y in zip(oa, ob))
+
+
 def test_host_buffer_entry_point_pageable_and_large():
     # Pageable host tensors take the copy-engine path; pinned ones the mapped-copy kernels. Both
     # on a shape with a split combine and several copy rounds per thread.
