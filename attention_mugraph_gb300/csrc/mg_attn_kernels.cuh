@@ -497,44 +497,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- TMA producer
         // Lane 0 issues every copy. Early loads: Q and the first STAGES steps' tiles go out before
         // the wait for the previous grid (the host allows it only when that grid writes none of
-        // Q, K and V), so their DRAM latency overlaps the previous call's end; the whole warp then
-        // waits (after lane 0's issues: a lane blocked in the wait would hold back the others).
-        bool q_armed = false;
-        int armed[STAGES];
-#pragma unroll
-        for (int s = 0; s < STAGES; ++s)
-            armed[s] = 0;
-        bool ok = true;
-        int t = 0;  // the next step to issue (lane 0)
-        // One step's copies into stage t % STAGES, once that stage is free.
-        auto issue = [&](int t) {
-            const int s = t % STAGES;
-            const int n0 = tile_of(t < T1 ? t : t - T1) * kBlockN;
-            const int bt = batch_of(t < T1 ? t : t - T1);
-            const uint32_t sK = sStage0 + s * C::kStageBytes;
-            const uint32_t sV = sK + C::kKBytes;
-            // K and V land on separate barriers: S = Q.K need not wait for V. A step of the
-            // row-maximum pass loads no V; its V barrier phase completes on a plain arrival,
-            // so every step advances every barrier of its stage by one phase.
-            ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), C::kKBytes);
-            if (t < T1)
-                ptx::mbar_arrive(bar(BI::kVFull + s));
-            else
-                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
-            ++armed[s];
-            // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
-            ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, bt);
-            ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, bt);
-            // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
-            if (t >= T1) {
-#pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, bt);
+        // Q, K and V), so their DRAM latency overlaps the previous call's end. The other lanes
+        // take the wait only once lane 0 has issued them (a lane blocked in the wait would hold
+        // lane 0 back): the warp meets at a __syncwarp from both paths.
+        if (lane != 0) {
+            if (p.early_loads) {
+                __syncwarp();
+                ptx::griddep_wait();
+                ptx::griddep_launch_dependents();
             }
-        };
-        if (lane == 0) {
+        } else {
+            bool q_armed = false;
+            int armed[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s)
+                armed[s] = 0;
+            bool ok = true;
+            // One step's copies into stage t % STAGES, once that stage is free.
+            auto issue = [&](int t) {
+                const int s = t % STAGES;
+                const int n0 = tile_of(t < T1 ? t : t - T1) * kBlockN;
+                const int bt = batch_of(t < T1 ? t : t - T1);
+                const uint32_t sK = sStage0 + s * C::kStageBytes;
+                const uint32_t sV = sK + C::kKBytes;
+                // K and V land on separate barriers: S = Q.K need not wait for V. A step of the
+                // row-maximum pass loads no V; its V barrier phase completes on a plain arrival,
+                // so every step advances every barrier of its stage by one phase.
+                ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), C::kKBytes);
+                if (t < T1)
+                    ptx::mbar_arrive(bar(BI::kVFull + s));
+                else
+                    ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), C::kVBytes);
+                ++armed[s];
+                // K[b, 0:d, n0:n0+64] and K[b, 0:d, n0+64:n0+128]: d rows of 128 bytes each.
+                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, bt);
+                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, bt);
+                // V[b, n0:n0+128, 64c:64c+64]: 128 rows of 128 bytes each.
+                if (t >= T1) {
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        ptx::tma_load_3d(sV + c * C::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, bt);
+                }
+            };
             if (p.inject_timeout)
                 ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
+            int t = 0;  // the next step to issue
             if (ok) {
                 if constexpr (kSK) {
                     // One compact Q tile per segment (kSkQRows rows of 128-byte chunks: the tensor
@@ -557,13 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (; t < U && t < STAGES; ++t)  // the stages are free: no wait
                         issue(t);
             }
-        }
-        if (p.early_loads) {
-            __syncwarp();
-            ptx::griddep_wait();
-            ptx::griddep_launch_dependents();
-        }
-        if (lane == 0) {
+            if (p.early_loads) {
+                __syncwarp();
+                ptx::griddep_wait();
+                ptx::griddep_launch_dependents();
+            }
             for (; ok && t < U; ++t) {
                 const int s = t % STAGES;
                 const uint32_t round = static_cast<uint32_t>(t / STAGES);

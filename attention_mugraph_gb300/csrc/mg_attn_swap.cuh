@@ -194,31 +194,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         // Lane 0 issues every copy; early loads as in the one-tile kernel (Q and the first STAGES
-        // tiles before the warp's wait for the previous grid).
-        bool q_armed = false;
-        int armed[STAGES];
+        // tiles before the warp's wait for the previous grid, which the other lanes take only
+        // once lane 0 has issued them: the warp meets at a __syncwarp from both paths).
+        if (lane != 0) {
+            if (p.early_loads) {
+                __syncwarp();
+                ptx::griddep_wait();
+                ptx::griddep_launch_dependents();
+            }
+        } else {
+            bool q_armed = false;
+            int armed[STAGES];
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s)
-            armed[s] = 0;
-        bool ok = true;
-        int t = 0;  // the next tile to issue (lane 0)
-        auto issue = [&](int t) {
-            const int s = t % STAGES;
-            const int n0 = tile_of(t) * kBlockN;
-            const uint32_t sK = sStage0 + s * kSwapStageBytes;
-            const uint32_t sV = sK + D * kBlockN * 2;
-            ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), D * kBlockN * 2);
-            ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), kBlockN * D * 2);
-            ++armed[s];
-            ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
-            ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
+            for (int s = 0; s < STAGES; ++s)
+                armed[s] = 0;
+            bool ok = true;
+            auto issue = [&](int t) {
+                const int s = t % STAGES;
+                const int n0 = tile_of(t) * kBlockN;
+                const uint32_t sK = sStage0 + s * kSwapStageBytes;
+                const uint32_t sV = sK + D * kBlockN * 2;
+                ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), D * kBlockN * 2);
+                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), kBlockN * D * 2);
+                ++armed[s];
+                ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
+                ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                ptx::tma_load_3d(sV + c * TileCfg<D>::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
-        };
-        if (lane == 0) {
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_load_3d(sV + c * TileCfg<D>::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
+            };
             if (p.inject_timeout)
                 ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
+            int t = 0;  // the next tile to issue
             if (ok) {
                 // Q[b, 0:16, 64c:64c+64] (the tensor map's box is 16 rows; rows past M read as zero).
                 ptx::mbar_arrive_expect_tx(bar(BI::kQFull), kSwapQBytes);
@@ -227,16 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d(sQ + c * kSwapChunk, &tmQ, bar(BI::kQFull), c * 64, 0, b);
                 if (p.early_loads)
-                    for (; t < T && t < STAGES; ++t)
+                    for (; t < T && t < STAGES; ++t)  // the stages are free: no wait
                         issue(t);
             }
-        }
-        if (p.early_loads) {
-            __syncwarp();
-            ptx::griddep_wait();
-            ptx::griddep_launch_dependents();
-        }
-        if (lane == 0) {
+            if (p.early_loads) {
+                __syncwarp();
+                ptx::griddep_wait();
+                ptx::griddep_launch_dependents();
+            }
             for (; ok && t < T; ++t) {
                 const int s = t % STAGES;
                 const uint32_t round = static_cast<uint32_t>(t / STAGES);
