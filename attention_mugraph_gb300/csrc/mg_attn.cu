@@ -505,12 +505,14 @@ cudaError_t launch_copy(const CopyJobs &jobs, int num_sms, bool pdl, cudaStream_
 // Whether the current device can hold all ctas / n clusters of n CTAs of the fused kernel at
 // once (one wave: a cluster left for a second wave would double the time). Sizes above 8 need
 // the non-portable opt-in. Clears any error it provokes.
-bool cluster_schedulable(FwdKernel fwd, int n, int ctas, int smem)
+// How many clusters of n CTAs of `fwd` (with `smem` bytes of dynamic shared memory each) the
+// device holds at once; -1 if the query fails.
+int max_active_clusters(FwdKernel fwd, int n, int ctas, int smem)
 {
     if (n > 8 && cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd),
                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        return -1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
@@ -526,9 +528,86 @@ bool cluster_schedulable(FwdKernel fwd, int n, int ctas, int smem)
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(fwd), &cfg) != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        return -1;
     }
-    return clusters >= (ctas + n - 1) / n;
+    return clusters;
+}
+
+// The kernel's dynamic shared-memory limit raised to the plan's (before any occupancy query: at
+// the default 48 KB limit the query would refuse the launch).
+cudaError_t raise_smem_limit(FwdKernel fwd, int smem)
+{
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+// Places the on-chip combine's clusters on the device (the plan's kernel limit already raised).
+// Back to back, a call's CTAs start while the previous call runs (programmatic dependent launch)
+// and load early, but a cluster starts only where the device has room for it beside the previous
+// call's clusters; the device holds fewer clusters of 13-16 CTAs than of 11-12 (GB300: 7 and 8).
+// Without an explicit n_split, when two calls' clusters do not fit side by side, a smaller
+// cluster with at most one more column tile per CTA that lets them is taken; failing that, when
+// even one call's clusters do not fit, a smaller cluster that fits (same bound), and failing
+// that the second-kernel combine. Measured on GB300 (us per call, back to back): (2, 256, 4096,
+// 64) 5.80 with 12 splits against 6.21 with 16 (of which 7 clusters fit at once, not the 8 of
+// two calls); (4, 256, 4096, 64) 7.23 with 11 against 8.41 with 16 through the second kernel.
+mg_status place_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int sms,
+                         int smem_optin, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags,
+                         FwdKernel *fwd)
+{
+    if (info->cluster_ctas == 0)
+        return MG_OK;
+    const int n = info->cluster_ctas;
+    const int units = info->grid_ctas / n;
+    const int act = max_active_clusters(*fwd, n, info->grid_ctas, info->smem_bytes);
+    if (act >= 2 * units)
+        return MG_OK;
+    mg_attn_options o{};
+    if (opts)
+        o = *opts;
+    // The one-tile kernel's two-pass variants stream each tile twice: one more tile per CTA costs
+    // them more than the overlap gains (QK-norm on (2, 256, 4096, 64): 10.58 us with 12 splits
+    // against 9.59 with 16), so they change the cluster only when it does not fit.
+    const bool two_pass = (*flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) && info->swap_ab == 0;
+    if (o.n_split == 0) {
+        const int t = (info->n_tiles + n - 1) / n;
+        for (int pass = two_pass ? 1 : 0; pass < 2; ++pass) {
+            if (pass == 1 && act >= units)
+                break;
+            for (int c = n - 1; c >= 2 && (info->n_tiles + c - 1) / c <= t + 1; --c) {
+                mg_attn_options oc = o;
+                oc.n_split = c;
+                mg_attn_plan_info ic;
+                unsigned long long to = 0;
+                int fl = 0;
+                if (decide(B, M, N, d, &oc, sms, smem_optin, &ic, &to, &fl) != MG_OK || ic.cluster_ctas != c)
+                    continue;
+                FwdKernel f = plan_kernel(ic, fl);
+                if (raise_smem_limit(f, ic.smem_bytes) != cudaSuccess) {
+                    cudaGetLastError();
+                    continue;
+                }
+                const int u = ic.grid_ctas / c;
+                if (max_active_clusters(f, c, ic.grid_ctas, ic.smem_bytes) >= (pass == 0 ? 2 * u : u)) {
+                    *info = ic;
+                    *timeout_ns = to;
+                    *flags = fl;
+                    *fwd = f;
+                    return MG_OK;
+                }
+            }
+        }
+    }
+    if (act >= units)
+        return MG_OK;
+    // The device cannot place the clusters: plan again with the second-kernel combine (whose
+    // kernel carries that epilogue: its limit is raised as well).
+    o.flags |= MG_FLAG_NO_CLUSTER;
+    mg_status st = decide(B, M, N, d, &o, sms, smem_optin, info, timeout_ns, flags);
+    if (st != MG_OK)
+        return st;
+    *fwd = plan_kernel(*info, *flags);
+    const cudaError_t e = raise_smem_limit(*fwd, info->smem_bytes);
+    return e == cudaSuccess ? MG_OK : cuda_fail(e, "cudaFuncSetAttribute");
 }
 
 // Launch attributes of the fused kernel: programmatic dependent launch and the cluster shape.
@@ -659,19 +738,8 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
         return fail(MG_ERR_UNSUPPORTED, "no sm_103a kernel image for device %d", dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
-    if (info.cluster_ctas > 0 && !cluster_schedulable(fwd, info.cluster_ctas, info.grid_ctas, info.smem_bytes)) {
-        // The device cannot place the cluster: plan again with the second-kernel combine.
-        mg_attn_options o{};
-        if (opts)
-            o = *opts;
-        o.flags |= MG_FLAG_NO_CLUSTER;
-        if ((st = decide(B, M, N, d, &o, sms, smem_optin, &info, &timeout_ns, &flags)) != MG_OK)
-            return st;
-        fwd = plan_kernel(info, flags);
-        if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      info.smem_bytes)) != cudaSuccess)
-            return cuda_fail(e, "cudaFuncSetAttribute");
-    }
+    if ((st = place_clusters(B, M, N, d, opts, sms, smem_optin, &info, &timeout_ns, &flags, &fwd)) != MG_OK)
+        return st;
 
     struct mg_attn_plan *p = new (std::nothrow) struct mg_attn_plan();
     if (!p)
@@ -1132,17 +1200,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, in.smem_bytes);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
-    if (in.cluster_ctas > 0 && !cluster_schedulable(fwd, in.cluster_ctas, in.grid_ctas, in.smem_bytes)) {
-        mg_attn_options o{};
-        o.flags = MG_FLAG_NO_CLUSTER;
-        if ((st = decide(B, M, N, d, &o, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags)) != MG_OK)
-            return st;
-        // The fallback's kernel carries the second kernel's epilogue: its limit is set as well.
-        fwd = plan_kernel(in, 0);
-        if ((e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fwd), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      in.smem_bytes)) != cudaSuccess)
-            return cuda_fail(e, "cudaFuncSetAttribute");
-    }
+    if ((st = place_clusters(B, M, N, d, nullptr, sd->sms, sd->smem_optin, &in, &timeout_ns, &flags, &fwd)) != MG_OK)
+        return st;
     if (in.workspace_bytes > static_cast<int64_t>(MG_ATTN_STATIC_SCRATCH_BYTES))
         return fail(MG_ERR_INVALID_ARG,
                     "shape needs %lld bytes of split scratch; the static scratch holds %u bytes "

@@ -348,6 +348,22 @@ def test_swap_ab_matches_one_tile_kernel_and_is_reproducible():
     assert_parity(O3, ref, "one-tile")
 
 
+def test_cluster_placement_for_back_to_back_calls():
+    # Without an explicit n_split, a plan takes a cluster size whose clusters of two back-to-back
+    # calls the device holds at once (GB300 holds 7 clusters of 13-16 CTAs, 8 of 11-12), within
+    # one more column tile per CTA; an explicit n_split is kept.
+    gqa = mg.Plan(2, 256, 4096, 64).info
+    assert gqa["cluster_ctas"] == gqa["n_split"] and 11 <= gqa["n_split"] <= 12
+    assert mg.Plan(2, 256, 4096, 64, n_split=16).info["cluster_ctas"] == 16
+    assert mg.Plan(1, 256, 4096, 64).info["cluster_ctas"] == 16  # two calls: 4 clusters
+    b4 = mg.Plan(4, 256, 4096, 64).info  # 16-CTA clusters do not fit once: a smaller cluster
+    assert b4["cluster_ctas"] == b4["n_split"] and 11 <= b4["n_split"] <= 12 and b4["kernels_per_run"] == 1
+    for shape in [(2, 256, 4096, 64), (4, 256, 4096, 64)]:
+        q, k, v = inputs.make_inputs(*shape, 0.5, seed=sum(shape))
+        O, plan = run_gpu(q, k, v)
+        assert_parity(O, oracle.attention(q, k, v), f"{shape} n_split={plan.info['n_split']}")
+
+
 def test_k_zero_gives_mean_of_v_with_ragged_tail():
     # Scores 0 everywhere -> every weight is exp(0)=1: any column past N that leaked into the row
     # sum (zero-filled K gives exp(0)=1 too) would pull the mean toward 0.
