@@ -546,10 +546,11 @@ cudaError_t raise_smem_limit(FwdKernel fwd, int smem)
 // call's clusters; the device holds fewer clusters of 13-16 CTAs than of 11-12 (GB300: 7 and 8).
 // Without an explicit n_split, when two calls' clusters do not fit side by side, a smaller
 // cluster with at most one more column tile per CTA that lets them is taken; failing that, when
-// even one call's clusters do not fit, a smaller cluster that fits (same bound), and failing
-// that the second-kernel combine. Measured on GB300 (us per call, back to back): (2, 256, 4096,
-// 64) 5.80 with 12 splits against 6.21 with 16 (of which 7 clusters fit at once, not the 8 of
-// two calls); (4, 256, 4096, 64) 7.23 with 11 against 8.41 with 16 through the second kernel.
+// even one call's clusters do not fit, a smaller cluster that fits with at most two more, and
+// failing that the second-kernel combine. Measured on GB300 (us per call, back to back):
+// (2, 256, 4096, 64) 5.80 with 12 splits against 6.21 with 16 (of which 7 clusters fit at once,
+// not the 8 of two calls); (4, 256, 4096, 64) 7.22 with 12 against 8.41 with 16 through the
+// second kernel; (8, 256, 4096, 64) 8.11 with 6 against 9.66 with 9 through the second kernel.
 mg_status place_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int sms,
                          int smem_optin, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags,
                          FwdKernel *fwd)
@@ -573,7 +574,7 @@ mg_status place_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_at
         for (int pass = two_pass ? 1 : 0; pass < 2; ++pass) {
             if (pass == 1 && act >= units)
                 break;
-            for (int c = n - 1; c >= 2 && (info->n_tiles + c - 1) / c <= t + 1; --c) {
+            for (int c = n - 1; c >= 2 && (info->n_tiles + c - 1) / c <= t + 1 + pass; --c) {
                 mg_attn_options oc = o;
                 oc.n_split = c;
                 mg_attn_plan_info ic;

@@ -296,9 +296,10 @@ mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info);
  * touching any GPU. Same validation and error codes as mg_attn_plan_ex (minus device errors).
  * The one decision it cannot take is the placement of the on-chip combine's clusters, which
  * mg_attn_plan_ex asks the device about: how many clusters of the chosen size it holds at once.
- * Without an explicit n_split the plan then takes a smaller cluster (at most one more column
- * tile per CTA) when that lets the clusters of two back-to-back calls be resident together, or
- * when the chosen clusters do not fit at all, and otherwise falls back to the second kernel;
+ * Without an explicit n_split the plan then takes a smaller cluster when that lets the clusters
+ * of two back-to-back calls be resident together (at most one more column tile per CTA), or
+ * when the chosen clusters do not fit at all (at most two more), and otherwise falls back to
+ * the second kernel;
  * the one-tile kernel's two-pass variants keep the chosen cluster whenever it fits.
  */
 mg_status mg_attn_query(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts,

@@ -358,7 +358,9 @@ def test_cluster_placement_for_back_to_back_calls():
     assert mg.Plan(1, 256, 4096, 64).info["cluster_ctas"] == 16  # two calls: 4 clusters
     b4 = mg.Plan(4, 256, 4096, 64).info  # 16-CTA clusters do not fit once: a smaller cluster
     assert b4["cluster_ctas"] == b4["n_split"] and 11 <= b4["n_split"] <= 12 and b4["kernels_per_run"] == 1
-    for shape in [(2, 256, 4096, 64), (4, 256, 4096, 64)]:
+    b8 = mg.Plan(8, 256, 4096, 64).info  # 9-CTA clusters do not fit once: at most two more tiles
+    assert b8["cluster_ctas"] == b8["n_split"] == 6 and b8["kernels_per_run"] == 1
+    for shape in [(2, 256, 4096, 64), (4, 256, 4096, 64), (8, 256, 4096, 64)]:
         q, k, v = inputs.make_inputs(*shape, 0.5, seed=sum(shape))
         O, plan = run_gpu(q, k, v)
         assert_parity(O, oracle.attention(q, k, v), f"{shape} n_split={plan.info['n_split']}")
