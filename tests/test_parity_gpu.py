@@ -64,6 +64,50 @@ def test_workload_parity_full_size(name):
     assert_parity(O, ref, f"{name} n_split={plan.info['n_split']}")
 
 
+@pytest.mark.parametrize("name", inputs.CONFIG_ORDER)
+def test_workload_parity_in_the_bench_launch_configuration(name):
+    # The benchmark's timed launch: back-to-back calls captured in one CUDA graph over rotating
+    # input sets (so every call but the graph's first loads its inputs early, while the previous
+    # call runs), the default plan (cluster placement included), replayed twice. Every output is
+    # checked: in full against the oracle for the smaller workloads, on 64 sampled rows per
+    # batch set for the two largest.
+    sets = [inputs.make_config(name, seed=s)[:3] for s in range(3)]
+    B, M, N, d = inputs.CONFIGS[name][:4]
+    plan = mg.Plan(B, M, N, d)
+    dev = [tuple(t.cuda() for t in x) for x in sets]
+    outs = [torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda") for _ in range(6)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.run(*dev[0], outs[0])  # an eager call first, as the bench's warm-up
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        for i, o in enumerate(outs):
+            plan.run(*dev[i % 3], o)
+        g.capture_end()
+    for _ in range(2):
+        with torch.cuda.stream(s):
+            g.replay()
+    s.synchronize()
+    assert plan.status() == mg.MG_OK
+    big = B * N * d * 2 * 2 > 100_000_000
+    rng = np.random.default_rng(5)
+    for j, (q, k, v) in enumerate(sets):
+        if big:
+            rows = np.sort(rng.choice(B * M, size=min(64, B * M), replace=False))
+            ref = oracle.attention_rows(q, k, v, rows)
+        else:
+            ref = oracle.attention(q, k, v)
+        for i in range(j, 6, 3):
+            o = outs[i].float().cpu().numpy().astype(np.float64)
+            got = o.reshape(B * M, d)[rows] if big else o
+            err = np.abs(got - ref)
+            assert np.isfinite(got).all() and (err <= 2e-3 * (1.0 + np.abs(ref))).all(), \
+                f"{name} call {i} (set {j}) n_split={plan.info['n_split']}: max err {err.max():.3e}"
+
+
 SWEEP = [  # (B, M, N, d, n_split) with ragged M (not a multiple of 128) and N (not of 128)
     (1, 1, 8, 64, 0), (1, 1, 8, 128, 0), (3, 129, 136, 64, 0), (2, 300, 1000, 64, 3),
     (1, 127, 4104, 128, 0), (2, 200, 2056, 64, 1), (1, 128, 128, 64, 1), (4, 64, 6216, 64, 7),
