@@ -821,21 +821,31 @@ mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info)
     return MG_OK;
 }
 
-// The output ranges of the last call enqueued on each stream (O as passed to mg_attn_run; hO and
-// its device address for mg_attn_run_host). A call's first kernel (the host-buffer call's copy
-// kernel, or the fused kernel) may load its inputs before the previous kernel on its stream has
-// finished, and only that kernel: every earlier one has completed by the time it can start (each
-// of this library's kernels releases its dependents only after its own wait, and a kernel of
-// another origin releases them when it completes). So the loads are early unless an input shares
-// bytes with the previous call's output on that stream (a chain of calls) or with the call's own
-// output, or the previous call is unknown: the first call on a stream (or one whose record was
-// displaced by 64 newer streams), and the first call of a stream capture. Calls enqueued under
-// capture are recorded apart from the stream's eager calls (keyed by the capture's id), since
-// the captured kernels run later, as one graph.
+// The output ranges of the last kWindow calls enqueued on each stream (O as passed to
+// mg_attn_run; hO and its device address for mg_attn_run_host). A call's first kernel (the
+// host-buffer call's copy kernel, or the fused kernel) may read its inputs before the previous
+// grid on its stream has completed. Which earlier kernels can still run then:
+// * A kernel that releases its dependents after its own wait (every kernel of this library but
+//   the fused kernel started at level 2, and a kernel of another origin, which releases them when
+//   it completes unless it triggers early itself) has every kernel before it completed by the
+//   time the next one can start.
+// * A fused kernel at level 2 releases them at its start. A kernel cannot complete before the one
+//   before it, so when kernel i still runs every later kernel does too, all their CTAs resident
+//   (none can exit before its wait). Level 2 is used only for grids of at least kEarlyMinCtas
+//   CTAs of one per SM, so fewer than kWindow such kernels fit the device together.
+// So the reads are early only when the previous call on the stream is known and no input shares
+// bytes with the outputs of the last kWindow calls or with the call's own output. The first call
+// on a stream, or one whose records were displaced by kStreamSlots newer streams, is not known,
+// and nor is the first call of a stream capture. Calls enqueued under capture are recorded apart
+// from the stream's eager calls, keyed by the capture's id, since the captured kernels run later
+// as one graph.
+constexpr int kWindow = 16;
+constexpr int kEarlyMinCtas = 10;  // 152 SMs / 10 < kWindow
 struct OutRanges {
     cudaStream_t stream = nullptr;
-    unsigned long long capture = 0;            // the capture's id, 0 for eager calls
-    uintptr_t lo[2] = {0, 0}, hi[2] = {0, 0};  // [lo, hi) ranges; empty when lo == hi
+    unsigned long long capture = 0;                     // the capture's id, 0 for eager calls
+    uintptr_t lo[kWindow][2] = {}, hi[kWindow][2] = {};  // [lo, hi) ranges; empty when lo == hi
+    int calls = 0;                                       // calls recorded (the newest at (calls-1) % kWindow)
     unsigned long long age = 0;
     bool used = false;
 };
@@ -865,12 +875,16 @@ OutRanges *find_slot(cudaStream_t stream, unsigned long long capture, bool claim
         if (!r.used || (oldest->used && r.age < oldest->age))
             oldest = &r;
     }
-    return claim ? oldest : nullptr;
+    if (claim) {
+        *oldest = OutRanges{};
+        return oldest;
+    }
+    return nullptr;
 }
 
-// The output ranges of the last call enqueued on `stream` under the same capture (or none);
-// `used` is false when that call is unknown.
-OutRanges last_outputs(cudaStream_t stream)
+// The output ranges of the recent calls enqueued on `stream` under the same capture (or none);
+// `used` is false when the previous call is unknown.
+OutRanges recent_outputs(cudaStream_t stream)
 {
     const unsigned long long capture = capture_of(stream);
     if (capture == ~0ull)
@@ -890,10 +904,12 @@ void record_outputs(cudaStream_t stream, const void *a, size_t na, const void *b
     slot->stream = stream;
     slot->capture = capture;
     slot->age = ++g_out_clock;
-    slot->lo[0] = reinterpret_cast<uintptr_t>(a);
-    slot->hi[0] = slot->lo[0] + (a ? na : 0);
-    slot->lo[1] = reinterpret_cast<uintptr_t>(b);
-    slot->hi[1] = slot->lo[1] + (b ? nb : 0);
+    const int k = slot->calls % kWindow;
+    slot->lo[k][0] = reinterpret_cast<uintptr_t>(a);
+    slot->hi[k][0] = slot->lo[k][0] + (a ? na : 0);
+    slot->lo[k][1] = reinterpret_cast<uintptr_t>(b);
+    slot->hi[k][1] = slot->lo[k][1] + (b ? nb : 0);
+    ++slot->calls;
 }
 
 bool overlaps_range(const void *p, size_t n, uintptr_t lo, uintptr_t hi)
@@ -902,25 +918,51 @@ bool overlaps_range(const void *p, size_t n, uintptr_t lo, uintptr_t hi)
     return lo < hi && x < hi && lo < x + n;
 }
 
-// Whether a call's first kernel may load its inputs before the previous grid on `stream` has
+// Whether a call's first kernel may read its inputs before the previous grid on `stream` has
 // completed: the previous call is known and no input (n[i] bytes at p[i], host or device address)
-// shares bytes with its outputs or with this call's own output [o, o + no).
+// shares bytes with the outputs of the last kWindow calls or with this call's own output
+// [o, o + no).
 bool may_load_early(cudaStream_t stream, const void *const *p, const size_t *n, int count, const void *o, size_t no)
 {
-    const OutRanges prev = last_outputs(stream);
-    if (!prev.used)
+    const OutRanges prev = recent_outputs(stream);
+    if (!prev.used || prev.calls == 0)
         return false;
     const uintptr_t ol = reinterpret_cast<uintptr_t>(o);
+    const int recorded = prev.calls < kWindow ? prev.calls : kWindow;
     for (int i = 0; i < count; ++i) {
         if (!p[i])
             continue;
         if (overlaps_range(p[i], n[i], ol, ol + no))
             return false;
-        for (int r = 0; r < 2; ++r)
-            if (overlaps_range(p[i], n[i], prev.lo[r], prev.hi[r]))
-                return false;
+        for (int k = 0; k < recorded; ++k)
+            for (int r = 0; r < 2; ++r)
+                if (overlaps_range(p[i], n[i], prev.lo[k][r], prev.hi[k][r]))
+                    return false;
     }
     return true;
+}
+
+// How much of the fused kernel may run before the previous grid on the stream completes
+// (FwdParams::early): 1, its first copies, where may_load_early allows; 2, everything but its
+// global writes, with its dependents released at its start, for the one-tile and few-row kernels
+// under the split schedule with grids of at least kEarlyMinCtas CTAs, but not the one-tile
+// kernel's QK-norm (its key scales go through global memory). Measured on GB300 (us per call,
+// back to back): level 1 against 0, gqa 6.17 against 6.50, tiny 4.56 against 5.44, gqa_b8 9.86
+// against 10.03, long_kv 14.52 against 14.82, decode 46.0 against 46.7, decode_m1 24.6 against
+// 25.0; level 2, gqa 3.59 against 5.81 (two calls' clusters resident together, their work
+// overlapping), tiny 1.66 against 4.47, (1, 256, 4096, 64) 2.15 against 5.61.
+int early_level(const mg_attn_plan_info &in, int flags, cudaStream_t stream, const void *Q, const void *K,
+                const void *V, const void *O)
+{
+    if (in.q_tiles_per_cta != 1)
+        return 0;
+    const size_t bq = static_cast<size_t>(in.B * in.M * in.d) * 2, bk = static_cast<size_t>(in.B * in.d * in.N) * 2;
+    const void *inp[3] = {Q, K, V};
+    const size_t nb[3] = {bq, bk, bk};
+    if (!may_load_early(stream, inp, nb, 3, O, bq))
+        return 0;
+    const bool qk_one_tile = (flags & MG_FLAG_QK_NORM) && in.swap_ab == 0;
+    return in.schedule == 0 && !qk_one_tile && in.grid_ctas >= kEarlyMinCtas ? 2 : 1;
 }
 
 // mg_attn_run's work; `allow_early`: the fused kernel may load Q, K and V before the previous
@@ -975,19 +1017,9 @@ static mg_status run_fused(mg_attn_plan_t plan, const void *Q, const void *K, co
 
     cudaLaunchAttribute attr[2];
     const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
-    // Early loads (the one-tile and few-row kernels; not with the injected timeout, whose wait
-    // comes before the loads). Measured on GB300 (us per call, back to back, against
-    // MG_FLAG_NO_EARLY_LOADS): gqa 6.17 against 6.50, tiny 4.56 against 5.44, gqa_b8 9.86
-    // against 10.03, long_kv 14.52 against 14.82, decode 46.0 against 46.7, decode_m1 24.6
-    // against 25.0.
-    prm.early_loads = 0;
-    if (allow_early && pdl && !prm.inject_timeout && in.q_tiles_per_cta == 1 &&
-        !(plan->flags & MG_FLAG_NO_EARLY_LOADS)) {
-        const size_t bq = static_cast<size_t>(B * M * d) * 2, bk = static_cast<size_t>(B * d * N) * 2;
-        const void *inp[3] = {Q, K, V};
-        const size_t nb[3] = {bq, bk, bk};
-        prm.early_loads = may_load_early(reinterpret_cast<cudaStream_t>(stream), inp, nb, 3, O, bq) ? 1 : 0;
-    }
+    prm.early = allow_early && pdl && !prm.inject_timeout && !(plan->flags & MG_FLAG_NO_EARLY_LOADS)
+                    ? early_level(in, plan->flags, reinterpret_cast<cudaStream_t>(stream), Q, K, V, O)
+                    : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(in.grid_ctas), 1, 1);
@@ -1242,12 +1274,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.col_scale = nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
-    {
-        const size_t bq = static_cast<size_t>(B * M * d) * 2, bk = static_cast<size_t>(B * d * N) * 2;
-        const void *inp[3] = {Q, K, V};
-        const size_t nb[3] = {bq, bk, bk};
-        prm.early_loads = may_load_early(reinterpret_cast<cudaStream_t>(stream), inp, nb, 3, O, bq) ? 1 : 0;
-    }
+    prm.early = early_level(in, flags, reinterpret_cast<cudaStream_t>(stream), Q, K, V, O);
     prm.sk_units = static_cast<long long>(in.m_tiles) * in.n_tiles;
     prm.sk_ctas = in.grid_ctas;
     prm.sk_slots = in.n_split;

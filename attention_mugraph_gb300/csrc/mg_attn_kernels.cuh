@@ -134,8 +134,11 @@ struct FwdParams {
     int *status;             // [0] sticky status, [1] which wait ran out
     unsigned long long timeout_ns;
     int inject_timeout;
-    int early_loads;         // the load warp issues Q and the first STAGES K/V tiles before it waits
-                             // for the previous grid (the host found that grid writes none of them)
+    int early;               // what runs before the wait for the previous grid (the host found that no
+                             // kernel that may still run writes Q, K or V): 0 nothing; 1 the load
+                             // warp's Q and first STAGES K/V copies; 2 everything but the global
+                             // writes, with the dependents released at the start (not with QK-norm's
+                             // key scales or the stream-K schedule, which write global memory midway)
     long long sk_units;      // stream-K: B * n_tiles units (row tile, column tile)
     int sk_ctas;             // stream-K: G, the grid
     int sk_slots;            // stream-K: partial slots per row tile (the second kernel's split count)
@@ -188,6 +191,7 @@ __device__ __forceinline__ bool wait_bounded(const WaitCtx &w, uint32_t bar, uin
             return false;
         if (ptx::globaltimer_ns() - t0 > w.timeout_ns) {
             *w.abort_flag = 1;
+            ptx::griddep_wait();  // (early start) global memory only after the previous grid
             if (atomicCAS(w.status, 0, kStatusTimeout) == 0)
                 atomicExch(w.status + 1, where);
             return false;
@@ -481,11 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPushX && cluster)
         ptx::cluster_arrive_release();
 
-    // Everything above touched only on-chip state; global memory waits for the previous grid,
-    // except the early loads of the load warp (below). Every thread releases the dependents only
-    // after its own wait, so a grid launched after this one never starts before the one before
-    // this one has completed.
-    if (!(warp == 0 && p.early_loads)) {
+    // Everything above touched only on-chip state; global memory waits for the previous grid.
+    // early == 1: the load warp's first copies go out before its wait (below); every thread
+    // releases the dependents after its own wait, so a grid launched after this one never starts
+    // before the one before this one has completed. early == 2: the dependents are released now,
+    // every role runs without the wait, and each global write waits for the previous grid first
+    // (the reads of Q, K and V may then overlap kernels further back; the host checks its recent
+    // outputs for that).
+    if (p.early == 2) {
+        ptx::griddep_launch_dependents();
+    } else if (!(warp == 0 && p.early == 1)) {
         ptx::griddep_wait();
         ptx::griddep_launch_dependents();
     }
@@ -501,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // take the wait only once lane 0 has issued them (a lane blocked in the wait would hold
         // lane 0 back): the warp meets at a __syncwarp from both paths.
         if (lane != 0) {
-            if (p.early_loads) {
+            if (p.early == 1) {
                 __syncwarp();
                 ptx::griddep_wait();
                 ptx::griddep_launch_dependents();
@@ -560,11 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < C::kChunks; ++c)  // Q[b, m0:m0+128, 64c:64c+64]
                         ptx::tma_load_3d(sQ + c * C::kChunkRows128, &tmQ, bar(BI::kQFull), c * 64, m0, b);
                 }
-                if (p.early_loads)
+                if (p.early == 1)
                     for (; t < U && t < STAGES; ++t)  // the stages are free: no wait
                         issue(t);
             }
-            if (p.early_loads) {
+            if (p.early == 1) {
                 __syncwarp();
                 ptx::griddep_wait();
                 ptx::griddep_launch_dependents();
@@ -809,6 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sum_sq_cols(*reinterpret_cast<const uint4 *>(kp + k * 1024), sq);
                     const float c = __frsqrt_rn(reduce_scatter8(sq, lane) * (1.f / D) + kQkNormEps);
                     cs_tile[my_col] = c;
+                    if (p.early == 2)  // (the host does not start this variant early; kept safe)
+                        ptx::griddep_wait();
                     if (tile_of(u) * kBlockN + my_col < p.N)
                         col_scale[static_cast<size_t>(tile_of(u)) * kBlockN + my_col] = c;
                 }
@@ -990,6 +1001,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
             } else {
                 ptx::tc_fence_after();
+                if (p.early == 2)  // (the host does not start this schedule early; kept safe)
+                    ptx::griddep_wait();
                 const int r = r0 + k;
                 const int c_first = static_cast<int>(sk_cta_of(static_cast<long long>(r) * p.n_tiles, p.sk_units, p.sk_ctas));
                 const int c_last = static_cast<int>(
@@ -1165,11 +1178,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (cluster) {
                 if (g == 0)
                     stage_lm[row * C::kLmw + D / 32] = m;
-            } else if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
-                const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
-                p.ws_l[r] = l;
-                if (kSafeMax)
-                    p.ws_m[r] = m;
+            } else {
+                if (p.early == 2)
+                    ptx::griddep_wait();  // the global writes below (and the TMA store) come after it
+                if (p.n_split > 1 && g == 0 && m0 + row < p.M) {
+                    const size_t r = (static_cast<size_t>(j) * p.B + b) * p.M + m0 + row;
+                    p.ws_l[r] = l;
+                    if (kSafeMax)
+                        p.ws_m[r] = m;
+                }
             }
             if (!cluster) {
                 ptx::fence_proxy_async_smem();
@@ -1336,6 +1353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w.y = ptx::pack_half2(a[2] * inv, a[3] * inv);
                 w.z = ptx::pack_half2(a[4] * inv, a[5] * inv);
                 w.w = ptx::pack_half2(a[6] * inv, a[7] * inv);
+                if (p.early == 2)
+                    ptx::griddep_wait();
                 *reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * p.M + m0 + rr) * D + gq * 8) = w;
             }
         };

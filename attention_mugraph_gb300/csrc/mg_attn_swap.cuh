@@ -182,9 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    // Global memory waits for the previous grid, except the load warp's early loads (as in the
-    // one-tile kernel); every thread releases the dependents only after its own wait.
-    if (!(warp == 0 && p.early_loads)) {
+    // Global memory waits for the previous grid as in the one-tile kernel: early == 1, the load
+    // warp's first copies before its wait; early == 2, the dependents released now and only the
+    // global writes after the wait.
+    if (p.early == 2) {
+        ptx::griddep_launch_dependents();
+    } else if (!(warp == 0 && p.early == 1)) {
         ptx::griddep_wait();
         ptx::griddep_launch_dependents();
     }
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tiles before the warp's wait for the previous grid, which the other lanes take only
         // once lane 0 has issued them: the warp meets at a __syncwarp from both paths).
         if (lane != 0) {
-            if (p.early_loads) {
+            if (p.early == 1) {
                 __syncwarp();
                 ptx::griddep_wait();
                 ptx::griddep_launch_dependents();
@@ -233,11 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d(sQ + c * kSwapChunk, &tmQ, bar(BI::kQFull), c * 64, 0, b);
-                if (p.early_loads)
+                if (p.early == 1)
                     for (; t < T && t < STAGES; ++t)  // the stages are free: no wait
                         issue(t);
             }
-            if (p.early_loads) {
+            if (p.early == 1) {
                 __syncwarp();
                 ptx::griddep_wait();
                 ptx::griddep_launch_dependents();
@@ -661,6 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int c = q4 * 32 + lane;  // output column
             const int mq = p.M < kSwapNQ ? p.M : kSwapNQ;
+            if (p.early == 2 && !p.cluster_reduce)
+                ptx::griddep_wait();  // O or the partials are written below
 #pragma unroll
             for (int q = 0; q < kSwapNQ; ++q) {
                 if (q < mq) {
@@ -774,6 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                if (p.early == 2)
+                    ptx::griddep_wait();
                 p.O[(static_cast<size_t>(b) * p.M + q) * D + c] = __float2half_rn(os * __frcp_rn(ls));
             }
         }

@@ -13,12 +13,17 @@ its own wait, so a kernel completes only after its wait and the completions stay
     copy kernel, late form:     wait; release dependents; load the inputs; store them into staging
     attention kernel (host):    wait; release dependents; read staging; write O
     attention kernel (device),
-      early form:               load the inputs; wait; release dependents; write O
-      late form:                wait; release dependents; load the inputs; write O
+      level 2:                  release dependents; load the inputs; wait; write O
+      level 1:                  load the inputs; wait; release dependents; write O
+      level 0:                  wait; release dependents; load the inputs; write O
 
-The early forms are used unless an input shares bytes with the call's own O or with the previous
-call's O on the stream (what the previous kernel may still be writing), or the call is the
-first on the stream (its previous kernel unknown). The caller writes a call's inputs before it
+A kernel at level 2 releases its dependents at its start, so the kernels after it may start (and
+load) while kernels before it still run; the device holds fewer than W = 16 of them at once
+(grids of at least 10 CTAs, one per SM), which the model, without resources, takes as a bound on
+the calls it runs. The early forms (copy early, device levels 1 and 2) are used unless an input
+shares bytes with the call's own O or with the O of one of the last W calls on the stream, or
+the call is the first on the stream (its previous kernel unknown); level 2 only for calls of
+kind "device" (large grids), level 1 for "device_small". The caller writes a call's inputs before it
 enqueues the call. The scheduler interleaves the kernels' steps at random within those rules and
 checks every read: staging is read only after the copy that filled it for this call has
 completed, staging is not overwritten while an earlier call still reads it, and every input read
@@ -38,8 +43,8 @@ class ProtocolError(AssertionError):
 class StreamSim:
     def __init__(self, calls, seed: int, mutations=()):
         """calls: list of (inputs, output) or (inputs, output, kind) buffer names, kind "host"
-        (the default) or "device", e.g. [("x0", "o0"), ("o0", "o1", "device")] (the second call
-        reads the first call's output)."""
+        (the default), "device" or "device_small", e.g. [("x0", "o0"), ("o0", "o1", "device")]
+        (the second call reads the first call's output)."""
         calls = [c if len(c) == 3 else (c[0], c[1], "host") for c in calls]
         self.calls = calls
         self.rng = random.Random(seed)
@@ -48,24 +53,28 @@ class StreamSim:
         self.staging = None      # (call, complete) of the staged inputs
         self.staging_readers = set()
         self.kernels = []        # in stream order: dicts with name, state
+        W = 16
         for k, (inp, out, kind) in enumerate(calls):
             # The entry points' rule: load early unless the input is this call's output or the
-            # previous call's output on the stream, or the call is the stream's first (mutations:
-            # no rule, or the own output only).
-            prev_out = calls[k - 1][1] if k > 0 else None
+            # output of one of the last W calls on the stream, or the call is the stream's first
+            # (mutations: no rule, the own output only, the previous call's output only).
+            recent = [c[1] for c in calls[max(0, k - W):k]]
             if "early_despite_alias" in self.mut:
                 early = True
             elif "alias_own_only" in self.mut:
                 early = inp != out
+            elif "window_1" in self.mut:
+                early = k > 0 and inp != out and inp != calls[k - 1][1]
             else:
-                early = k > 0 and inp != out and inp != prev_out
+                early = k > 0 and inp != out and inp not in recent
             if kind == "host":
                 self.kernels.append({"name": f"copy{k}", "call": k, "kind": "copy", "early": early,
                                      "inp": inp, "out": out})
                 self.kernels.append({"name": f"attn{k}", "call": k, "kind": "attn", "inp": inp, "out": out})
             else:
+                level = (2 if kind == "device" else 1) if early else 0
                 self.kernels.append({"name": f"dattn{k}", "call": k, "kind": "dattn", "early": early,
-                                     "inp": inp, "out": out})
+                                     "level": level, "inp": inp, "out": out})
         for kern in self.kernels:
             kern.update(started=False, triggered=False, waited=False, done=False)
         # the host wrote every call's inputs before enqueueing it; an input that is an earlier call's
@@ -105,6 +114,9 @@ class StreamSim:
         k = kern["call"]
         if kern["kind"] == "dattn":
             loaded = None
+            if kern["level"] == 2:
+                kern["triggered"] = True  # the dependents released at the start
+                yield
             if kern["early"]:
                 loaded = self.version.get(kern["inp"])
                 yield

@@ -18,6 +18,10 @@ CHAINS = {
     "device_chained": [("x", "a", "device"), ("a", "b", "device"), ("b", "c", "device"), ("c", "d", "device")],
     "device_in_place": [("h", "h", "device")] * 4,
     "mixed_chained": [("x", "a"), ("a", "b", "device"), ("b", "c"), ("c", "d", "device"), ("d", "e", "device")],
+    # level 2 (dependents released at the start): a call reading the output of a call further back
+    "device_skip": [("x0", "a", "device"), ("x1", "b", "device"), ("x2", "c", "device"), ("a", "d", "device"),
+                    ("x3", "e", "device"), ("b", "f", "device")],
+    "small_skip": [("x0", "a", "device_small"), ("x1", "b", "device_small"), ("a", "c", "device_small")],
 }
 
 
@@ -79,3 +83,25 @@ def test_device_chains_need_the_previous_output_in_the_rule():
 def test_first_call_is_not_early():
     sim = sm.StreamSim(CHAINS["device_distinct"], 0)
     assert [k["early"] for k in sim.kernels] == [False, True, True]
+
+
+def test_level2_needs_the_window():
+    # With dependents released at the start, a call may run while calls further back than the
+    # previous one still write; comparing the inputs with the previous call's output alone reads
+    # stale data, the window of recent outputs does not.
+    for seed in range(300):
+        sm.StreamSim(CHAINS["device_skip"], seed).run()
+    msg = caught("device_skip", "window_1")
+    assert msg is not None and "loaded an input" in msg, msg
+
+
+def test_level1_needs_only_the_previous_output():
+    # Kernels that release their dependents after their own wait: the previous call's output is
+    # the only one that can still be written, so the narrower comparison suffices there.
+    for seed in range(300):
+        sm.StreamSim(CHAINS["small_skip"], seed, mutations=("window_1",)).run()
+
+
+def test_levels_as_chosen():
+    sim = sm.StreamSim([("x0", "a", "device"), ("x1", "b", "device_small"), ("a", "c", "device")], 0)
+    assert [k["level"] for k in sim.kernels] == [0, 1, 0]

@@ -608,6 +608,32 @@ def test_device_chained_calls(which, kw):
         prev = r
 
 
+@pytest.mark.parametrize("shape,back", [((2, 256, 4096, 64), 2), ((2, 64, 1024, 64), 5), ((16, 8, 32768, 128), 2)])
+def test_device_calls_reading_an_output_further_back(shape, back):
+    # Back to back on one stream, call i's Q is call (i - back)'s O. These plans start at level 2
+    # (dependents released at the start: a call may run while calls before the previous one still
+    # do); the library compares the inputs with the outputs of its recent calls, not only the
+    # previous one. Bit for bit against the same calls run one at a time, synchronised.
+    B, M, N, d = shape
+    plan = mg.Plan(B, M, N, d)
+    n = back + 6
+    qs = [t.cuda() for t in (inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=200 + i)[0] for i in range(n))]
+    _, k, v = inputs.make_inputs(B, M, N, d, 0.5 if d == 64 else 0.25, seed=199)
+    k, v = k.cuda(), v.cuda()
+    outs = [torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda") for _ in range(n)]
+    for i in range(n):
+        plan.run(outs[i - back] if i >= back else qs[i], k, v, outs[i])
+    torch.cuda.synchronize()
+    ref_plan = mg.Plan(B, M, N, d, flags=EARLY_OFF)
+    refs = []
+    for i in range(n):
+        r = torch.full((B, M, d), float("nan"), dtype=torch.float16, device="cuda")
+        ref_plan.run(refs[i - back] if i >= back else qs[i], k, v, r)
+        torch.cuda.synchronize()
+        refs.append(r)
+        assert torch.equal(r, outs[i]), f"call {i} (reads call {i - back})"
+
+
 def test_device_chain_in_captured_graph():
     # Two calls captured into one graph, the second reading the first's O as Q, replayed three
     # times: within the capture the first call has no known predecessor (no early loads) and the
