@@ -73,6 +73,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // The deepest K/V ring that fits.
 int auto_stages(int64_t d) { return d == 64 ? 6 : 3; }
 
+// Grids of at least this many CTAs (one per SM) may start early at level 2 (FwdParams::early):
+// fewer of them than the window of recent outputs (below) fit the device at once.
+constexpr int kEarlyMinCtas = 10;
+
 using FwdKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                            const CUtensorMap, const mg::FwdParams);
 
@@ -551,9 +555,9 @@ cudaError_t raise_smem_limit(FwdKernel fwd, int smem)
 // (2, 256, 4096, 64) 5.80 with 12 splits against 6.21 with 16 (of which 7 clusters fit at once,
 // not the 8 of two calls); (4, 256, 4096, 64) 7.22 with 12 against 8.41 with 16 through the
 // second kernel; (8, 256, 4096, 64) 8.11 with 6 against 9.66 with 9 through the second kernel.
-mg_status place_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int sms,
-                         int smem_optin, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags,
-                         FwdKernel *fwd)
+mg_status fit_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int sms,
+                       int smem_optin, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags,
+                       FwdKernel *fwd)
 {
     if (info->cluster_ctas == 0)
         return MG_OK;
@@ -609,6 +613,73 @@ mg_status place_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_at
     *fwd = plan_kernel(*info, *flags);
     const cudaError_t e = raise_smem_limit(*fwd, info->smem_bytes);
     return e == cudaSuccess ? MG_OK : cuda_fail(e, "cudaFuncSetAttribute");
+}
+
+// Split count for back-to-back calls that start early (level 2, FwdParams::early): such calls
+// overlap as far as the device holds their clusters, so a call's cost is its latency divided by
+// the number of calls in flight, not its latency. A smaller split count puts more column tiles on
+// each CTA (a longer call) but lets more calls be resident together. Without an explicit n_split,
+// for a cluster plan that may start early, the split count from the one placed down to 2 that
+// keeps at most max(8, the placed count's) column tiles per CTA and a grid of at least
+// kEarlyMinCtas CTAs, and that maximises min(4, clusters the device holds / clusters per call,
+// SMs / grid) is taken (the larger on a tie). Measured on GB300 (us per call, back to back at
+// level 2; isolated, each call between events of its own): (2, 256, 4096, 64) 6 splits 1.83 and
+// 12.64 against 12 splits 3.67 and 12.45; 8 splits 2.36 and 12.48; 4 splits 1.81 and 14.5;
+// (4, 256, 4096, 64) 4 splits 2.40 against 6 splits 3.48 and 12 splits 7.32; (2, 256, 4096, 128)
+// 6 splits 2.44 against 12 splits 4.51.
+mg_status pipeline_splits(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int sms,
+                          int smem_optin, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags,
+                          FwdKernel *fwd)
+{
+    if (info->cluster_ctas < 2 || (opts && opts->n_split != 0) || info->schedule != 0 || info->q_tiles_per_cta != 1 ||
+        ((*flags & MG_FLAG_QK_NORM) && info->swap_ab == 0))
+        return MG_OK;
+    const int n = info->cluster_ctas;
+    const int units = info->grid_ctas / n;
+    auto tiles = [&](int c) { return (info->n_tiles + c - 1) / c; };
+    auto in_flight = [&](FwdKernel f, int c, int grid, int smem) {
+        const int a = max_active_clusters(f, c, grid, smem) / units;
+        const int by_sms = sms / grid;
+        const int m = a < by_sms ? a : by_sms;
+        return m < 4 ? m : 4;
+    };
+    const int bound = tiles(n) > 8 ? tiles(n) : 8;
+    int best = in_flight(*fwd, n, info->grid_ctas, info->smem_bytes);
+    mg_attn_options o{};
+    if (opts)
+        o = *opts;
+    for (int c = n - 1; c >= 2 && tiles(c) <= bound && units * c >= kEarlyMinCtas; --c) {
+        mg_attn_options oc = o;
+        oc.n_split = c;
+        mg_attn_plan_info ic;
+        unsigned long long to = 0;
+        int fl = 0;
+        if (decide(B, M, N, d, &oc, sms, smem_optin, &ic, &to, &fl) != MG_OK || ic.cluster_ctas != c)
+            continue;
+        FwdKernel f = plan_kernel(ic, fl);
+        if (raise_smem_limit(f, ic.smem_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        const int k = in_flight(f, c, ic.grid_ctas, ic.smem_bytes);
+        if (k > best) {
+            best = k;
+            *info = ic;
+            *timeout_ns = to;
+            *flags = fl;
+            *fwd = f;
+        }
+    }
+    return MG_OK;
+}
+
+// Cluster placement, then the split count for calls that start early.
+mg_status place_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_options *opts, int sms,
+                         int smem_optin, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags,
+                         FwdKernel *fwd)
+{
+    const mg_status st = fit_clusters(B, M, N, d, opts, sms, smem_optin, info, timeout_ns, flags, fwd);
+    return st == MG_OK ? pipeline_splits(B, M, N, d, opts, sms, smem_optin, info, timeout_ns, flags, fwd) : st;
 }
 
 // Launch attributes of the fused kernel: programmatic dependent launch and the cluster shape.
@@ -840,7 +911,7 @@ mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info)
 // from the stream's eager calls, keyed by the capture's id, since the captured kernels run later
 // as one graph.
 constexpr int kWindow = 16;
-constexpr int kEarlyMinCtas = 10;  // 152 SMs / 10 < kWindow
+static_assert(152 / kEarlyMinCtas < kWindow, "the window must cover every kernel that can still run");
 struct OutRanges {
     cudaStream_t stream = nullptr;
     unsigned long long capture = 0;                     // the capture's id, 0 for eager calls

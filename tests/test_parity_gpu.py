@@ -393,18 +393,24 @@ def test_swap_ab_matches_one_tile_kernel_and_is_reproducible():
 
 
 def test_cluster_placement_for_back_to_back_calls():
-    # Without an explicit n_split, a plan takes a cluster size whose clusters of two back-to-back
-    # calls the device holds at once (GB300 holds 7 clusters of 13-16 CTAs, 8 of 11-12), within
-    # one more column tile per CTA; an explicit n_split is kept.
+    # Without an explicit n_split, the plan asks the device how many clusters it holds at once
+    # (GB300: 23 of 6 CTAs, 15 of 7-9, 8 of 11-12, 7 of 13-16). It first keeps the clusters of one
+    # call placeable (a smaller cluster, else the second kernel), then, for calls that start early,
+    # takes the split count that lets the most calls be in flight (up to 4) within max(8, placed)
+    # column tiles per CTA. An explicit n_split is kept.
     gqa = mg.Plan(2, 256, 4096, 64).info
-    assert gqa["cluster_ctas"] == gqa["n_split"] and 11 <= gqa["n_split"] <= 12
+    assert gqa["cluster_ctas"] == gqa["n_split"] == 6
     assert mg.Plan(2, 256, 4096, 64, n_split=16).info["cluster_ctas"] == 16
-    assert mg.Plan(1, 256, 4096, 64).info["cluster_ctas"] == 16  # two calls: 4 clusters
-    b4 = mg.Plan(4, 256, 4096, 64).info  # 16-CTA clusters do not fit once: a smaller cluster
-    assert b4["cluster_ctas"] == b4["n_split"] and 11 <= b4["n_split"] <= 12 and b4["kernels_per_run"] == 1
-    b8 = mg.Plan(8, 256, 4096, 64).info  # 9-CTA clusters do not fit once: at most two more tiles
-    assert b8["cluster_ctas"] == b8["n_split"] == 6 and b8["kernels_per_run"] == 1
-    for shape in [(2, 256, 4096, 64), (4, 256, 4096, 64), (8, 256, 4096, 64)]:
+    assert mg.Plan(1, 256, 4096, 64).info["n_split"] == 12
+    assert mg.Plan(2, 64, 1024, 64).info["n_split"] == 8  # 4 tiny calls in flight already
+    b4 = mg.Plan(4, 256, 4096, 64).info
+    assert b4["cluster_ctas"] == b4["n_split"] == 4 and b4["kernels_per_run"] == 1
+    b8 = mg.Plan(8, 256, 4096, 64).info  # 9-CTA clusters do not fit once: a smaller cluster
+    assert b8["cluster_ctas"] == b8["n_split"] and 4 <= b8["n_split"] <= 6 and b8["kernels_per_run"] == 1
+    assert mg.Plan(16, 256, 4096, 64).info["n_split"] == 4
+    # QK-norm's one-tile form never starts early: its split count is the placed one.
+    assert mg.Plan(2, 256, 4096, 64, flags=mg.MG_FLAG_QK_NORM).info["n_split"] == 16
+    for shape in [(2, 256, 4096, 64), (4, 256, 4096, 64), (8, 256, 4096, 64), (1, 256, 4096, 64)]:
         q, k, v = inputs.make_inputs(*shape, 0.5, seed=sum(shape))
         O, plan = run_gpu(q, k, v)
         assert_parity(O, oracle.attention(q, k, v), f"{shape} n_split={plan.info['n_split']}")
