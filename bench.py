@@ -559,11 +559,14 @@ def main():
     bound = "hbm" if t_hbm >= t_tensor else "tensor"
     # The fused kernel's average launch duration. When a step is that one kernel, the timed
     # region itself (CUDA events on the launching stream around K back-to-back launches) gives it;
-    # events recorded around each single launch would add their own latency to a few-µs kernel.
+    # events recorded around each single launch would add their own latency to a few-µs kernel
+    # and end the overlap of consecutive launches (a launch that starts early runs beside the one
+    # before it), so that figure is reported beside as the launch timed alone.
     # With a second (combine) kernel per step, the per-launch events bracket the fused kernel.
     if info["kernels_per_run"] == 1:
         dur_us = ms_graph * 1e3 / args.steps
-        dur_source = "timed region / steps (one kernel per step)"
+        dur_source = ("timed region / steps (one kernel per step; consecutive launches overlap, so "
+                      "this is the time each launch adds to the sequence)"
     else:
         dur_us = fwd_us
         dur_source = "mean of CUDA events recorded around each fused-kernel launch"
