@@ -566,7 +566,7 @@ def main():
     if info["kernels_per_run"] == 1:
         dur_us = ms_graph * 1e3 / args.steps
         dur_source = ("timed region / steps (one kernel per step; consecutive launches overlap, so "
-                      "this is the time each launch adds to the sequence)"
+                      "this is the time each launch adds to the sequence)")
     else:
         dur_us = fwd_us
         dur_source = "mean of CUDA events recorded around each fused-kernel launch"
