@@ -339,9 +339,17 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         else
             push = false;
     }
-    const uint32_t smem = pair   ? mg::pair_smem_bytes(stages)
-                          : swap ? mg::swap_smem_bytes(stages, safe)
-                                 : mg::fwd_smem_bytes(static_cast<int>(d), stages, push);
+    uint32_t smem = pair   ? mg::pair_smem_bytes(stages)
+                    : swap ? mg::swap_smem_bytes(stages, safe)
+                           : mg::fwd_smem_bytes(static_cast<int>(d), stages, push);
+    // QK-norm in the one-tile kernel under the split schedule: the CTA's key-vector scales (128
+    // floats per column tile) in shared memory after the fixed layout, where they fit beside the
+    // ring, so that no global memory is written before the epilogue (the call may start early).
+    if (qk_norm && !pair && !swap && !stream_k) {
+        const int64_t per_cta = (n_tiles + n_split - 1) / n_split;
+        if (static_cast<int64_t>(smem) + per_cta * mg::kBlockN * 4 <= max_smem)
+            smem += static_cast<uint32_t>(per_cta * mg::kBlockN * 4);
+    }
     if (static_cast<int64_t>(smem) > max_smem ||
         !(pair ? pair_kernel(stages)
                : swap ? swap_kernel(stages, o.flags)
@@ -537,6 +545,17 @@ int max_active_clusters(FwdKernel fwd, int n, int ctas, int smem)
     return clusters;
 }
 
+// QK-norm in the one-tile kernel: how many column tiles of key-vector scales the plan keeps in
+// shared memory (the bytes decide() added past the fixed layout), 0 when they go through global
+// memory.
+int qk_cs_tiles(const mg_attn_plan_info &in, int flags)
+{
+    if (!(flags & MG_FLAG_QK_NORM) || in.swap_ab != 0 || in.q_tiles_per_cta != 1 || in.schedule != 0)
+        return 0;
+    const int fixed = static_cast<int>(mg::fwd_smem_bytes(static_cast<int>(in.d), in.stages, in.xchg_push != 0));
+    return (in.smem_bytes - fixed) / (mg::kBlockN * 4);
+}
+
 // The kernel's dynamic shared-memory limit raised to the plan's (before any occupancy query: at
 // the default 48 KB limit the query would refuse the launch).
 cudaError_t raise_smem_limit(FwdKernel fwd, int smem)
@@ -631,8 +650,10 @@ mg_status pipeline_splits(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
                           int smem_optin, mg_attn_plan_info *info, unsigned long long *timeout_ns, int *flags,
                           FwdKernel *fwd)
 {
+    // (QK-norm in the one-tile kernel starts early only with its key scales in shared memory.)
+    const bool qk_one_tile = (*flags & MG_FLAG_QK_NORM) && info->swap_ab == 0;
     if (info->cluster_ctas < 2 || (opts && opts->n_split != 0) || info->schedule != 0 || info->q_tiles_per_cta != 1 ||
-        ((*flags & MG_FLAG_QK_NORM) && info->swap_ab == 0))
+        (qk_one_tile && qk_cs_tiles(*info, *flags) == 0))
         return MG_OK;
     const int n = info->cluster_ctas;
     const int units = info->grid_ctas / n;
@@ -654,7 +675,8 @@ mg_status pipeline_splits(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
         mg_attn_plan_info ic;
         unsigned long long to = 0;
         int fl = 0;
-        if (decide(B, M, N, d, &oc, sms, smem_optin, &ic, &to, &fl) != MG_OK || ic.cluster_ctas != c)
+        if (decide(B, M, N, d, &oc, sms, smem_optin, &ic, &to, &fl) != MG_OK || ic.cluster_ctas != c ||
+            (qk_one_tile && qk_cs_tiles(ic, fl) == 0))
             continue;
         FwdKernel f = plan_kernel(ic, fl);
         if (raise_smem_limit(f, ic.smem_bytes) != cudaSuccess) {
@@ -1032,8 +1054,8 @@ int early_level(const mg_attn_plan_info &in, int flags, cudaStream_t stream, con
     const size_t nb[3] = {bq, bk, bk};
     if (!may_load_early(stream, inp, nb, 3, O, bq))
         return 0;
-    const bool qk_one_tile = (flags & MG_FLAG_QK_NORM) && in.swap_ab == 0;
-    return in.schedule == 0 && !qk_one_tile && in.grid_ctas >= kEarlyMinCtas ? 2 : 1;
+    const bool qk_global = (flags & MG_FLAG_QK_NORM) && in.swap_ab == 0 && qk_cs_tiles(in, flags) == 0;
+    return in.schedule == 0 && !qk_global && in.grid_ctas >= kEarlyMinCtas ? 2 : 1;
 }
 
 // mg_attn_run's work; `allow_early`: the fused kernel may load Q, K and V before the previous
@@ -1088,6 +1110,7 @@ static mg_status run_fused(mg_attn_plan_t plan, const void *Q, const void *K, co
 
     cudaLaunchAttribute attr[2];
     const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
+    prm.cs_tiles = qk_cs_tiles(in, plan->flags);
     prm.early = allow_early && pdl && !prm.inject_timeout && !(plan->flags & MG_FLAG_NO_EARLY_LOADS)
                     ? early_level(in, plan->flags, reinterpret_cast<cudaStream_t>(stream), Q, K, V, O)
                     : 0;
@@ -1345,6 +1368,7 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
     prm.col_scale = nullptr;
     prm.timeout_ns = timeout_ns;
     prm.inject_timeout = 0;
+    prm.cs_tiles = qk_cs_tiles(in, flags);
     prm.early = early_level(in, flags, reinterpret_cast<cudaStream_t>(stream), Q, K, V, O);
     prm.sk_units = static_cast<long long>(in.m_tiles) * in.n_tiles;
     prm.sk_ctas = in.grid_ctas;

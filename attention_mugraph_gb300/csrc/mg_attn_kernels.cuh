@@ -138,7 +138,10 @@ struct FwdParams {
                              // kernel that may still run writes Q, K or V): 0 nothing; 1 the load
                              // warp's Q and first STAGES K/V copies; 2 everything but the global
                              // writes, with the dependents released at the start (not with QK-norm's
-                             // key scales or the stream-K schedule, which write global memory midway)
+                             // key scales in global memory or the stream-K schedule, which write
+                             // global memory midway)
+    int cs_tiles;            // QK-norm: the CTA's key-vector scales kept in shared memory, this many
+                             // tiles of 128 after the fixed layout (0: in col_scale, global memory)
     long long sk_units;      // stream-K: B * n_tiles units (row tile, column tile)
     int sk_ctas;             // stream-K: G, the grid
     int sk_slots;            // stream-K: partial slots per row tile (the second kernel's split count)
@@ -400,6 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(l_xchg + 2 * kBlockM);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    // QK-norm with p.cs_tiles: the key-vector scales of this CTA's tiles, past the fixed layout.
+    float *cs_smem = reinterpret_cast<float *>(smem + (fwd_smem_bytes(D, STAGES, kPushX) - 1024u));
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
 
     const int warp = threadIdx.x >> 5;
@@ -757,8 +762,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         // QK-norm variant: a is this row's query scale, 1/rms of the Q tile's row (read from shared
         // memory once; rows past M take 1, their scores are 0 anyway); the key-vector scales c of
-        // the split's columns are computed by the row-maximum pass below and kept in global
-        // memory (L2) for the main pass.
+        // the split's columns are computed by the row-maximum pass below and kept for the main
+        // pass in shared memory (p.cs_tiles; then the call may start early) or else in global
+        // memory (L2).
         float a_row = 1.f;
         float *col_scale = nullptr;
         if constexpr (kQk) {
@@ -818,10 +824,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sum_sq_cols(*reinterpret_cast<const uint4 *>(kp + k * 1024), sq);
                     const float c = __frsqrt_rn(reduce_scatter8(sq, lane) * (1.f / D) + kQkNormEps);
                     cs_tile[my_col] = c;
-                    if (p.early == 2)  // (the host does not start this variant early; kept safe)
-                        ptx::griddep_wait();
-                    if (tile_of(u) * kBlockN + my_col < p.N)
-                        col_scale[static_cast<size_t>(tile_of(u)) * kBlockN + my_col] = c;
+                    if (p.cs_tiles) {
+                        cs_smem[u * kBlockN + my_col] = c;  // u < T <= p.cs_tiles
+                    } else {
+                        if (p.early == 2)  // (the host starts this form early only with p.cs_tiles)
+                            ptx::griddep_wait();
+                        if (tile_of(u) * kBlockN + my_col < p.N)
+                            col_scale[static_cast<size_t>(tile_of(u)) * kBlockN + my_col] = c;
+                    }
                 }
                 w_ok = w_ok && warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);
                 w_ok = group_barrier_and(w_ok);
@@ -953,7 +963,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nv = n_valid - half * 64;
                     uint32_t w[32];
                     if constexpr (kQk) {
-                        const float *cs = col_scale + static_cast<size_t>(tile_of(t)) * kBlockN + half * 64;
+                        const float *cs = (p.cs_tiles ? cs_smem + t * kBlockN
+                                                      : col_scale + static_cast<size_t>(tile_of(t)) * kBlockN) +
+                                          half * 64;
                         if (nv >= 64) {
                             exp_slice_scaled<false>(r0, 0, nv, w, acc, cs, arow, shift);
                             exp_slice_scaled<false>(r1, 32, nv, w + 16, acc, cs + 32, arow, shift);

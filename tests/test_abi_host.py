@@ -247,15 +247,24 @@ def test_query_safe_softmax_workspace():
 
 
 def test_query_qk_norm_plan():
-    # QK-norm computes its scales inside the fused kernel (no extra launch) and keeps the key
-    # scales in the workspace: B*N of them and 128 spare floats; as it implies the max-subtracted
-    # evaluation, also one row maximum per split and row. Shared memory and stages are unchanged.
+    # QK-norm computes its scales inside the fused kernel (no extra launch). The workspace has
+    # room for the key scales (B*N of them and 128 spare floats); as QK-norm implies the
+    # max-subtracted evaluation, also one row maximum per split and row. Where they fit beside the
+    # ring, the CTA's key scales stay in shared memory instead (128 floats per column tile of the
+    # CTA), so that nothing global is written before the epilogue. Stages are unchanged.
     plain = mg.mg_attn_query(2, 256, 4096, 64, 152)
     qk = mg.mg_attn_query(2, 256, 4096, 64, 152, flags=mg.MG_FLAG_QK_NORM)
-    assert qk["smem_bytes"] == plain["smem_bytes"] and qk["stages"] == 6
+    tiles = -(-qk["n_tiles"] // qk["n_split"])
+    assert qk["smem_bytes"] == plain["smem_bytes"] + tiles * 128 * 4 and qk["stages"] == 6
     assert qk["kernels_per_run"] == plain["kernels_per_run"]
     assert qk["workspace_bytes"] == plain["workspace_bytes"] + 256 + (2 * 4096 + 128) * 4
-    assert mg.mg_attn_query(2, 256, 4096, 128, 152, flags=mg.MG_FLAG_QK_NORM)["stages"] == 3
+    # Head dim 128, three stages: no room beside the ring; the scales go through global memory.
+    qk128 = mg.mg_attn_query(2, 256, 4096, 128, 152, flags=mg.MG_FLAG_QK_NORM)
+    assert qk128["stages"] == 3
+    assert qk128["smem_bytes"] == mg.mg_attn_query(2, 256, 4096, 128, 152)["smem_bytes"]
+    # 64 column tiles per CTA do not fit either (32 KB of scales).
+    one = mg.mg_attn_query(1, 128, 8192, 64, 152, n_split=1, flags=mg.MG_FLAG_QK_NORM)
+    assert one["smem_bytes"] == mg.mg_attn_query(1, 128, 8192, 64, 152, n_split=1)["smem_bytes"]
     B, M, N, d = 2, 256, 65536, 64
     a = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_QK_NORM)
     b = mg.mg_attn_query(B, M, N, d, 152, flags=mg.MG_FLAG_SAFE_SOFTMAX)

@@ -408,8 +408,10 @@ def test_cluster_placement_for_back_to_back_calls():
     b8 = mg.Plan(8, 256, 4096, 64).info  # 9-CTA clusters do not fit once: a smaller cluster
     assert b8["cluster_ctas"] == b8["n_split"] and 4 <= b8["n_split"] <= 6 and b8["kernels_per_run"] == 1
     assert mg.Plan(16, 256, 4096, 64).info["n_split"] == 4
-    # QK-norm's one-tile form never starts early: its split count is the placed one.
-    assert mg.Plan(2, 256, 4096, 64, flags=mg.MG_FLAG_QK_NORM).info["n_split"] == 16
+    # QK-norm's one-tile form starts early only with its key scales in shared memory: there it
+    # takes the same count; at head dim 128 (no room beside the ring) it keeps the placed one.
+    assert mg.Plan(2, 256, 4096, 64, flags=mg.MG_FLAG_QK_NORM).info["n_split"] == 6
+    assert mg.Plan(2, 256, 4096, 128, flags=mg.MG_FLAG_QK_NORM).info["n_split"] == 16
     for shape in [(2, 256, 4096, 64), (4, 256, 4096, 64), (8, 256, 4096, 64), (1, 256, 4096, 64)]:
         q, k, v = inputs.make_inputs(*shape, 0.5, seed=sum(shape))
         O, plan = run_gpu(q, k, v)
