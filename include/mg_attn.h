@@ -83,13 +83,12 @@ typedef enum {
                                       each key vector K[b,:,n] normalised over d: x / sqrt(mean(x^2) + eps),
                                       eps = MG_QKNORM_EPS, no weight. The fused kernel computes the scales
                                       1/rms in fp32 (a query row's from the Q tile it holds, a key vector's
-                                      in the row-maximum pass from the K tile it streams, kept in the plan's
-                                      workspace for the main pass) and applies them to the scores in fp32,
-                                      so Q and K stay the fp16 MMA operands and K is read twice, as without
-                                      the flag (the key scales stay in the CTA's shared memory where they
-                                      fit beside the ring: head dim 64, at most 33 column tiles per CTA;
-                                      else they go through the workspace). Normalised scores reach +-d,
-                                      past the fp16 range of exp, so
+                                      in the row-maximum pass from the K tile it streams, kept for the main
+                                      pass in the CTA's shared memory where they fit beside the ring, head
+                                      dim 64 with at most 33 column tiles per CTA, else in the plan's
+                                      workspace) and applies them to the scores in fp32, so Q and K stay the
+                                      fp16 MMA operands and K is read twice, as without the flag.
+                                      Normalised scores reach +-d, past the fp16 range of exp, so
                                       the flag implies MG_FLAG_SAFE_SOFTMAX. Under the few-row
                                       specialisation (MG_FLAG_SWAP_AB) it runs in one pass (K read once):
                                       the key scales come from each K tile in shared memory. */
