@@ -124,10 +124,10 @@ typedef enum {
                                       barrier; one pipeline stage fewer), instead of the owners reading them
                                       out of every CTA's shared memory after a cluster barrier (the default,
                                       pulled form). Opt-in: measured on GB300 it is slower; see info.xchg_push */
-#define MG_FLAG_NO_EARLY_LOADS 0x1000 /* the fused kernel loads nothing before the previous kernel on the
-                                      stream has completed (see mg_attn_run: by default it may load Q, K
-                                      and V earlier when that kernel is one of this library's and writes
-                                      none of them) */
+#define MG_FLAG_NO_EARLY_LOADS 0x1000 /* the fused kernel reads nothing before the previous kernel on the
+                                      stream has completed and releases the next one only after that (see
+                                      mg_attn_run: by default it may read Q, K and V earlier, and start the
+                                      next call early, when no recent call of this library wrote them) */
 #define MG_FLAG_INJECT_TIMEOUT 0x2 /* test hook: before issuing any copy, the load warp waits on a
                                       barrier nothing arrives on, so the bounded-wait path runs and
                                       the plan's status becomes MG_ERR_TIMEOUT; O is then undefined */
@@ -199,12 +199,15 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d,
  * (see the top of this file), 16-byte aligned; O must not overlap the inputs. The caller
  * keeps ownership of all four. With programmatic dependent launch (the default) the
  * kernels wait for all prior work on `stream` before writing global memory. The fused kernel
- * may load Q, K and V (the Q tile and the first pipeline stages) before the previous kernel on
- * the stream has completed, when the library knows that kernel: the previous call on the same
- * stream (and the same stream capture) was one of this library's, and none of Q, K and V shares
- * bytes with that call's output or with O. A kernel of another origin that runs right before
- * the call and releases its dependents before it completes (programmatic dependent launch) must
- * not write Q, K or V; MG_FLAG_NO_EARLY_LOADS turns the early loads off.
+ * may read Q, K and V before the kernels before it on the stream have completed, when the
+ * library knows them: the previous call on the same stream (and the same stream capture) was
+ * one of this library's, and none of Q, K and V shares bytes with the outputs of the last 16
+ * calls on that stream or with O. Then, for grids of at least 10 CTAs, it also releases the
+ * next kernel at its start and computes everything before its wait (back-to-back calls
+ * overlap); otherwise only its first copies go out early. A kernel of another origin that runs
+ * right before the call and releases its dependents before it completes (programmatic
+ * dependent launch) must not write Q, K or V, nor may calls on one stream be enqueued from
+ * several host threads at once; MG_FLAG_NO_EARLY_LOADS turns the early reads off.
  * Errors: MG_ERR_INVALID_ARG (NULL plan or pointer), MG_ERR_LAYOUT (misaligned pointer),
  * MG_ERR_CUDA (descriptor encoding or launch failed; the plan's device must be current).
  * In-kernel timeouts are not visible here; see mg_attn_get_status.
