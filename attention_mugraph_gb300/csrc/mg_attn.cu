@@ -639,9 +639,10 @@ mg_status fit_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn
 // the number of calls in flight, not its latency. A smaller split count puts more column tiles on
 // each CTA (a longer call) but lets more calls be resident together. Without an explicit n_split,
 // for a cluster plan that may start early, the split count from the one placed down to 2 that
-// keeps at most max(8, the placed count's) column tiles per CTA and a grid of at least
-// kEarlyMinCtas CTAs, and that maximises min(4, clusters the device holds / clusters per call,
-// SMs / grid) is taken (the larger on a tie). Measured on GB300 (us per call, back to back at
+// keeps at most max(8, the placed count's) column tiles per CTA (twice the placed count's when
+// that lets no second call in) and a grid of at least kEarlyMinCtas CTAs, and that maximises
+// min(4, clusters the device holds / clusters per call, SMs / grid) is taken (the larger on a
+// tie). Measured on GB300 (us per call, back to back at
 // level 2; isolated, each call between events of its own): (2, 256, 4096, 64) 6 splits 1.83 and
 // 12.64 against 12 splits 3.67 and 12.45; 8 splits 2.36 and 12.48; 4 splits 1.81 and 14.5;
 // (4, 256, 4096, 64) 4 splits 2.40 against 6 splits 3.48 and 12 splits 7.32; (2, 256, 4096, 128)
@@ -664,8 +665,15 @@ mg_status pipeline_splits(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
         const int m = a < by_sms ? a : by_sms;
         return m < 4 ? m : 4;
     };
-    const int bound = tiles(n) > 8 ? tiles(n) : 8;
     int best = in_flight(*fwd, n, info->grid_ctas, info->smem_bytes);
+    // A placed count that lets no second call in takes up to twice its tiles per CTA, except in
+    // the one-tile kernel's two-pass variants, whose calls alone would lose more than their
+    // overlap gains (measured on GB300, (16, 256, 4096, 64), 4 against 2 splits, back to back /
+    // alone in us: plain 9.13 / 14.6 against 6.93 / 18.7; max-subtracted 12.2 / 18.6 against
+    // 9.55 / 24.9; QK-norm 16.5 / 22.8 against 13.4 / 34.9).
+    const bool two_pass = (*flags & (MG_FLAG_SAFE_SOFTMAX | MG_FLAG_QK_NORM)) && info->swap_ab == 0;
+    const int base = best >= 2 || two_pass ? tiles(n) : 2 * tiles(n);
+    const int bound = base > 8 ? base : 8;
     mg_attn_options o{};
     if (opts)
         o = *opts;
