@@ -163,7 +163,7 @@ FwdKernel fwd_kernel(int64_t d, int stages, int flags)
     return fwd_kernel_variant<mg::kPlain>(d, stages);
 }
 
-using CombineKernel = void (*)(const float *, const float *, const float *, __half *, int, int);
+using CombineKernel = void (*)(const float *, const float *, const float *, __half *, int, int, int);
 
 template <int D>
 CombineKernel combine_kernel_d(int n_split)
@@ -1153,7 +1153,8 @@ static mg_status run_fused(mg_attn_plan_t plan, const void *Q, const void *K, co
         cc.blockDim = dim3(256, 1, 1);
         cc.dynamicSmemBytes = 0;
         cc.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, pdl, 0));
-        void *cargs[6] = {&wo, &wl, &wm, &out, &rows, &n_split};
+        int early = prm.early == 2 ? 1 : 0;
+        void *cargs[7] = {&wo, &wl, &wm, &out, &rows, &n_split, &early};
         e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(plan->combine), cargs);
         if (e != cudaSuccess)
             return cuda_fail(e, "launch mg_attn_combine");
@@ -1407,7 +1408,8 @@ mg_status mg_attn_run_noalloc(int64_t B, int64_t M, int64_t N, int64_t d, const 
         cc.dynamicSmemBytes = 0;
         cc.numAttrs = static_cast<unsigned>(fused_launch_attrs(attr, true, 0));
         const float *wm = nullptr;
-        void *cargs[6] = {&wo, &wl, &wm, &out, &rows, &n_split};
+        int early = prm.early == 2 ? 1 : 0;
+        void *cargs[7] = {&wo, &wl, &wm, &out, &rows, &n_split, &early};
         e = cudaLaunchKernelExC(&cc, reinterpret_cast<const void *>(combine_kernel(d, n_split)), cargs);
         if (e != cudaSuccess)
             return cuda_fail(e, "launch mg_attn_combine");

@@ -35,14 +35,22 @@ struct CombineCfg {
 template <int D>
 __global__ void __launch_bounds__(256)
     mg_attn_combine(const float *__restrict__ ws_o, const float *__restrict__ ws_l, const float *__restrict__ ws_m,
-                    __half *__restrict__ O, int rows, int n_split)
+                    __half *__restrict__ O, int rows, int n_split, int early)
 {
     using CC = CombineCfg<D>;
     __shared__ float4 part_o[CC::kParts][CC::kRows][CC::kGroups];
     __shared__ float part_l[CC::kParts][CC::kRows];
 
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
+    // Everything here waits for the fused kernel. early: that kernel started early (its
+    // dependents released at its start), so this one releases the next call's fused kernel
+    // before its wait too, and the next call overlaps this call's end.
+    if (early) {
+        ptx::griddep_launch_dependents();
+        ptx::griddep_wait();
+    } else {
+        ptx::griddep_wait();
+        ptx::griddep_launch_dependents();
+    }
 
     const int g = threadIdx.x % CC::kGroups;
     const int part = (threadIdx.x / CC::kGroups) % CC::kParts;
@@ -116,15 +124,24 @@ struct WideCombineCfg {
 template <int D, int BATCH>
 __global__ void __launch_bounds__(256, BATCH == 4 ? 4 : 3)
     mg_attn_combine_wide(const float *__restrict__ ws_o, const float *__restrict__ ws_l,
-                         const float *__restrict__ ws_m, __half *__restrict__ O, int rows, int n_split)
+                         const float *__restrict__ ws_m, __half *__restrict__ O, int rows, int n_split,
+                         int early)
 {
     using CC = WideCombineCfg<D>;
     __shared__ float4 part_o[CC::kParts][CC::kRows][CC::kGroups];
     __shared__ float part_l[CC::kParts][CC::kRows];
     __shared__ float part_m[CC::kParts][CC::kRows];
 
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
+    // Everything here waits for the fused kernel. early: that kernel started early (its
+    // dependents released at its start), so this one releases the next call's fused kernel
+    // before its wait too, and the next call overlaps this call's end.
+    if (early) {
+        ptx::griddep_launch_dependents();
+        ptx::griddep_wait();
+    } else {
+        ptx::griddep_wait();
+        ptx::griddep_launch_dependents();
+    }
 
     const int g = threadIdx.x % CC::kGroups;
     const int part = (threadIdx.x / CC::kGroups) % CC::kParts;

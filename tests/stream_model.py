@@ -23,7 +23,12 @@ load) while kernels before it still run; the device holds fewer than W = 16 of t
 the calls it runs. The early forms (copy early, device levels 1 and 2) are used unless an input
 shares bytes with the call's own O or with the O of one of the last W calls on the stream, or
 the call is the first on the stream (its previous kernel unknown); level 2 only for calls of
-kind "device" (large grids), level 1 for "device_small". The caller writes a call's inputs before it
+kind "device" (large grids), level 1 for "device_small". A call of kind "device_split" is a
+level-2-capable device call whose split partials go through the plan's workspace: its fused
+kernel writes them (after its wait) and a second kernel sums them into O:
+
+    combine kernel:             (after a level-2 fused kernel) release dependents; wait; read the
+                                workspace; write O.  Otherwise: wait; release dependents; ... The caller writes a call's inputs before it
 enqueues the call. The scheduler interleaves the kernels' steps at random within those rules and
 checks every read: staging is read only after the copy that filled it for this call has
 completed, staging is not overwritten while an earlier call still reads it, and every input read
@@ -52,6 +57,7 @@ class StreamSim:
         self.version = {}        # buffer -> which call's value it holds ("host" for host-written inputs)
         self.staging = None      # (call, complete) of the staged inputs
         self.staging_readers = set()
+        self.ws_readers = set()       # combine kernels reading the plan's workspace
         self.kernels = []        # in stream order: dicts with name, state
         W = 16
         for k, (inp, out, kind) in enumerate(calls):
@@ -72,9 +78,13 @@ class StreamSim:
                                      "inp": inp, "out": out})
                 self.kernels.append({"name": f"attn{k}", "call": k, "kind": "attn", "inp": inp, "out": out})
             else:
-                level = (2 if kind == "device" else 1) if early else 0
+                level = (2 if kind in ("device", "device_split") else 1) if early else 0
+                split = kind == "device_split"
                 self.kernels.append({"name": f"dattn{k}", "call": k, "kind": "dattn", "early": early,
-                                     "level": level, "inp": inp, "out": out})
+                                     "level": level, "inp": inp, "out": "ws" if split else out})
+                if split:
+                    self.kernels.append({"name": f"comb{k}", "call": k, "kind": "comb",
+                                         "level": level, "inp": "ws", "out": out})
         for kern in self.kernels:
             kern.update(started=False, triggered=False, waited=False, done=False)
         # the host wrote every call's inputs before enqueueing it; an input that is an earlier call's
@@ -130,7 +140,28 @@ class StreamSim:
                 yield
             if loaded != self.expect[k]:
                 raise ProtocolError(f"dattn{k} loaded an input holding {loaded!r}, not {self.expect[k]!r}")
+            if kern["out"] == "ws" and self.ws_readers:
+                raise ProtocolError(f"dattn{k} writes the workspace while {sorted(self.ws_readers)} read it")
             self.version[kern["out"]] = k
+        elif kern["kind"] == "comb":
+            if kern["level"] == 2:
+                kern["triggered"] = True
+                yield
+            if "combine_no_wait" not in self.mut:
+                while not self._may_pass_wait(i):
+                    yield
+            kern["waited"] = True
+            kern["triggered"] = True
+            yield
+            if self.version.get("ws") != k:
+                raise ProtocolError(f"comb{k} reads the workspace holding {self.version.get('ws')!r}")
+            self.ws_readers.add(k)
+            yield
+            self.ws_readers.discard(k)
+            self.version[kern["out"]] = k
+            if "combine_no_wait" in self.mut:
+                while not self._may_pass_wait(i):  # completion still in stream order
+                    yield
         elif kern["kind"] == "copy":
             loaded = None
             if kern["early"]:

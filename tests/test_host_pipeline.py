@@ -22,6 +22,9 @@ CHAINS = {
     "device_skip": [("x0", "a", "device"), ("x1", "b", "device"), ("x2", "c", "device"), ("a", "d", "device"),
                     ("x3", "e", "device"), ("b", "f", "device")],
     "small_skip": [("x0", "a", "device_small"), ("x1", "b", "device_small"), ("a", "c", "device_small")],
+    # partials through the workspace and a combine kernel, which releases the next call early too
+    "split_chain": [("x0", "a", "device_split"), ("x1", "b", "device_split"), ("a", "c", "device_split"),
+                    ("x2", "d", "device"), ("c", "e", "device_split")],
 }
 
 
@@ -105,3 +108,15 @@ def test_level1_needs_only_the_previous_output():
 def test_levels_as_chosen():
     sim = sm.StreamSim([("x0", "a", "device"), ("x1", "b", "device_small"), ("a", "c", "device")], 0)
     assert [k["level"] for k in sim.kernels] == [0, 1, 0]
+
+
+def test_combine_kernel_released_early():
+    # After a fused kernel that started early, the combine kernel releases the next call at its
+    # start as well: the next fused kernel then runs beside this call's combine, and its writes
+    # of the shared workspace still wait for the combine to complete.
+    for seed in range(300):
+        sm.StreamSim(CHAINS["split_chain"], seed).run()
+    msg = caught("split_chain", "combine_no_wait")
+    assert msg is not None and "workspace" in msg, msg
+    msg = caught("split_chain", "window_1")
+    assert msg is not None and "loaded an input" in msg, msg
