@@ -1119,7 +1119,7 @@ static mg_status run_fused(mg_attn_plan_t plan, const void *Q, const void *K, co
     cudaLaunchAttribute attr[2];
     const bool pdl = (plan->flags & MG_FLAG_NO_PDL) == 0;
     prm.cs_tiles = qk_cs_tiles(in, plan->flags);
-    prm.early = allow_early && pdl && !prm.inject_timeout && !(plan->flags & MG_FLAG_NO_EARLY_LOADS)
+    prm.early = allow_early && pdl && !(plan->flags & MG_FLAG_NO_EARLY_LOADS)
                     ? early_level(in, plan->flags, reinterpret_cast<cudaStream_t>(stream), Q, K, V, O)
                     : 0;
 

@@ -194,7 +194,8 @@ __device__ __forceinline__ bool wait_bounded(const WaitCtx &w, uint32_t bar, uin
             return false;
         if (ptx::globaltimer_ns() - t0 > w.timeout_ns) {
             *w.abort_flag = 1;
-            ptx::griddep_wait();  // (early start) global memory only after the previous grid
+            ptx::griddep_wait();  // (early start, or an early load warp) global memory only after
+                                  // the previous grid
             if (atomicCAS(w.status, 0, kStatusTimeout) == 0)
                 atomicExch(w.status + 1, where);
             return false;

@@ -757,6 +757,24 @@ def test_misaligned_pointer_rejected():
     assert e.value.status == mg.MG_ERR_LAYOUT
 
 
+@pytest.mark.parametrize("flags", [0, mg.MG_FLAG_NO_CLUSTER])
+def test_bounded_wait_with_early_start(flags):
+    # Two calls back to back on distinct buffers, each with a wait that runs out after 2 ms: the
+    # second starts early (its dependents released at its start, everything but its global writes
+    # before its wait), so both unwind while overlapping; the status is written only after the
+    # wait for the previous grid, and the context stays usable.
+    q, k, v, _ = inputs.make_config("tiny")
+    plan = mg.Plan(2, 64, 1024, 64, flags=mg.MG_FLAG_INJECT_TIMEOUT | flags, timeout_ns=2_000_000)
+    assert plan.info["grid_ctas"] >= 10
+    sets = [tuple(t.cuda() for t in (q, k, v)) for _ in range(2)]
+    outs = [torch.zeros((2, 64, 64), dtype=torch.float16, device="cuda") for _ in range(2)]
+    for x, o in zip(sets, outs):
+        plan.run(*x, o)
+    assert plan.status() == mg.MG_ERR_TIMEOUT
+    O2, _ = run_gpu(q, k, v, flags=flags)
+    assert_parity(O2, oracle.attention(q, k, v), "after timeouts")
+
+
 @pytest.mark.parametrize("flags", [0, mg.MG_FLAG_PUSH_COMBINE, mg.MG_FLAG_NO_CLUSTER])
 def test_bounded_wait_reports_timeout_and_context_survives(flags):
     # The load warp waits on a barrier nothing arrives on (before issuing any copy); the wait
