@@ -37,6 +37,7 @@ MG_FLAG_SWAP_AB = 0x200
 MG_FLAG_NO_SWAP_AB = 0x400
 MG_FLAG_PUSH_COMBINE = 0x800
 MG_FLAG_NO_EARLY_LOADS = 0x1000
+MG_FLAG_ISOLATED = 0x2000
 MG_QKNORM_EPS = 1e-6
 
 # Every function include/mg_attn.h declares.

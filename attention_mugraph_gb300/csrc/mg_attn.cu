@@ -228,7 +228,7 @@ mg_status decide(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn_optio
         (o.flags & ~(MG_FLAG_NO_PDL | MG_FLAG_INJECT_TIMEOUT | MG_FLAG_NO_CLUSTER | MG_FLAG_SAFE_SOFTMAX |
                      MG_FLAG_QK_NORM | MG_FLAG_Q_PAIRS | MG_FLAG_NO_Q_PAIRS | MG_FLAG_STREAM_K |
                      MG_FLAG_NO_STREAM_K | MG_FLAG_SWAP_AB | MG_FLAG_NO_SWAP_AB | MG_FLAG_PUSH_COMBINE |
-                     MG_FLAG_NO_EARLY_LOADS)) != 0)
+                     MG_FLAG_NO_EARLY_LOADS | MG_FLAG_ISOLATED)) != 0)
         return fail(MG_ERR_CONFIG, "unknown option bits");
     if (o.timeout_ns != 0 && (o.timeout_ns < 1000 || o.timeout_ns > 60000000000LL))
         return fail(MG_ERR_CONFIG, "timeout_ns out of range [1e3, 6e10]");
@@ -654,7 +654,7 @@ mg_status pipeline_splits(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     // (QK-norm in the one-tile kernel starts early only with its key scales in shared memory.)
     const bool qk_one_tile = (*flags & MG_FLAG_QK_NORM) && info->swap_ab == 0;
     if (info->cluster_ctas < 2 || (opts && opts->n_split != 0) || info->schedule != 0 || info->q_tiles_per_cta != 1 ||
-        (qk_one_tile && qk_cs_tiles(*info, *flags) == 0))
+        (qk_one_tile && qk_cs_tiles(*info, *flags) == 0) || (*flags & (MG_FLAG_ISOLATED | MG_FLAG_NO_EARLY_LOADS)))
         return MG_OK;
     const int n = info->cluster_ctas;
     const int units = info->grid_ctas / n;

@@ -124,6 +124,10 @@ typedef enum {
                                       barrier; one pipeline stage fewer), instead of the owners reading them
                                       out of every CTA's shared memory after a cluster barrier (the default,
                                       pulled form). Opt-in: measured on GB300 it is slower; see info.xchg_push */
+#define MG_FLAG_ISOLATED 0x2000     /* plan for calls that do not overlap (each between kernels of other
+                                      work, or after a call whose output it reads): keep the split count
+                                      chosen for one call's latency instead of lowering it so that several
+                                      back-to-back calls fit the device at once (see mg_attn_query) */
 #define MG_FLAG_NO_EARLY_LOADS 0x1000 /* the fused kernel reads nothing before the previous kernel on the
                                       stream has completed and releases the next one only after that (see
                                       mg_attn_run: by default it may read Q, K and V earlier, and start the
@@ -301,7 +305,8 @@ mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info);
  * touching any GPU. Same validation and error codes as mg_attn_plan_ex (minus device errors).
  * The one decision it cannot take is the placement of the on-chip combine's clusters, which
  * mg_attn_plan_ex asks the device about: how many clusters of the chosen size it holds at once.
- * Without an explicit n_split the plan then takes a smaller cluster when that lets the clusters
+ * Without an explicit n_split (and without MG_FLAG_ISOLATED for the second step) the plan then
+ * takes a smaller cluster when that lets the clusters
  * of two back-to-back calls be resident together (at most one more column tile per CTA), or
  * when the chosen clusters do not fit at all (at most two more), and otherwise falls back to
  * the second kernel;

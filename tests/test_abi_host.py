@@ -318,6 +318,7 @@ def test_query_push_combine():
     ((2, 256, 4096, 64), {"stages": 7}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x4000}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"flags": 0x8000}, mg.MG_ERR_CONFIG),
+    ((2, 256, 4096, 64), {"flags": 0x10000}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 64), {"timeout_ns": 5}, mg.MG_ERR_CONFIG),
     ((2, 256, 4096, 128), {"stages": 4}, mg.MG_ERR_INSUFFICIENT_SMEM),
     ((2, 256, 4096, 64), {"max_smem_optin": 100000}, mg.MG_ERR_INSUFFICIENT_SMEM),
