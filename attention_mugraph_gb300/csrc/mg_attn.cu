@@ -654,7 +654,7 @@ mg_status pipeline_splits(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     // (QK-norm in the one-tile kernel starts early only with its key scales in shared memory.)
     const bool qk_one_tile = (*flags & MG_FLAG_QK_NORM) && info->swap_ab == 0;
     if (info->cluster_ctas < 2 || (opts && opts->n_split != 0) || info->schedule != 0 || info->q_tiles_per_cta != 1 ||
-        (qk_one_tile && qk_cs_tiles(*info, *flags) == 0) || (*flags & (MG_FLAG_ISOLATED | MG_FLAG_NO_EARLY_LOADS)))
+        (qk_one_tile && qk_cs_tiles(*info, *flags) == 0) || (*flags & MG_FLAG_ISOLATED))
         return MG_OK;
     const int n = info->cluster_ctas;
     const int units = info->grid_ctas / n;

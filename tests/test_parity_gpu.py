@@ -403,7 +403,8 @@ def test_cluster_placement_for_back_to_back_calls():
     assert mg.Plan(2, 256, 4096, 64, n_split=16).info["cluster_ctas"] == 16
     # Planned for calls that do not overlap: the count placed for one call's latency.
     assert mg.Plan(2, 256, 4096, 64, flags=mg.MG_FLAG_ISOLATED).info["n_split"] == 12
-    assert mg.Plan(2, 256, 4096, 64, flags=mg.MG_FLAG_NO_EARLY_LOADS).info["n_split"] == 12
+    # MG_FLAG_NO_EARLY_LOADS changes when a call's kernels run, not the plan.
+    assert mg.Plan(2, 256, 4096, 64, flags=mg.MG_FLAG_NO_EARLY_LOADS).info["n_split"] == 6
     assert mg.Plan(1, 256, 4096, 64).info["n_split"] == 12
     assert mg.Plan(2, 64, 1024, 64).info["n_split"] == 8  # 4 tiny calls in flight already
     b4 = mg.Plan(4, 256, 4096, 64).info
