@@ -73,9 +73,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // The deepest K/V ring that fits.
 int auto_stages(int64_t d) { return d == 64 ? 6 : 3; }
 
-// Grids of at least this many CTAs (one per SM) may start early at level 2 (FwdParams::early):
-// fewer of them than the window of recent outputs (below) fit the device at once.
-constexpr int kEarlyMinCtas = 10;
+// The window of recent calls whose outputs an early read is compared with (see recent_outputs).
+constexpr int kWindow = 16;
+
+// The smallest grid (CTAs of one per SM) that may start early at level 2 (FwdParams::early) on a
+// device with `sms` SMs: fewer than kWindow such grids fit the device at once (10 on 152 SMs).
+int early_min_ctas(int sms) { return sms / kWindow + 1; }
 
 using FwdKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                            const CUtensorMap, const mg::FwdParams);
@@ -640,7 +643,7 @@ mg_status fit_clusters(int64_t B, int64_t M, int64_t N, int64_t d, const mg_attn
 // each CTA (a longer call) but lets more calls be resident together. Without an explicit n_split,
 // for a cluster plan that may start early, the split count from the one placed down to 2 that
 // keeps at most max(8, the placed count's) column tiles per CTA (twice the placed count's when
-// that lets no second call in) and a grid of at least kEarlyMinCtas CTAs, and that maximises
+// that lets no second call in) and a grid of at least early_min_ctas CTAs, and that maximises
 // min(4, clusters the device holds / clusters per call, SMs / grid) is taken (the larger on a
 // tie). Measured on GB300 (us per call, back to back at
 // level 2; isolated, each call between events of its own): (2, 256, 4096, 64) 6 splits 1.83 and
@@ -677,7 +680,7 @@ mg_status pipeline_splits(int64_t B, int64_t M, int64_t N, int64_t d, const mg_a
     mg_attn_options o{};
     if (opts)
         o = *opts;
-    for (int c = n - 1; c >= 2 && tiles(c) <= bound && units * c >= kEarlyMinCtas; --c) {
+    for (int c = n - 1; c >= 2 && tiles(c) <= bound && units * c >= early_min_ctas(sms); --c) {
         mg_attn_options oc = o;
         oc.n_split = c;
         mg_attn_plan_info ic;
@@ -932,16 +935,15 @@ mg_status mg_attn_get_info(mg_attn_plan_t plan, mg_attn_plan_info *info)
 //   time the next one can start.
 // * A fused kernel at level 2 releases them at its start. A kernel cannot complete before the one
 //   before it, so when kernel i still runs every later kernel does too, all their CTAs resident
-//   (none can exit before its wait). Level 2 is used only for grids of at least kEarlyMinCtas
-//   CTAs of one per SM, so fewer than kWindow such kernels fit the device together.
+//   (none can exit before its wait). Level 2 is used only for grids of at least
+//   early_min_ctas(SMs) CTAs of one per SM, so fewer than kWindow such kernels fit the device
+//   together.
 // So the reads are early only when the previous call on the stream is known and no input shares
 // bytes with the outputs of the last kWindow calls or with the call's own output. The first call
 // on a stream, or one whose records were displaced by kStreamSlots newer streams, is not known,
 // and nor is the first call of a stream capture. Calls enqueued under capture are recorded apart
 // from the stream's eager calls, keyed by the capture's id, since the captured kernels run later
 // as one graph.
-constexpr int kWindow = 16;
-static_assert(152 / kEarlyMinCtas < kWindow, "the window must cover every kernel that can still run");
 struct OutRanges {
     cudaStream_t stream = nullptr;
     unsigned long long capture = 0;                     // the capture's id, 0 for eager calls
@@ -1046,7 +1048,7 @@ bool may_load_early(cudaStream_t stream, const void *const *p, const size_t *n, 
 // How much of the fused kernel may run before the previous grid on the stream completes
 // (FwdParams::early): 1, its first copies, where may_load_early allows; 2, everything but its
 // global writes, with its dependents released at its start, for the one-tile and few-row kernels
-// under the split schedule with grids of at least kEarlyMinCtas CTAs, but not the one-tile
+// under the split schedule with grids of at least early_min_ctas CTAs, but not the one-tile
 // kernel's QK-norm (its key scales go through global memory). Measured on GB300 (us per call,
 // back to back): level 1 against 0, gqa 6.17 against 6.50, tiny 4.56 against 5.44, gqa_b8 9.86
 // against 10.03, long_kv 14.52 against 14.82, decode 46.0 against 46.7, decode_m1 24.6 against
@@ -1063,7 +1065,7 @@ int early_level(const mg_attn_plan_info &in, int flags, cudaStream_t stream, con
     if (!may_load_early(stream, inp, nb, 3, O, bq))
         return 0;
     const bool qk_global = (flags & MG_FLAG_QK_NORM) && in.swap_ab == 0 && qk_cs_tiles(in, flags) == 0;
-    return in.schedule == 0 && !qk_global && in.grid_ctas >= kEarlyMinCtas ? 2 : 1;
+    return in.schedule == 0 && !qk_global && in.grid_ctas >= early_min_ctas(in.num_sms) ? 2 : 1;
 }
 
 // mg_attn_run's work; `allow_early`: the fused kernel may load Q, K and V before the previous
