@@ -53,6 +53,12 @@ constexpr uint32_t kSwapChunk = kSwapNQ * 128;                   // one such chu
 constexpr uint32_t kSwapStageBytes = 2u * kSwapD * kBlockN * 2;  // K + V tile
 constexpr uint32_t kSwapPBytes = kSwapNQ * kBlockN * 2;          // P^T: two 64-key chunks of 16 rows
 constexpr int kSwapPBuffers = 3;
+// A stage's K tile is free once its S^T product completes, and the load warp issues K tile
+// t + kSwapKLead before V tile t: the K stream runs ahead of the V stream, whose stages are held
+// until P.V. The QK-norm form reads the K tile until its P^T is written, so both halves are
+// released after P.V there and K takes no lead (a K tile issued ahead would wait for the release
+// of a stage whose V tile it is itself queued in front of, once the lead reaches the ring depth).
+constexpr int kSwapKLead = 2;
 constexpr uint32_t kSwapTmemCols = 64;                           // S^T buffers at 0 and 16, O^T at 32 (and 48)
 constexpr uint32_t kSwapTmemO = 32;
 // Forms of the few-row kernel: the graph as written; ONLINE (max-subtracted, one pass); ONLINE
@@ -131,7 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *m_fin = m_red + 2 * 2 * kGroupWarps * kSwapNQ;     // ONLINE: group 1's final maxima
     float *a_sc = m_fin + kSwapNQ;                            // QK-norm: the query scales
     uint64_t *bars = reinterpret_cast<uint64_t *>(ONLINE ? a_sc + kSwapNQ : m_red);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + BI::kCount);
+    // After the common barriers: the K halves of the stages released on their own (kKvEmpty then
+    // releases the V halves).
+    constexpr int kKEmpty = BI::kCount;
+    constexpr int kKLead = QKN ? 0 : kSwapKLead;
+    static_assert((kKEmpty + STAGES) * 8 + 8 <= 512, "barrier area overflow");
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + kKEmpty + STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
 
@@ -152,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(BI::kKFull + s), 1);
             ptx::mbar_init(bar(BI::kVFull + s), 1);
             ptx::mbar_init(bar(BI::kKvEmpty + s), 1);
+            ptx::mbar_init(bar(kKEmpty + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(bar(BI::kSFull + s), 1);
@@ -207,28 +219,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             bool q_armed = false;
-            int armed[STAGES];
+            int armed_k[STAGES], armed_v[STAGES];
 #pragma unroll
             for (int s = 0; s < STAGES; ++s)
-                armed[s] = 0;
+                armed_k[s] = armed_v[s] = 0;
             bool ok = true;
-            auto issue = [&](int t) {
+            auto issue_k = [&](int t) {
                 const int s = t % STAGES;
-                const int n0 = tile_of(t) * kBlockN;
                 const uint32_t sK = sStage0 + s * kSwapStageBytes;
-                const uint32_t sV = sK + D * kBlockN * 2;
+                const int n0 = tile_of(t) * kBlockN;
                 ptx::mbar_arrive_expect_tx(bar(BI::kKFull + s), D * kBlockN * 2);
-                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), kBlockN * D * 2);
-                ++armed[s];
+                ++armed_k[s];
                 ptx::tma_load_3d(sK, &tmK, bar(BI::kKFull + s), n0, 0, b);
                 ptx::tma_load_3d(sK + D * 128, &tmK, bar(BI::kKFull + s), n0 + 64, 0, b);
+            };
+            auto issue_v = [&](int t) {
+                const int s = t % STAGES;
+                const uint32_t sV = sStage0 + s * kSwapStageBytes + D * kBlockN * 2;
+                const int n0 = tile_of(t) * kBlockN;
+                ptx::mbar_arrive_expect_tx(bar(BI::kVFull + s), kBlockN * D * 2);
+                ++armed_v[s];
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d(sV + c * TileCfg<D>::kChunkRows128, &tmV, bar(BI::kVFull + s), c * 64, n0, b);
             };
             if (p.inject_timeout)
                 ok = wait_bounded(wc, bar(BI::kNever), 0, BI::kNever);
-            int t = 0;  // the next tile to issue
+            int tk = 0, tv = 0;  // the next K and V tiles to issue
             if (ok) {
                 // Q[b, 0:16, 64c:64c+64] (the tensor map's box is 16 rows; rows past M read as zero).
                 ptx::mbar_arrive_expect_tx(bar(BI::kQFull), kSwapQBytes);
@@ -237,37 +254,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d(sQ + c * kSwapChunk, &tmQ, bar(BI::kQFull), c * 64, 0, b);
                 if (p.early == 1)
-                    for (; t < T && t < STAGES; ++t)  // the stages are free: no wait
-                        issue(t);
+                    for (; tk < T && tk < STAGES; ++tk) {  // the stages are free: no wait
+                        issue_k(tk);
+                        issue_v(tk);
+                    }
+                tv = tk;
             }
             if (p.early == 1) {
                 __syncwarp();
                 ptx::griddep_wait();
                 ptx::griddep_launch_dependents();
             }
-            for (; ok && t < T; ++t) {
-                const int s = t % STAGES;
-                const uint32_t round = static_cast<uint32_t>(t / STAGES);
-                if (t >= STAGES && !wait_bounded(wc, bar(BI::kKvEmpty + s), (round & 1u) ^ 1u, BI::kKvEmpty + s)) {
-                    ok = false;
-                    break;
+            // K tile tk once its stage's previous K is consumed, up to kKLead tiles ahead of the
+            // V stream; otherwise V tile tv once its stage's previous V is.
+            while (ok && tv < T) {
+                if (tk < T && tk <= tv + kKLead) {
+                    const int s = tk % STAGES;
+                    if (tk >= STAGES && !wait_bounded(wc, bar(kKEmpty + s), ((tk / STAGES) & 1u) ^ 1u, kKEmpty + s))
+                        ok = false;
+                    else
+                        issue_k(tk++);
+                } else {
+                    const int s = tv % STAGES;
+                    if (tv >= STAGES &&
+                        !wait_bounded(wc, bar(BI::kKvEmpty + s), ((tv / STAGES) & 1u) ^ 1u, BI::kKvEmpty + s))
+                        ok = false;
+                    else
+                        issue_v(tv++);
                 }
-                issue(t);
             }
-            if (ok) {
-                for (int u = T - STAGES > 0 ? T - STAGES : 0; ok && u < T; ++u)
-                    ok = wait_bounded(wc, bar(BI::kKvEmpty + u % STAGES), static_cast<uint32_t>(u / STAGES) & 1u,
-                                      BI::kKvEmpty + u % STAGES);
+            // The releases of the last stages land before the CTA exits.
+            for (int u = T - STAGES > 0 ? T - STAGES : 0; ok && u < T; ++u) {
+                const uint32_t ph = static_cast<uint32_t>(u / STAGES) & 1u;
+                ok = wait_bounded(wc, bar(kKEmpty + u % STAGES), ph, kKEmpty + u % STAGES) &&
+                     wait_bounded(wc, bar(BI::kKvEmpty + u % STAGES), ph, BI::kKvEmpty + u % STAGES);
             }
             if (*abort_flag) {
                 if (q_armed)
                     wait_drain(bar(BI::kQFull), 0, p.timeout_ns);
 #pragma unroll
-                for (int s = 0; s < STAGES; ++s)
-                    if (armed[s] > 0) {
-                        wait_drain(bar(BI::kKFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
-                        wait_drain(bar(BI::kVFull + s), static_cast<uint32_t>(armed[s] - 1) & 1u, p.timeout_ns);
-                    }
+                for (int s = 0; s < STAGES; ++s) {
+                    if (armed_k[s] > 0)
+                        wait_drain(bar(BI::kKFull + s), static_cast<uint32_t>(armed_k[s] - 1) & 1u, p.timeout_ns);
+                    if (armed_v[s] > 0)
+                        wait_drain(bar(BI::kVFull + s), static_cast<uint32_t>(armed_v[s] - 1) & 1u, p.timeout_ns);
+                }
             }
         }
     } else if (warp == 1) {
@@ -301,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ss(tmem + sb * kSwapNQ, a_k + static_cast<uint64_t>(k * (2048 >> 4)), b_q[k], idesc_s,
                                     k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
+                if constexpr (!QKN)
+                    ptx::mma_commit(bar(kKEmpty + s));
             }
             __syncwarp();
         }
@@ -342,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     ptx::sdesc_sw128(sP + (k >> 2) * kSwapChunk + (k & 3) * 32, 16, 1024), idesc_o,
                                     (v >= first || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
+                if constexpr (QKN)  // the softmax warps read this K tile until its P^T is written
+                    ptx::mma_commit(bar(kKEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
                 if (v == T - 1)
                     ptx::mma_commit(bar(BI::kOFull));

@@ -41,6 +41,10 @@ PLAIN, SAFE, QKNORM, ONLINE = 0, 1, 2, 3
 # change of its running maxima, after the P.V product of the group's previous tile (t - 2) has
 # completed and before P of tile t is announced.
 GROUP_WARPS = 4
+# Split release (`k_lead` set; the few-row kernel): a stage's K half and V half are released by
+# barriers of their own, KEmpty (committed after the stage's S product, or with `k_at_pv` after
+# its P.V product, where the softmax warps read the K tile: `softmax_reads_k`) and KvEmpty (after
+# P.V); the producer issues K tile t + k_lead before V tile t.
 
 
 class ProtocolError(AssertionError):
@@ -82,9 +86,12 @@ class Barrier:
 
 class Sim:
     def __init__(self, T: int, stages: int, pbufs: int, variant: int, seed: int, mutations=(),
-                 abort_rate: float = 0.0):
+                 abort_rate: float = 0.0, k_lead=None, k_at_pv: bool = False, softmax_reads_k: bool = False):
         if T < 1 or stages < 2 or pbufs < 2:
             raise ValueError("T >= 1, stages >= 2, pbufs >= 2")
+        if k_lead is not None and variant not in (PLAIN, ONLINE):
+            raise ValueError("the split release is modelled for the one-pass forms")
+        self.k_lead, self.k_at_pv, self.sm_reads_k = k_lead, k_at_pv, softmax_reads_k
         self.T, self.S, self.P, self.var = T, stages, pbufs, variant
         self.safe = variant in (SAFE, QKNORM)
         self.qk = variant == QKNORM
@@ -106,6 +113,8 @@ class Sim:
             mk(f"KFull{s}", 1)
             mk(f"VFull{s}", 1)
             mk(f"KvEmpty{s}", 1)
+            if k_lead is not None:
+                mk(f"KEmpty{s}", 1)
         for g in range(2):
             mk(f"SFull{g}", 1)
             mk(f"SEmpty{g}", GROUP_WARPS)
@@ -151,6 +160,9 @@ class Sim:
     # of the participants' predicates; ("drain", kind) waits, ignoring the abort, until the
     # role's copies ("tma") or tensor-core operations ("pipe") have completed.
     def _producer(self):
+        if self.k_lead is not None:
+            yield from self._producer_split()
+            return
         S = self.S
         ok = True
         yield ("do", lambda: self._tma_q())
@@ -171,6 +183,51 @@ class Sim:
                     break
         if self.abort:
             yield ("drain", "tma")
+
+    def _producer_split(self):
+        S, U = self.S, self.U
+        ok = True
+        yield ("do", lambda: self._tma_q())
+        tk = tv = 0
+        while ok and tv < U:
+            if tk < U and tk <= tv + self.k_lead:
+                s, rnd = tk % S, tk // S
+                if tk >= S and "producer_no_kempty_wait" not in self.mut:
+                    if not (yield self.wait(f"KEmpty{s}", (rnd & 1) ^ 1, rnd - 1, f"producer K {tk}")):
+                        ok = False
+                        break
+                yield ("do", lambda t=tk, s=s: self._issue_k(t, s))
+                tk += 1
+            else:
+                s, rnd = tv % S, tv // S
+                if tv >= S:
+                    if not (yield self.wait(f"KvEmpty{s}", (rnd & 1) ^ 1, rnd - 1, f"producer V {tv}")):
+                        ok = False
+                        break
+                yield ("do", lambda t=tv, s=s: self._issue_v(t, s))
+                tv += 1
+        if ok:
+            for u in range(max(U - S, 0), U):
+                ok = (yield self.wait(f"KEmpty{u % S}", (u // S) & 1, u // S, f"producer tail K {u}")) and \
+                     (yield self.wait(f"KvEmpty{u % S}", (u // S) & 1, u // S, f"producer tail V {u}"))
+                if not ok:
+                    break
+        if self.abort:
+            yield ("drain", "tma")
+
+    def _issue_k(self, t, s):
+        if self.k_readers[s] and not self.abort:
+            self.fail(f"K stage {s} overwritten for tile {t} while still read")
+        self.kst[s] = None
+        self.bars[f"KFull{s}"].arrive(expect_tx=1)
+        self.tma.append((f"KFull{s}", 1, lambda: self.kst.__setitem__(s, t)))
+
+    def _issue_v(self, t, s):
+        if self.v_readers[s] and not self.abort:
+            self.fail(f"V stage {s} overwritten for tile {t} while still read")
+        self.vst[s] = None
+        self.bars[f"VFull{s}"].arrive(expect_tx=1)
+        self.tma.append((f"VFull{s}", 1, lambda: self.vst.__setitem__(s, t)))
 
     def _tma_q(self):
         self.bars["QFull"].arrive(expect_tx=1)
@@ -229,6 +286,8 @@ class Sim:
 
         self.pipe.append(("mma", done))
         self.pipe.append(("commit", f"SFull{sb}"))
+        if self.k_lead is not None and not self.k_at_pv:
+            self.pipe.append(("commit", f"KEmpty{s}"))
         if not self.qk and u < self.T1:
             self.pipe.append(("commit", f"KvEmpty{s}"))
 
@@ -279,6 +338,8 @@ class Sim:
 
         self.pipe.append(("mma", done))
         self.pipe.append(("commit", f"KvEmpty{s}"))
+        if self.k_lead is not None and self.k_at_pv:
+            self.pipe.append(("commit", f"KEmpty{s}"))
         self.pipe.append(("commit", f"PEmpty{pb}"))
         if v == self.T - 1:
             self.pipe.append(("commit", "OFull"))
@@ -331,6 +392,14 @@ class Sim:
         while ok and u < self.U:
             t = u - self.T1
             pb = t % P
+            if self.sm_reads_k:
+                # The few-row QK-norm form: the key scales from the K tile, before S is read.
+                s = u % S
+                if not (yield self.wait(f"KFull{s}", (u // S) & 1, u // S, f"{who} K {u}")):
+                    ok = False
+                    break
+                yield ("do", lambda s=s, u=u: self._read_k(s, u, +1))
+                yield ("do", lambda s=s: self._read_k(s, None, -1))
             if not (yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")):
                 ok = False
                 break

@@ -193,27 +193,83 @@ def test_segment_unwinding_from_any_wait_is_clean():
         pm.SegmentSim(segs, stages, pbufs, seed, abort_rate=0.02).run()
 
 
-# ------------------------------------------------------------------ few-row kernel, one-pass max-subtracted
+# ------------------------------------------------------------------ few-row kernel
+# The few-row kernel releases a stage's K and V halves on barriers of their own and issues K tile
+# t + 2 before V tile t (the graph as written and the one-pass max-subtracted form); its QK-norm
+# form reads each K tile in the softmax warps, releases both halves after P.V and takes no lead.
+SWAP_LEAD = 2
+SWAP_FORMS = {
+    "plain": dict(variant=pm.PLAIN, k_lead=SWAP_LEAD),
+    "max-subtracted": dict(variant=pm.ONLINE, k_lead=SWAP_LEAD),
+    "qk-norm": dict(variant=pm.ONLINE, k_lead=0, k_at_pv=True, softmax_reads_k=True),
+}
 
+
+def swap_sim(form, T, stages, pbufs, seed, **kw):
+    args = dict(SWAP_FORMS[form])
+    args.update(kw)
+    variant = args.pop("variant")
+    return pm.Sim(T, stages, pbufs, variant, seed, **args)
+
+
+@pytest.mark.parametrize("form", list(SWAP_FORMS))
 @pytest.mark.parametrize("stages,pbufs", [(3, 3), (2, 3)])
-def test_online_protocol_as_built_is_clean(stages, pbufs):
-    # The graph as written's protocol plus, per tile, the group's rescale of its own O after the
-    # P.V product of its previous tile (a wait on that tile's P-buffer barrier).
+def test_swap_protocol_as_built_is_clean(form, stages, pbufs):
+    # The max-subtracted form adds, per tile, the group's rescale of its own O after the P.V
+    # product of its previous tile (a wait on that tile's P-buffer barrier).
     for T, seed in itertools.product((1, 2, 3, 4, 7, 12), range(12)):
-        pm.Sim(T, stages, pbufs, pm.ONLINE, seed).run()
+        swap_sim(form, T, stages, pbufs, seed).run()
+
+
+@pytest.mark.parametrize("lead", [0, 1, 3, 4])
+def test_swap_protocol_is_clean_for_other_k_leads(lead):
+    # K released after S: any lead is free of deadlock (a K tile waits only for S products, which
+    # need no V tile the producer has still to issue).
+    for T, (stages, pbufs), seed in itertools.product((1, 3, 7, 12), [(3, 3), (2, 3)], range(6)):
+        swap_sim("plain", T, stages, pbufs, seed, k_lead=lead).run()
+        swap_sim("max-subtracted", T, stages, pbufs, seed, k_lead=lead).run()
+
+
+def swap_caught(form, tries=40, **kw):
+    for T, (stages, pbufs), seed in itertools.product((3, 5, 8), [(3, 3), (2, 3)], range(tries)):
+        try:
+            swap_sim(form, T, stages, pbufs, seed, **kw).run()
+        except pm.ProtocolError as e:
+            return str(e)
+    return None
+
+
+def test_swap_k_stage_refilled_without_its_wait_is_caught():
+    msg = swap_caught("plain", mutations=("producer_no_kempty_wait",))
+    assert msg is not None and "K stage" in msg
+
+
+def test_swap_qk_norm_k_released_after_s_is_caught():
+    # The softmax warps read the K tile for the key scales: a release after S alone lets the
+    # producer overwrite it under them.
+    msg = swap_caught("qk-norm", k_at_pv=False)
+    assert msg is not None and "K stage" in msg
+
+
+def test_swap_qk_norm_k_lead_up_to_the_ring_depth_deadlocks():
+    # With both halves released after P.V, a K tile issued ring-depth tiles ahead waits for the
+    # P.V product of a tile whose V tile is queued behind it.
+    msg = swap_caught("qk-norm", k_lead=3)
+    assert msg is not None and "deadlock" in msg
 
 
 def test_online_rescale_needs_its_wait():
     hit = None
     for T, (stages, pbufs), seed in itertools.product((3, 5, 8), [(3, 3), (2, 3)], range(60)):
         try:
-            pm.Sim(T, stages, pbufs, pm.ONLINE, seed, mutations=("online_no_rescale_wait",)).run()
+            swap_sim("max-subtracted", T, stages, pbufs, seed, mutations=("online_no_rescale_wait",)).run()
         except pm.ProtocolError as e:
             hit = str(e)
             break
     assert hit is not None and "rescales its O" in hit
 
 
-def test_online_unwinding_from_any_wait_is_clean():
+@pytest.mark.parametrize("form", list(SWAP_FORMS))
+def test_swap_unwinding_from_any_wait_is_clean(form):
     for T, (stages, pbufs), seed in itertools.product((1, 2, 3, 5, 8), [(3, 3), (2, 3)], range(12)):
-        pm.Sim(T, stages, pbufs, pm.ONLINE, seed, abort_rate=0.02).run()
+        swap_sim(form, T, stages, pbufs, seed, abort_rate=0.02).run()
