@@ -53,11 +53,10 @@ constexpr uint32_t kSwapChunk = kSwapNQ * 128;                   // one such chu
 constexpr uint32_t kSwapStageBytes = 2u * kSwapD * kBlockN * 2;  // K + V tile
 constexpr uint32_t kSwapPBytes = kSwapNQ * kBlockN * 2;          // P^T: two 64-key chunks of 16 rows
 constexpr int kSwapPBuffers = 3;
-// A stage's K tile is free once its S^T product completes, and the load warp issues K tile
-// t + kSwapKLead before V tile t: the K stream runs ahead of the V stream, whose stages are held
-// until P.V. The QK-norm form reads the K tile until its P^T is written, so both halves are
-// released after P.V there and K takes no lead (a K tile issued ahead would wait for the release
-// of a stage whose V tile it is itself queued in front of, once the lead reaches the ring depth).
+// A stage's K tile is free once its S^T product completes (in the QK-norm form also once the
+// four warps of the tile's group have read it for the key scales), and the load warp issues K
+// tile t + kSwapKLead before V tile t: the K stream runs ahead of the V stream, whose stages are
+// held until P.V.
 constexpr int kSwapKLead = 2;
 constexpr uint32_t kSwapTmemCols = 64;                           // S^T buffers at 0 and 16, O^T at 32 (and 48)
 constexpr uint32_t kSwapTmemO = 32;
@@ -140,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // After the common barriers: the K halves of the stages released on their own (kKvEmpty then
     // releases the V halves).
     constexpr int kKEmpty = BI::kCount;
-    constexpr int kKLead = QKN ? 0 : kSwapKLead;
     static_assert((kKEmpty + STAGES) * 8 + 8 <= 512, "barrier area overflow");
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + kKEmpty + STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -163,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(BI::kKFull + s), 1);
             ptx::mbar_init(bar(BI::kVFull + s), 1);
             ptx::mbar_init(bar(BI::kKvEmpty + s), 1);
-            ptx::mbar_init(bar(kKEmpty + s), 1);
+            ptx::mbar_init(bar(kKEmpty + s), QKN ? 1 + kGroupWarps : 1);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(bar(BI::kSFull + s), 1);
@@ -265,10 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::griddep_wait();
                 ptx::griddep_launch_dependents();
             }
-            // K tile tk once its stage's previous K is consumed, up to kKLead tiles ahead of the
-            // V stream; otherwise V tile tv once its stage's previous V is.
+            // K tile tk once its stage's previous K is consumed, up to kSwapKLead tiles ahead of
+            // the V stream; otherwise V tile tv once its stage's previous V is.
             while (ok && tv < T) {
-                if (tk < T && tk <= tv + kKLead) {
+                if (tk < T && tk <= tv + kSwapKLead) {
                     const int s = tk % STAGES;
                     if (tk >= STAGES && !wait_bounded(wc, bar(kKEmpty + s), ((tk / STAGES) & 1u) ^ 1u, kKEmpty + s))
                         ok = false;
@@ -332,8 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_f16_ss(tmem + sb * kSwapNQ, a_k + static_cast<uint64_t>(k * (2048 >> 4)), b_q[k], idesc_s,
                                     k > 0 ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kSFull + sb));
-                if constexpr (!QKN)
-                    ptx::mma_commit(bar(kKEmpty + s));
+                ptx::mma_commit(bar(kKEmpty + s));
             }
             __syncwarp();
         }
@@ -375,8 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     ptx::sdesc_sw128(sP + (k >> 2) * kSwapChunk + (k & 3) * 32, 16, 1024), idesc_o,
                                     (v >= first || k > 0) ? 1u : 0u);
                 ptx::mma_commit(bar(BI::kKvEmpty + s));
-                if constexpr (QKN)  // the softmax warps read this K tile until its P^T is written
-                    ptx::mma_commit(bar(kKEmpty + s));
                 ptx::mma_commit(bar(BI::kPEmpty + pb));
                 if (v == T - 1)
                     ptx::mma_commit(bar(BI::kOFull));
@@ -475,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool w_ok = ok;
                 float cn = 1.f;  // QK-norm: this thread's key scale c_n = 1/rms(K[:, n])
                 if constexpr (QKN) {
-                    // From the K tile in shared memory, while the tensor core computes S^T (the K
-                    // stage is released only after this tile's P.V, which waits for this group).
+                    // From the K tile in shared memory, while the tensor core computes S^T; each
+                    // warp's read is one of the arrivals that release the tile's K half.
                     const int st = u % STAGES;
                     w_ok = w_ok && warp_wait(bar(BI::kKFull + st), static_cast<uint32_t>(u / STAGES) & 1u, BI::kKFull + st);
                     if (w_ok) {
@@ -488,6 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sum_sq_cols(*reinterpret_cast<const uint4 *>(kp + k * 1024), sq);
                         const float c = __frsqrt_rn(reduce_scatter8(sq, lane) * (1.f / D) + kQkNormEps);
                         cn = __shfl_sync(0xffffffffu, c, c_src);
+                        if (lane == 0)  // every lane's loads are in c (the shuffles above)
+                            ptx::mbar_arrive(bar(kKEmpty + st));
                     }
                 }
                 w_ok = w_ok && warp_wait(bar(BI::kSFull + g), static_cast<uint32_t>(u >> 1) & 1u, BI::kSFull + g);

@@ -43,8 +43,9 @@ PLAIN, SAFE, QKNORM, ONLINE = 0, 1, 2, 3
 GROUP_WARPS = 4
 # Split release (`k_lead` set; the few-row kernel): a stage's K half and V half are released by
 # barriers of their own, KEmpty (committed after the stage's S product, or with `k_at_pv` after
-# its P.V product, where the softmax warps read the K tile: `softmax_reads_k`) and KvEmpty (after
-# P.V); the producer issues K tile t + k_lead before V tile t.
+# its P.V product) and KvEmpty (after P.V); the producer issues K tile t + k_lead before V tile t.
+# Where the softmax warps read the K tile too (`softmax_reads_k`, the QK-norm form), KEmpty also
+# counts one arrival from each warp of the tile's group once it has read it (`k_softmax_release`).
 
 
 class ProtocolError(AssertionError):
@@ -86,12 +87,14 @@ class Barrier:
 
 class Sim:
     def __init__(self, T: int, stages: int, pbufs: int, variant: int, seed: int, mutations=(),
-                 abort_rate: float = 0.0, k_lead=None, k_at_pv: bool = False, softmax_reads_k: bool = False):
+                 abort_rate: float = 0.0, k_lead=None, k_at_pv: bool = False, softmax_reads_k: bool = False,
+                 k_softmax_release: bool = False):
         if T < 1 or stages < 2 or pbufs < 2:
             raise ValueError("T >= 1, stages >= 2, pbufs >= 2")
         if k_lead is not None and variant not in (PLAIN, ONLINE):
             raise ValueError("the split release is modelled for the one-pass forms")
         self.k_lead, self.k_at_pv, self.sm_reads_k = k_lead, k_at_pv, softmax_reads_k
+        self.k_sm_release = k_softmax_release
         self.T, self.S, self.P, self.var = T, stages, pbufs, variant
         self.safe = variant in (SAFE, QKNORM)
         self.qk = variant == QKNORM
@@ -114,7 +117,7 @@ class Sim:
             mk(f"VFull{s}", 1)
             mk(f"KvEmpty{s}", 1)
             if k_lead is not None:
-                mk(f"KEmpty{s}", 1)
+                mk(f"KEmpty{s}", 1 + (GROUP_WARPS if k_softmax_release else 0))
         for g in range(2):
             mk(f"SFull{g}", 1)
             mk(f"SEmpty{g}", GROUP_WARPS)
@@ -400,6 +403,8 @@ class Sim:
                     break
                 yield ("do", lambda s=s, u=u: self._read_k(s, u, +1))
                 yield ("do", lambda s=s: self._read_k(s, None, -1))
+                if self.k_sm_release:
+                    yield ("do", lambda s=s: self.bars[f"KEmpty{s}"].arrive())
             if not (yield self.wait(f"SFull{g}", (u >> 1) & 1, u >> 1, f"{who} S {u}")):
                 ok = False
                 break

@@ -195,13 +195,14 @@ def test_segment_unwinding_from_any_wait_is_clean():
 
 # ------------------------------------------------------------------ few-row kernel
 # The few-row kernel releases a stage's K and V halves on barriers of their own and issues K tile
-# t + 2 before V tile t (the graph as written and the one-pass max-subtracted form); its QK-norm
-# form reads each K tile in the softmax warps, releases both halves after P.V and takes no lead.
+# t + 2 before V tile t. Its QK-norm form also reads each K tile in the softmax warps (the key
+# scales): there the K half is released once the S product has completed and every warp of the
+# tile's group has read it.
 SWAP_LEAD = 2
 SWAP_FORMS = {
     "plain": dict(variant=pm.PLAIN, k_lead=SWAP_LEAD),
     "max-subtracted": dict(variant=pm.ONLINE, k_lead=SWAP_LEAD),
-    "qk-norm": dict(variant=pm.ONLINE, k_lead=0, k_at_pv=True, softmax_reads_k=True),
+    "qk-norm": dict(variant=pm.ONLINE, k_lead=SWAP_LEAD, softmax_reads_k=True, k_softmax_release=True),
 }
 
 
@@ -244,18 +245,20 @@ def test_swap_k_stage_refilled_without_its_wait_is_caught():
     assert msg is not None and "K stage" in msg
 
 
-def test_swap_qk_norm_k_released_after_s_is_caught():
+def test_swap_qk_norm_k_released_after_s_alone_is_caught():
     # The softmax warps read the K tile for the key scales: a release after S alone lets the
     # producer overwrite it under them.
-    msg = swap_caught("qk-norm", k_at_pv=False)
+    msg = swap_caught("qk-norm", k_softmax_release=False)
     assert msg is not None and "K stage" in msg
 
 
-def test_swap_qk_norm_k_lead_up_to_the_ring_depth_deadlocks():
-    # With both halves released after P.V, a K tile issued ring-depth tiles ahead waits for the
-    # P.V product of a tile whose V tile is queued behind it.
-    msg = swap_caught("qk-norm", k_lead=3)
+def test_swap_k_released_after_pv_with_a_lead_of_the_ring_depth_deadlocks():
+    # Both halves released after P.V (an earlier form of the QK-norm kernel): a K tile issued
+    # ring-depth tiles ahead waits for the P.V product of a tile whose V tile is queued behind it.
+    msg = swap_caught("qk-norm", k_softmax_release=False, k_at_pv=True, k_lead=3)
     assert msg is not None and "deadlock" in msg
+    for T, seed in itertools.product((3, 7), range(6)):
+        swap_sim("qk-norm", T, 3, 3, seed, k_softmax_release=False, k_at_pv=True, k_lead=0).run()
 
 
 def test_online_rescale_needs_its_wait():
