@@ -107,13 +107,18 @@ def source_code_text(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
-def kernel_source_digest():
-    """Digest of the fused kernel's code (its two headers, comments left out), recorded beside the
-    ncu counters in the committed summary; a change of code invalidates the recorded traffic."""
+FUSED_SOURCES = ("attention_mugraph_gb300/csrc/mg_attn_kernels.cuh", "attention_mugraph_gb300/csrc/ptx.cuh")
+FEW_ROW_SOURCES = ("attention_mugraph_gb300/csrc/mg_attn_swap.cuh",) + FUSED_SOURCES
+
+
+def kernel_source_digest(sources=FUSED_SOURCES):
+    """Digest of a kernel's code (by default the fused kernel's two headers; FEW_ROW_SOURCES for
+    the few-row kernel; comments left out), recorded beside the ncu counters in the committed
+    summary; a change of code invalidates the recorded traffic."""
     import hashlib
 
     h = hashlib.sha256()
-    for rel in ("attention_mugraph_gb300/csrc/mg_attn_kernels.cuh", "attention_mugraph_gb300/csrc/ptx.cuh"):
+    for rel in sources:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             h.update(source_code_text(f.read()).encode())
     return h.hexdigest()[:16]
