@@ -206,7 +206,8 @@ mg_status mg_attn_plan_ex(int64_t B, int64_t M, int64_t N, int64_t d,
  * may read Q, K and V before the kernels before it on the stream have completed, when the
  * library knows them: the previous call on the same stream (and the same stream capture) was
  * one of this library's, and none of Q, K and V shares bytes with the outputs of the last 16
- * calls on that stream or with O. Then, for grids of at least 10 CTAs, it also releases the
+ * calls on that stream or with O. Then, for grids of more than SMs / 16 CTAs (10 on a 152-SM
+ * GB300: fewer than 16 such grids fit the device at once, one CTA per SM), it also releases the
  * next kernel at its start and computes everything before its wait (back-to-back calls
  * overlap); otherwise only its first copies go out early. A kernel of another origin that runs
  * right before the call and releases its dependents before it completes (programmatic

@@ -19,7 +19,7 @@ its own wait, so a kernel completes only after its wait and the completions stay
 
 A kernel at level 2 releases its dependents at its start, so the kernels after it may start (and
 load) while kernels before it still run; the device holds fewer than W = 16 of them at once
-(grids of at least 10 CTAs, one per SM), which the model, without resources, takes as a bound on
+(grids of more than SMs / 16 CTAs, one per SM), which the model, without resources, takes as a bound on
 the calls it runs. The early forms (copy early, device levels 1 and 2) are used unless an input
 shares bytes with the call's own O or with the O of one of the last W calls on the stream, or
 the call is the first on the stream (its previous kernel unknown); level 2 only for calls of
