@@ -497,7 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before the one before this one has completed. early == 2: the dependents are released now,
     // every role runs without the wait, and each global write waits for the previous grid first
     // (the reads of Q, K and V may then overlap kernels further back; the host checks its recent
-    // outputs for that).
+    // outputs for that). The release comes after this CTA's tensor-memory allocation: a CTA of a
+    // later grid that shares the SM could otherwise hold the columns this one still has to
+    // allocate while it waits for this grid to complete.
     if (p.early == 2) {
         ptx::griddep_launch_dependents();
     } else if (!(warp == 0 && p.early == 1)) {
