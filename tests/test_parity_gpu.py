@@ -354,6 +354,30 @@ def test_swap_ab_specialisation(B, M, N, d, n_split):
     assert_parity(O, ref, f"swap-AB {B, M, N, d} n_split={plan.info['n_split']}")
 
 
+# The few-row kernel releases each stage's K half after its S^T product (in the QK-norm form also
+# after the softmax warps' reads of the key scales) and issues K tiles two ahead of V: rings of 2
+# and 3 stages, several tiles per CTA and a ragged last tile (N a multiple of 8, the layout rule),
+# for the graph as written and both one-pass variants.
+SWAP_RING_CASES = [  # (B, M, N, n_split, stages)
+    (2, 8, 128 * 11 + 40, 2, 2),
+    (2, 8, 128 * 11 + 40, 2, 3),
+    (3, 1, 128 * 7 + 8, 1, 2),
+    (1, 16, 128 * 13, 3, 3),
+]
+
+
+@pytest.mark.parametrize("flags", [0, mg.MG_FLAG_SAFE_SOFTMAX, mg.MG_FLAG_QK_NORM])
+@pytest.mark.parametrize("B,M,N,n_split,stages", SWAP_RING_CASES)
+def test_swap_ab_split_ring_release(B, M, N, n_split, stages, flags):
+    d = 128
+    q, k, v = inputs.make_inputs(B, M, N, d, 0.25, seed=B * 31 + M + N + stages)
+    ref = (oracle.attention_qknorm(q, k, v, eps=mg.MG_QKNORM_EPS) if flags == mg.MG_FLAG_QK_NORM
+           else oracle.attention(q, k, v))
+    O, plan = run_gpu(q, k, v, n_split=n_split, stages=stages, flags=flags | mg.MG_FLAG_SWAP_AB)
+    assert plan.info["swap_ab"] == 1 and plan.info["stages"] == stages
+    assert_parity(O, ref, f"swap-AB ring {B, M, N} n_split={n_split} stages={stages} flags={flags:#x}")
+
+
 SWAP_CLUSTER_SHAPES = [  # (B, M, N, n_split): head dim 128, few rows, split partials
     (64, 1, 4096, 2),     # the launch example's shapes, as planned
     (4, 8, 8192, 16),     # 16 ranks of 8 columns each
